@@ -1,0 +1,132 @@
+"""Planted mistakes in the oracle must be caught by its pins -- CPU only.
+
+Each case swaps one oracle function for a copy with one plausible mistake (a
+dropped scale, a wrong head mapping, an off-by-one mask, a wrong log base, a
+most-recently-used eviction, pages ignored in matching, a merge without
+weights, segments not split where a member ends) and checks that at least one
+pin test then fails.  Nothing here touches a GPU.
+"""
+
+import math
+
+import numpy as np
+import pytest
+
+import oracle.attention as OA
+import oracle.groups as OG
+import oracle.tree as OT
+from tests import test_oracle_attention as TA
+from tests import test_oracle_groups as TG
+from tests import test_oracle_tree as TT
+
+
+def _fails(fn, *args, **kw):
+    try:
+        fn(*args, **kw)
+    except AssertionError:
+        return True
+    return False
+
+
+def test_dropped_softmax_scale_is_caught(monkeypatch):
+    good = OA.softmax_attend
+    monkeypatch.setattr(OA, "softmax_attend", lambda q, K, V, s: good(q, K, V, 1.0))
+    assert _fails(TA.test_decode_equals_sdpa_float64, 4, 2, 64)
+
+
+def test_log2_lse_is_caught(monkeypatch):
+    good = OA.softmax_attend
+
+    def bad(q, K, V, s):
+        o, lse = good(q, K, V, s)
+        return o, lse / math.log(2)
+    monkeypatch.setattr(OA, "softmax_attend", bad)
+    monkeypatch.setattr(TA, "softmax_attend", bad)
+    assert _fails(TA.test_uniform_logits_closed_form)
+
+
+def test_wrong_gqa_mapping_is_caught(monkeypatch):
+    def bad(q, k_pool, v_pool, req_to_token, seq_lens, sm_scale=None, requests=None):
+        q = np.asarray(q, dtype=np.float64)
+        B, Hq, d = q.shape
+        sm_scale = 1 / math.sqrt(d) if sm_scale is None else sm_scale
+        O, L = np.zeros((B, Hq, d)), np.full((B, Hq), -math.inf)
+        for r in range(B):
+            n = int(seq_lens[r])
+            K = np.asarray(k_pool[np.asarray(req_to_token[r, :n])], dtype=np.float64)
+            V = np.asarray(v_pool[np.asarray(req_to_token[r, :n])], dtype=np.float64)
+            for h in range(Hq):
+                O[r, h], L[r, h] = OA.softmax_attend(q[r, h], K[:, h % K.shape[1]], V[:, h % K.shape[1]], sm_scale)
+        return O, L
+    monkeypatch.setattr(TA, "decode_attention", bad)
+    assert _fails(TA.test_decode_equals_sdpa_float64, 32, 8, 128)
+
+
+def test_causal_off_by_one_is_caught(monkeypatch):
+    def bad(q_new, k_pool, v_pool, req_to_token, prefix_lens, extend_lens, sm_scale=None, rows=None):
+        # attends to positions 0..p-1 instead of 0..p
+        shifted = [max(p - 1, 0) for p in prefix_lens]
+        return OA.extend_attention(q_new, k_pool, v_pool, req_to_token, shifted, extend_lens, sm_scale, rows)
+    monkeypatch.setattr(TA, "extend_attention", bad)
+    assert _fails(TA.test_extend_one_token_after_prefix_is_decode)
+
+
+def test_unweighted_merge_is_caught(monkeypatch):
+    def bad(parts):
+        live = [p for p in parts if p[1] != -math.inf]
+        return sum(np.asarray(p[0]) for p in live) / len(live), max(p[1] for p in live)
+    monkeypatch.setattr(TA, "lse_merge", bad)
+    assert _fails(TA.test_lse_merge_closed_form)
+
+
+def test_mru_eviction_is_caught(monkeypatch):
+    def bad_evict(self, num_tokens):
+        freed = 0
+        while freed < num_tokens:
+            cands = self._candidates()
+            if not cands:
+                break
+            victim = max(cands, key=lambda n: (n.last_access, n.nid))
+            del victim.parent.children[victim.key]
+            self.free.append(victim.page)
+            freed += self.P
+        return freed
+    monkeypatch.setattr(OT.RadixTrie, "evict", bad_evict)
+    assert _fails(TT.test_eviction_order_is_lru_on_a_fixed_history)
+
+
+def test_match_ignoring_pages_is_caught(monkeypatch):
+    good = OT.RadixTrie.match
+
+    def bad(self, tokens):
+        m, slots, node = good(self, tokens)
+        # claims the partial page too when the next page starts the same way
+        extra = 0
+        child = next((c for k, c in node.children.items() if len(tokens) > m and k[0] == tokens[m]), None)
+        if child is not None:
+            extra = 1
+            slots = slots + [child.page * self.P]
+        return m + extra, slots, node
+    monkeypatch.setattr(OT.RadixTrie, "match", bad)
+    assert any(_fails(TT.test_match_equals_bruteforce_lcp, 2, s) for s in range(10))
+
+
+def test_segments_not_split_at_member_end_are_caught(monkeypatch):
+    def bad(req_to_token, seq_lens):
+        # a request that ended stays a member of the segments that continue
+        # its path, so groups are not split where a member ends
+        rows = [list(req_to_token[i, :int(n)]) for i, n in enumerate(seq_lens)]
+        B = len(rows)
+        segs = {}
+        for r in range(B):
+            L, prev, start = len(rows[r]), None, 0
+            for j in range(L + 1):
+                M = None if j == L else tuple(
+                    q for q in range(B) if rows[q][:min(j + 1, len(rows[q]))] == rows[r][:min(j + 1, len(rows[q]))])
+                if j > 0 and M != prev:
+                    segs[(prev, start)] = j
+                    start = j
+                prev = M
+        return OG._pack(sorted((min(M), b, e, M) for (M, b), e in segs.items()))
+    monkeypatch.setattr(TG, "prefix_groups", bad)
+    assert _fails(TG.test_conversation_tree_figure, "tests/golden")
