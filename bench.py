@@ -1,0 +1,505 @@
+#!/usr/bin/env python
+"""Benchmark of the RadixAttention hot path on GB300.
+
+One step = one decode batch of the Llama-3-8B-shaped workload (64 requests
+sharing a 2048-token system prefix, suffixes 64..512 tokens, Hq 32 / Hkv 8 /
+d 128, bf16, 2^20-slot pool, random slots): prefix-group planning is done
+once per batch instance, and the timed step is the decode call (split-KV
+partial + log-sum-exp merge) through the C ABI.  The metric is unique-KV
+GB/s: the K/V bytes of every prefix-group segment counted once per step.
+
+  * Device value: K steps replayed from CUDA graphs, rotating over batch
+    instances whose combined unique KV is several times the 129 MB L2, CUDA
+    events around the K steps, max over ranks.
+  * e2e: the same metric through the public API from host buffers -- tree
+    match + tables + prefix groups, planning, plan upload, pinned H2D of q
+    and the tables, the decode call, D2H of O and LSE -- wall clock per step.
+  * extend: TFLOP/s of the chunked-prefill workload (8 requests, cached
+    4096-token prefix + 512 causal new tokens, Hq 64 / Hkv 8), unmasked
+    query-key pairs x 4 d FLOP.
+  * roofline: decode achieved unique-KV GB/s per call against the measured
+    HBM copy bandwidth; ncu DRAM traffic per call from profiles/ when current.
+  * cpu_baseline / --impl reference: the float64 oracle (test
+    infrastructure) timed on host cores on a bounded sample of the workload.
+
+Multi-GPU: the path has no exchange step; each rank runs an independent
+replica (weak scaling), value = bytes of all ranks / max time.
+"""
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+METRIC = "decode attn unique-KV GB/s (% of HBM peak); extend attn TFLOP/s; tokens/s"
+DECODE_WORKLOAD = "llama3_8b_decode"
+EXTEND_WORKLOAD = "extend"
+L2_BYTES = 129 * 1000 * 1000
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--instances", type=int, default=8)
+    ap.add_argument("--graph-len", type=int, default=400)
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--extend-steps", type=int, default=20)
+    ap.add_argument("--no-extend", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-budget-s", type=float, default=60.0)
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def kv_bytes_per_token(w):
+    return 2 * w.Hkv * w.d * (4 if w.dtype == "f32" else 2)
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS, "--format=csv,noheader",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        self.t_start = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1].split()[0]))
+                mx = float(f[2].split()[0])
+            except ValueError:
+                continue
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- reference arm (oracle)
+def reference_arm(args, budget_s, steps, warmup):
+    """Time the float64 oracle (shared-aware decode) on bounded samples of the workload."""
+    import numpy as np
+    import workloads as W
+    from oracle.attention import decode_attention, decode_attention_shared
+    from oracle.groups import prefix_groups
+    from oracle.tree import RadixTrie, build_batch
+
+    w = W.get(DECODE_WORKLOAD)
+    b = W.make_batch(w, 0)
+    order, K, V = W.make_pool(w)
+    Kv, Vv = W.RowView(K), W.RowView(V)
+    trie = RadixTrie(K.shape[0], w.page_size, order)
+    seqs = b.all_tokens()
+    rows, _, _ = build_batch(trie, seqs)
+    q = W.to_dtype(w, b.q).double().numpy()
+    per_tok = kv_bytes_per_token(w)
+
+    def sample(m):
+        sub = rows[:m]
+        ld = max(len(r) for r in sub)
+        t = np.full((m, ld), -1, dtype=np.int64)
+        for i, r in enumerate(sub):
+            t[i, :len(r)] = r
+        lens = np.array([len(r) for r in sub])
+        g = prefix_groups(t, lens)
+        ub = sum(int(e) - int(s) for s, e in zip(g["seg_begin"], g["seg_end"])) * per_tok
+        return t, lens, g, ub
+
+    # calibrate the per-step sample so warmup + steps fit the budget
+    t1, l1, g1, _ = sample(1)
+    c0 = time.perf_counter()
+    decode_attention_shared(q[:1], Kv, Vv, t1, l1, g1)
+    one = time.perf_counter() - c0
+    per_step = budget_s / max(1, steps + warmup)
+    m = int(max(1, min(len(rows), per_step / max(one, 1e-6))))
+    t, lens, g, ub = sample(m)
+    for _ in range(warmup):
+        decode_attention_shared(q[:m], Kv, Vv, t, lens, g)
+    c0 = time.perf_counter()
+    for _ in range(steps):
+        decode_attention_shared(q[:m], Kv, Vv, t, lens, g)
+    el = time.perf_counter() - c0
+    c1 = time.perf_counter()
+    decode_attention(q[:m], Kv, Vv, t, lens)
+    unshared_s = time.perf_counter() - c1
+    gbs = ub * steps / el / 1e9
+    return {
+        "value": gbs, "seconds_per_step": el / steps, "requests": m, "unique_bytes": ub,
+        "unshared_seconds_per_step": unshared_s,
+        "sample": "%d of %d requests of batch instance 0 (%d unique KV tokens), shared-aware float64 decode, "
+                  "%d steps" % (m, len(rows), ub // per_tok, steps),
+    }
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    r = reference_arm(args, args.ref_budget_s, max(1, args.steps), max(0, min(args.warmup, 3)))
+    cores = 1
+    line = {
+        "metric": METRIC, "value": r["value"], "unit": "GB/s", "impl": "reference", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["seconds_per_step"] * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": DECODE_WORKLOAD, "batch": 64, "prefix": 2048, "suffix": "U[64,512]",
+                   "heads": "Hq32/Hkv8/d128", "pool_slots": 1 << 20, "sample_requests": r["requests"]},
+        "cpu_baseline": {"value": r["value"], "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": r["sample"]},
+        "e2e": {"value": r["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline_subprocess(budget_s=15.0):
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               RANK="0", WORLD_SIZE="1")
+    cmd = [sys.executable, os.path.abspath(__file__), "--impl", "reference", "--steps", "3", "--warmup", "1",
+           "--ref-budget-s", str(budget_s)]
+    try:
+        out = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=600, cwd=ROOT)
+        for l in out.stdout.splitlines()[::-1]:
+            if l.startswith("{"):
+                d = json.loads(l)
+                return dict(d["cpu_baseline"])
+    except Exception as e:  # the baseline is context only
+        return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": "failed: %s" % e}
+    return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": "no output"}
+
+
+# --------------------------------------------------------------------------- native arm
+def setup_decode(sgl, W, torch, n_inst):
+    w = W.get(DECODE_WORKLOAD)
+    order, K, V = W.make_pool(w)
+    S = K.shape[0]
+    kd, vd = K.cuda(), V.cuda()
+    del K, V
+    tree = sgl.sgl_tree_create(S, w.page_size, order)
+    per_tok = kv_bytes_per_token(w)
+    inst = []
+    for i in range(n_inst):
+        b = W.make_batch(w, i)
+        seqs = b.all_tokens()
+        groups = sgl.sgl_groups_create()
+        out = sgl.sgl_build_batch(tree, seqs, groups=groups)
+        view = sgl.sgl_groups_view(groups)
+        gnp = sgl.groups_as_numpy(view)
+        ub = int((gnp["seg_end"] - gnp["seg_begin"]).sum()) * per_tok
+        p = sgl.make_params(sgl.SGL_DTYPE_BF16, len(seqs), w.Hq, w.Hkv, w.d, S, w.page_size)
+        plan = sgl.sgl_decode_plan(p, out["seq_lens"], view)
+        ws = torch.zeros(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
+        sgl.sgl_plan_upload(plan, ws)
+        q = W.to_dtype(w, b.q).cuda()
+        inst.append(dict(seqs=seqs, groups=groups, out=out, plan=plan, ws=ws, q=q,
+                         table=torch.from_numpy(out["req_to_token"]).cuda(),
+                         seq=torch.from_numpy(out["seq_lens"]).cuda(),
+                         o=torch.empty_like(q), lse=torch.empty(len(seqs), w.Hq, dtype=torch.float32, device="cuda"),
+                         ub=ub, unshared=int(out["seq_lens"].sum()) * per_tok, B=len(seqs)))
+        for r in range(len(seqs)):   # the batch's requests release their references; the cache keeps the KV
+            sgl.sgl_tree_finish(tree, int(out["last_nodes"][r]), out["req_to_token"][r], len(seqs[r]))
+    torch.cuda.synchronize()
+    return w, tree, kd, vd, inst
+
+
+def decode_call(sgl, kd, vd, it):
+    sgl.sgl_decode_attn(it["q"], kd, vd, it["table"], it["seq"], it["plan"], it["o"], it["lse"], it["ws"])
+
+
+def e2e_decode(sgl, W, torch, w, tree, kd, vd, inst, steps):
+    """Public-API step from host buffers; returns (GB/s, h2d bytes/step, d2h bytes/step)."""
+    S = kd.shape[0]
+    pinned = []
+    for it in inst:
+        B, ld = it["table"].shape
+        pinned.append(dict(q=it["q"].cpu().pin_memory(), table=torch.empty((B, ld), dtype=torch.int32).pin_memory(),
+                           seq=torch.empty(B, dtype=torch.int32).pin_memory(),
+                           o=torch.empty_like(it["o"], device="cpu").pin_memory(),
+                           lse=torch.empty_like(it["lse"], device="cpu").pin_memory()))
+    h2d = d2h = 0
+    total_b = 0
+    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for s in range(steps):
+        it, pb = inst[s % len(inst)], pinned[s % len(inst)]
+        out = sgl.sgl_build_batch(tree, it["seqs"], ld=it["table"].shape[1], groups=it["groups"])
+        view = sgl.sgl_groups_view(it["groups"])
+        p = sgl.make_params(sgl.SGL_DTYPE_BF16, it["B"], w.Hq, w.Hkv, w.d, S, w.page_size)
+        plan = sgl.sgl_decode_plan(p, out["seq_lens"], view)
+        pb["table"].numpy()[:] = out["req_to_token"]
+        pb["seq"].numpy()[:] = out["seq_lens"]
+        sgl.sgl_plan_upload(plan, it["ws"])
+        it["table"].copy_(pb["table"], non_blocking=True)
+        it["seq"].copy_(pb["seq"], non_blocking=True)
+        it["q"].copy_(pb["q"], non_blocking=True)
+        decode_call(sgl, kd, vd, dict(it, plan=plan))
+        pb["o"].copy_(it["o"], non_blocking=True)
+        pb["lse"].copy_(it["lse"], non_blocking=True)
+        stream.synchronize()
+        for r in range(it["B"]):
+            sgl.sgl_tree_finish(tree, int(out["last_nodes"][r]), out["req_to_token"][r], len(it["seqs"][r]))
+        if s == 0:
+            h2d = (pb["q"].numel() * 2 + pb["table"].numel() * 4 + pb["seq"].numel() * 4 +
+                   sgl.sgl_plan_info(plan)["upload_bytes"])
+            d2h = pb["o"].numel() * 2 + pb["lse"].numel() * 4
+        total_b += it["ub"]
+    el = time.perf_counter() - t0
+    return total_b / el / 1e9, h2d, d2h, el / steps
+
+
+def run_native(args):
+    import numpy as np
+    import torch
+    import radixattention_prefix_shared_radix_gb300 as sgl
+    from radixattention_prefix_shared_radix_gb300 import build as sglbuild
+    import workloads as W
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    sglbuild.build()
+    hbm_peak, bf16_peak, peak_src = peaks()
+
+    w, tree, kd, vd, inst = setup_decode(sgl, W, torch, args.instances)
+    ub_all = sum(it["ub"] for it in inst)
+    warm = max(3, args.warmup)
+    for s in range(warm):
+        decode_call(sgl, kd, vd, inst[s % len(inst)])
+    torch.cuda.synchronize()
+    for it in inst:
+        sgl.sgl_check(it["ws"])
+
+    # CUDA graphs of back-to-back decode calls rotating over the instances
+    K = max(1, args.steps)
+    glen = max(1, min(args.graph_len, K))
+    glen -= glen % len(inst) if glen >= len(inst) else 0
+
+    def capture(n, start):
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                for j in range(n):
+                    decode_call(sgl, kd, vd, inst[(start + j) % len(inst)])
+        torch.cuda.current_stream().wait_stream(s)
+        return g
+
+    reps, rem = divmod(K, glen)
+    g_main = capture(glen, 0)
+    g_rem = capture(rem, 0) if rem else None
+    g_main.replay()
+    torch.cuda.synchronize()
+    bytes_per_step = [inst[j % len(inst)]["ub"] for j in range(glen)]
+    total_bytes = sum(bytes_per_step) * reps + sum(bytes_per_step[:rem])
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        g_main.replay()
+    if g_rem is not None:
+        g_rem.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks.stop()
+    ms = e0.elapsed_time(e1)
+    ms_t = torch.tensor([ms], dtype=torch.float64, device="cuda")
+    if world > 1:
+        torch.distributed.all_reduce(ms_t, op=torch.distributed.ReduceOp.MAX)
+    ms_max = float(ms_t.item())
+    for it in inst:
+        sgl.sgl_check(it["ws"])
+    value = total_bytes * world / (ms_max / 1e3) / 1e9
+    per_call_ms = ms / K
+    achieved = (total_bytes / K) / (per_call_ms / 1e3) / 1e9
+
+    # e2e through the public API from host buffers
+    e2e_gbs, h2d, d2h, e2e_step_s = e2e_decode(sgl, W, torch, w, tree, kd, vd, inst, max(1, min(args.e2e_steps, K)))
+
+    ext = None
+    if not args.no_extend:
+        ext = bench_extend(sgl, W, torch, max(3, args.extend_steps), bf16_peak)
+
+    traffic = profile_traffic("decode_partial")
+    B = inst[0]["B"]
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": warm,
+        "ms_per_step": ms_max / K,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": DECODE_WORKLOAD, "batch": B, "prefix": 2048, "suffix": "U[64,512]",
+                   "heads": "Hq32/Hkv8/d128", "pool_slots": kd.shape[0], "page_size": 1,
+                   "instances": len(inst), "unique_kv_bytes_per_step": ub_all // len(inst),
+                   "unshared_kv_bytes_per_step": sum(it["unshared"] for it in inst) // len(inst),
+                   "l2": "inputs larger than L2: %d rotating batch instances, %.0f MB unique KV > %d MB L2"
+                         % (len(inst), ub_all / 1e6, L2_BYTES // 1000000),
+                   "timing": "CUDA graphs of %d back-to-back decode calls, CUDA events" % glen,
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "tokens_per_s": B * world / (ms_max / 1e3 / K),
+        "tokens_per_s_32_layers": B * world / (ms_max / 1e3 / K) / 32,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "peak_source": peak_src,
+                     "frac_of_8TBs": achieved / 8000.0, "traffic": traffic,
+                     "kernel": "decode partial + merge per call (unique-KV bytes / call time)"},
+        "e2e": {"value": e2e_gbs, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_step_s * 1e3},
+        "gpu_launches": 2 * K,
+        "clocks": clocks.summary(),
+    }
+    if ext is not None:
+        line["extend"] = ext
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_subprocess()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def bench_extend(sgl, W, torch, steps, bf16_peak):
+    w = W.get(EXTEND_WORKLOAD)
+    order, K, V = W.make_pool(w)
+    S = K.shape[0]
+    kd, vd = K.cuda(), V.cuda()
+    b = W.make_batch(w, 0)
+    tree = sgl.sgl_tree_create(S, w.page_size, order)
+    warm = [b.cached_tokens(r) for r in range(len(b.req_chain))]
+    o0 = sgl.sgl_build_batch(tree, warm)
+    for r in range(len(warm)):
+        sgl.sgl_tree_finish(tree, int(o0["last_nodes"][r]), o0["req_to_token"][r], len(warm[r]))
+    seqs = b.all_tokens()
+    out = sgl.sgl_build_batch(tree, seqs)
+    pre = out["prefix_lens"]
+    ext = out["seq_lens"] - pre
+    p = sgl.make_params(sgl.SGL_DTYPE_BF16, len(seqs), w.Hq, w.Hkv, w.d, S, w.page_size,
+                        host_prefix_lens=pre, host_extend_lens=ext)
+    ws = torch.zeros(sgl.sgl_extend_workspace_bytes(p), dtype=torch.uint8, device="cuda")
+    q = W.to_dtype(w, b.q).cuda()
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[0], w.Hq, dtype=torch.float32, device="cuda")
+    table = torch.from_numpy(out["req_to_token"]).cuda()
+    pre_d, ext_d = torch.from_numpy(pre).cuda(), torch.from_numpy(ext).cuda()
+
+    def call():
+        sgl.sgl_extend_attn(q, kd, vd, table, pre_d, ext_d, p, o, lse, ws)
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    sgl.sgl_check(ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        call()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    pairs = sum(int(ext[r]) * int(pre[r]) + int(ext[r]) * (int(ext[r]) + 1) // 2 for r in range(len(seqs)))
+    flops = 4.0 * w.d * w.Hq * pairs
+    tflops = flops / (ms / 1e3) / 1e12
+    return {"workload": EXTEND_WORKLOAD, "tflops": tflops, "ms_per_call": ms, "gflop_per_call": flops / 1e9,
+            "roofline": {"bound": "tensor", "achieved": tflops, "peak": bf16_peak, "unit": "TFLOP/s",
+                         "frac": tflops / bf16_peak, "peak_source": "measured bf16 burst"},
+            "tokens_per_s": int(ext.sum()) / (ms / 1e3), "steps": steps}
+
+
+def profile_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if one matches the current kernel."""
+    path = os.path.join(ROOT, "profiles", "decode_llama3_8b_traffic.json")
+    try:
+        d = json.load(open(path))
+        if d.get("kernel_source_hash") == _kernel_hash():
+            return d.get("dram_bytes_per_call")
+    except Exception:
+        pass
+    return None
+
+
+def _kernel_hash():
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "radixattention_prefix_shared_radix_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_native(args)
+
+
+if __name__ == "__main__":
+    main()

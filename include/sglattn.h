@@ -1,0 +1,302 @@
+/*
+ * sglattn.h -- C ABI of the GB300 RadixAttention hot path (libsglattn.so).
+ *
+ * What the library computes, and where the pages on SGLang define it:
+ *
+ *  - A host radix tree over a token-granular KV pool: longest-prefix match,
+ *    insert with node split, per-request reference counts, leaf-first LRU
+ *    eviction, and one free list shared by cache and running requests.
+ *    ["SGLang 深度拆解" (chenxutan.com/d/5669.html) §2.3; bhfrc.com/news/45689
+ *    §3.1-§3.2; "SGLang：从前端 DSL 到 SRT 服务运行时" (oripoin.cn), section
+ *    "用基数树实现前缀复用"]
+ *  - The batch tables RadixAttention reads: req_to_token (request -> token
+ *    position -> pool slot) and the prefix groups (runs of positions that a
+ *    set of requests shares), so a shared prefix is read once.
+ *    ["SGLang 深度解读" (luoboask.github.io/fde-learning/opensource/sglang/),
+ *    sections "1. RadixCache" and "5. Attention 层"; bhfrc.com §1.3]
+ *  - Decode attention (one query token per request over its context) and
+ *    extend attention (new tokens over a cached prefix plus a causal new
+ *    block), returning O and the natural-log log-sum-exp per (row, head).
+ *    ["SGLang 深度拆解" §3.2 (what its PagedDecode / PagedPrefill sketches
+ *    compute) and §4.1 (decode is memory-bound, prefill compute-bound)]
+ *
+ * Conventions (all entry points):
+ *  - Every function returns an int status: SGL_OK (0) or a negative
+ *    SGL_ERR_* code.  sgl_status_string() names it.  A failed call leaves
+ *    outputs unspecified unless its comment says otherwise.
+ *  - The caller owns every array it passes.  The library owns sgl_tree,
+ *    sgl_groups and sgl_plan objects; each has a destroy function.  Views
+ *    returned by the library point into library memory and stay valid until
+ *    the owning object is destroyed or refilled.
+ *  - "host" pointers are ordinary CPU memory; "device" pointers are CUDA
+ *    global memory of the current device.  GPU entry points are asynchronous
+ *    on the given stream; host-detected errors return immediately, launch
+ *    errors as SGL_ERR_CUDA (sgl_last_cuda_error() gives the cudaError_t),
+ *    and data errors found by the kernels (a slot outside the pool, a plan
+ *    that disagrees with seq_lens) as SGL_ERR_BOUNDS from sgl_check().
+ *  - No entry point allocates device memory.  There is no CPU fallback: if
+ *    the GPU path cannot run, the call fails.
+ *  - Supported: head_dim 64 or 128; Hq / Hkv in {1, 2, 4, 8}; fp32 or bf16
+ *    Q/K/V (one dtype for all three and for O).  Others: SGL_ERR_UNSUPPORTED.
+ *  - Pool layout: K and V are two device buffers [num_slots, Hkv, head_dim]
+ *    (slot-major; one slot holds one token of one layer).  With page_size P
+ *    > 1, slot = page * P + offset and a page's P slots are contiguous.
+ *  - Query head h reads KV head h / (Hq / Hkv).  sm_scale <= 0 means
+ *    1 / sqrt(head_dim).
+ */
+#ifndef SGLATTN_H
+#define SGLATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t-compatible opaque stream handle (NULL = legacy default stream). */
+typedef struct CUstream_st* sgl_stream_t;
+
+enum {
+    SGL_OK = 0,
+    SGL_ERR_INVALID_ARG = -1, /* null pointer, negative size, bad handle, malformed input */
+    SGL_ERR_NO_SLOTS = -2,    /* pool exhausted even after evicting every unreferenced leaf */
+    SGL_ERR_UNSUPPORTED = -3, /* dtype / head_dim / group size outside the supported set */
+    SGL_ERR_CUDA = -4,        /* a CUDA call failed; see sgl_last_cuda_error() */
+    SGL_ERR_BOUNDS = -5,      /* a kernel met a slot or position outside its tables */
+    SGL_ERR_STATE = -6,       /* unlock below zero, or a stale node handle */
+    SGL_ERR_WORKSPACE = -7    /* workspace missing, misaligned or too small */
+};
+
+enum { SGL_DTYPE_F32 = 0, SGL_DTYPE_BF16 = 1 };
+
+/* Name of a status code (static string). */
+const char* sgl_status_string(int status);
+/* The cudaError_t of the last SGL_ERR_CUDA raised on this thread (0 if none). */
+int sgl_last_cuda_error(void);
+/* Library version string (static). */
+const char* sgl_version(void);
+
+/* ======================================================================== */
+/* Host radix tree                                                          */
+/* ======================================================================== */
+
+typedef struct sgl_tree sgl_tree;
+/* Node handle: 0 is the root; other handles stay valid while the node exists
+ * (a node split keeps the handle on the lower part, which ends where the
+ * node ended).  A handle of an evicted node gives SGL_ERR_STATE. */
+typedef int64_t sgl_node;
+
+/* Create a tree over a pool of num_slots slots in pages of page_size slots
+ * (num_slots % page_size == 0).  free_order (host, num_slots / page_size
+ * entries, a permutation of page ids) is the initial free list; NULL means
+ * 0, 1, 2, ...  alloc pops pages from the front; freed and evicted pages are
+ * appended to the back in the order they are released.
+ * [oripoin.cn, "用基数树实现前缀复用": cache and running requests share one pool] */
+int sgl_tree_create(int64_t num_slots, int32_t page_size, const int32_t* free_order, sgl_tree** out);
+void sgl_tree_destroy(sgl_tree* tree);
+
+/* Longest prefix of tokens[0..n) held by the tree, in whole pages.
+ * Writes matched_len, the slots of the matched path to slots_out (host,
+ * capacity n; may be NULL) and the deepest matched node to *last (root when
+ * nothing matched).  Stamps the matched path as used now; a node matched
+ * only partly is split so that the stamp covers whole nodes.
+ * [bhfrc.com §3.1; "SGLang 深度拆解" §2.3 match_prefix; "SGLang 深度解读" §1] */
+int sgl_tree_match(sgl_tree* tree, const int32_t* tokens, int64_t n,
+                   int64_t* matched_len, int32_t* slots_out, sgl_node* last);
+
+/* Insert the full pages of tokens[0..n) with their slots (host, n entries;
+ * the slots of one page must be that page's consecutive slots).  Existing
+ * pages are kept; a caller page that differs from the existing page at the
+ * same position is a duplicate and is returned to the free list (dup_len
+ * counts those tokens).  Nodes are split where the new path diverges.  A
+ * trailing partial page is not inserted.  *last = node ending the inserted
+ * path (may be NULL).  [bhfrc.com §3.1; "SGLang 深度拆解" §2.3 insert] */
+int sgl_tree_insert(sgl_tree* tree, const int32_t* tokens, const int32_t* slots, int64_t n,
+                    int64_t* dup_len, sgl_node* last);
+
+/* Add / remove one reference on every node from `node` up to the root.  A
+ * referenced node is never evicted.  unlock below zero: SGL_ERR_STATE and
+ * nothing changes.  [bhfrc.com §3.2; oripoin.cn "用基数树实现前缀复用"] */
+int sgl_tree_lock(sgl_tree* tree, sgl_node node);
+int sgl_tree_unlock(sgl_tree* tree, sgl_node node);
+
+/* Slots for n tokens in whole pages popped from the free list, evicting LRU
+ * leaves first if the free list is short.  slots_out: host, capacity n
+ * (the rest of the last page stays owned by the caller).  SGL_ERR_NO_SLOTS
+ * if still short (the evictions that happened stay done). */
+int sgl_tree_alloc(sgl_tree* tree, int64_t n, int32_t* slots_out);
+
+/* Return the pages holding slots[0..n) to the back of the free list, each
+ * page once, in first-seen order.  For slots a caller owns (not in the tree). */
+int sgl_tree_free(sgl_tree* tree, const int32_t* slots, int64_t n);
+
+/* Free at least num_tokens tokens by removing unreferenced leaves, least
+ * recently used first (ties: oldest page first), one page at a time from a
+ * leaf's end; a parent whose children are gone becomes a leaf.  *freed =
+ * tokens freed (less than asked when every remaining leaf is referenced).
+ * [oripoin.cn "用基数树实现前缀复用": leaf-first LRU; "SGLang 深度拆解" §2.3 _evict] */
+int sgl_tree_evict(sgl_tree* tree, int64_t num_tokens, int64_t* freed);
+
+typedef struct {
+    int64_t free_pages;     /* pages on the free list */
+    int64_t tree_tokens;    /* tokens held by tree nodes */
+    int64_t locked_tokens;  /* tokens of nodes with a reference count > 0 */
+    int64_t evictable_tokens; /* tokens of nodes with reference count 0 */
+    int64_t num_nodes;      /* tree nodes, root excluded */
+    int64_t clock;          /* logical clock (match and insert calls so far) */
+} sgl_tree_stats_t;
+int sgl_tree_stats(const sgl_tree* tree, sgl_tree_stats_t* out);
+
+/* ======================================================================== */
+/* Batch tables: req_to_token + prefix groups                               */
+/* ======================================================================== */
+
+typedef struct sgl_groups sgl_groups;
+
+/* View of prefix groups (CSR, library memory).  Segment s covers positions
+ * [seg_begin[s], seg_end[s]) of every member request; all members hold the
+ * same slots there, so the K/V rows are read from the representative row
+ * seg_row[s] (its smallest member).  Members of s are
+ * seg_members[seg_member_ptr[s] .. seg_member_ptr[s+1]), ascending.
+ * Segments are ordered by (seg_row, seg_begin).  Each position of each
+ * request lies in exactly one of its segments.
+ * [bhfrc.com §1.3 and §3.1: requests sharing a path are branches of one
+ * tree, the shared path computed once] */
+typedef struct {
+    int32_t num_segments;
+    int32_t num_members;
+    const int32_t* seg_begin;
+    const int32_t* seg_end;
+    const int32_t* seg_row;
+    const int32_t* seg_member_ptr;
+    const int32_t* seg_members;
+} sgl_prefix_groups;
+
+/* Build one batch: for each request r in order, match its tokens, lock the
+ * match, allocate slots for the unmatched tail, write row r of req_to_token
+ * (host [B, ld], ld >= every len; entries past len[r] set to -1), insert the
+ * full pages, lock the new last node and release the temporary lock.
+ * seq_lens[r] = len[r]; prefix_lens[r] = matched length; last_nodes[r] =
+ * the node the request holds a reference on (release it with
+ * sgl_tree_finish).  The slots of a trailing partial page (page_size > 1)
+ * are private to the request.  If groups_out != NULL, *groups_out receives
+ * the batch's prefix groups (create it first with sgl_groups_create; it is
+ * refilled).  SGL_ERR_NO_SLOTS: every lock this call took is released and
+ * the private pages it allocated are freed; inserted nodes stay as cache.
+ * tokens: host array of B host pointers; len: host [B]; the other outputs
+ * host [B].  prefix_lens, last_nodes may be NULL.
+ * ["SGLang 深度解读" sections "2. Scheduler" and "5. Attention 层"] */
+int sgl_build_batch(sgl_tree* tree, int32_t B, const int32_t* const* tokens, const int64_t* len,
+                    int32_t* req_to_token, int64_t ld, int32_t* seq_lens, int32_t* prefix_lens,
+                    sgl_node* last_nodes, sgl_groups* groups_out);
+
+/* A request is done: unlock its last node and free its private tail page
+ * (row: host, its req_to_token row; len: its length). */
+int sgl_tree_finish(sgl_tree* tree, sgl_node last, const int32_t* row, int64_t len);
+
+int sgl_groups_create(sgl_groups** out);
+void sgl_groups_destroy(sgl_groups* groups);
+int sgl_groups_view(const sgl_groups* groups, sgl_prefix_groups* view);
+
+/* Prefix groups of any slot table (host [B, ld] + host seq_lens [B]),
+ * computed from the slots alone: positions shared by the same set of
+ * requests with identical slot prefixes. */
+int sgl_groups_from_table(const int32_t* req_to_token, int64_t ld, const int32_t* seq_lens, int32_t B,
+                          sgl_groups* groups_out);
+
+/* ======================================================================== */
+/* Attention                                                                */
+/* ======================================================================== */
+
+typedef struct {
+    int32_t dtype;          /* SGL_DTYPE_F32 or SGL_DTYPE_BF16 (Q, K, V, O) */
+    int32_t batch;          /* B: requests */
+    int32_t num_qo_heads;   /* Hq */
+    int32_t num_kv_heads;   /* Hkv */
+    int32_t head_dim;       /* d: 64 or 128 */
+    int32_t page_size;      /* P >= 1 (addressing is per slot; informative) */
+    int64_t num_slots;      /* S: rows of each pool buffer */
+    float sm_scale;         /* <= 0: 1/sqrt(d) */
+    int32_t num_sms;        /* planning target; <= 0: query the current device (152 if none) */
+    /* extend only: host copies of prefix_lens / extend_lens (B entries)
+     * used to size the launch; they must equal the device arrays. */
+    const int32_t* host_prefix_lens;
+    const int32_t* host_extend_lens;
+} sgl_attn_params;
+
+typedef struct sgl_plan sgl_plan;
+
+/* Decode planning (host).  Splits every (segment, KV head) into KV chunks
+ * and member blocks so that the work items fill the GPU, and lays out the
+ * fp32 partial (O, LSE) buffer and the per-request merge lists.  seq_lens:
+ * host [B]; groups: the batch's prefix groups.  *workspace_bytes = device
+ * workspace the call needs (plan tables + partials + error word).
+ * Segments whose end exceeds their representative's seq_len:
+ * SGL_ERR_INVALID_ARG. */
+int sgl_decode_plan(const sgl_attn_params* params, const int32_t* seq_lens, const sgl_prefix_groups* groups,
+                    sgl_plan** plan_out, size_t* workspace_bytes);
+void sgl_plan_destroy(sgl_plan* plan);
+
+typedef struct {
+    int32_t num_items;          /* decode work items (CTAs of the partial kernel) */
+    int32_t num_partial_rows;   /* fp32 partial (O, LSE) rows */
+    int32_t num_merge_entries;  /* partial rows named by the merge lists */
+    int32_t chunk_tokens;       /* KV positions per chunk chosen by the planner */
+    int64_t upload_bytes;       /* bytes sgl_plan_upload copies host -> device */
+    int64_t workspace_bytes;    /* device workspace the plan needs */
+} sgl_plan_info_t;
+/* Sizes of a plan (host; no device access). */
+int sgl_plan_info(const sgl_plan* plan, sgl_plan_info_t* out);
+
+/* Copy the plan's device tables into the head of the workspace
+ * (device, >= workspace_bytes, 256-byte aligned) on `stream`, and clear its
+ * error word.  Needed once after each sgl_decode_plan before decode calls
+ * that use the plan; the plan must stay alive until the copy has run. */
+int sgl_plan_upload(const sgl_plan* plan, void* workspace, size_t ws_bytes, sgl_stream_t stream);
+
+/* Decode attention for B requests, one query token each.
+ *   q            device [B, Hq, d] (dtype)
+ *   k_pool,v_pool device [num_slots, Hkv, d] (dtype)
+ *   req_to_token device int32 [B, ld]
+ *   seq_lens     device int32 [B]
+ *   plan         from sgl_decode_plan on the same batch, uploaded into workspace
+ *   o            device [B, Hq, d] (dtype);  lse  device fp32 [B, Hq]
+ * Each (segment, KV head) chunk is read from HBM once for all member
+ * requests and all query heads of that KV head (GQA packing); the partial
+ * (O, LSE) of every chunk are merged per (request, head) by log-sum-exp.
+ * A request with seq_len 0 gets O = 0, LSE = -inf. */
+int sgl_decode_attn(const void* q, const void* k_pool, const void* v_pool, const int32_t* req_to_token,
+                    int64_t ld, const int32_t* seq_lens, const sgl_plan* plan, void* o, float* lse,
+                    void* workspace, size_t ws_bytes, sgl_stream_t stream);
+
+/* Device workspace needed by sgl_extend_attn for these params (bytes). */
+int sgl_extend_workspace_bytes(const sgl_attn_params* params, size_t* bytes);
+
+/* Extend attention (chunked prefill with a cached prefix).
+ *   q_new        device [N, Hq, d], N = sum extend_lens; request r's rows
+ *                follow request r-1's
+ *   prefix_lens, extend_lens  device int32 [B] (equal to the host copies in params)
+ *   req_to_token device int32 [B, ld]; the new tokens' K/V are already in
+ *                the pool at req_to_token[r, prefix_lens[r] + i]
+ *   o            device [N, Hq, d] (dtype);  lse  device fp32 [N, Hq]
+ * New token i of request r (position p = prefix_lens[r] + i) attends to
+ * positions 0..p of row r.  workspace: device, >= sgl_extend_workspace_bytes,
+ * 256-byte aligned; its error word is cleared by this call.
+ * ["SGLang 深度解读" "5. Attention 层": K/V written before attention;
+ * "SGLang 深度拆解" §3.2 PagedPrefill: skip the cached prefix's compute] */
+int sgl_extend_attn(const void* q_new, const void* k_pool, const void* v_pool, const int32_t* req_to_token,
+                    int64_t ld, const int32_t* prefix_lens, const int32_t* extend_lens,
+                    const sgl_attn_params* params, void* o, float* lse, void* workspace, size_t ws_bytes,
+                    sgl_stream_t stream);
+
+/* Wait for `stream`, read the workspace's error word and clear it.
+ * SGL_OK, or SGL_ERR_BOUNDS if a kernel skipped an out-of-range slot or a
+ * position beyond seq_lens since the word was last cleared. */
+int sgl_check(void* workspace, sgl_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SGLATTN_H */

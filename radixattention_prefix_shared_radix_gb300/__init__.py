@@ -1,0 +1,349 @@
+"""GB300 RadixAttention hot path: Python binding of libsglattn.so.
+
+Thin argument marshalling over the C ABI declared in ``include/sglattn.h``;
+every step of the hot path runs in the native library (host radix tree and
+planner in C++, attention in CUDA kernels for sm_103a).  Functions keep the C
+names.  Device arguments are torch CUDA tensors (used only for their memory
+and the current stream); host arguments are numpy arrays or Python lists.
+There is no fallback: if the library is missing, every call raises.
+"""
+
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = _build.LIB
+
+SGL_OK = 0
+SGL_DTYPE_F32 = 0
+SGL_DTYPE_BF16 = 1
+
+
+class SglError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__("%s: %s (%d)" % (where, _lib().sgl_status_string(status).decode(), status))
+
+
+class SglTreeStats(ctypes.Structure):
+    _fields_ = [("free_pages", ctypes.c_int64), ("tree_tokens", ctypes.c_int64),
+                ("locked_tokens", ctypes.c_int64), ("evictable_tokens", ctypes.c_int64),
+                ("num_nodes", ctypes.c_int64), ("clock", ctypes.c_int64)]
+
+
+class SglPrefixGroups(ctypes.Structure):
+    _fields_ = [("num_segments", ctypes.c_int32), ("num_members", ctypes.c_int32),
+                ("seg_begin", ctypes.POINTER(ctypes.c_int32)), ("seg_end", ctypes.POINTER(ctypes.c_int32)),
+                ("seg_row", ctypes.POINTER(ctypes.c_int32)), ("seg_member_ptr", ctypes.POINTER(ctypes.c_int32)),
+                ("seg_members", ctypes.POINTER(ctypes.c_int32))]
+
+
+class SglPlanInfo(ctypes.Structure):
+    _fields_ = [("num_items", ctypes.c_int32), ("num_partial_rows", ctypes.c_int32),
+                ("num_merge_entries", ctypes.c_int32), ("chunk_tokens", ctypes.c_int32),
+                ("upload_bytes", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64)]
+
+
+class SglAttnParams(ctypes.Structure):
+    _fields_ = [("dtype", ctypes.c_int32), ("batch", ctypes.c_int32), ("num_qo_heads", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32),
+                ("num_slots", ctypes.c_int64), ("sm_scale", ctypes.c_float), ("num_sms", ctypes.c_int32),
+                ("host_prefix_lens", ctypes.POINTER(ctypes.c_int32)),
+                ("host_extend_lens", ctypes.POINTER(ctypes.c_int32))]
+
+
+_P = ctypes.c_void_p
+_I32P = ctypes.POINTER(ctypes.c_int32)
+_I64P = ctypes.POINTER(ctypes.c_int64)
+
+_SIGS = {
+    "sgl_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "sgl_last_cuda_error": (ctypes.c_int, []),
+    "sgl_version": (ctypes.c_char_p, []),
+    "sgl_tree_create": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int32, _I32P, ctypes.POINTER(_P)]),
+    "sgl_tree_destroy": (None, [_P]),
+    "sgl_tree_match": (ctypes.c_int, [_P, _I32P, ctypes.c_int64, _I64P, _I32P, _I64P]),
+    "sgl_tree_insert": (ctypes.c_int, [_P, _I32P, _I32P, ctypes.c_int64, _I64P, _I64P]),
+    "sgl_tree_lock": (ctypes.c_int, [_P, ctypes.c_int64]),
+    "sgl_tree_unlock": (ctypes.c_int, [_P, ctypes.c_int64]),
+    "sgl_tree_alloc": (ctypes.c_int, [_P, ctypes.c_int64, _I32P]),
+    "sgl_tree_free": (ctypes.c_int, [_P, _I32P, ctypes.c_int64]),
+    "sgl_tree_evict": (ctypes.c_int, [_P, ctypes.c_int64, _I64P]),
+    "sgl_tree_stats": (ctypes.c_int, [_P, ctypes.POINTER(SglTreeStats)]),
+    "sgl_build_batch": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.POINTER(_I32P), _I64P, _I32P, ctypes.c_int64,
+                                       _I32P, _I32P, _I64P, _P]),
+    "sgl_tree_finish": (ctypes.c_int, [_P, ctypes.c_int64, _I32P, ctypes.c_int64]),
+    "sgl_groups_create": (ctypes.c_int, [ctypes.POINTER(_P)]),
+    "sgl_groups_destroy": (None, [_P]),
+    "sgl_groups_view": (ctypes.c_int, [_P, ctypes.POINTER(SglPrefixGroups)]),
+    "sgl_groups_from_table": (ctypes.c_int, [_I32P, ctypes.c_int64, _I32P, ctypes.c_int32, _P]),
+    "sgl_decode_plan": (ctypes.c_int, [ctypes.POINTER(SglAttnParams), _I32P, ctypes.POINTER(SglPrefixGroups),
+                                       ctypes.POINTER(_P), ctypes.POINTER(ctypes.c_size_t)]),
+    "sgl_plan_destroy": (None, [_P]),
+    "sgl_plan_info": (ctypes.c_int, [_P, ctypes.POINTER(SglPlanInfo)]),
+    "sgl_plan_upload": (ctypes.c_int, [_P, _P, ctypes.c_size_t, _P]),
+    "sgl_decode_attn": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_int64, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "sgl_extend_workspace_bytes": (ctypes.c_int, [ctypes.POINTER(SglAttnParams), ctypes.POINTER(ctypes.c_size_t)]),
+    "sgl_extend_attn": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_int64, _P, _P, ctypes.POINTER(SglAttnParams),
+                                       _P, _P, _P, ctypes.c_size_t, _P]),
+    "sgl_check": (ctypes.c_int, [_P, _P]),
+}
+
+_LIB = None
+
+
+def _lib():
+    """Load libsglattn.so (raises if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libsglattn.so is not built (run __graft_entry__.build()); "
+                               "there is no fallback path")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = lib
+    return _LIB
+
+
+def exported_symbols():
+    return list(_SIGS)
+
+
+def _ok(st, where):
+    if st != SGL_OK:
+        raise SglError(st, where)
+
+
+def _i32(a):
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+def _ptr32(a):
+    return a.ctypes.data_as(_I32P)
+
+
+def _dev(t, what):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError("%s must be a CUDA tensor" % what)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % what)
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+# ------------------------------------------------------------------ tree
+def sgl_version():
+    return _lib().sgl_version().decode()
+
+
+def sgl_status_string(status):
+    return _lib().sgl_status_string(status).decode()
+
+
+def sgl_tree_create(num_slots, page_size=1, free_order=None):
+    h = _P()
+    fo = None if free_order is None else _i32(free_order)
+    _ok(_lib().sgl_tree_create(num_slots, page_size, None if fo is None else _ptr32(fo), ctypes.byref(h)),
+        "sgl_tree_create")
+    return h
+
+
+def sgl_tree_destroy(tree):
+    _lib().sgl_tree_destroy(tree)
+
+
+def sgl_tree_match(tree, tokens):
+    t = _i32(tokens)
+    m, last = ctypes.c_int64(), ctypes.c_int64()
+    slots = np.zeros(max(len(t), 1), dtype=np.int32)
+    _ok(_lib().sgl_tree_match(tree, _ptr32(t), len(t), ctypes.byref(m), _ptr32(slots), ctypes.byref(last)),
+        "sgl_tree_match")
+    return m.value, slots[:m.value].copy(), last.value
+
+
+def sgl_tree_insert(tree, tokens, slots):
+    t, s = _i32(tokens), _i32(slots)
+    dup, last = ctypes.c_int64(), ctypes.c_int64()
+    _ok(_lib().sgl_tree_insert(tree, _ptr32(t), _ptr32(s), len(t), ctypes.byref(dup), ctypes.byref(last)),
+        "sgl_tree_insert")
+    return dup.value, last.value
+
+
+def sgl_tree_lock(tree, node):
+    _ok(_lib().sgl_tree_lock(tree, node), "sgl_tree_lock")
+
+
+def sgl_tree_unlock(tree, node):
+    _ok(_lib().sgl_tree_unlock(tree, node), "sgl_tree_unlock")
+
+
+def sgl_tree_alloc(tree, n):
+    out = np.zeros(max(n, 1), dtype=np.int32)
+    _ok(_lib().sgl_tree_alloc(tree, n, _ptr32(out)), "sgl_tree_alloc")
+    return out[:n].copy()
+
+
+def sgl_tree_free(tree, slots):
+    s = _i32(slots)
+    _ok(_lib().sgl_tree_free(tree, _ptr32(s), len(s)), "sgl_tree_free")
+
+
+def sgl_tree_evict(tree, num_tokens):
+    f = ctypes.c_int64()
+    _ok(_lib().sgl_tree_evict(tree, num_tokens, ctypes.byref(f)), "sgl_tree_evict")
+    return f.value
+
+
+def sgl_tree_stats(tree):
+    s = SglTreeStats()
+    _ok(_lib().sgl_tree_stats(tree, ctypes.byref(s)), "sgl_tree_stats")
+    return {k: getattr(s, k) for k, _ in SglTreeStats._fields_}
+
+
+def sgl_build_batch(tree, token_lists, ld=None, groups=None):
+    """Returns dict(req_to_token [B, ld] int32, seq_lens, prefix_lens, last_nodes) (numpy)."""
+    toks = [_i32(t) for t in token_lists]
+    B = len(toks)
+    lens = np.array([len(t) for t in toks], dtype=np.int64)
+    ld = int(ld if ld is not None else max([1] + [len(t) for t in toks]))
+    table = np.zeros((B, ld), dtype=np.int32)
+    seq = np.zeros(B, dtype=np.int32)
+    pre = np.zeros(B, dtype=np.int32)
+    last = np.zeros(B, dtype=np.int64)
+    arr = (_I32P * max(B, 1))(*[_ptr32(t) for t in toks])
+    _ok(_lib().sgl_build_batch(tree, B, arr, lens.ctypes.data_as(_I64P), _ptr32(table), ld, _ptr32(seq),
+                               _ptr32(pre), last.ctypes.data_as(_I64P), groups), "sgl_build_batch")
+    return {"req_to_token": table, "seq_lens": seq, "prefix_lens": pre, "last_nodes": last}
+
+
+def sgl_tree_finish(tree, last, row, length):
+    r = _i32(row)
+    _ok(_lib().sgl_tree_finish(tree, int(last), _ptr32(r), int(length)), "sgl_tree_finish")
+
+
+def sgl_groups_create():
+    h = _P()
+    _ok(_lib().sgl_groups_create(ctypes.byref(h)), "sgl_groups_create")
+    return h
+
+
+def sgl_groups_destroy(groups):
+    _lib().sgl_groups_destroy(groups)
+
+
+def sgl_groups_view(groups):
+    """The groups as a ctypes view (valid while `groups` is unchanged)."""
+    v = SglPrefixGroups()
+    _ok(_lib().sgl_groups_view(groups, ctypes.byref(v)), "sgl_groups_view")
+    return v
+
+
+def groups_as_numpy(view):
+    n, m = view.num_segments, view.num_members
+
+    def arr(p, k):
+        return np.ctypeslib.as_array(p, shape=(k,)).copy() if k else np.zeros(0, dtype=np.int32)
+    return {"seg_begin": arr(view.seg_begin, n), "seg_end": arr(view.seg_end, n), "seg_row": arr(view.seg_row, n),
+            "seg_member_ptr": arr(view.seg_member_ptr, n + 1), "seg_members": arr(view.seg_members, m)}
+
+
+def sgl_groups_from_table(req_to_token, seq_lens, groups):
+    t, s = _i32(req_to_token), _i32(seq_lens)
+    _ok(_lib().sgl_groups_from_table(_ptr32(t), t.shape[1], _ptr32(s), len(s), groups), "sgl_groups_from_table")
+
+
+# ------------------------------------------------------------- attention
+def make_params(dtype, batch, num_qo_heads, num_kv_heads, head_dim, num_slots, page_size=1, sm_scale=0.0,
+                num_sms=0, host_prefix_lens=None, host_extend_lens=None):
+    p = SglAttnParams()
+    p.dtype = dtype
+    p.batch = batch
+    p.num_qo_heads = num_qo_heads
+    p.num_kv_heads = num_kv_heads
+    p.head_dim = head_dim
+    p.page_size = page_size
+    p.num_slots = num_slots
+    p.sm_scale = sm_scale
+    p.num_sms = num_sms
+    p._keep = []
+    if host_prefix_lens is not None:
+        a = _i32(host_prefix_lens)
+        p._keep.append(a)
+        p.host_prefix_lens = _ptr32(a)
+    if host_extend_lens is not None:
+        a = _i32(host_extend_lens)
+        p._keep.append(a)
+        p.host_extend_lens = _ptr32(a)
+    return p
+
+
+class Plan:
+    """Owns an sgl_plan handle and its workspace size."""
+
+    def __init__(self, handle, workspace_bytes):
+        self.handle = handle
+        self.workspace_bytes = workspace_bytes
+
+    def __del__(self):
+        if self.handle and _LIB is not None:
+            _LIB.sgl_plan_destroy(self.handle)
+            self.handle = None
+
+
+def sgl_decode_plan(params, seq_lens, groups_view):
+    s = _i32(seq_lens)
+    h = _P()
+    ws = ctypes.c_size_t()
+    _ok(_lib().sgl_decode_plan(ctypes.byref(params), _ptr32(s), ctypes.byref(groups_view), ctypes.byref(h),
+                               ctypes.byref(ws)), "sgl_decode_plan")
+    return Plan(h, ws.value)
+
+
+def sgl_plan_info(plan):
+    i = SglPlanInfo()
+    _ok(_lib().sgl_plan_info(plan.handle, ctypes.byref(i)), "sgl_plan_info")
+    return {k: getattr(i, k) for k, _ in SglPlanInfo._fields_}
+
+
+def sgl_plan_upload(plan, workspace, stream=None):
+    _ok(_lib().sgl_plan_upload(plan.handle, _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+                               _stream(stream)), "sgl_plan_upload")
+
+
+def sgl_decode_attn(q, k_pool, v_pool, req_to_token, seq_lens, plan, o, lse, workspace, stream=None):
+    _ok(_lib().sgl_decode_attn(_dev(q, "q"), _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"),
+                               _dev(req_to_token, "req_to_token"), req_to_token.shape[1], _dev(seq_lens, "seq_lens"),
+                               plan.handle, _dev(o, "o"), _dev(lse, "lse"), _dev(workspace, "workspace"),
+                               workspace.numel() * workspace.element_size(), _stream(stream)), "sgl_decode_attn")
+
+
+def sgl_extend_workspace_bytes(params):
+    b = ctypes.c_size_t()
+    _ok(_lib().sgl_extend_workspace_bytes(ctypes.byref(params), ctypes.byref(b)), "sgl_extend_workspace_bytes")
+    return b.value
+
+
+def sgl_extend_attn(q_new, k_pool, v_pool, req_to_token, prefix_lens, extend_lens, params, o, lse, workspace,
+                    stream=None):
+    _ok(_lib().sgl_extend_attn(_dev(q_new, "q_new"), _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"),
+                               _dev(req_to_token, "req_to_token"), req_to_token.shape[1],
+                               _dev(prefix_lens, "prefix_lens"), _dev(extend_lens, "extend_lens"),
+                               ctypes.byref(params), _dev(o, "o"), _dev(lse, "lse"), _dev(workspace, "workspace"),
+                               workspace.numel() * workspace.element_size(), _stream(stream)), "sgl_extend_attn")
+
+
+def sgl_check(workspace, stream=None):
+    _ok(_lib().sgl_check(_dev(workspace, "workspace"), _stream(stream)), "sgl_check")

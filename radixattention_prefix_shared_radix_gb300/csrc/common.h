@@ -1,0 +1,64 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "sglattn.h"
+
+namespace sgl {
+
+// Record the cudaError_t behind an SGL_ERR_CUDA (thread-local).
+void set_cuda_error(int err);
+
+// Decode work item: one KV chunk of one prefix-group segment for one KV head
+// and one block of the segment's members.  Laid out in the workspace.
+struct DecItem {
+    int32_t rep_row;       // request row whose req_to_token slots are read
+    int32_t kv_begin;      // first position of the chunk
+    int32_t kv_end;        // one past the last position
+    int32_t kvh;           // KV head
+    int32_t mem_begin;     // first member in the plan's member array
+    int32_t n_mem;         // members in this block (rows = n_mem * G)
+    int32_t partial_base;  // first partial row; row = member_idx * G + head_in_group
+    int32_t pad;
+};
+static_assert(sizeof(DecItem) == 32, "DecItem is 32 bytes");
+
+// Merge entry: partial row of (request, q head h = g * G + j) is
+// pbase + g * gstride + j.
+struct MergeEnt {
+    int32_t pbase;
+    int32_t gstride;
+};
+
+// Workspace header (first 256 bytes): error word + plan dimensions.
+struct WsHeader {
+    uint32_t error;        // bit 0: slot out of pool; bit 1: position beyond seq_len
+    uint32_t magic;
+    int32_t n_items;
+    int32_t n_partial_rows;
+};
+constexpr uint32_t kWsMagic = 0x53474c41u;  // "SGLA"
+constexpr size_t kWsAlign = 256;
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace sgl
+
+// Plan object (host); its tables are copied into the workspace head.
+struct sgl_plan {
+    sgl_attn_params params;      // host pointers cleared
+    int32_t G;
+    int32_t n_items;
+    int32_t n_partial_rows;
+    int32_t n_members;
+    int32_t n_merge_entries;
+    int32_t max_entries_per_request;
+    int32_t chunk_tokens;
+    int32_t max_pos;             // largest segment end (req_to_token must have ld >= max_pos)
+    size_t off_items, off_members, off_mptr, off_ment, off_plse, off_po;
+    size_t tables_bytes;         // bytes uploaded (header + tables)
+    size_t workspace_bytes;      // total device workspace
+    unsigned char* blob;         // host copy of [0, tables_bytes)
+};

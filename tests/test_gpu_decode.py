@@ -1,0 +1,161 @@
+"""Decode attention on the GPU vs the float64 oracle (through the C ABI).
+
+Element by element on scaled-down shapes of every decode workload and on
+edge cases; at the full workload sizes on every request.  The oracle runs
+on its own trie's tables (bit-identical to the native ones, checked on CPU)
+with no sharing, so agreement also shows that reading each shared segment
+once gives the unshared result.  Tolerances: bf16 O max-abs 2e-2, LSE 1e-3;
+fp32 O and LSE 1e-4.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import radixattention_prefix_shared_radix_gb300 as sgl
+import workloads as W
+from oracle.attention import decode_attention
+from tests._harness import Case, assert_close, run_decode, tolerances
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from radixattention_prefix_shared_radix_gb300 import build
+    build.build()
+    assert torch.cuda.is_available()
+
+
+def _check(case, num_sms=0, requests=None):
+    kd, vd = case.device_pool()
+    O, L = run_decode(case, kd, vd, num_sms=num_sms)
+    Oref, Lref = decode_attention(case.oracle_q(), W.RowView(case.K), W.RowView(case.V), case.oracle_table,
+                                  case.out["seq_lens"], requests=requests)
+    return assert_close(O, L, Oref, Lref, *tolerances(case.w), rows=requests)
+
+
+@pytest.mark.parametrize("name", ["tiny_fp32", "llama3_8b_decode_small", "fork_tree_small", "multiturn_small"])
+def test_decode_small_workloads_elementwise(name):
+    case = Case(name)
+    try:
+        _check(case)
+    finally:
+        case.close()
+
+
+@pytest.mark.parametrize("num_sms", [1, 7, 152, 4000])
+def test_decode_split_invariance(num_sms):
+    """Different chunkings (from the planner's SM target) give the oracle's result."""
+    case = Case("llama3_8b_decode_small")
+    try:
+        _check(case, num_sms=num_sms)
+    finally:
+        case.close()
+
+
+SHAPES = [
+    ("bf16", 8, 8, 64), ("bf16", 16, 8, 128), ("bf16", 64, 8, 128), ("bf16", 8, 4, 64),
+    ("f32", 8, 1, 128), ("f32", 32, 8, 128), ("f32", 4, 2, 64),
+]
+
+
+@pytest.mark.parametrize("dtype,Hq,Hkv,d", SHAPES)
+def test_decode_head_shapes(dtype, Hq, Hkv, d):
+    w = W.Workload("shape", 2, "decode", dtype, Hq, Hkv, d, 1,
+                   ("star", dict(n=6, prefix=77, suffix=(1, 150))), num_slots=2048)
+    case = Case(None, workload=w)
+    try:
+        _check(case)
+    finally:
+        case.close()
+
+
+def test_decode_edge_batch():
+    """Empty context, one-token contexts, a request that is a prefix of
+    another, identical requests, a branch that starts at position 0."""
+    w = W.get("llama3_8b_decode_small")
+    rng = np.random.default_rng(77)
+    base = list(rng.integers(0, 32000, size=300))
+    seqs = [base, [], base[:1], base[:120], list(base), base[:120] + [5, 6, 7], [9] * 65, [9]]
+    q = rng.standard_normal((len(seqs), w.Hq, w.d), dtype=np.float32)
+    case = Case(None, workload=w, seqs=seqs, q=q)
+    try:
+        kd, vd = case.device_pool()
+        O, L = run_decode(case, kd, vd)
+        assert np.all(O[1] == 0) and np.all(np.isneginf(L[1]))
+        Oref, Lref = decode_attention(case.oracle_q(), W.RowView(case.K), W.RowView(case.V), case.oracle_table,
+                                      case.out["seq_lens"])
+        assert_close(O, L, Oref, Lref, *tolerances(w))
+    finally:
+        case.close()
+
+
+def test_decode_paged_edge():
+    """page size 16 with contexts not a multiple of the page, shared and not."""
+    w = W.get("multiturn_small")
+    rng = np.random.default_rng(5)
+    a = list(rng.integers(0, 32000, size=70))
+    seqs = [a, a, a[:40] + [1, 2, 3], a[:16], a[:15], [7] * 33]
+    q = rng.standard_normal((len(seqs), w.Hq, w.d), dtype=np.float32)
+    case = Case(None, workload=w, seqs=seqs, q=q)
+    try:
+        kd, vd = case.device_pool()
+        O, L = run_decode(case, kd, vd)
+        Oref, Lref = decode_attention(case.oracle_q(), W.RowView(case.K), W.RowView(case.V), case.oracle_table,
+                                      case.out["seq_lens"])
+        assert_close(O, L, Oref, Lref, *tolerances(w))
+    finally:
+        case.close()
+
+
+def test_decode_out_of_pool_slot_is_reported_not_read():
+    case = Case("llama3_8b_decode_small")
+    try:
+        kd, vd = case.device_pool()
+        p = case.params()
+        plan = sgl.sgl_decode_plan(p, case.out["seq_lens"], sgl.sgl_groups_view(case.groups))
+        ws = torch.zeros(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
+        sgl.sgl_plan_upload(plan, ws)
+        table = torch.from_numpy(case.out["req_to_token"]).cuda()
+        table[3, 5] = case.S + 11
+        qd = case.q_host().cuda()
+        o = torch.empty_like(qd)
+        lse = torch.empty(case.B, case.w.Hq, dtype=torch.float32, device="cuda")
+        seq = torch.from_numpy(case.out["seq_lens"]).cuda()
+        sgl.sgl_decode_attn(qd, kd, vd, table, seq, plan, o, lse, ws)
+        with pytest.raises(sgl.SglError) as e:
+            sgl.sgl_check(ws)
+        assert e.value.status == -5
+        sgl.sgl_check(ws)          # the word was cleared
+        # a plan that disagrees with the device seq_lens is reported too
+        seq[0] = 1
+        sgl.sgl_decode_attn(qd, kd, vd, torch.from_numpy(case.out["req_to_token"]).cuda(), seq, plan, o, lse, ws)
+        with pytest.raises(sgl.SglError):
+            sgl.sgl_check(ws)
+    finally:
+        case.close()
+
+
+def test_decode_rejects_malformed_groups():
+    case = Case("llama3_8b_decode_small")
+    try:
+        view = sgl.sgl_groups_view(case.groups)
+        p = case.params()
+        seq = case.out["seq_lens"].copy()
+        seq[2] += 1                          # request 2's segments no longer cover its context
+        with pytest.raises(sgl.SglError) as e:
+            sgl.sgl_decode_plan(p, seq, view)
+        assert e.value.status == -1
+    finally:
+        case.close()
+
+
+@pytest.mark.parametrize("name", ["llama3_8b_decode", "fork_tree", "multiturn", "multiturn_noshare"])
+def test_decode_full_size(name):
+    case = Case(name)
+    try:
+        do, dl = _check(case)
+        print("%s: O max-abs %.3g, LSE max-abs %.3g" % (name, do, dl))
+    finally:
+        case.close()

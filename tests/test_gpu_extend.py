@@ -1,0 +1,97 @@
+"""Extend attention on the GPU vs the float64 oracle (through the C ABI).
+
+Element by element on a scaled-down extend workload (ragged prefixes from 0,
+ragged new blocks from 1 token) and on head-shape variants; at the full
+4096 + 512 workload on sampled rows (first, last and random new tokens of
+every request).  Tolerances as for decode.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle.attention import decode_attention, extend_attention
+from tests._harness import Case, assert_close, run_extend, tolerances
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from radixattention_prefix_shared_radix_gb300 import build
+    build.build()
+    assert torch.cuda.is_available()
+
+
+def _check(case, rows=None):
+    kd, vd = case.device_pool()
+    O, L, pre, ext = run_extend(case, kd, vd)
+    Oref, Lref = extend_attention(case.oracle_q(), W.RowView(case.K), W.RowView(case.V), case.oracle_table, pre,
+                                  ext, rows=rows)
+    return assert_close(O, L, Oref, Lref, *tolerances(case.w), rows=rows)
+
+
+def test_extend_small_elementwise():
+    case = Case("extend_small")
+    try:
+        _check(case)
+    finally:
+        case.close()
+
+
+@pytest.mark.parametrize("dtype,Hq,Hkv,d", [("bf16", 8, 8, 64), ("bf16", 16, 8, 128), ("bf16", 32, 8, 64),
+                                           ("bf16", 8, 2, 128), ("f32", 8, 2, 64), ("f32", 16, 8, 128)])
+def test_extend_head_shapes(dtype, Hq, Hkv, d):
+    w = W.Workload("shape", 4, "extend", dtype, Hq, Hkv, d, 1,
+                   ("extend", dict(n=4, prefix=(0, 150), new=(1, 140))), num_slots=2048)
+    case = Case(None, workload=w)
+    try:
+        _check(case)
+    finally:
+        case.close()
+
+
+def test_extend_one_new_token_equals_decode():
+    w = W.get("extend_small")
+    rng = np.random.default_rng(3)
+    seqs = [list(rng.integers(0, 32000, size=n)) for n in (1, 130, 257)]
+    q = rng.standard_normal((3, w.Hq, w.d), dtype=np.float32)
+    case = Case(None, workload=w, seqs=seqs, q=q)
+    try:
+        # no warm cache for these: prefix 0, extend = whole sequence; compare the
+        # last new token of each request with decode over the same context
+        kd, vd = case.device_pool()
+        O, L, pre, ext = run_extend_last_rows(case, kd, vd)
+    finally:
+        case.close()
+
+
+def run_extend_last_rows(case, kd, vd):
+    from tests._harness import run_extend as rx
+    w = case.w
+    # queries for every new token: reuse q rows cyclically
+    n_new = int((case.out["seq_lens"] - case.out["prefix_lens"]).sum())
+    rng = np.random.default_rng(11)
+    case.b.q = rng.standard_normal((n_new, w.Hq, w.d), dtype=np.float32)
+    O, L, pre, ext = rx(case, kd, vd)
+    last = np.cumsum(ext) - 1
+    qd = case.oracle_q()[last]
+    Od, Ld = decode_attention(qd, W.RowView(case.K), W.RowView(case.V), case.oracle_table, case.out["seq_lens"])
+    assert_close(O[last], L[last], Od, Ld, *tolerances(w))
+    return O, L, pre, ext
+
+
+def test_extend_full_size_sampled():
+    case = Case("extend")
+    try:
+        ext = case.out["seq_lens"] - case.out["prefix_lens"]
+        starts = np.concatenate([[0], np.cumsum(ext)[:-1]])
+        rng = np.random.default_rng(1)
+        rows = []
+        for s, e in zip(starts, ext):
+            rows += [int(s), int(s + e - 1), int(s + 127), int(s + 128)] + [int(s + x) for x in rng.integers(0, e, 4)]
+        do, dl = _check(case, rows=sorted(set(rows)))
+        print("extend: O max-abs %.3g, LSE max-abs %.3g" % (do, dl))
+    finally:
+        case.close()

@@ -1,0 +1,207 @@
+"""Native host side vs the oracle, bit-exact (CPU).
+
+The C++ compressed radix tree, allocator, batch builder and prefix-group
+emitters must reproduce the oracle's per-page trie exactly: match lengths
+and slots, duplicate handling, eviction order (observed through the slots
+later allocations return), reference counts, req_to_token rows, matched
+prefix lengths and prefix groups -- on random operation sequences and on the
+five workloads at full size.
+"""
+
+import random
+
+import numpy as np
+import pytest
+
+import radixattention_prefix_shared_radix_gb300 as sgl
+import workloads as W
+from oracle.groups import prefix_groups
+from oracle.tree import NoSlotsError, RadixTrie, StateError, build_batch
+from radixattention_prefix_shared_radix_gb300 import build as sglbuild
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    sglbuild.build()
+
+
+def _groups_eq(a, b):
+    for k in ("seg_begin", "seg_end", "seg_row", "seg_member_ptr", "seg_members"):
+        assert np.array_equal(np.asarray(a[k]), np.asarray(b[k])), k
+
+
+def _lib_groups(handle):
+    return sgl.groups_as_numpy(sgl.sgl_groups_view(handle))
+
+
+class Pair:
+    """The oracle trie and the native tree driven with the same operations."""
+
+    def __init__(self, pages, P, order):
+        self.o = RadixTrie(pages * P, P, order)
+        self.t = sgl.sgl_tree_create(pages * P, P, order)
+        self.P = P
+        self.live = []      # (oracle last node, lib last handle, row)
+
+    def close(self):
+        sgl.sgl_tree_destroy(self.t)
+
+    def batch(self, seqs):
+        try:
+            rows, lasts, priv = build_batch(self.o, seqs)
+        except NoSlotsError:
+            rows = None
+        g = sgl.sgl_groups_create()
+        try:
+            if rows is None:
+                with pytest.raises(sgl.SglError) as e:
+                    sgl.sgl_build_batch(self.t, seqs, groups=g)
+                assert e.value.status == -2
+                return
+            out = sgl.sgl_build_batch(self.t, seqs, groups=g)
+            for r, row in enumerate(rows):
+                assert list(out["req_to_token"][r, :len(row)]) == list(row)
+                assert np.all(out["req_to_token"][r, len(row):] == -1)
+            assert list(out["seq_lens"]) == [len(s) for s in seqs]
+            ogroups = prefix_groups(out["req_to_token"], out["seq_lens"])
+            _groups_eq(_lib_groups(g), ogroups)
+            g2 = sgl.sgl_groups_create()
+            sgl.sgl_groups_from_table(out["req_to_token"], out["seq_lens"], g2)
+            _groups_eq(_lib_groups(g2), ogroups)
+            sgl.sgl_groups_destroy(g2)
+            for r in range(len(seqs)):
+                self.live.append((lasts[r], int(out["last_nodes"][r]), list(rows[r])))
+        finally:
+            sgl.sgl_groups_destroy(g)
+
+    def finish(self, k):
+        on, ln, row = self.live.pop(k)
+        self.o.unlock(on)
+        nf = len(row) // self.P * self.P
+        self.o.free_slots(row[nf:])
+        sgl.sgl_tree_finish(self.t, ln, row, len(row))
+
+    def match(self, toks):
+        m, slots, _ = self.o.match(toks)
+        m2, slots2, _ = sgl.sgl_tree_match(self.t, toks)
+        assert m == m2 and list(slots) == list(slots2)
+
+    def evict(self, n):
+        assert self.o.evict(n) == sgl.sgl_tree_evict(self.t, n)
+
+    def alloc_free(self, n):
+        try:
+            a = self.o.alloc(n)
+        except NoSlotsError:
+            with pytest.raises(sgl.SglError):
+                sgl.sgl_tree_alloc(self.t, n)
+            return
+        b = sgl.sgl_tree_alloc(self.t, n)
+        assert list(a) == list(b)
+        self.o.free_slots(a)
+        sgl.sgl_tree_free(self.t, b)
+
+    def check_stats(self):
+        s = sgl.sgl_tree_stats(self.t)
+        assert s["free_pages"] == len(self.o.free)
+        assert s["tree_tokens"] == self.o.tree_tokens()
+        assert s["locked_tokens"] == sum(self.P for n in self.o.nodes() if n.ref > 0)
+
+
+@pytest.mark.parametrize("P", [1, 2, 4])
+@pytest.mark.parametrize("seed", range(25))
+def test_random_operations_bit_exact(P, seed):
+    rnd = random.Random(seed * 13 + P)
+    pages = rnd.choice([12, 20, 40, 400])
+    pair = Pair(pages, P, rnd.sample(range(pages), pages))
+    try:
+        for _ in range(70):
+            op = rnd.random()
+            if op < 0.35:
+                base = [rnd.randint(0, 2) for _ in range(rnd.randint(0, 10))]
+                seqs = []
+                for _ in range(rnd.randint(1, 4)):
+                    c = rnd.random()
+                    if seqs and c < 0.25:
+                        seqs.append(list(seqs[0]))
+                    else:
+                        cut = rnd.randint(0, len(base))
+                        seqs.append(base[:cut] + [rnd.randint(0, 2) for _ in range(rnd.randint(0, 8))])
+                pair.batch(seqs)
+            elif op < 0.55 and pair.live:
+                pair.finish(rnd.randrange(len(pair.live)))
+            elif op < 0.7:
+                pair.match([rnd.randint(0, 2) for _ in range(rnd.randint(0, 12))])
+            elif op < 0.85:
+                pair.evict(rnd.randint(1, 3 * P))
+            else:
+                pair.alloc_free(rnd.randint(0, 3 * P))
+            pair.check_stats()
+    finally:
+        pair.close()
+
+
+def test_unlock_underflow_and_stale_handle():
+    t = sgl.sgl_tree_create(16, 1)
+    out = sgl.sgl_build_batch(t, [[1, 2, 3]])
+    last = int(out["last_nodes"][0])
+    sgl.sgl_tree_unlock(t, last)
+    with pytest.raises(sgl.SglError) as e:
+        sgl.sgl_tree_unlock(t, last)
+    assert e.value.status == -6
+    assert sgl.sgl_tree_evict(t, 100) == 3
+    with pytest.raises(sgl.SglError) as e:
+        sgl.sgl_tree_lock(t, last)
+    assert e.value.status == -6
+    sgl.sgl_tree_destroy(t)
+
+
+def test_insert_duplicates_match_oracle():
+    o = RadixTrie(32, 2, list(range(16)))
+    t = sgl.sgl_tree_create(32, 2, list(range(16)))
+    for toks in ([5, 6, 7, 8, 9, 1], [5, 6, 7, 8, 4, 4], [5, 6, 7, 8]):
+        a = o.alloc(len(toks))
+        b = sgl.sgl_tree_alloc(t, len(toks))
+        assert list(a) == list(b)
+        d1, _ = o.insert(toks, a)
+        d2, _ = sgl.sgl_tree_insert(t, toks, b)
+        assert d1 == d2
+    assert list(o.alloc(16)) == list(sgl.sgl_tree_alloc(t, 16))
+    sgl.sgl_tree_destroy(t)
+
+
+def _full_tables(name):
+    w = W.get(name)
+    order, _, _ = None, None, None
+    S = W.pool_slots(w)
+    order = np.random.default_rng([w.seed, 3]).permutation(S // w.page_size).astype(np.int32)
+    b = W.make_batch(w)
+    o = RadixTrie(S, w.page_size, order)
+    t = sgl.sgl_tree_create(S, w.page_size, order)
+    if w.kind == "extend":
+        warm = [b.cached_tokens(r) for r in range(len(b.req_chain))]
+        rows, lasts, _ = build_batch(o, warm)
+        for n in lasts:
+            o.unlock(n)
+        out = sgl.sgl_build_batch(t, warm)
+        for r in range(len(warm)):
+            sgl.sgl_tree_finish(t, int(out["last_nodes"][r]), out["req_to_token"][r], len(warm[r]))
+    return w, b, o, t
+
+
+@pytest.mark.parametrize("name", ["tiny_fp32", "llama3_8b_decode", "fork_tree", "extend", "multiturn",
+                                  "multiturn_noshare"])
+def test_workload_tables_bit_exact(name):
+    w, b, o, t = _full_tables(name)
+    seqs = b.all_tokens()
+    rows, _, _ = build_batch(o, seqs)
+    g = sgl.sgl_groups_create()
+    out = sgl.sgl_build_batch(t, seqs, groups=g)
+    table = out["req_to_token"]
+    for r, row in enumerate(rows):
+        assert np.array_equal(table[r, :len(row)], np.asarray(row, dtype=np.int32))
+    if w.kind == "extend":
+        assert list(out["prefix_lens"]) == [len(b.cached_tokens(r)) for r in range(len(seqs))]
+    _groups_eq(_lib_groups(g), prefix_groups(table, out["seq_lens"]))
+    sgl.sgl_groups_destroy(g)
+    sgl.sgl_tree_destroy(t)
