@@ -36,7 +36,8 @@ struct MergeEnt {
 struct WsHeader {
     uint32_t error;        // bit 0: slot out of pool; bit 1: position beyond seq_len
     uint32_t magic;
-    int32_t n_items;
+    int32_t n_items;             // all work items: wide ones first, then narrow ones
+    int32_t n_wide;              // items with more than 8 query rows (tcgen05 tile kernel)
     int32_t n_partial_rows;
 };
 constexpr uint32_t kWsMagic = 0x53474c41u;  // "SGLA"
@@ -50,14 +51,15 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 struct sgl_plan {
     sgl_attn_params params;      // host pointers cleared
     int32_t G;
-    int32_t n_items;
+    int32_t n_items;             // all work items: wide ones first, then narrow ones
+    int32_t n_wide;              // items with more than 8 query rows (tcgen05 tile kernel)
     int32_t n_partial_rows;
     int32_t n_members;
     int32_t n_merge_entries;
     int32_t max_entries_per_request;
     int32_t chunk_tokens;
     int32_t max_pos;             // largest segment end (req_to_token must have ld >= max_pos)
-    size_t off_items, off_members, off_mptr, off_ment, off_plse, off_po;
+    size_t off_items, off_members, off_mptr, off_ment, off_plse, off_po, off_cnt;
     size_t tables_bytes;         // bytes uploaded (header + tables)
     size_t workspace_bytes;      // total device workspace
     unsigned char* blob;         // host copy of [0, tables_bytes)

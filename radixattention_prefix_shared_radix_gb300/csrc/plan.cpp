@@ -7,15 +7,16 @@
 // referenced many times" ("SGLang：从前端 DSL 到 SRT 服务运行时", section
 // "用基数树实现前缀复用"; bhfrc.com/news/45689 §1.3).  The pages give no
 // kernel schedule; this one is ours:
-//   * members are packed in blocks of up to 64 query rows (member x query
-//     head of the KV head), the rows one tensor-core tile pass covers;
-//   * every (segment, member block, KV head) is split along positions into
-//     chunks of C tokens, C a multiple of the 64-token KV tile, sized so the
-//     whole batch yields about 4 work items per SM; segments shorter than C
-//     are one chunk;
-//   * items are ordered chunk-major with the KV head innermost, so CTAs that
-//     run together read the heads of the same tokens (one token's K for all
-//     heads is one contiguous row of the slot-major pool);
+//   * a segment with at most 8 query rows (member x query head of a KV
+//     head) is narrow: its chunks go to a one-warp-per-item kernel, chunk
+//     length sized for ~24 warps of work per SM (>= 64 positions);
+//   * a wider segment (a prefix shared by many requests) is split into member
+//     blocks of up to 128 rows (one tensor-core tile), each chunk read once per
+//     block by a CTA that stages it in shared memory (tcgen05 kernel), chunk
+//     length a multiple of the 128-position KV block sized for ~1 CTA per SM;
+//   * items are ordered chunk-major with the KV head innermost, so work that
+//     runs together reads the heads of the same tokens (one token's K for
+//     all heads is one contiguous row of the slot-major pool);
 //   * each item writes its rows' normalised partial O and LSE (fp32); a
 //     request's merge list names every partial row it must combine.
 
@@ -104,26 +105,41 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
         if (at != seq_lens[r]) return SGL_ERR_INVALID_ARG;
     }
 
-    const int32_t MB = std::max(1, 64 / G);   // members per block: at most 64 query rows
-    double units = 0;
+    // Narrow segments (at most 8 query rows: member x query head of a KV
+    // head) go to the one-warp-per-item kernel; wider ones to the CTA kernel
+    // in member blocks of up to 64 rows.
+    const int32_t MBn = std::max(1, 8 / G);
+    const int32_t MBw = std::max(1, 128 / G);
+    double units_n = 0, units_w = 0;
     for (int32_t s = 0; s < nseg; ++s) {
-        int32_t nmem = g->seg_member_ptr[s + 1] - g->seg_member_ptr[s];
-        units += (double)(g->seg_end[s] - g->seg_begin[s]) * ((nmem + MB - 1) / MB) * Hkv;
+        const int32_t nmem = g->seg_member_ptr[s + 1] - g->seg_member_ptr[s];
+        const double len = (double)(g->seg_end[s] - g->seg_begin[s]);
+        if (nmem <= MBn)
+            units_n += len * Hkv;
+        else
+            units_w += len * ((nmem + MBw - 1) / MBw) * Hkv;
     }
     const int sms = query_num_sms(p->num_sms);
-    const double target = 4.0 * sms;
-    int64_t C = (int64_t)std::ceil(units / target);
-    C = std::max<int64_t>(64, (C + 63) / 64 * 64);
+    // narrow: ~24 warps of work per SM (16-position steps, chunks of >= 64)
+    int64_t Cn = (int64_t)std::ceil(units_n / (24.0 * sms));
+    Cn = std::max<int64_t>(64, (Cn + 15) / 16 * 16);
+    // wide: ~1 CTA of work per SM (128-position KV blocks)
+    int64_t Cw = (int64_t)std::ceil(units_w / (1.0 * sms));
+    Cw = std::max<int64_t>(128, (Cw + 127) / 128 * 128);
+    const int64_t C = Cn;
 
-    std::vector<sgl::DecItem> items;
+    std::vector<sgl::DecItem> wide, narrow;
     std::vector<std::vector<sgl::MergeEnt>> ents(B);
     int64_t prow = 0;
     for (int32_t s = 0; s < nseg; ++s) {
         const int32_t b = g->seg_begin[s], e = g->seg_end[s];
         const int32_t m0 = g->seg_member_ptr[s], nmem = g->seg_member_ptr[s + 1] - m0;
+        const bool is_narrow = nmem <= MBn;
+        const int32_t MB = is_narrow ? MBn : MBw;
+        const int64_t CS = is_narrow ? Cn : Cw;
         const int32_t nblk = (nmem + MB - 1) / MB;
-        for (int64_t cb = b; cb < e; cb += C) {
-            const int32_t ce = (int32_t)std::min<int64_t>(e, cb + C);
+        for (int64_t cb = b; cb < e; cb += CS) {
+            const int32_t ce = (int32_t)std::min<int64_t>(e, cb + CS);
             for (int32_t blk = 0; blk < nblk; ++blk) {
                 const int32_t mb = blk * MB, nm = std::min(MB, nmem - mb);
                 const int64_t base0 = prow;
@@ -137,7 +153,7 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
                     it.n_mem = nm;
                     it.partial_base = (int32_t)prow;
                     it.pad = 0;
-                    items.push_back(it);
+                    (is_narrow ? narrow : wide).push_back(it);
                     prow += (int64_t)nm * G;
                 }
                 for (int32_t i = 0; i < nm; ++i) {
@@ -148,6 +164,8 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
         }
     }
     if (prow > INT32_MAX / 256) return SGL_ERR_UNSUPPORTED;
+    std::vector<sgl::DecItem> items(wide);
+    items.insert(items.end(), narrow.begin(), narrow.end());
 
     sgl_plan* plan = new (std::nothrow) sgl_plan();
     if (!plan) return SGL_ERR_INVALID_ARG;
@@ -156,6 +174,7 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
     plan->params.host_extend_lens = nullptr;
     plan->G = G;
     plan->n_items = (int32_t)items.size();
+    plan->n_wide = (int32_t)wide.size();
     plan->n_partial_rows = (int32_t)prow;
     plan->n_members = g->num_members;
     int64_t n_ent = 0;
@@ -179,7 +198,8 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
     plan->tables_bytes = align_up(plan->off_ment + (size_t)n_ent * sizeof(sgl::MergeEnt), A);
     plan->off_plse = plan->tables_bytes;
     plan->off_po = align_up(plan->off_plse + (size_t)prow * 4, A);
-    plan->workspace_bytes = align_up(plan->off_po + (size_t)prow * p->head_dim * 4, A);
+    plan->off_cnt = align_up(plan->off_po + (size_t)prow * p->head_dim * 4, A);
+    plan->workspace_bytes = align_up(plan->off_cnt + (size_t)B * Hkv * 4, A);
 
     plan->blob = new (std::nothrow) unsigned char[plan->tables_bytes];
     if (!plan->blob) {

@@ -118,7 +118,9 @@ def test_decode_out_of_pool_slot_is_reported_not_read():
         ws = torch.zeros(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
         sgl.sgl_plan_upload(plan, ws)
         table = torch.from_numpy(case.out["req_to_token"]).cuda()
-        table[3, 5] = case.S + 11
+        # a position of request 3's own suffix (shared prefix positions are
+        # read from the segment's representative row, row 0)
+        table[3, int(case.out["seq_lens"][3]) - 1] = case.S + 11
         qd = case.q_host().cuda()
         o = torch.empty_like(qd)
         lse = torch.empty(case.B, case.w.Hq, dtype=torch.float32, device="cuda")
