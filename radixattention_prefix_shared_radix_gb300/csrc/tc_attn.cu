@@ -28,7 +28,8 @@
 // operand) into the TMEM accumulator.  O is rescaled in TMEM only when a
 // row's max grows by more than 8 (a factor 2^8, harmless in fp32), so most
 // blocks need no correction pass.  S_{j+1} runs on the tensor core while the
-// softmax of block j runs.  All waits are bounded: one that gives up sets bit
+// softmax of block j runs; the softmax reads its whole 128-score row with
+// four TMEM loads in flight and a single wait.  All waits are bounded: one that gives up sets bit
 // 2 of the workspace error word and the kernel runs to its end without
 // hanging (its results are then garbage, and flagged).
 
@@ -87,6 +88,20 @@ __device__ __forceinline__ void tld32(uint32_t taddr, float (&v)[32]) {
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
+// Same load without the wait: several can be in flight before one tld_wait().
+__device__ __forceinline__ void tld32_nw(uint32_t taddr, float* v) {
+    uint32_t* r = reinterpret_cast<uint32_t*>(v);
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%"
+        "19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+          "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
+
 __device__ __forceinline__ void tst32(uint32_t taddr, const float (&v)[32]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%"
@@ -152,7 +167,6 @@ constexpr int B_SFULL = B_KVEMPTY + kNS;     // + buffer
 constexpr int B_SFREE = B_SFULL + 2;         // + buffer
 constexpr int B_PFULL = B_SFREE + 2;
 constexpr int B_OFULL = B_PFULL + 1;
-constexpr int B_COUNT = B_OFULL + 1;
 
 template <bool DEC>
 __device__ void tile_setup(const TcArgs& a, int* info) {
@@ -368,26 +382,57 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_attn_kernel(const TcArgs a) 
             tc_fence_after();
             const int pos0 = kv_begin + j * 128;
             const bool full_blk = pos0 + 127 < kv_end && pos0 + 127 <= lim;
+            // the whole S row in registers: four loads in flight, one wait
+            float srow[128];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tld32_nw(tl + sb * 128 + 32 * c, srow + 32 * c);
+            tld_wait();
             float mx = -INFINITY;
+            if (full_blk) {
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                tld32(tl + sb * 128 + 32 * c, v);
+                for (int k = 0; k < 128; ++k) {
+                    srow[k] *= sc;
+                    mx = fmaxf(mx, srow[k]);
+                }
+            } else {
 #pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    const int pos = pos0 + 32 * c + k;
-                    const float s = (full_blk || (pos < kv_end && pos <= lim)) ? v[k] * sc : -INFINITY;
-                    mx = fmaxf(mx, s);
+                for (int k = 0; k < 128; ++k) {
+                    const int pos = pos0 + k;
+                    srow[k] = (pos < kv_end && pos <= lim) ? srow[k] * sc : -INFINITY;
+                    mx = fmaxf(mx, srow[k]);
                 }
             }
             const float m_new = fmaxf(m_used, mx);
             const bool need = m_new > m_used + 8.f;   // also true for the first finite max
+            const float m_old = m_used;
+            if (need) {
+                if (m_used != -INFINITY) l *= exp2f(m_used - m_new);
+                m_used = m_new;
+            }
+            const float mu = m_used == -INFINITY ? 0.f : m_used;
+            // P must not overwrite the tile PV_{j-1} is still reading
             if (j > 0) {
                 wait(B_OFULL, (j - 1) & 1);
                 tc_fence_after();
-                const bool rescale = need && m_used != -INFINITY;
-                if (__any_sync(0xffffffffu, rescale)) {
-                    const float al = rescale ? exp2f(m_used - m_new) : 1.f;
+            }
 #pragma unroll
+            for (int c = 0; c < 16; ++c) {       // 8 positions per 16-byte chunk of the P row
+                uint32_t pk[4];
+#pragma unroll
+                for (int k = 0; k < 8; k += 2) {
+                    const float p0 = exp2f(srow[8 * c + k] - mu);      // -inf -> 0
+                    const float p1 = exp2f(srow[8 * c + k + 1] - mu);
+                    l += p0 + p1;
+                    pk[k / 2] = pack_bf16(p0, p1);
+                }
+                *reinterpret_cast<uint4*>(sPg + sw128(i, c)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+            // O holds blocks < j scaled to the old max: rescale before PV_j adds to it
+            if (j > 0) {
+                const bool rescale = need && m_old != -INFINITY;
+                if (__any_sync(0xffffffffu, rescale)) {
+                    const float al = rescale ? exp2f(m_old - m_new) : 1.f;
+#pragma unroll 1
                     for (int c = 0; c < D / 32; ++c) {
                         tld32(tO + ((uint32_t)(warp * 32) << 16) + 32 * c, v);
 #pragma unroll
@@ -395,30 +440,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_attn_kernel(const TcArgs a) 
                         tst32(tO + ((uint32_t)(warp * 32) << 16) + 32 * c, v);
                     }
                 }
-            }
-            if (need) {
-                if (m_used != -INFINITY) l *= exp2f(m_used - m_new);
-                m_used = m_new;
-            }
-            const float mu = m_used == -INFINITY ? 0.f : m_used;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                tld32(tl + sb * 128 + 32 * c, v);
-                uint32_t pk[16];
-#pragma unroll
-                for (int k = 0; k < 32; k += 2) {
-                    const int pos = pos0 + 32 * c + k;
-                    const bool ok0 = full_blk || (pos < kv_end && pos <= lim);
-                    const bool ok1 = full_blk || (pos + 1 < kv_end && pos + 1 <= lim);
-                    const float p0 = ok0 ? exp2f(v[k] * sc - mu) : 0.f;
-                    const float p1 = ok1 ? exp2f(v[k + 1] * sc - mu) : 0.f;
-                    l += p0 + p1;
-                    pk[k / 2] = pack_bf16(p0, p1);
-                }
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4)
-                    *reinterpret_cast<uint4*>(sPg + sw128(i, 4 * c + q4)) =
-                        make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -432,7 +453,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_attn_kernel(const TcArgs a) 
         }
         const float inv = l > 0.f ? 1.f / l : 0.f;
         const float lse = l > 0.f ? (m_used + log2f(l)) * kLn2 : -INFINITY;
-#pragma unroll
+#pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
             if (nb > 0)
                 tld32(tO + ((uint32_t)(warp * 32) << 16) + 32 * c, v);
