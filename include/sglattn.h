@@ -295,6 +295,28 @@ int sgl_extend_attn(const void* q_new, const void* k_pool, const void* v_pool, c
  * position beyond seq_lens since the word was last cleared. */
 int sgl_check(void* workspace, sgl_stream_t stream);
 
+/* Decode attention without a caller-provided workspace.
+ * No counterpart on the pages: this is a convenience for callers that cannot
+ * allocate device memory -- code running while a stream is captured into a
+ * CUDA graph (cudaMalloc is not allowed there), serving loops whose device
+ * memory belongs to another allocator, or latency-critical paths that avoid
+ * cudaMalloc because it can synchronize the device.
+ * Same arguments and result as sgl_decode_attn minus the workspace; the
+ * plan is uploaded by the call itself.  Scratch is a fixed 64 MiB array in
+ * the library's device image, held by every GPU that loads the library
+ * until the process exits; a plan whose workspace_bytes exceeds 64 MiB is
+ * rejected with SGL_ERR_WORKSPACE before any GPU work.  The first call on a
+ * device looks the array's address up (cudaGetSymbolAddress), so make that
+ * first call before any stream capture.  All calls share the array: calls
+ * that may overlap on the GPU (different streams, or before the previous
+ * call has finished reading it) race and must not be issued.  Out-of-range
+ * slots are skipped as in sgl_decode_attn, but their error word cannot be
+ * read back (there is no workspace pointer to give sgl_check).
+ * Allocates nothing: no cudaMalloc, cudaFree or allocating library call. */
+int sgl_decode_attn_noalloc(const void* q, const void* k_pool, const void* v_pool, const int32_t* req_to_token,
+                            int64_t ld, const int32_t* seq_lens, const sgl_plan* plan, void* o, float* lse,
+                            sgl_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -91,6 +91,7 @@ _SIGS = {
     "sgl_extend_attn": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_int64, _P, _P, ctypes.POINTER(SglAttnParams),
                                        _P, _P, _P, ctypes.c_size_t, _P]),
     "sgl_check": (ctypes.c_int, [_P, _P]),
+    "sgl_decode_attn_noalloc": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_int64, _P, _P, _P, _P, _P]),
 }
 
 _LIB = None
@@ -347,3 +348,11 @@ def sgl_extend_attn(q_new, k_pool, v_pool, req_to_token, prefix_lens, extend_len
 
 def sgl_check(workspace, stream=None):
     _ok(_lib().sgl_check(_dev(workspace, "workspace"), _stream(stream)), "sgl_check")
+
+
+def sgl_decode_attn_noalloc(q, k_pool, v_pool, req_to_token, seq_lens, plan, o, lse, stream=None):
+    """Decode with the library's fixed device scratch (for callers that cannot allocate)."""
+    _ok(_lib().sgl_decode_attn_noalloc(_dev(q, "q"), _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"),
+                                       _dev(req_to_token, "req_to_token"), req_to_token.shape[1],
+                                       _dev(seq_lens, "seq_lens"), plan.handle, _dev(o, "o"), _dev(lse, "lse"),
+                                       _stream(stream)), "sgl_decode_attn_noalloc")
