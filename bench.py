@@ -54,6 +54,7 @@ def parse():
     ap.add_argument("--no-extend", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-budget-s", type=float, default=60.0)
+    ap.add_argument("--num-sms", type=int, default=0, help="decode planning target (0: the device's SM count)")
     return ap.parse_args()
 
 
@@ -218,7 +219,7 @@ def cpu_baseline_subprocess(budget_s=15.0):
 
 
 # --------------------------------------------------------------------------- native arm
-def setup_decode(sgl, W, torch, n_inst):
+def setup_decode(sgl, W, torch, n_inst, num_sms=0):
     w = W.get(DECODE_WORKLOAD)
     order, K, V = W.make_pool(w)
     S = K.shape[0]
@@ -235,7 +236,7 @@ def setup_decode(sgl, W, torch, n_inst):
         view = sgl.sgl_groups_view(groups)
         gnp = sgl.groups_as_numpy(view)
         ub = int((gnp["seg_end"] - gnp["seg_begin"]).sum()) * per_tok
-        p = sgl.make_params(sgl.SGL_DTYPE_BF16, len(seqs), w.Hq, w.Hkv, w.d, S, w.page_size)
+        p = sgl.make_params(sgl.SGL_DTYPE_BF16, len(seqs), w.Hq, w.Hkv, w.d, S, w.page_size, num_sms=num_sms)
         plan = sgl.sgl_decode_plan(p, out["seq_lens"], view)
         ws = torch.zeros(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
         sgl.sgl_plan_upload(plan, ws)
@@ -255,7 +256,7 @@ def decode_call(sgl, kd, vd, it):
     sgl.sgl_decode_attn(it["q"], kd, vd, it["table"], it["seq"], it["plan"], it["o"], it["lse"], it["ws"])
 
 
-def e2e_decode(sgl, W, torch, w, tree, kd, vd, inst, steps):
+def e2e_decode(sgl, W, torch, w, tree, kd, vd, inst, steps, num_sms=0):
     """Public-API step from host buffers; returns (GB/s, h2d bytes/step, d2h bytes/step)."""
     S = kd.shape[0]
     pinned = []
@@ -274,7 +275,7 @@ def e2e_decode(sgl, W, torch, w, tree, kd, vd, inst, steps):
         it, pb = inst[s % len(inst)], pinned[s % len(inst)]
         out = sgl.sgl_build_batch(tree, it["seqs"], ld=it["table"].shape[1], groups=it["groups"])
         view = sgl.sgl_groups_view(it["groups"])
-        p = sgl.make_params(sgl.SGL_DTYPE_BF16, it["B"], w.Hq, w.Hkv, w.d, S, w.page_size)
+        p = sgl.make_params(sgl.SGL_DTYPE_BF16, it["B"], w.Hq, w.Hkv, w.d, S, w.page_size, num_sms=num_sms)
         plan = sgl.sgl_decode_plan(p, out["seq_lens"], view)
         pb["table"].numpy()[:] = out["req_to_token"]
         pb["seq"].numpy()[:] = out["seq_lens"]
@@ -312,7 +313,7 @@ def run_native(args):
     sglbuild.build()
     hbm_peak, bf16_peak, peak_src = peaks()
 
-    w, tree, kd, vd, inst = setup_decode(sgl, W, torch, args.instances)
+    w, tree, kd, vd, inst = setup_decode(sgl, W, torch, args.instances, args.num_sms)
     ub_all = sum(it["ub"] for it in inst)
     warm = max(3, args.warmup)
     for s in range(warm):
@@ -374,13 +375,17 @@ def run_native(args):
     achieved = (total_bytes / K) / (per_call_ms / 1e3) / 1e9
 
     # e2e through the public API from host buffers
-    e2e_gbs, h2d, d2h, e2e_step_s = e2e_decode(sgl, W, torch, w, tree, kd, vd, inst, max(1, min(args.e2e_steps, K)))
+    e2e_gbs, h2d, d2h, e2e_step_s = e2e_decode(sgl, W, torch, w, tree, kd, vd, inst, max(1, min(args.e2e_steps, K)),
+                                                    args.num_sms)
 
     ext = None
     if not args.no_extend:
         ext = bench_extend(sgl, W, torch, max(3, args.extend_steps), bf16_peak)
 
     traffic = profile_traffic("decode_partial")
+    info0 = sgl.sgl_plan_info(inst[0]["plan"])
+    launches_per_call = (1 + (1 if info0["num_wide_items"] > 0 else 0) +
+                         (1 if info0["num_items"] > info0["num_wide_items"] else 0))  # prefix tiles, narrow, merge
     B = inst[0]["B"]
     line = {
         "metric": METRIC,
@@ -411,7 +416,7 @@ def run_native(args):
                      "kernel": "decode partial + merge per call (unique-KV bytes / call time)"},
         "e2e": {"value": e2e_gbs, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_step_s * 1e3},
-        "gpu_launches": 2 * K,
+        "gpu_launches": K * launches_per_call,
         "clocks": clocks.summary(),
     }
     if ext is not None:

@@ -239,7 +239,8 @@ int sgl_decode_plan(const sgl_attn_params* params, const int32_t* seq_lens, cons
 void sgl_plan_destroy(sgl_plan* plan);
 
 typedef struct {
-    int32_t num_items;          /* decode work items (CTAs of the partial kernel) */
+    int32_t num_items;          /* decode work items (all kinds) */
+    int32_t num_wide_items;     /* of which shared-segment tiles (tensor-core tile kernel) */
     int32_t num_partial_rows;   /* fp32 partial (O, LSE) rows */
     int32_t num_merge_entries;  /* partial rows named by the merge lists */
     int32_t chunk_tokens;       /* KV positions per chunk chosen by the planner */

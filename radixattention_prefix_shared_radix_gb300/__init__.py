@@ -43,7 +43,7 @@ class SglPrefixGroups(ctypes.Structure):
 
 
 class SglPlanInfo(ctypes.Structure):
-    _fields_ = [("num_items", ctypes.c_int32), ("num_partial_rows", ctypes.c_int32),
+    _fields_ = [("num_items", ctypes.c_int32), ("num_wide_items", ctypes.c_int32), ("num_partial_rows", ctypes.c_int32),
                 ("num_merge_entries", ctypes.c_int32), ("chunk_tokens", ctypes.c_int32),
                 ("upload_bytes", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64)]
 

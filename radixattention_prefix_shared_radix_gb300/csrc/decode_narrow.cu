@@ -91,15 +91,14 @@ __global__ void __launch_bounds__(128)
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;   // rows 2t, 2t+1
 
     const int32_t* trow = r2t + (int64_t)it.rep_row * ld;
+    // slots of positions p0 + lane (lanes 0..15), loaded one step ahead
+    int32_t raw = (lane < 16 && b + lane < e) ? __ldg(trow + b + lane) : -1;
     for (int p0 = b; p0 < e; p0 += 16) {
-        // slot of position p0 + lane (lanes 0..15)
-        int32_t sl = -1;
-        if (lane < 16 && p0 + lane < e) {
-            sl = __ldg(trow + p0 + lane);
-            if (sl < 0 || sl >= num_slots) {
-                atomicOr(err, 1u);
-                sl = -1;
-            }
+        int32_t sl = raw;
+        raw = (lane < 16 && p0 + 16 + lane < e) ? __ldg(trow + p0 + 16 + lane) : -1;
+        if (lane < 16 && p0 + lane < e && (sl < 0 || sl >= num_slots)) {
+            atomicOr(err, 1u);
+            sl = -1;
         }
         const int32_t sk0 = __shfl_sync(0xffffffffu, sl, g), sk1 = __shfl_sync(0xffffffffu, sl, g + 8);
         const int32_t sv0 = __shfl_sync(0xffffffffu, sl, 2 * t), sv1 = __shfl_sync(0xffffffffu, sl, 2 * t + 1);
@@ -220,32 +219,89 @@ __global__ void __launch_bounds__(128)
     }
 }
 
-// Merge: one CTA per (request, KV head); thread u handles query head
-// j = u / (D/4) of the group and four consecutive head-dim elements.
+// Merge: one CTA per (request, KV head).  The partial rows and LSEs of all
+// the request's entries for the G heads are staged in shared memory in one
+// parallel sweep; then thread u (query head j = u / (D/4), four head-dim
+// elements) forms the LSE-weighted sum with its loads issued four at a time.
+constexpr int kMergeStage = 2048;   // staged (entry, head) pairs; more fall back to direct loads
+
 template <typename OutT, int D>
 __global__ void __launch_bounds__(128)
     decode_merge2(const float* __restrict__ po, const float* __restrict__ plse, const int32_t* __restrict__ mptr,
                   const MergeEnt* __restrict__ ment, OutT* __restrict__ o, float* __restrict__ lse, int Hq, int Hkv,
                   int G) {
     constexpr int C4 = D / 4;
+    __shared__ int s_row[kMergeStage];
+    __shared__ float s_lse[kMergeStage];
+    __shared__ float s_max[8];
     const int r = blockIdx.x / Hkv, kvh = blockIdx.x % Hkv;
-    const int e0 = __ldg(mptr + r), e1 = __ldg(mptr + r + 1);
+    const int e0 = __ldg(mptr + r), E = __ldg(mptr + r + 1) - e0;
+    const bool staged = E * G <= kMergeStage;
+    if (staged) {
+        for (int idx = threadIdx.x; idx < E * G; idx += blockDim.x) {
+            const int e = idx / G, j = idx % G;
+            const MergeEnt me = ment[e0 + e];
+            const int prow = me.pbase + kvh * me.gstride + j;
+            s_row[idx] = prow;
+            s_lse[idx] = plse[prow];
+        }
+        __syncthreads();
+        if (threadIdx.x < G) {
+            float M = -INFINITY;
+            for (int e = 0; e < E; ++e) M = fmaxf(M, s_lse[e * G + threadIdx.x]);
+            s_max[threadIdx.x] = M;
+        }
+        __syncthreads();
+    }
     for (int u = threadIdx.x; u < G * C4; u += blockDim.x) {
         const int j = u / C4, c4 = u % C4;
-        float M = -INFINITY;
-        for (int e = e0; e < e1; ++e) {
-            const MergeEnt me = ment[e];
-            M = fmaxf(M, plse[me.pbase + kvh * me.gstride + j]);
+        float M;
+        if (staged) {
+            M = s_max[j];
+        } else {
+            M = -INFINITY;
+            for (int e = 0; e < E; ++e) {
+                const MergeEnt me = ment[e0 + e];
+                M = fmaxf(M, plse[me.pbase + kvh * me.gstride + j]);
+            }
         }
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         float L = 0.f;
         if (M != -INFINITY) {
-#pragma unroll 4
-            for (int e = e0; e < e1; ++e) {
-                const MergeEnt me = ment[e];
-                const int64_t prow = me.pbase + kvh * me.gstride + j;
-                const float w = exp2f((plse[prow] - M) * kLog2e);
-                const float4 vv = *(reinterpret_cast<const float4*>(po + prow * D) + c4);
+            int e = 0;
+            if (staged) {
+                for (; e + 4 <= E; e += 4) {
+                    float4 vv[4];
+                    float w[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int idx = (e + k) * G + j;
+                        vv[k] = *(reinterpret_cast<const float4*>(po + (int64_t)s_row[idx] * D) + c4);
+                        w[k] = exp2f((s_lse[idx] - M) * kLog2e);
+                    }
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        acc.x += w[k] * vv[k].x;
+                        acc.y += w[k] * vv[k].y;
+                        acc.z += w[k] * vv[k].z;
+                        acc.w += w[k] * vv[k].w;
+                        L += w[k];
+                    }
+                }
+            }
+            for (; e < E; ++e) {
+                int prow;
+                float l;
+                if (staged) {
+                    prow = s_row[e * G + j];
+                    l = s_lse[e * G + j];
+                } else {
+                    const MergeEnt me = ment[e0 + e];
+                    prow = me.pbase + kvh * me.gstride + j;
+                    l = plse[prow];
+                }
+                const float w = exp2f((l - M) * kLog2e);
+                const float4 vv = *(reinterpret_cast<const float4*>(po + (int64_t)prow * D) + c4);
                 acc.x += w * vv.x;
                 acc.y += w * vv.y;
                 acc.z += w * vv.z;

@@ -233,6 +233,7 @@ void sgl_plan_destroy(sgl_plan* plan) {
 int sgl_plan_info(const sgl_plan* plan, sgl_plan_info_t* out) {
     if (!plan || !out) return SGL_ERR_INVALID_ARG;
     out->num_items = plan->n_items;
+    out->num_wide_items = plan->n_wide;
     out->num_partial_rows = plan->n_partial_rows;
     out->num_merge_entries = plan->n_merge_entries;
     out->chunk_tokens = plan->chunk_tokens;
