@@ -12,26 +12,27 @@
 //     section "用基数树实现前缀复用"); output = normalised partial rows merged
 //     later by log-sum-exp.
 //
-// CTA roles (288 threads):
+// CTA roles (224 threads; two CTAs share an SM, so two independent tiles keep
+// the tensor core and the softmax units busy in turn):
 //   warps 0-3  softmax: thread i owns query row i == TMEM lane i;
-//   warp  4    allocates TMEM; one thread issues every tcgen05.mma;
-//   warps 5-8  gather: slot lookup in req_to_token and 16-byte cp.async of the
+//   warp  4    allocates TMEM (256 columns); one thread issues every MMA;
+//   warps 5-6  gather: slot lookup in req_to_token and 16-byte cp.async of the
 //              K and V rows (head_dim x 2 contiguous bytes each in the
 //              slot-major pool) into 128B-swizzled tiles, consecutive lanes on
 //              consecutive chunks of a row; each thread signals the stage's
-//              mbarrier when its copies land.
-// Per KV block j:  S_j = Q K_j^T  (M 128, N 128, K d; both operands K-major)
-// into one of two TMEM score buffers; the softmax threads read their row,
-// keep a running max m and sum l in base 2 (scores pre-scaled by
-// sm_scale*log2 e), write P_j = 2^(s - m) as bf16 to shared memory, and the
-// MMA thread issues O += P_j V_j (M 128, N d, K 128; V read as an MN-major
-// operand) into the TMEM accumulator.  O is rescaled in TMEM only when a
-// row's max grows by more than 8 (a factor 2^8, harmless in fp32), so most
-// blocks need no correction pass.  S_{j+1} runs on the tensor core while the
-// softmax of block j runs; the softmax reads its whole 128-score row with
-// four TMEM loads in flight and a single wait.  All waits are bounded: one that gives up sets bit
-// 2 of the workspace error word and the kernel runs to its end without
-// hanging (its results are then garbage, and flagged).
+//              mbarrier when its copies land.  K and V have separate 2-stage
+//              rings: K_{j+2} may load as soon as S_j is done.
+// Per 64-position KV block j:  S_j = Q K_j^T (M 128, N 64, K d; both operands
+// K-major) into one of two TMEM score buffers.  The softmax threads read their
+// row (two TMEM loads in flight, one wait), keep a running max m and sum l in
+// base 2 (scores pre-scaled by sm_scale*log2 e), and write P_j = 2^(s - m) as
+// bf16 pairs back into the first half of the same TMEM buffer; the MMA thread
+// then issues O += P_j V_j with A read from TMEM (M 128, N d, K 64; V an
+// MN-major smem operand) and S_{j+2} into the freed buffer.  O lives in TMEM
+// and is rescaled only when a row's max grows by more than 8 (a factor 2^8,
+// harmless in fp32).  All waits are bounded: one that gives up sets bit 2 of
+// the workspace error word and the kernel runs to its end without hanging
+// (its results are then garbage, and flagged).
 
 #include "device_common.cuh"
 
@@ -40,14 +41,15 @@ namespace {
 
 using namespace sgldev;
 
-constexpr int kTcThreads = 288;
-constexpr int kNS = 2;               // KV stages
-constexpr int kRegion = 128 * 128;   // one SW128 region: 128 rows x 128 bytes
+constexpr int kTcThreads = 224;
+constexpr int kBN = 64;                  // KV positions per block
+constexpr int kQRegion = 128 * 128;      // SW128 region of a 128-row tile: 128 rows x 128 bytes
+constexpr int kKRegion = kBN * 128;      // SW128 region of a 64-row tile
 
-// 16-byte chunk c of row r of a 128-row bf16 tile kept as 64-column SW128
-// regions (the canonical K-major / MN-major 128B-swizzle layout).
-__device__ __forceinline__ uint32_t sw128(int r, int c) {
-    return (uint32_t)((c >> 3) * kRegion + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+// 16-byte chunk c of row r of a bf16 tile kept as 64-column SW128 regions of
+// `region` bytes each (the canonical K-major / MN-major 128B-swizzle layout).
+__device__ __forceinline__ uint32_t sw128(int r, int c, int region) {
+    return (uint32_t)((c >> 3) * region + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
 __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
@@ -66,6 +68,25 @@ __device__ __forceinline__ void tc_mma(uint32_t tmem, uint64_t a, uint64_t b, ui
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(
             tmem),
         "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+// O += A B with A (M x 16) read from TMEM as packed bf16 pairs.
+__device__ __forceinline__ void tc_mma_tmem_a(uint32_t tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                              uint32_t acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::
+            "r"(tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc));
+}
+__device__ __forceinline__ void tst32u(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%"
+        "18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+        "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+        "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
 }
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar)
@@ -148,12 +169,12 @@ struct TcArgs {
 
 template <int D>
 struct TcLayout {
-    static constexpr int TILE = 128 * D * 2;
+    static constexpr int QTILE = 128 * D * 2;
+    static constexpr int KTILE = kBN * D * 2;
     static constexpr int OFF_Q = 0;
-    static constexpr int OFF_K = OFF_Q + TILE;
-    static constexpr int OFF_V = OFF_K + kNS * TILE;
-    static constexpr int OFF_P = OFF_V + kNS * TILE;
-    static constexpr int OFF_BAR = OFF_P + 2 * kRegion;
+    static constexpr int OFF_K = OFF_Q + QTILE;          // 2 stages
+    static constexpr int OFF_V = OFF_K + 2 * KTILE;      // 2 stages
+    static constexpr int OFF_BAR = OFF_V + 2 * KTILE;
     static constexpr int OFF_INFO = OFF_BAR + 16 * 8;
     static constexpr int OFF_TMEM = OFF_INFO + 16 * 4;
     static constexpr int TOTAL = OFF_TMEM + 16 + 1024;   // + alignment slack
@@ -161,12 +182,13 @@ struct TcLayout {
 
 // barrier indices
 constexpr int B_QFULL = 0;
-constexpr int B_KVFULL = 1;                  // + stage
-constexpr int B_KVEMPTY = B_KVFULL + kNS;    // + stage
-constexpr int B_SFULL = B_KVEMPTY + kNS;     // + buffer
-constexpr int B_SFREE = B_SFULL + 2;         // + buffer
-constexpr int B_PFULL = B_SFREE + 2;
-constexpr int B_OFULL = B_PFULL + 1;
+constexpr int B_KFULL = 1;     // + stage
+constexpr int B_KEMPTY = 3;    // + stage
+constexpr int B_VFULL = 5;     // + stage
+constexpr int B_VEMPTY = 7;    // + stage
+constexpr int B_SFULL = 9;     // + buffer
+constexpr int B_PFULL = 11;
+constexpr int B_OFULL = 12;
 
 template <bool DEC>
 __device__ void tile_setup(const TcArgs& a, int* info) {
@@ -223,15 +245,13 @@ __device__ void tile_setup(const TcArgs& a, int* info) {
 }
 
 template <int D, bool DEC>
-__global__ void __launch_bounds__(kTcThreads, 1) tc_attn_kernel(const TcArgs a) {
+__global__ void __maxnreg__(128) tc_attn_kernel(const TcArgs a) {
     using Lay = TcLayout<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sQ = smem_u32(sm + Lay::OFF_Q);
     const uint32_t sK = smem_u32(sm + Lay::OFF_K);
     const uint32_t sV = smem_u32(sm + Lay::OFF_V);
-    uint8_t* sPg = sm + Lay::OFF_P;
-    const uint32_t sP = smem_u32(sPg);
     const uint32_t bar0 = smem_u32(sm + Lay::OFF_BAR);
     int* info = reinterpret_cast<int*>(sm + Lay::OFF_INFO);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + Lay::OFF_TMEM);
@@ -243,31 +263,30 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_attn_kernel(const TcArgs a) 
     if (!info[0]) return;
     const int kv_row = info[1], kv_begin = info[2], kv_end = info[3], kvh = info[4], rows = info[5];
     const int i6 = info[6], i7 = info[7];
-    const int nb = (kv_end - kv_begin + 127) / 128;
+    const int nb = (kv_end - kv_begin + kBN - 1) / kBN;
 
     if (tid == 0) {
-        mbar_init(bar(B_QFULL), 128);
-        for (int s = 0; s < kNS; ++s) {
-            mbar_init(bar(B_KVFULL + s), 128);
-            mbar_init(bar(B_KVEMPTY + s), 1);
-        }
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(bar(B_SFULL + s), 1);
-            mbar_init(bar(B_SFREE + s), 128);
+        mbar_init(bar(B_QFULL), 64);
+        for (int s2 = 0; s2 < 2; ++s2) {
+            mbar_init(bar(B_KFULL + s2), 64);
+            mbar_init(bar(B_KEMPTY + s2), 1);
+            mbar_init(bar(B_VFULL + s2), 64);
+            mbar_init(bar(B_VEMPTY + s2), 1);
+            mbar_init(bar(B_SFULL + s2), 1);
         }
         mbar_init(bar(B_PFULL), 128);
         mbar_init(bar(B_OFULL), 1);
         mbar_fence_init();
     }
     if (warp == 4) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;\n" ::"r"(smem_u32(tslot)));
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 256;\n" ::"r"(smem_u32(tslot)));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tbase = *tslot;
-    const uint32_t tO = tbase + 256;
+    const uint32_t tbase = *tslot;     // S buffers at columns 0 and 64, O at 128
+    const uint32_t tO = tbase + 128;
     bool timed_out = false;
     auto wait = [&](int b, uint32_t par) {
         if (!mbar_wait(bar(b), par)) {
@@ -278,93 +297,99 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_attn_kernel(const TcArgs a) 
 
     if (warp >= 5) {
         // ------------------------------------------------------------ gather
-        // Coalesced: consecutive lanes take consecutive 16-byte chunks of one
-        // row (CPR lanes per row, 32/CPR rows per instruction); lane l of
-        // gather warp w looks up the slot of row 32w + l, shared by shuffle.
-        constexpr int CPR = D / 8;                 // chunks per row
-        constexpr int RPI = 32 / CPR;              // rows per instruction
+        constexpr int CPR = D / 8;                 // 16-byte chunks per row
+        constexpr int RPI = 32 / CPR;              // rows per warp instruction
         const int gw = warp - 5;
         const int sub = lane / CPR, ch = lane % CPR;
-        {
 #pragma unroll 4
-            for (int k = 0; k < 32 / RPI; ++k) {
-                const int r = gw * 32 + k * RPI + sub;
-                const bool ok = r < rows;
-                const bf16* src = a.q;
-                if (ok) {
-                    int64_t qr;
-                    if constexpr (DEC)
-                        qr = (int64_t)__ldg(a.members + i6 + r / a.G) * a.Hq + kvh * a.G + r % a.G;
-                    else
-                        qr = ((int64_t)i6 + r / a.G) * a.Hq + kvh * a.G + r % a.G;
-                    src = a.q + qr * D + ch * 8;
-                }
-                cp_async16(sQ + sw128(r, ch), src, ok);
+        for (int k = 0; k < 64 / RPI; ++k) {       // 64 query rows per gather warp
+            const int r = gw * 64 + k * RPI + sub;
+            const bool ok = r < rows;
+            const bf16* src = a.q;
+            if (ok) {
+                int64_t qr;
+                if constexpr (DEC)
+                    qr = (int64_t)__ldg(a.members + i6 + r / a.G) * a.Hq + kvh * a.G + r % a.G;
+                else
+                    qr = ((int64_t)i6 + r / a.G) * a.Hq + kvh * a.G + r % a.G;
+                src = a.q + qr * D + ch * 8;
             }
-            cp_async_arrive_noinc(bar(B_QFULL));
+            cp_async16(sQ + sw128(r, ch, kQRegion), src, ok);
         }
+        cp_async_arrive_noinc(bar(B_QFULL));
         const int32_t* trow = a.r2t + (int64_t)kv_row * a.ld;
-        const int myrow = gw * 32 + lane;
-        int32_t raw_next = -1;
-        if (nb > 0 && kv_begin + myrow < kv_end) raw_next = __ldg(trow + kv_begin + myrow);
+        const int myrow = gw * 32 + lane;          // this lane looks up the slot of row myrow
+        int32_t raw_next = (nb > 0 && kv_begin + myrow < kv_end) ? __ldg(trow + kv_begin + myrow) : -1;
         for (int j = 0; j < nb; ++j) {
-            const int st = j % kNS;
-            wait(B_KVEMPTY + st, ((j / kNS) & 1) ^ 1);
-            const int pos = kv_begin + j * 128 + myrow;
+            const int st = j & 1;
+            const uint32_t par = ((j >> 1) & 1) ^ 1;
+            const int pos = kv_begin + j * kBN + myrow;
             int32_t s = raw_next;
-            raw_next = -1;
-            if (j + 1 < nb && pos + 128 < kv_end) raw_next = __ldg(trow + pos + 128);
+            raw_next = (j + 1 < nb && pos + kBN < kv_end) ? __ldg(trow + pos + kBN) : -1;
             bool ok = pos < kv_end;
             if (ok && (s < 0 || s >= a.num_slots)) {
                 atomicOr(a.err, 1u);
                 ok = false;
             }
             if (!ok) s = -1;
-            const uint32_t kd = sK + st * Lay::TILE, vd = sV + st * Lay::TILE;
+            const uint32_t kd = sK + st * Lay::KTILE, vd = sV + st * Lay::KTILE;
+            wait(B_KEMPTY + st, par);
 #pragma unroll 4
             for (int k = 0; k < 32 / RPI; ++k) {
-                const int rl = k * RPI + sub;                       // row within this warp's 32
+                const int rl = k * RPI + sub;
                 const int32_t sr = __shfl_sync(0xffffffffu, s, rl);
-                const int r = gw * 32 + rl;
-                const bool rok = sr >= 0;
-                const int64_t off = rok ? ((int64_t)sr * a.Hkv + kvh) * D + ch * 8 : 0;
-                cp_async16(kd + sw128(r, ch), a.kp + off, rok);
-                cp_async16(vd + sw128(r, ch), a.vp + off, rok);
+                const int64_t off = sr >= 0 ? ((int64_t)sr * a.Hkv + kvh) * D + ch * 8 : 0;
+                cp_async16(kd + sw128(gw * 32 + rl, ch, kKRegion), a.kp + off, sr >= 0);
             }
-            cp_async_arrive_noinc(bar(B_KVFULL + st));
+            cp_async_arrive_noinc(bar(B_KFULL + st));
+            wait(B_VEMPTY + st, par);
+#pragma unroll 4
+            for (int k = 0; k < 32 / RPI; ++k) {
+                const int rl = k * RPI + sub;
+                const int32_t sr = __shfl_sync(0xffffffffu, s, rl);
+                const int64_t off = sr >= 0 ? ((int64_t)sr * a.Hkv + kvh) * D + ch * 8 : 0;
+                cp_async16(vd + sw128(gw * 32 + rl, ch, kKRegion), a.vp + off, sr >= 0);
+            }
+            cp_async_arrive_noinc(bar(B_VFULL + st));
         }
         asm volatile("cp.async.wait_all;\n" ::: "memory");
     } else if (warp == 4) {
         // ------------------------------------------------------------ MMA
         if (lane == 0) {
-            constexpr uint32_t IS = idesc_bf16(128, 128, false);
+            constexpr uint32_t IS = idesc_bf16(128, kBN, false);
             constexpr uint32_t IO = idesc_bf16(128, D, true);
             wait(B_QFULL, 0);
-            for (int j = 0; j < nb; ++j) {
-                const int st = j % kNS, sb = j & 1;
-                wait(B_KVFULL + st, (j / kNS) & 1);
-                if (j >= 2) wait(B_SFREE + sb, ((j >> 1) - 1) & 1);
+            auto issue_s = [&](int j) {
+                const int st = j & 1;
+                wait(B_KFULL + st, (j >> 1) & 1);
                 fence_proxy_async_smem();
                 tc_fence_after();
-                const uint32_t kb = sK + st * Lay::TILE;
+                const uint32_t kb = sK + st * Lay::KTILE;
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t off = (ks >> 2) * kRegion + (ks & 3) * 32;
-                    tc_mma(tbase + sb * 128, sdesc(sQ + off, 16, 1024), sdesc(kb + off, 16, 1024), IS, ks > 0);
+                    const uint32_t qoff = (ks >> 2) * kQRegion + (ks & 3) * 32;
+                    const uint32_t koff = (ks >> 2) * kKRegion + (ks & 3) * 32;
+                    tc_mma(tbase + (j & 1) * 64, sdesc(sQ + qoff, 16, 1024), sdesc(kb + koff, 16, 1024), IS, ks > 0);
                 }
-                tc_commit(bar(B_SFULL + sb));
+                tc_commit(bar(B_SFULL + (j & 1)));
+                tc_commit(bar(B_KEMPTY + st));
+            };
+            if (nb > 0) issue_s(0);
+            if (nb > 1) issue_s(1);
+            for (int j = 0; j < nb; ++j) {
+                const int st = j & 1;
                 wait(B_PFULL, j & 1);
+                wait(B_VFULL + st, (j >> 1) & 1);
                 fence_proxy_async_smem();
                 tc_fence_after();
-                const uint32_t vb = sV + st * Lay::TILE;
+                const uint32_t vb = sV + st * Lay::KTILE;
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t aoff = (kk >> 2) * kRegion + (kk & 3) * 32;
-                    tc_mma(tO, sdesc(sP + aoff, 16, 1024), sdesc(vb + kk * 2048, kRegion, 1024), IO,
-                           (j > 0 || kk > 0) ? 1u : 0u);
-                }
+                for (int kk = 0; kk < kBN / 16; ++kk)
+                    tc_mma_tmem_a(tO, tbase + (j & 1) * 64 + kk * 8, sdesc(vb + kk * 2048, kKRegion, 1024), IO,
+                                  (j > 0 || kk > 0) ? 1u : 0u);
                 tc_commit(bar(B_OFULL));
-                tc_commit(bar(B_KVEMPTY + st));
+                tc_commit(bar(B_VEMPTY + st));
+                if (j + 2 < nb) issue_s(j + 2);   // into the buffer P_j occupies: runs after PV_j
             }
         }
         __syncwarp();
@@ -372,31 +397,30 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_attn_kernel(const TcArgs a) 
         // ------------------------------------------------------------ softmax
         const int i = tid;
         const uint32_t tl = tbase + ((uint32_t)(warp * 32) << 16);
+        const uint32_t tlO = tO + ((uint32_t)(warp * 32) << 16);
         const int lim = DEC ? 0x7fffffff : i7 + i / a.G;
         const float sc = a.scale_log2;
         float m_used = -INFINITY, l = 0.f;
-        float v[32];
         for (int j = 0; j < nb; ++j) {
-            const int sb = j & 1;
-            wait(B_SFULL + sb, (j >> 1) & 1);
+            const int b = j & 1;
+            wait(B_SFULL + b, (j >> 1) & 1);
             tc_fence_after();
-            const int pos0 = kv_begin + j * 128;
-            const bool full_blk = pos0 + 127 < kv_end && pos0 + 127 <= lim;
-            // the whole S row in registers: four loads in flight, one wait
-            float srow[128];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tld32_nw(tl + sb * 128 + 32 * c, srow + 32 * c);
+            const int pos0 = kv_begin + j * kBN;
+            const bool full_blk = pos0 + kBN - 1 < kv_end && pos0 + kBN - 1 <= lim;
+            float srow[kBN];
+            tld32_nw(tl + b * 64, srow);
+            tld32_nw(tl + b * 64 + 32, srow + 32);
             tld_wait();
             float mx = -INFINITY;
             if (full_blk) {
 #pragma unroll
-                for (int k = 0; k < 128; ++k) {
+                for (int k = 0; k < kBN; ++k) {
                     srow[k] *= sc;
                     mx = fmaxf(mx, srow[k]);
                 }
             } else {
 #pragma unroll
-                for (int k = 0; k < 128; ++k) {
+                for (int k = 0; k < kBN; ++k) {
                     const int pos = pos0 + k;
                     srow[k] = (pos < kv_end && pos <= lim) ? srow[k] * sc : -INFINITY;
                     mx = fmaxf(mx, srow[k]);
@@ -410,41 +434,35 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_attn_kernel(const TcArgs a) 
                 m_used = m_new;
             }
             const float mu = m_used == -INFINITY ? 0.f : m_used;
-            // P must not overwrite the tile PV_{j-1} is still reading
+            uint32_t pk[kBN / 2];
+#pragma unroll
+            for (int k = 0; k < kBN; k += 2) {
+                const float p0 = exp2f(srow[k] - mu);      // -inf -> 0
+                const float p1 = exp2f(srow[k + 1] - mu);
+                l += p0 + p1;
+                pk[k / 2] = pack_bf16(p0, p1);
+            }
+            tst32u(tl + b * 64, pk);                         // P_j over the consumed scores
+            // PV_{j-1} is consumed every block (so the barrier is never two
+            // phases ahead of this wait); it is normally long done by now.
             if (j > 0) {
                 wait(B_OFULL, (j - 1) & 1);
                 tc_fence_after();
             }
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {       // 8 positions per 16-byte chunk of the P row
-                uint32_t pk[4];
-#pragma unroll
-                for (int k = 0; k < 8; k += 2) {
-                    const float p0 = exp2f(srow[8 * c + k] - mu);      // -inf -> 0
-                    const float p1 = exp2f(srow[8 * c + k + 1] - mu);
-                    l += p0 + p1;
-                    pk[k / 2] = pack_bf16(p0, p1);
-                }
-                *reinterpret_cast<uint4*>(sPg + sw128(i, c)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            }
             // O holds blocks < j scaled to the old max: rescale before PV_j adds to it
-            if (j > 0) {
-                const bool rescale = need && m_old != -INFINITY;
-                if (__any_sync(0xffffffffu, rescale)) {
-                    const float al = rescale ? exp2f(m_old - m_new) : 1.f;
+            if (j > 0 && __any_sync(0xffffffffu, need && m_old != -INFINITY)) {
+                const float al = (need && m_old != -INFINITY) ? exp2f(m_old - m_new) : 1.f;
+                float v[32];
 #pragma unroll 1
-                    for (int c = 0; c < D / 32; ++c) {
-                        tld32(tO + ((uint32_t)(warp * 32) << 16) + 32 * c, v);
+                for (int c = 0; c < D / 32; ++c) {
+                    tld32(tlO + 32 * c, v);
 #pragma unroll
-                        for (int k = 0; k < 32; ++k) v[k] *= al;
-                        tst32(tO + ((uint32_t)(warp * 32) << 16) + 32 * c, v);
-                    }
+                    for (int k = 0; k < 32; ++k) v[k] *= al;
+                    tst32(tlO + 32 * c, v);
                 }
             }
-            fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(bar(B_PFULL));
-            mbar_arrive(bar(B_SFREE + sb));
         }
         // epilogue
         if (nb > 0) {
@@ -453,10 +471,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_attn_kernel(const TcArgs a) 
         }
         const float inv = l > 0.f ? 1.f / l : 0.f;
         const float lse = l > 0.f ? (m_used + log2f(l)) * kLn2 : -INFINITY;
+        float v[32];
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
             if (nb > 0)
-                tld32(tO + ((uint32_t)(warp * 32) << 16) + 32 * c, v);
+                tld32(tlO + 32 * c, v);
             else
 #pragma unroll
                 for (int k = 0; k < 32; ++k) v[k] = 0.f;
@@ -490,7 +509,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_attn_kernel(const TcArgs a) 
     __syncthreads();
     if (warp == 4) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;\n" ::"r"(tbase));
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 256;\n" ::"r"(tbase));
     }
 }
 

@@ -161,3 +161,16 @@ def test_decode_full_size(name):
         print("%s: O max-abs %.3g, LSE max-abs %.3g" % (name, do, dl))
     finally:
         case.close()
+
+
+def test_decode_rescale_path_with_growing_scores():
+    """Large scores late in shared prefixes force the tensor-core tiles' running-max rescale."""
+    w = W.get("llama3_8b_decode_small")
+    order, K, V = W.make_pool(w)
+    K = K.clone()
+    K[::89] *= 30.0
+    case = Case(None, workload=w, pool=(order, K, V))
+    try:
+        _check(case)
+    finally:
+        case.close()

@@ -95,3 +95,19 @@ def test_extend_full_size_sampled():
         print("extend: O max-abs %.3g, LSE max-abs %.3g" % (do, dl))
     finally:
         case.close()
+
+
+def test_rescale_path_with_growing_scores():
+    """Scores that jump by far more than 2^8 late in the context force the
+    running-max rescale of the tensor-core accumulator (rare with N(0,1) data)."""
+    w = W.Workload("jump", 4, "extend", "bf16", 16, 8, 128, 1,
+                   ("extend", dict(n=3, prefix=(200, 700), new=(1, 150))), num_slots=4096)
+    order, K, V = W.make_pool(w)
+    K = K.clone()
+    # every 97th slot gets a large K: its score is ~30x typical, far above 2^8 in probability
+    K[::97] *= 30.0
+    case = Case(None, workload=w, pool=(order, K, V))
+    try:
+        _check(case)
+    finally:
+        case.close()
