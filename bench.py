@@ -55,6 +55,11 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-budget-s", type=float, default=60.0)
     ap.add_argument("--num-sms", type=int, default=0, help="decode planning target (0: the device's SM count)")
+    ap.add_argument("--only", choices=["all", "decode", "extend"], default="all",
+                    help="decode: skip the extend line; extend: time only the extend workload (profiling)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--pool-slots", type=int, default=0,
+                    help="decode pool size override (0: the workload's 2^20 slots); small pools serve ncu captures")
     return ap.parse_args()
 
 
@@ -219,8 +224,11 @@ def cpu_baseline_subprocess(budget_s=15.0):
 
 
 # --------------------------------------------------------------------------- native arm
-def setup_decode(sgl, W, torch, n_inst, num_sms=0):
+def setup_decode(sgl, W, torch, n_inst, num_sms=0, pool_slots=0):
+    import dataclasses
     w = W.get(DECODE_WORKLOAD)
+    if pool_slots:
+        w = dataclasses.replace(w, num_slots=int(pool_slots))
     order, K, V = W.make_pool(w)
     S = K.shape[0]
     kd, vd = K.cuda(), V.cuda()
@@ -312,8 +320,14 @@ def run_native(args):
         dist.init_process_group("nccl")
     sglbuild.build()
     hbm_peak, bf16_peak, peak_src = peaks()
+    if args.only == "extend":
+        ext = bench_extend(sgl, W, torch, max(3, args.extend_steps), bf16_peak)
+        if rank == 0:
+            print(json.dumps({"metric": "extend attn TFLOP/s", "value": ext["tflops"], "unit": "TFLOP/s",
+                              "n_gpus": world, "extend": ext}), flush=True)
+        return
 
-    w, tree, kd, vd, inst = setup_decode(sgl, W, torch, args.instances, args.num_sms)
+    w, tree, kd, vd, inst = setup_decode(sgl, W, torch, args.instances, args.num_sms, args.pool_slots)
     ub_all = sum(it["ub"] for it in inst)
     warm = max(3, args.warmup)
     for s in range(warm):
@@ -375,11 +389,13 @@ def run_native(args):
     achieved = (total_bytes / K) / (per_call_ms / 1e3) / 1e9
 
     # e2e through the public API from host buffers
-    e2e_gbs, h2d, d2h, e2e_step_s = e2e_decode(sgl, W, torch, w, tree, kd, vd, inst, max(1, min(args.e2e_steps, K)),
-                                                    args.num_sms)
+    e2e_gbs = h2d = d2h = e2e_step_s = None
+    if not args.no_e2e:
+        e2e_gbs, h2d, d2h, e2e_step_s = e2e_decode(sgl, W, torch, w, tree, kd, vd, inst,
+                                                   max(1, min(args.e2e_steps, K)), args.num_sms)
 
     ext = None
-    if not args.no_extend:
+    if not args.no_extend and args.only == "all":
         ext = bench_extend(sgl, W, torch, max(3, args.extend_steps), bf16_peak)
 
     traffic = profile_traffic("decode_partial")
@@ -415,7 +431,7 @@ def run_native(args):
                      "frac_of_8TBs": achieved / 8000.0, "traffic": traffic,
                      "kernel": "decode partial + merge per call (unique-KV bytes / call time)"},
         "e2e": {"value": e2e_gbs, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_step_s * 1e3},
+                "ms_per_step": e2e_step_s * 1e3 if e2e_step_s else None},
         "gpu_launches": K * launches_per_call,
         "clocks": clocks.summary(),
     }
