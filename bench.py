@@ -17,8 +17,10 @@ GB/s: the K/V bytes of every prefix-group segment counted once per step.
   * extend: TFLOP/s of the chunked-prefill workload (8 requests, cached
     4096-token prefix + 512 causal new tokens, Hq 64 / Hkv 8), unmasked
     query-key pairs x 4 d FLOP.
-  * roofline: decode achieved unique-KV GB/s per call against the measured
-    HBM copy bandwidth; ncu DRAM traffic per call from profiles/ when current.
+  * roofline: the decode call is one kernel launch (the fused persistent
+    kernel); achieved = unique-KV bytes per call / call time, against the
+    measured HBM copy bandwidth; ncu DRAM traffic per call from profiles/
+    when current.
   * cpu_baseline / --impl reference: the float64 oracle (test
     infrastructure) timed on host cores on a bounded sample of the workload.
 
@@ -399,9 +401,7 @@ def run_native(args):
         ext = bench_extend(sgl, W, torch, max(3, args.extend_steps), bf16_peak)
 
     traffic = profile_traffic("decode_partial")
-    info0 = sgl.sgl_plan_info(inst[0]["plan"])
-    launches_per_call = (1 + (1 if info0["num_wide_items"] > 0 else 0) +
-                         (1 if info0["num_items"] > info0["num_wide_items"] else 0))  # prefix tiles, narrow, merge
+    launches_per_call = 1   # bf16 decode: one fused persistent kernel per call
     B = inst[0]["B"]
     line = {
         "metric": METRIC,
@@ -429,7 +429,7 @@ def run_native(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "peak_source": peak_src,
                      "frac_of_8TBs": achieved / 8000.0, "traffic": traffic,
-                     "kernel": "decode partial + merge per call (unique-KV bytes / call time)"},
+                     "kernel": "decode_fused_kernel (one launch per decode call: unique-KV bytes / call time)"},
         "e2e": {"value": e2e_gbs, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_step_s * 1e3 if e2e_step_s else None},
         "gpu_launches": K * launches_per_call,

@@ -1,24 +1,23 @@
-// RadixAttention kernels for sm_103a and the GPU entry points of the C ABI.
+// GPU entry points of the C ABI, and the fp32 kernels.
 //
 // Decode ("SGLang 深度拆解" (chenxutan.com/d/5669.html) §3.2 PagedDecode and
 // §4.1: one query token against the whole history, memory-bound) is split
-// along the KV sequence into the planner's work items.  One CTA takes one
-// (segment chunk, KV head, member block): it gathers the chunk's K/V rows
-// through req_to_token ONCE into shared memory and runs every member
-// request's query heads of that KV head against them ("computed once,
-// referenced many times", oripoin.cn section "用基数树实现前缀复用").  Query
-// rows (member x head) are packed 16 to a tensor-core tile.  Each item writes
-// a normalised partial (O, LSE); a second kernel merges a request's partials
-// by log-sum-exp with warp shuffles.
+// along the KV sequence into the planner's work items: a chunk of a prefix-
+// group segment is read once for all its member requests and all query heads
+// of a KV head ("computed once, referenced many times", "SGLang：从前端 DSL 到
+// SRT 服务运行时", section "用基数树实现前缀复用").  Each item writes normalised
+// partial rows (O, LSE) that a log-sum-exp merge combines per (request, head).
+//   * bf16: one launch of the fused persistent kernel (decode_fused.cu):
+//     tcgen05 tiles for shared segments, streaming warps for the rest, merge
+//     by the last producer of each (request, KV head).
+//   * fp32 (exact CUDA-core arithmetic): one CTA per work item, then a merge
+//     launch, one warp per (request, KV head).
 //
 // Extend ("SGLang 深度拆解" §3.2 PagedPrefill; "SGLang 深度解读" section
-// "5. Attention 层": the new tokens' K/V are in the pool before attention)
-// packs (new token x query head of one KV head) rows 128 to a CTA and walks
-// the cached prefix plus the causal part of the new block.
+// "5. Attention 层": the new tokens' K/V are in the pool before attention):
+// bf16 on the tcgen05 tile kernel (tc_attn.cu), fp32 one warp per
+// (new token, query head).
 //
-// Gathers: slots are random per token, so every K/V row (head_dim x 2 bytes,
-// 16-byte aligned) is fetched with 16-byte cp.async into an XOR-swizzled
-// shared-memory tile (conflict-free ldmatrix), three tiles in flight.
 // Softmax runs in base 2 on scores pre-multiplied by sm_scale * log2(e);
 // LSE is returned in natural log.  Slots outside the pool are skipped and
 // flagged in the workspace error word; nothing traps.
@@ -32,25 +31,17 @@
 
 #include "common.h"
 #include "device_common.cuh"
+#include "merge.cuh"
 
 namespace sgl {
 template <int D>
-int launch_decode_narrow(const DecItem* items, int n_items, const void* q, const void* kp, const void* vp,
-                         const int32_t* r2t, int64_t ld, const int32_t* seq_lens, const int32_t* members, float* po,
-                         float* plse, uint32_t* err, int Hq, int Hkv, int G, int64_t num_slots, float scale_log2,
-                         cudaStream_t s);
+int launch_decode_fused(const sgl_plan* plan, const void* q, const void* kp, const void* vp, const int32_t* r2t,
+                        int64_t ld, const int32_t* seq_lens, void* o, float* lse, unsigned char* ws, float scale_log2,
+                        cudaStream_t s);
 template <int D>
 int launch_extend_tc(const void* q, const void* kp, const void* vp, const int32_t* r2t, int64_t ld,
                      const int32_t* pre, const int32_t* ext, int B, int64_t n_rows, int64_t tiles, void* o, float* lse,
                      uint32_t* err, int Hq, int Hkv, int64_t num_slots, float scale_log2, cudaStream_t s);
-template <int D>
-int launch_decode_wide_tc(const DecItem* items, int n_items, const void* q, const void* kp, const void* vp,
-                          const int32_t* r2t, int64_t ld, const int32_t* seq_lens, const int32_t* members, float* po,
-                          float* plse, uint32_t* err, int Hq, int Hkv, int64_t num_slots, float scale_log2,
-                          cudaStream_t s);
-template <int D>
-int launch_decode_merge(bool bf16_out, const float* po, const float* plse, const int32_t* mptr, const MergeEnt* ment,
-                        void* o, float* lse, int B, int Hq, int Hkv, int G, cudaStream_t s);
 }  // namespace sgl
 
 namespace {
@@ -112,6 +103,18 @@ __global__ void __launch_bounds__(128)
         for (int e = 0; e < E; ++e) po[prow * D + lane * E + e] = o[e] * inv;
         if (lane == 0) plse[prow] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
     }
+}
+
+// fp32 merge: one warp per (request, KV head).
+template <int D>
+__global__ void __launch_bounds__(128) decode_merge_f32(const sgl::MergeArgs m, int n_pairs) {
+    const int idx = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (idx >= n_pairs) return;
+    const int e0 = __ldg(m.mptr + idx), E = __ldg(m.mptr + idx + 1) - e0;
+    if (E == 0)
+        sgl::merge_empty<float, D>(m, idx, lane);
+    else
+        sgl::merge_warp<float, D>(m, idx, e0, E, lane);
 }
 
 // ---------------------------------------------------------------------------
@@ -191,11 +194,6 @@ int cuda_status(cudaError_t e) {
     return SGL_ERR_CUDA;
 }
 
-template <typename K>
-cudaError_t allow_smem(K kernel, int bytes) {
-    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-}
-
 float scale_log2_of(const sgl_attn_params* p) {
     const float sc = p->sm_scale > 0.f ? p->sm_scale : 1.0f / std::sqrt(static_cast<float>(p->head_dim));
     return sc * kLog2e;
@@ -203,44 +201,31 @@ float scale_log2_of(const sgl_attn_params* p) {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-int device_sms() {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
-        cudaGetLastError();
-        return 152;
-    }
-    return n;
-}
-
 template <int D>
 int launch_decode(const sgl_plan* plan, const void* q, const void* kp, const void* vp, const int32_t* r2t,
                   int64_t ld, const int32_t* seq_lens, void* o, float* lse, unsigned char* ws, cudaStream_t s) {
     const sgl_attn_params& p = plan->params;
+    const float sl2 = scale_log2_of(&p);
+    if (p.batch == 0) return SGL_OK;
+    if (p.dtype == SGL_DTYPE_BF16) {
+        const int e = sgl::launch_decode_fused<D>(plan, q, kp, vp, r2t, ld, seq_lens, o, lse, ws, sl2, s);
+        if (e) return cuda_status(static_cast<cudaError_t>(e));
+        return SGL_OK;
+    }
     const auto* items = reinterpret_cast<const sgl::DecItem*>(ws + plan->off_items);
     const auto* members = reinterpret_cast<const int32_t*>(ws + plan->off_members);
-    const auto* mptr = reinterpret_cast<const int32_t*>(ws + plan->off_mptr);
-    const auto* ment = reinterpret_cast<const sgl::MergeEnt*>(ws + plan->off_ment);
     float* plse = reinterpret_cast<float*>(ws + plan->off_plse);
     float* po = reinterpret_cast<float*>(ws + plan->off_po);
     uint32_t* err = reinterpret_cast<uint32_t*>(ws);
-    const float sl2 = scale_log2_of(&p);
-    const int Hq = p.num_qo_heads, Hkv = p.num_kv_heads, G = plan->G, B = p.batch;
-    if (B == 0) return SGL_OK;
-    if (p.dtype == SGL_DTYPE_BF16) {
-        int e = sgl::launch_decode_wide_tc<D>(items, plan->n_wide, q, kp, vp, r2t, ld, seq_lens, members, po, plse,
-                                              err, Hq, Hkv, p.num_slots, sl2, s);
-        if (e) return cuda_status(static_cast<cudaError_t>(e));
-        e = sgl::launch_decode_narrow<D>(items + plan->n_wide, plan->n_items - plan->n_wide, q, kp, vp, r2t, ld,
-                                             seq_lens, members, po, plse, err, Hq, Hkv, G, p.num_slots, sl2, s);
-        if (e) return cuda_status(static_cast<cudaError_t>(e));
-    } else if (plan->n_items > 0) {
+    const int Hq = p.num_qo_heads, Hkv = p.num_kv_heads, G = plan->G;
+    if (plan->n_items > 0)
         decode_partial_f32<D><<<plan->n_items, 128, 0, s>>>(
             static_cast<const float*>(q), static_cast<const float*>(kp), static_cast<const float*>(vp), r2t, ld,
             seq_lens, items, members, po, plse, err, Hq, Hkv, G, p.num_slots, sl2);
-    }
-    int e = sgl::launch_decode_merge<D>(p.dtype == SGL_DTYPE_BF16, po, plse, mptr, ment, o, lse, B, Hq, Hkv, G, s);
-    if (e) return cuda_status(static_cast<cudaError_t>(e));
+    sgl::MergeArgs m{po, plse, reinterpret_cast<const int32_t*>(ws + plan->off_mptr),
+                     reinterpret_cast<const int32_t*>(ws + plan->off_ment), o, lse, Hq, Hkv, G};
+    const int n_pairs = p.batch * Hkv;
+    decode_merge_f32<D><<<(n_pairs + 3) / 4, 128, 0, s>>>(m, n_pairs);
     return cuda_status(cudaGetLastError());
 }
 

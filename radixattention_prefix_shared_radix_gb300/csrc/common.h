@@ -25,20 +25,21 @@ struct DecItem {
 };
 static_assert(sizeof(DecItem) == 32, "DecItem is 32 bytes");
 
-// Merge entry: partial row of (request, q head h = g * G + j) is
-// pbase + g * gstride + j.
-struct MergeEnt {
-    int32_t pbase;
-    int32_t gstride;
-};
+// Decode schedule constants (bf16 fused kernel): each CTA runs the tile
+// roles (7 warps) for its prefix-group tiles and kDecNarrowWarps streaming
+// warps for narrow items; a streaming warp holds at most kDecMaxItemsPerWarp
+// items and member rows (one lane each).
+constexpr int kDecNarrowWarps = 5;
+constexpr int kDecMaxItemsPerWarp = 32;
 
 // Workspace header (first 256 bytes): error word + plan dimensions.
 struct WsHeader {
     uint32_t error;        // bit 0: slot out of pool; bit 1: position beyond seq_len
     uint32_t magic;
     int32_t n_items;             // all work items: wide ones first, then narrow ones
-    int32_t n_wide;              // items with more than 8 query rows (tcgen05 tile kernel)
+    int32_t n_wide;              // items with more than 8 query rows (tcgen05 tiles)
     int32_t n_partial_rows;
+    int32_t n_ctas;              // CTAs of the fused decode kernel
 };
 constexpr uint32_t kWsMagic = 0x53474c41u;  // "SGLA"
 constexpr size_t kWsAlign = 256;
@@ -52,14 +53,19 @@ struct sgl_plan {
     sgl_attn_params params;      // host pointers cleared
     int32_t G;
     int32_t n_items;             // all work items: wide ones first, then narrow ones
-    int32_t n_wide;              // items with more than 8 query rows (tcgen05 tile kernel)
+    int32_t n_wide;              // items with more than 8 query rows (tcgen05 tiles)
     int32_t n_partial_rows;
+    int32_t n_ctas;              // fused decode kernel: CTAs (wide items wptr[c]..wptr[c+1])
     int32_t n_members;
     int32_t n_merge_entries;
     int32_t max_entries_per_request;
     int32_t chunk_tokens;
     int32_t max_pos;             // largest segment end (req_to_token must have ld >= max_pos)
-    size_t off_items, off_members, off_mptr, off_ment, off_plse, off_po, off_cnt;
+    // workspace offsets: items, members, wptr [n_ctas+1], nptr [n_ctas*kDecNarrowWarps+1]
+    // (item ranges of the tile roles / of each streaming warp), mptr [B*Hkv+1]
+    // and ment (first partial row of each merge entry of (request, KV head)),
+    // then the fp32 partial LSEs and rows and the merge counters.
+    size_t off_items, off_members, off_wptr, off_nptr, off_mptr, off_ment, off_plse, off_po, off_cnt;
     size_t tables_bytes;         // bytes uploaded (header + tables)
     size_t workspace_bytes;      // total device workspace
     unsigned char* blob;         // host copy of [0, tables_bytes)

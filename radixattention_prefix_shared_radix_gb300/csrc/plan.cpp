@@ -1,5 +1,5 @@
 // Prefix-group scheduler for decode: turns the batch's prefix groups into
-// GPU work items and the per-request merge lists.
+// GPU work items and the per-(request, KV head) merge lists.
 //
 // A segment (a run of positions shared by a set of member requests, read
 // from one representative row) is the unit of sharing: its K/V are read
@@ -7,18 +7,16 @@
 // referenced many times" ("SGLang：从前端 DSL 到 SRT 服务运行时", section
 // "用基数树实现前缀复用"; bhfrc.com/news/45689 §1.3).  The pages give no
 // kernel schedule; this one is ours:
-//   * a segment with at most 8 query rows (member x query head of a KV
-//     head) is narrow: its chunks go to a one-warp-per-item kernel, chunk
-//     length sized for ~24 warps of work per SM (>= 64 positions);
-//   * a wider segment (a prefix shared by many requests) is split into member
-//     blocks of up to 128 rows (one tensor-core tile), each chunk read once per
-//     block by a CTA that stages it in shared memory (tcgen05 kernel), chunk
-//     length a multiple of the 128-position KV block sized for ~1 CTA per SM;
-//   * items are ordered chunk-major with the KV head innermost, so work that
-//     runs together reads the heads of the same tokens (one token's K for
-//     all heads is one contiguous row of the slot-major pool);
-//   * each item writes its rows' normalised partial O and LSE (fp32); a
-//     request's merge list names every partial row it must combine.
+//   * a segment with more than 8 query rows (member x query head of a KV
+//     head; a prefix shared by many requests) becomes tensor-core tiles:
+//     member blocks of up to 128 rows x chunks of whole 128-position
+//     multiples (~1 tile of work per SM), dealt round-robin to the CTAs;
+//   * every other segment (at most 8 rows: a request's own suffix, or a
+//     small group) is narrow: its positions, per KV head, are cut into equal
+//     shares, one per streaming warp, so all warps stream the same bytes;
+//   * each item writes its rows' normalised partial O and LSE (fp32); the
+//     merge list of (request, KV head) names every partial row to combine.
+// The fp32 path runs the same items one CTA each.
 
 #include <algorithm>
 #include <cmath>
@@ -106,66 +104,134 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
     }
 
     // Narrow segments (at most 8 query rows: member x query head of a KV
-    // head) go to the one-warp-per-item kernel; wider ones to the CTA kernel
-    // in member blocks of up to 64 rows.
+    // head) go to the streaming warps; wider ones to the tensor-core tiles
+    // in member blocks of up to 128 rows.
     const int32_t MBn = std::max(1, 8 / G);
     const int32_t MBw = std::max(1, 128 / G);
-    double units_n = 0, units_w = 0;
+    const int sms = query_num_sms(p->num_sms);
+
+    // wide items: chunk-major, member block, KV head innermost
+    double units_w = 0;
     for (int32_t s = 0; s < nseg; ++s) {
         const int32_t nmem = g->seg_member_ptr[s + 1] - g->seg_member_ptr[s];
-        const double len = (double)(g->seg_end[s] - g->seg_begin[s]);
-        if (nmem <= MBn)
-            units_n += len * Hkv;
-        else
-            units_w += len * ((nmem + MBw - 1) / MBw) * Hkv;
+        if (nmem > MBn)
+            units_w += (double)(g->seg_end[s] - g->seg_begin[s]) * ((nmem + MBw - 1) / MBw) * Hkv;
     }
-    const int sms = query_num_sms(p->num_sms);
-    // narrow: ~24 warps of work per SM (16-position steps, chunks of >= 64)
-    int64_t Cn = (int64_t)std::ceil(units_n / (24.0 * sms));
-    Cn = std::max<int64_t>(64, (Cn + 15) / 16 * 16);
-    // wide: ~1 CTA of work per SM (128-position KV blocks)
+    // ~1 tile of work per SM, whole 128-position multiples
     int64_t Cw = (int64_t)std::ceil(units_w / (1.0 * sms));
     Cw = std::max<int64_t>(128, (Cw + 127) / 128 * 128);
-    const int64_t C = Cn;
-
-    std::vector<sgl::DecItem> wide, narrow;
-    std::vector<std::vector<sgl::MergeEnt>> ents(B);
-    int64_t prow = 0;
+    std::vector<sgl::DecItem> wide;
+    struct Unit {   // narrow work: one member block of a segment for one KV head
+        int32_t rep_row, b, e, kvh, mem_begin, n_mem;
+    };
+    std::vector<Unit> units;
+    int64_t units_n = 0;
     for (int32_t s = 0; s < nseg; ++s) {
         const int32_t b = g->seg_begin[s], e = g->seg_end[s];
         const int32_t m0 = g->seg_member_ptr[s], nmem = g->seg_member_ptr[s + 1] - m0;
-        const bool is_narrow = nmem <= MBn;
-        const int32_t MB = is_narrow ? MBn : MBw;
-        const int64_t CS = is_narrow ? Cn : Cw;
-        const int32_t nblk = (nmem + MB - 1) / MB;
-        for (int64_t cb = b; cb < e; cb += CS) {
-            const int32_t ce = (int32_t)std::min<int64_t>(e, cb + CS);
+        if (nmem <= MBn) {
+            for (int32_t h = 0; h < Hkv; ++h) {
+                units.push_back({g->seg_row[s], b, e, h, m0, nmem});
+                units_n += e - b;
+            }
+            continue;
+        }
+        const int32_t nblk = (nmem + MBw - 1) / MBw;
+        for (int64_t cb = b; cb < e; cb += Cw) {
+            const int32_t ce = (int32_t)std::min<int64_t>(e, cb + Cw);
             for (int32_t blk = 0; blk < nblk; ++blk) {
-                const int32_t mb = blk * MB, nm = std::min(MB, nmem - mb);
-                const int64_t base0 = prow;
-                for (int32_t h = 0; h < Hkv; ++h) {
-                    sgl::DecItem it;
-                    it.rep_row = g->seg_row[s];
-                    it.kv_begin = (int32_t)cb;
-                    it.kv_end = ce;
-                    it.kvh = h;
-                    it.mem_begin = m0 + mb;
-                    it.n_mem = nm;
-                    it.partial_base = (int32_t)prow;
-                    it.pad = 0;
-                    (is_narrow ? narrow : wide).push_back(it);
-                    prow += (int64_t)nm * G;
-                }
-                for (int32_t i = 0; i < nm; ++i) {
-                    int32_t r = g->seg_members[m0 + mb + i];
-                    ents[r].push_back({(int32_t)(base0 + (int64_t)i * G), nm * G});
-                }
+                const int32_t mb = blk * MBw, nm = std::min(MBw, nmem - mb);
+                for (int32_t h = 0; h < Hkv; ++h)
+                    wide.push_back({g->seg_row[s], (int32_t)cb, ce, h, m0 + mb, nm, 0, 0});
             }
         }
     }
-    if (prow > INT32_MAX / 256) return SGL_ERR_UNSUPPORTED;
-    std::vector<sgl::DecItem> items(wide);
-    items.insert(items.end(), narrow.begin(), narrow.end());
+
+    // Narrow units are cut into equal shares of positions, one share per
+    // streaming warp (n_ctas CTAs x kDecNarrowWarps warps), so every warp
+    // streams about the same number of bytes; a cut makes two items (two
+    // partials).  Pieces shorter than one 16-position step are avoided; the
+    // member rows of a warp's items (sum of n_mem, >= its item count) are at
+    // most kDecMaxItemsPerWarp: one lane per item and per deferred merge.
+    constexpr int NW = sgl::kDecNarrowWarps;
+    // Streaming warps that share their SM with tile roles stream slower
+    // (measured ~0.73x on the Llama-3-8B-shaped batch); they get
+    // proportionally smaller shares.
+    constexpr double kTileCtaShare = 0.73;
+    int64_t n_ctas = sms;
+    std::vector<std::vector<sgl::DecItem>> warp_items;
+    for (int attempt = 0;; ++attempt) {
+        const int64_t nwt = n_ctas * NW;
+        const int64_t n_tile_ctas = std::min<int64_t>((int64_t)wide.size(), n_ctas);   // round-robin below
+        const double weight = (double)NW * ((double)(n_ctas - n_tile_ctas) + kTileCtaShare * (double)n_tile_ctas);
+        int64_t T = std::max<int64_t>(16, (int64_t)std::ceil((double)units_n / weight));
+        bool ok = false;
+        for (int tries = 0; tries < 64 && !ok; ++tries, T += 16) {
+            auto cap_of = [&](int64_t w) {
+                const bool tile_cta = w / NW < n_tile_ctas;
+                const int64_t c = tile_cta ? (int64_t)std::ceil(kTileCtaShare * (double)T) : T;
+                return std::max<int64_t>(16, (c + 15) / 16 * 16);
+            };
+            warp_items.assign((size_t)nwt, {});
+            int64_t w = 0, cap = cap_of(0), mem_rows = 0;
+            bool fail = false;
+            for (const Unit& u : units) {
+                int64_t pos = u.b;
+                while (pos < u.e && !fail) {
+                    if (cap < 16 || mem_rows + u.n_mem > sgl::kDecMaxItemsPerWarp) {
+                        if (++w >= nwt) {
+                            fail = true;
+                            break;
+                        }
+                        cap = cap_of(w);
+                        mem_rows = 0;
+                    }
+                    int64_t take = std::min<int64_t>(u.e - pos, cap);
+                    if (u.e - pos - take < 16) take = u.e - pos;   // no tail piece under one step
+                    warp_items[w].push_back({u.rep_row, (int32_t)pos, (int32_t)(pos + take), u.kvh, u.mem_begin,
+                                             u.n_mem, 0, 0});
+                    pos += take;
+                    cap -= take;
+                    mem_rows += u.n_mem;
+                }
+                if (fail) break;
+            }
+            ok = !fail;
+        }
+        if (ok) break;
+        if (n_ctas > (int64_t)1 << 20) return SGL_ERR_UNSUPPORTED;
+        n_ctas *= 2;   // too many items per warp: more warps
+    }
+    // wide items round-robin over the CTAs
+    std::vector<std::vector<sgl::DecItem>> cta_items((size_t)n_ctas);
+    for (size_t i = 0; i < wide.size(); ++i) cta_items[i % (size_t)n_ctas].push_back(wide[i]);
+
+    // final item order: wide items by CTA, then narrow items by warp;
+    // partial rows in item order
+    std::vector<sgl::DecItem> items;
+    std::vector<int32_t> wptr, nptr;
+    wptr.push_back(0);
+    for (auto& v : cta_items) {
+        items.insert(items.end(), v.begin(), v.end());
+        wptr.push_back((int32_t)items.size());
+    }
+    const int32_t n_wide = (int32_t)items.size();
+    nptr.push_back(n_wide);
+    for (auto& v : warp_items) {
+        items.insert(items.end(), v.begin(), v.end());
+        nptr.push_back((int32_t)items.size());
+    }
+    std::vector<std::vector<int32_t>> ents((size_t)B * Hkv);
+    int64_t prow = 0;
+    for (auto& it : items) {
+        it.partial_base = (int32_t)prow;
+        for (int32_t i = 0; i < it.n_mem; ++i) {
+            const int32_t r = g->seg_members[it.mem_begin + i];
+            ents[(size_t)r * Hkv + it.kvh].push_back((int32_t)(prow + (int64_t)i * G));
+        }
+        prow += (int64_t)it.n_mem * G;
+        if (prow > INT32_MAX / 256) return SGL_ERR_UNSUPPORTED;
+    }
 
     sgl_plan* plan = new (std::nothrow) sgl_plan();
     if (!plan) return SGL_ERR_INVALID_ARG;
@@ -174,8 +240,9 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
     plan->params.host_extend_lens = nullptr;
     plan->G = G;
     plan->n_items = (int32_t)items.size();
-    plan->n_wide = (int32_t)wide.size();
+    plan->n_wide = n_wide;
     plan->n_partial_rows = (int32_t)prow;
+    plan->n_ctas = (int32_t)n_ctas;
     plan->n_members = g->num_members;
     int64_t n_ent = 0;
     int32_t max_ent = 0;
@@ -184,7 +251,7 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
         max_ent = std::max<int32_t>(max_ent, (int32_t)v.size());
     }
     plan->n_merge_entries = (int32_t)n_ent;
-    plan->chunk_tokens = (int32_t)C;
+    plan->chunk_tokens = (int32_t)Cw;
     plan->max_pos = 0;
     for (int32_t s = 0; s < nseg; ++s) plan->max_pos = std::max(plan->max_pos, g->seg_end[s]);
     plan->max_entries_per_request = max_ent;
@@ -193,9 +260,11 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
     const size_t A = sgl::kWsAlign;
     plan->off_items = A;
     plan->off_members = align_up(plan->off_items + items.size() * sizeof(sgl::DecItem), A);
-    plan->off_mptr = align_up(plan->off_members + (size_t)g->num_members * 4, A);
-    plan->off_ment = align_up(plan->off_mptr + (size_t)(B + 1) * 4, A);
-    plan->tables_bytes = align_up(plan->off_ment + (size_t)n_ent * sizeof(sgl::MergeEnt), A);
+    plan->off_wptr = align_up(plan->off_members + (size_t)g->num_members * 4, A);
+    plan->off_nptr = align_up(plan->off_wptr + wptr.size() * 4, A);
+    plan->off_mptr = align_up(plan->off_nptr + nptr.size() * 4, A);
+    plan->off_ment = align_up(plan->off_mptr + ((size_t)B * Hkv + 1) * 4, A);
+    plan->tables_bytes = align_up(plan->off_ment + (size_t)n_ent * 4, A);
     plan->off_plse = plan->tables_bytes;
     plan->off_po = align_up(plan->off_plse + (size_t)prow * 4, A);
     plan->off_cnt = align_up(plan->off_po + (size_t)prow * p->head_dim * 4, A);
@@ -207,18 +276,20 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
         return SGL_ERR_INVALID_ARG;
     }
     std::memset(plan->blob, 0, plan->tables_bytes);
-    sgl::WsHeader hdr{0u, sgl::kWsMagic, plan->n_items, plan->n_partial_rows};
+    sgl::WsHeader hdr{0u, sgl::kWsMagic, plan->n_items, plan->n_wide, plan->n_partial_rows, plan->n_ctas};
     std::memcpy(plan->blob, &hdr, sizeof(hdr));
     if (!items.empty()) std::memcpy(plan->blob + plan->off_items, items.data(), items.size() * sizeof(sgl::DecItem));
     if (g->num_members) std::memcpy(plan->blob + plan->off_members, g->seg_members, (size_t)g->num_members * 4);
+    std::memcpy(plan->blob + plan->off_wptr, wptr.data(), wptr.size() * 4);
+    std::memcpy(plan->blob + plan->off_nptr, nptr.data(), nptr.size() * 4);
     int32_t* mptr = reinterpret_cast<int32_t*>(plan->blob + plan->off_mptr);
-    sgl::MergeEnt* ment = reinterpret_cast<sgl::MergeEnt*>(plan->blob + plan->off_ment);
+    int32_t* ment = reinterpret_cast<int32_t*>(plan->blob + plan->off_ment);
     int64_t at = 0;
-    for (int32_t r = 0; r < B; ++r) {
-        mptr[r] = (int32_t)at;
-        for (auto& e : ents[r]) ment[at++] = e;
+    for (size_t i = 0; i < ents.size(); ++i) {
+        mptr[i] = (int32_t)at;
+        for (int32_t e : ents[i]) ment[at++] = e;
     }
-    mptr[B] = (int32_t)at;
+    mptr[ents.size()] = (int32_t)at;
     *plan_out = plan;
     *workspace_bytes = plan->workspace_bytes;
     return SGL_OK;
