@@ -17,7 +17,7 @@ GB/s: the K/V bytes of every prefix-group segment counted once per step.
   * extend: TFLOP/s of the chunked-prefill workload (8 requests, cached
     4096-token prefix + 512 causal new tokens, Hq 64 / Hkv 8), unmasked
     query-key pairs x 4 d FLOP.
-  * roofline: the decode call is one kernel launch (the fused persistent
+  * roofline: the decode call (the persistent partial kernel + the merge
     kernel); achieved = unique-KV bytes per call / call time, against the
     measured HBM copy bandwidth; ncu DRAM traffic per call from profiles/
     when current.
@@ -401,7 +401,7 @@ def run_native(args):
         ext = bench_extend(sgl, W, torch, max(3, args.extend_steps), bf16_peak)
 
     traffic = profile_traffic("decode_partial")
-    launches_per_call = 1   # bf16 decode: one fused persistent kernel per call
+    launches_per_call = 2   # bf16 decode: the persistent partial kernel and the merge kernel
     B = inst[0]["B"]
     line = {
         "metric": METRIC,
@@ -429,7 +429,7 @@ def run_native(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "peak_source": peak_src,
                      "frac_of_8TBs": achieved / 8000.0, "traffic": traffic,
-                     "kernel": "decode_fused_kernel (one launch per decode call: unique-KV bytes / call time)"},
+                     "kernel": "decode call = decode_fused_kernel + decode_merge_kernel (unique-KV bytes / call time)"},
         "e2e": {"value": e2e_gbs, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_step_s * 1e3 if e2e_step_s else None},
         "gpu_launches": K * launches_per_call,

@@ -7,9 +7,9 @@
 // of a KV head ("computed once, referenced many times", "SGLang：从前端 DSL 到
 // SRT 服务运行时", section "用基数树实现前缀复用").  Each item writes normalised
 // partial rows (O, LSE) that a log-sum-exp merge combines per (request, head).
-//   * bf16: one launch of the fused persistent kernel (decode_fused.cu):
-//     tcgen05 tiles for shared segments, streaming warps for the rest, merge
-//     by the last producer of each (request, KV head).
+//   * bf16: the persistent decode kernel (decode_fused.cu): tcgen05 tiles
+//     for shared segments beside producer/consumer streaming warps for the
+//     rest; then the merge launch, one warp per (request, KV head).
 //   * fp32 (exact CUDA-core arithmetic): one CTA per work item, then a merge
 //     launch, one warp per (request, KV head).
 //
@@ -103,18 +103,6 @@ __global__ void __launch_bounds__(128)
         for (int e = 0; e < E; ++e) po[prow * D + lane * E + e] = o[e] * inv;
         if (lane == 0) plse[prow] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
     }
-}
-
-// fp32 merge: one warp per (request, KV head).
-template <int D>
-__global__ void __launch_bounds__(128) decode_merge_f32(const sgl::MergeArgs m, int n_pairs) {
-    const int idx = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-    if (idx >= n_pairs) return;
-    const int e0 = __ldg(m.mptr + idx), E = __ldg(m.mptr + idx + 1) - e0;
-    if (E == 0)
-        sgl::merge_empty<float, D>(m, idx, lane);
-    else
-        sgl::merge_warp<float, D>(m, idx, e0, E, lane);
 }
 
 // ---------------------------------------------------------------------------
@@ -225,7 +213,7 @@ int launch_decode(const sgl_plan* plan, const void* q, const void* kp, const voi
     sgl::MergeArgs m{po, plse, reinterpret_cast<const int32_t*>(ws + plan->off_mptr),
                      reinterpret_cast<const int32_t*>(ws + plan->off_ment), o, lse, Hq, Hkv, G};
     const int n_pairs = p.batch * Hkv;
-    decode_merge_f32<D><<<(n_pairs + 3) / 4, 128, 0, s>>>(m, n_pairs);
+    sgl::decode_merge_kernel<float, D><<<(n_pairs + 3) / 4, 128, 0, s>>>(m, n_pairs);
     return cuda_status(cudaGetLastError());
 }
 

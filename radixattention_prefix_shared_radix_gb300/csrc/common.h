@@ -25,11 +25,12 @@ struct DecItem {
 };
 static_assert(sizeof(DecItem) == 32, "DecItem is 32 bytes");
 
-// Decode schedule constants (bf16 fused kernel): each CTA runs the tile
+// Decode schedule constants (bf16 persistent kernel): each CTA runs the tile
 // roles (7 warps) for its prefix-group tiles and kDecNarrowWarps streaming
-// warps for narrow items; a streaming warp holds at most kDecMaxItemsPerWarp
-// items and member rows (one lane each).
-constexpr int kDecNarrowWarps = 5;
+// consumer warps for narrow items (fed by kDecNarrowWarps / 2 producer
+// warps); a consumer holds at most kDecMaxItemsPerWarp items and member rows
+// (one lane each).
+constexpr int kDecNarrowWarps = 4;
 constexpr int kDecMaxItemsPerWarp = 32;
 
 // Workspace header (first 256 bytes): error word + plan dimensions.

@@ -248,6 +248,25 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
         if (mbar_try(bar, parity)) return true;
     return false;
 }
+// Same wait, but each try suspends the thread for up to `hint_ns` until the
+// phase completes instead of returning at once: waiting warps then stop
+// issuing polls that compete with the copies they wait for.  Bounded by
+// kSleepLimit tries (seconds in total).
+constexpr uint32_t kSleepLimit = 1u << 16;
+__device__ __forceinline__ bool mbar_try_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity) {
+    for (uint32_t i = 0; i < kSleepLimit; ++i)
+        if (mbar_try_sleep(bar, parity, 20000u)) return true;
+    return false;
+}
 // Global -> shared bulk copy of `bytes` (multiple of 16, both addresses
 // 16-byte aligned), completing on mbarrier `bar`.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {

@@ -139,4 +139,17 @@ __device__ __forceinline__ void merge_empty(const MergeArgs& m, int idx, int lan
     }
 }
 
+// One warp per (request, KV head) pair: the log-sum-exp merge of its
+// entries, or O = 0 / LSE = -inf for a pair without entries (seq_len 0).
+template <typename OutT, int D>
+__global__ void __launch_bounds__(128) decode_merge_kernel(const MergeArgs m, int n_pairs) {
+    const int idx = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (idx >= n_pairs) return;
+    const int e0 = __ldg(m.mptr + idx), E = __ldg(m.mptr + idx + 1) - e0;
+    if (E == 0)
+        merge_empty<OutT, D>(m, idx, lane);
+    else
+        merge_warp<OutT, D>(m, idx, e0, E, lane);
+}
+
 }  // namespace sgl

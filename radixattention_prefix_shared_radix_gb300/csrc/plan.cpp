@@ -155,9 +155,9 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
     // most kDecMaxItemsPerWarp: one lane per item and per deferred merge.
     constexpr int NW = sgl::kDecNarrowWarps;
     // Streaming warps that share their SM with tile roles stream slower
-    // (measured ~0.73x on the Llama-3-8B-shaped batch); they get
+    // (measured ~0.62x on the Llama-3-8B-shaped batch); they get
     // proportionally smaller shares.
-    constexpr double kTileCtaShare = 0.73;
+    constexpr double kTileCtaShare = 0.62;
     int64_t n_ctas = sms;
     std::vector<std::vector<sgl::DecItem>> warp_items;
     for (int attempt = 0;; ++attempt) {
