@@ -25,13 +25,10 @@ struct DecItem {
 };
 static_assert(sizeof(DecItem) == 32, "DecItem is 32 bytes");
 
-// Decode schedule constants (bf16 persistent kernel): each CTA runs the tile
+// Decode schedule constant (bf16 persistent kernel): each CTA runs the tile
 // roles (7 warps) for its prefix-group tiles and kDecNarrowWarps streaming
-// consumer warps for narrow items (fed by kDecNarrowWarps / 2 producer
-// warps); a consumer holds at most kDecMaxItemsPerWarp items and member rows
-// (one lane each).
+// consumer warps for narrow pieces, each fed by its own producer warp.
 constexpr int kDecNarrowWarps = 4;
-constexpr int kDecMaxItemsPerWarp = 32;
 
 // Workspace header (first 256 bytes): error word + plan dimensions.
 struct WsHeader {
@@ -57,16 +54,19 @@ struct sgl_plan {
     int32_t n_wide;              // items with more than 8 query rows (tcgen05 tiles)
     int32_t n_partial_rows;
     int32_t n_ctas;              // fused decode kernel: CTAs (wide items wptr[c]..wptr[c+1])
+    int32_t n_narrow;            // narrow pieces (items n_wide .. n_items-1, longest first)
+    int32_t n_init;              // pieces assigned at launch (consumer w starts on piece w)
     int32_t n_members;
     int32_t n_merge_entries;
     int32_t max_entries_per_request;
     int32_t chunk_tokens;
     int32_t max_pos;             // largest segment end (req_to_token must have ld >= max_pos)
-    // workspace offsets: items, members, wptr [n_ctas+1], nptr [n_ctas*kDecNarrowWarps+1]
-    // (item ranges of the tile roles / of each streaming warp), mptr [B*Hkv+1]
-    // and ment (first partial row of each merge entry of (request, KV head)),
-    // then the fp32 partial LSEs and rows and the merge counters.
-    size_t off_items, off_members, off_wptr, off_nptr, off_mptr, off_ment, off_plse, off_po, off_cnt;
+    // workspace offsets: items, members, wptr [n_ctas+1] (wide items of each
+    // CTA), sched [2] (run-time piece counter and finished-producer count,
+    // restored by the kernel), mptr [B*Hkv+1] and ment (first partial row of
+    // each merge entry of (request, KV head)), then the fp32 partial LSEs and
+    // rows and a spare counter area.
+    size_t off_items, off_members, off_wptr, off_sched, off_mptr, off_ment, off_plse, off_po, off_cnt;
     size_t tables_bytes;         // bytes uploaded (header + tables)
     size_t workspace_bytes;      // total device workspace
     unsigned char* blob;         // host copy of [0, tables_bytes)

@@ -14,9 +14,11 @@
 //               rows (member request x query head of one KV head);
 //   warps 7-10  streaming producers: each issues the cp.async gathers of one
 //               consumer's K/V rows into its shared-memory ring;
-//   warps 11-14 streaming consumers: each runs its own list of narrow items
-//               (at most 8 query rows: one request's G heads, or a few
-//               members of a small group) on the tensor cores.
+//   warps 11-14 streaming consumers: each runs narrow pieces (at most 8
+//               query rows: one request's G heads, or a few members of a
+//               small group) on the tensor cores: its launch piece, then
+//               pieces its producer takes from a run-time counter, so faster
+//               SMs stream more and all finish together.
 // The tiles are bound by latency and the tensor pipe, the streams by HBM; the
 // two run side by side on every SM.  Producers and consumers are separate
 // warps so the copies keep flowing while the consumers compute, and there is
@@ -25,13 +27,14 @@
 // cycles once the SM's load pipe is busy, so the SM's issue rate (and HBM
 // bandwidth) grows with the number of issuing warps.
 //
-// Streaming ring per consumer: 4 stages of 16 positions (K and V rows, 8 KB),
-// a FULL mbarrier per stage (each producer lane arrives when its copies have
-// landed: cp.async.mbarrier.arrive.noinc) and an EMPTY mbarrier (the consumer
-// arrives when it has read the stage).  The producer looks slots up six steps
-// ahead with 4-byte cp.async into a small slot ring, so no register ever
-// waits on a load in flight; its own cp.async groups order slot lookups
-// before their use.
+// Streaming ring per consumer: 4 stages of 16 positions (K and V rows, 8 KB)
+// with a descriptor each (first position, piece, flags), a FULL mbarrier per
+// stage (each producer lane arrives when its copies have landed:
+// cp.async.mbarrier.arrive.noinc, and lane 0 once more to release the
+// descriptor) and an EMPTY mbarrier (the consumer arrives when it has read
+// the stage).  The producer looks slots up six steps ahead with 4-byte
+// cp.async into a small slot ring, so no register ever waits on a load in
+// flight; its own cp.async groups order slot lookups before their use.
 //
 // Consumer, per 16-position step (mma.sync m16n8k16, bf16 in, fp32 acc;
 // query rows in the MMA's N dimension):
@@ -39,8 +42,9 @@
 //   O^T [d x 8 rows]     += V^T [d x 16 pos] . P^T [16 pos x 8 rows]
 // K and V rows are XOR-swizzled [16 x d] tiles (ldmatrix for K,
 // ldmatrix.trans for V^T, conflict-free); P^T moves from the accumulator
-// layout to the B-operand layout with movmatrix.  The next item's query rows
-// are fetched while the current item runs.
+// layout to the B-operand layout with movmatrix.  The next piece's query rows
+// are fetched while the current piece runs (the producer announces the piece
+// in shared memory as soon as it starts looking it up).
 //
 // Every item writes normalised partial rows (O fp32, LSE natural log); the
 // merge launch (merge.cuh) combines each (request, KV head)'s partials once
@@ -62,6 +66,7 @@ constexpr int kNS = 4;                                   // ring stages per cons
 constexpr int kNP = 16;                                  // KV positions per step
 constexpr int kQD = 6;                                   // slot lookups ahead (steps per consumer)
 constexpr int kSQ = 8;                                   // slot ring entries per consumer
+constexpr int kSlotEntry = kNP * 4 + 16;                 // 16 slots + KV head, piece, position, flags
 constexpr int kFirstProducer = kTileThreads / 32;
 constexpr int kFirstConsumer = kFirstProducer + kProducers;
 constexpr int kFusedThreads = 32 * (kFirstConsumer + kConsumers);
@@ -73,10 +78,12 @@ struct FusedLayout {
     static constexpr int TILEB = kNP * D * 2;            // one K (or V) tile of a step
     static constexpr int STAGE = 2 * TILEB;
     static constexpr int RING = kNS * STAGE;             // per consumer
-    static constexpr int SLOTW = kSQ * kNP * 4 + kSQ * 4;   // slots + KV heads per consumer
+    static constexpr int SLOTW = kSQ * kSlotEntry;       // slot ring per consumer
     static constexpr int OFF_RING = (TL::END + 127) / 128 * 128;
     static constexpr int OFF_SLOT = OFF_RING + kConsumers * RING;
-    static constexpr int OFF_SBAR = OFF_SLOT + kConsumers * SLOTW;   // FULL[kNS], EMPTY[kNS] per consumer
+    static constexpr int OFF_DESC = OFF_SLOT + kConsumers * SLOTW;   // kNS stage descriptors (16 B) per consumer
+    static constexpr int OFF_ANN = OFF_DESC + kConsumers * kNS * 16; // announced piece per consumer
+    static constexpr int OFF_SBAR = OFF_ANN + kConsumers * 16;       // FULL[kNS], EMPTY[kNS] per consumer
     static constexpr int END = OFF_SBAR + kConsumers * 2 * kNS * 8;
     static constexpr int TOTAL = END + 1024;             // + alignment slack
     static_assert(TOTAL <= 232448, "shared memory per CTA");
@@ -85,7 +92,10 @@ struct FusedLayout {
 struct FusedArgs {
     TcArgs t;
     const int32_t* wptr;   // [n_ctas + 1] wide items of each CTA
-    const int32_t* nptr;   // [n_ctas * kConsumers + 1] narrow items of each consumer
+    const DecItem* narrow; // narrow pieces, longest first
+    int n_narrow;
+    int n_init;            // pieces assigned at launch: consumer w starts on piece w
+    uint32_t* sched;       // [2] next piece to hand out, producers finished (restored at the end)
 };
 
 __device__ __forceinline__ uint32_t movtrans(uint32_t x) {
@@ -94,44 +104,31 @@ __device__ __forceinline__ uint32_t movtrans(uint32_t x) {
     return y;
 }
 
-// Fields of a warp's items, lane k holding item it0 + k (at most 32 items).
-struct ItemFields {
-    int row = 0, b = 0, e = 0, h = 0, mb = 0, nm = 0, pb = 0;
-    __device__ __forceinline__ void load(const DecItem* items, int it0, int n_it, int lane) {
-        if (lane < n_it) {
-            const int4* ip = reinterpret_cast<const int4*>(items + it0 + lane);
-            const int4 x = __ldg(ip), y = __ldg(ip + 1);
-            row = x.x;
-            b = x.y;
-            e = x.z;
-            h = x.w;
-            mb = y.x;
-            nm = y.y;
-            pb = y.z;
-        }
-    }
-};
-
-__device__ __forceinline__ int fld(int v, int k) { return __shfl_sync(0xffffffffu, v, k); }
-
-__device__ __forceinline__ int total_steps(const ItemFields& it, int n_it, int lane) {
-    int s = lane < n_it ? (it.e - it.b + kNP - 1) / kNP : 0;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    return s;
+__device__ __forceinline__ int ld_volatile_shared_s32(uint32_t addr) {
+    int32_t v;
+    asm volatile("ld.volatile.shared.b32 %0, [%1];\n" : "=r"(v) : "r"(addr) : "memory");
+    return v;
 }
 
-// ---------------------------------------------------------------------------
-// Producer: NCP consumers' rings, steps interleaved
-// ---------------------------------------------------------------------------
-struct SlotCursor {        // the next step of one consumer whose slots are looked up
-    int si, sp, n;         // item, position, steps looked up so far
-};
+// stage descriptor flags
+constexpr int kFirst = 1;   // first step of its piece
+constexpr int kEnd = 4;     // no more pieces: the consumer stops
 
-template <int D, int NCP>
-__device__ __noinline__ void stream_producer(const FusedArgs& f, const int (&it0)[NCP], const int (&n_it)[NCP],
-                                             const uint32_t (&ring)[NCP], const uint32_t (&sring)[NCP],
-                                             const uint32_t (&full)[NCP], const uint32_t (&empty)[NCP], int lane) {
+// ---------------------------------------------------------------------------
+// Producer
+// ---------------------------------------------------------------------------
+// Walks this consumer's pieces (its launch piece, then pieces taken from the
+// run-time counter), looks up each step's slots kQD steps ahead (4-byte
+// cp.async into the slot ring, with the step's KV head, piece, position and
+// flags beside them), and for each step waits for the ring stage to be free,
+// issues the K/V row copies, writes the stage descriptor and arrives on the
+// stage's FULL barrier (32 lanes when their copies land + lane 0 releasing the
+// descriptor).  The next piece is fetched in phases spread over the steps
+// (take a number from the counter; load its record), so no register waits on
+// a load in flight.
+template <int D>
+__device__ __noinline__ void stream_producer(const FusedArgs& f, int gw, uint32_t ring, uint32_t sring,
+                                             uint32_t desc, uint32_t ann, uint32_t full, uint32_t empty, int lane) {
     using Lay = FusedLayout<D>;
     constexpr int CPR = D / 8;                 // 16-byte chunks per row
     constexpr int RPI = 32 / CPR;              // rows per warp instruction
@@ -144,107 +141,161 @@ __device__ __noinline__ void stream_producer(const FusedArgs& f, const int (&it0
     uint32_t* const err = f.t.err;
     const int Hkv = f.t.Hkv;
     const int64_t num_slots = f.t.num_slots;
+    const DecItem* const pieces = f.narrow;
+    const int n_narrow = f.n_narrow;
+    uint32_t* const sched = f.sched;
 
-    ItemFields it[NCP];
-    int steps[NCP];
-    SlotCursor cur[NCP];
-#pragma unroll
-    for (int c = 0; c < NCP; ++c) {
-        it[c].load(f.t.items, it0[c], n_it[c], lane);
-        steps[c] = total_steps(it[c], n_it[c], lane);
-        cur[c] = {0, fld(it[c].b, 0), 0};
-        while (cur[c].si < n_it[c] && cur[c].sp >= fld(it[c].e, cur[c].si)) {
-            ++cur[c].si;
-            if (cur[c].si < n_it[c]) cur[c].sp = fld(it[c].b, cur[c].si);
+    // next-piece pipeline: 0 take a number, 1 number in flight (lane 0),
+    // 2 record in flight, 3 ready; `none` once the counter ran out
+    int nx_id = 0, nx_stage = 0, nx_row = 0, nx_b = 0, nx_e = 0, nx_h = 0, taken = 0;
+    bool none = false;
+    auto load_record = [&]() {
+        if (nx_id < n_narrow) {
+            const int4 x = __ldg(reinterpret_cast<const int4*>(pieces + nx_id));
+            nx_row = x.x;
+            nx_b = x.y;
+            nx_e = x.z;
+            nx_h = x.w;
+        } else {
+            none = true;
         }
+    };
+    if (gw < f.n_init) {
+        nx_id = gw;
+        load_record();
+        nx_stage = 2;
     }
-    // slots of consumer c's next step into its slot ring (kPastEnd beyond the
-    // item), its KV head into the head ring (-1: no step)
-    auto look_up = [&](int c) {
-        SlotCursor& q = cur[c];
-        const int ent = q.n & (kSQ - 1);
-        const uint32_t hring = sring[c] + kSQ * kNP * 4;
-        int kvh = -1;
-        if (q.si < n_it[c]) {
-            const int row = fld(it[c].row, q.si), e = fld(it[c].e, q.si);
-            kvh = fld(it[c].h, q.si);
-            const int p = q.sp + lane;
-            const uint32_t dst = sring[c] + (ent * kNP + lane) * 4;
+    auto advance = [&]() {
+        if (none) return;
+        if (nx_stage == 0) {
+            if (lane == 0) taken = (int)atomicAdd(sched, 1u);
+            nx_stage = 1;
+        } else if (nx_stage == 1) {
+            nx_id = __shfl_sync(0xffffffffu, taken, 0);
+            load_record();
+            nx_stage = 2;
+        } else if (nx_stage == 2) {
+            nx_stage = 3;
+        }
+    };
+
+    // slot cursor over the current piece
+    bool have = false, done = false;
+    int cur_id = 0, row = 0, e = 0, h = 0, sp = 0, nlook = 0;
+    auto look_up = [&]() {
+        const int ent = nlook & (kSQ - 1);
+        const uint32_t eb = sring + ent * kSlotEntry;
+        int kvh = -1, id = 0, p0 = 0, flags = 0;
+        if (!done && (!have || sp >= e)) {
+            while (!none && nx_stage < 3) advance();
+            if (none) {
+                have = false;
+                done = true;
+            } else {
+                have = true;
+                cur_id = nx_id;
+                row = nx_row;
+                sp = nx_b;
+                e = nx_e;
+                h = nx_h;
+                flags = kFirst;
+                nx_stage = 0;
+                if (lane == 0) st_shared_s32(ann, cur_id);   // lets the consumer fetch its query rows early
+            }
+        }
+        if (have && !done) {
+            kvh = h;
+            id = cur_id;
+            p0 = sp;
+            const int p = sp + lane;
             if (lane < kNP) {
                 if (p < e)
-                    cp_async4(dst, r2t + (int64_t)row * ld + p);
+                    cp_async4(eb + lane * 4, r2t + (int64_t)row * ld + p);
                 else
-                    st_shared_s32(dst, kPastEnd);
+                    st_shared_s32(eb + lane * 4, kPastEnd);
             }
-            q.sp += kNP;
-            while (q.si < n_it[c] && q.sp >= fld(it[c].e, q.si)) {
-                ++q.si;
-                if (q.si < n_it[c]) q.sp = fld(it[c].b, q.si);
-            }
+            sp += kNP;
         }
-        if (lane == 0) st_shared_s32(hring + ent * 4, kvh);
-        ++q.n;
+        if (lane == 0) {
+            st_shared_s32(eb + 64, kvh);
+            st_shared_s32(eb + 68, id);
+            st_shared_s32(eb + 72, p0);
+            st_shared_s32(eb + 76, flags);
+        }
+        ++nlook;
+        advance();
     };
-    for (int k = 0; k < kQD; ++k)
-#pragma unroll
-        for (int c = 0; c < NCP; ++c) look_up(c);
+#pragma unroll 1
+    for (int k = 0; k < kQD; ++k) look_up();
     cp_async_commit();
     cp_async_wait<0>();
     __syncwarp();
 
-    // Round r issues step r of each consumer (one cp.async group each, empty
-    // once a consumer has no steps left, so the group count stays regular:
-    // the lookup of (c, r) is in the group committed NCP*kQD groups earlier).
     bool timed_out = false;
-    int rounds = 0;
-#pragma unroll
-    for (int c = 0; c < NCP; ++c) rounds = steps[c] > rounds ? steps[c] : rounds;
-    for (int r = 0; r < rounds; ++r) {
-#pragma unroll
-        for (int c = 0; c < NCP; ++c) {
-            cp_async_wait<NCP * kQD - 1>();
-            __syncwarp();
-            if (r < steps[c]) {
-                const int st = r % kNS;
-                if (!timed_out && !mbar_wait_sleep(empty[c] + 8 * st, ((r / kNS) & 1) ^ 1)) {
-                    atomicOr(err, 4u);
-                    timed_out = true;
-                }
-                const int ent = r & (kSQ - 1);
-                const int kvh = ld_shared_s32(sring[c] + kSQ * kNP * 4 + ent * 4);
-                int32_t sl = lane < kNP ? ld_shared_s32(sring[c] + (ent * kNP + lane) * 4) : kPastEnd;
-                if (sl == kPastEnd) {
-                    sl = -1;
-                } else if (sl < 0 || sl >= num_slots) {
-                    atomicOr(err, 1u);
-                    sl = -1;
-                }
-                const uint32_t kd = ring[c] + st * Lay::STAGE, vd = kd + Lay::TILEB;
-                const int ch = lane % CPR;
-#pragma unroll
-                for (int k = 0; k < kNP / RPI; ++k) {
-                    const int rl = k * RPI + lane / CPR;
-                    const int32_t sr = __shfl_sync(0xffffffffu, sl, rl);
-                    const int64_t off = sr >= 0 ? ((int64_t)sr * Hkv + (kvh < 0 ? 0 : kvh)) * D + ch * 8 : 0;
-                    cp_async16(kd + swz<D>(rl, ch), kp + off, sr >= 0);
-                    cp_async16(vd + swz<D>(rl, ch), vp + off, sr >= 0);
-                }
-                cp_async_arrive_noinc(full[c] + 8 * st);
-            }
-            __syncwarp();   // every lane has read entry r before it is refilled
-            look_up(c);     // step r + kQD
-            cp_async_commit();
+    for (int r = 0;; ++r) {
+        // the lookup of step r was committed kQD groups ago
+        cp_async_wait<kQD - 1>();
+        __syncwarp();
+        const int ent = r & (kSQ - 1);
+        const uint32_t eb = sring + ent * kSlotEntry;
+        const int kvh = ld_shared_s32(eb + 64);
+        const int st = r % kNS;
+        if (!timed_out && !mbar_wait_sleep(empty + 8 * st, ((r / kNS) & 1) ^ 1)) {
+            atomicOr(err, 4u);
+            timed_out = true;
         }
+        if (kvh >= 0) {
+            int32_t sl = lane < kNP ? ld_shared_s32(eb + lane * 4) : kPastEnd;
+            if (sl == kPastEnd) {
+                sl = -1;
+            } else if (sl < 0 || sl >= num_slots) {
+                atomicOr(err, 1u);
+                sl = -1;
+            }
+            const uint32_t kd = ring + st * Lay::STAGE, vd = kd + Lay::TILEB;
+            const int ch = lane % CPR;
+#pragma unroll
+            for (int k = 0; k < kNP / RPI; ++k) {
+                const int rl = k * RPI + lane / CPR;
+                const int32_t sr = __shfl_sync(0xffffffffu, sl, rl);
+                const int64_t off = sr >= 0 ? ((int64_t)sr * Hkv + kvh) * D + ch * 8 : 0;
+                cp_async16(kd + swz<D>(rl, ch), kp + off, sr >= 0);
+                cp_async16(vd + swz<D>(rl, ch), vp + off, sr >= 0);
+            }
+        }
+        if (lane == 0) {
+            const uint32_t db = desc + st * 16;
+            st_shared_s32(db, ld_shared_s32(eb + 72));                  // first position
+            st_shared_s32(db + 4, ld_shared_s32(eb + 68));              // piece
+            st_shared_s32(db + 8, kvh >= 0 ? ld_shared_s32(eb + 76) : kEnd);
+        }
+        cp_async_arrive_noinc(full + 8 * st);    // each lane, when its copies have landed
+        __syncwarp();
+        if (lane == 0) mbar_arrive(full + 8 * st);   // releases the descriptor
+        if (kvh < 0) break;
+        __syncwarp();   // every lane has read entry r before it is refilled
+        look_up();      // step r + kQD
+        cp_async_commit();
     }
     cp_async_wait<0>();
+    // The last producer to finish restores the counter for the next call
+    // (every producer has taken its last number by then).
+    if (lane == 0) {
+        const uint32_t total = gridDim.x * (uint32_t)kProducers;
+        if (atomicAdd(sched + 1, 1u) + 1 == total) {
+            sched[0] = (uint32_t)f.n_init;
+            sched[1] = 0u;
+            __threadfence();
+        }
+    }
 }
 
 // ---------------------------------------------------------------------------
 // Consumer
 // ---------------------------------------------------------------------------
 template <int D>
-__device__ __noinline__ void stream_consumer(const FusedArgs& f, int it0, int n_it, uint32_t ring, uint32_t full,
-                                             uint32_t empty, int lane) {
+__device__ __noinline__ void stream_consumer(const FusedArgs& f, uint32_t ring, uint32_t desc, uint32_t ann,
+                                             uint32_t full, uint32_t empty, int lane) {
     using Lay = FusedLayout<D>;
     constexpr int MT = D / 16;                 // m-tiles of O^T
     const int g = lane >> 2, t = lane & 3;
@@ -256,62 +307,48 @@ __device__ __noinline__ void stream_consumer(const FusedArgs& f, int it0, int n_
     uint32_t* const err = f.t.err;
     const int Hq = f.t.Hq, G = f.t.G;
     const float sc = f.t.scale_log2;
+    const DecItem* const pieces = f.narrow;
 
-    // it.e is the planned end (steps are counted on it), f_ec the end clamped
-    // to the row's seq_len (masks); the clamp does not hold up anything else
-    ItemFields it;
-    it.load(f.t.items, it0, n_it, lane);
-    const int total = total_steps(it, n_it, lane);
-    int f_ec = it.e;
-    if (lane < n_it) {
-        const int len = __ldg(seq_lens + it.row);
-        if (it.e > len) {
-            atomicOr(err, 2u);
-            f_ec = len > it.b ? len : it.b;
-        }
-    }
-
-    // query rows: the next item's member index is loaded one step before its
-    // query words, so neither load stalls the warp
-    uint32_t qcur[D / 8], qnext[D / 8];
-    int mnext = 0, m_item = -1, q_item = -1;
-    auto q_member = [&](int k) {   // phase 1: member request of row g of item k
-        if (k < n_it) {
-            const int rows = fld(it.nm, k) * G, mb = fld(it.mb, k);
-            mnext = g < rows ? __ldg(members + mb + g / G) : -1;
-            m_item = k;
-        }
-    };
-    auto q_words = [&]() {         // phase 2: its query words into qnext
-        if (m_item < 0) return;
-        const int kvh = fld(it.h, m_item);
-        const bool ok = mnext >= 0;
-        const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-            qp + ((int64_t)(ok ? mnext : 0) * Hq + kvh * G + g % G) * D);
+    // Prefetch of a piece's record, seq_len clamp, member and query words, one
+    // phase per step (1 record in flight, 2 member and seq_len in flight,
+    // 3 query words in flight), started when the producer announces it.
+    int pf_id = -1, pf_stage = 0;
+    int pf_b = 0, pf_e = 0, pf_h = 0, pf_mb = 0, pf_nm = 0, pf_pb = 0, pf_row = 0, pf_mem = 0, pf_len = 0;
+    uint32_t qnext[D / 8];
+    auto pf_step = [&]() {
+        if (pf_stage == 1) {
+            const int4* rp = reinterpret_cast<const int4*>(pieces + pf_id);
+            const int4 x = __ldg(rp), y = __ldg(rp + 1);
+            pf_row = x.x;
+            pf_b = x.y;
+            pf_e = x.z;
+            pf_h = x.w;
+            pf_mb = y.x;
+            pf_nm = y.y;
+            pf_pb = y.z;
+            pf_stage = 2;
+        } else if (pf_stage == 2) {
+            pf_len = __ldg(seq_lens + pf_row);
+            pf_mem = g < pf_nm * G ? __ldg(members + pf_mb + g / G) : -1;
+            pf_stage = 3;
+        } else if (pf_stage == 3) {
+            const bool ok = pf_mem >= 0;
+            const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+                qp + ((int64_t)(ok ? pf_mem : 0) * Hq + pf_h * G + g % G) * D);
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-            qnext[2 * ks] = ok ? __ldg(qrow + 8 * ks + t) : 0u;
-            qnext[2 * ks + 1] = ok ? __ldg(qrow + 8 * ks + 4 + t) : 0u;
+            for (int ks = 0; ks < D / 16; ++ks) {
+                qnext[2 * ks] = ok ? __ldg(qrow + 8 * ks + t) : 0u;
+                qnext[2 * ks + 1] = ok ? __ldg(qrow + 8 * ks + 4 + t) : 0u;
+            }
+            pf_stage = 4;
         }
-        q_item = m_item;
-        m_item = -1;
     };
-    q_member(0);
 
+    uint32_t qcur[D / 8];
     float o[MT][4];
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    auto start_item = [&](int k) {
-#pragma unroll
-        for (int i = 0; i < MT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-        m0 = m1 = -INFINITY;
-        l0 = l1 = 0.f;
-        if (q_item != k) q_words();   // item k's member index is in flight (short previous item)
-#pragma unroll
-        for (int w = 0; w < D / 8; ++w) qcur[w] = qnext[w];
-        q_member(k + 1);
-    };
-    auto finish_item = [&](int k) {
-        const int rows = fld(it.nm, k) * G, pb = fld(it.pb, k);
+    int cur_id = -1, cur_pb = 0, cur_rows = 0, cm = 0;
+    auto finish_item = [&]() {
         float s0 = l0, s1 = l1;
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
@@ -319,39 +356,60 @@ __device__ __noinline__ void stream_consumer(const FusedArgs& f, int it0, int n_
             s1 += __shfl_xor_sync(0xffffffffu, s1, off);
         }
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int r = 2 * t + h;
-            if (r < rows) {
-                const float ll = h ? s1 : s0, mm = h ? m1 : m0;
+        for (int hh = 0; hh < 2; ++hh) {
+            const int r = 2 * t + hh;
+            if (r < cur_rows) {
+                const float ll = hh ? s1 : s0, mm = hh ? m1 : m0;
                 const float inv = ll > 0.f ? 1.f / ll : 0.f;
-                float* dst = po + ((int64_t)pb + r) * D + g;
+                float* dst = po + ((int64_t)cur_pb + r) * D + g;
 #pragma unroll
                 for (int i = 0; i < MT; ++i) {
-                    dst[16 * i] = o[i][h] * inv;
-                    dst[16 * i + 8] = o[i][2 + h] * inv;
+                    dst[16 * i] = o[i][hh] * inv;
+                    dst[16 * i + 8] = o[i][2 + hh] * inv;
                 }
-                if (g == 0) plse[(int64_t)pb + r] = ll > 0.f ? (mm + log2f(ll)) * kLn2 : -INFINITY;
+                if (g == 0) plse[(int64_t)cur_pb + r] = ll > 0.f ? (mm + log2f(ll)) * kLn2 : -INFINITY;
             }
         }
     };
+    auto start_item = [&](int id) {
+        if (pf_id != id) {
+            pf_id = id;
+            pf_stage = 1;
+        }
+        while (pf_stage < 4) pf_step();   // normally done during the previous piece
+#pragma unroll
+        for (int w = 0; w < D / 8; ++w) qcur[w] = qnext[w];
+        cur_id = id;
+        cur_pb = pf_pb;
+        cur_rows = pf_nm * G;
+        cm = pf_e;
+        if (pf_e > pf_len) {   // planned beyond seq_len: mask the excess, flag it
+            if (lane == 0) atomicOr(err, 2u);
+            cm = pf_len > pf_b ? pf_len : pf_b;
+        }
+        pf_id = -1;
+        pf_stage = 0;
+#pragma unroll
+        for (int i = 0; i < MT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+        m0 = m1 = -INFINITY;
+        l0 = l1 = 0.f;
+    };
 
-    int ci = 0;
-    start_item(0);
-    while (ci < n_it && fld(it.e, ci) <= fld(it.b, ci)) {   // leading empty items
-        finish_item(ci);
-        ++ci;
-        if (ci < n_it) start_item(ci);
-    }
-    int cp0 = ci < n_it ? fld(it.b, ci) : 0;
-    int ce = ci < n_it ? fld(it.e, ci) : 0, cm = ci < n_it ? fld(f_ec, ci) : 0;
     bool timed_out = false;
-    for (int c = 0; c < total; ++c) {
+    for (int c = 0;; ++c) {
         const int st = c % kNS;
         if (!timed_out && !mbar_wait_sleep(full + 8 * st, (c / kNS) & 1)) {
             atomicOr(err, 4u);
             timed_out = true;
         }
-        // ---- one step of item ci at positions cp0 .. cp0+15
+        const uint32_t db = desc + st * 16;
+        const int cp0 = ld_shared_s32(db), id = ld_shared_s32(db + 4), flags = ld_shared_s32(db + 8);
+        if ((flags & kEnd) || timed_out) break;
+        if (flags & kFirst) {
+            if (cur_id >= 0) finish_item();
+            start_item(id);
+        }
+        // ---- one step of the current piece at positions cp0 .. cp0+15
         const uint32_t kb = ring + st * Lay::STAGE, vb = kb + Lay::TILEB;
         // two accumulators halve the dependent MMA chain
         float s[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
@@ -410,24 +468,17 @@ __device__ __noinline__ void stream_consumer(const FusedArgs& f, int it0, int n_
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(empty + 8 * st);   // the stage may be refilled
-        if (m_item >= 0) q_words();   // one step after the member index was requested
-        cp0 += kNP;
-        if (cp0 >= ce) {
-            finish_item(ci);
-            ++ci;
-            while (ci < n_it) {
-                start_item(ci);
-                if (fld(it.e, ci) > fld(it.b, ci)) break;
-                finish_item(ci);   // empty item: LSE -inf partial
-                ++ci;
-            }
-            if (ci < n_it) {
-                cp0 = fld(it.b, ci);
-                ce = fld(it.e, ci);
-                cm = fld(f_ec, ci);
+        // the next piece's query rows: start when the producer announces it
+        if (pf_stage == 0) {
+            const int a_id = ld_volatile_shared_s32(ann);
+            if (a_id > cur_id) {
+                pf_id = a_id;
+                pf_stage = 1;
             }
         }
+        if (pf_stage > 0 && pf_stage < 4) pf_step();
     }
+    if (cur_id >= 0) finish_item();
 }
 
 // ---------------------------------------------------------------------------
@@ -466,11 +517,13 @@ __global__ void __maxnreg__(128) decode_fused_kernel(const __grid_constant__ Fus
     auto empty_of = [&](int c) { return sbar + (uint32_t)(c * 2 * kNS + kNS) * 8; };
     if (tid == 0) {
         if (tiles) tc_init_barriers<D, true>(smem_u32(sm + TL::OFF_BAR));
-        for (int c = 0; c < kConsumers; ++c)
+        for (int c = 0; c < kConsumers; ++c) {
             for (int s = 0; s < kNS; ++s) {
-                mbar_init(full_of(c) + 8 * s, 32);    // the producer's 32 lanes
+                mbar_init(full_of(c) + 8 * s, 33);    // the producer's 32 lanes + its descriptor release
                 mbar_init(empty_of(c) + 8 * s, 1);    // the consumer
             }
+            st_shared_s32(smem_u32(sm + Lay::OFF_ANN + 16 * c), -1);
+        }
         mbar_fence_init();
     }
     if (tiles && warp == 4) {
@@ -494,29 +547,14 @@ __global__ void __maxnreg__(128) decode_fused_kernel(const __grid_constant__ Fus
             }
         }
     } else if (warp < kFirstConsumer) {
-        constexpr int NCP = kConsumers / kProducers;
-        const int p = warp - kFirstProducer;
-        int it0[NCP], n_it[NCP];
-        uint32_t ring[NCP], sring[NCP], full[NCP], empty[NCP];
-        bool any = false;
-#pragma unroll
-        for (int k = 0; k < NCP; ++k) {
-            const int c = NCP * p + k, gw = blockIdx.x * kConsumers + c;
-            it0[k] = __ldg(f.nptr + gw);
-            n_it[k] = __ldg(f.nptr + gw + 1) - it0[k];
-            ring[k] = smem_u32(sm + Lay::OFF_RING + c * Lay::RING);
-            sring[k] = smem_u32(sm + Lay::OFF_SLOT + c * Lay::SLOTW);
-            full[k] = full_of(c);
-            empty[k] = empty_of(c);
-            any |= n_it[k] > 0;
-        }
-        if (any) stream_producer<D, NCP>(f, it0, n_it, ring, sring, full, empty, lane);
+        const int c = warp - kFirstProducer;
+        stream_producer<D>(f, blockIdx.x * kConsumers + c, smem_u32(sm + Lay::OFF_RING + c * Lay::RING),
+                           smem_u32(sm + Lay::OFF_SLOT + c * Lay::SLOTW), smem_u32(sm + Lay::OFF_DESC + c * kNS * 16),
+                           smem_u32(sm + Lay::OFF_ANN + 16 * c), full_of(c), empty_of(c), lane);
     } else {
-        const int c = warp - kFirstConsumer, gw = blockIdx.x * kConsumers + c;
-        const int it0 = __ldg(f.nptr + gw), n_it = __ldg(f.nptr + gw + 1) - it0;
-        if (n_it > 0)
-            stream_consumer<D>(f, it0, n_it, smem_u32(sm + Lay::OFF_RING + c * Lay::RING), full_of(c), empty_of(c),
-                               lane);
+        const int c = warp - kFirstConsumer;
+        stream_consumer<D>(f, smem_u32(sm + Lay::OFF_RING + c * Lay::RING), smem_u32(sm + Lay::OFF_DESC + c * kNS * 16),
+                           smem_u32(sm + Lay::OFF_ANN + 16 * c), full_of(c), empty_of(c), lane);
     }
     tc_fence_before();
     __syncthreads();
@@ -556,14 +594,17 @@ int launch_decode_fused(const sgl_plan* plan, const void* q, const void* kp, con
     a.num_slots = p.num_slots;
     a.scale_log2 = scale_log2;
     f.wptr = reinterpret_cast<const int32_t*>(ws + plan->off_wptr);
-    f.nptr = reinterpret_cast<const int32_t*>(ws + plan->off_nptr);
+    f.narrow = a.items + plan->n_wide;
+    f.n_narrow = plan->n_narrow;
+    f.n_init = plan->n_init;
+    f.sched = reinterpret_cast<uint32_t*>(ws + plan->off_sched);
     decode_fused_kernel<D><<<plan->n_ctas, kFusedThreads, Lay::TOTAL, s>>>(f);
     int e = (int)cudaGetLastError();
     if (e) return e;
     MergeArgs m{a.po, a.plse, reinterpret_cast<const int32_t*>(ws + plan->off_mptr),
                 reinterpret_cast<const int32_t*>(ws + plan->off_ment), o, lse, a.Hq, a.Hkv, a.G};
     const int n_pairs = p.batch * a.Hkv;
-    decode_merge_kernel<bf16, D><<<(n_pairs + 3) / 4, 128, 0, s>>>(m, n_pairs);
+    decode_merge_kernel<bf16, D><<<(n_pairs * a.G + 3) / 4, 128, 0, s>>>(m, n_pairs);
     return (int)cudaGetLastError();
 }
 

@@ -1,4 +1,4 @@
-// Log-sum-exp merge of decode partials, one warp per (request, KV head).
+// Log-sum-exp merge of decode partials, one warp per (request, query head).
 //
 // Every decode work item writes, for each of its query rows, the softmax-
 // normalised partial O over its KV chunk and that chunk's LSE (natural log).
@@ -7,10 +7,10 @@
 //   O = sum_e w_e O_e / sum_e w_e,   LSE = M + log(sum_e w_e),
 // which equals attention over the concatenated chunks ("SGLang 深度拆解"
 // (chenxutan.com/d/5669.html) §3.2 PagedDecode, split along the KV
-// sequence).  Every lane accumulates D/32 columns of each head; the entries
-// are taken in batches whose LSEs and rows are all in flight together, with
-// the running maximum rescaling earlier batches (online form of the same
-// sum), so a merge costs about two dependent loads plus one per batch.
+// sequence).  Every lane accumulates D/32 columns of one query head; the
+// entries are taken in batches whose LSEs and rows are all in flight
+// together, with the running maximum rescaling earlier batches (online form
+// of the same sum).
 // Partials are read with ld.global.cg: they were written by other SMs during
 // the same kernel (L1 is not coherent).
 #pragma once
@@ -32,124 +32,98 @@ struct MergeArgs {
     int Hq, Hkv, G;
 };
 
-template <typename OutT, int D, int G>
-__device__ __noinline__ void merge_warp_g(const MergeArgs& m, int idx, int e0, int E, int lane) {
+// Head j of pair idx = (request, KV head), whose entries are
+// ment[e0 .. e0+E): entry e's row for head j is ment[e0 + e] + j.
+template <typename OutT, int D>
+__device__ __noinline__ void merge_head(const MergeArgs& m, int idx, int j, int e0, int E, int lane) {
     constexpr int VPL = D / 32;             // columns per lane
-    constexpr int U = 24 / G;               // entries whose loads are in flight together
+    constexpr int U = 16;                   // entries whose rows are in flight together
     const int r = idx / m.Hkv, h = idx - r * m.Hkv;
-    float M[G], L[G], acc[G][VPL];
+    float M = -INFINITY, L = 0.f, acc[VPL];
 #pragma unroll
-    for (int j = 0; j < G; ++j) {
-        M[j] = -INFINITY;
-        L[j] = 0.f;
-#pragma unroll
-        for (int v = 0; v < VPL; ++v) acc[j][v] = 0.f;
-    }
-    // Online over batches of U entries: a batch's LSEs and rows are loaded
-    // together; the running maxima rescale what was accumulated before.
+    for (int v = 0; v < VPL; ++v) acc[v] = 0.f;
     for (int b = 0; b < E; b += 32) {
         const int n = min(32, E - b);
-        const int pb = lane < n ? __ldg(m.ment + e0 + b + lane) : 0;
+        const int prow = lane < n ? __ldg(m.ment + e0 + b + lane) + j : 0;
+        const float ls = lane < n ? __ldcg(m.plse + prow) : -INFINITY;
         for (int k = 0; k < n; k += U) {
-            float x[U][G][VPL], ls[U][G];
+            float x[U][VPL], lu[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const bool ok = k + u < n;
-                const int pk = __shfl_sync(0xffffffffu, pb, ok ? k + u : 0);
-#pragma unroll
-                for (int j = 0; j < G; ++j) {
-                    ls[u][j] = ok ? __ldcg(m.plse + pk + j) : -INFINITY;
-                    const float* src = m.po + ((int64_t)pk + j) * D + lane * VPL;
-                    if constexpr (VPL == 4) {
-                        const float4 t = ok ? __ldcg(reinterpret_cast<const float4*>(src)) : make_float4(0.f, 0.f, 0.f, 0.f);
-                        x[u][j][0] = t.x;
-                        x[u][j][1] = t.y;
-                        x[u][j][2] = t.z;
-                        x[u][j][3] = t.w;
-                    } else {
-                        const float2 t = ok ? __ldcg(reinterpret_cast<const float2*>(src)) : make_float2(0.f, 0.f);
-                        x[u][j][0] = t.x;
-                        x[u][j][1] = t.y;
-                    }
+                const int pk = __shfl_sync(0xffffffffu, prow, ok ? k + u : 0);
+                lu[u] = __shfl_sync(0xffffffffu, ls, ok ? k + u : 0);
+                if (!ok) lu[u] = -INFINITY;
+                const float* src = m.po + (int64_t)pk * D + lane * VPL;
+                if constexpr (VPL == 4) {
+                    const float4 t4 = ok ? __ldcg(reinterpret_cast<const float4*>(src)) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    x[u][0] = t4.x;
+                    x[u][1] = t4.y;
+                    x[u][2] = t4.z;
+                    x[u][3] = t4.w;
+                } else {
+                    const float2 t2 = ok ? __ldcg(reinterpret_cast<const float2*>(src)) : make_float2(0.f, 0.f);
+                    x[u][0] = t2.x;
+                    x[u][1] = t2.y;
                 }
             }
+            // online form: the running maximum rescales earlier batches
+            float mx = M;
 #pragma unroll
-            for (int j = 0; j < G; ++j) {
-                float mx = M[j];
+            for (int u = 0; u < U; ++u) mx = fmaxf(mx, lu[u]);
+            if (mx == -INFINITY) continue;
+            const float sc = exp2f((M - mx) * kLog2e);   // 0 while nothing was accumulated
+            L *= sc;
 #pragma unroll
-                for (int u = 0; u < U; ++u) mx = fmaxf(mx, ls[u][j]);
-                if (mx == -INFINITY) continue;
-                const float sc = exp2f((M[j] - mx) * kLog2e);   // 0 while nothing was accumulated
-                L[j] *= sc;
+            for (int v = 0; v < VPL; ++v) acc[v] *= sc;
 #pragma unroll
-                for (int v = 0; v < VPL; ++v) acc[j][v] *= sc;
+            for (int u = 0; u < U; ++u) {
+                const float w = exp2f((lu[u] - mx) * kLog2e);
+                L += w;
 #pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const float w = exp2f((ls[u][j] - mx) * kLog2e);
-                    L[j] += w;
-#pragma unroll
-                    for (int v = 0; v < VPL; ++v) acc[j][v] = fmaf(w, x[u][j][v], acc[j][v]);
-                }
-                M[j] = mx;
+                for (int v = 0; v < VPL; ++v) acc[v] = fmaf(w, x[u][v], acc[v]);
             }
+            M = mx;
         }
     }
-#pragma unroll
-    for (int j = 0; j < G; ++j) {
-        const float inv = L[j] > 0.f ? 1.f / L[j] : 0.f;
-        const int64_t orow = (int64_t)r * m.Hq + h * G + j;
-        OutT* dst = static_cast<OutT*>(m.o) + orow * D + lane * VPL;
-        if constexpr (sizeof(OutT) == 2) {
-            if constexpr (VPL == 4) {
-                uint2 pk;
-                pk.x = pack_bf16(acc[j][0] * inv, acc[j][1] * inv);
-                pk.y = pack_bf16(acc[j][2] * inv, acc[j][3] * inv);
-                *reinterpret_cast<uint2*>(dst) = pk;
-            } else {
-                *reinterpret_cast<uint32_t*>(dst) = pack_bf16(acc[j][0] * inv, acc[j][1] * inv);
-            }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    const int64_t orow = (int64_t)r * m.Hq + h * m.G + j;
+    OutT* dst = static_cast<OutT*>(m.o) + orow * D + lane * VPL;
+    if constexpr (sizeof(OutT) == 2) {
+        if constexpr (VPL == 4) {
+            uint2 pk;
+            pk.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+            pk.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+            *reinterpret_cast<uint2*>(dst) = pk;
         } else {
-#pragma unroll
-            for (int v = 0; v < VPL; ++v) dst[v] = acc[j][v] * inv;
+            *reinterpret_cast<uint32_t*>(dst) = pack_bf16(acc[0] * inv, acc[1] * inv);
         }
-        if (lane == 0) m.lse[orow] = L[j] > 0.f ? M[j] + logf(L[j]) : -INFINITY;
+    } else {
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) dst[v] = acc[v] * inv;
     }
+    if (lane == 0) m.lse[orow] = L > 0.f ? M + logf(L) : -INFINITY;
 }
 
-// Merge pair idx = (request, KV head) whose entries are ment[e0 .. e0+E).
+// One warp per (request, KV head, query head of the group): the log-sum-exp
+// merge of its entries, or O = 0 / LSE = -inf when the pair has no entries
+// (seq_len 0).  A warp's loads are one round trip for the entry range, one
+// for the entry rows, then the partial rows and LSEs together.
 template <typename OutT, int D>
-__device__ __forceinline__ void merge_warp(const MergeArgs& m, int idx, int e0, int E, int lane) {
-    switch (m.G) {
-        case 1: merge_warp_g<OutT, D, 1>(m, idx, e0, E, lane); break;
-        case 2: merge_warp_g<OutT, D, 2>(m, idx, e0, E, lane); break;
-        case 4: merge_warp_g<OutT, D, 4>(m, idx, e0, E, lane); break;
-        default: merge_warp_g<OutT, D, 8>(m, idx, e0, E, lane); break;
-    }
-}
-
-// (request, KV head) pairs without any partial (seq_len 0): O = 0, LSE = -inf.
-template <typename OutT, int D>
-__device__ __forceinline__ void merge_empty(const MergeArgs& m, int idx, int lane) {
-    const int r = idx / m.Hkv, h = idx - r * m.Hkv;
-    for (int j = 0; j < m.G; ++j) {
+__global__ void __launch_bounds__(128) decode_merge_kernel(const MergeArgs m, int n_pairs) {
+    const int w = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    const int idx = w / m.G, j = w - idx * m.G;
+    if (idx >= n_pairs) return;
+    const int e0 = __ldg(m.mptr + idx), E = __ldg(m.mptr + idx + 1) - e0;
+    if (E == 0) {
+        const int r = idx / m.Hkv, h = idx - r * m.Hkv;
         const int64_t orow = (int64_t)r * m.Hq + h * m.G + j;
         OutT* dst = static_cast<OutT*>(m.o) + orow * D;
         for (int c = lane; c < D; c += 32) dst[c] = OutT(0.f);
         if (lane == 0) m.lse[orow] = -INFINITY;
+        return;
     }
-}
-
-// One warp per (request, KV head) pair: the log-sum-exp merge of its
-// entries, or O = 0 / LSE = -inf for a pair without entries (seq_len 0).
-template <typename OutT, int D>
-__global__ void __launch_bounds__(128) decode_merge_kernel(const MergeArgs m, int n_pairs) {
-    const int idx = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-    if (idx >= n_pairs) return;
-    const int e0 = __ldg(m.mptr + idx), E = __ldg(m.mptr + idx + 1) - e0;
-    if (E == 0)
-        merge_empty<OutT, D>(m, idx, lane);
-    else
-        merge_warp<OutT, D>(m, idx, e0, E, lane);
+    merge_head<OutT, D>(m, idx, j, e0, E, lane);
 }
 
 }  // namespace sgl

@@ -12,8 +12,8 @@
 //     member blocks of up to 128 rows x chunks of whole 128-position
 //     multiples (~1 tile of work per SM), dealt round-robin to the CTAs;
 //   * every other segment (at most 8 rows: a request's own suffix, or a
-//     small group) is narrow: its positions, per KV head, are cut into equal
-//     shares, one per streaming warp, so all warps stream the same bytes;
+//     small group) is narrow: its positions, per KV head, are cut into
+//     pieces handed to the streaming warps at run time, longest first;
 //   * each item writes its rows' normalised partial O and LSE (fp32); the
 //     merge list of (request, KV head) names every partial row to combine.
 // The fp32 path runs the same items one CTA each.
@@ -147,80 +147,44 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
         }
     }
 
-    // Narrow units are cut into equal shares of positions, one share per
-    // streaming warp (n_ctas CTAs x kDecNarrowWarps warps), so every warp
-    // streams about the same number of bytes; a cut makes two items (two
-    // partials).  Pieces shorter than one 16-position step are avoided; the
-    // member rows of a warp's items (sum of n_mem, >= its item count) are at
-    // most kDecMaxItemsPerWarp: one lane per item and per deferred merge.
-    constexpr int NW = sgl::kDecNarrowWarps;
-    // Streaming warps that share their SM with tile roles stream slower
-    // (measured ~0.62x on the Llama-3-8B-shaped batch); they get
-    // proportionally smaller shares.
-    constexpr double kTileCtaShare = 0.62;
-    int64_t n_ctas = sms;
-    std::vector<std::vector<sgl::DecItem>> warp_items;
-    for (int attempt = 0;; ++attempt) {
-        const int64_t nwt = n_ctas * NW;
-        const int64_t n_tile_ctas = std::min<int64_t>((int64_t)wide.size(), n_ctas);   // round-robin below
-        const double weight = (double)NW * ((double)(n_ctas - n_tile_ctas) + kTileCtaShare * (double)n_tile_ctas);
-        int64_t T = std::max<int64_t>(16, (int64_t)std::ceil((double)units_n / weight));
-        bool ok = false;
-        for (int tries = 0; tries < 64 && !ok; ++tries, T += 16) {
-            auto cap_of = [&](int64_t w) {
-                const bool tile_cta = w / NW < n_tile_ctas;
-                const int64_t c = tile_cta ? (int64_t)std::ceil(kTileCtaShare * (double)T) : T;
-                return std::max<int64_t>(16, (c + 15) / 16 * 16);
-            };
-            warp_items.assign((size_t)nwt, {});
-            int64_t w = 0, cap = cap_of(0), mem_rows = 0;
-            bool fail = false;
-            for (const Unit& u : units) {
-                int64_t pos = u.b;
-                while (pos < u.e && !fail) {
-                    if (cap < 16 || mem_rows + u.n_mem > sgl::kDecMaxItemsPerWarp) {
-                        if (++w >= nwt) {
-                            fail = true;
-                            break;
-                        }
-                        cap = cap_of(w);
-                        mem_rows = 0;
-                    }
-                    int64_t take = std::min<int64_t>(u.e - pos, cap);
-                    if (u.e - pos - take < 16) take = u.e - pos;   // no tail piece under one step
-                    warp_items[w].push_back({u.rep_row, (int32_t)pos, (int32_t)(pos + take), u.kvh, u.mem_begin,
-                                             u.n_mem, 0, 0});
-                    pos += take;
-                    cap -= take;
-                    mem_rows += u.n_mem;
-                }
-                if (fail) break;
-            }
-            ok = !fail;
+    // Narrow units are cut into pieces of at most Pmax positions (about two
+    // pieces per streaming consumer; a cut makes one more partial to merge),
+    // no piece shorter than one 16-position step unless its unit is, ordered
+    // longest first.  Consumer w starts on piece w; the rest are handed out
+    // at run time from a counter, so SMs that stream faster take more.
+    const int64_t n_ctas = sms;
+    const int64_t n_cons = n_ctas * sgl::kDecNarrowWarps;
+    int64_t Pmax = (int64_t)std::ceil((double)units_n / (2.0 * (double)n_cons));
+    Pmax = std::min<int64_t>(1024, std::max<int64_t>(64, (Pmax + 15) / 16 * 16));
+    std::vector<sgl::DecItem> narrow;
+    for (const Unit& u : units) {
+        for (int64_t pos = u.b; pos < u.e;) {
+            int64_t take = std::min<int64_t>(u.e - pos, Pmax);
+            if (u.e - pos - take < 16) take = u.e - pos;   // no tail piece under one step
+            narrow.push_back({u.rep_row, (int32_t)pos, (int32_t)(pos + take), u.kvh, u.mem_begin, u.n_mem, 0, 0});
+            pos += take;
         }
-        if (ok) break;
-        if (n_ctas > (int64_t)1 << 20) return SGL_ERR_UNSUPPORTED;
-        n_ctas *= 2;   // too many items per warp: more warps
     }
+    std::stable_sort(narrow.begin(), narrow.end(), [](const sgl::DecItem& x, const sgl::DecItem& y) {
+        return (x.kv_end - x.kv_begin) > (y.kv_end - y.kv_begin);
+    });
+    const int64_t n_init = std::min<int64_t>((int64_t)narrow.size(), n_cons);
+
     // wide items round-robin over the CTAs
     std::vector<std::vector<sgl::DecItem>> cta_items((size_t)n_ctas);
     for (size_t i = 0; i < wide.size(); ++i) cta_items[i % (size_t)n_ctas].push_back(wide[i]);
 
-    // final item order: wide items by CTA, then narrow items by warp;
-    // partial rows in item order
+    // final item order: wide items by CTA, then the narrow pieces; partial
+    // rows in item order
     std::vector<sgl::DecItem> items;
-    std::vector<int32_t> wptr, nptr;
+    std::vector<int32_t> wptr;
     wptr.push_back(0);
     for (auto& v : cta_items) {
         items.insert(items.end(), v.begin(), v.end());
         wptr.push_back((int32_t)items.size());
     }
     const int32_t n_wide = (int32_t)items.size();
-    nptr.push_back(n_wide);
-    for (auto& v : warp_items) {
-        items.insert(items.end(), v.begin(), v.end());
-        nptr.push_back((int32_t)items.size());
-    }
+    items.insert(items.end(), narrow.begin(), narrow.end());
     std::vector<std::vector<int32_t>> ents((size_t)B * Hkv);
     int64_t prow = 0;
     for (auto& it : items) {
@@ -243,6 +207,8 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
     plan->n_wide = n_wide;
     plan->n_partial_rows = (int32_t)prow;
     plan->n_ctas = (int32_t)n_ctas;
+    plan->n_narrow = (int32_t)narrow.size();
+    plan->n_init = (int32_t)n_init;
     plan->n_members = g->num_members;
     int64_t n_ent = 0;
     int32_t max_ent = 0;
@@ -261,8 +227,8 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
     plan->off_items = A;
     plan->off_members = align_up(plan->off_items + items.size() * sizeof(sgl::DecItem), A);
     plan->off_wptr = align_up(plan->off_members + (size_t)g->num_members * 4, A);
-    plan->off_nptr = align_up(plan->off_wptr + wptr.size() * 4, A);
-    plan->off_mptr = align_up(plan->off_nptr + nptr.size() * 4, A);
+    plan->off_sched = align_up(plan->off_wptr + wptr.size() * 4, A);
+    plan->off_mptr = align_up(plan->off_sched + 2 * 4, A);
     plan->off_ment = align_up(plan->off_mptr + ((size_t)B * Hkv + 1) * 4, A);
     plan->tables_bytes = align_up(plan->off_ment + (size_t)n_ent * 4, A);
     plan->off_plse = plan->tables_bytes;
@@ -281,7 +247,9 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
     if (!items.empty()) std::memcpy(plan->blob + plan->off_items, items.data(), items.size() * sizeof(sgl::DecItem));
     if (g->num_members) std::memcpy(plan->blob + plan->off_members, g->seg_members, (size_t)g->num_members * 4);
     std::memcpy(plan->blob + plan->off_wptr, wptr.data(), wptr.size() * 4);
-    std::memcpy(plan->blob + plan->off_nptr, nptr.data(), nptr.size() * 4);
+    // run-time piece counter: next piece to hand out, producers finished
+    const uint32_t sched[2] = {(uint32_t)n_init, 0u};
+    std::memcpy(plan->blob + plan->off_sched, sched, sizeof(sched));
     int32_t* mptr = reinterpret_cast<int32_t*>(plan->blob + plan->off_mptr);
     int32_t* ment = reinterpret_cast<int32_t*>(plan->blob + plan->off_ment);
     int64_t at = 0;

@@ -401,21 +401,21 @@ __device__ __forceinline__ void tc_tile_run(const TcArgs& a, const TileInfo& ti,
             tld32_nw(tl + b * 64, srow);
             tld32_nw(tl + b * 64 + 32, srow + 32);
             tld_wait();
+            // max on the raw scores (the scale is positive), scaled once; the
+            // scale is folded into the exponent's FMA below
             float mx = -INFINITY;
             if (full_blk) {
 #pragma unroll
-                for (int k = 0; k < kBN; ++k) {
-                    srow[k] *= sc;
-                    mx = fmaxf(mx, srow[k]);
-                }
+                for (int k = 0; k < kBN; ++k) mx = fmaxf(mx, srow[k]);
             } else {
 #pragma unroll
                 for (int k = 0; k < kBN; ++k) {
                     const int pos = pos0 + k;
-                    srow[k] = (pos < kv_end && pos <= lim) ? srow[k] * sc : -INFINITY;
+                    srow[k] = (pos < kv_end && pos <= lim) ? srow[k] : -INFINITY;
                     mx = fmaxf(mx, srow[k]);
                 }
             }
+            mx *= sc;
             const float m_new = fmaxf(m_used, mx);
             const bool need = m_new > m_used + 8.f;   // also true for the first finite max
             const float m_old = m_used;
@@ -423,12 +423,12 @@ __device__ __forceinline__ void tc_tile_run(const TcArgs& a, const TileInfo& ti,
                 if (m_used != -INFINITY) l *= exp2f(m_used - m_new);
                 m_used = m_new;
             }
-            const float mu = m_used == -INFINITY ? 0.f : m_used;
+            const float nmu = m_used == -INFINITY ? 0.f : -m_used;
             uint32_t pk[kBN / 2];
 #pragma unroll
             for (int k = 0; k < kBN; k += 2) {
-                const float p0 = exp2f(srow[k] - mu);      // -inf -> 0
-                const float p1 = exp2f(srow[k + 1] - mu);
+                const float p0 = exp2f(fmaf(srow[k], sc, nmu));      // -inf -> 0
+                const float p1 = exp2f(fmaf(srow[k + 1], sc, nmu));
                 l += p0 + p1;
                 pk[k / 2] = pack_bf16(p0, p1);
             }

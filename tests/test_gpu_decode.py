@@ -174,3 +174,51 @@ def test_decode_rescale_path_with_growing_scores():
         _check(case)
     finally:
         case.close()
+
+
+@pytest.mark.parametrize("num_sms", [0, 3])
+def test_decode_repeated_calls_share_one_upload(num_sms):
+    """Calls after one plan upload give identical results: the kernel hands
+    narrow pieces out from a run-time counter and restores it at the end of
+    every call, so the tenth call without a new upload sees what the first
+    saw.  Also captures three calls in a CUDA graph and replays it."""
+    case = Case("fork_tree_small")
+    try:
+        kd, vd = case.device_pool()
+        p = case.params(num_sms=num_sms)
+        plan = sgl.sgl_decode_plan(p, case.out["seq_lens"], sgl.sgl_groups_view(case.groups))
+        ws = torch.zeros(max(plan.workspace_bytes, 256), dtype=torch.uint8, device="cuda")
+        sgl.sgl_plan_upload(plan, ws)
+        qd = case.q_host().cuda()
+        table = torch.from_numpy(case.out["req_to_token"]).cuda()
+        seq = torch.from_numpy(case.out["seq_lens"]).cuda()
+        o = torch.empty_like(qd)
+        lse = torch.empty(case.B, case.w.Hq, dtype=torch.float32, device="cuda")
+        sgl.sgl_decode_attn(qd, kd, vd, table, seq, plan, o, lse, ws)
+        sgl.sgl_check(ws)
+        o0, l0 = o.clone(), lse.clone()
+        for _ in range(9):
+            o.zero_()
+            sgl.sgl_decode_attn(qd, kd, vd, table, seq, plan, o, lse, ws)
+        sgl.sgl_check(ws)
+        assert torch.equal(o, o0) and torch.equal(lse, l0)
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                for _ in range(3):
+                    sgl.sgl_decode_attn(qd, kd, vd, table, seq, plan, o, lse, ws)
+        torch.cuda.current_stream().wait_stream(s)
+        for _ in range(4):
+            o.zero_()
+            g.replay()
+        torch.cuda.synchronize()
+        sgl.sgl_check(ws)
+        assert torch.equal(o, o0) and torch.equal(lse, l0)
+        Oref, Lref = decode_attention(case.oracle_q(), W.RowView(case.K), W.RowView(case.V), case.oracle_table,
+                                      case.out["seq_lens"])
+        assert_close(o.double().cpu().numpy(), lse.cpu().numpy().astype(np.float64), Oref, Lref,
+                     *tolerances(case.w))
+    finally:
+        case.close()
