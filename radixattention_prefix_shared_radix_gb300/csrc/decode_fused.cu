@@ -42,9 +42,10 @@
 //   O^T [d x 8 rows]     += V^T [d x 16 pos] . P^T [16 pos x 8 rows]
 // K and V rows are XOR-swizzled [16 x d] tiles (ldmatrix for K,
 // ldmatrix.trans for V^T, conflict-free); P^T moves from the accumulator
-// layout to the B-operand layout with movmatrix.  The next piece's query rows
-// are fetched while the current piece runs (the producer announces the piece
-// in shared memory as soon as it starts looking it up).
+// layout to the B-operand layout with movmatrix.  A piece's query rows are
+// staged by the producer with the piece's first step (two Q slots, released
+// by the consumer through a QEMPTY barrier), so the consumer's loop touches
+// nothing but shared memory.
 //
 // Every item writes normalised partial rows (O fp32, LSE natural log); the
 // merge launch (merge.cuh) combines each (request, KV head)'s partials once
@@ -66,7 +67,7 @@ constexpr int kNS = 4;                                   // ring stages per cons
 constexpr int kNP = 16;                                  // KV positions per step
 constexpr int kQD = 6;                                   // slot lookups ahead (steps per consumer)
 constexpr int kSQ = 8;                                   // slot ring entries per consumer
-constexpr int kSlotEntry = kNP * 4 + 16;                 // 16 slots + KV head, piece, position, flags
+constexpr int kSlotEntry = 128;                         // 16 slots + step and piece fields (see below)
 constexpr int kFirstProducer = kTileThreads / 32;
 constexpr int kFirstConsumer = kFirstProducer + kProducers;
 constexpr int kFusedThreads = 32 * (kFirstConsumer + kConsumers);
@@ -81,10 +82,11 @@ struct FusedLayout {
     static constexpr int SLOTW = kSQ * kSlotEntry;       // slot ring per consumer
     static constexpr int OFF_RING = (TL::END + 127) / 128 * 128;
     static constexpr int OFF_SLOT = OFF_RING + kConsumers * RING;
-    static constexpr int OFF_DESC = OFF_SLOT + kConsumers * SLOTW;   // kNS stage descriptors (16 B) per consumer
-    static constexpr int OFF_ANN = OFF_DESC + kConsumers * kNS * 16; // announced piece per consumer
-    static constexpr int OFF_SBAR = OFF_ANN + kConsumers * 16;       // FULL[kNS], EMPTY[kNS] per consumer
-    static constexpr int END = OFF_SBAR + kConsumers * 2 * kNS * 8;
+    static constexpr int QSLOT = 8 * D * 2;              // query rows of one piece (at most 8)
+    static constexpr int OFF_DESC = OFF_SLOT + kConsumers * SLOTW;   // kNS stage descriptors (32 B) per consumer
+    static constexpr int OFF_Q = (OFF_DESC + kConsumers * kNS * 32 + 127) / 128 * 128;   // 2 Q slots per consumer
+    static constexpr int OFF_SBAR = OFF_Q + kConsumers * 2 * QSLOT;  // FULL[kNS], EMPTY[kNS], QEMPTY[2] per consumer
+    static constexpr int END = OFF_SBAR + kConsumers * (2 * kNS + 2) * 8;
     static constexpr int TOTAL = END + 1024;             // + alignment slack
     static_assert(TOTAL <= 232448, "shared memory per CTA");
 };
@@ -111,24 +113,34 @@ __device__ __forceinline__ int ld_volatile_shared_s32(uint32_t addr) {
 }
 
 // stage descriptor flags
-constexpr int kFirst = 1;   // first step of its piece
+constexpr int kFirst = 1;   // first step of its piece: its query rows are in the stage's Q slot
 constexpr int kEnd = 4;     // no more pieces: the consumer stops
+
+// slot-ring entry (one looked-up step): 16 slots, then
+constexpr int kEntKvh = 64, kEntId = 68, kEntP0 = 72, kEntFlags = 76, kEntCm = 80, kEntPb = 84, kEntRows = 88;
+constexpr int kEntMem = 96;   // 8 ints: member request of each query row (first step only)
+// stage descriptor
+constexpr int kDescP0 = 0, kDescFlags = 4, kDescCm = 8, kDescPb = 12, kDescRows = 16, kDescQ = 20;
 
 // ---------------------------------------------------------------------------
 // Producer
 // ---------------------------------------------------------------------------
 // Walks this consumer's pieces (its launch piece, then pieces taken from the
 // run-time counter), looks up each step's slots kQD steps ahead (4-byte
-// cp.async into the slot ring, with the step's KV head, piece, position and
-// flags beside them), and for each step waits for the ring stage to be free,
-// issues the K/V row copies, writes the stage descriptor and arrives on the
-// stage's FULL barrier (32 lanes when their copies land + lane 0 releasing the
-// descriptor).  The next piece is fetched in phases spread over the steps
-// (take a number from the counter; load its record), so no register waits on
-// a load in flight.
+// cp.async into the slot ring, with the step's KV head, position and flags,
+// and for a first step the piece's partial base, rows, clamped end and the
+// member request of each query row), and for each step waits for the ring
+// stage to be free, issues the K/V row copies (and, for a first step, the
+// piece's query rows into one of two Q slots once the consumer has released
+// it), writes the stage descriptor and arrives on the stage's FULL barrier
+// (32 lanes when their copies land + lane 0 releasing the descriptor).  The
+// next piece is fetched in phases spread over the steps (take a number from
+// the counter; load its record; load its members and seq_len), so no register
+// waits on a load in flight.
 template <int D>
 __device__ __noinline__ void stream_producer(const FusedArgs& f, int gw, uint32_t ring, uint32_t sring,
-                                             uint32_t desc, uint32_t ann, uint32_t full, uint32_t empty, int lane) {
+                                             uint32_t desc, uint32_t qbuf, uint32_t full, uint32_t empty,
+                                             uint32_t qempty, int lane) {
     using Lay = FusedLayout<D>;
     constexpr int CPR = D / 8;                 // 16-byte chunks per row
     constexpr int RPI = 32 / CPR;              // rows per warp instruction
@@ -136,26 +148,35 @@ __device__ __noinline__ void stream_producer(const FusedArgs& f, int gw, uint32_
     // argument fields in registers: every cp.async below clobbers memory
     const bf16* const kp = f.t.kp;
     const bf16* const vp = f.t.vp;
+    const bf16* const qp = f.t.q;
     const int32_t* const r2t = f.t.r2t;
+    const int32_t* const members = f.t.members;
+    const int32_t* const seq_lens = f.t.seq_lens;
     const int64_t ld = f.t.ld;
     uint32_t* const err = f.t.err;
-    const int Hkv = f.t.Hkv;
+    const int Hq = f.t.Hq, Hkv = f.t.Hkv, G = f.t.G;
     const int64_t num_slots = f.t.num_slots;
     const DecItem* const pieces = f.narrow;
     const int n_narrow = f.n_narrow;
     uint32_t* const sched = f.sched;
 
     // next-piece pipeline: 0 take a number, 1 number in flight (lane 0),
-    // 2 record in flight, 3 ready; `none` once the counter ran out
-    int nx_id = 0, nx_stage = 0, nx_row = 0, nx_b = 0, nx_e = 0, nx_h = 0, taken = 0;
+    // 2 record in flight, 3 members / seq_len in flight, 4 ready;
+    // `none` once the counter ran out
+    int nx_id = 0, nx_stage = 0, taken = 0;
+    int nx_row = 0, nx_b = 0, nx_e = 0, nx_h = 0, nx_mb = 0, nx_nm = 0, nx_pb = 0, nx_mem = 0, nx_len = 0;
     bool none = false;
     auto load_record = [&]() {
         if (nx_id < n_narrow) {
-            const int4 x = __ldg(reinterpret_cast<const int4*>(pieces + nx_id));
+            const int4* rp = reinterpret_cast<const int4*>(pieces + nx_id);
+            const int4 x = __ldg(rp), y = __ldg(rp + 1);
             nx_row = x.x;
             nx_b = x.y;
             nx_e = x.z;
             nx_h = x.w;
+            nx_mb = y.x;
+            nx_nm = y.y;
+            nx_pb = y.z;
         } else {
             none = true;
         }
@@ -163,7 +184,11 @@ __device__ __noinline__ void stream_producer(const FusedArgs& f, int gw, uint32_
     if (gw < f.n_init) {
         nx_id = gw;
         load_record();
-        nx_stage = 2;
+        nx_stage = 3;
+        if (!none) {   // launch piece: wait for its record here, once
+            nx_len = __ldg(seq_lens + nx_row);
+            nx_mem = lane < nx_nm * G ? __ldg(members + nx_mb + lane / G) : 0;
+        }
     }
     auto advance = [&]() {
         if (none) return;
@@ -175,37 +200,50 @@ __device__ __noinline__ void stream_producer(const FusedArgs& f, int gw, uint32_
             load_record();
             nx_stage = 2;
         } else if (nx_stage == 2) {
+            nx_len = __ldg(seq_lens + nx_row);
+            nx_mem = lane < nx_nm * G ? __ldg(members + nx_mb + lane / G) : 0;
             nx_stage = 3;
+        } else if (nx_stage == 3) {
+            nx_stage = 4;
         }
     };
+    if (gw < f.n_init) nx_stage = 4;
 
     // slot cursor over the current piece
     bool have = false, done = false;
-    int cur_id = 0, row = 0, e = 0, h = 0, sp = 0, nlook = 0;
+    int row = 0, e = 0, h = 0, sp = 0, nlook = 0;
     auto look_up = [&]() {
         const int ent = nlook & (kSQ - 1);
         const uint32_t eb = sring + ent * kSlotEntry;
-        int kvh = -1, id = 0, p0 = 0, flags = 0;
+        int kvh = -1, p0 = 0, flags = 0;
         if (!done && (!have || sp >= e)) {
-            while (!none && nx_stage < 3) advance();
+            while (!none && nx_stage < 4) advance();
             if (none) {
                 have = false;
                 done = true;
             } else {
                 have = true;
-                cur_id = nx_id;
                 row = nx_row;
                 sp = nx_b;
                 e = nx_e;
                 h = nx_h;
                 flags = kFirst;
+                int cm = nx_e;
+                if (nx_e > nx_len) {   // planned beyond seq_len: mask the excess, flag it
+                    if (lane == 0) atomicOr(err, 2u);
+                    cm = nx_len > nx_b ? nx_len : nx_b;
+                }
+                if (lane == 0) {
+                    st_shared_s32(eb + kEntCm, cm);
+                    st_shared_s32(eb + kEntPb, nx_pb);
+                    st_shared_s32(eb + kEntRows, nx_nm * G);
+                }
+                if (lane < 8) st_shared_s32(eb + kEntMem + 4 * lane, nx_mem);
                 nx_stage = 0;
-                if (lane == 0) st_shared_s32(ann, cur_id);   // lets the consumer fetch its query rows early
             }
         }
         if (have && !done) {
             kvh = h;
-            id = cur_id;
             p0 = sp;
             const int p = sp + lane;
             if (lane < kNP) {
@@ -217,10 +255,9 @@ __device__ __noinline__ void stream_producer(const FusedArgs& f, int gw, uint32_
             sp += kNP;
         }
         if (lane == 0) {
-            st_shared_s32(eb + 64, kvh);
-            st_shared_s32(eb + 68, id);
-            st_shared_s32(eb + 72, p0);
-            st_shared_s32(eb + 76, flags);
+            st_shared_s32(eb + kEntKvh, kvh);
+            st_shared_s32(eb + kEntP0, p0);
+            st_shared_s32(eb + kEntFlags, flags);
         }
         ++nlook;
         advance();
@@ -232,18 +269,21 @@ __device__ __noinline__ void stream_producer(const FusedArgs& f, int gw, uint32_
     __syncwarp();
 
     bool timed_out = false;
+    int nq = 0;   // pieces started (Q slot uses)
     for (int r = 0;; ++r) {
         // the lookup of step r was committed kQD groups ago
         cp_async_wait<kQD - 1>();
         __syncwarp();
         const int ent = r & (kSQ - 1);
         const uint32_t eb = sring + ent * kSlotEntry;
-        const int kvh = ld_shared_s32(eb + 64);
+        const int kvh = ld_shared_s32(eb + kEntKvh);
+        const int flags = ld_shared_s32(eb + kEntFlags);
         const int st = r % kNS;
         if (!timed_out && !mbar_wait_sleep(empty + 8 * st, ((r / kNS) & 1) ^ 1)) {
             atomicOr(err, 4u);
             timed_out = true;
         }
+        const uint32_t db = desc + st * 32;
         if (kvh >= 0) {
             int32_t sl = lane < kNP ? ld_shared_s32(eb + lane * 4) : kPastEnd;
             if (sl == kPastEnd) {
@@ -262,12 +302,35 @@ __device__ __noinline__ void stream_producer(const FusedArgs& f, int gw, uint32_
                 cp_async16(kd + swz<D>(rl, ch), kp + off, sr >= 0);
                 cp_async16(vd + swz<D>(rl, ch), vp + off, sr >= 0);
             }
+            if (flags & kFirst) {
+                // the piece's query rows (at most 8) into Q slot nq & 1, swizzled
+                const int qs = nq & 1;
+                if (!timed_out && !mbar_wait_sleep(qempty + 8 * qs, ((nq >> 1) & 1) ^ 1)) {
+                    atomicOr(err, 4u);
+                    timed_out = true;
+                }
+                const int rows = ld_shared_s32(eb + kEntRows);
+                const uint32_t qd = qbuf + qs * Lay::QSLOT;
+#pragma unroll
+                for (int k = 0; k < 8 / RPI; ++k) {
+                    const int rq = k * RPI + lane / CPR;
+                    const bool ok = rq < rows;
+                    const int mem = ld_shared_s32(eb + kEntMem + 4 * rq);
+                    const bf16* src = ok ? qp + ((int64_t)mem * Hq + kvh * G + rq % G) * D + ch * 8 : qp;
+                    cp_async16(qd + swz<D>(rq, ch), src, ok);
+                }
+                if (lane == 0) {
+                    st_shared_s32(db + kDescCm, ld_shared_s32(eb + kEntCm));
+                    st_shared_s32(db + kDescPb, ld_shared_s32(eb + kEntPb));
+                    st_shared_s32(db + kDescRows, rows);
+                    st_shared_s32(db + kDescQ, qs);
+                }
+                ++nq;
+            }
         }
         if (lane == 0) {
-            const uint32_t db = desc + st * 16;
-            st_shared_s32(db, ld_shared_s32(eb + 72));                  // first position
-            st_shared_s32(db + 4, ld_shared_s32(eb + 68));              // piece
-            st_shared_s32(db + 8, kvh >= 0 ? ld_shared_s32(eb + 76) : kEnd);
+            st_shared_s32(db + kDescP0, ld_shared_s32(eb + kEntP0));
+            st_shared_s32(db + kDescFlags, kvh >= 0 ? flags : kEnd);
         }
         cp_async_arrive_noinc(full + 8 * st);    // each lane, when its copies have landed
         __syncwarp();
@@ -291,63 +354,24 @@ __device__ __noinline__ void stream_producer(const FusedArgs& f, int gw, uint32_
 }
 
 // ---------------------------------------------------------------------------
-// Consumer
+// Consumer: only shared memory in its loop (stages, descriptors, Q slots)
 // ---------------------------------------------------------------------------
 template <int D>
-__device__ __noinline__ void stream_consumer(const FusedArgs& f, uint32_t ring, uint32_t desc, uint32_t ann,
-                                             uint32_t full, uint32_t empty, int lane) {
+__device__ __noinline__ void stream_consumer(const FusedArgs& f, uint32_t ring, uint32_t desc, uint32_t qbuf,
+                                             uint32_t full, uint32_t empty, uint32_t qempty, int lane) {
     using Lay = FusedLayout<D>;
     constexpr int MT = D / 16;                 // m-tiles of O^T
     const int g = lane >> 2, t = lane & 3;
-    const bf16* const qp = f.t.q;
-    const int32_t* const members = f.t.members;
-    const int32_t* const seq_lens = f.t.seq_lens;
     float* const po = f.t.po;
     float* const plse = f.t.plse;
     uint32_t* const err = f.t.err;
-    const int Hq = f.t.Hq, G = f.t.G;
     const float sc = f.t.scale_log2;
-    const DecItem* const pieces = f.narrow;
-
-    // Prefetch of a piece's record, seq_len clamp, member and query words, one
-    // phase per step (1 record in flight, 2 member and seq_len in flight,
-    // 3 query words in flight), started when the producer announces it.
-    int pf_id = -1, pf_stage = 0;
-    int pf_b = 0, pf_e = 0, pf_h = 0, pf_mb = 0, pf_nm = 0, pf_pb = 0, pf_row = 0, pf_mem = 0, pf_len = 0;
-    uint32_t qnext[D / 8];
-    auto pf_step = [&]() {
-        if (pf_stage == 1) {
-            const int4* rp = reinterpret_cast<const int4*>(pieces + pf_id);
-            const int4 x = __ldg(rp), y = __ldg(rp + 1);
-            pf_row = x.x;
-            pf_b = x.y;
-            pf_e = x.z;
-            pf_h = x.w;
-            pf_mb = y.x;
-            pf_nm = y.y;
-            pf_pb = y.z;
-            pf_stage = 2;
-        } else if (pf_stage == 2) {
-            pf_len = __ldg(seq_lens + pf_row);
-            pf_mem = g < pf_nm * G ? __ldg(members + pf_mb + g / G) : -1;
-            pf_stage = 3;
-        } else if (pf_stage == 3) {
-            const bool ok = pf_mem >= 0;
-            const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-                qp + ((int64_t)(ok ? pf_mem : 0) * Hq + pf_h * G + g % G) * D);
-#pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-                qnext[2 * ks] = ok ? __ldg(qrow + 8 * ks + t) : 0u;
-                qnext[2 * ks + 1] = ok ? __ldg(qrow + 8 * ks + 4 + t) : 0u;
-            }
-            pf_stage = 4;
-        }
-    };
 
     uint32_t qcur[D / 8];
     float o[MT][4];
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    int cur_id = -1, cur_pb = 0, cur_rows = 0, cm = 0;
+    bool have = false;
+    int cur_pb = 0, cur_rows = 0, cm = 0;
     auto finish_item = [&]() {
         float s0 = l0, s1 = l1;
 #pragma unroll
@@ -371,43 +395,40 @@ __device__ __noinline__ void stream_consumer(const FusedArgs& f, uint32_t ring, 
             }
         }
     };
-    auto start_item = [&](int id) {
-        if (pf_id != id) {
-            pf_id = id;
-            pf_stage = 1;
-        }
-        while (pf_stage < 4) pf_step();   // normally done during the previous piece
-#pragma unroll
-        for (int w = 0; w < D / 8; ++w) qcur[w] = qnext[w];
-        cur_id = id;
-        cur_pb = pf_pb;
-        cur_rows = pf_nm * G;
-        cm = pf_e;
-        if (pf_e > pf_len) {   // planned beyond seq_len: mask the excess, flag it
-            if (lane == 0) atomicOr(err, 2u);
-            cm = pf_len > pf_b ? pf_len : pf_b;
-        }
-        pf_id = -1;
-        pf_stage = 0;
-#pragma unroll
-        for (int i = 0; i < MT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-        m0 = m1 = -INFINITY;
-        l0 = l1 = 0.f;
-    };
 
     bool timed_out = false;
+    int nq = 0;
     for (int c = 0;; ++c) {
         const int st = c % kNS;
         if (!timed_out && !mbar_wait_sleep(full + 8 * st, (c / kNS) & 1)) {
             atomicOr(err, 4u);
             timed_out = true;
         }
-        const uint32_t db = desc + st * 16;
-        const int cp0 = ld_shared_s32(db), id = ld_shared_s32(db + 4), flags = ld_shared_s32(db + 8);
+        const uint32_t db = desc + st * 32;
+        const int cp0 = ld_shared_s32(db + kDescP0), flags = ld_shared_s32(db + kDescFlags);
         if ((flags & kEnd) || timed_out) break;
         if (flags & kFirst) {
-            if (cur_id >= 0) finish_item();
-            start_item(id);
+            if (have) finish_item();
+            have = true;
+            cm = ld_shared_s32(db + kDescCm);
+            cur_pb = ld_shared_s32(db + kDescPb);
+            cur_rows = ld_shared_s32(db + kDescRows);
+            const int qs = ld_shared_s32(db + kDescQ);
+            // Q^T fragments: row g (the N index), k-step ks -> chunks 2ks, 2ks+1
+            const uint32_t qb = qbuf + qs * Lay::QSLOT;
+#pragma unroll
+            for (int kp2 = 0; kp2 < D / 32; ++kp2) {
+                const int rq = lane & 7, chunk = 4 * kp2 + (lane >> 3);
+                ldsm_x4(qb + swz<D>(rq, chunk), qcur[4 * kp2], qcur[4 * kp2 + 1], qcur[4 * kp2 + 2],
+                        qcur[4 * kp2 + 3]);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(qempty + 8 * qs);   // the Q slot may be refilled
+            ++nq;
+#pragma unroll
+            for (int i = 0; i < MT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+            m0 = m1 = -INFINITY;
+            l0 = l1 = 0.f;
         }
         // ---- one step of the current piece at positions cp0 .. cp0+15
         const uint32_t kb = ring + st * Lay::STAGE, vb = kb + Lay::TILEB;
@@ -468,17 +489,8 @@ __device__ __noinline__ void stream_consumer(const FusedArgs& f, uint32_t ring, 
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(empty + 8 * st);   // the stage may be refilled
-        // the next piece's query rows: start when the producer announces it
-        if (pf_stage == 0) {
-            const int a_id = ld_volatile_shared_s32(ann);
-            if (a_id > cur_id) {
-                pf_id = a_id;
-                pf_stage = 1;
-            }
-        }
-        if (pf_stage > 0 && pf_stage < 4) pf_step();
     }
-    if (cur_id >= 0) finish_item();
+    if (have) finish_item();
 }
 
 // ---------------------------------------------------------------------------
@@ -513,8 +525,9 @@ __global__ void __maxnreg__(128) decode_fused_kernel(const __grid_constant__ Fus
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + TL::OFF_TMEM);
     int* info = reinterpret_cast<int*>(sm + TL::OFF_INFO);
     const uint32_t sbar = smem_u32(sm + Lay::OFF_SBAR);
-    auto full_of = [&](int c) { return sbar + (uint32_t)(c * 2 * kNS) * 8; };
-    auto empty_of = [&](int c) { return sbar + (uint32_t)(c * 2 * kNS + kNS) * 8; };
+    auto full_of = [&](int c) { return sbar + (uint32_t)(c * (2 * kNS + 2)) * 8; };
+    auto empty_of = [&](int c) { return sbar + (uint32_t)(c * (2 * kNS + 2) + kNS) * 8; };
+    auto qempty_of = [&](int c) { return sbar + (uint32_t)(c * (2 * kNS + 2) + 2 * kNS) * 8; };
     if (tid == 0) {
         if (tiles) tc_init_barriers<D, true>(smem_u32(sm + TL::OFF_BAR));
         for (int c = 0; c < kConsumers; ++c) {
@@ -522,7 +535,8 @@ __global__ void __maxnreg__(128) decode_fused_kernel(const __grid_constant__ Fus
                 mbar_init(full_of(c) + 8 * s, 33);    // the producer's 32 lanes + its descriptor release
                 mbar_init(empty_of(c) + 8 * s, 1);    // the consumer
             }
-            st_shared_s32(smem_u32(sm + Lay::OFF_ANN + 16 * c), -1);
+            mbar_init(qempty_of(c), 1);
+            mbar_init(qempty_of(c) + 8, 1);
         }
         mbar_fence_init();
     }
@@ -549,12 +563,12 @@ __global__ void __maxnreg__(128) decode_fused_kernel(const __grid_constant__ Fus
     } else if (warp < kFirstConsumer) {
         const int c = warp - kFirstProducer;
         stream_producer<D>(f, blockIdx.x * kConsumers + c, smem_u32(sm + Lay::OFF_RING + c * Lay::RING),
-                           smem_u32(sm + Lay::OFF_SLOT + c * Lay::SLOTW), smem_u32(sm + Lay::OFF_DESC + c * kNS * 16),
-                           smem_u32(sm + Lay::OFF_ANN + 16 * c), full_of(c), empty_of(c), lane);
+                           smem_u32(sm + Lay::OFF_SLOT + c * Lay::SLOTW), smem_u32(sm + Lay::OFF_DESC + c * kNS * 32),
+                           smem_u32(sm + Lay::OFF_Q + c * 2 * Lay::QSLOT), full_of(c), empty_of(c), qempty_of(c), lane);
     } else {
         const int c = warp - kFirstConsumer;
-        stream_consumer<D>(f, smem_u32(sm + Lay::OFF_RING + c * Lay::RING), smem_u32(sm + Lay::OFF_DESC + c * kNS * 16),
-                           smem_u32(sm + Lay::OFF_ANN + 16 * c), full_of(c), empty_of(c), lane);
+        stream_consumer<D>(f, smem_u32(sm + Lay::OFF_RING + c * Lay::RING), smem_u32(sm + Lay::OFF_DESC + c * kNS * 32),
+                           smem_u32(sm + Lay::OFF_Q + c * 2 * Lay::QSLOT), full_of(c), empty_of(c), qempty_of(c), lane);
     }
     tc_fence_before();
     __syncthreads();
