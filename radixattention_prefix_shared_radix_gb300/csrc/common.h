@@ -55,7 +55,8 @@ struct sgl_plan {
     int32_t n_partial_rows;
     int32_t n_ctas;              // fused decode kernel: CTAs (wide items wptr[c]..wptr[c+1])
     int32_t n_narrow;            // narrow pieces (items n_wide .. n_items-1, longest first)
-    int32_t n_init;              // pieces assigned at launch (consumer w starts on piece w)
+    int32_t n_init;              // pieces assigned at launch (streaming consumer w starts on piece w)
+    int32_t n_tile_ctas;         // CTAs 0 .. n_tile_ctas-1 run the wide items, then stream
     int32_t n_members;
     int32_t n_merge_entries;
     int32_t max_entries_per_request;

@@ -19,15 +19,20 @@
 //               small group) on the tensor cores: its launch piece, then
 //               pieces its producer takes from a run-time counter, so faster
 //               SMs stream more and all finish together.
-// The tiles are bound by latency and the tensor pipe, the streams by HBM; the
-// two run side by side on every SM.  Producers and consumers are separate
+// The tiles are bound by latency and the tensor pipe, the streams by HBM.
+// The planner puts the wide items on the first CTAs (as many as balance the
+// streaming work); their streaming warps wait at a barrier until the tiles are
+// done and then take pieces from the run-time counter, so an SM never runs
+// both kinds at once (measured: co-running them cost the streams most of
+// their instruction-cache hits).  Producers and consumers are separate
 // warps so the copies keep flowing while the consumers compute, and there is
 // one producer per consumer: measured on GB300, a warp issuing random
 // 256-byte-row cp.async gathers gets one instruction through every ~80-100
 // cycles once the SM's load pipe is busy, so the SM's issue rate (and HBM
 // bandwidth) grows with the number of issuing warps.
 //
-// Streaming ring per consumer: 4 stages of 16 positions (K and V rows, 8 KB)
+// Streaming ring per consumer: 4 stages of 16 positions (K and V rows, 8 KB;
+// 6 stages in CTAs without tiles, which use the tile roles' shared memory)
 // with a descriptor each (first position, piece, flags), a FULL mbarrier per
 // stage (each producer lane arrives when its copies have landed:
 // cp.async.mbarrier.arrive.noinc, and lane 0 once more to release the
@@ -63,30 +68,35 @@ using namespace tc;
 
 constexpr int kConsumers = kDecNarrowWarps;              // streaming consumer warps per CTA
 constexpr int kProducers = kConsumers;                   // one per consumer
-constexpr int kNS = 4;                                   // ring stages per consumer
+constexpr int kNS = 4;                                   // ring stages per consumer (tile CTA)
+constexpr int kNSF = 4;                                  // ring stages per consumer (streaming CTA)
 constexpr int kNP = 16;                                  // KV positions per step
 constexpr int kQD = 6;                                   // slot lookups ahead (steps per consumer)
 constexpr int kSQ = 8;                                   // slot ring entries per consumer
 constexpr int kSlotEntry = 128;                         // 16 slots + step and piece fields (see below)
+constexpr int kGrabAhead = 4;                            // take the next piece this many steps before the end
 constexpr int kFirstProducer = kTileThreads / 32;
 constexpr int kFirstConsumer = kFirstProducer + kProducers;
 constexpr int kFusedThreads = 32 * (kFirstConsumer + kConsumers);
-static_assert(kSQ >= kQD && (kSQ & (kSQ - 1)) == 0, "slot ring");
+static_assert(kSQ >= kQD && (kSQ & (kSQ - 1)) == 0 && kQD >= kNSF - 1, "slot ring");
 
 template <int D>
 struct FusedLayout {
     using TL = TcLayout<D, true>;
     static constexpr int TILEB = kNP * D * 2;            // one K (or V) tile of a step
     static constexpr int STAGE = 2 * TILEB;
-    static constexpr int RING = kNS * STAGE;             // per consumer
+    static constexpr int RING = kNS * STAGE;             // per consumer, beside the tile roles
+    static constexpr int RING_F = kNSF * STAGE;          // per consumer, CTA without tiles (from offset 0)
     static constexpr int SLOTW = kSQ * kSlotEntry;       // slot ring per consumer
     static constexpr int OFF_RING = (TL::END + 127) / 128 * 128;
-    static constexpr int OFF_SLOT = OFF_RING + kConsumers * RING;
+    static constexpr int END_RINGS = (OFF_RING + kConsumers * RING) > kConsumers * RING_F
+                                         ? (OFF_RING + kConsumers * RING) : kConsumers * RING_F;
+    static constexpr int OFF_SLOT = END_RINGS;
     static constexpr int QSLOT = 8 * D * 2;              // query rows of one piece (at most 8)
-    static constexpr int OFF_DESC = OFF_SLOT + kConsumers * SLOTW;   // kNS stage descriptors (32 B) per consumer
-    static constexpr int OFF_Q = (OFF_DESC + kConsumers * kNS * 32 + 127) / 128 * 128;   // 2 Q slots per consumer
-    static constexpr int OFF_SBAR = OFF_Q + kConsumers * 2 * QSLOT;  // FULL[kNS], EMPTY[kNS], QEMPTY[2] per consumer
-    static constexpr int END = OFF_SBAR + kConsumers * (2 * kNS + 2) * 8;
+    static constexpr int OFF_DESC = OFF_SLOT + kConsumers * SLOTW;   // kNSF stage descriptors (32 B) per consumer
+    static constexpr int OFF_Q = (OFF_DESC + kConsumers * kNSF * 32 + 127) / 128 * 128;   // 2 Q slots per consumer
+    static constexpr int OFF_SBAR = OFF_Q + kConsumers * 2 * QSLOT;  // FULL[kNSF], EMPTY[kNSF], QEMPTY[2] per consumer
+    static constexpr int END = OFF_SBAR + kConsumers * (2 * kNSF + 2) * 8;
     static constexpr int TOTAL = END + 1024;             // + alignment slack
     static_assert(TOTAL <= 232448, "shared memory per CTA");
 };
@@ -96,7 +106,8 @@ struct FusedArgs {
     const int32_t* wptr;   // [n_ctas + 1] wide items of each CTA
     const DecItem* narrow; // narrow pieces, longest first
     int n_narrow;
-    int n_init;            // pieces assigned at launch: consumer w starts on piece w
+    int n_init;            // pieces assigned at launch: streaming consumer w starts on piece w
+    int n_tile_ctas;       // CTAs 0 .. n_tile_ctas-1 run the wide items first
     uint32_t* sched;       // [2] next piece to hand out, producers finished (restored at the end)
 };
 
@@ -137,7 +148,7 @@ constexpr int kDescP0 = 0, kDescFlags = 4, kDescCm = 8, kDescPb = 12, kDescRows 
 // next piece is fetched in phases spread over the steps (take a number from
 // the counter; load its record; load its members and seq_len), so no register
 // waits on a load in flight.
-template <int D>
+template <int D, int NS>
 __device__ __noinline__ void stream_producer(const FusedArgs& f, int gw, uint32_t ring, uint32_t sring,
                                              uint32_t desc, uint32_t qbuf, uint32_t full, uint32_t empty,
                                              uint32_t qempty, int lane) {
@@ -181,14 +192,20 @@ __device__ __noinline__ void stream_producer(const FusedArgs& f, int gw, uint32_
             none = true;
         }
     };
-    if (gw < f.n_init) {
+    // the launch piece: its record is waited for once; its seq_len and
+    // members are loaded now and used only when its first step is issued
+    const bool launch = gw >= 0 && gw < f.n_init;
+    int lp_len = 0, lp_mem = 0, lp_b = 0, lp_e = 0, lp_pb = 0, lp_rows = 0;
+    if (launch) {
         nx_id = gw;
         load_record();
         nx_stage = 3;
-        if (!none) {   // launch piece: wait for its record here, once
-            nx_len = __ldg(seq_lens + nx_row);
-            nx_mem = lane < nx_nm * G ? __ldg(members + nx_mb + lane / G) : 0;
-        }
+        lp_len = __ldg(seq_lens + nx_row);
+        lp_mem = lane < nx_nm * G ? __ldg(members + nx_mb + lane / G) : 0;
+        lp_b = nx_b;
+        lp_e = nx_e;
+        lp_pb = nx_pb;
+        lp_rows = nx_nm * G;
     }
     auto advance = [&]() {
         if (none) return;
@@ -207,7 +224,8 @@ __device__ __noinline__ void stream_producer(const FusedArgs& f, int gw, uint32_
             nx_stage = 4;
         }
     };
-    if (gw < f.n_init) nx_stage = 4;
+    if (launch) nx_stage = 4;
+    bool launch_entry_pending = launch;
 
     // slot cursor over the current piece
     bool have = false, done = false;
@@ -228,17 +246,21 @@ __device__ __noinline__ void stream_producer(const FusedArgs& f, int gw, uint32_
                 e = nx_e;
                 h = nx_h;
                 flags = kFirst;
-                int cm = nx_e;
-                if (nx_e > nx_len) {   // planned beyond seq_len: mask the excess, flag it
-                    if (lane == 0) atomicOr(err, 2u);
-                    cm = nx_len > nx_b ? nx_len : nx_b;
+                if (launch_entry_pending) {
+                    launch_entry_pending = false;   // fields come from lp_* when step 0 is issued
+                } else {
+                    int cm = nx_e;
+                    if (nx_e > nx_len) {   // planned beyond seq_len: mask the excess, flag it
+                        if (lane == 0) atomicOr(err, 2u);
+                        cm = nx_len > nx_b ? nx_len : nx_b;
+                    }
+                    if (lane == 0) {
+                        st_shared_s32(eb + kEntCm, cm);
+                        st_shared_s32(eb + kEntPb, nx_pb);
+                        st_shared_s32(eb + kEntRows, nx_nm * G);
+                    }
+                    if (lane < 8) st_shared_s32(eb + kEntMem + 4 * lane, nx_mem);
                 }
-                if (lane == 0) {
-                    st_shared_s32(eb + kEntCm, cm);
-                    st_shared_s32(eb + kEntPb, nx_pb);
-                    st_shared_s32(eb + kEntRows, nx_nm * G);
-                }
-                if (lane < 8) st_shared_s32(eb + kEntMem + 4 * lane, nx_mem);
                 nx_stage = 0;
             }
         }
@@ -260,7 +282,10 @@ __device__ __noinline__ void stream_producer(const FusedArgs& f, int gw, uint32_
             st_shared_s32(eb + kEntFlags, flags);
         }
         ++nlook;
-        advance();
+        // Take the next number only near the end of the current piece: the
+        // counter then runs dry only when the work does, and CTAs that join
+        // late (tile CTAs) still find pieces.
+        if (nx_stage != 0 || !have || done || (e - sp + kNP - 1) / kNP <= kGrabAhead) advance();
     };
 #pragma unroll 1
     for (int k = 0; k < kQD; ++k) look_up();
@@ -278,8 +303,8 @@ __device__ __noinline__ void stream_producer(const FusedArgs& f, int gw, uint32_
         const uint32_t eb = sring + ent * kSlotEntry;
         const int kvh = ld_shared_s32(eb + kEntKvh);
         const int flags = ld_shared_s32(eb + kEntFlags);
-        const int st = r % kNS;
-        if (!timed_out && !mbar_wait_sleep(empty + 8 * st, ((r / kNS) & 1) ^ 1)) {
+        const int st = r % NS;
+        if (!timed_out && !mbar_wait_sleep(empty + 8 * st, ((r / NS) & 1) ^ 1)) {
             atomicOr(err, 4u);
             timed_out = true;
         }
@@ -309,19 +334,34 @@ __device__ __noinline__ void stream_producer(const FusedArgs& f, int gw, uint32_
                     atomicOr(err, 4u);
                     timed_out = true;
                 }
-                const int rows = ld_shared_s32(eb + kEntRows);
+                const bool lp = launch && r == 0;   // the launch piece's first step
+                int cm, pb, rows;
+                if (lp) {
+                    cm = lp_e;
+                    if (lp_e > lp_len) {
+                        if (lane == 0) atomicOr(err, 2u);
+                        cm = lp_len > lp_b ? lp_len : lp_b;
+                    }
+                    pb = lp_pb;
+                    rows = lp_rows;
+                } else {
+                    cm = ld_shared_s32(eb + kEntCm);
+                    pb = ld_shared_s32(eb + kEntPb);
+                    rows = ld_shared_s32(eb + kEntRows);
+                }
                 const uint32_t qd = qbuf + qs * Lay::QSLOT;
 #pragma unroll
                 for (int k = 0; k < 8 / RPI; ++k) {
                     const int rq = k * RPI + lane / CPR;
                     const bool ok = rq < rows;
-                    const int mem = ld_shared_s32(eb + kEntMem + 4 * rq);
+                    const int lpm = __shfl_sync(0xffffffffu, lp_mem, rq);
+                    const int mem = lp ? lpm : ld_shared_s32(eb + kEntMem + 4 * rq);
                     const bf16* src = ok ? qp + ((int64_t)mem * Hq + kvh * G + rq % G) * D + ch * 8 : qp;
                     cp_async16(qd + swz<D>(rq, ch), src, ok);
                 }
                 if (lane == 0) {
-                    st_shared_s32(db + kDescCm, ld_shared_s32(eb + kEntCm));
-                    st_shared_s32(db + kDescPb, ld_shared_s32(eb + kEntPb));
+                    st_shared_s32(db + kDescCm, cm);
+                    st_shared_s32(db + kDescPb, pb);
                     st_shared_s32(db + kDescRows, rows);
                     st_shared_s32(db + kDescQ, qs);
                 }
@@ -356,7 +396,7 @@ __device__ __noinline__ void stream_producer(const FusedArgs& f, int gw, uint32_
 // ---------------------------------------------------------------------------
 // Consumer: only shared memory in its loop (stages, descriptors, Q slots)
 // ---------------------------------------------------------------------------
-template <int D>
+template <int D, int NS>
 __device__ __noinline__ void stream_consumer(const FusedArgs& f, uint32_t ring, uint32_t desc, uint32_t qbuf,
                                              uint32_t full, uint32_t empty, uint32_t qempty, int lane) {
     using Lay = FusedLayout<D>;
@@ -399,8 +439,8 @@ __device__ __noinline__ void stream_consumer(const FusedArgs& f, uint32_t ring, 
     bool timed_out = false;
     int nq = 0;
     for (int c = 0;; ++c) {
-        const int st = c % kNS;
-        if (!timed_out && !mbar_wait_sleep(full + 8 * st, (c / kNS) & 1)) {
+        const int st = c % NS;
+        if (!timed_out && !mbar_wait_sleep(full + 8 * st, (c / NS) & 1)) {
             atomicOr(err, 4u);
             timed_out = true;
         }
@@ -525,13 +565,13 @@ __global__ void __maxnreg__(128) decode_fused_kernel(const __grid_constant__ Fus
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + TL::OFF_TMEM);
     int* info = reinterpret_cast<int*>(sm + TL::OFF_INFO);
     const uint32_t sbar = smem_u32(sm + Lay::OFF_SBAR);
-    auto full_of = [&](int c) { return sbar + (uint32_t)(c * (2 * kNS + 2)) * 8; };
-    auto empty_of = [&](int c) { return sbar + (uint32_t)(c * (2 * kNS + 2) + kNS) * 8; };
-    auto qempty_of = [&](int c) { return sbar + (uint32_t)(c * (2 * kNS + 2) + 2 * kNS) * 8; };
+    auto full_of = [&](int c) { return sbar + (uint32_t)(c * (2 * kNSF + 2)) * 8; };
+    auto empty_of = [&](int c) { return sbar + (uint32_t)(c * (2 * kNSF + 2) + kNSF) * 8; };
+    auto qempty_of = [&](int c) { return sbar + (uint32_t)(c * (2 * kNSF + 2) + 2 * kNSF) * 8; };
     if (tid == 0) {
         if (tiles) tc_init_barriers<D, true>(smem_u32(sm + TL::OFF_BAR));
         for (int c = 0; c < kConsumers; ++c) {
-            for (int s = 0; s < kNS; ++s) {
+            for (int s = 0; s < kNSF; ++s) {
                 mbar_init(full_of(c) + 8 * s, 33);    // the producer's 32 lanes + its descriptor release
                 mbar_init(empty_of(c) + 8 * s, 1);    // the consumer
             }
@@ -548,6 +588,7 @@ __global__ void __maxnreg__(128) decode_fused_kernel(const __grid_constant__ Fus
     __syncthreads();
     tc_fence_after();
 
+    constexpr int kStreamGate = 3;   // named barrier: tile roles done -> streaming may start
     if (warp < kFirstProducer) {
         if (tiles) {
             const uint32_t tbase = *tslot;
@@ -559,16 +600,32 @@ __global__ void __maxnreg__(128) decode_fused_kernel(const __grid_constant__ Fus
                 tc_tile_run<D, true>(f.t, ti, sm, tbase, st, tid);
                 named_bar(kTileBar, kTileThreads);
             }
+            asm volatile("bar.arrive %0, %1;\n" ::"r"(kStreamGate), "r"(kFusedThreads) : "memory");
         }
     } else if (warp < kFirstConsumer) {
         const int c = warp - kFirstProducer;
-        stream_producer<D>(f, blockIdx.x * kConsumers + c, smem_u32(sm + Lay::OFF_RING + c * Lay::RING),
-                           smem_u32(sm + Lay::OFF_SLOT + c * Lay::SLOTW), smem_u32(sm + Lay::OFF_DESC + c * kNS * 32),
-                           smem_u32(sm + Lay::OFF_Q + c * 2 * Lay::QSLOT), full_of(c), empty_of(c), qempty_of(c), lane);
+        if (tiles) named_bar(kStreamGate, kFusedThreads);
+        const int gws = (int)blockIdx.x >= f.n_tile_ctas ? ((int)blockIdx.x - f.n_tile_ctas) * kConsumers + c : -1;
+        const uint32_t sring = smem_u32(sm + Lay::OFF_SLOT + c * Lay::SLOTW);
+        const uint32_t desc = smem_u32(sm + Lay::OFF_DESC + c * kNSF * 32);
+        const uint32_t qb = smem_u32(sm + Lay::OFF_Q + c * 2 * Lay::QSLOT);
+        if (tiles)
+            stream_producer<D, kNS>(f, gws, smem_u32(sm + Lay::OFF_RING + c * Lay::RING), sring, desc, qb, full_of(c),
+                                    empty_of(c), qempty_of(c), lane);
+        else
+            stream_producer<D, kNSF>(f, gws, smem_u32(sm + c * Lay::RING_F), sring, desc, qb, full_of(c), empty_of(c),
+                                     qempty_of(c), lane);
     } else {
         const int c = warp - kFirstConsumer;
-        stream_consumer<D>(f, smem_u32(sm + Lay::OFF_RING + c * Lay::RING), smem_u32(sm + Lay::OFF_DESC + c * kNS * 32),
-                           smem_u32(sm + Lay::OFF_Q + c * 2 * Lay::QSLOT), full_of(c), empty_of(c), qempty_of(c), lane);
+        if (tiles) named_bar(kStreamGate, kFusedThreads);
+        const uint32_t desc = smem_u32(sm + Lay::OFF_DESC + c * kNSF * 32);
+        const uint32_t qb = smem_u32(sm + Lay::OFF_Q + c * 2 * Lay::QSLOT);
+        if (tiles)
+            stream_consumer<D, kNS>(f, smem_u32(sm + Lay::OFF_RING + c * Lay::RING), desc, qb, full_of(c), empty_of(c),
+                                    qempty_of(c), lane);
+        else
+            stream_consumer<D, kNSF>(f, smem_u32(sm + c * Lay::RING_F), desc, qb, full_of(c), empty_of(c), qempty_of(c),
+                                     lane);
     }
     tc_fence_before();
     __syncthreads();
@@ -611,6 +668,7 @@ int launch_decode_fused(const sgl_plan* plan, const void* q, const void* kp, con
     f.narrow = a.items + plan->n_wide;
     f.n_narrow = plan->n_narrow;
     f.n_init = plan->n_init;
+    f.n_tile_ctas = plan->n_tile_ctas;
     f.sched = reinterpret_cast<uint32_t*>(ws + plan->off_sched);
     decode_fused_kernel<D><<<plan->n_ctas, kFusedThreads, Lay::TOTAL, s>>>(f);
     int e = (int)cudaGetLastError();

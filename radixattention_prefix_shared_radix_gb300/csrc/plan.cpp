@@ -10,7 +10,8 @@
 //   * a segment with more than 8 query rows (member x query head of a KV
 //     head; a prefix shared by many requests) becomes tensor-core tiles:
 //     member blocks of up to 128 rows x chunks of whole 128-position
-//     multiples (~1 tile of work per SM), dealt round-robin to the CTAs;
+//     multiples, dealt to a set of tile CTAs sized with the streaming work
+//     (cost model below);
 //   * every other segment (at most 8 rows: a request's own suffix, or a
 //     small group) is narrow: its positions, per KV head, are cut into
 //     pieces handed to the streaming warps at run time, longest first;
@@ -110,22 +111,12 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
     const int32_t MBw = std::max(1, 128 / G);
     const int sms = query_num_sms(p->num_sms);
 
-    // wide items: chunk-major, member block, KV head innermost
-    double units_w = 0;
-    for (int32_t s = 0; s < nseg; ++s) {
-        const int32_t nmem = g->seg_member_ptr[s + 1] - g->seg_member_ptr[s];
-        if (nmem > MBn)
-            units_w += (double)(g->seg_end[s] - g->seg_begin[s]) * ((nmem + MBw - 1) / MBw) * Hkv;
-    }
-    // ~1 tile of work per SM, whole 128-position multiples
-    int64_t Cw = (int64_t)std::ceil(units_w / (1.0 * sms));
-    Cw = std::max<int64_t>(128, (Cw + 127) / 128 * 128);
-    std::vector<sgl::DecItem> wide;
     struct Unit {   // narrow work: one member block of a segment for one KV head
         int32_t rep_row, b, e, kvh, mem_begin, n_mem;
     };
     std::vector<Unit> units;
     int64_t units_n = 0;
+    int64_t max_wide = 0;
     for (int32_t s = 0; s < nseg; ++s) {
         const int32_t b = g->seg_begin[s], e = g->seg_end[s];
         const int32_t m0 = g->seg_member_ptr[s], nmem = g->seg_member_ptr[s + 1] - m0;
@@ -134,8 +125,54 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
                 units.push_back({g->seg_row[s], b, e, h, m0, nmem});
                 units_n += e - b;
             }
-            continue;
+        } else {
+            max_wide = std::max<int64_t>(max_wide, e - b);
         }
+    }
+    const int64_t n_ctas = sms;
+    // Wide chunks run on tile CTAs whose streaming warps start only when
+    // their tiles are done (so the two never compete for an SM's issue slots
+    // and instruction cache); the other CTAs stream from the start.  Chunk
+    // length and tile CTA count come from a cost model of this kernel on
+    // GB300 (measured): a tile costs ~6 us plus ~1 us per 64-position block;
+    // a streaming SM handles ~82 (d=128) position-heads per us after ~5 us
+    // of start-up.  The chunk length with the earliest estimated finish is
+    // taken (tile CTAs at most half the CTAs).
+    auto wide_items_for = [&](int64_t Cw) {
+        int64_t n = 0;
+        for (int32_t s = 0; s < nseg; ++s) {
+            const int32_t nmem = g->seg_member_ptr[s + 1] - g->seg_member_ptr[s];
+            if (nmem > MBn)
+                n += (g->seg_end[s] - g->seg_begin[s] + Cw - 1) / Cw * ((nmem + MBw - 1) / MBw) * Hkv;
+        }
+        return n;
+    };
+    const double rate = 82.0 * 128.0 / p->head_dim;   // streamed position-heads per us per SM
+    int64_t Cw = 128, n_tile_ctas = 0;
+    if (max_wide > 0) {
+        double best = 1e300;
+        const int64_t top = std::min<int64_t>((max_wide + 127) / 128 * 128, 128 * 256);
+        for (int64_t c = 128; c <= top; c += 128) {
+            const int64_t nw = wide_items_for(c);
+            const int64_t T = std::max<int64_t>(1, std::min<int64_t>(nw, n_ctas / 2));
+            const double per = (double)((nw + T - 1) / T);
+            const double tile_us = per * (6.0 + (double)c / 64.0);
+            // streaming CTAs work from ~5 us; a tile CTA streams only what is
+            // left when its tiles are done, which the estimate ignores
+            const double F = std::max(tile_us, 5.0 + (double)units_n /
+                                                     ((double)std::max<int64_t>(1, n_ctas - T) * rate));
+            if (F < best) {
+                best = F;
+                Cw = c;
+                n_tile_ctas = T;
+            }
+        }
+    }
+    std::vector<sgl::DecItem> wide;
+    for (int32_t s = 0; s < nseg; ++s) {
+        const int32_t b = g->seg_begin[s], e = g->seg_end[s];
+        const int32_t m0 = g->seg_member_ptr[s], nmem = g->seg_member_ptr[s + 1] - m0;
+        if (nmem <= MBn) continue;
         const int32_t nblk = (nmem + MBw - 1) / MBw;
         for (int64_t cb = b; cb < e; cb += Cw) {
             const int32_t ce = (int32_t)std::min<int64_t>(e, cb + Cw);
@@ -150,11 +187,12 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
     // Narrow units are cut into pieces of at most Pmax positions (about two
     // pieces per streaming consumer; a cut makes one more partial to merge),
     // no piece shorter than one 16-position step unless its unit is, ordered
-    // longest first.  Consumer w starts on piece w; the rest are handed out
-    // at run time from a counter, so SMs that stream faster take more.
-    const int64_t n_ctas = sms;
-    const int64_t n_cons = n_ctas * sgl::kDecNarrowWarps;
-    int64_t Pmax = (int64_t)std::ceil((double)units_n / (2.0 * (double)n_cons));
+    // longest first.  Each consumer of a streaming CTA starts on its own
+    // piece; the rest (and all work of tile CTAs' consumers, once their tiles
+    // are done) are handed out at run time from a counter, so SMs that stream
+    // faster take more.
+    const int64_t n_cons = (n_ctas - n_tile_ctas) * sgl::kDecNarrowWarps;
+    int64_t Pmax = (int64_t)std::ceil((double)units_n / (2.0 * (double)std::max<int64_t>(1, n_cons)));
     Pmax = std::min<int64_t>(1024, std::max<int64_t>(64, (Pmax + 15) / 16 * 16));
     std::vector<sgl::DecItem> narrow;
     for (const Unit& u : units) {
@@ -170,9 +208,9 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
     });
     const int64_t n_init = std::min<int64_t>((int64_t)narrow.size(), n_cons);
 
-    // wide items round-robin over the CTAs
+    // wide items round-robin over the tile CTAs (the first n_tile_ctas)
     std::vector<std::vector<sgl::DecItem>> cta_items((size_t)n_ctas);
-    for (size_t i = 0; i < wide.size(); ++i) cta_items[i % (size_t)n_ctas].push_back(wide[i]);
+    for (size_t i = 0; i < wide.size(); ++i) cta_items[i % (size_t)std::max<int64_t>(1, n_tile_ctas)].push_back(wide[i]);
 
     // final item order: wide items by CTA, then the narrow pieces; partial
     // rows in item order
@@ -209,6 +247,7 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
     plan->n_ctas = (int32_t)n_ctas;
     plan->n_narrow = (int32_t)narrow.size();
     plan->n_init = (int32_t)n_init;
+    plan->n_tile_ctas = (int32_t)n_tile_ctas;
     plan->n_members = g->num_members;
     int64_t n_ent = 0;
     int32_t max_ent = 0;
