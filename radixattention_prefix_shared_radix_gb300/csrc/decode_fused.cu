@@ -31,8 +31,7 @@
 // cycles once the SM's load pipe is busy, so the SM's issue rate (and HBM
 // bandwidth) grows with the number of issuing warps.
 //
-// Streaming ring per consumer: 4 stages of 16 positions (K and V rows, 8 KB;
-// 6 stages in CTAs without tiles, which use the tile roles' shared memory)
+// Streaming ring per consumer: 4 stages of 16 positions (K and V rows, 8 KB)
 // with a descriptor each (first position, piece, flags), a FULL mbarrier per
 // stage (each producer lane arrives when its copies have landed:
 // cp.async.mbarrier.arrive.noinc, and lane 0 once more to release the
