@@ -216,7 +216,7 @@ typedef struct {
     int32_t num_kv_heads;   /* Hkv */
     int32_t head_dim;       /* d: 64 or 128 */
     int32_t page_size;      /* P >= 1 (addressing is per slot; informative) */
-    int64_t num_slots;      /* S: rows of each pool buffer */
+    int64_t num_slots;      /* S: rows of each pool buffer; S * Hkv < 2^31 */
     float sm_scale;         /* <= 0: 1/sqrt(d) */
     int32_t num_sms;        /* planning target; <= 0: query the current device (152 if none) */
     /* extend only: host copies of prefix_lens / extend_lens (B entries)

@@ -227,7 +227,7 @@ int launch_extend(const sgl_attn_params* p, const void* q, const void* kp, const
     const int tq = 128 / G;
     for (int r = 0; r < B; ++r) {
         total_rows += p->host_extend_lens[r];
-        tiles += (p->host_extend_lens[r] + tq - 1) / tq;
+        tiles += ((p->host_extend_lens[r] + tq - 1) / tq + 1) / 2;   // CTAs: pairs of query tiles
     }
     if (total_rows == 0) return SGL_OK;
     if (p->dtype == SGL_DTYPE_BF16) {

@@ -75,13 +75,14 @@ constexpr int kSQ = 8;                                   // slot ring entries pe
 constexpr int kSlotEntry = 128;                         // 16 slots + step and piece fields (see below)
 constexpr int kGrabAhead = 4;                            // take the next piece this many steps before the end
 constexpr int kFirstProducer = kTileThreads / 32;
+static_assert(kTileThreads == DecCfg<128>::kThreads, "tile roles: 7 warps");
 constexpr int kFirstConsumer = kFirstProducer + kProducers;
 constexpr int kFusedThreads = 32 * (kFirstConsumer + kConsumers);
 static_assert(kSQ >= kQD && (kSQ & (kSQ - 1)) == 0 && kQD >= kNSF - 1, "slot ring");
 
 template <int D>
 struct FusedLayout {
-    using TL = TcLayout<D, true>;
+    using TL = typename DecCfg<D>::Lay;
     static constexpr int TILEB = kNP * D * 2;            // one K (or V) tile of a step
     static constexpr int STAGE = 2 * TILEB;
     static constexpr int RING = kNS * STAGE;             // per consumer, beside the tile roles
@@ -553,9 +554,12 @@ __device__ __forceinline__ void dec_tile_info(const TcArgs& a, int w, int* info)
 }
 
 template <int D>
-__global__ void __maxnreg__(128) decode_fused_kernel(const __grid_constant__ FusedArgs f) {
+__global__ void __maxnreg__(128) decode_fused_kernel(const __grid_constant__ FusedArgs f,
+                                                     const __grid_constant__ CUtensorMap tmk,
+                                                     const __grid_constant__ CUtensorMap tmv) {
     using Lay = FusedLayout<D>;
-    using TL = TcLayout<D, true>;
+    using TC = DecCfg<D>;
+    using TL = typename TC::Lay;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -568,7 +572,7 @@ __global__ void __maxnreg__(128) decode_fused_kernel(const __grid_constant__ Fus
     auto empty_of = [&](int c) { return sbar + (uint32_t)(c * (2 * kNSF + 2) + kNSF) * 8; };
     auto qempty_of = [&](int c) { return sbar + (uint32_t)(c * (2 * kNSF + 2) + 2 * kNSF) * 8; };
     if (tid == 0) {
-        if (tiles) tc_init_barriers<D, true>(smem_u32(sm + TL::OFF_BAR));
+        if (tiles) tc_init_barriers<TC>(smem_u32(sm + TL::OFF_BAR));
         for (int c = 0; c < kConsumers; ++c) {
             for (int s = 0; s < kNSF; ++s) {
                 mbar_init(full_of(c) + 8 * s, 33);    // the producer's 32 lanes + its descriptor release
@@ -595,8 +599,8 @@ __global__ void __maxnreg__(128) decode_fused_kernel(const __grid_constant__ Fus
             for (int w = w0; w < w1; ++w) {
                 if (tid == 0) dec_tile_info(f.t, w, info);
                 named_bar(kTileBar, kTileThreads);
-                const TileInfo ti{info[0], info[1], info[2], info[3], info[4], info[5], info[6]};
-                tc_tile_run<D, true>(f.t, ti, sm, tbase, st, tid);
+                const TileInfo ti{info[0], info[1], info[2], info[3], {info[4], 0}, {info[5], 0}, {info[6], 0}};
+                tc_tile_run<TC>(f.t, &tmk, &tmv, ti, sm, tbase, st, tid);
                 named_bar(kTileBar, kTileThreads);
             }
             asm volatile("bar.arrive %0, %1;\n" ::"r"(kStreamGate), "r"(kFusedThreads) : "memory");
@@ -645,6 +649,10 @@ int launch_decode_fused(const sgl_plan* plan, const void* q, const void* kp, con
                                                       cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::TOTAL);
     if (attr) return attr;
     const sgl_attn_params& p = plan->params;
+    // the tiles' TMA views of the pools (unused, and left zero, without tiles)
+    CUtensorMap mk{}, mv{};
+    if (plan->n_wide > 0)
+        if (const int e = tc::encode_pool_maps(kp, vp, p.num_slots, p.num_kv_heads, D, &mk, &mv)) return e;
     FusedArgs f{};
     TcArgs& a = f.t;
     a.q = static_cast<const bf16*>(q);
@@ -669,7 +677,7 @@ int launch_decode_fused(const sgl_plan* plan, const void* q, const void* kp, con
     f.n_init = plan->n_init;
     f.n_tile_ctas = plan->n_tile_ctas;
     f.sched = reinterpret_cast<uint32_t*>(ws + plan->off_sched);
-    decode_fused_kernel<D><<<plan->n_ctas, kFusedThreads, Lay::TOTAL, s>>>(f);
+    decode_fused_kernel<D><<<plan->n_ctas, kFusedThreads, Lay::TOTAL, s>>>(f, mk, mv);
     int e = (int)cudaGetLastError();
     if (e) return e;
     MergeArgs m{a.po, a.plse, reinterpret_cast<const int32_t*>(ws + plan->off_mptr),

@@ -63,6 +63,34 @@ __device__ __forceinline__ void mma16816(float* c, const uint32_t* a, uint32_t b
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// 2^x in one MUFU operation (results below 2^-126 flush to zero, which the
+// softmax weights tolerate: they are summed with weights of at least 1).
+__device__ __forceinline__ float ex2_ftz(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+// (y0, y1) = (x0, x1) * s + (c, c): one packed fp32x2 FMA (sm_100+).
+__device__ __forceinline__ void ffma2_sc(float& y0, float& y1, float x0, float x1, float s, float c) {
+    asm("{\n .reg .b64 a, b, c, d;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %4};\n mov.b64 c, {%5, %5};\n"
+        " fma.rn.f32x2 d, a, b, c;\n mov.b64 {%0, %1}, d;\n}"
+        : "=f"(y0), "=f"(y1)
+        : "f"(x0), "f"(x1), "f"(s), "f"(c));
+}
+// (a0, a1) += (x0, x1): one packed fp32x2 add.
+__device__ __forceinline__ void fadd2_acc(float& a0, float& a1, float x0, float x1) {
+    asm("{\n .reg .b64 a, b, d;\n mov.b64 a, {%0, %1};\n mov.b64 b, {%2, %3};\n add.f32x2 d, a, b;\n"
+        " mov.b64 {%0, %1}, d;\n}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(x0), "f"(x1));
+}
+// max(a, b, c) in one instruction (sm_100+).
+__device__ __forceinline__ float fmax3f(float a, float b, float c) {
+    float y;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+    return y;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
@@ -273,6 +301,19 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
                  "l"(src), "r"(bytes), "r"(bar)
                  : "memory");
+}
+// TMA gather of four 128-byte row pieces: rows r0..r3, columns x..x+63 (bf16)
+// of the 2-D tensor `tmap` (box 64 x 1, 128-byte swizzle) into 512
+// consecutive shared bytes at `dst`, completing `bar`'s transaction count.
+// x * 2 bytes must be a multiple of 16; the swizzle follows the shared
+// address, so dst = region + 128 * row keeps the 128B-swizzle layout.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, int x, int r0, int r1, int r2, int r3,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+        "%3, %4, %5, %6}], [%7];\n" ::"r"(dst),
+        "l"(tmap), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
+        : "memory");
 }
 // Arrive on `bar` once every cp.async this thread issued so far has landed
 // (the barrier's expected count includes this arrival).

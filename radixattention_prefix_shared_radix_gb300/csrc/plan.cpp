@@ -54,7 +54,8 @@ int check_params(const sgl_attn_params* p) {
     if (p->num_qo_heads % p->num_kv_heads) return SGL_ERR_UNSUPPORTED;
     int G = p->num_qo_heads / p->num_kv_heads;
     if (G != 1 && G != 2 && G != 4 && G != 8) return SGL_ERR_UNSUPPORTED;
-    if (p->num_slots > INT32_MAX) return SGL_ERR_UNSUPPORTED;
+    // slot * Hkv + head is a 32-bit row coordinate of the pools' TMA view
+    if (p->num_slots * p->num_kv_heads > INT32_MAX) return SGL_ERR_UNSUPPORTED;
     return SGL_OK;
 }
 

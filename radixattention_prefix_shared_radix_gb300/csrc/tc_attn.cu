@@ -6,12 +6,17 @@
 // 0 .. prefix_len + i of its req_to_token row (the cached prefix plus the
 // causal part of the new block).
 //
-// One CTA per tile of 128 rows = (new token x query head of one KV head),
-// 128/G new tokens of one request; grid (tiles, KV heads).  The tile runs the
-// tcgen05 roles of tc_tile.cuh over positions 0 .. prefix_len + last new
-// token of the tile, with the causal limit applied per row in the softmax.
-// 224 threads, ~98 KB of shared memory and 256 TMEM columns per CTA, so two
-// tiles share an SM and take turns on the tensor core and the softmax units.
+// One CTA per pair of query tiles of 128 rows = (new token x query head of
+// one KV head), 128/G new tokens per tile, consecutive tiles of one request;
+// grid (pairs, KV heads).  The pair shares one K/V stream (TMA gathers into
+// 4-stage rings for d = 128, 8 for d = 64) and runs the tcgen05 roles of
+// tc_tile.cuh over positions 0 .. prefix_len + the pair's last new token,
+// with the causal limit applied per row in the softmax.  352 threads (two
+// softmax warpgroups, one MMA warp, two gather warps), ~193 KB of shared
+// memory and all 512 TMEM columns: one CTA per SM, whose two query tiles
+// take turns on the tensor core while each other's softmax runs.
+
+#include <cudaTypedefs.h>
 
 #include "tc_tile.cuh"
 
@@ -21,89 +26,154 @@ namespace {
 using namespace sgldev;
 using namespace tc;
 
-// Tile (blockIdx.x, blockIdx.y) of the extend batch; false if empty.
+template <int D>
+using ExtCfg = TcCfg<D, false, 2, 4 * (128 / D), 4 * (128 / D)>;
+
+// Query tile pair (blockIdx.x, blockIdx.y) of the extend batch; false if empty.
 __device__ bool extend_tile_info(const TcArgs& a, int* info) {
     const int tq = 128 / a.G;
-    int acc_t = 0, acc_q = 0, req = -1, tile0 = 0, qoff = 0;
+    int acc_c = 0, acc_q = 0, req = -1, c0 = 0, qoff = 0;
     for (int r = 0; r < a.B; ++r) {
         const int e = __ldg(a.extend_lens + r);
         const int nt = e > 0 ? (e + tq - 1) / tq : 0;
-        if ((int)blockIdx.x < acc_t + nt) {
+        const int nc = (nt + 1) / 2;
+        if ((int)blockIdx.x < acc_c + nc) {
             req = r;
-            tile0 = acc_t;
+            c0 = acc_c;
             qoff = acc_q;
             break;
         }
-        acc_t += nt;
+        acc_c += nc;
         acc_q += e > 0 ? e : 0;
     }
     if (req < 0) return false;
     const int pre = __ldg(a.prefix_lens + req), ext = __ldg(a.extend_lens + req);
-    const int t0 = ((int)blockIdx.x - tile0) * tq;
-    const int ntok = min(tq, ext - t0);
-    if (pre < 0 || ntok <= 0 || (int64_t)pre + ext > a.ld || (int64_t)qoff + t0 + ntok > a.n_rows) {
+    const int t0 = ((int)blockIdx.x - c0) * 2 * tq;
+    const int na = min(tq, ext - t0), nb2 = min(tq, ext - t0 - tq);
+    const int ntok = na + (nb2 > 0 ? nb2 : 0);
+    if (pre < 0 || na <= 0 || (int64_t)pre + ext > a.ld || (int64_t)qoff + t0 + ntok > a.n_rows) {
         atomicOr(a.err, 2u);
         return false;
     }
-    info[0] = req;                // KV row
-    info[1] = 0;                  // kv_begin
-    info[2] = pre + t0 + ntok;    // kv_end
-    info[3] = blockIdx.y;         // KV head
-    info[4] = ntok * a.G;         // rows
-    info[5] = qoff + t0;          // first q row
-    info[6] = pre + t0;           // causal limit of the tile's first new token
+    info[0] = req;                        // KV row
+    info[1] = 0;                          // kv_begin
+    info[2] = pre + t0 + ntok;            // kv_end
+    info[3] = blockIdx.y;                 // KV head
+    info[4] = na * a.G;                   // rows of tile 0
+    info[5] = nb2 > 0 ? nb2 * a.G : 0;    // rows of tile 1 (0: absent)
+    info[6] = qoff + t0;                  // first q row of tile 0
+    info[7] = qoff + t0 + tq;             // first q row of tile 1
+    info[8] = pre + t0;                   // causal limit of tile 0's first new token
+    info[9] = pre + t0 + tq;              // causal limit of tile 1's first new token
     return true;
 }
 
 template <int D>
-__global__ void __maxnreg__(128) extend_tc_kernel(const TcArgs a) {
-    using Lay = TcLayout<D>;
+__global__ void __launch_bounds__(ExtCfg<D>::kThreads, 1)
+    extend_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
+    using C = ExtCfg<D>;
+    using Lay = typename C::Lay;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     int* info = reinterpret_cast<int*>(sm + Lay::OFF_INFO);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + Lay::OFF_TMEM);
     const int tid = threadIdx.x, warp = tid >> 5;
-    if (tid == 0) info[7] = extend_tile_info(a, info) ? 1 : 0;
+    if (tid == 0) info[15] = extend_tile_info(a, info) ? 1 : 0;
     __syncthreads();
-    if (!info[7]) return;
+    if (!info[15]) return;
     if (tid == 0) {
-        tc_init_barriers<D, false>(smem_u32(sm + Lay::OFF_BAR));
+        tc_init_barriers<C>(smem_u32(sm + Lay::OFF_BAR));
         mbar_fence_init();
     }
-    if (warp == 4) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 256;\n" ::"r"(smem_u32(tslot)));
+    if (warp == C::kMmaWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;\n" ::"r"(smem_u32(tslot)));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = *tslot;
-    const TileInfo ti{info[0], info[1], info[2], info[3], info[4], info[5], info[6]};
+    const TileInfo ti{info[0], info[1], info[2], info[3], {info[4], info[5]}, {info[6], info[7]}, {info[8], info[9]}};
     TcState st{0u, 0u, false};
-    tc_tile_run<D, false>(a, ti, sm, tbase, st, tid);
+    tc_tile_run<C>(a, &tmk, &tmv, ti, sm, tbase, st, tid);
     tc_fence_before();
     __syncthreads();
-    if (warp == 4) {
+    if (warp == C::kMmaWarp) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 256;\n" ::"r"(tbase));
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;\n" ::"r"(tbase));
     }
 }
 
 template <int D>
 constexpr int extend_smem() {
-    return TcLayout<D>::END + 1024;   // + alignment slack
+    return ExtCfg<D>::Lay::END + 1024;   // + alignment slack
 }
+static_assert(extend_smem<128>() <= 232448 && extend_smem<64>() <= 232448, "shared memory per CTA");
+static_assert(extend_smem<128>() > 116 * 1024 && extend_smem<64>() > 116 * 1024,
+              "one CTA per SM: each allocates all 512 TMEM columns");
 
 }  // namespace
 
-// Extend over all requests: grid (tiles of 128/G new tokens, KV heads).
+namespace tc {
+
+int encode_pool_maps(const void* kp, const void* vp, int64_t num_slots, int Hkv, int D, CUtensorMap* mk,
+                     CUtensorMap* mv) {
+    static PFN_cuTensorMapEncodeTiled_v12000 enc = [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            fn = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }();
+    if (!enc) return (int)cudaErrorNotSupported;
+    struct Cache {
+        const void *kp = nullptr, *vp = nullptr;
+        int64_t ns = -1;
+        int hkv = 0, d = 0;
+        CUtensorMap mk, mv;
+    };
+    thread_local Cache c;
+    if (c.kp != kp || c.vp != vp || c.ns != num_slots || c.hkv != Hkv || c.d != D) {
+        const cuuint64_t rows = (cuuint64_t)num_slots * (cuuint64_t)Hkv;
+        if (rows == 0 || rows > (cuuint64_t)INT32_MAX) return (int)cudaErrorInvalidValue;
+        const cuuint64_t gdim[2] = {(cuuint64_t)D, rows};
+        const cuuint64_t gstride[1] = {(cuuint64_t)D * 2};
+        const cuuint32_t box[2] = {64, 1};
+        const cuuint32_t estride[2] = {1, 1};
+        for (int w = 0; w < 2; ++w) {
+            CUresult r = enc(w ? &c.mv : &c.mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(w ? vp : kp),
+                             gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            if (r != CUDA_SUCCESS) {
+                c.kp = nullptr;
+                return (int)cudaErrorInvalidValue;
+            }
+        }
+        c.kp = kp;
+        c.vp = vp;
+        c.ns = num_slots;
+        c.hkv = Hkv;
+        c.d = D;
+    }
+    *mk = c.mk;
+    *mv = c.mv;
+    return 0;
+}
+
+}  // namespace tc
+
+// Extend over all requests: grid (pairs of query tiles of 128/G new tokens, KV heads).
 template <int D>
 int launch_extend_tc(const void* q, const void* kp, const void* vp, const int32_t* r2t, int64_t ld,
-                     const int32_t* pre, const int32_t* ext, int B, int64_t n_rows, int64_t tiles, void* o, float* lse,
+                     const int32_t* pre, const int32_t* ext, int B, int64_t n_rows, int64_t ctas, void* o, float* lse,
                      uint32_t* err, int Hq, int Hkv, int64_t num_slots, float scale_log2, cudaStream_t s) {
     static const int attr = (int)cudaFuncSetAttribute(extend_tc_kernel<D>,
                                                       cudaFuncAttributeMaxDynamicSharedMemorySize, extend_smem<D>());
     if (attr) return attr;
+    CUtensorMap mk, mv;
+    if (const int e = tc::encode_pool_maps(kp, vp, num_slots, Hkv, D, &mk, &mv)) return e;
     TcArgs a{};
     a.q = static_cast<const bf16*>(q);
     a.kp = static_cast<const bf16*>(kp);
@@ -122,7 +192,7 @@ int launch_extend_tc(const void* q, const void* kp, const void* vp, const int32_
     a.G = Hq / Hkv;
     a.num_slots = num_slots;
     a.scale_log2 = scale_log2;
-    extend_tc_kernel<D><<<dim3((unsigned)tiles, (unsigned)Hkv), kTileThreads, extend_smem<D>(), s>>>(a);
+    extend_tc_kernel<D><<<dim3((unsigned)ctas, (unsigned)Hkv), ExtCfg<D>::kThreads, extend_smem<D>(), s>>>(a, mk, mv);
     return (int)cudaGetLastError();
 }
 
