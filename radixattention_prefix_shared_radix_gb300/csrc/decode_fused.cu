@@ -9,11 +9,13 @@
 // read once: a segment shared by many requests is read once for all of them.
 //
 // One CTA per SM (the planner's n_ctas), 480 threads:
-//   warps 0-6   the tcgen05 tile roles (tc_tile.cuh) over this CTA's wide
-//               items: a chunk of a shared segment against up to 128 query
-//               rows (member request x query head of one KV head);
+//   warps 0-10  (CTAs with wide items) the tcgen05 tile roles of
+//               tc_tile.cuh over this CTA's wide items: a chunk of a shared
+//               segment against up to 128 query rows (member request x query
+//               head of one KV head); warps 5-10 are the tiles' gather team;
 //   warps 7-10  streaming producers: each issues the cp.async gathers of one
-//               consumer's K/V rows into its shared-memory ring;
+//               consumer's K/V rows into its shared-memory ring (in CTAs
+//               with wide items, once the tiles are done);
 //   warps 11-14 streaming consumers: each runs narrow pieces (at most 8
 //               query rows: one request's G heads, or a few members of a
 //               small group) on the tensor cores: its launch piece, then
@@ -74,8 +76,9 @@ constexpr int kQD = 6;                                   // slot lookups ahead (
 constexpr int kSQ = 8;                                   // slot ring entries per consumer
 constexpr int kSlotEntry = 128;                         // 16 slots + step and piece fields (see below)
 constexpr int kGrabAhead = 4;                            // take the next piece this many steps before the end
-constexpr int kFirstProducer = kTileThreads / 32;
-static_assert(kTileThreads == DecCfg<128>::kThreads, "tile roles: 7 warps");
+constexpr int kFirstProducer = 7;                        // after the tile roles' softmax, MMA and own gather warps
+static_assert(DecCfg<128>::kThreads == 32 * (kFirstProducer + kProducers) && DecCfg<64>::kThreads == DecCfg<128>::kThreads,
+              "the tile roles' gather team is warps 5 .. 10: two of its own and the four producers");
 constexpr int kFirstConsumer = kFirstProducer + kProducers;
 constexpr int kFusedThreads = 32 * (kFirstConsumer + kConsumers);
 static_assert(kSQ >= kQD && (kSQ & (kSQ - 1)) == 0 && kQD >= kNSF - 1, "slot ring");
@@ -592,22 +595,25 @@ __global__ void __maxnreg__(128) decode_fused_kernel(const __grid_constant__ Fus
     tc_fence_after();
 
     constexpr int kStreamGate = 3;   // named barrier: tile roles done -> streaming may start
-    if (warp < kFirstProducer) {
-        if (tiles) {
-            const uint32_t tbase = *tslot;
-            TcState st{0u, 0u, false};
-            for (int w = w0; w < w1; ++w) {
-                if (tid == 0) dec_tile_info(f.t, w, info);
-                named_bar(kTileBar, kTileThreads);
-                const TileInfo ti{info[0], info[1], info[2], info[3], {info[4], 0}, {info[5], 0}, {info[6], 0}};
-                tc_tile_run<TC>(f.t, &tmk, &tmv, ti, sm, tbase, st, tid);
-                named_bar(kTileBar, kTileThreads);
-            }
-            asm volatile("bar.arrive %0, %1;\n" ::"r"(kStreamGate), "r"(kFusedThreads) : "memory");
+    constexpr int kTileWarps = TC::kThreads / 32;   // softmax, MMA, gather team (incl. the producers)
+    if (tiles && warp < kTileWarps) {
+        // the tile roles; the producer warps are part of the gather team and
+        // go on to stream once the CTA's tiles are done
+        const uint32_t tbase = *tslot;
+        TcState st{0u, 0u, false};
+        for (int w = w0; w < w1; ++w) {
+            if (tid == 0) dec_tile_info(f.t, w, info);
+            named_bar(kTileBar, TC::kThreads);
+            const TileInfo ti{info[0], info[1], info[2], info[3], {info[4], 0}, {info[5], 0}, {info[6], 0}};
+            tc_tile_run<TC>(f.t, &tmk, &tmv, ti, sm, tbase, st, tid);
+            named_bar(kTileBar, TC::kThreads);
         }
-    } else if (warp < kFirstConsumer) {
+        asm volatile("bar.arrive %0, %1;\n" ::"r"(kStreamGate), "r"(kFusedThreads) : "memory");
+    }
+    // streaming warps of CTAs with tiles start once the tiles are done
+    if (tiles && warp >= kTileWarps) named_bar(kStreamGate, kFusedThreads);
+    if (warp >= kFirstProducer && warp < kFirstConsumer) {
         const int c = warp - kFirstProducer;
-        if (tiles) named_bar(kStreamGate, kFusedThreads);
         const int gws = (int)blockIdx.x >= f.n_tile_ctas ? ((int)blockIdx.x - f.n_tile_ctas) * kConsumers + c : -1;
         const uint32_t sring = smem_u32(sm + Lay::OFF_SLOT + c * Lay::SLOTW);
         const uint32_t desc = smem_u32(sm + Lay::OFF_DESC + c * kNSF * 32);
@@ -618,9 +624,8 @@ __global__ void __maxnreg__(128) decode_fused_kernel(const __grid_constant__ Fus
         else
             stream_producer<D, kNSF>(f, gws, smem_u32(sm + c * Lay::RING_F), sring, desc, qb, full_of(c), empty_of(c),
                                      qempty_of(c), lane);
-    } else {
+    } else if (warp >= kFirstConsumer) {
         const int c = warp - kFirstConsumer;
-        if (tiles) named_bar(kStreamGate, kFusedThreads);
         const uint32_t desc = smem_u32(sm + Lay::OFF_DESC + c * kNSF * 32);
         const uint32_t qb = smem_u32(sm + Lay::OFF_Q + c * 2 * Lay::QSLOT);
         if (tiles)

@@ -8,13 +8,14 @@
 //
 // One CTA per pair of query tiles of 128 rows = (new token x query head of
 // one KV head), 128/G new tokens per tile, consecutive tiles of one request;
-// grid (pairs, KV heads).  The pair shares one K/V stream (TMA gathers into
-// 4-stage rings for d = 128, 8 for d = 64) and runs the tcgen05 roles of
-// tc_tile.cuh over positions 0 .. prefix_len + the pair's last new token,
-// with the causal limit applied per row in the softmax.  352 threads (two
-// softmax warpgroups, one MMA warp, two gather warps), ~193 KB of shared
-// memory and all 512 TMEM columns: one CTA per SM, whose two query tiles
-// take turns on the tensor core while each other's softmax runs.
+// grid (pairs, KV heads).  The pair shares one K/V stream of 128-position
+// blocks (2-stage rings for d = 128, 4 for d = 64, filled by a team of six
+// gather warps) and runs the tcgen05 roles of tc_tile.cuh over positions
+// 0 .. prefix_len + the pair's last new token, with the causal limit applied
+// per row in the softmax.  480 threads (two softmax warpgroups, one MMA warp,
+// six gather warps), ~193 KB of shared memory and all 512 TMEM columns: one
+// CTA per SM, whose two query tiles take turns on the tensor core while each
+// other's softmax runs.
 
 #include <cudaTypedefs.h>
 
@@ -26,8 +27,11 @@ namespace {
 using namespace sgldev;
 using namespace tc;
 
+// two query tiles, 128-position blocks (S MMAs of N = 128: an M = 128
+// tcgen05 MMA costs about the same time for N = 64 as for N = 128), one score
+// buffer each, 2 K/V stages (4 for d = 64), a gather team of 6 warps
 template <int D>
-using ExtCfg = TcCfg<D, false, 2, 4 * (128 / D), 4 * (128 / D)>;
+using ExtCfg = TcCfg<D, false, 2, 2 * (128 / D), 6, 128, 1>;
 
 // Query tile pair (blockIdx.x, blockIdx.y) of the extend batch; false if empty.
 __device__ bool extend_tile_info(const TcArgs& a, int* info) {

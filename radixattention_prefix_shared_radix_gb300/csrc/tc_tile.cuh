@@ -1,43 +1,42 @@
-// One attention tile on the 5th-generation tensor cores (tcgen05 + TMEM):
-// 128 query rows against the KV positions [kv_begin, kv_end) of one
-// req_to_token row, gathered 64 positions at a time.  Used by the extend
-// kernel (one tile per CTA) and by the fused decode kernel (the CTA's
+// Attention tiles on the 5th-generation tensor cores (tcgen05 + TMEM): NQ
+// query tiles of 128 rows against the KV positions [kv_begin, kv_end) of one
+// req_to_token row, gathered 64 positions at a time into one K/V stream that
+// the query tiles share.  Used by the extend kernel (two query tiles per CTA)
+// and by the fused decode kernel (one query tile at a time, the CTA's
 // prefix-group tiles one after another).
 //
-// Roles, by warp of the 224 tile threads:
-//   warps 0-3  softmax: thread i owns query row i == TMEM lane i;
-//   warp  4    one thread issues every MMA (the warp also owns TMEM);
-//   warp  5    (extend) gathers half of the Q rows; then the K block of
-//              every step;
-//   warp  6    (extend) gathers the other Q rows; then the V block of every
-//              step.
-// Q is a 128B-swizzled smem tile in extend.  In decode tiles it lives in
-// TMEM instead (columns 256..256+d/2, bf16 pairs, written by the softmax
-// threads from their own rows) and S = Q K^T reads A from TMEM, which leaves
-// 64 KB of shared memory to the tile so the fused decode kernel can give the
-// rest to its streaming warps.
-// A gather warp looks up the block's slots in req_to_token one block ahead
-// and fetches the block's 64 K (or V) rows with one warp instruction of TMA
-// gathers: each lane issues a tile::gather4 of four rows x 128 bytes (rows
-// of the pool viewed as a 2-D tensor [slot * Hkv + head, d]) into the
-// 128B-swizzled tile, and lane 0 arms the stage's mbarrier with the block's
-// byte count.  Positions past the end of the range re-read the range's last
-// position (finite data; their scores are masked), so no row is ever out of
-// bounds.  K and V have separate 2-stage rings and separate warps, so K_{j+2}
-// loads as soon as S_j is done whatever V is doing.
-// Per 64-position KV block j:  S_j = Q K_j^T (M 128, N 64, K d; both operands
-// K-major) into one of two TMEM score buffers.  The softmax threads read their
-// row (two TMEM loads in flight, one wait), keep a running max m and sum l in
-// base 2 (scores pre-scaled by sm_scale*log2 e), and write P_j = 2^(s - m) as
-// bf16 pairs back into the first half of the same TMEM buffer; the MMA thread
-// then issues O += P_j V_j with A read from TMEM (M 128, N d, K 64; V an
-// MN-major smem operand) and S_{j+2} into the freed buffer.  O lives in TMEM
-// and is rescaled only when a row's max grows by more than 8 (a factor 2^8,
-// harmless in fp32).
+// Roles, by warp of the C::kThreads tile threads:
+//   warps 0 .. 4 NQ - 1   softmax: query tile w / 4, thread = query row =
+//                         TMEM lane;
+//   warp 4 NQ             one thread issues every MMA (the warp owns TMEM);
+//   the next NG warps     the gather team: the K and V rows of every block
+//                         as TMA tile::gather4 copies (four rows of 128
+//                         bytes each, rows of the pool viewed as a 2-D
+//                         tensor [slot * Hkv + head, d]) into 128B-swizzled
+//                         tiles; extend's Q tiles with 16-byte cp.async.
+// Measured on GB300: a warp gets one random-row gather through every ~110
+// cycles, whether one lane issues them or many, so the gather rate grows with
+// the number of warps that issue; hence a team.
+// In decode tiles Q lives in TMEM (columns 256..256+d/2, bf16 pairs, written
+// by the softmax threads from their own rows) and S = Q K^T reads A from
+// TMEM, which leaves the CTA's shared memory to its streaming warps.
+// The gather team looks up each block's slots in req_to_token one block
+// ahead.
+// Per 64-position KV block j and query tile q:  S = Q K_j^T (M 128, N 64, K
+// d; both operands K-major) into one of two TMEM score buffers.  The softmax
+// threads read their row (two TMEM loads in flight, one wait), keep a running
+// max m and sum l in base 2 (scores scaled by sm_scale*log2 e inside the
+// exponent's FMA), and write P_j = 2^(s - m) as bf16 pairs back into the first
+// half of the same TMEM buffer; the MMA thread then issues O += P_j V_j with A
+// read from TMEM (M 128, N d, K 64; V an MN-major smem operand) and S_{j+2}
+// into the freed buffer.  O lives in TMEM and is rescaled only when a row's
+// max grows by more than 8 (a factor 2^8, harmless in fp32), by the warp that
+// owns the row, which then waits for PV_{j-1}; otherwise the softmax never
+// waits for the PV products.
 //
-// Barrier phases run on across tiles: J counts the blocks and T the tiles
-// this CTA has processed, so a CTA can run any number of tiles back to back
-// (separated by a barrier of the 224 tile threads).  All waits are bounded:
+// Barrier phases run on across tiles: J counts the blocks and T the tile sets
+// this CTA has processed, so a CTA can run any number of tile sets back to
+// back (separated by a barrier of the tile threads).  All waits are bounded:
 // one that gives up sets bit 2 of the error word and the code runs to its end
 // without hanging (its results are then garbage, and flagged).
 
@@ -52,11 +51,8 @@ namespace tc {
 
 using namespace sgldev;
 
-constexpr int kTileThreads = 224;        // threads of a one-query-tile set (7 warps)
-constexpr int kBN = 64;                  // KV positions per block
 constexpr int kQRegion = 128 * 128;      // SW128 region of a 128-row tile: 128 rows x 128 bytes
-constexpr int kKRegion = kBN * 128;      // SW128 region of a 64-row tile
-constexpr int kTileBar = 1;              // named barrier of the 224 tile threads
+constexpr int kTileBar = 1;              // named barrier of the tile threads
 
 // 16-byte chunk c of row r of a bf16 tile kept as 64-column SW128 regions of
 // `region` bytes each (the canonical K-major / MN-major 128B-swizzle layout).
@@ -160,59 +156,72 @@ struct TcArgs {
 
 // Shared memory of the tile roles (offsets from a 1024-byte aligned base):
 // NQ query tiles (extend: 128B-swizzled smem tiles; decode: none, Q lives in
-// TMEM), NSK K stages and NSV V stages of 64 positions, the barriers and a
+// TMEM), NS K stages and NS V stages of BN positions, the barriers and a
 // small broadcast area.
-template <int D, bool DEC, int NQ, int NSK, int NSV>
+template <int D, bool DEC, int NQ, int NS, int BN>
 struct TcLayout {
     static constexpr int QTILE = DEC ? 0 : 128 * D * 2;
-    static constexpr int KTILE = kBN * D * 2;
+    static constexpr int KREGION = BN * 128;             // SW128 region: BN rows x 64 columns
+    static constexpr int KTILE = BN * D * 2;
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + NQ * QTILE;
-    static constexpr int OFF_V = OFF_K + NSK * KTILE;
-    static constexpr int OFF_BAR = OFF_V + NSV * KTILE;
+    static constexpr int OFF_V = OFF_K + NS * KTILE;
+    static constexpr int OFF_BAR = OFF_V + NS * KTILE;
     static constexpr int OFF_INFO = OFF_BAR + 48 * 8;    // tile description broadcast (16 ints)
     static constexpr int OFF_TMEM = OFF_INFO + 16 * 4;   // TMEM base address
     static constexpr int END = OFF_TMEM + 16;
 };
 
 // Tile roles and their barriers for NQ query tiles that share one K/V stream
-// of NSK + NSV stages.  Warps 0 .. 4 NQ - 1: softmax (warp w serves query
+// of NS stages each for K and V, BN positions per block, NSB TMEM score
+// buffers per query tile.  Warps 0 .. 4 NQ - 1: softmax (warp w serves query
 // tile w / 4, TMEM lanes 32 (w % 4) ..); warp 4 NQ: MMA issue + TMEM owner;
-// warp 4 NQ + 1: K gathers; warp 4 NQ + 2: V gathers.
-template <int D, bool DEC, int NQ, int NSK, int NSV>
+// warps 4 NQ + 1 .. 4 NQ + NG: the gather team.
+//
+// TMEM columns of query tile q: S buffers at q * 256 + BN b (b < NSB), O at
+// q * 256 + NSB * BN; decode's Q after O.  P_j (bf16 pairs) overwrites the
+// first BN / 2 columns of its own S buffer.
+template <int D, bool DEC, int NQ, int NS, int NG, int BN, int NSB>
 struct TcCfg {
     static_assert(NQ == 1 || (NQ == 2 && !DEC), "decode tiles use one query tile (Q lives in TMEM)");
-    static_assert(NSK >= 2 && NSV >= 2, "the S lookahead needs two K stages");
-    using Lay = TcLayout<D, DEC, NQ, NSK, NSV>;
-    static constexpr int kD = D, kNQ = NQ, kNSK = NSK, kNSV = NSV;
+    static_assert(BN == 64 || BN == 128, "KV block of 64 or 128 positions");
+    static_assert(NSB == 1 || NSB == 2, "one or two score buffers");
+    static_assert(NS >= NSB, "the S lookahead needs as many K stages as score buffers");
+    static_assert(NSB * BN + 128 + (DEC ? D / 2 : 0) <= (NQ == 2 ? 256 : 512), "TMEM columns");
+    static_assert(NQ == 1 || NSB == 1, "two query tiles alternate on one score buffer each");
+    using Lay = TcLayout<D, DEC, NQ, NS, BN>;
+    static constexpr int kD = D, kNQ = NQ, kNS = NS, kNG = NG, kBN = BN, kNSB = NSB;
     static constexpr bool kDec = DEC;
-    static constexpr int kThreads = 32 * (4 * NQ + 3);
+    static constexpr int kThreads = 32 * (4 * NQ + 1 + NG);
     static constexpr int kMmaWarp = 4 * NQ;
-    static constexpr int kTmemCols = (DEC || NQ == 2) ? 512 : 256;
+    static constexpr int kOCol = NSB * BN;               // O's column within a query tile's 256
+    static constexpr int kQCol = kOCol + 128;            // decode: Q's columns
     // barrier indices
     static constexpr int QFULL = 0;
     static constexpr int KFULL(int s) { return 1 + s; }
-    static constexpr int KEMPTY(int s) { return 1 + NSK + s; }
-    static constexpr int VFULL(int s) { return 1 + 2 * NSK + s; }
-    static constexpr int VEMPTY(int s) { return 1 + 2 * NSK + NSV + s; }
-    // per query tile: S ready and P ready per TMEM score buffer b = block & 1
-    // (one barrier per buffer, so the softmax warps can never be two phases
-    // ahead of the MMA thread's wait: block j + 2 needs S_{j+2}, which is
-    // issued only after the MMA thread has consumed block j's P), O updated
-    static constexpr int SFULL(int q, int b) { return 1 + 2 * NSK + 2 * NSV + 5 * q + b; }
-    static constexpr int PFULL(int q, int b) { return 1 + 2 * NSK + 2 * NSV + 5 * q + 2 + b; }
-    static constexpr int OFULL(int q) { return 1 + 2 * NSK + 2 * NSV + 5 * q + 4; }
+    static constexpr int KEMPTY(int s) { return 1 + NS + s; }
+    static constexpr int VFULL(int s) { return 1 + 2 * NS + s; }
+    static constexpr int VEMPTY(int s) { return 1 + 3 * NS + s; }
+    // per query tile: S ready and P ready per score buffer (one barrier per
+    // buffer, so the softmax warps can never be two phases ahead of the MMA
+    // thread's wait: block j + NSB needs S_{j+NSB}, which is issued only after
+    // the MMA thread has consumed block j's P), O updated
+    static constexpr int SFULL(int q, int b) { return 1 + 4 * NS + 5 * q + b; }
+    static constexpr int PFULL(int q, int b) { return 1 + 4 * NS + 5 * q + 2 + b; }
+    static constexpr int OFULL(int q) { return 1 + 4 * NS + 5 * q + 4; }
     // every MMA of the tile set has finished (one phase per tile set, so
     // the waits on it are never ambiguous, unlike a wait on OFULL's last
     // phase when earlier phases may still be pending)
-    static constexpr int DONE = 1 + 2 * NSK + 2 * NSV + 5 * NQ;
+    static constexpr int DONE = 1 + 4 * NS + 5 * NQ;
     static constexpr int kNumBars = DONE + 1;
     static_assert(kNumBars <= 48, "barrier area");
 };
 
-// The decode tiles' configuration (one query tile, Q in TMEM, 2 + 2 stages).
+// The decode tiles' configuration: one query tile with Q in TMEM, 64-position
+// blocks, two score buffers, two K/V stages (the tile CTAs leave most of
+// their shared memory to their streaming warps), a gather team of six warps.
 template <int D>
-using DecCfg = TcCfg<D, true, 1, 2, 2>;
+using DecCfg = TcCfg<D, true, 1, 2, 6, 64, 2>;
 
 struct TileInfo {
     int kv_row, kv_begin, kv_end, kvh;
@@ -230,22 +239,21 @@ struct TcState {
 template <class C>
 __device__ __forceinline__ void tc_init_barriers(uint32_t bar0) {
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
-    mbar_init(bar(C::QFULL), C::kDec ? 128 : 64);   // Q writers: softmax threads (decode) / gather lanes (extend)
-    // FULL: lane 0's expect_tx (the TMA gathers complete the bytes); EMPTY:
-    // the MMA thread's commit
-    for (int s2 = 0; s2 < C::kNSK; ++s2) {
-        mbar_init(bar(C::KFULL(s2)), 1);
+    // Q writers: the softmax threads (decode) or the gather team's lanes (extend)
+    mbar_init(bar(C::QFULL), C::kDec ? 128 : 32 * C::kNG);
+    // FULL: one expect_tx arrival per gather warp (its TMA gathers complete
+    // the bytes); EMPTY: the MMA thread's commit
+    for (int s2 = 0; s2 < C::kNS; ++s2) {
+        mbar_init(bar(C::KFULL(s2)), C::kNG);
         mbar_init(bar(C::KEMPTY(s2)), 1);
-    }
-    for (int s2 = 0; s2 < C::kNSV; ++s2) {
-        mbar_init(bar(C::VFULL(s2)), 1);
+        mbar_init(bar(C::VFULL(s2)), C::kNG);
         mbar_init(bar(C::VEMPTY(s2)), 1);
     }
     for (int q = 0; q < C::kNQ; ++q) {
-        mbar_init(bar(C::SFULL(q, 0)), 1);
-        mbar_init(bar(C::SFULL(q, 1)), 1);
-        mbar_init(bar(C::PFULL(q, 0)), 128);
-        mbar_init(bar(C::PFULL(q, 1)), 128);
+        for (int b = 0; b < C::kNSB; ++b) {
+            mbar_init(bar(C::SFULL(q, b)), 1);
+            mbar_init(bar(C::PFULL(q, b)), 128);
+        }
         mbar_init(bar(C::OFULL(q)), 1);
     }
     mbar_init(bar(C::DONE), 1);
@@ -253,18 +261,18 @@ __device__ __forceinline__ void tc_init_barriers(uint32_t bar0) {
 
 // Run one set of NQ query tiles with the C::kThreads tile threads (tid =
 // threadIdx.x < C::kThreads).  `sm` is the 1024-aligned shared base, `tbase`
-// the CTA's TMEM columns: query tile q has its S buffers at columns
-// 256 q + {0, 64} and O at 256 q + 128; decode keeps Q at column 256.  On
-// return the tiles' O / LSE (extend) or partial rows (decode) are written by
-// the softmax threads; the caller separates tile sets with a barrier of the
-// tile threads.  A query tile with no rows is skipped entirely, which keeps
-// the barrier phases consistent only for the CTA's last tile set (extend
-// CTAs run one set; decode tiles always have rows).
+// the CTA's TMEM columns.  On return the tiles' O / LSE (extend) or partial
+// rows (decode) are written by the softmax threads; the caller separates tile
+// sets with a barrier of the tile threads.  A query tile with no rows is
+// skipped entirely, which keeps the barrier phases consistent only for the
+// CTA's last tile set (extend CTAs run one set; decode tiles always have
+// rows).
 template <class C>
 __device__ __forceinline__ void tc_tile_run(const TcArgs& a, const CUtensorMap* tmk, const CUtensorMap* tmv,
                                             const TileInfo& ti, uint8_t* sm, uint32_t tbase, TcState& stt, int tid) {
     using Lay = typename C::Lay;
-    constexpr int D = C::kD, NQ = C::kNQ, NSK = C::kNSK, NSV = C::kNSV;
+    constexpr int D = C::kD, NQ = C::kNQ, NS = C::kNS, NG = C::kNG, BN = C::kBN, NSB = C::kNSB;
+    constexpr int KR = Lay::KREGION;
     constexpr bool DEC = C::kDec;
     const uint32_t sQ = smem_u32(sm + Lay::OFF_Q);
     const uint32_t sK = smem_u32(sm + Lay::OFF_K);
@@ -274,6 +282,8 @@ __device__ __forceinline__ void tc_tile_run(const TcArgs& a, const CUtensorMap* 
     // argument fields in registers (the asm statements below clobber memory,
     // which would otherwise force a reload through the reference each time)
     const bf16* const a_q = a.q;
+    const bf16* const a_kp = a.kp;
+    const bf16* const a_vp = a.vp;
     const int32_t* const a_r2t = a.r2t;
     const int64_t a_ld = a.ld;
     const int32_t* const a_members = a.members;
@@ -287,9 +297,8 @@ __device__ __forceinline__ void tc_tile_run(const TcArgs& a, const CUtensorMap* 
     const float a_scale = a.scale_log2;
     const int warp = tid >> 5, lane = tid & 31;
     const int kv_row = ti.kv_row, kv_begin = ti.kv_begin, kv_end = ti.kv_end, kvh = ti.kvh;
-    const int nb = (kv_end - kv_begin + kBN - 1) / kBN;
+    const int nb = (kv_end - kv_begin + BN - 1) / BN;
     const uint32_t J0 = stt.J;
-    const uint32_t tQ = tbase + 256;
     // after one wait has given up, the tile's results are garbage (flagged):
     // later waits return at once so the CTA finishes promptly
     auto wait = [&](int b, uint32_t par) {
@@ -302,83 +311,100 @@ __device__ __forceinline__ void tc_tile_run(const TcArgs& a, const CUtensorMap* 
 
     if (warp > C::kMmaWarp) {
         // ------------------------------------------------------------ gather
-        const int gw = warp - C::kMmaWarp - 1;     // 0: K, 1: V
+        const int g = warp - C::kMmaWarp - 1;
         if constexpr (!DEC) {
-            // Q: rows 64 gw .. 64 gw + 63 of every query tile (once, 16-byte cp.async)
-            constexpr int CPR = D / 8;             // 16-byte chunks per row
-            constexpr int RPI = 32 / CPR;          // rows per warp instruction
+            // Q: 128 rows per query tile (once, 16-byte cp.async, zero-filled
+            // past the tile's rows)
+            constexpr int CPR = D / 8;
+            constexpr int RPI = 32 / CPR;
+            constexpr int QI = 128 / RPI;
             const int sub = lane / CPR, ch = lane % CPR;
 #pragma unroll
             for (int q = 0; q < NQ; ++q) {
-#pragma unroll
-                for (int k = 0; k < 64 / RPI; ++k) {
-                    const int r = gw * 64 + k * RPI + sub;
-                    const bool ok = r < (q ? ti.rows[1] : ti.rows[0]);
-                    const int64_t qr = ((int64_t)(q ? ti.i6[1] : ti.i6[0]) + r / a_G) * a_Hq + kvh * a_G + r % a_G;
+                const int rq = q ? ti.rows[1] : ti.rows[0], i6q = q ? ti.i6[1] : ti.i6[0];
+                for (int t = g; t < QI; t += NG) {
+                    const int r = t * RPI + sub;
+                    const bool ok = r < rq;
+                    const int64_t qr = ((int64_t)i6q + r / a_G) * a_Hq + kvh * a_G + r % a_G;
                     const bf16* src = ok ? a_q + qr * D + ch * 8 : a_q;
                     cp_async16(sQ + q * Lay::QTILE + sw128(r, ch, kQRegion), src, ok);
                 }
             }
             cp_async_arrive_noinc(bar(C::QFULL));
         }
-        // lane = (half, quad): rows 4 quad .. 4 quad + 3, columns 64 half ..
-        constexpr int H = D / 64;                  // 128-byte halves of a row
-        constexpr int NS = NSK > NSV ? NSK : NSV;
-        const int ns = gw ? NSV : NSK;
-        const int quad = lane & 15, half = lane >> 4;
+        // K and V blocks: NOP TMA gathers each (four rows x 128 bytes: rows
+        // 4 quad .. 4 quad + 3, columns 64 half ..), OPW of them per team warp
+        // (lane l issues op g OPW + l).  Positions past the range re-read the
+        // range's last position (finite data, masked scores), so every row is
+        // inside the pool.
+        constexpr int H = D / 64;
+        constexpr int NOP = BN / 4 * H;
+        constexpr int OPW = (NOP + NG - 1) / NG;
+        static_assert(OPW <= 32, "one gather per lane");
+        const int o = g * OPW + lane;
+        const int nmine = max(0, min(NOP - g * OPW, OPW));   // ops of this warp
+        const bool mine = lane < nmine;
+        const int half = o % H, quad = o / H;
+        const uint32_t bytes = (uint32_t)nmine * 512u;
         const int32_t* trow = a_r2t + (int64_t)kv_row * a_ld;
         int32_t nx[4];
         auto fetch = [&](int j) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const int p = min(kv_begin + j * kBN + 4 * quad + i, kv_end - 1);
-                nx[i] = j < nb ? __ldg(trow + p) : 0;
+                const int p = min(kv_begin + j * BN + 4 * quad + i, kv_end - 1);
+                nx[i] = (mine && j < nb) ? __ldg(trow + p) : 0;
             }
         };
         fetch(0);
-        const CUtensorMap* tm = gw ? tmv : tmk;
-        const uint32_t ring = gw ? sV : sK;
         int issued = 0;
         for (int j = 0; j < nb; ++j) {
             const uint32_t J = J0 + j;
-            const int st = (int)(J % (uint32_t)ns);
-            const uint32_t ph = (J / (uint32_t)ns) & 1u;
+            const int st = (int)(J % (uint32_t)NS);
+            const uint32_t ph = (J / (uint32_t)NS) & 1u;
             int r[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 int32_t sl = nx[i];
                 if (sl < 0 || sl >= a_num_slots) {
-                    if (half == 0) atomicOr(a_err, 1u);
+                    if (mine && half == 0) atomicOr(a_err, 1u);
                     sl = 0;
                 }
                 r[i] = sl * a_Hkv + kvh;
             }
             fetch(j + 1);
-            wait(gw ? C::VEMPTY(st) : C::KEMPTY(st), ph ^ 1u);
-            if (stt.timed_out) break;   // issue nothing into a stage that may be in use
-            const int bfull = gw ? C::VFULL(st) : C::KFULL(st);
-            if (lane == 0) mbar_expect_tx(bar(bfull), (uint32_t)(kBN * D * 2));
-            __syncwarp();
-            if (half < H)
-                tma_gather4(ring + st * Lay::KTILE + half * kKRegion + quad * 512, tm, half * 64, r[0], r[1], r[2],
-                            r[3], bar(bfull));
+            // K rows once S_{j-NS} has read the stage, then V rows once
+            // PV_{j-NS} has: separate waits, so that K of a block never waits
+            // for a PV product (the MMA thread may need that K before it
+            // commits the PV that frees the V stage)
+#pragma unroll
+            for (int part = 0; part < 2; ++part) {
+                wait(part ? C::VEMPTY(st) : C::KEMPTY(st), ph ^ 1u);
+                if (stt.timed_out) break;   // issue nothing into a stage that may be in use
+                const int bfull = part ? C::VFULL(st) : C::KFULL(st);
+                if (lane == 0) mbar_expect_tx(bar(bfull), bytes);
+                __syncwarp();
+                if (mine)
+                    tma_gather4((part ? sV : sK) + st * Lay::KTILE + half * KR + quad * 512, part ? tmv : tmk, half * 64,
+                                r[0], r[1], r[2], r[3], bar(bfull));
+            }
+            if (stt.timed_out) break;
             issued = j + 1;
         }
         // This warp's copies have landed before it leaves the tile (normally
-        // long since: the MMA thread consumed them).  Only this warp arms the
-        // FULL barriers, so the last armed phase of each stage is the one to
+        // long since: the MMA thread consumed them).  A FULL phase needs this
+        // warp's arrival, so the last armed phase of each stage is the one to
         // wait for; the waits are bounded.
-        for (int j = max(0, issued - ns); j < issued; ++j) {
+        for (int j = max(0, issued - NS); j < issued; ++j) {
             const uint32_t J = J0 + j;
-            const int st = (int)(J % (uint32_t)ns);
-            if (!mbar_wait(bar(gw ? C::VFULL(st) : C::KFULL(st)), (J / (uint32_t)ns) & 1u)) atomicOr(a_err, 4u);
+            const int st = (int)(J % (uint32_t)NS);
+            if (!mbar_wait(bar(C::KFULL(st)), (J / (uint32_t)NS) & 1u)) atomicOr(a_err, 4u);
+            if (!mbar_wait(bar(C::VFULL(st)), (J / (uint32_t)NS) & 1u)) atomicOr(a_err, 4u);
         }
-        (void)NS;
         if constexpr (!DEC) asm volatile("cp.async.wait_all;\n" ::: "memory");
     } else if (warp == C::kMmaWarp) {
         // ------------------------------------------------------------ MMA
         if (lane == 0) {
-            constexpr uint32_t IS = idesc_bf16(128, kBN, false);
+            constexpr uint32_t IS = idesc_bf16(128, BN, false);
             constexpr uint32_t IO = idesc_bf16(128, D, true);
             const bool has0 = ti.rows[0] > 0, has1 = NQ > 1 && ti.rows[1] > 0;
             auto has = [&](int q) { return q ? has1 : has0; };
@@ -386,51 +412,62 @@ __device__ __forceinline__ void tc_tile_run(const TcArgs& a, const CUtensorMap* 
             // extend's Q tiles were written by cp.async (generic proxy) and
             // are read by the tensor cores (async proxy)
             if constexpr (!DEC) fence_proxy_async_smem();
-            auto issue_s = [&](int j) {
-                const uint32_t J = J0 + j;
-                const int st = (int)(J % (uint32_t)NSK);
-                wait(C::KFULL(st), (J / (uint32_t)NSK) & 1u);
-                tc_fence_after();
-                const uint32_t kb = sK + st * Lay::KTILE;
+            // S of block j for query tile q into its score buffer
+            auto mma_s = [&](int q, uint32_t J, uint32_t kb) {
+                const uint32_t tS = tbase + 256 * q + (J % NSB) * BN;
 #pragma unroll
-                for (int q = 0; q < NQ; ++q) {
-                    if (!has(q)) continue;
-                    const uint32_t tS = tbase + 256 * q + (J & 1) * 64;
-#pragma unroll
-                    for (int ks = 0; ks < D / 16; ++ks) {
-                        const uint32_t koff = (ks >> 2) * kKRegion + (ks & 3) * 32;
-                        if constexpr (DEC) {
-                            tc_mma_tmem_a(tS, tQ + ks * 8, sdesc(kb + koff, 16, 1024), IS, ks > 0);
-                        } else {
-                            const uint32_t qoff = q * Lay::QTILE + (ks >> 2) * kQRegion + (ks & 3) * 32;
-                            tc_mma(tS, sdesc(sQ + qoff, 16, 1024), sdesc(kb + koff, 16, 1024), IS, ks > 0);
-                        }
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t koff = (ks >> 2) * KR + (ks & 3) * 32;
+                    if constexpr (DEC) {
+                        tc_mma_tmem_a(tS, tbase + C::kQCol + ks * 8, sdesc(kb + koff, 16, 1024), IS, ks > 0);
+                    } else {
+                        const uint32_t qoff = q * Lay::QTILE + (ks >> 2) * kQRegion + (ks & 3) * 32;
+                        tc_mma(tS, sdesc(sQ + qoff, 16, 1024), sdesc(kb + koff, 16, 1024), IS, ks > 0);
                     }
-                    tc_commit(bar(C::SFULL(q, J & 1)));
                 }
-                tc_commit(bar(C::KEMPTY(st)));
+                tc_commit(bar(C::SFULL(q, J % NSB)));
             };
-            if (nb > 0) issue_s(0);
-            if (nb > 1) issue_s(1);
+            auto k_ready = [&](uint32_t J) {
+                wait(C::KFULL(J % NS), (J / NS) & 1u);
+                tc_fence_after();
+                return sK + (J % NS) * Lay::KTILE;
+            };
+            // S lookahead: the first NSB blocks
+            for (int j = 0; j < NSB && j < nb; ++j) {
+                const uint32_t kb = k_ready(J0 + j);
+#pragma unroll
+                for (int q = 0; q < NQ; ++q)
+                    if (has(q)) mma_s(q, J0 + j, kb);
+                tc_commit(bar(C::KEMPTY((J0 + j) % NS)));
+            }
             for (int j = 0; j < nb; ++j) {
                 const uint32_t J = J0 + j;
-                const int st = (int)(J % (uint32_t)NSV);
-                wait(C::VFULL(st), (J / (uint32_t)NSV) & 1u);
+                const int st = (int)(J % (uint32_t)NS);
+                wait(C::VFULL(st), (J / (uint32_t)NS) & 1u);
                 const uint32_t vb = sV + st * Lay::KTILE;
+                // S_{j+NSB} reuses block j's score buffer: issued right after
+                // PV_j (the tensor pipe runs one thread's MMAs in order)
+                const bool next = j + NSB < nb;
+                uint32_t kb = 0u;   // K of block j + NSB, waited for once, after the first PV
 #pragma unroll
                 for (int q = 0; q < NQ; ++q) {
                     if (!has(q)) continue;
-                    wait(C::PFULL(q, J & 1), (J >> 1) & 1);
+                    wait(C::PFULL(q, J % NSB), (J / NSB) & 1u);
                     tc_fence_after();
-                    const uint32_t tP = tbase + 256 * q + (J & 1) * 64;
+                    const uint32_t tP = tbase + 256 * q + (J % NSB) * BN;
 #pragma unroll
-                    for (int kk = 0; kk < kBN / 16; ++kk)
-                        tc_mma_tmem_a(tbase + 256 * q + 128, tP + kk * 8, sdesc(vb + kk * 2048, kKRegion, 1024), IO,
+                    for (int kk = 0; kk < BN / 16; ++kk)
+                        tc_mma_tmem_a(tbase + 256 * q + C::kOCol, tP + kk * 8, sdesc(vb + kk * 2048, KR, 1024), IO,
                                       (j > 0 || kk > 0) ? 1u : 0u);
                     tc_commit(bar(C::OFULL(q)));
+                    if (q == NQ - 1 || !has(NQ - 1)) tc_commit(bar(C::VEMPTY(st)));   // after the block's last PV
+                    if (next) {
+                        if (!kb) kb = k_ready(J + NSB);
+                        mma_s(q, J + NSB, kb);
+                    }
                 }
-                tc_commit(bar(C::VEMPTY(st)));
-                if (j + 2 < nb) issue_s(j + 2);   // into the buffers P_j occupies: runs after PV_j
+                if (!has0 && !has1) tc_commit(bar(C::VEMPTY(st)));   // (no PV at all)
+                if (next) tc_commit(bar(C::KEMPTY((J + NSB) % NS)));
             }
             // every MMA of the tile set has finished before this thread
             // leaves it (the commit covers all earlier MMAs; bounded wait)
@@ -446,13 +483,13 @@ __device__ __forceinline__ void tc_tile_run(const TcArgs& a, const CUtensorMap* 
         const int rows = q ? ti.rows[1] : ti.rows[0], i6 = q ? ti.i6[1] : ti.i6[0], i7 = q ? ti.i7[1] : ti.i7[0];
         const uint32_t lq = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t tl = tbase + 256 * q + lq;
-        const uint32_t tlO = tl + 128;
+        const uint32_t tlO = tl + C::kOCol;
         const int lim = DEC ? 0x7fffffff : i7 + i / a_G;
         const float sc = a_scale;
         float m_used = -INFINITY, l0 = 0.f, l1 = 0.f;   // l = l0 + l1 (packed pair sums)
         if constexpr (DEC) {
             // this row's query (member request i / G, head kvh * G + i % G) into TMEM
-            const uint32_t tlQ = tQ + lq;
+            const uint32_t tlQ = tbase + C::kQCol + lq;
             const bool ok = i < rows;
             const int mem = ok ? __ldg(a_members + i6 + i / a_G) : 0;
             const uint4* src = reinterpret_cast<const uint4*>(a_q + ((int64_t)mem * a_Hq + kvh * a_G + i % a_G) * D);
@@ -472,77 +509,99 @@ __device__ __forceinline__ void tc_tile_run(const TcArgs& a, const CUtensorMap* 
             tc_fence_before();
             mbar_arrive(bar(C::QFULL));
         }
+        // O (rows of this warp) times f, in TMEM
+        auto scale_o = [&](float f) {
+            float v[32];
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                tld32(tlO + 32 * c, v);
+#pragma unroll
+                for (int k = 0; k < 32; ++k) v[k] *= f;
+                tst32(tlO + 32 * c, v);
+            }
+        };
         if (rows > 0) {
             for (int j = 0; j < nb; ++j) {
                 const uint32_t J = J0 + j;
-                const int b = J & 1;
-                wait(C::SFULL(q, b), (J >> 1) & 1);
+                const int b = (int)(J % NSB);
+                wait(C::SFULL(q, b), (J / NSB) & 1u);
                 tc_fence_after();
-                const int pos0 = kv_begin + j * kBN;
-                const bool full_blk = pos0 + kBN - 1 < kv_end && pos0 + kBN - 1 <= lim;
-                float srow[kBN];
-                tld32_nw(tl + b * 64, srow);
-                tld32_nw(tl + b * 64 + 32, srow + 32);
-                tld_wait();
-                // max on the raw scores (the scale is positive), scaled once;
-                // the scale is folded into the exponent's FMA below.  Four
-                // independent chains of 3-input max keep the dependency chain
-                // short.
-                if (!full_blk) {
+                // With one score buffer, S_j was issued after PV_{j-1}: O is
+                // final for blocks < j.  With two, a warp that rescales waits
+                // for PV_{j-1} first (the OFULL barrier cannot run two phases
+                // ahead of this wait: its next phase needs this warp's P_j).
+                bool o_ready = NSB == 1 || j == 0;
+                const uint32_t tS = tl + b * BN;
+                // the block in 64-column halves: max, then 2^(s sc - m) as bf16
+                // pairs into the block's first BN / 2 columns
+#pragma unroll 1
+                for (int h = 0; h < BN / 64; ++h) {
+                    const int pos0 = kv_begin + j * BN + 64 * h;
+                    const bool full_blk = pos0 + 63 < kv_end && pos0 + 63 <= lim;
+                    float srow[64];
+                    tld32_nw(tS + 64 * h, srow);
+                    tld32_nw(tS + 64 * h + 32, srow + 32);
+                    tld_wait();
+                    // max on the raw scores (the scale is positive), scaled
+                    // once; four independent chains of 3-input max
+                    if (!full_blk) {
 #pragma unroll
-                    for (int k = 0; k < kBN; ++k) {
-                        const int pos = pos0 + k;
-                        srow[k] = (pos < kv_end && pos <= lim) ? srow[k] : -INFINITY;
+                        for (int k = 0; k < 64; ++k) {
+                            const int pos = pos0 + k;
+                            srow[k] = (pos < kv_end && pos <= lim) ? srow[k] : -INFINITY;
+                        }
                     }
-                }
-                float mc[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                    float mc[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                for (int k = 0; k < kBN; k += 8) {
+                    for (int k = 0; k < 64; k += 8) {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) mc[c] = fmax3f(mc[c], srow[k + 2 * c], srow[k + 2 * c + 1]);
-                }
-                const float mx = fmax3f(mc[0], mc[1], fmaxf(mc[2], mc[3])) * sc;
-                const float m_new = fmaxf(m_used, mx);
-                const bool need = m_new > m_used + 8.f;   // also true for the first finite max
-                const float m_old = m_used;
-                if (need) {
-                    if (m_used != -INFINITY) {
-                        const float f = exp2f(m_used - m_new);
+                        for (int c = 0; c < 4; ++c) mc[c] = fmax3f(mc[c], srow[k + 2 * c], srow[k + 2 * c + 1]);
+                    }
+                    const float mx = fmax3f(mc[0], mc[1], fmaxf(mc[2], mc[3])) * sc;
+                    const float m_new = fmaxf(m_used, mx);
+                    const bool need = m_new > m_used + 8.f;   // also true for the first finite max
+                    const bool resc = need && m_used != -INFINITY;
+                    if (__any_sync(0xffffffffu, resc)) {
+                        const float f = resc ? exp2f(m_used - m_new) : 1.f;
                         l0 *= f;
                         l1 *= f;
-                    }
-                    m_used = m_new;
-                }
-                const float nmu = m_used == -INFINITY ? 0.f : -m_used;
-                // p = 2^(s sc - m): one packed FMA per pair, one MUFU op each,
-                // one packed add into the pair sums, one conversion per pair
-                uint32_t pk[kBN / 2];
+                        // O holds blocks < j at the old max
+                        if (j > 0) {
+                            if (!o_ready) {
+                                wait(C::OFULL(q), (J - 1) & 1);
+                                tc_fence_after();
+                                o_ready = true;
+                            }
+                            scale_o(f);
+                        }
+                        // this block's earlier halves are at the old max too
+                        for (int h2 = 0; h2 < h; ++h2) {
+                            uint32_t w[32];
+                            tld32_nw(tS + 32 * h2, reinterpret_cast<float*>(w));
+                            tld_wait();
 #pragma unroll
-                for (int k = 0; k < kBN; k += 2) {
-                    float x0, x1;
-                    ffma2_sc(x0, x1, srow[k], srow[k + 1], sc, nmu);
-                    const float p0 = ex2_ftz(x0), p1 = ex2_ftz(x1);   // -inf -> 0
-                    fadd2_acc(l0, l1, p0, p1);
-                    pk[k / 2] = pack_bf16(p0, p1);
-                }
-                tst32u(tl + b * 64, pk);                         // P_j over the consumed scores
-                // O holds blocks < j scaled to the old max: a warp with a row
-                // whose max grew rescales its rows once PV_{j-1} has finished.
-                // Other warps do not touch O and go on without waiting: the
-                // OFULL barrier cannot run two phases ahead of a waiter (its
-                // next phase needs this warp's P_j), so skipped waits are safe.
-                if (j > 0 && __any_sync(0xffffffffu, need && m_old != -INFINITY)) {
-                    wait(C::OFULL(q), (J - 1) & 1);
-                    tc_fence_after();
-                    const float al = (need && m_old != -INFINITY) ? exp2f(m_old - m_new) : 1.f;
-                    float v[32];
-#pragma unroll 1
-                    for (int c = 0; c < D / 32; ++c) {
-                        tld32(tlO + 32 * c, v);
-#pragma unroll
-                        for (int k = 0; k < 32; ++k) v[k] *= al;
-                        tst32(tlO + 32 * c, v);
+                            for (int k = 0; k < 32; ++k) {
+                                const __nv_bfloat162 v2 = *reinterpret_cast<const __nv_bfloat162*>(&w[k]);
+                                w[k] = pack_bf16(__low2float(v2) * f, __high2float(v2) * f);
+                            }
+                            tst32u(tS + 32 * h2, w);
+                        }
                     }
+                    if (need) m_used = m_new;
+                    const float nmu = m_used == -INFINITY ? 0.f : -m_used;
+                    // p = 2^(s sc - m): one packed FMA per pair, one MUFU op
+                    // each, one packed add into the pair sums, one conversion
+                    // per pair
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int k = 0; k < 64; k += 2) {
+                        float x0, x1;
+                        ffma2_sc(x0, x1, srow[k], srow[k + 1], sc, nmu);
+                        const float p0 = ex2_ftz(x0), p1 = ex2_ftz(x1);   // -inf -> 0
+                        fadd2_acc(l0, l1, p0, p1);
+                        pk[k / 2] = pack_bf16(p0, p1);
+                    }
+                    tst32u(tS + 32 * h, pk);   // P over scores already read
                 }
                 tc_fence_before();
                 mbar_arrive(bar(C::PFULL(q, b)));
