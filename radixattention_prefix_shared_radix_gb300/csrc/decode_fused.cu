@@ -69,7 +69,7 @@ using namespace tc;
 
 constexpr int kConsumers = kDecNarrowWarps;              // streaming consumer warps per CTA
 constexpr int kProducers = kConsumers;                   // one per consumer
-constexpr int kNS = 4;                                   // ring stages per consumer (tile CTA)
+constexpr int kNS = 2;                                   // ring stages per consumer (tile CTA: beside the tiles' K/V rings)
 constexpr int kNSF = 4;                                  // ring stages per consumer (streaming CTA)
 constexpr int kNP = 16;                                  // KV positions per step
 constexpr int kQD = 6;                                   // slot lookups ahead (steps per consumer)
@@ -173,6 +173,9 @@ __device__ __noinline__ void stream_producer(const FusedArgs& f, int gw, uint32_
     const DecItem* const pieces = f.narrow;
     const int n_narrow = f.n_narrow;
     uint32_t* const sched = f.sched;
+    // streamed K/V rows are read once: evict them from L2 first, which keeps
+    // the code, the tables and the partial rows there across calls
+    const uint64_t kv_pol = l2_evict_first_policy();
 
     // next-piece pipeline: 0 take a number, 1 number in flight (lane 0),
     // 2 record in flight, 3 members / seq_len in flight, 4 ready;
@@ -232,6 +235,8 @@ __device__ __noinline__ void stream_producer(const FusedArgs& f, int gw, uint32_
 
     // slot cursor over the current piece
     bool have = false, done = false;
+    bool prologue = true;   // the first kQD lookups: no grab-ahead, which would put the next piece's
+                            // dependent loads (counter, record, members) before the first step
     int row = 0, e = 0, h = 0, sp = 0, nlook = 0;
     auto look_up = [&]() {
         const int ent = nlook & (kSQ - 1);
@@ -288,13 +293,16 @@ __device__ __noinline__ void stream_producer(const FusedArgs& f, int gw, uint32_
         // Take the next number only near the end of the current piece: the
         // counter then runs dry only when the work does, and CTAs that join
         // late (tile CTAs) still find pieces.
-        if (nx_stage != 0 || !have || done || (e - sp + kNP - 1) / kNP <= kGrabAhead) advance();
+        if (!prologue && (nx_stage != 0 || !have || done || (e - sp + kNP - 1) / kNP <= kGrabAhead)) advance();
     };
+    // one cp.async group per step's lookup: the first step waits for its
+    // own slots only
 #pragma unroll 1
-    for (int k = 0; k < kQD; ++k) look_up();
-    cp_async_commit();
-    cp_async_wait<0>();
-    __syncwarp();
+    for (int k = 0; k < kQD; ++k) {
+        look_up();
+        cp_async_commit();
+    }
+    prologue = false;
 
     bool timed_out = false;
     int nq = 0;   // pieces started (Q slot uses)
@@ -327,8 +335,8 @@ __device__ __noinline__ void stream_producer(const FusedArgs& f, int gw, uint32_
                 const int rl = k * RPI + lane / CPR;
                 const int32_t sr = __shfl_sync(0xffffffffu, sl, rl);
                 const int64_t off = sr >= 0 ? ((int64_t)sr * Hkv + kvh) * D + ch * 8 : 0;
-                cp_async16(kd + swz<D>(rl, ch), kp + off, sr >= 0);
-                cp_async16(vd + swz<D>(rl, ch), vp + off, sr >= 0);
+                cp_async16_pol(kd + swz<D>(rl, ch), kp + off, sr >= 0, kv_pol);
+                cp_async16_pol(vd + swz<D>(rl, ch), vp + off, sr >= 0, kv_pol);
             }
             if (flags & kFirst) {
                 // the piece's query rows (at most 8) into Q slot nq & 1, swizzled
@@ -566,6 +574,11 @@ __global__ void __maxnreg__(128) decode_fused_kernel(const __grid_constant__ Fus
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // launched as a programmatic dependent of the previous kernel in the
+    // stream: everything before its completion is visible after this wait;
+    // the merge launch may be scheduled from now on (it waits for this grid)
+    grid_dep_wait();
+    grid_dep_launch();
     const int w0 = __ldg(f.wptr + blockIdx.x), w1 = __ldg(f.wptr + blockIdx.x + 1);
     const bool tiles = w1 > w0;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + TL::OFF_TMEM);
@@ -682,14 +695,28 @@ int launch_decode_fused(const sgl_plan* plan, const void* q, const void* kp, con
     f.n_init = plan->n_init;
     f.n_tile_ctas = plan->n_tile_ctas;
     f.sched = reinterpret_cast<uint32_t*>(ws + plan->off_sched);
-    decode_fused_kernel<D><<<plan->n_ctas, kFusedThreads, Lay::TOTAL, s>>>(f, mk, mv);
-    int e = (int)cudaGetLastError();
+    // Both launches are programmatic dependents of the kernel before them:
+    // each waits (griddepcontrol.wait) before its first memory access, so
+    // only the launch and scheduling overlap the previous grid's tail.
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)plan->n_ctas);
+    cfg.blockDim = dim3(kFusedThreads);
+    cfg.dynamicSmemBytes = Lay::TOTAL;
+    cfg.stream = s;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    int e = (int)cudaLaunchKernelEx(&cfg, decode_fused_kernel<D>, f, mk, mv);
     if (e) return e;
     MergeArgs m{a.po, a.plse, reinterpret_cast<const int32_t*>(ws + plan->off_mptr),
                 reinterpret_cast<const int32_t*>(ws + plan->off_ment), o, lse, a.Hq, a.Hkv, a.G};
     const int n_pairs = p.batch * a.Hkv;
-    decode_merge_kernel<bf16, D><<<(n_pairs * a.G + 3) / 4, 128, 0, s>>>(m, n_pairs);
-    return (int)cudaGetLastError();
+    cfg.gridDim = dim3((unsigned)((n_pairs * a.G + 3) / 4));
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    return (int)cudaLaunchKernelEx(&cfg, decode_merge_kernel<bf16, D>, m, n_pairs);
 }
 
 template int launch_decode_fused<64>(const sgl_plan*, const void*, const void*, const void*, const int32_t*, int64_t,

@@ -25,6 +25,27 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool v
     const int n = valid ? 16 : 0;
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(n) : "memory");
 }
+// Programmatic dependent launch: wait until the grids this one depends on
+// have completed and their writes are visible (a no-op without such a
+// dependency), and let the grids that depend on this one be scheduled now
+// (they wait in turn before touching memory).
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+
+// An L2 policy that evicts the lines it tags first: for data read exactly
+// once, so that it does not push the kernels' code and tables out of L2.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(pol));
+    return pol;
+}
+// cp_async16 with an L2 cache policy.
+__device__ __forceinline__ void cp_async16_pol(uint32_t dst, const void* src, bool valid, uint64_t pol) {
+    const int n = valid ? 16 : 0;
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;\n" ::"r"(dst), "l"(src), "r"(n),
+                 "l"(pol)
+                 : "memory");
+}
 // 4-byte copy (cached in L1), no zero fill.
 __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(dst), "l"(src) : "memory");

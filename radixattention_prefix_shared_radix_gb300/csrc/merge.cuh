@@ -19,6 +19,8 @@
 
 namespace sgl {
 
+using sgldev::grid_dep_launch;
+using sgldev::grid_dep_wait;
 using sgldev::kLog2e;
 using sgldev::pack_bf16;
 
@@ -111,6 +113,8 @@ __device__ __noinline__ void merge_head(const MergeArgs& m, int idx, int j, int 
 // for the entry rows, then the partial rows and LSEs together.
 template <typename OutT, int D>
 __global__ void __launch_bounds__(128) decode_merge_kernel(const MergeArgs m, int n_pairs) {
+    grid_dep_wait();     // the partials of the launch before
+    grid_dep_launch();
     const int w = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     const int idx = w / m.G, j = w - idx * m.G;
     if (idx >= n_pairs) return;

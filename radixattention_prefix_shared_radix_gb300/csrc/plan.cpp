@@ -135,10 +135,10 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
     // their tiles are done (so the two never compete for an SM's issue slots
     // and instruction cache); the other CTAs stream from the start.  Chunk
     // length and tile CTA count come from a cost model of this kernel on
-    // GB300 (measured): a tile costs ~6 us plus ~1 us per 64-position block;
-    // a streaming SM handles ~82 (d=128) position-heads per us after ~5 us
-    // of start-up.  The chunk length with the earliest estimated finish is
-    // taken (tile CTAs at most half the CTAs).
+    // GB300 (measured): a tile costs ~2 us plus ~2.5 us per 128-position
+    // block; a streaming SM handles ~64 (d=128) position-heads per us after
+    // ~6 us of start-up.  The chunk length with the earliest estimated finish
+    // is taken (tile CTAs at most half the CTAs).
     auto wide_items_for = [&](int64_t Cw) {
         int64_t n = 0;
         for (int32_t s = 0; s < nseg; ++s) {
@@ -148,7 +148,7 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
         }
         return n;
     };
-    const double rate = 82.0 * 128.0 / p->head_dim;   // streamed position-heads per us per SM
+    const double rate = 64.0 * 128.0 / p->head_dim;   // streamed position-heads per us per SM
     int64_t Cw = 128, n_tile_ctas = 0;
     if (max_wide > 0) {
         double best = 1e300;
@@ -157,10 +157,10 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
             const int64_t nw = wide_items_for(c);
             const int64_t T = std::max<int64_t>(1, std::min<int64_t>(nw, n_ctas / 2));
             const double per = (double)((nw + T - 1) / T);
-            const double tile_us = per * (6.0 + (double)c / 64.0);
+            const double tile_us = per * (2.0 + 2.5 * (double)c / 128.0);
             // streaming CTAs work from ~5 us; a tile CTA streams only what is
             // left when its tiles are done, which the estimate ignores
-            const double F = std::max(tile_us, 5.0 + (double)units_n /
+            const double F = std::max(tile_us, 6.0 + (double)units_n /
                                                      ((double)std::max<int64_t>(1, n_ctas - T) * rate));
             if (F < best) {
                 best = F;

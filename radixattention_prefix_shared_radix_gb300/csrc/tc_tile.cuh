@@ -217,11 +217,11 @@ struct TcCfg {
     static_assert(kNumBars <= 48, "barrier area");
 };
 
-// The decode tiles' configuration: one query tile with Q in TMEM, 64-position
-// blocks, two score buffers, two K/V stages (the tile CTAs leave most of
-// their shared memory to their streaming warps), a gather team of six warps.
+// The decode tiles' configuration: one query tile with Q in TMEM, 128-position
+// blocks (S MMAs of N = 128), two score buffers so that the softmax of block
+// j + 1 overlaps PV_j and S_{j+2}, two K/V stages, a gather team of six warps.
 template <int D>
-using DecCfg = TcCfg<D, true, 1, 2, 6, 64, 2>;
+using DecCfg = TcCfg<D, true, 1, 2, 6, 128, 2>;
 
 struct TileInfo {
     int kv_row, kv_begin, kv_end, kvh;
