@@ -185,15 +185,17 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
         }
     }
 
-    // Narrow units are cut into pieces of at most Pmax positions (about two
-    // pieces per streaming consumer; a cut makes one more partial to merge),
+    // Narrow units are cut into pieces of at most Pmax positions (about one
+    // even share of a streaming consumer: measured on GB300, half that size
+    // cost ~1 us more per call in per-piece work, 0.6 of it starved the
+    // tail; a cut makes one more partial to merge),
     // no piece shorter than one 16-position step unless its unit is, ordered
     // longest first.  Each consumer of a streaming CTA starts on its own
     // piece; the rest (and all work of tile CTAs' consumers, once their tiles
     // are done) are handed out at run time from a counter, so SMs that stream
     // faster take more.
     const int64_t n_cons = (n_ctas - n_tile_ctas) * sgl::kDecNarrowWarps;
-    int64_t Pmax = (int64_t)std::ceil((double)units_n / (2.0 * (double)std::max<int64_t>(1, n_cons)));
+    int64_t Pmax = (int64_t)std::ceil((double)units_n / (double)std::max<int64_t>(1, n_cons));
     Pmax = std::min<int64_t>(1024, std::max<int64_t>(64, (Pmax + 15) / 16 * 16));
     std::vector<sgl::DecItem> narrow;
     for (const Unit& u : units) {
