@@ -486,10 +486,31 @@ def bench_extend(sgl, W, torch, steps, bf16_peak):
     pairs = sum(int(ext[r]) * int(pre[r]) + int(ext[r]) * (int(ext[r]) + 1) // 2 for r in range(len(seqs)))
     flops = 4.0 * w.d * w.Hq * pairs
     tflops = flops / (ms / 1e3) / 1e12
+
+    # the same step with the KV write fused in (new K/V scattered into the
+    # pool by the extend kernel itself)
+    kf, vf = W.make_new_kv(w, int(ext.sum()))
+    kn, vn = W.to_dtype(w, kf).cuda(), W.to_dtype(w, vf).cuda()
+
+    def call_kv():
+        sgl.sgl_extend_attn_kvwrite(q, kn, vn, kd, vd, table, pre_d, ext_d, p, o, lse, ws)
+
+    for _ in range(3):
+        call_kv()
+    torch.cuda.synchronize()
+    sgl.sgl_check(ws)
+    e0.record()
+    for _ in range(steps):
+        call_kv()
+    e1.record()
+    torch.cuda.synchronize()
+    ms_kv = e0.elapsed_time(e1) / steps
     return {"workload": EXTEND_WORKLOAD, "tflops": tflops, "ms_per_call": ms, "gflop_per_call": flops / 1e9,
             "roofline": {"bound": "tensor", "achieved": tflops, "peak": bf16_peak, "unit": "TFLOP/s",
                          "frac": tflops / bf16_peak, "peak_source": "measured bf16 burst"},
-            "tokens_per_s": int(ext.sum()) / (ms / 1e3), "steps": steps}
+            "tokens_per_s": int(ext.sum()) / (ms / 1e3), "steps": steps,
+            "kv_write_fused": {"ms_per_call": ms_kv, "tflops": flops / (ms_kv / 1e3) / 1e12,
+                               "kv_bytes_written": int(kn.numel() * 2 * 2)}}
 
 
 def profile_traffic(kernel):

@@ -291,6 +291,28 @@ int sgl_extend_attn(const void* q_new, const void* k_pool, const void* v_pool, c
                     const sgl_attn_params* params, void* o, float* lse, void* workspace, size_t ws_bytes,
                     sgl_stream_t stream);
 
+/* Extend attention with the KV write fused in (chunked prefill step).
+ *   k_new, v_new device [N, Hkv, d] (dtype), rows ordered like q_new: the
+ *                new tokens' K and V, which this call stores into
+ *   k_pool, v_pool device [num_slots, Hkv, d] at the slots
+ *                req_to_token[r, prefix_lens[r] + i] (caller-owned; the rest
+ *                of the pool is only read)
+ * Otherwise as sgl_extend_attn, whose result this call equals after the
+ * same rows have been written: new token i of request r attends to the
+ * cached positions 0..prefix_lens[r]-1 (read from the pool) and to new
+ * tokens 0..i (read from k_new / v_new directly in the bf16 path; the fp32
+ * path writes the pool first and reads it).  An out-of-pool slot is not
+ * written and sets SGL_ERR_BOUNDS for sgl_check.  Repeated calls over the
+ * chunks of a long prompt (prefix_lens = tokens already cached) are a
+ * chunked prefill.
+ * ["SGLang 深度解读" "5. Attention 层": the new tokens' K/V are stored into
+ * token_to_kv_pool at their req_to_token slots before attention;
+ * "SGLang：从前端 DSL 到 SRT 服务运行时": chunked prefill] */
+int sgl_extend_attn_kvwrite(const void* q_new, const void* k_new, const void* v_new, void* k_pool, void* v_pool,
+                            const int32_t* req_to_token, int64_t ld, const int32_t* prefix_lens,
+                            const int32_t* extend_lens, const sgl_attn_params* params, void* o, float* lse,
+                            void* workspace, size_t ws_bytes, sgl_stream_t stream);
+
 /* Wait for `stream`, read the workspace's error word and clear it.
  * SGL_OK, or SGL_ERR_BOUNDS if a kernel skipped an out-of-range slot or a
  * position beyond seq_lens since the word was last cleared. */

@@ -15,7 +15,10 @@ Sources (page title, section):
     sketches and are not followed; only what they compute is).
   * "SGLang：从前端 DSL 到 SRT 服务运行时", section "用基数树实现前缀复用": a
     shared prefix is computed once and referenced many times -- the basis of
-    ``decode_attention_shared``, which must equal ``decode_attention``.
+    ``decode_attention_shared``, which must equal ``decode_attention``; and
+    its chunked prefill (a long prompt cut into pieces, each prefilled on top
+    of the pieces before it) -- the basis of ``extend_attention_kvwrite``
+    called chunk by chunk.
 
 Definitions (plain softmax attention; readings listed in the design doc):
   s_j  = sm_scale * <q[r, h], K[slot(r, j), h // G]>,  j < seq_len[r]
@@ -180,3 +183,56 @@ def extend_attention(q_new, k_pool, v_pool, req_to_token, prefix_lens, extend_le
                     q_new[row0 + i, h], K[:p + 1, h // G], V[:p + 1, h // G], sm_scale)
         row0 += ext
     return O, LSE
+
+
+def kv_write(k_pool, v_pool, k_new, v_new, req_to_token, prefix_lens, extend_lens):
+    """Store the new tokens' K/V into the pool ("SGLang 深度解读", section
+    "5. Attention 层": K/V go to token_to_kv_pool at their req_to_token slots
+    before attention).
+
+    k_pool, v_pool: numpy arrays [S, Hkv, d] (modified in place, any dtype);
+    k_new, v_new [N, Hkv, d] rows ordered request by request; new token i of
+    request r goes to slot req_to_token[r, prefix_lens[r] + i].
+    """
+    table = np.asarray(req_to_token)
+    row = 0
+    for r in range(len(prefix_lens)):
+        pre, ext = int(prefix_lens[r]), int(extend_lens[r])
+        for i in range(ext):
+            slot = int(table[r, pre + i])
+            k_pool[slot] = k_new[row]
+            v_pool[slot] = v_new[row]
+            row += 1
+    return k_pool, v_pool
+
+
+class _Overlay:
+    """Rows of ``base`` with some slots replaced (a pool after a KV write,
+    without copying the whole pool)."""
+
+    def __init__(self, base, slots, rows):
+        self.base = base
+        self.new = {int(s): np.asarray(r, dtype=np.float64) for s, r in zip(slots, rows)}
+
+    def __getitem__(self, slots):
+        slots = np.asarray(slots, dtype=np.int64)
+        out = np.array(_rows(self.base, slots), dtype=np.float64)
+        for j, s in enumerate(slots):
+            if int(s) in self.new:
+                out[j] = self.new[int(s)]
+        return out
+
+
+def extend_attention_kvwrite(q_new, k_new, v_new, k_pool, v_pool, req_to_token, prefix_lens, extend_lens,
+                             sm_scale=None, rows=None):
+    """Extend with the KV write first: ``kv_write`` of the new rows, then
+    ``extend_attention`` over the written pool (the pool itself is not
+    modified; the written rows are overlaid)."""
+    table = np.asarray(req_to_token)
+    slots = []
+    for r in range(len(prefix_lens)):
+        pre, ext = int(prefix_lens[r]), int(extend_lens[r])
+        slots.extend(int(table[r, pre + i]) for i in range(ext))
+    kn, vn = _f64(k_new), _f64(v_new)
+    return extend_attention(q_new, _Overlay(k_pool, slots, kn), _Overlay(v_pool, slots, vn), table, prefix_lens,
+                            extend_lens, sm_scale=sm_scale, rows=rows)

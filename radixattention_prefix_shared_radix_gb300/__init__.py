@@ -90,6 +90,8 @@ _SIGS = {
     "sgl_extend_workspace_bytes": (ctypes.c_int, [ctypes.POINTER(SglAttnParams), ctypes.POINTER(ctypes.c_size_t)]),
     "sgl_extend_attn": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_int64, _P, _P, ctypes.POINTER(SglAttnParams),
                                        _P, _P, _P, ctypes.c_size_t, _P]),
+    "sgl_extend_attn_kvwrite": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, ctypes.c_int64, _P, _P,
+                                               ctypes.POINTER(SglAttnParams), _P, _P, _P, ctypes.c_size_t, _P]),
     "sgl_check": (ctypes.c_int, [_P, _P]),
     "sgl_decode_attn_noalloc": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_int64, _P, _P, _P, _P, _P]),
 }
@@ -344,6 +346,17 @@ def sgl_extend_attn(q_new, k_pool, v_pool, req_to_token, prefix_lens, extend_len
                                _dev(prefix_lens, "prefix_lens"), _dev(extend_lens, "extend_lens"),
                                ctypes.byref(params), _dev(o, "o"), _dev(lse, "lse"), _dev(workspace, "workspace"),
                                workspace.numel() * workspace.element_size(), _stream(stream)), "sgl_extend_attn")
+
+
+def sgl_extend_attn_kvwrite(q_new, k_new, v_new, k_pool, v_pool, req_to_token, prefix_lens, extend_lens, params, o,
+                            lse, workspace, stream=None):
+    _ok(_lib().sgl_extend_attn_kvwrite(_dev(q_new, "q_new"), _dev(k_new, "k_new"), _dev(v_new, "v_new"),
+                                       _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"),
+                                       _dev(req_to_token, "req_to_token"), req_to_token.shape[1],
+                                       _dev(prefix_lens, "prefix_lens"), _dev(extend_lens, "extend_lens"),
+                                       ctypes.byref(params), _dev(o, "o"), _dev(lse, "lse"),
+                                       _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+                                       _stream(stream)), "sgl_extend_attn_kvwrite")
 
 
 def sgl_check(workspace, stream=None):

@@ -39,9 +39,10 @@ int launch_decode_fused(const sgl_plan* plan, const void* q, const void* kp, con
                         int64_t ld, const int32_t* seq_lens, void* o, float* lse, unsigned char* ws, float scale_log2,
                         cudaStream_t s);
 template <int D>
-int launch_extend_tc(const void* q, const void* kp, const void* vp, const int32_t* r2t, int64_t ld,
-                     const int32_t* pre, const int32_t* ext, int B, int64_t n_rows, int64_t tiles, void* o, float* lse,
-                     uint32_t* err, int Hq, int Hkv, int64_t num_slots, float scale_log2, cudaStream_t s);
+int launch_extend_tc(const void* q, const void* kp, const void* vp, const void* kn, const void* vn, void* kw, void* vw,
+                     const int32_t* r2t, int64_t ld, const int32_t* pre, const int32_t* ext, int B, int64_t n_rows,
+                     int64_t tiles, void* o, float* lse, uint32_t* err, int Hq, int Hkv, int64_t num_slots,
+                     float scale_log2, cudaStream_t s);
 }  // namespace sgl
 
 namespace {
@@ -171,6 +172,38 @@ __global__ void __launch_bounds__(128)
     if (lane == 0) lse[nrow * Hq + h] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
 }
 
+// KV write (fp32 path): new token i of request r -> pool slot
+// req_to_token[r, prefix_len + i], for K and V, `rb` bytes per (token, head)
+// row, one thread per 16-byte chunk.  Out-of-pool slots are skipped and set
+// bit 0 of the error word.
+__global__ void kv_scatter(const uint4* __restrict__ kn, const uint4* __restrict__ vn, uint4* __restrict__ kw,
+                           uint4* __restrict__ vw, const int32_t* __restrict__ r2t, int64_t ld,
+                           const int32_t* __restrict__ pre, const int32_t* __restrict__ ext, int B, int64_t n_rows,
+                           int Hkv, int chunks, int64_t num_slots, uint32_t* err) {
+    const int64_t per_row = (int64_t)Hkv * chunks;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n_rows * per_row * 2;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const bool v = i >= n_rows * per_row;
+        const int64_t k = v ? i - n_rows * per_row : i;
+        const int64_t row = k / per_row, within = k - row * per_row;
+        // request of this new-token row
+        int r = 0;
+        int64_t acc = 0;
+        for (; r < B; ++r) {
+            const int e = __ldg(ext + r);
+            if (row < acc + e) break;
+            acc += e;
+        }
+        if (r >= B) continue;
+        const int32_t sl = __ldg(r2t + (int64_t)r * ld + __ldg(pre + r) + (row - acc));
+        if (sl < 0 || sl >= num_slots) {
+            if (within == 0) atomicOr(err, 1u);
+            continue;
+        }
+        (v ? vw : kw)[(int64_t)sl * per_row + within] = (v ? vn : kn)[row * per_row + within];
+    }
+}
+
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
@@ -218,9 +251,9 @@ int launch_decode(const sgl_plan* plan, const void* q, const void* kp, const voi
 }
 
 template <int D>
-int launch_extend(const sgl_attn_params* p, const void* q, const void* kp, const void* vp, const int32_t* r2t,
-                  int64_t ld, const int32_t* pre, const int32_t* ext, void* o, float* lse, uint32_t* err,
-                  cudaStream_t s) {
+int launch_extend(const sgl_attn_params* p, const void* q, const void* kp, const void* vp, const void* kn,
+                  const void* vn, void* kw, void* vw, const int32_t* r2t, int64_t ld, const int32_t* pre,
+                  const int32_t* ext, void* o, float* lse, uint32_t* err, cudaStream_t s) {
     const int Hq = p->num_qo_heads, Hkv = p->num_kv_heads, G = Hq / Hkv, B = p->batch;
     const float sl2 = scale_log2_of(p);
     int64_t total_rows = 0, tiles = 0;
@@ -232,10 +265,17 @@ int launch_extend(const sgl_attn_params* p, const void* q, const void* kp, const
     if (total_rows == 0) return SGL_OK;
     if (p->dtype == SGL_DTYPE_BF16) {
         if (tiles > INT32_MAX) return SGL_ERR_UNSUPPORTED;
-        int e = sgl::launch_extend_tc<D>(q, kp, vp, r2t, ld, pre, ext, B, total_rows, tiles, o, lse, err, Hq, Hkv,
-                                         p->num_slots, sl2, s);
+        int e = sgl::launch_extend_tc<D>(q, kp, vp, kn, vn, kw, vw, r2t, ld, pre, ext, B, total_rows, tiles, o, lse,
+                                         err, Hq, Hkv, p->num_slots, sl2, s);
         if (e) return cuda_status(static_cast<cudaError_t>(e));
     } else {
+        if (kn) {
+            // the new K/V into the pool first (the exact path reads the pool)
+            const int chunks = D * 4 / 16;
+            kv_scatter<<<1024, 256, 0, s>>>(static_cast<const uint4*>(kn), static_cast<const uint4*>(vn),
+                                            static_cast<uint4*>(kw), static_cast<uint4*>(vw), r2t, ld, pre, ext, B,
+                                            total_rows, Hkv, chunks, p->num_slots, err);
+        }
         const int64_t warps = total_rows * Hq;
         if ((warps + 3) / 4 > INT32_MAX) return SGL_ERR_UNSUPPORTED;
         extend_f32<D><<<static_cast<unsigned>((warps + 3) / 4), 128, 0, s>>>(
@@ -284,9 +324,10 @@ int sgl_decode_attn(const void* q, const void* k_pool, const void* v_pool, const
     return launch_decode<64>(plan, q, k_pool, v_pool, req_to_token, ld, seq_lens, o, lse, ws, s);
 }
 
-int sgl_extend_attn(const void* q_new, const void* k_pool, const void* v_pool, const int32_t* req_to_token,
-                    int64_t ld, const int32_t* prefix_lens, const int32_t* extend_lens, const sgl_attn_params* params,
-                    void* o, float* lse, void* workspace, size_t ws_bytes, sgl_stream_t stream) {
+static int extend_impl(const void* q_new, const void* k_new, const void* v_new, const void* k_pool,
+                       const void* v_pool, void* k_pool_w, void* v_pool_w, const int32_t* req_to_token, int64_t ld,
+                       const int32_t* prefix_lens, const int32_t* extend_lens, const sgl_attn_params* params, void* o,
+                       float* lse, void* workspace, size_t ws_bytes, sgl_stream_t stream) {
     int st = sgl::check_params(params);
     if (st) return st;
     const int32_t B = params->batch;
@@ -299,16 +340,34 @@ int sgl_extend_attn(const void* q_new, const void* k_pool, const void* v_pool, c
         rows += params->host_extend_lens[r];
     }
     if (rows > 0 && (!q_new || !k_pool || !v_pool || !req_to_token || !o || !lse)) return SGL_ERR_INVALID_ARG;
+    if (rows > 0 && k_new && (!v_new || !aligned(k_new, 16) || !aligned(v_new, 16))) return SGL_ERR_INVALID_ARG;
+    if (rows * params->num_kv_heads > INT32_MAX) return SGL_ERR_UNSUPPORTED;
     if (!workspace || !aligned(workspace, sgl::kWsAlign) || ws_bytes < sgl::kWsAlign) return SGL_ERR_WORKSPACE;
     if (!aligned(q_new, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(o, 16))
         return SGL_ERR_INVALID_ARG;
     auto s = reinterpret_cast<cudaStream_t>(stream);
     uint32_t* err = static_cast<uint32_t*>(workspace);
     if (params->head_dim == 128)
-        return launch_extend<128>(params, q_new, k_pool, v_pool, req_to_token, ld, prefix_lens, extend_lens, o, lse,
-                                  err, s);
-    return launch_extend<64>(params, q_new, k_pool, v_pool, req_to_token, ld, prefix_lens, extend_lens, o, lse, err,
-                             s);
+        return launch_extend<128>(params, q_new, k_pool, v_pool, k_new, v_new, k_pool_w, v_pool_w, req_to_token, ld,
+                                  prefix_lens, extend_lens, o, lse, err, s);
+    return launch_extend<64>(params, q_new, k_pool, v_pool, k_new, v_new, k_pool_w, v_pool_w, req_to_token, ld,
+                             prefix_lens, extend_lens, o, lse, err, s);
+}
+
+int sgl_extend_attn(const void* q_new, const void* k_pool, const void* v_pool, const int32_t* req_to_token,
+                    int64_t ld, const int32_t* prefix_lens, const int32_t* extend_lens, const sgl_attn_params* params,
+                    void* o, float* lse, void* workspace, size_t ws_bytes, sgl_stream_t stream) {
+    return extend_impl(q_new, nullptr, nullptr, k_pool, v_pool, nullptr, nullptr, req_to_token, ld, prefix_lens,
+                       extend_lens, params, o, lse, workspace, ws_bytes, stream);
+}
+
+int sgl_extend_attn_kvwrite(const void* q_new, const void* k_new, const void* v_new, void* k_pool, void* v_pool,
+                            const int32_t* req_to_token, int64_t ld, const int32_t* prefix_lens,
+                            const int32_t* extend_lens, const sgl_attn_params* params, void* o, float* lse,
+                            void* workspace, size_t ws_bytes, sgl_stream_t stream) {
+    if (params && params->batch > 0 && (!k_new || !v_new)) return SGL_ERR_INVALID_ARG;
+    return extend_impl(q_new, k_new, v_new, k_pool, v_pool, k_pool, v_pool, req_to_token, ld, prefix_lens, extend_lens,
+                       params, o, lse, workspace, ws_bytes, stream);
 }
 
 int sgl_check(void* workspace, sgl_stream_t stream) {

@@ -617,8 +617,8 @@ __global__ void __maxnreg__(128) decode_fused_kernel(const __grid_constant__ Fus
         for (int w = w0; w < w1; ++w) {
             if (tid == 0) dec_tile_info(f.t, w, info);
             named_bar(kTileBar, TC::kThreads);
-            const TileInfo ti{info[0], info[1], info[2], info[3], {info[4], 0}, {info[5], 0}, {info[6], 0}};
-            tc_tile_run<TC>(f.t, &tmk, &tmv, ti, sm, tbase, st, tid);
+            const TileInfo ti{info[0], info[1], info[2], info[3], {info[4], 0}, {info[5], 0}, {info[6], 0}, INT_MAX, 0};
+            tc_tile_run<TC>(f.t, &tmk, &tmv, nullptr, nullptr, ti, sm, tbase, st, tid);
             named_bar(kTileBar, TC::kThreads);
         }
         asm volatile("bar.arrive %0, %1;\n" ::"r"(kStreamGate), "r"(kFusedThreads) : "memory");

@@ -4,6 +4,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <climits>
 #include <cstdint>
 
 #include "common.h"
@@ -334,6 +335,15 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, int 
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
         "%3, %4, %5, %6}], [%7];\n" ::"r"(dst),
         "l"(tmap), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
+        : "memory");
+}
+// TMA load of one 128-byte row piece: row y, columns x..x+63 (bf16) of the
+// 2-D tensor `tmap` (box 64 x 1, 128-byte swizzle) into `dst`.
+__device__ __forceinline__ void tma_load_row(uint32_t dst, const void* tmap, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];\n" ::"r"(dst),
+        "l"(tmap), "r"(x), "r"(y), "r"(bar)
         : "memory");
 }
 // Arrive on `bar` once every cp.async this thread issued so far has landed

@@ -69,12 +69,17 @@ __device__ bool extend_tile_info(const TcArgs& a, int* info) {
     info[7] = qoff + t0 + tq;             // first q row of tile 1
     info[8] = pre + t0;                   // causal limit of tile 0's first new token
     info[9] = pre + t0 + tq;              // causal limit of tile 1's first new token
+    // fused KV write: positions from pre on are read from the new K/V, whose
+    // row qoff holds position pre
+    info[10] = a.kn != nullptr ? pre : INT_MAX;
+    info[11] = qoff;
     return true;
 }
 
 template <int D>
 __global__ void __launch_bounds__(ExtCfg<D>::kThreads, 1)
-    extend_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
+    extend_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                     const __grid_constant__ CUtensorMap tnk, const __grid_constant__ CUtensorMap tnv) {
     using C = ExtCfg<D>;
     using Lay = typename C::Lay;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -97,9 +102,10 @@ __global__ void __launch_bounds__(ExtCfg<D>::kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = *tslot;
-    const TileInfo ti{info[0], info[1], info[2], info[3], {info[4], info[5]}, {info[6], info[7]}, {info[8], info[9]}};
+    const TileInfo ti{info[0], info[1], info[2], info[3], {info[4], info[5]}, {info[6], info[7]}, {info[8], info[9]},
+                      info[10], info[11]};
     TcState st{0u, 0u, false};
-    tc_tile_run<C>(a, &tmk, &tmv, ti, sm, tbase, st, tid);
+    tc_tile_run<C>(a, &tmk, &tmv, &tnk, &tnv, ti, sm, tbase, st, tid);
     tc_fence_before();
     __syncthreads();
     if (warp == C::kMmaWarp) {
@@ -120,8 +126,7 @@ static_assert(extend_smem<128>() > 116 * 1024 && extend_smem<64>() > 116 * 1024,
 
 namespace tc {
 
-int encode_pool_maps(const void* kp, const void* vp, int64_t num_slots, int Hkv, int D, CUtensorMap* mk,
-                     CUtensorMap* mv) {
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 enc = [] {
         void* fn = nullptr;
         cudaDriverEntryPointQueryResult q;
@@ -131,7 +136,25 @@ int encode_pool_maps(const void* kp, const void* vp, int64_t num_slots, int Hkv,
             fn = nullptr;
         return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }();
+    return enc;
+}
+
+int encode_rows_map(const void* base, int64_t rows, int D, CUtensorMap* m) {
+    const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return (int)cudaErrorNotSupported;
+    if (rows <= 0 || rows > (int64_t)INT32_MAX) return (int)cudaErrorInvalidValue;
+    const cuuint64_t gdim[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+    const cuuint64_t gstride[1] = {(cuuint64_t)D * 2};
+    const cuuint32_t box[2] = {64, 1};
+    const cuuint32_t estride[2] = {1, 1};
+    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride, box, estride,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? 0 : (int)cudaErrorInvalidValue;
+}
+
+int encode_pool_maps(const void* kp, const void* vp, int64_t num_slots, int Hkv, int D, CUtensorMap* mk,
+                     CUtensorMap* mv) {
     struct Cache {
         const void *kp = nullptr, *vp = nullptr;
         int64_t ns = -1;
@@ -140,21 +163,10 @@ int encode_pool_maps(const void* kp, const void* vp, int64_t num_slots, int Hkv,
     };
     thread_local Cache c;
     if (c.kp != kp || c.vp != vp || c.ns != num_slots || c.hkv != Hkv || c.d != D) {
-        const cuuint64_t rows = (cuuint64_t)num_slots * (cuuint64_t)Hkv;
-        if (rows == 0 || rows > (cuuint64_t)INT32_MAX) return (int)cudaErrorInvalidValue;
-        const cuuint64_t gdim[2] = {(cuuint64_t)D, rows};
-        const cuuint64_t gstride[1] = {(cuuint64_t)D * 2};
-        const cuuint32_t box[2] = {64, 1};
-        const cuuint32_t estride[2] = {1, 1};
-        for (int w = 0; w < 2; ++w) {
-            CUresult r = enc(w ? &c.mv : &c.mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(w ? vp : kp),
-                             gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-            if (r != CUDA_SUCCESS) {
-                c.kp = nullptr;
-                return (int)cudaErrorInvalidValue;
-            }
-        }
+        const int64_t rows = num_slots * (int64_t)Hkv;
+        c.kp = nullptr;
+        if (const int e = encode_rows_map(kp, rows, D, &c.mk)) return e;
+        if (const int e = encode_rows_map(vp, rows, D, &c.mv)) return e;
         c.kp = kp;
         c.vp = vp;
         c.ns = num_slots;
@@ -170,18 +182,27 @@ int encode_pool_maps(const void* kp, const void* vp, int64_t num_slots, int Hkv,
 
 // Extend over all requests: grid (pairs of query tiles of 128/G new tokens, KV heads).
 template <int D>
-int launch_extend_tc(const void* q, const void* kp, const void* vp, const int32_t* r2t, int64_t ld,
-                     const int32_t* pre, const int32_t* ext, int B, int64_t n_rows, int64_t ctas, void* o, float* lse,
+int launch_extend_tc(const void* q, const void* kp, const void* vp, const void* kn, const void* vn, void* kw, void* vw,
+                     const int32_t* r2t, int64_t ld, const int32_t* pre, const int32_t* ext, int B, int64_t n_rows,
+                     int64_t ctas, void* o, float* lse,
                      uint32_t* err, int Hq, int Hkv, int64_t num_slots, float scale_log2, cudaStream_t s) {
     static const int attr = (int)cudaFuncSetAttribute(extend_tc_kernel<D>,
                                                       cudaFuncAttributeMaxDynamicSharedMemorySize, extend_smem<D>());
     if (attr) return attr;
-    CUtensorMap mk, mv;
+    CUtensorMap mk, mv, nk{}, nv{};
     if (const int e = tc::encode_pool_maps(kp, vp, num_slots, Hkv, D, &mk, &mv)) return e;
+    if (kn) {
+        if (const int e = tc::encode_rows_map(kn, n_rows * Hkv, D, &nk)) return e;
+        if (const int e = tc::encode_rows_map(vn, n_rows * Hkv, D, &nv)) return e;
+    }
     TcArgs a{};
     a.q = static_cast<const bf16*>(q);
     a.kp = static_cast<const bf16*>(kp);
     a.vp = static_cast<const bf16*>(vp);
+    a.kn = static_cast<const bf16*>(kn);
+    a.vn = static_cast<const bf16*>(vn);
+    a.kw = static_cast<bf16*>(kw);
+    a.vw = static_cast<bf16*>(vw);
     a.r2t = r2t;
     a.ld = ld;
     a.prefix_lens = pre;
@@ -196,15 +217,15 @@ int launch_extend_tc(const void* q, const void* kp, const void* vp, const int32_
     a.G = Hq / Hkv;
     a.num_slots = num_slots;
     a.scale_log2 = scale_log2;
-    extend_tc_kernel<D><<<dim3((unsigned)ctas, (unsigned)Hkv), ExtCfg<D>::kThreads, extend_smem<D>(), s>>>(a, mk, mv);
+    extend_tc_kernel<D><<<dim3((unsigned)ctas, (unsigned)Hkv), ExtCfg<D>::kThreads, extend_smem<D>(), s>>>(a, mk, mv, nk, nv);
     return (int)cudaGetLastError();
 }
 
-template int launch_extend_tc<64>(const void*, const void*, const void*, const int32_t*, int64_t, const int32_t*,
-                                  const int32_t*, int, int64_t, int64_t, void*, float*, uint32_t*, int, int, int64_t,
-                                  float, cudaStream_t);
-template int launch_extend_tc<128>(const void*, const void*, const void*, const int32_t*, int64_t, const int32_t*,
-                                   const int32_t*, int, int64_t, int64_t, void*, float*, uint32_t*, int, int, int64_t,
-                                   float, cudaStream_t);
+template int launch_extend_tc<64>(const void*, const void*, const void*, const void*, const void*, void*, void*,
+                                  const int32_t*, int64_t, const int32_t*, const int32_t*, int, int64_t, int64_t, void*,
+                                  float*, uint32_t*, int, int, int64_t, float, cudaStream_t);
+template int launch_extend_tc<128>(const void*, const void*, const void*, const void*, const void*, void*, void*,
+                                   const int32_t*, int64_t, const int32_t*, const int32_t*, int, int64_t, int64_t,
+                                   void*, float*, uint32_t*, int, int, int64_t, float, cudaStream_t);
 
 }  // namespace sgl

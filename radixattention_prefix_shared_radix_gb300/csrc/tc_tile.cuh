@@ -133,6 +133,13 @@ struct TcArgs {
     const bf16* q;
     const bf16* kp;
     const bf16* vp;
+    // extend with the KV write fused in: the new tokens' K/V [n_rows, Hkv, d]
+    // (read for the new block instead of the pool) and the pools to write
+    // them into; null otherwise
+    const bf16* kn;
+    const bf16* vn;
+    bf16* kw;
+    bf16* vw;
     const int32_t* r2t;
     int64_t ld;
     // extend
@@ -228,6 +235,8 @@ struct TileInfo {
     int rows[2];   // query rows of each query tile (0: the tile is absent)
     int i6[2];     // extend: first q row of the tile; decode: first member index
     int i7[2];     // extend: causal limit of the tile's row 0; decode: first partial row
+    int new_pos;   // fused KV write: first position read from the new K/V (else INT_MAX)
+    int new_row;   // fused KV write: the new K/V row of position new_pos
 };
 
 struct TcState {
@@ -269,7 +278,8 @@ __device__ __forceinline__ void tc_init_barriers(uint32_t bar0) {
 // rows).
 template <class C>
 __device__ __forceinline__ void tc_tile_run(const TcArgs& a, const CUtensorMap* tmk, const CUtensorMap* tmv,
-                                            const TileInfo& ti, uint8_t* sm, uint32_t tbase, TcState& stt, int tid) {
+                                            const CUtensorMap* tnk, const CUtensorMap* tnv, const TileInfo& ti,
+                                            uint8_t* sm, uint32_t tbase, TcState& stt, int tid) {
     using Lay = typename C::Lay;
     constexpr int D = C::kD, NQ = C::kNQ, NS = C::kNS, NG = C::kNG, BN = C::kBN, NSB = C::kNSB;
     constexpr int KR = Lay::KREGION;
@@ -336,7 +346,9 @@ __device__ __forceinline__ void tc_tile_run(const TcArgs& a, const CUtensorMap* 
         // 4 quad .. 4 quad + 3, columns 64 half ..), OPW of them per team warp
         // (lane l issues op g OPW + l).  Positions past the range re-read the
         // range's last position (finite data, masked scores), so every row is
-        // inside the pool.
+        // inside the pool.  With the KV write fused, positions from new_pos on
+        // come from the new K/V tensor; a quad that straddles new_pos is
+        // loaded as four single rows.
         constexpr int H = D / 64;
         constexpr int NOP = BN / 4 * H;
         constexpr int OPW = (NOP + NG - 1) / NG;
@@ -347,12 +359,15 @@ __device__ __forceinline__ void tc_tile_run(const TcArgs& a, const CUtensorMap* 
         const int half = o % H, quad = o / H;
         const uint32_t bytes = (uint32_t)nmine * 512u;
         const int32_t* trow = a_r2t + (int64_t)kv_row * a_ld;
+        const int new_pos = ti.new_pos, new_row = ti.new_row;
         int32_t nx[4];
+        int npos0 = 0;   // first position of the quad being fetched
         auto fetch = [&](int j) {
+            npos0 = kv_begin + j * BN + 4 * quad;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const int p = min(kv_begin + j * BN + 4 * quad + i, kv_end - 1);
-                nx[i] = (mine && j < nb) ? __ldg(trow + p) : 0;
+                const int p = min(npos0 + i, kv_end - 1);
+                nx[i] = (mine && j < nb && p < new_pos) ? __ldg(trow + p) : 0;
             }
         };
         fetch(0);
@@ -361,15 +376,23 @@ __device__ __forceinline__ void tc_tile_run(const TcArgs& a, const CUtensorMap* 
             const uint32_t J = J0 + j;
             const int st = (int)(J % (uint32_t)NS);
             const uint32_t ph = (J / (uint32_t)NS) & 1u;
+            const int npos_cur = npos0;
             int r[4];
+            int nsrc = 0;   // rows of the quad read from the new K/V
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                int32_t sl = nx[i];
-                if (sl < 0 || sl >= a_num_slots) {
-                    if (mine && half == 0) atomicOr(a_err, 1u);
-                    sl = 0;
+                const int p = min(npos_cur + i, kv_end - 1);
+                if (p >= new_pos) {
+                    r[i] = (new_row + (p - new_pos)) * a_Hkv + kvh;
+                    ++nsrc;
+                } else {
+                    int32_t sl = nx[i];
+                    if (sl < 0 || sl >= a_num_slots) {
+                        if (mine && half == 0) atomicOr(a_err, 1u);
+                        sl = 0;
+                    }
+                    r[i] = sl * a_Hkv + kvh;
                 }
-                r[i] = sl * a_Hkv + kvh;
             }
             fetch(j + 1);
             // K rows once S_{j-NS} has read the stage, then V rows once
@@ -383,12 +406,50 @@ __device__ __forceinline__ void tc_tile_run(const TcArgs& a, const CUtensorMap* 
                 const int bfull = part ? C::VFULL(st) : C::KFULL(st);
                 if (lane == 0) mbar_expect_tx(bar(bfull), bytes);
                 __syncwarp();
-                if (mine)
-                    tma_gather4((part ? sV : sK) + st * Lay::KTILE + half * KR + quad * 512, part ? tmv : tmk, half * 64,
-                                r[0], r[1], r[2], r[3], bar(bfull));
+                if (mine) {
+                    const uint32_t dq = (part ? sV : sK) + st * Lay::KTILE + half * KR + quad * 512;
+                    if (nsrc == 0) {
+                        tma_gather4(dq, part ? tmv : tmk, half * 64, r[0], r[1], r[2], r[3], bar(bfull));
+                    } else if (nsrc == 4) {
+                        tma_gather4(dq, part ? tnv : tnk, half * 64, r[0], r[1], r[2], r[3], bar(bfull));
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const bool nw = min(npos_cur + i, kv_end - 1) >= new_pos;
+                            tma_load_row(dq + 128 * i, nw ? (part ? tnv : tnk) : (part ? tmv : tmk), half * 64, r[i],
+                                         bar(bfull));
+                        }
+                    }
+                }
             }
             if (stt.timed_out) break;
             issued = j + 1;
+        }
+        if constexpr (!DEC) {
+            // Fused KV write (after the gathers are issued, so that it overlaps the
+            // MMAs): this CTA's new tokens (its query tiles' rows / G)
+            // for KV head kvh go from the new K/V into their pool slots.  No
+            // CTA reads them from the pool in this launch: positions from
+            // new_pos on are gathered from the new K/V themselves.
+            if (a.kw != nullptr) {
+                constexpr int CH = D / 8;   // 16-byte chunks per row
+                const int n0 = ti.rows[0] / a_G, n1 = ti.rows[1] / a_G;
+                const int items = (n0 + n1) * 2 * CH;
+                const int32_t* trw = a_r2t + (int64_t)kv_row * a_ld;
+                for (int it = (g * 32 + lane); it < items; it += NG * 32) {
+                    const int ch = it % CH, kvsel = (it / CH) & 1, t = it / (2 * CH);
+                    const int row = t < n0 ? ti.i6[0] + t : ti.i6[1] + (t - n0);   // new K/V row
+                    const int pos = ti.new_pos + (row - ti.new_row);
+                    const int32_t sl = __ldg(trw + pos);
+                    if (sl < 0 || sl >= a_num_slots) {
+                        if (ch == 0) atomicOr(a_err, 1u);
+                        continue;
+                    }
+                    const uint4 v = __ldg(reinterpret_cast<const uint4*>((kvsel ? a.vn : a.kn) +
+                                                                         ((int64_t)row * a_Hkv + kvh) * D) + ch);
+                    reinterpret_cast<uint4*>((kvsel ? a.vw : a.kw) + ((int64_t)sl * a_Hkv + kvh) * D)[ch] = v;
+                }
+            }
         }
         // This warp's copies have landed before it leaves the tile (normally
         // long since: the MMA thread consumed them).  A FULL phase needs this
@@ -660,6 +721,8 @@ __device__ __forceinline__ void tc_tile_run(const TcArgs& a, const CUtensorMap* 
 // reused while the pools and shape are the same.  Returns a cudaError_t.
 int encode_pool_maps(const void* kp, const void* vp, int64_t num_slots, int Hkv, int D, CUtensorMap* mk,
                      CUtensorMap* mv);
+// Host: the same view of any [rows, D] bf16 tensor (not cached).
+int encode_rows_map(const void* base, int64_t rows, int D, CUtensorMap* m);
 
 }  // namespace tc
 }  // namespace sgl

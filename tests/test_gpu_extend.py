@@ -11,7 +11,7 @@ import pytest
 import torch
 
 import workloads as W
-from oracle.attention import decode_attention, extend_attention
+from oracle.attention import decode_attention, extend_attention, extend_attention_kvwrite, kv_write
 from tests._harness import Case, assert_close, run_extend, tolerances
 
 pytestmark = pytest.mark.gpu
@@ -109,5 +109,108 @@ def test_rescale_path_with_growing_scores():
     case = Case(None, workload=w, pool=(order, K, V))
     try:
         _check(case)
+    finally:
+        case.close()
+
+
+# ---------------------------------------------------------------------------
+# KV write fused into extend (chunked prefill)
+# ---------------------------------------------------------------------------
+def _bits(t):
+    """Raw bytes of a CPU tensor, for bit-exact pool comparisons."""
+    return t.contiguous().view(torch.uint8).numpy()
+
+
+def _run_kvwrite(case, kd, vd, kn, vn, pre, ext, q=None):
+    import radixattention_prefix_shared_radix_gb300 as sgl
+    p = case.params(host_prefix_lens=pre, host_extend_lens=ext)
+    ws = torch.zeros(sgl.sgl_extend_workspace_bytes(p), dtype=torch.uint8, device="cuda")
+    qd = (q if q is not None else case.q_host()).cuda()
+    table = torch.from_numpy(case.out["req_to_token"]).cuda()
+    o = torch.empty_like(qd)
+    lse = torch.empty(qd.shape[0], case.w.Hq, dtype=torch.float32, device="cuda")
+    sgl.sgl_extend_attn_kvwrite(qd, kn.cuda(), vn.cuda(), kd, vd, table, torch.from_numpy(pre).cuda(),
+                                torch.from_numpy(ext).cuda(), p, o, lse, ws)
+    sgl.sgl_check(ws)
+    return o.double().cpu().numpy(), lse.cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("name", ["extend_small", "extend_small_fp32"])
+def test_extend_kvwrite_elementwise_and_pool_bytes(name):
+    """The fused call equals the oracle's write-then-extend, and the pool
+    afterwards holds exactly the new rows at their slots (bit for bit)."""
+    w = W.get("extend_small")
+    if name.endswith("fp32"):
+        w = W.Workload("extend_small_fp32", w.number, "extend", "f32", w.Hq, w.Hkv, 64, 1, w.structure,
+                       num_slots=w.num_slots)
+    case = Case(None, workload=w)
+    try:
+        pre = case.out["prefix_lens"]
+        ext = case.out["seq_lens"] - pre
+        kf, vf = W.make_new_kv(w, int(ext.sum()))
+        kn, vn = W.to_dtype(w, kf), W.to_dtype(w, vf)
+        kd, vd = case.device_pool()
+        O, L = _run_kvwrite(case, kd, vd, kn, vn, pre, ext)
+        Oref, Lref = extend_attention_kvwrite(case.oracle_q(), kn.double().numpy(), vn.double().numpy(),
+                                              W.RowView(case.K), W.RowView(case.V), case.oracle_table, pre, ext)
+        assert_close(O, L, Oref, Lref, *tolerances(w))
+        Kexp, Vexp = kv_write(_bits(case.K).copy(), _bits(case.V).copy(), _bits(kn), _bits(vn),
+                              case.oracle_table, pre, ext)
+        assert np.array_equal(_bits(kd.cpu()), Kexp) and np.array_equal(_bits(vd.cpu()), Vexp)
+    finally:
+        case.close()
+
+
+def test_chunked_prefill_of_a_long_prompt():
+    """A 1500-token prompt prefilled in chunks of 256 (plus a ragged tail),
+    each chunk writing its K/V and attending to the chunks before it, equals
+    the oracle chunk by chunk; the cache then holds the whole prompt."""
+    w = W.Workload("chunked", 5, "extend", "bf16", 32, 8, 128, 1,
+                   ("extend", dict(n=1, prefix=(0, 0), new=(1500, 1500))), num_slots=4096)
+    case = Case(None, workload=w)
+    try:
+        L = int(case.out["seq_lens"][0])
+        kf, vf = W.make_new_kv(w, L)
+        kn, vn = W.to_dtype(w, kf), W.to_dtype(w, vf)
+        q = W.to_dtype(w, W.make_queries(w, L))   # the whole prompt's queries, chunk by chunk
+        kd, vd = case.device_pool()
+        Kc, Vc = _bits(case.K).copy(), _bits(case.V).copy()
+        for c0 in range(0, L, 256):
+            n = min(256, L - c0)
+            pre, ext = np.array([c0], dtype=np.int32), np.array([n], dtype=np.int32)
+            O, Lse = _run_kvwrite(case, kd, vd, kn[c0:c0 + n], vn[c0:c0 + n], pre, ext, q=q[c0:c0 + n])
+            Kcur = torch.from_numpy(Kc).view(torch.bfloat16).view(case.K.shape)
+            Vcur = torch.from_numpy(Vc).view(torch.bfloat16).view(case.V.shape)
+            Oref, Lref = extend_attention_kvwrite(q[c0:c0 + n].double().numpy(), kn[c0:c0 + n].double().numpy(),
+                                                  vn[c0:c0 + n].double().numpy(), W.RowView(Kcur), W.RowView(Vcur),
+                                                  case.oracle_table, pre, ext)
+            assert_close(O, Lse, Oref, Lref, *tolerances(w))
+            kv_write(Kc, Vc, _bits(kn[c0:c0 + n]), _bits(vn[c0:c0 + n]), case.oracle_table, pre, ext)
+        assert np.array_equal(_bits(kd.cpu()), Kc) and np.array_equal(_bits(vd.cpu()), Vc)
+    finally:
+        case.close()
+
+
+def test_extend_kvwrite_full_size_sampled():
+    case = Case("extend")
+    try:
+        w = case.w
+        pre = case.out["prefix_lens"]
+        ext = case.out["seq_lens"] - pre
+        kf, vf = W.make_new_kv(w, int(ext.sum()))
+        kn, vn = W.to_dtype(w, kf), W.to_dtype(w, vf)
+        kd, vd = case.device_pool()
+        O, L = _run_kvwrite(case, kd, vd, kn, vn, pre, ext)
+        starts = np.concatenate([[0], np.cumsum(ext)[:-1]])
+        rng = np.random.default_rng(2)
+        rows = []
+        for s, e in zip(starts, ext):
+            rows += [int(s), int(s + e - 1), int(s + 200)] + [int(s + x) for x in rng.integers(0, e, 3)]
+        rows = sorted(set(rows))
+        Oref, Lref = extend_attention_kvwrite(case.oracle_q(), kn.double().numpy(), vn.double().numpy(),
+                                              W.RowView(case.K), W.RowView(case.V), case.oracle_table, pre, ext,
+                                              rows=rows)
+        do, dl = assert_close(O, L, Oref, Lref, *tolerances(w), rows=rows)
+        print("extend kvwrite: O max-abs %.3g, LSE max-abs %.3g" % (do, dl))
     finally:
         case.close()

@@ -10,6 +10,9 @@
     equals the unsplit result (to 1e-12 in float64);
   * extend with no cached prefix is causal attention; extend of one token
     after a prefix is decode;
+  * the KV write stores each new row at its slot and nothing else (brute
+    force); a prompt prefilled chunk by chunk with the write fused in equals
+    causal SDPA over the whole prompt, and its last token equals decode;
   * the worked KV-byte example on the chenxutan.com page.
 """
 
@@ -24,7 +27,7 @@ import torch
 from scipy.special import logsumexp
 
 from oracle.attention import (decode_attention, decode_attention_shared, extend_attention,
-                              lse_merge, softmax_attend)
+                              extend_attention_kvwrite, kv_write, lse_merge, softmax_attend)
 from oracle.groups import prefix_groups
 from oracle.kvbytes import kv_bytes_per_token, unique_kv_bytes, unshared_kv_bytes
 from oracle.tree import RadixTrie, build_batch
@@ -188,3 +191,55 @@ def test_unique_vs_unshared_bytes():
     distinct = len({s for r in rows for s in r})
     assert unique_kv_bytes(g, 8, 128, 2) == distinct * 4096
     assert unshared_kv_bytes(lens, 8, 128, 2) == sum(len(r) for r in rows) * 4096
+
+
+def test_kv_write_stores_each_row_at_its_slot_only():
+    rng = np.random.default_rng(21)
+    S, Hkv, d = 96, 2, 4
+    K0, V0 = _pool(S, Hkv, d, 8)
+    pre, ext = [3, 0, 7], [5, 2, 1]
+    perm = rng.permutation(S)
+    rows = [list(perm[0:8]), list(perm[8:10]), list(perm[10:18])]
+    t, _ = _table(rows)
+    kn = rng.standard_normal((sum(ext), Hkv, d))
+    vn = rng.standard_normal((sum(ext), Hkv, d))
+    K, V = kv_write(K0.copy(), V0.copy(), kn, vn, t, pre, ext)
+    written = {}
+    row = 0
+    for r in range(3):
+        for i in range(ext[r]):
+            written[int(t[r, pre[r] + i])] = row
+            row += 1
+    for slot in range(S):
+        if slot in written:
+            assert np.array_equal(K[slot], kn[written[slot]]) and np.array_equal(V[slot], vn[written[slot]])
+        else:
+            assert np.array_equal(K[slot], K0[slot]) and np.array_equal(V[slot], V0[slot])
+
+
+def test_chunked_prefill_with_kv_write_is_causal_sdpa_and_ends_in_decode():
+    rng = np.random.default_rng(22)
+    Hq, Hkv, d, S = 4, 2, 16, 300
+    K, V = _pool(S, Hkv, d, 9)          # stale contents at the prompt's slots
+    L = 70
+    slots = list(rng.permutation(S)[:L])
+    t, _ = _table([slots])
+    q = rng.standard_normal((L, Hq, d))
+    kn = rng.standard_normal((L, Hkv, d))
+    vn = rng.standard_normal((L, Hkv, d))
+    O = np.zeros((L, Hq, d))
+    LSE = np.zeros((L, Hq))
+    Kc, Vc = K.copy(), V.copy()
+    for c0 in range(0, L, 16):          # chunks of 16 new tokens on top of the cached ones
+        n = min(16, L - c0)
+        O[c0:c0 + n], LSE[c0:c0 + n] = extend_attention_kvwrite(q[c0:c0 + n], kn[c0:c0 + n], vn[c0:c0 + n], Kc, Vc,
+                                                                 t, [c0], [n])
+        kv_write(Kc, Vc, kn[c0:c0 + n], vn[c0:c0 + n], t, [c0], [n])   # the cache after the chunk
+    qq = torch.from_numpy(q).permute(1, 0, 2)[None]
+    kk = torch.from_numpy(kn).permute(1, 0, 2)[None]
+    vv = torch.from_numpy(vn).permute(1, 0, 2)[None]
+    ref = torch.nn.functional.scaled_dot_product_attention(qq, kk, vv, is_causal=True, scale=1 / math.sqrt(d),
+                                                           enable_gqa=True)
+    assert np.allclose(O, ref[0].permute(1, 0, 2).numpy(), atol=1e-12)
+    Od, Ld = decode_attention(q[L - 1:L], Kc, Vc, t, [L])
+    assert np.allclose(O[L - 1:L], Od, atol=1e-13) and np.allclose(LSE[L - 1:L], Ld, atol=1e-13)

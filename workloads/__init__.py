@@ -231,6 +231,21 @@ def make_batch(name_or_workload, instance=0):
     return b
 
 
+def make_new_kv(w, n_rows, instance=0):
+    """K and V of n_rows new tokens [n_rows, Hkv, d] (float32 numpy, N(0,1)),
+    for the KV write fused into extend: default_rng([seed, 4, instance])."""
+    rng = np.random.default_rng([w.seed, 4, instance])
+    k = rng.standard_normal((n_rows, w.Hkv, w.d), dtype=np.float32)
+    v = rng.standard_normal((n_rows, w.Hkv, w.d), dtype=np.float32)
+    return k, v
+
+
+def make_queries(w, n_rows, instance=0):
+    """Queries of n_rows tokens [n_rows, Hq, d] (float32 numpy, N(0,1)):
+    default_rng([seed, 5, instance])."""
+    return np.random.default_rng([w.seed, 5, instance]).standard_normal((n_rows, w.Hq, w.d), dtype=np.float32)
+
+
 def pool_slots(w, instances=1):
     """Pool size in slots: fixed for most workloads; otherwise pool_factor x
     the pages the batch instances occupy (every segment rounded up to whole
