@@ -60,6 +60,7 @@ def parse():
     ap.add_argument("--only", choices=["all", "decode", "extend"], default="all",
                     help="decode: skip the extend line; extend: time only the extend workload (profiling)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-sched", action="store_true", help="skip the host scheduling simulation")
     ap.add_argument("--pool-slots", type=int, default=0,
                     help="decode pool size override (0: the workload's 2^20 slots); small pools serve ncu captures")
     return ap.parse_args()
@@ -437,6 +438,8 @@ def run_native(args):
     }
     if ext is not None:
         line["extend"] = ext
+    if rank == 0 and args.only == "all" and not args.no_sched:
+        line["scheduling"] = bench_scheduling(sgl, W, w)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_subprocess()
     if rank == 0:
@@ -511,6 +514,45 @@ def bench_extend(sgl, W, torch, steps, bf16_peak):
             "tokens_per_s": int(ext.sum()) / (ms / 1e3), "steps": steps,
             "kv_write_fused": {"ms_per_call": ms_kv, "tflops": flops / (ms_kv / 1e3) / 1e12,
                                "kv_bytes_written": int(kn.numel() * 2 * 2)}}
+
+
+def bench_scheduling(sgl, W, w):
+    """Cache-aware scheduling simulation (host, native tree) on two traces
+    shaped like the lecture notes' demos: few-shot serving (8 applications
+    with 2000-token system prompts, 600 requests arriving together) and
+    multi-turn chat (300 conversations x 6 turns on a 500-token system
+    prompt, 5-20 rounds between turns, a pool too small for every history).
+    Per policy: cache hit rate, prefill tokens computed, their KV bytes
+    (Llama-3-8B shape, one layer) and the simulation's host time."""
+    import numpy as np
+    per_tok = kv_bytes_per_token(w)
+    traces = {
+        "few_shot": (W.few_shot_trace(apps=8, sys_len=2000, n_requests=600, question=(50, 200), output=(50, 200)),
+                     1 << 20),
+        "multi_turn": (W.multi_turn_trace(conversations=300, turns=6, sys_len=500, user=(50, 150),
+                                          output=(50, 200), delay=(5, 20)), 1 << 18),
+    }
+    policies = {"fcfs_insert_at_prefill": (sgl.SGL_SCHED_FCFS, sgl.SGL_INSERT_AT_PREFILL, 0),
+                "lpm_insert_at_prefill": (sgl.SGL_SCHED_LPM, sgl.SGL_INSERT_AT_PREFILL, 64),
+                "lpm_insert_at_finish": (sgl.SGL_SCHED_LPM, sgl.SGL_INSERT_AT_FINISH, 64)}
+    out = {}
+    for name, (reqs, S) in traces.items():
+        res = {}
+        for pname, (pol, ins, defer) in policies.items():
+            order = np.random.default_rng([S, 11]).permutation(S).astype(np.int32)
+            tree = sgl.sgl_tree_create(S, 1, order)
+            t0 = time.perf_counter()
+            _, st = sgl.sgl_sim_run(tree, reqs, policy=pol, insert_at=ins, prefill_budget=2048, max_running=256,
+                                    defer_tokens=defer)
+            el = time.perf_counter() - t0
+            sgl.sgl_tree_destroy(tree)
+            res[pname] = {"hit_rate": st["cached_tokens"] / max(1, st["prompt_tokens"]),
+                          "prefill_tokens": st["prefill_tokens"], "prefill_kv_bytes": st["prefill_tokens"] * per_tok,
+                          "evicted_tokens": st["evicted_tokens"], "rounds": st["rounds"],
+                          "host_ms": el * 1e3, "host_us_per_round": el * 1e6 / max(1, st["rounds"])}
+        out[name] = {"requests": len(reqs), "pool_slots": S, "prefill_budget": 2048, "max_running": 256,
+                     "policies": res}
+    return out
 
 
 def profile_traffic(kernel):

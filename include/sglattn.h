@@ -291,6 +291,75 @@ int sgl_extend_attn(const void* q_new, const void* k_pool, const void* v_pool, c
                     const sgl_attn_params* params, void* o, float* lse, void* workspace, size_t ws_bytes,
                     sgl_stream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * Cache-aware scheduling simulation (host) over the radix tree.
+ * A round-based serving loop: every round, requests that have arrived join
+ * the waiting queue; the queue is ordered (FCFS: arrival order; LPM: longest
+ * cached prefix first, ties in queue order -- the match lengths are taken with
+ * sgl_tree_match, which also refreshes the matched nodes' LRU stamps); requests
+ * are admitted in that order while fewer than max_running run: the cached
+ * prefix is matched and locked, and slots for the rest of the prompt and all
+ * of the output are allocated (evicting LRU leaves); an allocation failure
+ * ends admission for the round.  Under LPM with defer_tokens > 0 a request is
+ * skipped for the round if a request admitted in the same round has the same
+ * cached length and the same next min(defer_tokens, uncached) prompt tokens
+ * (its prefix will be cached once that one is prefilled).  Then up to
+ * prefill_budget prompt tokens are prefilled, in admission order (chunked
+ * prefill); a request whose prompt is complete inserts the prompt into the
+ * tree now (SGL_INSERT_AT_PREFILL) or only at its end (SGL_INSERT_AT_FINISH).
+ * Every request whose prefill completed in an earlier round decodes one
+ * output token; after its last token the whole sequence is inserted, its
+ * references are released and a partial tail page is freed.  A request with
+ * depends_on = j arrives `delay` rounds after request j finishes (a later
+ * turn of a conversation).
+ * The tree is used and modified as a real scheduler would (its contents
+ * afterwards are the cache after the trace).
+ * Returns SGL_ERR_STATE if max_rounds pass before every request finished.
+ * ["SGLang：从前端 DSL 到 SRT 服务运行时" "用基数树实现前缀复用": cache-aware
+ * scheduling by longest shared prefix, leaf-first LRU eviction, reference
+ * counts; CS349D lecture-16 notes §3.1-3.3: continuous batching, chunked
+ * prefill budget, longest-prefix-first with deferral, insertion at prefill
+ * completion] */
+enum { SGL_SCHED_FCFS = 0, SGL_SCHED_LPM = 1 };
+enum { SGL_INSERT_AT_PREFILL = 0, SGL_INSERT_AT_FINISH = 1 };
+
+typedef struct {
+    int32_t policy;          /* SGL_SCHED_FCFS or SGL_SCHED_LPM */
+    int32_t insert_at;       /* SGL_INSERT_AT_PREFILL or SGL_INSERT_AT_FINISH */
+    int64_t prefill_budget;  /* prompt tokens prefilled per round, >= 1 */
+    int32_t max_running;     /* requests running at once, >= 1 */
+    int32_t defer_tokens;    /* LPM deferral window, >= 0 (0: off) */
+    int64_t max_rounds;      /* guard, >= 1 */
+} sgl_sim_config;
+
+typedef struct {
+    const int32_t* prompt;   /* host, prompt_len tokens (>= 1) */
+    int64_t prompt_len;
+    const int32_t* output;   /* host, the output_len tokens it generates (>= 1) */
+    int64_t output_len;
+    int64_t arrive_round;    /* used when depends_on < 0 (>= 0) */
+    int32_t depends_on;      /* -1, or an earlier request index */
+    int64_t delay;           /* rounds after depends_on finishes (>= 0) */
+} sgl_sim_request;
+
+typedef struct {
+    int64_t arrive_round, admit_round, cached_tokens, prefill_done_round, finish_round;
+} sgl_sim_result;
+
+typedef struct {
+    int64_t rounds;          /* rounds until every request finished */
+    int64_t prompt_tokens;   /* prompt tokens of all requests */
+    int64_t cached_tokens;   /* of which found in the tree at admission */
+    int64_t prefill_tokens;  /* prompt tokens prefilled (= prompt - cached) */
+    int64_t decode_tokens;   /* output tokens decoded */
+    int64_t evicted_tokens;  /* tree tokens evicted by admissions */
+} sgl_sim_stats;
+
+/* reqs, per_req: host arrays of n.  The tree: from sgl_tree_create, with
+ * whatever it already caches. */
+int sgl_sim_run(sgl_tree* tree, const sgl_sim_config* cfg, int32_t n, const sgl_sim_request* reqs,
+                sgl_sim_result* per_req, sgl_sim_stats* stats);
+
 /* Extend attention with the KV write fused in (chunked prefill step).
  *   k_new, v_new device [N, Hkv, d] (dtype), rows ordered like q_new: the
  *                new tokens' K and V, which this call stores into

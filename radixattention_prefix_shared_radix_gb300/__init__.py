@@ -56,6 +56,31 @@ class SglAttnParams(ctypes.Structure):
                 ("host_extend_lens", ctypes.POINTER(ctypes.c_int32))]
 
 
+class SglSimConfig(ctypes.Structure):
+    _fields_ = [("policy", ctypes.c_int32), ("insert_at", ctypes.c_int32), ("prefill_budget", ctypes.c_int64),
+                ("max_running", ctypes.c_int32), ("defer_tokens", ctypes.c_int32), ("max_rounds", ctypes.c_int64)]
+
+
+class SglSimRequest(ctypes.Structure):
+    _fields_ = [("prompt", ctypes.POINTER(ctypes.c_int32)), ("prompt_len", ctypes.c_int64),
+                ("output", ctypes.POINTER(ctypes.c_int32)), ("output_len", ctypes.c_int64),
+                ("arrive_round", ctypes.c_int64), ("depends_on", ctypes.c_int32), ("delay", ctypes.c_int64)]
+
+
+class SglSimResult(ctypes.Structure):
+    _fields_ = [("arrive_round", ctypes.c_int64), ("admit_round", ctypes.c_int64), ("cached_tokens", ctypes.c_int64),
+                ("prefill_done_round", ctypes.c_int64), ("finish_round", ctypes.c_int64)]
+
+
+class SglSimStats(ctypes.Structure):
+    _fields_ = [("rounds", ctypes.c_int64), ("prompt_tokens", ctypes.c_int64), ("cached_tokens", ctypes.c_int64),
+                ("prefill_tokens", ctypes.c_int64), ("decode_tokens", ctypes.c_int64),
+                ("evicted_tokens", ctypes.c_int64)]
+
+
+SGL_SCHED_FCFS, SGL_SCHED_LPM = 0, 1
+SGL_INSERT_AT_PREFILL, SGL_INSERT_AT_FINISH = 0, 1
+
 _P = ctypes.c_void_p
 _I32P = ctypes.POINTER(ctypes.c_int32)
 _I64P = ctypes.POINTER(ctypes.c_int64)
@@ -93,6 +118,8 @@ _SIGS = {
     "sgl_extend_attn_kvwrite": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, ctypes.c_int64, _P, _P,
                                                ctypes.POINTER(SglAttnParams), _P, _P, _P, ctypes.c_size_t, _P]),
     "sgl_check": (ctypes.c_int, [_P, _P]),
+    "sgl_sim_run": (ctypes.c_int, [_P, ctypes.POINTER(SglSimConfig), ctypes.c_int32, ctypes.POINTER(SglSimRequest),
+                                   ctypes.POINTER(SglSimResult), ctypes.POINTER(SglSimStats)]),
     "sgl_decode_attn_noalloc": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_int64, _P, _P, _P, _P, _P]),
 }
 
@@ -214,6 +241,33 @@ def sgl_tree_stats(tree):
     s = SglTreeStats()
     _ok(_lib().sgl_tree_stats(tree, ctypes.byref(s)), "sgl_tree_stats")
     return {k: getattr(s, k) for k, _ in SglTreeStats._fields_}
+
+
+def sgl_sim_run(tree, requests, policy=SGL_SCHED_LPM, insert_at=SGL_INSERT_AT_PREFILL, prefill_budget=2048,
+                max_running=256, defer_tokens=0, max_rounds=1 << 30):
+    """Cache-aware scheduling simulation (see sgl_sim_run in the C header).
+
+    requests: list of dicts with prompt, output (int sequences), and either
+    arrive_round or depends_on + delay.  Returns (per-request list of dicts,
+    stats dict).
+    """
+    n = len(requests)
+    keep = []
+    arr = (SglSimRequest * max(1, n))()
+    for i, r in enumerate(requests):
+        pr, out = _i32(r["prompt"]), _i32(r["output"])
+        keep += [pr, out]
+        arr[i].prompt, arr[i].prompt_len = _ptr32(pr), len(pr)
+        arr[i].output, arr[i].output_len = _ptr32(out), len(out)
+        arr[i].arrive_round = int(r.get("arrive_round", 0))
+        arr[i].depends_on = int(r.get("depends_on", -1))
+        arr[i].delay = int(r.get("delay", 0))
+    cfg = SglSimConfig(policy, insert_at, prefill_budget, max_running, defer_tokens, max_rounds)
+    res = (SglSimResult * max(1, n))()
+    st = SglSimStats()
+    _ok(_lib().sgl_sim_run(tree, ctypes.byref(cfg), n, arr, res, ctypes.byref(st)), "sgl_sim_run")
+    per = [{k: getattr(res[i], k) for k, _ in SglSimResult._fields_} for i in range(n)]
+    return per, {k: getattr(st, k) for k, _ in SglSimStats._fields_}
 
 
 def sgl_build_batch(tree, token_lists, ld=None, groups=None):

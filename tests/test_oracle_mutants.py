@@ -130,3 +130,37 @@ def test_segments_not_split_at_member_end_are_caught(monkeypatch):
         return OG._pack(sorted((min(M), b, e, M) for (M, b), e in segs.items()))
     monkeypatch.setattr(TG, "prefix_groups", bad)
     assert _fails(TG.test_conversation_tree_figure, "tests/golden")
+
+
+def test_kv_write_off_by_one_slot_is_caught(monkeypatch):
+    def bad(k_pool, v_pool, k_new, v_new, req_to_token, prefix_lens, extend_lens):
+        table = np.asarray(req_to_token)
+        row = 0
+        for r in range(len(prefix_lens)):
+            pre, ext = int(prefix_lens[r]), int(extend_lens[r])
+            for i in range(ext):
+                slot = int(table[r, max(0, pre + i - 1)])   # one position early
+                k_pool[slot] = k_new[row]
+                v_pool[slot] = v_new[row]
+                row += 1
+        return k_pool, v_pool
+    monkeypatch.setattr(OA, "kv_write", bad)
+    monkeypatch.setattr(TA, "kv_write", bad)
+    assert _fails(TA.test_kv_write_stores_each_row_at_its_slot_only)
+
+
+def test_scheduler_without_deferral_or_with_late_insertion_is_caught(monkeypatch):
+    import oracle.sched as OS
+    from tests import test_sched as TS
+    good = OS.simulate
+
+    def no_defer(trie, requests, **kw):
+        kw["defer_tokens"] = 0
+        return good(trie, requests, **kw)
+
+    def late_insert(trie, requests, **kw):
+        kw["insert_at"] = OS.AT_FINISH
+        return good(trie, requests, **kw)
+    for bad in (no_defer, late_insert):
+        monkeypatch.setattr(TS, "simulate", bad)
+        assert _fails(TS.test_few_shot_sharing_needs_insertion_at_prefill)

@@ -311,3 +311,50 @@ def to_dtype(w, x):
     import torch
     t = torch.from_numpy(np.ascontiguousarray(x))
     return t if w.dtype == "f32" else t.to(torch.bfloat16)
+
+
+# ---------------------------------------------------------------------------
+# Request traces for the cache-aware scheduling simulation (seeded, synthetic)
+# ---------------------------------------------------------------------------
+def few_shot_trace(apps, sys_len, n_requests, question=(16, 64), output=(8, 32), seed=7, spread=0):
+    """Few-shot serving: `apps` applications, each with its own system prompt
+    of sys_len tokens; n_requests requests, each an application's system
+    prompt followed by a fresh question, arriving at round 0 (or uniformly
+    over `spread` rounds).  Tokens are ids in [1, VOCAB)."""
+    rng = np.random.default_rng([seed, 6])
+    sys = [rng.integers(1, VOCAB, size=sys_len).astype(np.int32) for _ in range(apps)]
+    reqs = []
+    for i in range(n_requests):
+        app = int(rng.integers(0, apps))
+        q = rng.integers(1, VOCAB, size=int(rng.integers(question[0], question[1] + 1))).astype(np.int32)
+        out = rng.integers(1, VOCAB, size=int(rng.integers(output[0], output[1] + 1))).astype(np.int32)
+        reqs.append(dict(prompt=np.concatenate([sys[app], q]), output=out,
+                         arrive_round=int(rng.integers(0, spread + 1)) if spread else 0))
+    return reqs
+
+
+def multi_turn_trace(conversations, turns, sys_len, user=(16, 64), output=(16, 64), delay=(5, 20), seed=8):
+    """Multi-turn chat: every conversation starts with a shared system prompt
+    of sys_len tokens; turn t's prompt is turn t-1's prompt and output plus a
+    new user message, arriving delay rounds after turn t-1 finishes (the first
+    turns arrive over the first `conversations` rounds)."""
+    rng = np.random.default_rng([seed, 7])
+    sys = rng.integers(1, VOCAB, size=sys_len).astype(np.int32)
+    reqs = []
+    for c in range(conversations):
+        hist = sys
+        prev = -1
+        for t in range(turns):
+            u = rng.integers(1, VOCAB, size=int(rng.integers(user[0], user[1] + 1))).astype(np.int32)
+            out = rng.integers(1, VOCAB, size=int(rng.integers(output[0], output[1] + 1))).astype(np.int32)
+            prompt = np.concatenate([hist, u])
+            r = dict(prompt=prompt, output=out)
+            if prev < 0:
+                r["arrive_round"] = c
+            else:
+                r["depends_on"], r["delay"] = prev, int(rng.integers(delay[0], delay[1] + 1))
+            reqs.append(r)
+            prev = len(reqs) - 1
+            hist = np.concatenate([prompt, out])
+    # requests must come after the ones they depend on: order by conversation turn
+    return reqs
