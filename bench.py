@@ -61,6 +61,7 @@ def parse():
                     help="decode: skip the extend line; extend: time only the extend workload (profiling)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-sched", action="store_true", help="skip the host scheduling simulation")
+    ap.add_argument("--no-fp8", action="store_true", help="skip the FP8 KV decode object")
     ap.add_argument("--pool-slots", type=int, default=0,
                     help="decode pool size override (0: the workload's 2^20 slots); small pools serve ncu captures")
     return ap.parse_args()
@@ -397,6 +398,11 @@ def run_native(args):
         e2e_gbs, h2d, d2h, e2e_step_s = e2e_decode(sgl, W, torch, w, tree, kd, vd, inst,
                                                    max(1, min(args.e2e_steps, K)), args.num_sms)
 
+    fp8 = None
+    if not args.no_fp8:
+        fp8 = bench_fp8(sgl, W, torch, w, kd, vd, inst, min(K, 2000), hbm_peak, args.num_sms)
+        fp8["speedup_vs_bf16"] = per_call_ms / fp8["ms_per_call"]
+
     ext = None
     if not args.no_extend and args.only == "all":
         ext = bench_extend(sgl, W, torch, max(3, args.extend_steps), bf16_peak)
@@ -436,6 +442,8 @@ def run_native(args):
         "gpu_launches": K * launches_per_call,
         "clocks": clocks.summary(),
     }
+    if fp8 is not None:
+        line["fp8_kv"] = fp8
     if ext is not None:
         line["extend"] = ext
     if rank == 0 and args.only == "all" and not args.no_sched:
@@ -514,6 +522,67 @@ def bench_extend(sgl, W, torch, steps, bf16_peak):
             "tokens_per_s": int(ext.sum()) / (ms / 1e3), "steps": steps,
             "kv_write_fused": {"ms_per_call": ms_kv, "tflops": flops / (ms_kv / 1e3) / 1e12,
                                "kv_bytes_written": int(kn.numel() * 2 * 2)}}
+
+
+def bench_fp8(sgl, W, torch, w, kd, vd, inst, steps, hbm_peak, num_sms=0):
+    """The same decode batches on an FP8 (E4M3) copy of the pool: per-tensor
+    scales amax / 448, codes from torch's round-to-nearest conversion (input
+    preparation only; the decode call reads the codes)."""
+    S = kd.shape[0]
+
+    def quant(x):
+        amax = float(x.float().abs().max())
+        sc = amax / 448.0 if amax > 0 else 1.0
+        q = torch.empty(x.shape, dtype=torch.uint8, device="cuda")
+        step = 1 << 16
+        for i in range(0, x.shape[0], step):
+            q[i:i + step] = W.quantize_e4m3(x[i:i + step], sc)
+        return q, sc
+
+    k8, ks = quant(kd)
+    v8, vs = quant(vd)
+    per_tok = 2 * w.Hkv * w.d
+    calls = []
+    for it in inst:
+        gnp = sgl.groups_as_numpy(sgl.sgl_groups_view(it["groups"]))
+        p = sgl.make_params(sgl.SGL_DTYPE_BF16_FP8KV, it["B"], w.Hq, w.Hkv, w.d, S, w.page_size, num_sms=num_sms,
+                            k_scale=ks, v_scale=vs)
+        plan = sgl.sgl_decode_plan(p, it["out"]["seq_lens"], sgl.sgl_groups_view(it["groups"]))
+        ws = torch.zeros(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
+        sgl.sgl_plan_upload(plan, ws)
+        ub = int((gnp["seg_end"] - gnp["seg_begin"]).sum()) * per_tok
+        calls.append(dict(it, plan=plan, ws=ws, ub=ub, o=torch.empty_like(it["o"]), lse=torch.empty_like(it["lse"]),
+                          streamed=sgl.sgl_plan_info(plan)))
+    for s in range(max(3, len(calls))):
+        decode_call(sgl, k8, v8, calls[s % len(calls)])
+    torch.cuda.synchronize()
+    for c in calls:
+        sgl.sgl_check(c["ws"])
+    n = max(len(calls), steps - steps % len(calls))
+    g = torch.cuda.CUDAGraph()
+    st = torch.cuda.Stream()
+    st.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(st):
+        with torch.cuda.graph(g, stream=st):
+            for j in range(n):
+                decode_call(sgl, k8, v8, calls[j % len(calls)])
+    torch.cuda.current_stream().wait_stream(st)
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    for c in calls:
+        sgl.sgl_check(c["ws"])
+    ms = e0.elapsed_time(e1) / n
+    ub = sum(c["ub"] for c in calls) / len(calls)
+    gbs = ub / (ms / 1e3) / 1e9
+    return {"workload": DECODE_WORKLOAD, "kv_dtype": "e4m3 (per-tensor scales)", "ms_per_call": ms,
+            "unique_kv_bytes_per_call": int(ub), "unique_kv_gbs": gbs, "frac_of_hbm": gbs / hbm_peak,
+            "tokens_per_s": inst[0]["B"] / (ms / 1e3), "calls_timed": n,
+            "path": "streaming warps only (no tensor-core tile path for FP8 pools)"}
 
 
 def bench_scheduling(sgl, W, w):

@@ -68,7 +68,11 @@ enum {
     SGL_ERR_WORKSPACE = -7    /* workspace missing, misaligned or too small */
 };
 
-enum { SGL_DTYPE_F32 = 0, SGL_DTYPE_BF16 = 1 };
+enum { SGL_DTYPE_F32 = 0, SGL_DTYPE_BF16 = 1, SGL_DTYPE_BF16_FP8KV = 2 };
+/* SGL_DTYPE_BF16_FP8KV: Q and O bf16, the K and V pools FP8 E4M3 bytes
+ * (decode only); K = k_scale * pool value, V = v_scale * pool value
+ * (per-tensor scales in sgl_attn_params).  ["SGLang 深度拆解" (the FP8 KV
+ * cache halves the KV bytes); CS349D lecture-16 notes §4 (FP8 KV cache)] */
 
 /* Name of a status code (static string). */
 const char* sgl_status_string(int status);
@@ -210,7 +214,7 @@ int sgl_groups_from_table(const int32_t* req_to_token, int64_t ld, const int32_t
 /* ======================================================================== */
 
 typedef struct {
-    int32_t dtype;          /* SGL_DTYPE_F32 or SGL_DTYPE_BF16 (Q, K, V, O) */
+    int32_t dtype;          /* SGL_DTYPE_F32 or SGL_DTYPE_BF16 (Q, K, V, O), or SGL_DTYPE_BF16_FP8KV */
     int32_t batch;          /* B: requests */
     int32_t num_qo_heads;   /* Hq */
     int32_t num_kv_heads;   /* Hkv */
@@ -223,6 +227,9 @@ typedef struct {
      * used to size the launch; they must equal the device arrays. */
     const int32_t* host_prefix_lens;
     const int32_t* host_extend_lens;
+    /* SGL_DTYPE_BF16_FP8KV only: dequantisation scales of the K and V pools */
+    float k_scale;
+    float v_scale;
 } sgl_attn_params;
 
 typedef struct sgl_plan sgl_plan;

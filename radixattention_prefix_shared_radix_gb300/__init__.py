@@ -21,6 +21,7 @@ LIB_PATH = _build.LIB
 SGL_OK = 0
 SGL_DTYPE_F32 = 0
 SGL_DTYPE_BF16 = 1
+SGL_DTYPE_BF16_FP8KV = 2
 
 
 class SglError(RuntimeError):
@@ -53,7 +54,8 @@ class SglAttnParams(ctypes.Structure):
                 ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32),
                 ("num_slots", ctypes.c_int64), ("sm_scale", ctypes.c_float), ("num_sms", ctypes.c_int32),
                 ("host_prefix_lens", ctypes.POINTER(ctypes.c_int32)),
-                ("host_extend_lens", ctypes.POINTER(ctypes.c_int32))]
+                ("host_extend_lens", ctypes.POINTER(ctypes.c_int32)),
+                ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float)]
 
 
 class SglSimConfig(ctypes.Structure):
@@ -324,8 +326,10 @@ def sgl_groups_from_table(req_to_token, seq_lens, groups):
 
 # ------------------------------------------------------------- attention
 def make_params(dtype, batch, num_qo_heads, num_kv_heads, head_dim, num_slots, page_size=1, sm_scale=0.0,
-                num_sms=0, host_prefix_lens=None, host_extend_lens=None):
+                num_sms=0, host_prefix_lens=None, host_extend_lens=None, k_scale=1.0, v_scale=1.0):
     p = SglAttnParams()
+    p.k_scale = k_scale
+    p.v_scale = v_scale
     p.dtype = dtype
     p.batch = batch
     p.num_qo_heads = num_qo_heads

@@ -34,7 +34,7 @@
 #include "merge.cuh"
 
 namespace sgl {
-template <int D>
+template <int D, bool F8>
 int launch_decode_fused(const sgl_plan* plan, const void* q, const void* kp, const void* vp, const int32_t* r2t,
                         int64_t ld, const int32_t* seq_lens, void* o, float* lse, unsigned char* ws, float scale_log2,
                         cudaStream_t s);
@@ -228,8 +228,10 @@ int launch_decode(const sgl_plan* plan, const void* q, const void* kp, const voi
     const sgl_attn_params& p = plan->params;
     const float sl2 = scale_log2_of(&p);
     if (p.batch == 0) return SGL_OK;
-    if (p.dtype == SGL_DTYPE_BF16) {
-        const int e = sgl::launch_decode_fused<D>(plan, q, kp, vp, r2t, ld, seq_lens, o, lse, ws, sl2, s);
+    if (p.dtype == SGL_DTYPE_BF16 || p.dtype == SGL_DTYPE_BF16_FP8KV) {
+        const int e = p.dtype == SGL_DTYPE_BF16
+                          ? sgl::launch_decode_fused<D, false>(plan, q, kp, vp, r2t, ld, seq_lens, o, lse, ws, sl2, s)
+                          : sgl::launch_decode_fused<D, true>(plan, q, kp, vp, r2t, ld, seq_lens, o, lse, ws, sl2, s);
         if (e) return cuda_status(static_cast<cudaError_t>(e));
         return SGL_OK;
     }
@@ -330,6 +332,7 @@ static int extend_impl(const void* q_new, const void* k_new, const void* v_new, 
                        float* lse, void* workspace, size_t ws_bytes, sgl_stream_t stream) {
     int st = sgl::check_params(params);
     if (st) return st;
+    if (params->dtype == SGL_DTYPE_BF16_FP8KV) return SGL_ERR_UNSUPPORTED;   // FP8 KV: decode only
     const int32_t B = params->batch;
     if (B > 0 && (!params->host_extend_lens || !params->host_prefix_lens || !prefix_lens || !extend_lens))
         return SGL_ERR_INVALID_ARG;

@@ -83,10 +83,10 @@ constexpr int kFirstConsumer = kFirstProducer + kProducers;
 constexpr int kFusedThreads = 32 * (kFirstConsumer + kConsumers);
 static_assert(kSQ >= kQD && (kSQ & (kSQ - 1)) == 0 && kQD >= kNSF - 1, "slot ring");
 
-template <int D>
+template <int D, bool F8 = false>
 struct FusedLayout {
     using TL = typename DecCfg<D>::Lay;
-    static constexpr int TILEB = kNP * D * 2;            // one K (or V) tile of a step
+    static constexpr int TILEB = kNP * D * (F8 ? 1 : 2);   // one K (or V) tile of a step
     static constexpr int STAGE = 2 * TILEB;
     static constexpr int RING = kNS * STAGE;             // per consumer, beside the tile roles
     static constexpr int RING_F = kNSF * STAGE;          // per consumer, CTA without tiles (from offset 0)
@@ -98,7 +98,10 @@ struct FusedLayout {
     static constexpr int QSLOT = 8 * D * 2;              // query rows of one piece (at most 8)
     static constexpr int OFF_DESC = OFF_SLOT + kConsumers * SLOTW;   // kNSF stage descriptors (32 B) per consumer
     static constexpr int OFF_Q = (OFF_DESC + kConsumers * kNSF * 32 + 127) / 128 * 128;   // 2 Q slots per consumer
-    static constexpr int OFF_SBAR = OFF_Q + kConsumers * 2 * QSLOT;  // FULL[kNSF], EMPTY[kNSF], QEMPTY[2] per consumer
+    // FP8 pools: each consumer's step converted to f16 K and V tiles
+    static constexpr int CONVW = F8 ? 2 * kNP * D * 2 : 0;
+    static constexpr int OFF_CONV = OFF_Q + kConsumers * 2 * QSLOT;
+    static constexpr int OFF_SBAR = OFF_CONV + kConsumers * CONVW;   // FULL[kNSF], EMPTY[kNSF], QEMPTY[2] per consumer
     static constexpr int END = OFF_SBAR + kConsumers * (2 * kNSF + 2) * 8;
     static constexpr int TOTAL = END + 1024;             // + alignment slack
     static_assert(TOTAL <= 232448, "shared memory per CTA");
@@ -112,12 +115,41 @@ struct FusedArgs {
     int n_init;            // pieces assigned at launch: streaming consumer w starts on piece w
     int n_tile_ctas;       // CTAs 0 .. n_tile_ctas-1 run the wide items first
     uint32_t* sched;       // [2] next piece to hand out, producers finished (restored at the end)
+    float k_scale, v_scale;   // FP8 pools: dequantisation scales
 };
 
 __device__ __forceinline__ uint32_t movtrans(uint32_t x) {
     uint32_t y;
     asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
     return y;
+}
+
+// Four FP8 E4M3 values (one 32-bit word) as two f16x2 words, exactly (every
+// E4M3 value is an f16 value).
+__device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    asm("{\n .reg .b16 a, b;\n mov.b32 {a, b}, %2;\n cvt.rn.f16x2.e4m3x2 %0, a;\n cvt.rn.f16x2.e4m3x2 %1, b;\n}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
+}
+// bf16x2 -> f16x2 (query values: in range and exact for N(0,1)-sized data)
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t x) {
+    const float a = __uint_as_float(x << 16), b = __uint_as_float(x & 0xffff0000u);
+    uint32_t y;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(y) : "f"(b), "f"(a));
+    return y;
+}
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    uint32_t y;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(y) : "f"(hi), "f"(lo));
+    return y;
+}
+// D[16x8] += A[16x16] * B[16x8], f16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma16816_f16(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
 __device__ __forceinline__ int ld_volatile_shared_s32(uint32_t addr) {
@@ -151,11 +183,11 @@ constexpr int kDescP0 = 0, kDescFlags = 4, kDescCm = 8, kDescPb = 12, kDescRows 
 // next piece is fetched in phases spread over the steps (take a number from
 // the counter; load its record; load its members and seq_len), so no register
 // waits on a load in flight.
-template <int D, int NS>
+template <int D, int NS, bool F8 = false>
 __device__ __noinline__ void stream_producer(const FusedArgs& f, int gw, uint32_t ring, uint32_t sring,
                                              uint32_t desc, uint32_t qbuf, uint32_t full, uint32_t empty,
                                              uint32_t qempty, int lane) {
-    using Lay = FusedLayout<D>;
+    using Lay = FusedLayout<D, F8>;
     constexpr int CPR = D / 8;                 // 16-byte chunks per row
     constexpr int RPI = 32 / CPR;              // rows per warp instruction
     constexpr int32_t kPastEnd = INT32_MIN;
@@ -329,15 +361,32 @@ __device__ __noinline__ void stream_producer(const FusedArgs& f, int gw, uint32_
                 sl = -1;
             }
             const uint32_t kd = ring + st * Lay::STAGE, vd = kd + Lay::TILEB;
-            const int ch = lane % CPR;
+            if constexpr (F8) {
+                // FP8 rows of D bytes, row-major [16 x D] tiles (converted by the consumer)
+                constexpr int CPB = D / 16, RPB = 32 / CPB;
+                const int chb = lane % CPB;
+                const uint8_t* kp8 = reinterpret_cast<const uint8_t*>(kp);
+                const uint8_t* vp8 = reinterpret_cast<const uint8_t*>(vp);
 #pragma unroll
-            for (int k = 0; k < kNP / RPI; ++k) {
-                const int rl = k * RPI + lane / CPR;
-                const int32_t sr = __shfl_sync(0xffffffffu, sl, rl);
-                const int64_t off = sr >= 0 ? ((int64_t)sr * Hkv + kvh) * D + ch * 8 : 0;
-                cp_async16_pol(kd + swz<D>(rl, ch), kp + off, sr >= 0, kv_pol);
-                cp_async16_pol(vd + swz<D>(rl, ch), vp + off, sr >= 0, kv_pol);
+                for (int k = 0; k < kNP / RPB; ++k) {
+                    const int rl = k * RPB + lane / CPB;
+                    const int32_t sr = __shfl_sync(0xffffffffu, sl, rl);
+                    const int64_t off = sr >= 0 ? ((int64_t)sr * Hkv + kvh) * D + chb * 16 : 0;
+                    cp_async16_pol(kd + rl * D + chb * 16, kp8 + off, sr >= 0, kv_pol);
+                    cp_async16_pol(vd + rl * D + chb * 16, vp8 + off, sr >= 0, kv_pol);
+                }
+            } else {
+                const int ch = lane % CPR;
+#pragma unroll
+                for (int k = 0; k < kNP / RPI; ++k) {
+                    const int rl = k * RPI + lane / CPR;
+                    const int32_t sr = __shfl_sync(0xffffffffu, sl, rl);
+                    const int64_t off = sr >= 0 ? ((int64_t)sr * Hkv + kvh) * D + ch * 8 : 0;
+                    cp_async16_pol(kd + swz<D>(rl, ch), kp + off, sr >= 0, kv_pol);
+                    cp_async16_pol(vd + swz<D>(rl, ch), vp + off, sr >= 0, kv_pol);
+                }
             }
+            const int ch = lane % CPR;
             if (flags & kFirst) {
                 // the piece's query rows (at most 8) into Q slot nq & 1, swizzled
                 const int qs = nq & 1;
@@ -407,16 +456,19 @@ __device__ __noinline__ void stream_producer(const FusedArgs& f, int gw, uint32_
 // ---------------------------------------------------------------------------
 // Consumer: only shared memory in its loop (stages, descriptors, Q slots)
 // ---------------------------------------------------------------------------
-template <int D, int NS>
+template <int D, int NS, bool F8 = false>
 __device__ __noinline__ void stream_consumer(const FusedArgs& f, uint32_t ring, uint32_t desc, uint32_t qbuf,
-                                             uint32_t full, uint32_t empty, uint32_t qempty, int lane) {
-    using Lay = FusedLayout<D>;
+                                             uint32_t full, uint32_t empty, uint32_t qempty, uint32_t conv, int lane) {
+    using Lay = FusedLayout<D, F8>;
     constexpr int MT = D / 16;                 // m-tiles of O^T
     const int g = lane >> 2, t = lane & 3;
     float* const po = f.t.po;
     float* const plse = f.t.plse;
     uint32_t* const err = f.t.err;
-    const float sc = f.t.scale_log2;
+    // FP8 pools: the K scale goes into the score scale, the V scale into the
+    // final normalisation (both are per tensor, so they factor out)
+    const float sc = F8 ? f.t.scale_log2 * f.k_scale : f.t.scale_log2;
+    const float vsc = F8 ? f.v_scale : 1.f;
 
     uint32_t qcur[D / 8];
     float o[MT][4];
@@ -435,7 +487,7 @@ __device__ __noinline__ void stream_consumer(const FusedArgs& f, uint32_t ring, 
             const int r = 2 * t + hh;
             if (r < cur_rows) {
                 const float ll = hh ? s1 : s0, mm = hh ? m1 : m0;
-                const float inv = ll > 0.f ? 1.f / ll : 0.f;
+                const float inv = ll > 0.f ? vsc / ll : 0.f;
                 float* dst = po + ((int64_t)cur_pb + r) * D + g;
 #pragma unroll
                 for (int i = 0; i < MT; ++i) {
@@ -473,6 +525,10 @@ __device__ __noinline__ void stream_consumer(const FusedArgs& f, uint32_t ring, 
                 ldsm_x4(qb + swz<D>(rq, chunk), qcur[4 * kp2], qcur[4 * kp2 + 1], qcur[4 * kp2 + 2],
                         qcur[4 * kp2 + 3]);
             }
+            if constexpr (F8) {
+#pragma unroll
+                for (int k = 0; k < D / 8; ++k) qcur[k] = bf16x2_to_f16x2(qcur[k]);
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(qempty + 8 * qs);   // the Q slot may be refilled
             ++nq;
@@ -482,7 +538,40 @@ __device__ __noinline__ void stream_consumer(const FusedArgs& f, uint32_t ring, 
             l0 = l1 = 0.f;
         }
         // ---- one step of the current piece at positions cp0 .. cp0+15
-        const uint32_t kb = ring + st * Lay::STAGE, vb = kb + Lay::TILEB;
+        uint32_t kb = ring + st * Lay::STAGE, vb = kb + Lay::TILEB;
+        if constexpr (F8) {
+            // the stage's FP8 K and V rows -> f16 tiles in this consumer's
+            // scratch (lane: row lane / 2, half a row), then the stage is free
+            const int row = lane >> 1, hf = lane & 1;
+#pragma unroll
+            for (int kv = 0; kv < 2; ++kv) {
+                const uint32_t src = (kv ? vb : kb) + row * D + hf * (D / 2);
+                const uint32_t dstt = conv + kv * (kNP * D * 2);
+#pragma unroll
+                for (int j = 0; j < D / 32; ++j) {
+                    uint32_t w0, w1, w2, w3;
+                    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];\n"
+                                 : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
+                                 : "r"(src + 16 * j));
+                    uint32_t h[8];
+                    e4m3x4_to_f16(w0, h[0], h[1]);
+                    e4m3x4_to_f16(w1, h[2], h[3]);
+                    e4m3x4_to_f16(w2, h[4], h[5]);
+                    e4m3x4_to_f16(w3, h[6], h[7]);
+                    const int c0 = hf * (D / 16) + 2 * j;
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(dstt + swz<D>(row, c0)), "r"(h[0]),
+                                 "r"(h[1]), "r"(h[2]), "r"(h[3])
+                                 : "memory");
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(dstt + swz<D>(row, c0 + 1)),
+                                 "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7])
+                                 : "memory");
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty + 8 * st);   // the stage may be refilled
+            kb = conv;
+            vb = conv + kNP * D * 2;
+        }
         // two accumulators halve the dependent MMA chain
         float s[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -490,7 +579,10 @@ __device__ __noinline__ void stream_consumer(const FusedArgs& f, uint32_t ring, 
             uint32_t ka[4];
             const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
             ldsm_x4(kb + swz<D>(row, 2 * ks + (lane >> 4)), ka[0], ka[1], ka[2], ka[3]);
-            mma16816((ks & 1) ? s2 : s, ka, qcur[2 * ks], qcur[2 * ks + 1]);
+            if constexpr (F8)
+                mma16816_f16((ks & 1) ? s2 : s, ka, qcur[2 * ks], qcur[2 * ks + 1]);
+            else
+                mma16816((ks & 1) ? s2 : s, ka, qcur[2 * ks], qcur[2 * ks + 1]);
         }
 #pragma unroll
         for (int k = 0; k < 4; ++k) s[k] += s2[k];
@@ -529,17 +621,20 @@ __device__ __noinline__ void stream_consumer(const FusedArgs& f, uint32_t ring, 
         const float p10 = exp2f(s[2] - u0), p11 = exp2f(s[3] - u1);
         l0 += p00 + p10;
         l1 += p01 + p11;
-        const uint32_t pb0 = movtrans(pack_bf16(p00, p01));
-        const uint32_t pb1 = movtrans(pack_bf16(p10, p11));
+        const uint32_t pb0 = movtrans(F8 ? pack_f16(p00, p01) : pack_bf16(p00, p01));
+        const uint32_t pb1 = movtrans(F8 ? pack_f16(p10, p11) : pack_bf16(p10, p11));
 #pragma unroll
         for (int i = 0; i < MT; ++i) {
             uint32_t va[4];
             const int row = (lane & 7) + (lane >> 4) * 8;
             ldsm_x4_t(vb + swz<D>(row, 2 * i + ((lane >> 3) & 1)), va[0], va[1], va[2], va[3]);
-            mma16816(o[i], va, pb0, pb1);
+            if constexpr (F8)
+                mma16816_f16(o[i], va, pb0, pb1);
+            else
+                mma16816(o[i], va, pb0, pb1);
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(empty + 8 * st);   // the stage may be refilled
+        if (!F8 && lane == 0) mbar_arrive(empty + 8 * st);   // the stage may be refilled
     }
     if (have) finish_item();
 }
@@ -564,11 +659,11 @@ __device__ __forceinline__ void dec_tile_info(const TcArgs& a, int w, int* info)
     info[6] = it.partial_base;
 }
 
-template <int D>
+template <int D, bool F8>
 __global__ void __maxnreg__(128) decode_fused_kernel(const __grid_constant__ FusedArgs f,
                                                      const __grid_constant__ CUtensorMap tmk,
                                                      const __grid_constant__ CUtensorMap tmv) {
-    using Lay = FusedLayout<D>;
+    using Lay = FusedLayout<D, F8>;
     using TC = DecCfg<D>;
     using TL = typename TC::Lay;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -580,7 +675,7 @@ __global__ void __maxnreg__(128) decode_fused_kernel(const __grid_constant__ Fus
     grid_dep_wait();
     grid_dep_launch();
     const int w0 = __ldg(f.wptr + blockIdx.x), w1 = __ldg(f.wptr + blockIdx.x + 1);
-    const bool tiles = w1 > w0;
+    const bool tiles = !F8 && w1 > w0;   // FP8 pools have no tile path
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + TL::OFF_TMEM);
     int* info = reinterpret_cast<int*>(sm + TL::OFF_INFO);
     const uint32_t sbar = smem_u32(sm + Lay::OFF_SBAR);
@@ -609,7 +704,7 @@ __global__ void __maxnreg__(128) decode_fused_kernel(const __grid_constant__ Fus
 
     constexpr int kStreamGate = 3;   // named barrier: tile roles done -> streaming may start
     constexpr int kTileWarps = TC::kThreads / 32;   // softmax, MMA, gather team (incl. the producers)
-    if (tiles && warp < kTileWarps) {
+    if constexpr (!F8) if (tiles && warp < kTileWarps) {
         // the tile roles; the producer warps are part of the gather team and
         // go on to stream once the CTA's tiles are done
         const uint32_t tbase = *tslot;
@@ -632,21 +727,22 @@ __global__ void __maxnreg__(128) decode_fused_kernel(const __grid_constant__ Fus
         const uint32_t desc = smem_u32(sm + Lay::OFF_DESC + c * kNSF * 32);
         const uint32_t qb = smem_u32(sm + Lay::OFF_Q + c * 2 * Lay::QSLOT);
         if (tiles)
-            stream_producer<D, kNS>(f, gws, smem_u32(sm + Lay::OFF_RING + c * Lay::RING), sring, desc, qb, full_of(c),
-                                    empty_of(c), qempty_of(c), lane);
+            stream_producer<D, kNS, F8>(f, gws, smem_u32(sm + Lay::OFF_RING + c * Lay::RING), sring, desc, qb,
+                                        full_of(c), empty_of(c), qempty_of(c), lane);
         else
-            stream_producer<D, kNSF>(f, gws, smem_u32(sm + c * Lay::RING_F), sring, desc, qb, full_of(c), empty_of(c),
-                                     qempty_of(c), lane);
+            stream_producer<D, kNSF, F8>(f, gws, smem_u32(sm + c * Lay::RING_F), sring, desc, qb, full_of(c),
+                                         empty_of(c), qempty_of(c), lane);
     } else if (warp >= kFirstConsumer) {
         const int c = warp - kFirstConsumer;
         const uint32_t desc = smem_u32(sm + Lay::OFF_DESC + c * kNSF * 32);
         const uint32_t qb = smem_u32(sm + Lay::OFF_Q + c * 2 * Lay::QSLOT);
+        const uint32_t conv = smem_u32(sm + Lay::OFF_CONV + c * Lay::CONVW);
         if (tiles)
-            stream_consumer<D, kNS>(f, smem_u32(sm + Lay::OFF_RING + c * Lay::RING), desc, qb, full_of(c), empty_of(c),
-                                    qempty_of(c), lane);
+            stream_consumer<D, kNS, F8>(f, smem_u32(sm + Lay::OFF_RING + c * Lay::RING), desc, qb, full_of(c),
+                                        empty_of(c), qempty_of(c), conv, lane);
         else
-            stream_consumer<D, kNSF>(f, smem_u32(sm + c * Lay::RING_F), desc, qb, full_of(c), empty_of(c), qempty_of(c),
-                                     lane);
+            stream_consumer<D, kNSF, F8>(f, smem_u32(sm + c * Lay::RING_F), desc, qb, full_of(c), empty_of(c),
+                                         qempty_of(c), conv, lane);
     }
     tc_fence_before();
     __syncthreads();
@@ -658,12 +754,12 @@ __global__ void __maxnreg__(128) decode_fused_kernel(const __grid_constant__ Fus
 
 }  // namespace
 
-template <int D>
+template <int D, bool F8>
 int launch_decode_fused(const sgl_plan* plan, const void* q, const void* kp, const void* vp, const int32_t* r2t,
                         int64_t ld, const int32_t* seq_lens, void* o, float* lse, unsigned char* ws, float scale_log2,
                         cudaStream_t s) {
-    using Lay = FusedLayout<D>;
-    static const int attr = (int)cudaFuncSetAttribute(decode_fused_kernel<D>,
+    using Lay = FusedLayout<D, F8>;
+    static const int attr = (int)cudaFuncSetAttribute(decode_fused_kernel<D, F8>,
                                                       cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::TOTAL);
     if (attr) return attr;
     const sgl_attn_params& p = plan->params;
@@ -695,6 +791,8 @@ int launch_decode_fused(const sgl_plan* plan, const void* q, const void* kp, con
     f.n_init = plan->n_init;
     f.n_tile_ctas = plan->n_tile_ctas;
     f.sched = reinterpret_cast<uint32_t*>(ws + plan->off_sched);
+    f.k_scale = p.k_scale;
+    f.v_scale = p.v_scale;
     // Both launches are programmatic dependents of the kernel before them:
     // each waits (griddepcontrol.wait) before its first memory access, so
     // only the launch and scheduling overlap the previous grid's tail.
@@ -708,7 +806,7 @@ int launch_decode_fused(const sgl_plan* plan, const void* q, const void* kp, con
     cfg.stream = s;
     cfg.attrs = pdl;
     cfg.numAttrs = 1;
-    int e = (int)cudaLaunchKernelEx(&cfg, decode_fused_kernel<D>, f, mk, mv);
+    int e = (int)cudaLaunchKernelEx(&cfg, decode_fused_kernel<D, F8>, f, mk, mv);
     if (e) return e;
     MergeArgs m{a.po, a.plse, reinterpret_cast<const int32_t*>(ws + plan->off_mptr),
                 reinterpret_cast<const int32_t*>(ws + plan->off_ment), o, lse, a.Hq, a.Hkv, a.G};
@@ -719,9 +817,15 @@ int launch_decode_fused(const sgl_plan* plan, const void* q, const void* kp, con
     return (int)cudaLaunchKernelEx(&cfg, decode_merge_kernel<bf16, D>, m, n_pairs);
 }
 
-template int launch_decode_fused<64>(const sgl_plan*, const void*, const void*, const void*, const int32_t*, int64_t,
-                                     const int32_t*, void*, float*, unsigned char*, float, cudaStream_t);
-template int launch_decode_fused<128>(const sgl_plan*, const void*, const void*, const void*, const int32_t*, int64_t,
-                                      const int32_t*, void*, float*, unsigned char*, float, cudaStream_t);
+template int launch_decode_fused<64, false>(const sgl_plan*, const void*, const void*, const void*, const int32_t*,
+                                            int64_t, const int32_t*, void*, float*, unsigned char*, float, cudaStream_t);
+template int launch_decode_fused<128, false>(const sgl_plan*, const void*, const void*, const void*, const int32_t*,
+                                             int64_t, const int32_t*, void*, float*, unsigned char*, float,
+                                             cudaStream_t);
+template int launch_decode_fused<64, true>(const sgl_plan*, const void*, const void*, const void*, const int32_t*,
+                                           int64_t, const int32_t*, void*, float*, unsigned char*, float, cudaStream_t);
+template int launch_decode_fused<128, true>(const sgl_plan*, const void*, const void*, const void*, const int32_t*,
+                                            int64_t, const int32_t*, void*, float*, unsigned char*, float,
+                                            cudaStream_t);
 
 }  // namespace sgl

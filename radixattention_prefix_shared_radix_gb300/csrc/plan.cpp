@@ -49,7 +49,9 @@ int check_params(const sgl_attn_params* p) {
     if (!p) return SGL_ERR_INVALID_ARG;
     if (p->batch < 0 || p->num_qo_heads <= 0 || p->num_kv_heads <= 0 || p->num_slots < 0 || p->page_size < 1)
         return SGL_ERR_INVALID_ARG;
-    if (p->dtype != SGL_DTYPE_F32 && p->dtype != SGL_DTYPE_BF16) return SGL_ERR_UNSUPPORTED;
+    if (p->dtype != SGL_DTYPE_F32 && p->dtype != SGL_DTYPE_BF16 && p->dtype != SGL_DTYPE_BF16_FP8KV)
+        return SGL_ERR_UNSUPPORTED;
+    if (p->dtype == SGL_DTYPE_BF16_FP8KV && !(p->k_scale > 0.f && p->v_scale > 0.f)) return SGL_ERR_INVALID_ARG;
     if (p->head_dim != 64 && p->head_dim != 128) return SGL_ERR_UNSUPPORTED;
     if (p->num_qo_heads % p->num_kv_heads) return SGL_ERR_UNSUPPORTED;
     int G = p->num_qo_heads / p->num_kv_heads;
@@ -118,14 +120,18 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
     std::vector<Unit> units;
     int64_t units_n = 0;
     int64_t max_wide = 0;
+    // FP8 KV pools have no tensor-core tile path: every segment is streamed,
+    // a wide one in member blocks of the narrow width
+    const bool all_narrow = p->dtype == SGL_DTYPE_BF16_FP8KV;
     for (int32_t s = 0; s < nseg; ++s) {
         const int32_t b = g->seg_begin[s], e = g->seg_end[s];
         const int32_t m0 = g->seg_member_ptr[s], nmem = g->seg_member_ptr[s + 1] - m0;
-        if (nmem <= MBn) {
-            for (int32_t h = 0; h < Hkv; ++h) {
-                units.push_back({g->seg_row[s], b, e, h, m0, nmem});
-                units_n += e - b;
-            }
+        if (nmem <= MBn || all_narrow) {
+            for (int32_t mb = 0; mb < nmem; mb += MBn)
+                for (int32_t h = 0; h < Hkv; ++h) {
+                    units.push_back({g->seg_row[s], b, e, h, m0 + mb, std::min(MBn, nmem - mb)});
+                    units_n += e - b;
+                }
         } else {
             max_wide = std::max<int64_t>(max_wide, e - b);
         }
@@ -173,7 +179,7 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
     for (int32_t s = 0; s < nseg; ++s) {
         const int32_t b = g->seg_begin[s], e = g->seg_end[s];
         const int32_t m0 = g->seg_member_ptr[s], nmem = g->seg_member_ptr[s + 1] - m0;
-        if (nmem <= MBn) continue;
+        if (nmem <= MBn || all_narrow) continue;
         const int32_t nblk = (nmem + MBw - 1) / MBw;
         for (int64_t cb = b; cb < e; cb += Cw) {
             const int32_t ce = (int32_t)std::min<int64_t>(e, cb + Cw);

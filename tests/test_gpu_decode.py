@@ -222,3 +222,49 @@ def test_decode_repeated_calls_share_one_upload(num_sms):
                      *tolerances(case.w))
     finally:
         case.close()
+
+
+# ---------------------------------------------------------------------------
+# FP8 (E4M3) KV cache
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("name,num_sms", [("llama3_8b_decode_small", 0), ("llama3_8b_decode_small", 3),
+                                          ("multiturn_small", 0), ("fork_tree_small", 0)])
+def test_decode_fp8_kv_elementwise(name, num_sms):
+    """FP8 pools (per-tensor scales) against the oracle on the decoded values."""
+    from oracle.fp8 import DequantView
+    case = Case(name)
+    try:
+        ks, vs = 1.0 / 32, 1.0 / 48
+        k8, v8 = W.quantize_e4m3(case.K, ks), W.quantize_e4m3(case.V, vs)
+        w = case.w
+        p = sgl.make_params(sgl.SGL_DTYPE_BF16_FP8KV, case.B, w.Hq, w.Hkv, w.d, case.S, w.page_size,
+                            num_sms=num_sms, k_scale=ks, v_scale=vs)
+        plan = sgl.sgl_decode_plan(p, case.out["seq_lens"], sgl.sgl_groups_view(case.groups))
+        ws = torch.zeros(max(plan.workspace_bytes, 256), dtype=torch.uint8, device="cuda")
+        sgl.sgl_plan_upload(plan, ws)
+        qd = case.q_host().cuda()
+        table = torch.from_numpy(case.out["req_to_token"]).cuda()
+        seq = torch.from_numpy(case.out["seq_lens"]).cuda()
+        o = torch.empty_like(qd)
+        lse = torch.empty(case.B, w.Hq, dtype=torch.float32, device="cuda")
+        sgl.sgl_decode_attn(qd, k8.cuda(), v8.cuda(), table, seq, plan, o, lse, ws)
+        sgl.sgl_check(ws)
+        Oref, Lref = decode_attention(case.oracle_q(), DequantView(k8, ks), DequantView(v8, vs), case.oracle_table,
+                                      case.out["seq_lens"])
+        assert_close(o.double().cpu().numpy(), lse.cpu().numpy().astype(np.float64), Oref, Lref, *tolerances(w))
+        del plan
+    finally:
+        case.close()
+
+
+def test_fp8_kv_extend_is_unsupported():
+    w = W.get("extend_small")
+    p = sgl.make_params(sgl.SGL_DTYPE_BF16_FP8KV, 1, w.Hq, w.Hkv, w.d, 1024, 1, k_scale=1.0, v_scale=1.0,
+                        host_prefix_lens=np.array([0], dtype=np.int32), host_extend_lens=np.array([1], dtype=np.int32))
+    with pytest.raises(sgl.SglError):
+        sgl.sgl_extend_workspace_bytes(p)
+        z = torch.zeros(16, dtype=torch.uint8, device="cuda")
+        sgl.sgl_extend_attn(z, z, z, torch.zeros((1, 1), dtype=torch.int32, device="cuda"),
+                            torch.zeros(1, dtype=torch.int32, device="cuda"),
+                            torch.ones(1, dtype=torch.int32, device="cuda"), p, z, torch.zeros(1, device="cuda"),
+                            torch.zeros(256, dtype=torch.uint8, device="cuda"))

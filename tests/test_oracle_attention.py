@@ -243,3 +243,14 @@ def test_chunked_prefill_with_kv_write_is_causal_sdpa_and_ends_in_decode():
     assert np.allclose(O, ref[0].permute(1, 0, 2).numpy(), atol=1e-12)
     Od, Ld = decode_attention(q[L - 1:L], Kc, Vc, t, [L])
     assert np.allclose(O[L - 1:L], Od, atol=1e-13) and np.allclose(LSE[L - 1:L], Ld, atol=1e-13)
+
+
+def test_e4m3_decoding_equals_torch_for_all_codes():
+    from oracle.fp8 import e4m3_to_float
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = e4m3_to_float(codes)
+    both_nan = np.isnan(ref) & np.isnan(got)
+    assert np.array_equal(both_nan, np.isnan(ref)) and np.array_equal(got[~both_nan], ref[~both_nan])
+    # closed forms: largest finite 448, smallest subnormal 2^-9, one = 0x38
+    assert got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9 and got[0x38] == 1.0 and got[0xB8] == -1.0

@@ -1,0 +1,43 @@
+"""Decode planner invariants on the host (no GPU): the plan is host code, so
+its counts can be checked here against the batch's prefix groups."""
+
+import pytest
+
+import radixattention_prefix_shared_radix_gb300 as sgl
+from tests._harness import Case
+
+
+@pytest.fixture(scope="module")
+def case():
+    c = Case("llama3_8b_decode_small")
+    yield c
+    c.close()
+
+
+def _plan(case, dtype, **kw):
+    w = case.w
+    p = sgl.make_params(dtype, case.B, w.Hq, w.Hkv, w.d, case.S, w.page_size, num_sms=152, **kw)
+    plan = sgl.sgl_decode_plan(p, case.out["seq_lens"], sgl.sgl_groups_view(case.groups))
+    return sgl.sgl_plan_info(plan)
+
+
+def test_every_partial_row_group_is_merged_once(case):
+    G = case.w.Hq // case.w.Hkv
+    for dt, kw in ((sgl.SGL_DTYPE_BF16, {}), (sgl.SGL_DTYPE_BF16_FP8KV, dict(k_scale=0.5, v_scale=0.25))):
+        info = _plan(case, dt, **kw)
+        assert info["num_partial_rows"] == info["num_merge_entries"] * G
+
+
+def test_shared_prefix_takes_tiles_only_for_bf16(case):
+    # the batch shares a long prefix among more members than a streaming
+    # warp's 8 query rows, so bf16 plans tensor-core tiles for it
+    assert _plan(case, sgl.SGL_DTYPE_BF16)["num_wide_items"] > 0
+    # an FP8 pool streams every segment: no tile items may be planned (their
+    # partial rows would be merged without ever being written)
+    assert _plan(case, sgl.SGL_DTYPE_BF16_FP8KV, k_scale=0.5, v_scale=0.25)["num_wide_items"] == 0
+
+
+@pytest.mark.parametrize("ks,vs", [(0.0, 1.0), (1.0, -1.0)])
+def test_fp8_scales_must_be_positive(case, ks, vs):
+    with pytest.raises(sgl.SglError):
+        _plan(case, sgl.SGL_DTYPE_BF16_FP8KV, k_scale=ks, v_scale=vs)

@@ -358,3 +358,10 @@ def multi_turn_trace(conversations, turns, sys_len, user=(16, 64), output=(16, 6
             hist = np.concatenate([prompt, out])
     # requests must come after the ones they depend on: order by conversation turn
     return reqs
+
+
+def quantize_e4m3(t, scale):
+    """A pool for the FP8 KV cache: torch CPU tensor -> uint8 E4M3 codes of
+    t / scale (torch's round-to-nearest conversion)."""
+    import torch
+    return (t.float() / float(scale)).to(torch.float8_e4m3fn).view(torch.uint8)
