@@ -582,7 +582,7 @@ def bench_fp8(sgl, W, torch, w, kd, vd, inst, steps, hbm_peak, num_sms=0):
     return {"workload": DECODE_WORKLOAD, "kv_dtype": "e4m3 (per-tensor scales)", "ms_per_call": ms,
             "unique_kv_bytes_per_call": int(ub), "unique_kv_gbs": gbs, "frac_of_hbm": gbs / hbm_peak,
             "tokens_per_s": inst[0]["B"] / (ms / 1e3), "calls_timed": n,
-            "path": "streaming warps only (no tensor-core tile path for FP8 pools)"}
+            "path": "same plan as bf16: shared prefixes on tcgen05 tiles (codes converted to f16 in shared memory), the rest on streaming warps"}
 
 
 def bench_scheduling(sgl, W, w):

@@ -85,25 +85,31 @@ static_assert(kSQ >= kQD && (kSQ & (kSQ - 1)) == 0 && kQD >= kNSF - 1, "slot rin
 
 template <int D, bool F8 = false>
 struct FusedLayout {
-    using TL = typename DecCfg<D>::Lay;
+    using TL = typename DecCfg<D, F8>::Lay;
     static constexpr int TILEB = kNP * D * (F8 ? 1 : 2);   // one K (or V) tile of a step
     static constexpr int STAGE = 2 * TILEB;
     static constexpr int RING = kNS * STAGE;             // per consumer, beside the tile roles
     static constexpr int RING_F = kNSF * STAGE;          // per consumer, CTA without tiles (from offset 0)
     static constexpr int SLOTW = kSQ * kSlotEntry;       // slot ring per consumer
-    static constexpr int OFF_RING = (TL::END + 127) / 128 * 128;
+    // Layout from offset 0: the tile roles' K/V stages and barriers (TL, up
+    // to TL::KEEP), then the rings of a CTA with tiles, the slot rings,
+    // descriptors and Q slots.  These are used only once the CTA's tiles are
+    // done, so they may overlap the tiles' FP8 staging area (TL::KEEP ..
+    // TL::END).  A CTA without tiles puts its deeper rings at offset 0.  The
+    // streaming barriers, initialised at launch, come after everything.
+    static constexpr int OFF_RING = (TL::KEEP + 127) / 128 * 128;
     static constexpr int END_RINGS = (OFF_RING + kConsumers * RING) > kConsumers * RING_F
                                          ? (OFF_RING + kConsumers * RING) : kConsumers * RING_F;
     static constexpr int OFF_SLOT = END_RINGS;
     static constexpr int QSLOT = 8 * D * 2;              // query rows of one piece (at most 8)
     static constexpr int OFF_DESC = OFF_SLOT + kConsumers * SLOTW;   // kNSF stage descriptors (32 B) per consumer
     static constexpr int OFF_Q = (OFF_DESC + kConsumers * kNSF * 32 + 127) / 128 * 128;   // 2 Q slots per consumer
-    // FP8 pools: each consumer's step converted to f16 K and V tiles
-    static constexpr int CONVW = F8 ? 2 * kNP * D * 2 : 0;
-    static constexpr int OFF_CONV = OFF_Q + kConsumers * 2 * QSLOT;
-    static constexpr int OFF_SBAR = OFF_CONV + kConsumers * CONVW;   // FULL[kNSF], EMPTY[kNSF], QEMPTY[2] per consumer
+    static constexpr int END_Q = OFF_Q + kConsumers * 2 * QSLOT;
+    // FULL[kNSF], EMPTY[kNSF], QEMPTY[2] per consumer
+    static constexpr int OFF_SBAR = ((END_Q > TL::END ? END_Q : TL::END) + 7) / 8 * 8;
     static constexpr int END = OFF_SBAR + kConsumers * (2 * kNSF + 2) * 8;
     static constexpr int TOTAL = END + 1024;             // + alignment slack
+    static_assert(OFF_SBAR >= TL::END && OFF_SBAR >= END_Q, "streaming barriers clear of every other area");
     static_assert(TOTAL <= 232448, "shared memory per CTA");
 };
 
@@ -115,7 +121,6 @@ struct FusedArgs {
     int n_init;            // pieces assigned at launch: streaming consumer w starts on piece w
     int n_tile_ctas;       // CTAs 0 .. n_tile_ctas-1 run the wide items first
     uint32_t* sched;       // [2] next piece to hand out, producers finished (restored at the end)
-    float k_scale, v_scale;   // FP8 pools: dequantisation scales
 };
 
 __device__ __forceinline__ uint32_t movtrans(uint32_t x) {
@@ -124,25 +129,6 @@ __device__ __forceinline__ uint32_t movtrans(uint32_t x) {
     return y;
 }
 
-// Four FP8 E4M3 values (one 32-bit word) as two f16x2 words, exactly (every
-// E4M3 value is an f16 value).
-__device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
-    asm("{\n .reg .b16 a, b;\n mov.b32 {a, b}, %2;\n cvt.rn.f16x2.e4m3x2 %0, a;\n cvt.rn.f16x2.e4m3x2 %1, b;\n}"
-        : "=r"(lo), "=r"(hi)
-        : "r"(w));
-}
-// bf16x2 -> f16x2 (query values: in range and exact for N(0,1)-sized data)
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t x) {
-    const float a = __uint_as_float(x << 16), b = __uint_as_float(x & 0xffff0000u);
-    uint32_t y;
-    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(y) : "f"(b), "f"(a));
-    return y;
-}
-__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
-    uint32_t y;
-    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(y) : "f"(hi), "f"(lo));
-    return y;
-}
 // D[16x8] += A[16x16] * B[16x8], f16 inputs, fp32 accumulate.
 __device__ __forceinline__ void mma16816_f16(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
     asm volatile(
@@ -150,6 +136,25 @@ __device__ __forceinline__ void mma16816_f16(float* c, const uint32_t* a, uint32
         "{%0,%1,%2,%3};\n"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// 16-byte chunk c of row r of an FP8 [16 x D] stage tile (rows of D bytes),
+// XOR-swizzled so that the consumer's fragment reads (below) are free of
+// bank conflicts for D = 128 (two-way for D = 64).
+template <int D>
+__device__ __forceinline__ uint32_t fswz(int r, int c) {
+    return (uint32_t)(r * D + ((c ^ (D == 128 ? (r & 7) : ((r >> 1) & 3))) << 4));
+}
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+__device__ __forceinline__ void lds128(uint32_t addr, uint32_t* w) {
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];\n" : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "r"(addr));
+}
+__device__ __forceinline__ void lds64(uint32_t addr, uint32_t* w) {
+    asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];\n" : "=r"(w[0]), "=r"(w[1]) : "r"(addr));
 }
 
 __device__ __forceinline__ int ld_volatile_shared_s32(uint32_t addr) {
@@ -362,7 +367,7 @@ __device__ __noinline__ void stream_producer(const FusedArgs& f, int gw, uint32_
             }
             const uint32_t kd = ring + st * Lay::STAGE, vd = kd + Lay::TILEB;
             if constexpr (F8) {
-                // FP8 rows of D bytes, row-major [16 x D] tiles (converted by the consumer)
+                // FP8 rows of D bytes, [16 x D] tiles with swizzled chunks
                 constexpr int CPB = D / 16, RPB = 32 / CPB;
                 const int chb = lane % CPB;
                 const uint8_t* kp8 = reinterpret_cast<const uint8_t*>(kp);
@@ -372,8 +377,8 @@ __device__ __noinline__ void stream_producer(const FusedArgs& f, int gw, uint32_
                     const int rl = k * RPB + lane / CPB;
                     const int32_t sr = __shfl_sync(0xffffffffu, sl, rl);
                     const int64_t off = sr >= 0 ? ((int64_t)sr * Hkv + kvh) * D + chb * 16 : 0;
-                    cp_async16_pol(kd + rl * D + chb * 16, kp8 + off, sr >= 0, kv_pol);
-                    cp_async16_pol(vd + rl * D + chb * 16, vp8 + off, sr >= 0, kv_pol);
+                    cp_async16_pol(kd + fswz<D>(rl, chb), kp8 + off, sr >= 0, kv_pol);
+                    cp_async16_pol(vd + fswz<D>(rl, chb), vp8 + off, sr >= 0, kv_pol);
                 }
             } else {
                 const int ch = lane % CPR;
@@ -458,7 +463,7 @@ __device__ __noinline__ void stream_producer(const FusedArgs& f, int gw, uint32_
 // ---------------------------------------------------------------------------
 template <int D, int NS, bool F8 = false>
 __device__ __noinline__ void stream_consumer(const FusedArgs& f, uint32_t ring, uint32_t desc, uint32_t qbuf,
-                                             uint32_t full, uint32_t empty, uint32_t qempty, uint32_t conv, int lane) {
+                                             uint32_t full, uint32_t empty, uint32_t qempty, int lane) {
     using Lay = FusedLayout<D, F8>;
     constexpr int MT = D / 16;                 // m-tiles of O^T
     const int g = lane >> 2, t = lane & 3;
@@ -467,8 +472,8 @@ __device__ __noinline__ void stream_consumer(const FusedArgs& f, uint32_t ring, 
     uint32_t* const err = f.t.err;
     // FP8 pools: the K scale goes into the score scale, the V scale into the
     // final normalisation (both are per tensor, so they factor out)
-    const float sc = F8 ? f.t.scale_log2 * f.k_scale : f.t.scale_log2;
-    const float vsc = F8 ? f.v_scale : 1.f;
+    const float sc = F8 ? f.t.scale_log2 * f.t.k_scale : f.t.scale_log2;
+    const float vsc = F8 ? f.t.v_scale : 1.f;
 
     uint32_t qcur[D / 8];
     float o[MT][4];
@@ -488,11 +493,19 @@ __device__ __noinline__ void stream_consumer(const FusedArgs& f, uint32_t ring, 
             if (r < cur_rows) {
                 const float ll = hh ? s1 : s0, mm = hh ? m1 : m0;
                 const float inv = ll > 0.f ? vsc / ll : 0.f;
-                float* dst = po + ((int64_t)cur_pb + r) * D + g;
+                if constexpr (F8) {
+                    // m-tile i rows g, g + 8 stand for d = (D/8) g + 2i, + 1
+                    float* dst = po + ((int64_t)cur_pb + r) * D + (D / 8) * g;
 #pragma unroll
-                for (int i = 0; i < MT; ++i) {
-                    dst[16 * i] = o[i][hh] * inv;
-                    dst[16 * i + 8] = o[i][2 + hh] * inv;
+                    for (int i = 0; i < MT; ++i)
+                        *reinterpret_cast<float2*>(dst + 2 * i) = make_float2(o[i][hh] * inv, o[i][2 + hh] * inv);
+                } else {
+                    float* dst = po + ((int64_t)cur_pb + r) * D + g;
+#pragma unroll
+                    for (int i = 0; i < MT; ++i) {
+                        dst[16 * i] = o[i][hh] * inv;
+                        dst[16 * i + 8] = o[i][2 + hh] * inv;
+                    }
                 }
                 if (g == 0) plse[(int64_t)cur_pb + r] = ll > 0.f ? (mm + log2f(ll)) * kLn2 : -INFINITY;
             }
@@ -519,15 +532,21 @@ __device__ __noinline__ void stream_consumer(const FusedArgs& f, uint32_t ring, 
             const int qs = ld_shared_s32(db + kDescQ);
             // Q^T fragments: row g (the N index), k-step ks -> chunks 2ks, 2ks+1
             const uint32_t qb = qbuf + qs * Lay::QSLOT;
-#pragma unroll
-            for (int kp2 = 0; kp2 < D / 32; ++kp2) {
-                const int rq = lane & 7, chunk = 4 * kp2 + (lane >> 3);
-                ldsm_x4(qb + swz<D>(rq, chunk), qcur[4 * kp2], qcur[4 * kp2 + 1], qcur[4 * kp2 + 2],
-                        qcur[4 * kp2 + 3]);
-            }
             if constexpr (F8) {
+                // row g's elements (D/4) t .. (D/4) t + D/4 - 1, in order:
+                // k-step ks takes elements 4 ks .. 4 ks + 3 of the run (the
+                // order of the lane's K codes below), as f16
+#pragma unroll
+                for (int j = 0; j < D / 32; ++j) lds128(qb + swz<D>(g, (D / 32) * t + j), qcur + 4 * j);
 #pragma unroll
                 for (int k = 0; k < D / 8; ++k) qcur[k] = bf16x2_to_f16x2(qcur[k]);
+            } else {
+#pragma unroll
+                for (int kp2 = 0; kp2 < D / 32; ++kp2) {
+                    const int rq = lane & 7, chunk = 4 * kp2 + (lane >> 3);
+                    ldsm_x4(qb + swz<D>(rq, chunk), qcur[4 * kp2], qcur[4 * kp2 + 1], qcur[4 * kp2 + 2],
+                            qcur[4 * kp2 + 3]);
+                }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(qempty + 8 * qs);   // the Q slot may be refilled
@@ -538,51 +557,49 @@ __device__ __noinline__ void stream_consumer(const FusedArgs& f, uint32_t ring, 
             l0 = l1 = 0.f;
         }
         // ---- one step of the current piece at positions cp0 .. cp0+15
-        uint32_t kb = ring + st * Lay::STAGE, vb = kb + Lay::TILEB;
+        const uint32_t kb = ring + st * Lay::STAGE, vb = kb + Lay::TILEB;
+        // FP8 stages go straight from the codes into MMA fragments.  The d
+        // index of S^T = K Q^T is contracted, so lane (g, t) takes the D/4
+        // codes (D/4) t .. of K rows g and g + 8, in order, as its k-slots
+        // {2t, 2t+1, 2t+8, 2t+9} of k-steps 0, 1, ... (Q's fragments hold the
+        // same elements).  In O^T = V^T P^T, d is the M index: m-tile i rows
+        // g and g + 8 stand for d = (D/8) g + 2i and + 1, so the lane needs
+        // the D/8 codes (D/8) g .. of V rows 2t, 2t+1, 2t+8, 2t+9 (its
+        // k-slots), paired across rows with byte permutes.  The stage is
+        // free as soon as the codes are in registers.
+        constexpr int KWD = F8 ? D / 16 : 1, VWD = F8 ? D / 32 : 1;
+        uint32_t kw[2][KWD], vw[4][VWD];
         if constexpr (F8) {
-            // the stage's FP8 K and V rows -> f16 tiles in this consumer's
-            // scratch (lane: row lane / 2, half a row), then the stage is free
-            const int row = lane >> 1, hf = lane & 1;
 #pragma unroll
-            for (int kv = 0; kv < 2; ++kv) {
-                const uint32_t src = (kv ? vb : kb) + row * D + hf * (D / 2);
-                const uint32_t dstt = conv + kv * (kNP * D * 2);
+            for (int h = 0; h < 2; ++h) {
 #pragma unroll
-                for (int j = 0; j < D / 32; ++j) {
-                    uint32_t w0, w1, w2, w3;
-                    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];\n"
-                                 : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
-                                 : "r"(src + 16 * j));
-                    uint32_t h[8];
-                    e4m3x4_to_f16(w0, h[0], h[1]);
-                    e4m3x4_to_f16(w1, h[2], h[3]);
-                    e4m3x4_to_f16(w2, h[4], h[5]);
-                    e4m3x4_to_f16(w3, h[6], h[7]);
-                    const int c0 = hf * (D / 16) + 2 * j;
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(dstt + swz<D>(row, c0)), "r"(h[0]),
-                                 "r"(h[1]), "r"(h[2]), "r"(h[3])
-                                 : "memory");
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(dstt + swz<D>(row, c0 + 1)),
-                                 "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7])
-                                 : "memory");
-                }
+                for (int j = 0; j < D / 64; ++j) lds128(kb + fswz<D>(g + 8 * h, (D / 64) * t + j), kw[h] + 4 * j);
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int r = 2 * t + (e & 1) + 8 * (e >> 1);
+                if constexpr (D == 128)
+                    lds128(vb + fswz<D>(r, g), vw[e]);
+                else
+                    lds64(vb + fswz<D>(r, g >> 1) + 8 * (g & 1), vw[e]);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(empty + 8 * st);   // the stage may be refilled
-            kb = conv;
-            vb = conv + kNP * D * 2;
         }
         // two accumulators halve the dependent MMA chain
         float s[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
             uint32_t ka[4];
-            const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
-            ldsm_x4(kb + swz<D>(row, 2 * ks + (lane >> 4)), ka[0], ka[1], ka[2], ka[3]);
-            if constexpr (F8)
+            if constexpr (F8) {
+                e4m3x4_to_f16(kw[0][ks], ka[0], ka[2]);
+                e4m3x4_to_f16(kw[1][ks], ka[1], ka[3]);
                 mma16816_f16((ks & 1) ? s2 : s, ka, qcur[2 * ks], qcur[2 * ks + 1]);
-            else
+            } else {
+                const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
+                ldsm_x4(kb + swz<D>(row, 2 * ks + (lane >> 4)), ka[0], ka[1], ka[2], ka[3]);
                 mma16816((ks & 1) ? s2 : s, ka, qcur[2 * ks], qcur[2 * ks + 1]);
+            }
         }
 #pragma unroll
         for (int k = 0; k < 4; ++k) s[k] += s2[k];
@@ -626,12 +643,17 @@ __device__ __noinline__ void stream_consumer(const FusedArgs& f, uint32_t ring, 
 #pragma unroll
         for (int i = 0; i < MT; ++i) {
             uint32_t va[4];
-            const int row = (lane & 7) + (lane >> 4) * 8;
-            ldsm_x4_t(vb + swz<D>(row, 2 * i + ((lane >> 3) & 1)), va[0], va[1], va[2], va[3]);
-            if constexpr (F8)
+            if constexpr (F8) {
+                // bytes 2 (i & 1), + 1 of word i / 2 of rows (2t, 2t+1) and (2t+8, 2t+9)
+                const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;
+                e4m3x4_to_f16(prmt(vw[0][i / 2], vw[1][i / 2], sel), va[0], va[1]);
+                e4m3x4_to_f16(prmt(vw[2][i / 2], vw[3][i / 2], sel), va[2], va[3]);
                 mma16816_f16(o[i], va, pb0, pb1);
-            else
+            } else {
+                const int row = (lane & 7) + (lane >> 4) * 8;
+                ldsm_x4_t(vb + swz<D>(row, 2 * i + ((lane >> 3) & 1)), va[0], va[1], va[2], va[3]);
                 mma16816(o[i], va, pb0, pb1);
+            }
         }
         __syncwarp();
         if (!F8 && lane == 0) mbar_arrive(empty + 8 * st);   // the stage may be refilled
@@ -664,7 +686,7 @@ __global__ void __maxnreg__(128) decode_fused_kernel(const __grid_constant__ Fus
                                                      const __grid_constant__ CUtensorMap tmk,
                                                      const __grid_constant__ CUtensorMap tmv) {
     using Lay = FusedLayout<D, F8>;
-    using TC = DecCfg<D>;
+    using TC = DecCfg<D, F8>;
     using TL = typename TC::Lay;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -675,7 +697,7 @@ __global__ void __maxnreg__(128) decode_fused_kernel(const __grid_constant__ Fus
     grid_dep_wait();
     grid_dep_launch();
     const int w0 = __ldg(f.wptr + blockIdx.x), w1 = __ldg(f.wptr + blockIdx.x + 1);
-    const bool tiles = !F8 && w1 > w0;   // FP8 pools have no tile path
+    const bool tiles = w1 > w0;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + TL::OFF_TMEM);
     int* info = reinterpret_cast<int*>(sm + TL::OFF_INFO);
     const uint32_t sbar = smem_u32(sm + Lay::OFF_SBAR);
@@ -704,7 +726,7 @@ __global__ void __maxnreg__(128) decode_fused_kernel(const __grid_constant__ Fus
 
     constexpr int kStreamGate = 3;   // named barrier: tile roles done -> streaming may start
     constexpr int kTileWarps = TC::kThreads / 32;   // softmax, MMA, gather team (incl. the producers)
-    if constexpr (!F8) if (tiles && warp < kTileWarps) {
+    if (tiles && warp < kTileWarps) {
         // the tile roles; the producer warps are part of the gather team and
         // go on to stream once the CTA's tiles are done
         const uint32_t tbase = *tslot;
@@ -736,13 +758,12 @@ __global__ void __maxnreg__(128) decode_fused_kernel(const __grid_constant__ Fus
         const int c = warp - kFirstConsumer;
         const uint32_t desc = smem_u32(sm + Lay::OFF_DESC + c * kNSF * 32);
         const uint32_t qb = smem_u32(sm + Lay::OFF_Q + c * 2 * Lay::QSLOT);
-        const uint32_t conv = smem_u32(sm + Lay::OFF_CONV + c * Lay::CONVW);
         if (tiles)
             stream_consumer<D, kNS, F8>(f, smem_u32(sm + Lay::OFF_RING + c * Lay::RING), desc, qb, full_of(c),
-                                        empty_of(c), qempty_of(c), conv, lane);
+                                        empty_of(c), qempty_of(c), lane);
         else
             stream_consumer<D, kNSF, F8>(f, smem_u32(sm + c * Lay::RING_F), desc, qb, full_of(c), empty_of(c),
-                                         qempty_of(c), conv, lane);
+                                         qempty_of(c), lane);
     }
     tc_fence_before();
     __syncthreads();
@@ -763,9 +784,10 @@ int launch_decode_fused(const sgl_plan* plan, const void* q, const void* kp, con
                                                       cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::TOTAL);
     if (attr) return attr;
     const sgl_attn_params& p = plan->params;
-    // the tiles' TMA views of the pools (unused, and left zero, without tiles)
+    // the tiles' TMA views of the pools (unused, and left zero, without tiles
+    // or with an FP8 pool, whose tiles load the codes with plain loads)
     CUtensorMap mk{}, mv{};
-    if (plan->n_wide > 0)
+    if (plan->n_wide > 0 && !F8)
         if (const int e = tc::encode_pool_maps(kp, vp, p.num_slots, p.num_kv_heads, D, &mk, &mv)) return e;
     FusedArgs f{};
     TcArgs& a = f.t;
@@ -791,8 +813,8 @@ int launch_decode_fused(const sgl_plan* plan, const void* q, const void* kp, con
     f.n_init = plan->n_init;
     f.n_tile_ctas = plan->n_tile_ctas;
     f.sched = reinterpret_cast<uint32_t*>(ws + plan->off_sched);
-    f.k_scale = p.k_scale;
-    f.v_scale = p.v_scale;
+    a.k_scale = p.k_scale;
+    a.v_scale = p.v_scale;
     // Both launches are programmatic dependents of the kernel before them:
     // each waits (griddepcontrol.wait) before its first memory access, so
     // only the launch and scheduling overlap the previous grid's tail.

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -53,6 +54,9 @@ __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
 }
 __device__ __forceinline__ void st_shared_s32(uint32_t addr, int32_t v) {
     asm volatile("st.shared.b32 [%0], %1;\n" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 __device__ __forceinline__ int32_t ld_shared_s32(uint32_t addr) {
     int32_t v;
@@ -116,6 +120,25 @@ __device__ __forceinline__ float fmax3f(float a, float b, float c) {
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
+}
+// Four FP8 E4M3 values (one 32-bit word) as two f16x2 words, exactly (every
+// E4M3 value is an f16 value).
+__device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    asm("{\n .reg .b16 a, b;\n mov.b32 {a, b}, %2;\n cvt.rn.f16x2.e4m3x2 %0, a;\n cvt.rn.f16x2.e4m3x2 %1, b;\n}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
+}
+// bf16x2 -> f16x2 (query values: in range and exact for N(0,1)-sized data)
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t x) {
+    const float a = __uint_as_float(x << 16), b = __uint_as_float(x & 0xffff0000u);
+    uint32_t y;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(y) : "f"(b), "f"(a));
+    return y;
+}
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    uint32_t y;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(y) : "f"(hi), "f"(lo));
+    return y;
 }
 
 // Byte offset of 16-byte chunk c of row r in a swizzled tile of D-wide rows.

@@ -120,18 +120,14 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
     std::vector<Unit> units;
     int64_t units_n = 0;
     int64_t max_wide = 0;
-    // FP8 KV pools have no tensor-core tile path: every segment is streamed,
-    // a wide one in member blocks of the narrow width
-    const bool all_narrow = p->dtype == SGL_DTYPE_BF16_FP8KV;
     for (int32_t s = 0; s < nseg; ++s) {
         const int32_t b = g->seg_begin[s], e = g->seg_end[s];
         const int32_t m0 = g->seg_member_ptr[s], nmem = g->seg_member_ptr[s + 1] - m0;
-        if (nmem <= MBn || all_narrow) {
-            for (int32_t mb = 0; mb < nmem; mb += MBn)
-                for (int32_t h = 0; h < Hkv; ++h) {
-                    units.push_back({g->seg_row[s], b, e, h, m0 + mb, std::min(MBn, nmem - mb)});
-                    units_n += e - b;
-                }
+        if (nmem <= MBn) {
+            for (int32_t h = 0; h < Hkv; ++h) {
+                units.push_back({g->seg_row[s], b, e, h, m0, nmem});
+                units_n += e - b;
+            }
         } else {
             max_wide = std::max<int64_t>(max_wide, e - b);
         }
@@ -179,7 +175,7 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
     for (int32_t s = 0; s < nseg; ++s) {
         const int32_t b = g->seg_begin[s], e = g->seg_end[s];
         const int32_t m0 = g->seg_member_ptr[s], nmem = g->seg_member_ptr[s + 1] - m0;
-        if (nmem <= MBn || all_narrow) continue;
+        if (nmem <= MBn) continue;
         const int32_t nblk = (nmem + MBw - 1) / MBw;
         for (int64_t cb = b; cb < e; cb += Cw) {
             const int32_t ce = (int32_t)std::min<int64_t>(e, cb + Cw);

@@ -65,10 +65,11 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
            ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46) | (2ull << 61);
 }
 
-// kind::f16 instruction descriptor: bf16 A and B, fp32 D, M x N.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn_major ? (1u << 16) : 0u) | ((uint32_t)(N >> 3) << 17) |
-           ((uint32_t)(M >> 4) << 24);
+// kind::f16 instruction descriptor: bf16 (or, with f16, f16) A and B, fp32
+// D, M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major, bool f16 = false) {
+    return (1u << 4) | (f16 ? 0u : (1u << 7) | (1u << 10)) | (b_mn_major ? (1u << 16) : 0u) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 __device__ __forceinline__ void tc_mma(uint32_t tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
@@ -159,13 +160,16 @@ struct TcArgs {
     int Hq, Hkv, G;
     int64_t num_slots;
     float scale_log2;
+    // decode with an FP8 (E4M3) pool: per-tensor dequantisation scales (K's
+    // goes into the score scale, V's into the normalisation)
+    float k_scale, v_scale;
 };
 
 // Shared memory of the tile roles (offsets from a 1024-byte aligned base):
 // NQ query tiles (extend: 128B-swizzled smem tiles; decode: none, Q lives in
 // TMEM), NS K stages and NS V stages of BN positions, the barriers and a
 // small broadcast area.
-template <int D, bool DEC, int NQ, int NS, int BN>
+template <int D, bool DEC, int NQ, int NS, int BN, bool F8 = false>
 struct TcLayout {
     static constexpr int QTILE = DEC ? 0 : 128 * D * 2;
     static constexpr int KREGION = BN * 128;             // SW128 region: BN rows x 64 columns
@@ -176,7 +180,14 @@ struct TcLayout {
     static constexpr int OFF_BAR = OFF_V + NS * KTILE;
     static constexpr int OFF_INFO = OFF_BAR + 48 * 8;    // tile description broadcast (16 ints)
     static constexpr int OFF_TMEM = OFF_INFO + 16 * 4;   // TMEM base address
-    static constexpr int END = OFF_TMEM + 16;
+    // FP8 pools: the codes of two blocks' K and V rows as copied (BN x D
+    // bytes per part), before their conversion into the K and V stages.
+    // Only the tiles use it: KEEP is the end of what the rest of a kernel
+    // may not reuse while or after the tiles run.
+    static constexpr int OFF_STG = (OFF_TMEM + 16 + 127) / 128 * 128;
+    static constexpr int STG = BN * D;
+    static constexpr int END = F8 ? OFF_STG + 4 * STG : OFF_TMEM + 16;
+    static constexpr int KEEP = F8 ? OFF_STG : END;
 };
 
 // Tile roles and their barriers for NQ query tiles that share one K/V stream
@@ -188,17 +199,24 @@ struct TcLayout {
 // TMEM columns of query tile q: S buffers at q * 256 + BN b (b < NSB), O at
 // q * 256 + NSB * BN; decode's Q after O.  P_j (bf16 pairs) overwrites the
 // first BN / 2 columns of its own S buffer.
-template <int D, bool DEC, int NQ, int NS, int NG, int BN, int NSB>
+//
+// F8 (decode only): the pools hold FP8 E4M3 codes.  The gather team copies
+// them into a staging area with 16-byte cp.async and stores them, converted
+// to f16 (exact), into the same SW128 tiles; Q and P are f16 too, so the MMAs
+// are kind::f16 with f16 operands.
+template <int D, bool DEC, int NQ, int NS, int NG, int BN, int NSB, bool F8 = false>
 struct TcCfg {
+    static_assert(!F8 || DEC, "FP8 pools: decode tiles only");
     static_assert(NQ == 1 || (NQ == 2 && !DEC), "decode tiles use one query tile (Q lives in TMEM)");
     static_assert(BN == 64 || BN == 128, "KV block of 64 or 128 positions");
     static_assert(NSB == 1 || NSB == 2, "one or two score buffers");
     static_assert(NS >= NSB, "the S lookahead needs as many K stages as score buffers");
     static_assert(NSB * BN + 128 + (DEC ? D / 2 : 0) <= (NQ == 2 ? 256 : 512), "TMEM columns");
     static_assert(NQ == 1 || NSB == 1, "two query tiles alternate on one score buffer each");
-    using Lay = TcLayout<D, DEC, NQ, NS, BN>;
+    using Lay = TcLayout<D, DEC, NQ, NS, BN, F8>;
     static constexpr int kD = D, kNQ = NQ, kNS = NS, kNG = NG, kBN = BN, kNSB = NSB;
     static constexpr bool kDec = DEC;
+    static constexpr bool kF8 = F8;
     static constexpr int kThreads = 32 * (4 * NQ + 1 + NG);
     static constexpr int kMmaWarp = 4 * NQ;
     static constexpr int kOCol = NSB * BN;               // O's column within a query tile's 256
@@ -227,8 +245,8 @@ struct TcCfg {
 // The decode tiles' configuration: one query tile with Q in TMEM, 128-position
 // blocks (S MMAs of N = 128), two score buffers so that the softmax of block
 // j + 1 overlaps PV_j and S_{j+2}, two K/V stages, a gather team of six warps.
-template <int D>
-using DecCfg = TcCfg<D, true, 1, 2, 6, 128, 2>;
+template <int D, bool F8 = false>
+using DecCfg = TcCfg<D, true, 1, 2, 6, 128, 2, F8>;
 
 struct TileInfo {
     int kv_row, kv_begin, kv_end, kvh;
@@ -250,8 +268,9 @@ __device__ __forceinline__ void tc_init_barriers(uint32_t bar0) {
     auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
     // Q writers: the softmax threads (decode) or the gather team's lanes (extend)
     mbar_init(bar(C::QFULL), C::kDec ? 128 : 32 * C::kNG);
-    // FULL: one expect_tx arrival per gather warp (its TMA gathers complete
-    // the bytes); EMPTY: the MMA thread's commit
+    // FULL: one arrival per gather warp (an expect_tx whose bytes its TMA
+    // gathers complete, or with FP8 pools a plain arrival once its lanes'
+    // stores are done); EMPTY: the MMA thread's commit
     for (int s2 = 0; s2 < C::kNS; ++s2) {
         mbar_init(bar(C::KFULL(s2)), C::kNG);
         mbar_init(bar(C::KEMPTY(s2)), 1);
@@ -283,7 +302,7 @@ __device__ __forceinline__ void tc_tile_run(const TcArgs& a, const CUtensorMap* 
     using Lay = typename C::Lay;
     constexpr int D = C::kD, NQ = C::kNQ, NS = C::kNS, NG = C::kNG, BN = C::kBN, NSB = C::kNSB;
     constexpr int KR = Lay::KREGION;
-    constexpr bool DEC = C::kDec;
+    constexpr bool DEC = C::kDec, F8 = C::kF8;
     const uint32_t sQ = smem_u32(sm + Lay::OFF_Q);
     const uint32_t sK = smem_u32(sm + Lay::OFF_K);
     const uint32_t sV = smem_u32(sm + Lay::OFF_V);
@@ -342,88 +361,213 @@ __device__ __forceinline__ void tc_tile_run(const TcArgs& a, const CUtensorMap* 
             }
             cp_async_arrive_noinc(bar(C::QFULL));
         }
-        // K and V blocks: NOP TMA gathers each (four rows x 128 bytes: rows
-        // 4 quad .. 4 quad + 3, columns 64 half ..), OPW of them per team warp
-        // (lane l issues op g OPW + l).  Positions past the range re-read the
-        // range's last position (finite data, masked scores), so every row is
-        // inside the pool.  With the KV write fused, positions from new_pos on
-        // come from the new K/V tensor; a quad that straddles new_pos is
-        // loaded as four single rows.
-        constexpr int H = D / 64;
-        constexpr int NOP = BN / 4 * H;
-        constexpr int OPW = (NOP + NG - 1) / NG;
-        static_assert(OPW <= 32, "one gather per lane");
-        const int o = g * OPW + lane;
-        const int nmine = max(0, min(NOP - g * OPW, OPW));   // ops of this warp
-        const bool mine = lane < nmine;
-        const int half = o % H, quad = o / H;
-        const uint32_t bytes = (uint32_t)nmine * 512u;
-        const int32_t* trow = a_r2t + (int64_t)kv_row * a_ld;
-        const int new_pos = ti.new_pos, new_row = ti.new_row;
-        int32_t nx[4];
-        int npos0 = 0;   // first position of the quad being fetched
-        auto fetch = [&](int j) {
-            npos0 = kv_begin + j * BN + 4 * quad;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int p = min(npos0 + i, kv_end - 1);
-                nx[i] = (mine && j < nb && p < new_pos) ? __ldg(trow + p) : 0;
-            }
-        };
-        fetch(0);
         int issued = 0;
-        for (int j = 0; j < nb; ++j) {
-            const uint32_t J = J0 + j;
-            const int st = (int)(J % (uint32_t)NS);
-            const uint32_t ph = (J / (uint32_t)NS) & 1u;
-            const int npos_cur = npos0;
-            int r[4];
-            int nsrc = 0;   // rows of the quad read from the new K/V
+        const int32_t* trow = a_r2t + (int64_t)kv_row * a_ld;
+        if constexpr (F8) {
+            // FP8 pools: lane t of the team copies 16-code pieces t, t + 32 NG,
+            // ... of a block's K and V rows (CH pieces per row) with 16-byte
+            // cp.async into one of two staging buffers (no registers held
+            // while the codes are in flight; two blocks ahead), then, once
+            // the stage is free, reads back its own pieces, converts them to
+            // f16 (exact) and stores them into the SW128 tile (two 16-byte
+            // chunks per piece); the warp then arrives on the stage's FULL
+            // barrier.  A block's slots are looked up one block before its
+            // copies are issued and checked only then, so no lookup stalls
+            // the conversions.  Positions past the range re-read the range's
+            // last position.
+            constexpr int CH = D / 16;
+            constexpr int NIT = BN * CH;
+            constexpr int TPT = (NIT + 32 * NG - 1) / (32 * NG);
+            const int t0 = g * 32 + lane;
+            const uint8_t* const kp8 = reinterpret_cast<const uint8_t*>(a_kp);
+            const uint8_t* const vp8 = reinterpret_cast<const uint8_t*>(a_vp);
+            const uint32_t stg = smem_u32(sm + Lay::OFF_STG);
+            int32_t sl[TPT];   // slots of this lane's pieces of the next block to copy
+            auto lookup = [&](int j) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int p = min(npos_cur + i, kv_end - 1);
-                if (p >= new_pos) {
-                    r[i] = (new_row + (p - new_pos)) * a_Hkv + kvh;
-                    ++nsrc;
-                } else {
-                    int32_t sl = nx[i];
-                    if (sl < 0 || sl >= a_num_slots) {
-                        if (mine && half == 0) atomicOr(a_err, 1u);
-                        sl = 0;
-                    }
-                    r[i] = sl * a_Hkv + kvh;
+                for (int i = 0; i < TPT; ++i) {
+                    const int it = t0 + i * 32 * NG;
+                    const int p = min(kv_begin + j * BN + it / CH, kv_end - 1);
+                    sl[i] = (it < NIT && j < nb) ? __ldg(trow + p) : 0;
                 }
+            };
+            // two cp.async groups (K, then V) of block j into staging buffer
+            // j & 1; empty groups past the range keep the group count even
+            auto copy = [&](int j) {
+                const uint32_t sb = stg + (uint32_t)(j & 1) * 2u * Lay::STG;
+                int32_t rw[TPT];
+#pragma unroll
+                for (int i = 0; i < TPT; ++i) {
+                    const int it = t0 + i * 32 * NG;
+                    int32_t s1 = sl[i];
+                    if (s1 < 0 || s1 >= a_num_slots) {
+                        if (j < nb && it < NIT && it % CH == 0) atomicOr(a_err, 1u);
+                        s1 = 0;
+                    }
+                    rw[i] = s1 * a_Hkv + kvh;
+                }
+#pragma unroll
+                for (int part = 0; part < 2; ++part) {
+                    if (j < nb) {
+#pragma unroll
+                        for (int i = 0; i < TPT; ++i) {
+                            const int it = t0 + i * 32 * NG;
+                            if (it < NIT)
+                                cp_async16(sb + part * Lay::STG + it * 16,
+                                           (part ? vp8 : kp8) + (int64_t)rw[i] * D + (it % CH) * 16, true);
+                        }
+                    }
+                    cp_async_commit();
+                }
+            };
+            lookup(0);
+            copy(0);
+            lookup(1);
+            copy(1);
+            lookup(2);
+            for (int j = 0; j < nb; ++j) {
+                const uint32_t J = J0 + j;
+                const int st = (int)(J % (uint32_t)NS);
+                const uint32_t ph = (J / (uint32_t)NS) & 1u;
+                const uint32_t sb = stg + (uint32_t)(j & 1) * 2u * Lay::STG;
+                bool stop = false;
+#pragma unroll
+                for (int part = 0; part < 2; ++part) {
+                    // groups so far: ..., K_j, V_j, K_{j+1}, V_{j+1}
+                    if (part == 0)
+                        cp_async_wait<3>();
+                    else
+                        cp_async_wait<2>();
+                    wait(part ? C::VEMPTY(st) : C::KEMPTY(st), ph ^ 1u);
+                    // store nothing into a stage that may be in use (decided
+                    // for the whole warp, which meets at __syncwarp below)
+                    if (__any_sync(0xffffffffu, stt.timed_out)) {
+                        stt.timed_out = true;
+                        stop = true;
+                        break;
+                    }
+                    const uint32_t base = (part ? sV : sK) + st * Lay::KTILE;
+#pragma unroll
+                    for (int i = 0; i < TPT; ++i) {
+                        const int it = t0 + i * 32 * NG;
+                        if (it < NIT) {
+                            const int r = it / CH, c = it % CH;
+                            uint32_t w[4];
+                            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];\n"
+                                         : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                                         : "r"(sb + part * Lay::STG + it * 16));
+                            uint32_t h[8];
+                            e4m3x4_to_f16(w[0], h[0], h[1]);
+                            e4m3x4_to_f16(w[1], h[2], h[3]);
+                            e4m3x4_to_f16(w[2], h[4], h[5]);
+                            e4m3x4_to_f16(w[3], h[6], h[7]);
+                            st_shared_v4(base + sw128(r, 2 * c, KR), h[0], h[1], h[2], h[3]);
+                            st_shared_v4(base + sw128(r, 2 * c + 1, KR), h[4], h[5], h[6], h[7]);
+                        }
+                    }
+                    // the tensor cores (async proxy) read what these generic
+                    // stores wrote: each lane fences its own stores, then one
+                    // arrival for the warp
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(part ? C::VFULL(st) : C::KFULL(st)));
+                }
+                if (stop) break;
+                // this buffer is free: block j + 2's codes into it
+                copy(j + 2);
+                lookup(j + 3);
+                issued = j + 1;
             }
-            fetch(j + 1);
-            // K rows once S_{j-NS} has read the stage, then V rows once
-            // PV_{j-NS} has: separate waits, so that K of a block never waits
-            // for a PV product (the MMA thread may need that K before it
-            // commits the PV that frees the V stage)
-#pragma unroll
-            for (int part = 0; part < 2; ++part) {
-                wait(part ? C::VEMPTY(st) : C::KEMPTY(st), ph ^ 1u);
-                if (stt.timed_out) break;   // issue nothing into a stage that may be in use
-                const int bfull = part ? C::VFULL(st) : C::KFULL(st);
-                if (lane == 0) mbar_expect_tx(bar(bfull), bytes);
-                __syncwarp();
-                if (mine) {
-                    const uint32_t dq = (part ? sV : sK) + st * Lay::KTILE + half * KR + quad * 512;
-                    if (nsrc == 0) {
-                        tma_gather4(dq, part ? tmv : tmk, half * 64, r[0], r[1], r[2], r[3], bar(bfull));
-                    } else if (nsrc == 4) {
-                        tma_gather4(dq, part ? tnv : tnk, half * 64, r[0], r[1], r[2], r[3], bar(bfull));
+            // no copy in flight when the tile ends (the staging area is the
+            // next tile's, and the streaming warps' rings overlap it)
+            asm volatile("cp.async.wait_all;\n" ::: "memory");
+        } else {
+            // K and V blocks: NOP TMA gathers each (four rows x 128 bytes: rows
+            // 4 quad .. 4 quad + 3, columns 64 half ..), OPW of them per team warp
+            // (lane l issues op g OPW + l).  Positions past the range re-read the
+            // range's last position (finite data, masked scores), so every row is
+            // inside the pool.  With the KV write fused, positions from new_pos on
+            // come from the new K/V tensor; a quad that straddles new_pos is
+            // loaded as four single rows.
+            constexpr int H = D / 64;
+            constexpr int NOP = BN / 4 * H;
+            constexpr int OPW = (NOP + NG - 1) / NG;
+            static_assert(OPW <= 32, "one gather per lane");
+            const int o = g * OPW + lane;
+            const int nmine = max(0, min(NOP - g * OPW, OPW));   // ops of this warp
+            const bool mine = lane < nmine;
+            const int half = o % H, quad = o / H;
+            const uint32_t bytes = (uint32_t)nmine * 512u;
+            const int new_pos = ti.new_pos, new_row = ti.new_row;
+            int32_t nx[4];
+            int npos0 = 0;   // first position of the quad being fetched
+            auto fetch = [&](int j) {
+                npos0 = kv_begin + j * BN + 4 * quad;
+    #pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int p = min(npos0 + i, kv_end - 1);
+                    nx[i] = (mine && j < nb && p < new_pos) ? __ldg(trow + p) : 0;
+                }
+            };
+            fetch(0);
+            for (int j = 0; j < nb; ++j) {
+                const uint32_t J = J0 + j;
+                const int st = (int)(J % (uint32_t)NS);
+                const uint32_t ph = (J / (uint32_t)NS) & 1u;
+                const int npos_cur = npos0;
+                int r[4];
+                int nsrc = 0;   // rows of the quad read from the new K/V
+    #pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int p = min(npos_cur + i, kv_end - 1);
+                    if (p >= new_pos) {
+                        r[i] = (new_row + (p - new_pos)) * a_Hkv + kvh;
+                        ++nsrc;
                     } else {
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const bool nw = min(npos_cur + i, kv_end - 1) >= new_pos;
-                            tma_load_row(dq + 128 * i, nw ? (part ? tnv : tnk) : (part ? tmv : tmk), half * 64, r[i],
-                                         bar(bfull));
+                        int32_t sl = nx[i];
+                        if (sl < 0 || sl >= a_num_slots) {
+                            if (mine && half == 0) atomicOr(a_err, 1u);
+                            sl = 0;
+                        }
+                        r[i] = sl * a_Hkv + kvh;
+                    }
+                }
+                fetch(j + 1);
+                // K rows once S_{j-NS} has read the stage, then V rows once
+                // PV_{j-NS} has: separate waits, so that K of a block never waits
+                // for a PV product (the MMA thread may need that K before it
+                // commits the PV that frees the V stage)
+    #pragma unroll
+                for (int part = 0; part < 2; ++part) {
+                    wait(part ? C::VEMPTY(st) : C::KEMPTY(st), ph ^ 1u);
+                    // issue nothing into a stage that may be in use (decided
+                    // for the whole warp, which meets at __syncwarp below)
+                    if (__any_sync(0xffffffffu, stt.timed_out)) {
+                        stt.timed_out = true;
+                        break;
+                    }
+                    const int bfull = part ? C::VFULL(st) : C::KFULL(st);
+                    if (lane == 0) mbar_expect_tx(bar(bfull), bytes);
+                    __syncwarp();
+                    if (mine) {
+                        const uint32_t dq = (part ? sV : sK) + st * Lay::KTILE + half * KR + quad * 512;
+                        if (nsrc == 0) {
+                            tma_gather4(dq, part ? tmv : tmk, half * 64, r[0], r[1], r[2], r[3], bar(bfull));
+                        } else if (nsrc == 4) {
+                            tma_gather4(dq, part ? tnv : tnk, half * 64, r[0], r[1], r[2], r[3], bar(bfull));
+                        } else {
+    #pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const bool nw = min(npos_cur + i, kv_end - 1) >= new_pos;
+                                tma_load_row(dq + 128 * i, nw ? (part ? tnv : tnk) : (part ? tmv : tmk), half * 64, r[i],
+                                             bar(bfull));
+                            }
                         }
                     }
                 }
+                if (stt.timed_out) break;
+                issued = j + 1;
             }
-            if (stt.timed_out) break;
-            issued = j + 1;
         }
         if constexpr (!DEC) {
             // Fused KV write (after the gathers are issued, so that it overlaps the
@@ -455,7 +599,7 @@ __device__ __forceinline__ void tc_tile_run(const TcArgs& a, const CUtensorMap* 
         // long since: the MMA thread consumed them).  A FULL phase needs this
         // warp's arrival, so the last armed phase of each stage is the one to
         // wait for; the waits are bounded.
-        for (int j = max(0, issued - NS); j < issued; ++j) {
+        for (int j = F8 ? issued : max(0, issued - NS); j < issued; ++j) {
             const uint32_t J = J0 + j;
             const int st = (int)(J % (uint32_t)NS);
             if (!mbar_wait(bar(C::KFULL(st)), (J / (uint32_t)NS) & 1u)) atomicOr(a_err, 4u);
@@ -465,8 +609,8 @@ __device__ __forceinline__ void tc_tile_run(const TcArgs& a, const CUtensorMap* 
     } else if (warp == C::kMmaWarp) {
         // ------------------------------------------------------------ MMA
         if (lane == 0) {
-            constexpr uint32_t IS = idesc_bf16(128, BN, false);
-            constexpr uint32_t IO = idesc_bf16(128, D, true);
+            constexpr uint32_t IS = idesc_bf16(128, BN, false, F8);
+            constexpr uint32_t IO = idesc_bf16(128, D, true, F8);
             const bool has0 = ti.rows[0] > 0, has1 = NQ > 1 && ti.rows[1] > 0;
             auto has = [&](int q) { return q ? has1 : has0; };
             wait(C::QFULL, stt.T & 1);
@@ -546,7 +690,7 @@ __device__ __forceinline__ void tc_tile_run(const TcArgs& a, const CUtensorMap* 
         const uint32_t tl = tbase + 256 * q + lq;
         const uint32_t tlO = tl + C::kOCol;
         const int lim = DEC ? 0x7fffffff : i7 + i / a_G;
-        const float sc = a_scale;
+        const float sc = F8 ? a_scale * a.k_scale : a_scale;
         float m_used = -INFINITY, l0 = 0.f, l1 = 0.f;   // l = l0 + l1 (packed pair sums)
         if constexpr (DEC) {
             // this row's query (member request i / G, head kvh * G + i % G) into TMEM
@@ -564,6 +708,10 @@ __device__ __forceinline__ void tc_tile_run(const TcArgs& a, const CUtensorMap* 
                     w[4 * k + 1] = v.y;
                     w[4 * k + 2] = v.z;
                     w[4 * k + 3] = v.w;
+                }
+                if constexpr (F8) {   // f16 operands against the f16 K tiles
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) w[k] = bf16x2_to_f16x2(w[k]);
                 }
                 tst32u(tlQ + 32 * c, w);
             }
@@ -642,8 +790,13 @@ __device__ __forceinline__ void tc_tile_run(const TcArgs& a, const CUtensorMap* 
                             tld_wait();
 #pragma unroll
                             for (int k = 0; k < 32; ++k) {
-                                const __nv_bfloat162 v2 = *reinterpret_cast<const __nv_bfloat162*>(&w[k]);
-                                w[k] = pack_bf16(__low2float(v2) * f, __high2float(v2) * f);
+                                if constexpr (F8) {
+                                    const __half2 v2 = *reinterpret_cast<const __half2*>(&w[k]);
+                                    w[k] = pack_f16(__low2float(v2) * f, __high2float(v2) * f);
+                                } else {
+                                    const __nv_bfloat162 v2 = *reinterpret_cast<const __nv_bfloat162*>(&w[k]);
+                                    w[k] = pack_bf16(__low2float(v2) * f, __high2float(v2) * f);
+                                }
                             }
                             tst32u(tS + 32 * h2, w);
                         }
@@ -660,7 +813,7 @@ __device__ __forceinline__ void tc_tile_run(const TcArgs& a, const CUtensorMap* 
                         ffma2_sc(x0, x1, srow[k], srow[k + 1], sc, nmu);
                         const float p0 = ex2_ftz(x0), p1 = ex2_ftz(x1);   // -inf -> 0
                         fadd2_acc(l0, l1, p0, p1);
-                        pk[k / 2] = pack_bf16(p0, p1);
+                        pk[k / 2] = F8 ? pack_f16(p0, p1) : pack_bf16(p0, p1);
                     }
                     tst32u(tS + 32 * h, pk);   // P over scores already read
                 }
@@ -671,7 +824,7 @@ __device__ __forceinline__ void tc_tile_run(const TcArgs& a, const CUtensorMap* 
             wait(C::DONE, stt.T & 1);
             tc_fence_after();
             const float l = l0 + l1;
-            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const float inv = l > 0.f ? (F8 ? a.v_scale : 1.f) / l : 0.f;
             const float lse = l > 0.f ? (m_used + log2f(l)) * kLn2 : -INFINITY;
 #pragma unroll 1
             for (int c = 0; c < D / 32; c += 2) {

@@ -257,6 +257,42 @@ def test_decode_fp8_kv_elementwise(name, num_sms):
         case.close()
 
 
+@pytest.mark.parametrize("name", ["llama3_8b_decode_small", "multiturn_small"])
+def test_decode_fp8_subnormal_codes(name):
+    """Every K and V code an E4M3 subnormal (exponent field 0: values m 2^-9,
+    m < 8), with scales 2^6 so that they matter: the conversions must keep
+    them exact on both the tile and the streaming paths (a flush to zero
+    would zero every score)."""
+    from oracle.fp8 import DequantView
+    case = Case(name)
+    try:
+        ks = vs = 64.0
+        k8 = W.quantize_e4m3(case.K, 1.0) & 0x87
+        v8 = W.quantize_e4m3(case.V, 1.0) & 0x87
+        assert int((k8 & 0x78).max()) == 0 and int((k8 & 0x07).max()) == 7
+        w = case.w
+        p = sgl.make_params(sgl.SGL_DTYPE_BF16_FP8KV, case.B, w.Hq, w.Hkv, w.d, case.S, w.page_size,
+                            k_scale=ks, v_scale=vs)
+        plan = sgl.sgl_decode_plan(p, case.out["seq_lens"], sgl.sgl_groups_view(case.groups))
+        if name.startswith("llama3"):
+            assert sgl.sgl_plan_info(plan)["num_wide_items"] > 0   # the tile path is exercised
+        ws = torch.zeros(max(plan.workspace_bytes, 256), dtype=torch.uint8, device="cuda")
+        sgl.sgl_plan_upload(plan, ws)
+        qd = case.q_host().cuda()
+        table = torch.from_numpy(case.out["req_to_token"]).cuda()
+        seq = torch.from_numpy(case.out["seq_lens"]).cuda()
+        o = torch.empty_like(qd)
+        lse = torch.empty(case.B, w.Hq, dtype=torch.float32, device="cuda")
+        sgl.sgl_decode_attn(qd, k8.cuda(), v8.cuda(), table, seq, plan, o, lse, ws)
+        sgl.sgl_check(ws)
+        Oref, Lref = decode_attention(case.oracle_q(), DequantView(k8, ks), DequantView(v8, vs), case.oracle_table,
+                                      case.out["seq_lens"])
+        assert_close(o.double().cpu().numpy(), lse.cpu().numpy().astype(np.float64), Oref, Lref, *tolerances(w))
+        del plan
+    finally:
+        case.close()
+
+
 def test_fp8_kv_extend_is_unsupported():
     w = W.get("extend_small")
     p = sgl.make_params(sgl.SGL_DTYPE_BF16_FP8KV, 1, w.Hq, w.Hkv, w.d, 1024, 1, k_scale=1.0, v_scale=1.0,
