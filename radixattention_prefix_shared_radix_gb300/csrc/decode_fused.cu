@@ -91,12 +91,13 @@ struct FusedLayout {
     static constexpr int RING = kNS * STAGE;             // per consumer, beside the tile roles
     static constexpr int RING_F = kNSF * STAGE;          // per consumer, CTA without tiles (from offset 0)
     static constexpr int SLOTW = kSQ * kSlotEntry;       // slot ring per consumer
-    // Layout from offset 0: the tile roles' K/V stages and barriers (TL, up
-    // to TL::KEEP), then the rings of a CTA with tiles, the slot rings,
+    // Layout from offset 0: the tile roles' TMEM address and broadcast area
+    // (up to TL::KEEP), then the rings of a CTA with tiles, the slot rings,
     // descriptors and Q slots.  These are used only once the CTA's tiles are
-    // done, so they may overlap the tiles' FP8 staging area (TL::KEEP ..
-    // TL::END).  A CTA without tiles puts its deeper rings at offset 0.  The
-    // streaming barriers, initialised at launch, come after everything.
+    // done, so they overlap the rest of the tile roles' area (TL::KEEP ..
+    // TL::END: stages, barriers, staging).  A CTA without tiles puts its
+    // deeper rings at offset 0.  The streaming barriers, initialised at
+    // launch, come after everything.
     static constexpr int OFF_RING = (TL::KEEP + 127) / 128 * 128;
     static constexpr int END_RINGS = (OFF_RING + kConsumers * RING) > kConsumers * RING_F
                                          ? (OFF_RING + kConsumers * RING) : kConsumers * RING_F;
@@ -738,6 +739,8 @@ __global__ void __maxnreg__(128) decode_fused_kernel(const __grid_constant__ Fus
             tc_tile_run<TC>(f.t, &tmk, &tmv, nullptr, nullptr, ti, sm, tbase, st, tid);
             named_bar(kTileBar, TC::kThreads);
         }
+        // the streaming areas overlap the tile roles' barriers
+        if (tid == 0) tc_inval_barriers<TC>(smem_u32(sm + TL::OFF_BAR));
         asm volatile("bar.arrive %0, %1;\n" ::"r"(kStreamGate), "r"(kFusedThreads) : "memory");
     }
     // streaming warps of CTAs with tiles start once the tiles are done

@@ -166,28 +166,28 @@ struct TcArgs {
 };
 
 // Shared memory of the tile roles (offsets from a 1024-byte aligned base):
-// NQ query tiles (extend: 128B-swizzled smem tiles; decode: none, Q lives in
-// TMEM), NS K stages and NS V stages of BN positions, the barriers and a
-// small broadcast area.
+// the TMEM base address and a small broadcast area first; everything from
+// KEEP on is used only while the tiles run, so a kernel may reuse it once
+// its tiles are done: NQ query tiles (extend: 128B-swizzled smem tiles;
+// decode: none, Q lives in TMEM), NS K stages and NS V stages of BN
+// positions, the barriers and, with FP8 pools, the codes of two blocks' K
+// and V rows as copied (BN x D bytes per part) before their conversion into
+// the stages.
 template <int D, bool DEC, int NQ, int NS, int BN, bool F8 = false>
 struct TcLayout {
+    static constexpr int OFF_TMEM = 0;                   // TMEM base address
+    static constexpr int OFF_INFO = 16;                  // tile description broadcast (16 ints)
+    static constexpr int KEEP = 128;
     static constexpr int QTILE = DEC ? 0 : 128 * D * 2;
     static constexpr int KREGION = BN * 128;             // SW128 region: BN rows x 64 columns
     static constexpr int KTILE = BN * D * 2;
-    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_Q = 1024;
     static constexpr int OFF_K = OFF_Q + NQ * QTILE;
     static constexpr int OFF_V = OFF_K + NS * KTILE;
     static constexpr int OFF_BAR = OFF_V + NS * KTILE;
-    static constexpr int OFF_INFO = OFF_BAR + 48 * 8;    // tile description broadcast (16 ints)
-    static constexpr int OFF_TMEM = OFF_INFO + 16 * 4;   // TMEM base address
-    // FP8 pools: the codes of two blocks' K and V rows as copied (BN x D
-    // bytes per part), before their conversion into the K and V stages.
-    // Only the tiles use it: KEEP is the end of what the rest of a kernel
-    // may not reuse while or after the tiles run.
-    static constexpr int OFF_STG = (OFF_TMEM + 16 + 127) / 128 * 128;
+    static constexpr int OFF_STG = (OFF_BAR + 48 * 8 + 127) / 128 * 128;
     static constexpr int STG = BN * D;
-    static constexpr int END = F8 ? OFF_STG + 4 * STG : OFF_TMEM + 16;
-    static constexpr int KEEP = F8 ? OFF_STG : END;
+    static constexpr int END = OFF_STG + (F8 ? 4 * STG : 0);
 };
 
 // Tile roles and their barriers for NQ query tiles that share one K/V stream
@@ -244,9 +244,12 @@ struct TcCfg {
 
 // The decode tiles' configuration: one query tile with Q in TMEM, 128-position
 // blocks (S MMAs of N = 128), two score buffers so that the softmax of block
-// j + 1 overlaps PV_j and S_{j+2}, two K/V stages, a gather team of six warps.
+// j + 1 overlaps PV_j and S_{j+2}, a gather team of six warps, and three K/V
+// stages: with the S lookahead a K stage is free only once S of the block
+// two earlier has run, and the third stage gives the gather of K_{j+2} a
+// whole block more (two with FP8 pools, whose staging area takes the room).
 template <int D, bool F8 = false>
-using DecCfg = TcCfg<D, true, 1, 2, 6, 128, 2, F8>;
+using DecCfg = TcCfg<D, true, 1, F8 ? 2 : 3, 6, 128, 2, F8>;
 
 struct TileInfo {
     int kv_row, kv_begin, kv_end, kvh;
@@ -262,6 +265,14 @@ struct TcState {
     uint32_t T;        // tiles processed by this CTA so far
     bool timed_out;
 };
+
+// Every barrier of the tile roles invalidated (before their memory is
+// reused for something else).
+template <class C>
+__device__ __forceinline__ void tc_inval_barriers(uint32_t bar0) {
+    for (int i = 0; i < C::kNumBars; ++i)
+        asm volatile("mbarrier.inval.shared::cta.b64 [%0];\n" ::"r"(bar0 + 8u * (uint32_t)i) : "memory");
+}
 
 template <class C>
 __device__ __forceinline__ void tc_init_barriers(uint32_t bar0) {
