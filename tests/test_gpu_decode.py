@@ -257,6 +257,40 @@ def test_decode_fp8_kv_elementwise(name, num_sms):
         case.close()
 
 
+@pytest.mark.parametrize("name", ["llama3_8b_decode", "fork_tree"])
+def test_decode_fp8_full_size(name):
+    """FP8 pools at the full workload sizes, in the benchmark's launch
+    configuration (the device's SM count), on every request."""
+    from oracle.fp8 import DequantView
+    case = Case(name)
+    try:
+        ks, vs = 1.0 / 64, 1.0 / 64
+        k8d = W.quantize_e4m3(case.K.cuda(), ks)
+        v8d = W.quantize_e4m3(case.V.cuda(), vs)
+        w = case.w
+        p = sgl.make_params(sgl.SGL_DTYPE_BF16_FP8KV, case.B, w.Hq, w.Hkv, w.d, case.S, w.page_size,
+                            k_scale=ks, v_scale=vs)
+        plan = sgl.sgl_decode_plan(p, case.out["seq_lens"], sgl.sgl_groups_view(case.groups))
+        assert sgl.sgl_plan_info(plan)["num_wide_items"] > 0
+        ws = torch.zeros(max(plan.workspace_bytes, 256), dtype=torch.uint8, device="cuda")
+        sgl.sgl_plan_upload(plan, ws)
+        qd = case.q_host().cuda()
+        table = torch.from_numpy(case.out["req_to_token"]).cuda()
+        seq = torch.from_numpy(case.out["seq_lens"]).cuda()
+        o = torch.empty_like(qd)
+        lse = torch.empty(case.B, w.Hq, dtype=torch.float32, device="cuda")
+        sgl.sgl_decode_attn(qd, k8d, v8d, table, seq, plan, o, lse, ws)
+        sgl.sgl_check(ws)
+        Oref, Lref = decode_attention(case.oracle_q(), DequantView(k8d.cpu(), ks), DequantView(v8d.cpu(), vs),
+                                      case.oracle_table, case.out["seq_lens"])
+        do, dl = assert_close(o.double().cpu().numpy(), lse.cpu().numpy().astype(np.float64), Oref, Lref,
+                              *tolerances(w))
+        print("%s fp8: O max-abs %.3g, LSE max-abs %.3g" % (name, do, dl))
+        del plan
+    finally:
+        case.close()
+
+
 @pytest.mark.parametrize("name", ["llama3_8b_decode_small", "multiturn_small"])
 def test_decode_fp8_subnormal_codes(name):
     """Every K and V code an E4M3 subnormal (exponent field 0: values m 2^-9,

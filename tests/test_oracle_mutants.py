@@ -164,3 +164,22 @@ def test_scheduler_without_deferral_or_with_late_insertion_is_caught(monkeypatch
     for bad in (no_defer, late_insert):
         monkeypatch.setattr(TS, "simulate", bad)
         assert _fails(TS.test_few_shot_sharing_needs_insertion_at_prefill)
+
+
+@pytest.mark.parametrize("mistake", ["bias8", "subnormal_as_normal", "no_sign"])
+def test_e4m3_decoding_mistakes_are_caught(monkeypatch, mistake):
+    import oracle.fp8 as OF
+
+    def bad(codes):
+        b = np.asarray(codes, dtype=np.int64) & 0xFF
+        sign = 1.0 if mistake == "no_sign" else np.where(b >> 7, -1.0, 1.0)
+        e = (b >> 3) & 0xF
+        m = (b & 0x7).astype(np.float64)
+        normal = (1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - (8.0 if mistake == "bias8" else 7.0))
+        sub = normal if mistake == "subnormal_as_normal" else (m / 8.0) * 2.0 ** -6
+        val = np.where(e == 0, sub, normal)
+        val = np.where((e == 15) & ((b & 7) == 7), np.nan, val)
+        return sign * val
+
+    monkeypatch.setattr(OF, "e4m3_to_float", bad)
+    assert _fails(TA.test_e4m3_decoding_equals_torch_for_all_codes)
