@@ -19,11 +19,15 @@ groups     prefix groups (segments of positions shared by a set of requests)
 attention  decode / extend attention as naive softmax over gathered slots,
            the log-sum-exp merge, and the shared-aware decode that computes
            each shared segment once.
-kvbytes    the KV-bytes-per-token formula used for the roofline.
+kvbytes    the KV-bytes-per-token formulas (GQA and MLA) used for the roofline.
+fp8        E4M3 decoding and dequantised views of FP8 pools.
+sched      the round-based cache-aware scheduling simulation.
+mla        MLA decode attention in the latent space (one stored row per
+           token, read as key and, its latent prefix, as value).
 
 Every function is pinned by ``tests/test_oracle_*.py`` against facts the
 pages or the mathematics fix (brute force, closed forms, worked examples,
 library special cases).
 """
 
-from . import tree, groups, attention, kvbytes  # noqa: F401
+from . import tree, groups, attention, kvbytes, fp8, sched, mla  # noqa: F401

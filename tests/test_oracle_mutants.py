@@ -183,3 +183,36 @@ def test_e4m3_decoding_mistakes_are_caught(monkeypatch, mistake):
 
     monkeypatch.setattr(OF, "e4m3_to_float", bad)
     assert _fails(TA.test_e4m3_decoding_equals_torch_for_all_codes)
+
+
+def _mla_mutant(mistake):
+    def bad(q, kv_pool, req_to_token, seq_lens, dv, sm_scale=None, requests=None):
+        q = np.asarray(q, dtype=np.float64)
+        B, Hq, d = q.shape
+        if sm_scale is None:
+            sm_scale = 1.0 / math.sqrt(dv if mistake == "scale_by_dv" else d)
+        O = np.zeros((B, Hq, dv))
+        LSE = np.full((B, Hq), -math.inf)
+        for r in range(B):
+            L = int(seq_lens[r])
+            if L == 0:
+                continue
+            C = np.asarray(kv_pool[np.asarray(req_to_token[r, :L], dtype=np.int64)], dtype=np.float64).reshape(L, d)
+            for h in range(Hq):
+                s = sm_scale * (C[:, :dv] @ q[r, h, :dv] if mistake == "latent_only_scores" else C @ q[r, h])
+                m = s.max()
+                w = np.exp(s - m)
+                LSE[r, h] = m + math.log(w.sum())
+                V = C[:, d - dv:] if mistake == "value_suffix" else C[:, :dv]
+                O[r, h] = (w / w.sum()) @ V
+        return O, LSE
+    return bad
+
+
+@pytest.mark.parametrize("mistake", ["scale_by_dv", "latent_only_scores", "value_suffix"])
+def test_mla_mistakes_are_caught(monkeypatch, mistake):
+    from tests import test_oracle_mla as TM
+    monkeypatch.setattr(TM, "mla_decode_attention", _mla_mutant(mistake))
+    caught = (_fails(TM.test_mla_equals_sdpa_float64, 16, 576, 512) or _fails(TM.test_mla_identical_rows_closed_form)
+              or _fails(TM.test_mla_value_is_the_latent_prefix))
+    assert caught

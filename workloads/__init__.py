@@ -22,6 +22,14 @@ Workloads (shapes of the five configurations the hot path is measured on):
                       [1, 32768]; the members share the first
                       16*floor(0.8*L/16) tokens; page size 16.
   5 multiturn_noshare the same lengths with no sharing.
+  6 mla_decode        MLA (DeepSeek-Coder-V2-Lite attention shape after
+                      weight absorption): 16 query heads over ONE stored
+                      row per token of 576 elements (512-dim latent + 64-dim
+                      position part), the output the first 512; the batch
+                      of workload 2 (64 requests, 2048-token shared prefix,
+                      64..512-token suffixes); bf16, 2^20-slot pool.
+                      mla_decode_h128_small: 128 query heads (the
+                      DeepSeek-V3 shape) at test size.
 Scaled-down shapes of 2-5 (``*_small``) serve the element-by-element parity
 tests; they keep every structural feature (sharing, forks, raggedness,
 pages) at sizes the oracle finishes in seconds.
@@ -63,6 +71,7 @@ class Workload:
     structure: tuple          # (builder name, parameters)
     num_slots: int = 0        # 0: sized from the structure (pool_factor x need)
     pool_factor: float = 1.25
+    dv: int = 0               # MLA: output width (a prefix of the stored row); 0: not MLA
 
     @property
     def seed(self):
@@ -87,6 +96,8 @@ WORKLOADS = {
                           ("groups", dict(groups=64, size=4, median=3000, sigma=1.0, cap=32768, share=0.8))),
     "multiturn_noshare": Workload("multiturn_noshare", 5, "decode", "bf16", 32, 8, 128, 16,
                                   ("groups", dict(groups=64, size=4, median=3000, sigma=1.0, cap=32768, share=0.0))),
+    "mla_decode": Workload("mla_decode", 6, "decode", "bf16", 16, 1, 576, 1,
+                           ("star", dict(n=64, prefix=2048, suffix=(64, 512))), num_slots=1 << 20, dv=512),
     # scaled-down shapes for element-by-element parity
     "llama3_8b_decode_small": Workload("llama3_8b_decode_small", 2, "decode", "bf16", 32, 8, 128, 1,
                                        ("star", dict(n=8, prefix=300, suffix=(5, 130))), num_slots=8192),
@@ -97,6 +108,10 @@ WORKLOADS = {
                              ("extend", dict(n=3, prefix=(0, 300), new=(1, 200))), num_slots=4096),
     "multiturn_small": Workload("multiturn_small", 5, "decode", "bf16", 32, 8, 128, 16,
                                 ("groups", dict(groups=4, size=4, median=120, sigma=1.0, cap=700, share=0.8))),
+    "mla_decode_small": Workload("mla_decode_small", 6, "decode", "bf16", 16, 1, 576, 1,
+                                 ("star", dict(n=9, prefix=300, suffix=(5, 130))), num_slots=8192, dv=512),
+    "mla_decode_h128_small": Workload("mla_decode_h128_small", 6, "decode", "bf16", 128, 1, 576, 1,
+                                      ("star", dict(n=3, prefix=200, suffix=(1, 90))), num_slots=4096, dv=512),
 }
 
 
@@ -272,7 +287,7 @@ class RowView:
         return self.t.index_select(0, idx).double().numpy()
 
 
-def make_pool(name_or_workload, num_slots=None, threads=None):
+def make_pool(name_or_workload, num_slots=None, threads=None, only_k=False):
     """(free_order, K, V): the free-list permutation and the K/V pools.
 
     K and V are torch CPU tensors [S, Hkv, d] of the workload's dtype.  Each
@@ -289,7 +304,7 @@ def make_pool(name_or_workload, num_slots=None, threads=None):
     tdt = torch.float32 if w.dtype == "f32" else torch.bfloat16
     pools = []
     threads = threads or max(1, min(32, len(os.sched_getaffinity(0))))
-    for which in range(2):
+    for which in range(1 if only_k else 2):
         t = torch.empty((S, w.Hkv, w.d), dtype=tdt)
         flat = t.view(-1)
         n = flat.numel()
@@ -303,7 +318,17 @@ def make_pool(name_or_workload, num_slots=None, threads=None):
         with ThreadPoolExecutor(threads) as ex:
             list(ex.map(fill, range(-(-n // _POOL_BLOCK))))
         pools.append(t)
-    return order, pools[0], pools[1]
+    return order, pools[0], (pools[1] if len(pools) > 1 else None)
+
+
+def make_mla_pool(name_or_workload, num_slots=None):
+    """(free_order, KV): the free-list permutation and the MLA pool, a torch
+    CPU bf16 tensor [S, d] (one stored row per slot: latent then position
+    part), drawn like make_pool's K pool."""
+    w = get(name_or_workload) if isinstance(name_or_workload, str) else name_or_workload
+    assert w.dv, "not an MLA workload"
+    order, K, _ = make_pool(w, num_slots=num_slots, only_k=True)
+    return order, K.view(K.shape[0], w.d)
 
 
 def to_dtype(w, x):
