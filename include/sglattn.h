@@ -269,6 +269,7 @@ int sgl_plan_upload(const sgl_plan* plan, void* workspace, size_t ws_bytes, sgl_
  *   req_to_token device int32 [B, ld]
  *   seq_lens     device int32 [B]
  *   plan         from sgl_decode_plan on the same batch, uploaded into workspace
+ *                (an MLA plan: SGL_ERR_INVALID_ARG)
  *   o            device [B, Hq, d] (dtype);  lse  device fp32 [B, Hq]
  * Each (segment, KV head) chunk is read from HBM once for all member
  * requests and all query heads of that KV head (GQA packing); the partial
@@ -277,6 +278,55 @@ int sgl_plan_upload(const sgl_plan* plan, void* workspace, size_t ws_bytes, sgl_
 int sgl_decode_attn(const void* q, const void* k_pool, const void* v_pool, const int32_t* req_to_token,
                     int64_t ld, const int32_t* seq_lens, const sgl_plan* plan, void* o, float* lse,
                     void* workspace, size_t ws_bytes, sgl_stream_t stream);
+
+/* ---------------------------------------------------------------------
+ * MLA grouped decode (CS349D lecture-16 notes, SGLang case study: §4 "More
+ * engineering", DeepSeek's MLA with the decompression matrices absorbed
+ * into the query and output projections, attention run in the 576-dim
+ * latent space by a grouped decode kernel; §5.1: per token ONE stored row
+ * of a 512-dim latent plus a 64-dim position part, a single KV "head" read
+ * by every query head).
+ *
+ * For request r and query head h, with c_j the pool row of position j:
+ *   s_j = sm_scale * <q[r,h], c_j>  (all latent_dim + rope_dim elements),
+ *   O[r,h] = sum_j softmax(s)_j * c_j[0 : latent_dim],  LSE natural log.
+ * Shared prefix segments are read once for all member requests and all
+ * query heads (64 query rows per work item: members x heads).
+ * --------------------------------------------------------------------- */
+typedef struct {
+    int32_t batch;              /* B requests */
+    int32_t num_qo_heads;       /* Hq: 16, 32, 64 or 128 */
+    int32_t latent_dim;         /* 512 (the output width) */
+    int32_t rope_dim;           /* 64; a pool row holds latent_dim + rope_dim elements */
+    int64_t num_slots;          /* pool rows; num_slots <= INT32_MAX */
+    int32_t page_size;          /* >= 1 (slots of a page are consecutive) */
+    float sm_scale;             /* 0: 1/sqrt(latent_dim + rope_dim) */
+    int32_t num_sms;            /* planning target; 0: the current device's SM count */
+} sgl_mla_params;
+
+/* MLA decode planning (host).  Splits every prefix-group segment into
+ * member blocks of 64 / min(Hq, 64) requests (min(Hq, 64) query heads each)
+ * and KV chunks so that the work items fill the GPU, and lays out the fp32
+ * partial (O, LSE) rows and the per-(request, head group) merge lists.
+ * seq_lens: host [B].  *workspace_bytes as for sgl_decode_plan.  The plan
+ * works only with sgl_mla_decode_attn (and sgl_plan_upload / _info /
+ * _destroy).  Shapes other than the ones listed: SGL_ERR_UNSUPPORTED;
+ * malformed groups: SGL_ERR_INVALID_ARG. */
+int sgl_mla_decode_plan(const sgl_mla_params* params, const int32_t* seq_lens, const sgl_prefix_groups* groups,
+                        sgl_plan** plan_out, size_t* workspace_bytes);
+
+/* MLA decode attention, one query token per request.
+ *   q            device bf16 [B, Hq, latent_dim + rope_dim] (absorbed queries)
+ *   kv_pool      device bf16 [num_slots, latent_dim + rope_dim]
+ *   req_to_token device int32 [B, ld];  seq_lens device int32 [B]
+ *   plan         from sgl_mla_decode_plan on the same batch, uploaded into workspace
+ *   o            device bf16 [B, Hq, latent_dim];  lse device fp32 [B, Hq]
+ * Slots outside the pool are skipped and flagged in the workspace error
+ * word (sgl_check).  A request with seq_len 0 gets O = 0, LSE = -inf.
+ * A plan from sgl_decode_plan: SGL_ERR_INVALID_ARG. */
+int sgl_mla_decode_attn(const void* q, const void* kv_pool, const int32_t* req_to_token, int64_t ld,
+                        const int32_t* seq_lens, const sgl_plan* plan, void* o, float* lse, void* workspace,
+                        size_t ws_bytes, sgl_stream_t stream);
 
 /* Device workspace needed by sgl_extend_attn for these params (bytes). */
 int sgl_extend_workspace_bytes(const sgl_attn_params* params, size_t* bytes);

@@ -49,6 +49,12 @@ class SglPlanInfo(ctypes.Structure):
                 ("upload_bytes", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64)]
 
 
+class SglMlaParams(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("num_qo_heads", ctypes.c_int32), ("latent_dim", ctypes.c_int32),
+                ("rope_dim", ctypes.c_int32), ("num_slots", ctypes.c_int64), ("page_size", ctypes.c_int32),
+                ("sm_scale", ctypes.c_float), ("num_sms", ctypes.c_int32)]
+
+
 class SglAttnParams(ctypes.Structure):
     _fields_ = [("dtype", ctypes.c_int32), ("batch", ctypes.c_int32), ("num_qo_heads", ctypes.c_int32),
                 ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32),
@@ -123,6 +129,9 @@ _SIGS = {
     "sgl_sim_run": (ctypes.c_int, [_P, ctypes.POINTER(SglSimConfig), ctypes.c_int32, ctypes.POINTER(SglSimRequest),
                                    ctypes.POINTER(SglSimResult), ctypes.POINTER(SglSimStats)]),
     "sgl_decode_attn_noalloc": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_int64, _P, _P, _P, _P, _P]),
+    "sgl_mla_decode_plan": (ctypes.c_int, [ctypes.POINTER(SglMlaParams), _I32P, ctypes.POINTER(SglPrefixGroups),
+                                           ctypes.POINTER(_P), ctypes.POINTER(ctypes.c_size_t)]),
+    "sgl_mla_decode_attn": (ctypes.c_int, [_P, _P, _P, ctypes.c_int64, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
 }
 
 _LIB = None
@@ -389,6 +398,37 @@ def sgl_decode_attn(q, k_pool, v_pool, req_to_token, seq_lens, plan, o, lse, wor
                                _dev(req_to_token, "req_to_token"), req_to_token.shape[1], _dev(seq_lens, "seq_lens"),
                                plan.handle, _dev(o, "o"), _dev(lse, "lse"), _dev(workspace, "workspace"),
                                workspace.numel() * workspace.element_size(), _stream(stream)), "sgl_decode_attn")
+
+
+def make_mla_params(batch, num_qo_heads, num_slots, latent_dim=512, rope_dim=64, page_size=1, sm_scale=0.0,
+                    num_sms=0):
+    p = SglMlaParams()
+    p.batch = batch
+    p.num_qo_heads = num_qo_heads
+    p.latent_dim = latent_dim
+    p.rope_dim = rope_dim
+    p.num_slots = num_slots
+    p.page_size = page_size
+    p.sm_scale = sm_scale
+    p.num_sms = num_sms
+    return p
+
+
+def sgl_mla_decode_plan(params, seq_lens, groups_view):
+    s = _i32(seq_lens)
+    h = _P()
+    ws = ctypes.c_size_t()
+    _ok(_lib().sgl_mla_decode_plan(ctypes.byref(params), _ptr32(s), ctypes.byref(groups_view), ctypes.byref(h),
+                                   ctypes.byref(ws)), "sgl_mla_decode_plan")
+    return Plan(h, ws.value)
+
+
+def sgl_mla_decode_attn(q, kv_pool, req_to_token, seq_lens, plan, o, lse, workspace, stream=None):
+    _ok(_lib().sgl_mla_decode_attn(_dev(q, "q"), _dev(kv_pool, "kv_pool"), _dev(req_to_token, "req_to_token"),
+                                   req_to_token.shape[1], _dev(seq_lens, "seq_lens"), plan.handle, _dev(o, "o"),
+                                   _dev(lse, "lse"), _dev(workspace, "workspace"),
+                                   workspace.numel() * workspace.element_size(), _stream(stream)),
+        "sgl_mla_decode_attn")
 
 
 def sgl_extend_workspace_bytes(params):

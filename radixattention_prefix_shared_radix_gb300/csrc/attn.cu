@@ -312,7 +312,7 @@ int sgl_plan_upload(const sgl_plan* plan, void* workspace, size_t ws_bytes, sgl_
 int sgl_decode_attn(const void* q, const void* k_pool, const void* v_pool, const int32_t* req_to_token, int64_t ld,
                     const int32_t* seq_lens, const sgl_plan* plan, void* o, float* lse, void* workspace,
                     size_t ws_bytes, sgl_stream_t stream) {
-    if (!plan) return SGL_ERR_INVALID_ARG;
+    if (!plan || plan->kind != 0) return SGL_ERR_INVALID_ARG;
     const int32_t B = plan->params.batch;
     if (B > 0 && (!q || !o || !lse || !seq_lens)) return SGL_ERR_INVALID_ARG;
     if (plan->n_items > 0 && (!k_pool || !v_pool || !req_to_token || ld < plan->max_pos)) return SGL_ERR_INVALID_ARG;

@@ -11,6 +11,16 @@ namespace sgl {
 // Record the cudaError_t behind an SGL_ERR_CUDA (thread-local).
 void set_cuda_error(int err);
 
+// SM count to plan for: `requested` if positive, else the current device's
+// (152 when no device can be queried).
+int query_num_sms(int32_t requested);
+
+// Prefix groups of a batch of B requests checked against seq_lens (host):
+// every request's segments tile [0, seq_len) exactly, members are sorted,
+// every member holds the segment's positions, representatives are members.
+// SGL_OK or SGL_ERR_INVALID_ARG.
+int validate_groups(int32_t B, const int32_t* seq_lens, const sgl_prefix_groups* g);
+
 // Decode work item: one KV chunk of one prefix-group segment for one KV head
 // and one block of the segment's members.  Laid out in the workspace.
 struct DecItem {
@@ -48,6 +58,7 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Plan object (host); its tables are copied into the workspace head.
 struct sgl_plan {
+    int32_t kind;                // 0: GQA decode (sgl_decode_plan), 1: MLA decode (sgl_mla_decode_plan)
     sgl_attn_params params;      // host pointers cleared
     int32_t G;
     int32_t n_items;             // all work items: wide ones first, then narrow ones

@@ -39,7 +39,8 @@ struct MergeArgs {
 template <typename OutT, int D>
 __device__ __noinline__ void merge_head(const MergeArgs& m, int idx, int j, int e0, int E, int lane) {
     constexpr int VPL = D / 32;             // columns per lane
-    constexpr int U = 16;                   // entries whose rows are in flight together
+    constexpr int U = VPL > 4 ? 4 : 16;     // entries whose rows are in flight together
+    static_assert(VPL == 2 || VPL % 4 == 0, "columns per lane");
     const int r = idx / m.Hkv, h = idx - r * m.Hkv;
     float M = -INFINITY, L = 0.f, acc[VPL];
 #pragma unroll
@@ -57,12 +58,16 @@ __device__ __noinline__ void merge_head(const MergeArgs& m, int idx, int j, int 
                 lu[u] = __shfl_sync(0xffffffffu, ls, ok ? k + u : 0);
                 if (!ok) lu[u] = -INFINITY;
                 const float* src = m.po + (int64_t)pk * D + lane * VPL;
-                if constexpr (VPL == 4) {
-                    const float4 t4 = ok ? __ldcg(reinterpret_cast<const float4*>(src)) : make_float4(0.f, 0.f, 0.f, 0.f);
-                    x[u][0] = t4.x;
-                    x[u][1] = t4.y;
-                    x[u][2] = t4.z;
-                    x[u][3] = t4.w;
+                if constexpr (VPL % 4 == 0) {
+#pragma unroll
+                    for (int c = 0; c < VPL / 4; ++c) {
+                        const float4 t4 =
+                            ok ? __ldcg(reinterpret_cast<const float4*>(src) + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+                        x[u][4 * c] = t4.x;
+                        x[u][4 * c + 1] = t4.y;
+                        x[u][4 * c + 2] = t4.z;
+                        x[u][4 * c + 3] = t4.w;
+                    }
                 } else {
                     const float2 t2 = ok ? __ldcg(reinterpret_cast<const float2*>(src)) : make_float2(0.f, 0.f);
                     x[u][0] = t2.x;
@@ -92,7 +97,13 @@ __device__ __noinline__ void merge_head(const MergeArgs& m, int idx, int j, int 
     const int64_t orow = (int64_t)r * m.Hq + h * m.G + j;
     OutT* dst = static_cast<OutT*>(m.o) + orow * D + lane * VPL;
     if constexpr (sizeof(OutT) == 2) {
-        if constexpr (VPL == 4) {
+        if constexpr (VPL % 8 == 0) {
+#pragma unroll
+            for (int c = 0; c < VPL / 8; ++c)
+                reinterpret_cast<uint4*>(dst)[c] = make_uint4(
+                    pack_bf16(acc[8 * c] * inv, acc[8 * c + 1] * inv), pack_bf16(acc[8 * c + 2] * inv, acc[8 * c + 3] * inv),
+                    pack_bf16(acc[8 * c + 4] * inv, acc[8 * c + 5] * inv), pack_bf16(acc[8 * c + 6] * inv, acc[8 * c + 7] * inv));
+        } else if constexpr (VPL == 4) {
             uint2 pk;
             pk.x = pack_bf16(acc[0] * inv, acc[1] * inv);
             pk.y = pack_bf16(acc[2] * inv, acc[3] * inv);

@@ -1,0 +1,152 @@
+// Work items of the MLA grouped decode.
+//
+// MLA keeps ONE stored row per token (a 512-dim latent plus a 64-dim
+// position part) that every query head reads (CS349D lecture-16 notes,
+// SGLang case study, §4 "More engineering" and §5.1 "DP attention").  A
+// prefix-group segment is therefore read once for all its member requests
+// and all their query heads: the work unit is 64 query rows (member x head)
+// of one segment chunk.  With Hq query heads a unit holds 64 / min(Hq, 64)
+// members and min(Hq, 64) heads ("head group"; Hq = 128 has two groups of 64
+// heads that read the same rows).  Chunks are cut so that about four units
+// per SM exist (one CTA each, longest first); each writes normalised partial
+// rows that the log-sum-exp merge combines per (request, head group).
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "common.h"
+
+namespace {
+
+constexpr int32_t kMlaRows = 64;    // query rows of one work item
+constexpr int32_t kMlaBlock = 32;   // positions per block of the kernel
+
+}  // namespace
+
+extern "C" int sgl_mla_decode_plan(const sgl_mla_params* p, const int32_t* seq_lens, const sgl_prefix_groups* g,
+                                   sgl_plan** plan_out, size_t* workspace_bytes) {
+    if (!p || !g || !plan_out || !workspace_bytes) return SGL_ERR_INVALID_ARG;
+    if (p->batch < 0 || p->num_slots < 0 || p->page_size < 1 || !(p->sm_scale >= 0.f) || std::isinf(p->sm_scale))
+        return SGL_ERR_INVALID_ARG;
+    if (p->latent_dim != 512 || p->rope_dim != 64) return SGL_ERR_UNSUPPORTED;
+    const int32_t Hq = p->num_qo_heads;
+    if (Hq != 16 && Hq != 32 && Hq != 64 && Hq != 128) return SGL_ERR_UNSUPPORTED;
+    if (p->num_slots > INT32_MAX) return SGL_ERR_UNSUPPORTED;
+    const int32_t B = p->batch;
+    if (B > 0 && !seq_lens) return SGL_ERR_INVALID_ARG;
+    int st = sgl::validate_groups(B, seq_lens, g);
+    if (st) return st;
+
+    const int32_t Gp = std::min<int32_t>(Hq, kMlaRows);   // heads per group
+    const int32_t Hg = Hq / Gp;                           // head groups
+    const int32_t MB = kMlaRows / Gp;                     // members per item
+    const int32_t nseg = g->num_segments;
+    const int sms = sgl::query_num_sms(p->num_sms);
+
+    // chunk length: about four items per SM, whole 32-position blocks
+    int64_t work = 0;
+    for (int32_t s = 0; s < nseg; ++s) {
+        const int32_t nmem = g->seg_member_ptr[s + 1] - g->seg_member_ptr[s];
+        work += (int64_t)(g->seg_end[s] - g->seg_begin[s]) * ((nmem + MB - 1) / MB) * Hg;
+    }
+    int64_t C = (work + 4 * (int64_t)sms - 1) / std::max<int64_t>(1, 4 * (int64_t)sms);
+    C = std::min<int64_t>(2048, std::max<int64_t>(64, (C + kMlaBlock - 1) / kMlaBlock * kMlaBlock));
+
+    std::vector<sgl::DecItem> items;
+    for (int32_t s = 0; s < nseg; ++s) {
+        const int32_t b = g->seg_begin[s], e = g->seg_end[s];
+        const int32_t m0 = g->seg_member_ptr[s], nmem = g->seg_member_ptr[s + 1] - m0;
+        for (int32_t mb = 0; mb < nmem; mb += MB)
+            for (int32_t hg = 0; hg < Hg; ++hg)
+                for (int64_t cb = b; cb < e; cb += C) {
+                    const int32_t ce = (int32_t)std::min<int64_t>(e, cb + C);
+                    items.push_back({g->seg_row[s], (int32_t)cb, ce, hg, m0 + mb, std::min(MB, nmem - mb), 0, 0});
+                }
+    }
+    std::stable_sort(items.begin(), items.end(), [](const sgl::DecItem& x, const sgl::DecItem& y) {
+        return (x.kv_end - x.kv_begin) > (y.kv_end - y.kv_begin);
+    });
+    // partial rows in item order: member i of the item, head j of its group
+    // at partial_base + i * Gp + j; merge lists per (request, head group)
+    std::vector<std::vector<int32_t>> ents((size_t)B * Hg);
+    int64_t prow = 0;
+    for (auto& it : items) {
+        it.partial_base = (int32_t)prow;
+        for (int32_t i = 0; i < it.n_mem; ++i) {
+            const int32_t r = g->seg_members[it.mem_begin + i];
+            ents[(size_t)r * Hg + it.kvh].push_back((int32_t)(prow + (int64_t)i * Gp));
+        }
+        prow += (int64_t)it.n_mem * Gp;
+        if (prow > INT32_MAX / 1024) return SGL_ERR_UNSUPPORTED;
+    }
+    if (items.size() > (size_t)INT32_MAX) return SGL_ERR_UNSUPPORTED;
+
+    sgl_plan* plan = new (std::nothrow) sgl_plan();
+    if (!plan) return SGL_ERR_INVALID_ARG;
+    plan->kind = 1;
+    sgl_attn_params& ap = plan->params;
+    ap.dtype = SGL_DTYPE_BF16;
+    ap.batch = B;
+    ap.num_qo_heads = Hq;
+    ap.num_kv_heads = Hg;
+    ap.head_dim = p->latent_dim;
+    ap.page_size = p->page_size;
+    ap.num_slots = p->num_slots;
+    ap.sm_scale = p->sm_scale > 0.f ? p->sm_scale : (float)(1.0 / std::sqrt((double)(p->latent_dim + p->rope_dim)));
+    ap.num_sms = p->num_sms;
+    plan->G = Gp;
+    plan->n_items = (int32_t)items.size();
+    plan->n_wide = 0;
+    plan->n_partial_rows = (int32_t)prow;
+    plan->n_ctas = plan->n_items;
+    plan->n_members = g->num_members;
+    int64_t n_ent = 0;
+    int32_t max_ent = 0;
+    for (auto& v : ents) {
+        n_ent += (int64_t)v.size();
+        max_ent = std::max<int32_t>(max_ent, (int32_t)v.size());
+    }
+    plan->n_merge_entries = (int32_t)n_ent;
+    plan->max_entries_per_request = max_ent;
+    plan->chunk_tokens = (int32_t)C;
+    plan->max_pos = 0;
+    for (int32_t s = 0; s < nseg; ++s) plan->max_pos = std::max(plan->max_pos, g->seg_end[s]);
+
+    using sgl::align_up;
+    const size_t A = sgl::kWsAlign;
+    plan->off_items = A;
+    plan->off_members = align_up(plan->off_items + items.size() * sizeof(sgl::DecItem), A);
+    plan->off_wptr = align_up(plan->off_members + (size_t)g->num_members * 4, A);
+    plan->off_sched = plan->off_wptr;
+    plan->off_mptr = align_up(plan->off_sched + 2 * 4, A);
+    plan->off_ment = align_up(plan->off_mptr + ((size_t)B * Hg + 1) * 4, A);
+    plan->tables_bytes = align_up(plan->off_ment + (size_t)n_ent * 4, A);
+    plan->off_plse = plan->tables_bytes;
+    plan->off_po = align_up(plan->off_plse + (size_t)prow * 4, A);
+    plan->off_cnt = align_up(plan->off_po + (size_t)prow * p->latent_dim * 4, A);
+    plan->workspace_bytes = align_up(plan->off_cnt + (size_t)B * Hg * 4, A);
+
+    plan->blob = new (std::nothrow) unsigned char[plan->tables_bytes];
+    if (!plan->blob) {
+        delete plan;
+        return SGL_ERR_INVALID_ARG;
+    }
+    std::memset(plan->blob, 0, plan->tables_bytes);
+    sgl::WsHeader hdr{0u, sgl::kWsMagic, plan->n_items, 0, plan->n_partial_rows, plan->n_ctas};
+    std::memcpy(plan->blob, &hdr, sizeof(hdr));
+    if (!items.empty()) std::memcpy(plan->blob + plan->off_items, items.data(), items.size() * sizeof(sgl::DecItem));
+    if (g->num_members) std::memcpy(plan->blob + plan->off_members, g->seg_members, (size_t)g->num_members * 4);
+    int32_t* mptr = reinterpret_cast<int32_t*>(plan->blob + plan->off_mptr);
+    int32_t* ment = reinterpret_cast<int32_t*>(plan->blob + plan->off_ment);
+    int64_t at = 0;
+    for (size_t i = 0; i < ents.size(); ++i) {
+        mptr[i] = (int32_t)at;
+        for (int32_t e : ents[i]) ment[at++] = e;
+    }
+    mptr[ents.size()] = (int32_t)at;
+    *plan_out = plan;
+    *workspace_bytes = plan->workspace_bytes;
+    return SGL_OK;
+}

@@ -29,7 +29,7 @@
 
 #include "common.h"
 
-namespace {
+namespace sgl {
 
 int query_num_sms(int32_t requested) {
     if (requested > 0) return requested;
@@ -40,10 +40,6 @@ int query_num_sms(int32_t requested) {
     cudaGetLastError();
     return 152;
 }
-
-}  // namespace
-
-namespace sgl {
 
 int check_params(const sgl_attn_params* p) {
     if (!p) return SGL_ERR_INVALID_ARG;
@@ -61,19 +57,7 @@ int check_params(const sgl_attn_params* p) {
     return SGL_OK;
 }
 
-}  // namespace sgl
-
-extern "C" {
-
-int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl_prefix_groups* g,
-                    sgl_plan** plan_out, size_t* workspace_bytes) {
-    int st = sgl::check_params(p);
-    if (st) return st;
-    if (!g || !plan_out || !workspace_bytes) return SGL_ERR_INVALID_ARG;
-    const int32_t B = p->batch;
-    if (B > 0 && !seq_lens) return SGL_ERR_INVALID_ARG;
-    const int32_t G = p->num_qo_heads / p->num_kv_heads;
-    const int32_t Hkv = p->num_kv_heads;
+int validate_groups(int32_t B, const int32_t* seq_lens, const sgl_prefix_groups* g) {
     const int32_t nseg = g->num_segments;
     if (nseg < 0 || (nseg > 0 && (!g->seg_begin || !g->seg_end || !g->seg_row || !g->seg_member_ptr ||
                                   !g->seg_members)))
@@ -106,13 +90,32 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
         }
         if (at != seq_lens[r]) return SGL_ERR_INVALID_ARG;
     }
+    return SGL_OK;
+}
+
+}  // namespace sgl
+
+extern "C" {
+
+int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl_prefix_groups* g,
+                    sgl_plan** plan_out, size_t* workspace_bytes) {
+    int st = sgl::check_params(p);
+    if (st) return st;
+    if (!g || !plan_out || !workspace_bytes) return SGL_ERR_INVALID_ARG;
+    const int32_t B = p->batch;
+    if (B > 0 && !seq_lens) return SGL_ERR_INVALID_ARG;
+    const int32_t G = p->num_qo_heads / p->num_kv_heads;
+    const int32_t Hkv = p->num_kv_heads;
+    const int32_t nseg = g->num_segments;
+    st = sgl::validate_groups(B, seq_lens, g);
+    if (st) return st;
 
     // Narrow segments (at most 8 query rows: member x query head of a KV
     // head) go to the streaming warps; wider ones to the tensor-core tiles
     // in member blocks of up to 128 rows.
     const int32_t MBn = std::max(1, 8 / G);
     const int32_t MBw = std::max(1, 128 / G);
-    const int sms = query_num_sms(p->num_sms);
+    const int sms = sgl::query_num_sms(p->num_sms);
 
     struct Unit {   // narrow work: one member block of a segment for one KV head
         int32_t rep_row, b, e, kvh, mem_begin, n_mem;
