@@ -57,11 +57,12 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-budget-s", type=float, default=60.0)
     ap.add_argument("--num-sms", type=int, default=0, help="decode planning target (0: the device's SM count)")
-    ap.add_argument("--only", choices=["all", "decode", "extend"], default="all",
+    ap.add_argument("--only", choices=["all", "decode", "extend", "mla"], default="all",
                     help="decode: skip the extend line; extend: time only the extend workload (profiling)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-sched", action="store_true", help="skip the host scheduling simulation")
     ap.add_argument("--no-fp8", action="store_true", help="skip the FP8 KV decode object")
+    ap.add_argument("--no-mla", action="store_true", help="skip the MLA decode object")
     ap.add_argument("--pool-slots", type=int, default=0,
                     help="decode pool size override (0: the workload's 2^20 slots); small pools serve ncu captures")
     return ap.parse_args()
@@ -324,6 +325,12 @@ def run_native(args):
         dist.init_process_group("nccl")
     sglbuild.build()
     hbm_peak, bf16_peak, peak_src = peaks()
+    if args.only == "mla":
+        r = bench_mla(sgl, W, torch, max(4, min(args.steps, 2000)), bf16_peak, hbm_peak, args.num_sms)
+        if rank == 0:
+            print(json.dumps({"metric": "mla decode ms per call", "value": r["ms_per_call"], "unit": "ms",
+                              "n_gpus": world, "mla": r}), flush=True)
+        return
     if args.only == "extend":
         ext = bench_extend(sgl, W, torch, max(3, args.extend_steps), bf16_peak)
         if rank == 0:
@@ -398,6 +405,10 @@ def run_native(args):
         e2e_gbs, h2d, d2h, e2e_step_s = e2e_decode(sgl, W, torch, w, tree, kd, vd, inst,
                                                    max(1, min(args.e2e_steps, K)), args.num_sms)
 
+    mla = None
+    if not args.no_mla and args.only == "all":
+        mla = bench_mla(sgl, W, torch, min(K, 2000), bf16_peak, hbm_peak, args.num_sms)
+
     fp8 = None
     if not args.no_fp8:
         fp8 = bench_fp8(sgl, W, torch, w, kd, vd, inst, min(K, 2000), hbm_peak, args.num_sms)
@@ -444,6 +455,8 @@ def run_native(args):
     }
     if fp8 is not None:
         line["fp8_kv"] = fp8
+    if mla is not None:
+        line["mla"] = mla
     if ext is not None:
         line["extend"] = ext
     if rank == 0 and args.only == "all" and not args.no_sched:
@@ -583,6 +596,78 @@ def bench_fp8(sgl, W, torch, w, kd, vd, inst, steps, hbm_peak, num_sms=0):
             "unique_kv_bytes_per_call": int(ub), "unique_kv_gbs": gbs, "frac_of_hbm": gbs / hbm_peak,
             "tokens_per_s": inst[0]["B"] / (ms / 1e3), "calls_timed": n,
             "path": "same plan as bf16: shared prefixes on tcgen05 tiles (codes converted to f16 in shared memory), the rest on streaming warps"}
+
+
+def bench_mla(sgl, W, torch, steps, bf16_peak, hbm_peak, num_sms=0):
+    """MLA grouped decode on the mla_decode batch (Hq 16 over one 576-element
+    stored row per token, the Llama-3-8B batch structure), rotating over 4
+    batch instances; CUDA-graph loop, CUDA events."""
+    w = W.get("mla_decode")
+    order, KV = W.make_mla_pool(w)
+    S = KV.shape[0]
+    kvd = KV.cuda()
+    del KV
+    tree = sgl.sgl_tree_create(S, w.page_size, order)
+    calls = []
+    for i in range(4):
+        b = W.make_batch(w, i)
+        seqs = b.all_tokens()
+        groups = sgl.sgl_groups_create()
+        out = sgl.sgl_build_batch(tree, seqs, groups=groups)
+        gnp = sgl.groups_as_numpy(sgl.sgl_groups_view(groups))
+        p = sgl.make_mla_params(len(seqs), w.Hq, S, page_size=w.page_size, num_sms=num_sms)
+        plan = sgl.sgl_mla_decode_plan(p, out["seq_lens"], sgl.sgl_groups_view(groups))
+        ws = torch.zeros(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
+        sgl.sgl_plan_upload(plan, ws)
+        q = W.to_dtype(w, b.q).cuda()
+        calls.append(dict(q=q, table=torch.from_numpy(out["req_to_token"]).cuda(),
+                          seq=torch.from_numpy(out["seq_lens"]).cuda(), plan=plan, ws=ws, groups=groups,
+                          o=torch.empty(len(seqs), w.Hq, w.dv, dtype=torch.bfloat16, device="cuda"),
+                          lse=torch.empty(len(seqs), w.Hq, dtype=torch.float32, device="cuda"),
+                          ub=int((gnp["seg_end"] - gnp["seg_begin"]).sum()) * w.d * 2,
+                          flops=2.0 * int(out["seq_lens"].sum()) * w.Hq * (w.d + w.dv), B=len(seqs)))
+        for r in range(len(seqs)):
+            sgl.sgl_tree_finish(tree, int(out["last_nodes"][r]), out["req_to_token"][r], len(seqs[r]))
+
+    def call(c):
+        sgl.sgl_mla_decode_attn(c["q"], kvd, c["table"], c["seq"], c["plan"], c["o"], c["lse"], c["ws"])
+
+    for c in calls:
+        call(c)
+    torch.cuda.synchronize()
+    for c in calls:
+        sgl.sgl_check(c["ws"])
+    n = max(len(calls), steps - steps % len(calls))
+    g = torch.cuda.CUDAGraph()
+    st = torch.cuda.Stream()
+    st.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(st):
+        with torch.cuda.graph(g, stream=st):
+            for j in range(n):
+                call(calls[j % len(calls)])
+    torch.cuda.current_stream().wait_stream(st)
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    for c in calls:
+        sgl.sgl_check(c["ws"])
+    ms = e0.elapsed_time(e1) / n
+    ub = sum(c["ub"] for c in calls) / len(calls)
+    fl = sum(c["flops"] for c in calls) / len(calls)
+    info = sgl.sgl_plan_info(calls[0]["plan"])
+    tf = fl / (ms / 1e3) / 1e12
+    return {"workload": "mla_decode", "heads": "Hq16 / one 576-element row (512 latent + 64 position), bf16",
+            "batch": calls[0]["B"], "ms_per_call": ms, "unique_kv_bytes_per_call": int(ub),
+            "unique_kv_gbs": ub / (ms / 1e3) / 1e9, "frac_of_hbm": ub / (ms / 1e3) / 1e9 / hbm_peak,
+            "attention_tflops": tf,
+            "roofline": {"bound": "tensor (mma.sync)", "achieved": tf, "peak": bf16_peak, "unit": "TFLOP/s",
+                         "frac": tf / bf16_peak, "peak_source": "measured bf16 burst (tcgen05 / cuBLAS)"},
+            "items": info["num_items"], "chunk_tokens": info["chunk_tokens"], "calls_timed": n,
+            "tokens_per_s": calls[0]["B"] / (ms / 1e3)}
 
 
 def bench_scheduling(sgl, W, w):

@@ -109,19 +109,17 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const __grid_co
     const int R = it.n_mem * a.Gp;
     const int32_t* trow = a.r2t + (int64_t)it.rep_row * a.ld;
 
-    // slots of block j (warp 0): -1 past the range or outside the pool (flagged)
-    auto lookup = [&](int j) {
+    // slots of block j (warp 0): the raw lookup is issued one block before
+    // it is checked and stored (-1 past the range or outside the pool,
+    // flagged), so the load never stalls warp 0's share of the math
+    auto fetch = [&](int j) -> int {
+        const int p = b + j * kBN + lane;
+        return (warp == 0 && j < nb && p < e) ? __ldg(trow + p) : -1;
+    };
+    auto store = [&](int j, int sl) {
         if (warp == 0 && j < nb) {
-            const int p = b + j * kBN + lane;
-            int sl = -1;
-            if (p < e) {
-                sl = __ldg(trow + p);
-                if (sl < 0 || sl >= a.num_slots) {
-                    atomicOr(a.err, 1u);
-                    sl = -1;
-                }
-            }
-            slots[(j % kSlotRing) * kBN + lane] = sl;
+            if (b + j * kBN + lane < e && (sl < 0 || sl >= a.num_slots)) atomicOr(a.err, 1u);
+            slots[(j % kSlotRing) * kBN + lane] = (sl < 0 || sl >= a.num_slots) ? -1 : sl;
         }
     };
     // block j's rows into stage j % kStages (zeros for missing rows); one group
@@ -146,9 +144,10 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const __grid_co
         const int head = it.kvh * a.Gp + (ok ? r % a.Gp : 0);
         cp_async16(sQ + rswz(r, c), a.q + ((int64_t)mem * a.Hq + head) * kDC + c * 8, ok);
     }
-    lookup(0);
-    lookup(1);
-    lookup(2);
+    store(0, fetch(0));
+    store(1, fetch(1));
+    store(2, fetch(2));
+    int pend = fetch(3);   // block 3's raw slot, stored in the first iteration
     __syncthreads();
     copy(0);
     copy(1);
@@ -162,7 +161,8 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const __grid_co
     const int bar_id = 1 + rg;                                     // named barrier of the group
 
     for (int j = 0; j < nb; ++j) {
-        lookup(j + 3);
+        store(j + 3, pend);
+        pend = fetch(j + 4);
         copy(j + 2);
         cp_async_wait<2>();   // groups of blocks <= j + 2 committed: block j has landed
         __syncthreads();

@@ -7,8 +7,8 @@
 // and all their query heads: the work unit is 64 query rows (member x head)
 // of one segment chunk.  With Hq query heads a unit holds 64 / min(Hq, 64)
 // members and min(Hq, 64) heads ("head group"; Hq = 128 has two groups of 64
-// heads that read the same rows).  Chunks are cut so that about four units
-// per SM exist (one CTA each, longest first); each writes normalised partial
+// heads that read the same rows).  Chunks are cut so that about one unit per
+// SM exists (one CTA each, longest first); each writes normalised partial
 // rows that the log-sum-exp merge combines per (request, head group).
 #include <algorithm>
 #include <cmath>
@@ -45,14 +45,15 @@ extern "C" int sgl_mla_decode_plan(const sgl_mla_params* p, const int32_t* seq_l
     const int32_t nseg = g->num_segments;
     const int sms = sgl::query_num_sms(p->num_sms);
 
-    // chunk length: about four items per SM, whole 32-position blocks
+    // chunk length: about one item per SM (an item reloads its 72 KB of
+    // query rows, so items are kept long), whole 32-position blocks
     int64_t work = 0;
     for (int32_t s = 0; s < nseg; ++s) {
         const int32_t nmem = g->seg_member_ptr[s + 1] - g->seg_member_ptr[s];
         work += (int64_t)(g->seg_end[s] - g->seg_begin[s]) * ((nmem + MB - 1) / MB) * Hg;
     }
-    int64_t C = (work + 4 * (int64_t)sms - 1) / std::max<int64_t>(1, 4 * (int64_t)sms);
-    C = std::min<int64_t>(2048, std::max<int64_t>(64, (C + kMlaBlock - 1) / kMlaBlock * kMlaBlock));
+    int64_t C = (work + sms - 1) / std::max<int64_t>(1, sms);
+    C = std::min<int64_t>(4096, std::max<int64_t>(64, (C + kMlaBlock - 1) / kMlaBlock * kMlaBlock));
 
     std::vector<sgl::DecItem> items;
     for (int32_t s = 0; s < nseg; ++s) {
