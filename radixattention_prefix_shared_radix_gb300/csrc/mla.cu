@@ -50,7 +50,8 @@ struct MlaLayout {
     static constexpr int OFF_SLOT = OFF_P + kRT * kBN * 2;           // [ring][32] int32
     static constexpr int OFF_MX = OFF_SLOT + kSlotRing * kBN * 4;    // [4 groups][4 warps][16] fp32
     static constexpr int OFF_LS = OFF_MX + 16 * 16 * 4;              // the same, for the row sums
-    static constexpr int END = OFF_LS + 16 * 16 * 4;
+    static constexpr int OFF_MEM = OFF_LS + 16 * 16 * 4;             // the item's member requests (at most 4)
+    static constexpr int END = OFF_MEM + 16;
     static constexpr int TOTAL = END + 128;                          // + alignment slack
     static_assert(TOTAL <= 232448, "shared memory per CTA");
 };
@@ -136,19 +137,24 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const __grid_co
         cp_async_commit();
     };
 
+    // the first blocks' slot lookups and the item's members (at most 4: the
+    // rows' requests) all in flight together, then staged in shared memory
+    const int f0 = fetch(0), f1 = fetch(1), f2 = fetch(2);
+    int* mems = reinterpret_cast<int*>(sm + MlaLayout::OFF_MEM);
+    if (tid < kRT / 16 && tid < it.n_mem) mems[tid] = __ldg(a.members + it.mem_begin + tid);
+    store(0, f0);
+    store(1, f1);
+    store(2, f2);
+    int pend = fetch(3);   // block 3's raw slot, stored in the first iteration
+    __syncthreads();
     // the item's query rows (zeros past R), with block 0's copies
     for (int i = tid; i < kRT * kCPR; i += kThreads) {
         const int r = i / kCPR, c = i - r * kCPR;
         const bool ok = r < R;
-        const int mem = ok ? __ldg(a.members + it.mem_begin + r / a.Gp) : 0;
+        const int mem = ok ? mems[r / a.Gp] : 0;
         const int head = it.kvh * a.Gp + (ok ? r % a.Gp : 0);
         cp_async16(sQ + rswz(r, c), a.q + ((int64_t)mem * a.Hq + head) * kDC + c * 8, ok);
     }
-    store(0, fetch(0));
-    store(1, fetch(1));
-    store(2, fetch(2));
-    int pend = fetch(3);   // block 3's raw slot, stored in the first iteration
-    __syncthreads();
     copy(0);
     copy(1);
 
@@ -167,15 +173,25 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const __grid_co
         cp_async_wait<2>();   // groups of blocks <= j + 2 committed: block j has landed
         __syncthreads();
         const uint32_t st = sKV + (uint32_t)((j % kStages) * kBN * kRowB);
-        // ---- S for rows r0.., positions 8 wq.. (two accumulators)
+        // ---- S for rows r0.., positions 8 wq.. (two accumulators).  The
+        // fragments of k-step ks + 2 are loaded before the MMA of ks (the
+        // loads and MMAs are volatile asm, kept in source order), so an MMA
+        // never waits on the load just before it.
         float s[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
         if (active) {
-#pragma unroll 4
-            for (int ks = 0; ks < kDC / 16; ++ks) {
-                uint32_t qa[4], kb0, kb1;
-                ldsm_x4(sQ + rswz(r0 + (lane & 15), 2 * ks + (lane >> 4)), qa[0], qa[1], qa[2], qa[3]);
-                ldsm_x2(st + rswz(8 * wq + (lane & 7), 2 * ks + ((lane >> 3) & 1)), kb0, kb1);
-                mma16816((ks & 1) ? s2 : s, qa, kb0, kb1);
+            constexpr int NK = kDC / 16;
+            uint32_t qa[3][4], kb[3][2];
+            auto load_s = [&](int ks, int buf) {
+                ldsm_x4(sQ + rswz(r0 + (lane & 15), 2 * ks + (lane >> 4)), qa[buf][0], qa[buf][1], qa[buf][2],
+                        qa[buf][3]);
+                ldsm_x2(st + rswz(8 * wq + (lane & 7), 2 * ks + ((lane >> 3) & 1)), kb[buf][0], kb[buf][1]);
+            };
+            load_s(0, 0);
+            load_s(1, 1);
+#pragma unroll
+            for (int ks = 0; ks < NK; ++ks) {
+                if (ks + 2 < NK) load_s(ks + 2, (ks + 2) % 3);
+                mma16816((ks & 1) ? s2 : s, qa[ks % 3], kb[ks % 3][0], kb[ks % 3][1]);
             }
         }
         const int pos = b + j * kBN + 8 * wq + 2 * t;
@@ -230,18 +246,22 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const __grid_co
         named_bar(bar_id, 128);
         // ---- O[rows r0.., columns 128 wq..] += P V
         if (active) {
+            // 16 steps (k-step ks, column pair np): V fragments one step ahead
+            uint32_t pa[2][4], vb[2][4];
+            ldsm_x4(sP + pswz(r0 + (lane & 15), lane >> 4), pa[0][0], pa[0][1], pa[0][2], pa[0][3]);
+            ldsm_x4(sP + pswz(r0 + (lane & 15), 2 + (lane >> 4)), pa[1][0], pa[1][1], pa[1][2], pa[1][3]);
+            auto load_v = [&](int step, int buf) {
+                const int ks = step >> 3, np = step & 7;
+                ldsm_x4_t(st + rswz(16 * ks + (lane & 7) + ((lane >> 3) & 1) * 8, 16 * wq + 2 * np + (lane >> 4)),
+                          vb[buf][0], vb[buf][1], vb[buf][2], vb[buf][3]);
+            };
+            load_v(0, 0);
 #pragma unroll
-            for (int ks = 0; ks < kBN / 16; ++ks) {
-                uint32_t pa[4];
-                ldsm_x4(sP + pswz(r0 + (lane & 15), 2 * ks + (lane >> 4)), pa[0], pa[1], pa[2], pa[3]);
-#pragma unroll
-                for (int np = 0; np < 8; ++np) {
-                    uint32_t vb[4];
-                    ldsm_x4_t(st + rswz(16 * ks + (lane & 7) + ((lane >> 3) & 1) * 8, 16 * wq + 2 * np + (lane >> 4)),
-                              vb[0], vb[1], vb[2], vb[3]);
-                    mma16816(o[2 * np], pa, vb[0], vb[1]);
-                    mma16816(o[2 * np + 1], pa, vb[2], vb[3]);
-                }
+            for (int step = 0; step < 2 * 8; ++step) {
+                if (step + 1 < 16) load_v(step + 1, (step + 1) & 1);
+                const int ks = step >> 3, np = step & 7, bf = step & 1;
+                mma16816(o[2 * np], pa[ks], vb[bf][0], vb[bf][1]);
+                mma16816(o[2 * np + 1], pa[ks], vb[bf][2], vb[bf][3]);
             }
         }
         __syncthreads();   // stage j % kStages and P are free again
