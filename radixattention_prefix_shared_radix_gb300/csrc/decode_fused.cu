@@ -158,18 +158,12 @@ __device__ __forceinline__ void lds64(uint32_t addr, uint32_t* w) {
     asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];\n" : "=r"(w[0]), "=r"(w[1]) : "r"(addr));
 }
 
-__device__ __forceinline__ int ld_volatile_shared_s32(uint32_t addr) {
-    int32_t v;
-    asm volatile("ld.volatile.shared.b32 %0, [%1];\n" : "=r"(v) : "r"(addr) : "memory");
-    return v;
-}
-
 // stage descriptor flags
 constexpr int kFirst = 1;   // first step of its piece: its query rows are in the stage's Q slot
 constexpr int kEnd = 4;     // no more pieces: the consumer stops
 
 // slot-ring entry (one looked-up step): 16 slots, then
-constexpr int kEntKvh = 64, kEntId = 68, kEntP0 = 72, kEntFlags = 76, kEntCm = 80, kEntPb = 84, kEntRows = 88;
+constexpr int kEntKvh = 64, kEntP0 = 72, kEntFlags = 76, kEntCm = 80, kEntPb = 84, kEntRows = 88;
 constexpr int kEntMem = 96;   // 8 ints: member request of each query row (first step only)
 // stage descriptor
 constexpr int kDescP0 = 0, kDescFlags = 4, kDescCm = 8, kDescPb = 12, kDescRows = 16, kDescQ = 20;
