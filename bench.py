@@ -300,8 +300,7 @@ def e2e_decode(sgl, W, torch, w, tree, kd, vd, inst, steps, num_sms=0):
         pb["o"].copy_(it["o"], non_blocking=True)
         pb["lse"].copy_(it["lse"], non_blocking=True)
         stream.synchronize()
-        for r in range(it["B"]):
-            sgl.sgl_tree_finish(tree, int(out["last_nodes"][r]), out["req_to_token"][r], len(it["seqs"][r]))
+        sgl.sgl_tree_finish_batch(tree, out)
         if s == 0:
             h2d = (pb["q"].numel() * 2 + pb["table"].numel() * 4 + pb["seq"].numel() * 4 +
                    sgl.sgl_plan_info(plan)["upload_bytes"])

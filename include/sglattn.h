@@ -198,6 +198,12 @@ int sgl_build_batch(sgl_tree* tree, int32_t B, const int32_t* const* tokens, con
 /* A request is done: unlock its last node and free its private tail page
  * (row: host, its req_to_token row; len: its length). */
 int sgl_tree_finish(sgl_tree* tree, sgl_node last, const int32_t* row, int64_t len);
+/* sgl_tree_finish for requests 0 .. B-1 in order (a batch from
+ * sgl_build_batch): last host [B], req_to_token host [B, ld], seq_lens host
+ * [B].  Stops at the first error and returns it (earlier requests stay
+ * finished). */
+int sgl_tree_finish_batch(sgl_tree* tree, int32_t B, const sgl_node* last, const int32_t* req_to_token, int64_t ld,
+                          const int32_t* seq_lens);
 
 int sgl_groups_create(sgl_groups** out);
 void sgl_groups_destroy(sgl_groups* groups);

@@ -110,6 +110,7 @@ _SIGS = {
     "sgl_build_batch": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.POINTER(_I32P), _I64P, _I32P, ctypes.c_int64,
                                        _I32P, _I32P, _I64P, _P]),
     "sgl_tree_finish": (ctypes.c_int, [_P, ctypes.c_int64, _I32P, ctypes.c_int64]),
+    "sgl_tree_finish_batch": (ctypes.c_int, [_P, ctypes.c_int32, _I64P, _I32P, ctypes.c_int64, _I32P]),
     "sgl_groups_create": (ctypes.c_int, [ctypes.POINTER(_P)]),
     "sgl_groups_destroy": (None, [_P]),
     "sgl_groups_view": (ctypes.c_int, [_P, ctypes.POINTER(SglPrefixGroups)]),
@@ -291,7 +292,11 @@ def sgl_build_batch(tree, token_lists, ld=None, groups=None):
     seq = np.zeros(B, dtype=np.int32)
     pre = np.zeros(B, dtype=np.int32)
     last = np.zeros(B, dtype=np.int64)
-    arr = (_I32P * max(B, 1))(*[_ptr32(t) for t in toks])
+    # the rows' addresses as one array (cheaper than a ctypes pointer per row)
+    ptrs = np.fromiter((t.__array_interface__["data"][0] for t in toks), dtype=np.uint64, count=B)
+    if B == 0:
+        ptrs = np.zeros(1, dtype=np.uint64)
+    arr = ptrs.ctypes.data_as(ctypes.POINTER(_I32P))
     _ok(_lib().sgl_build_batch(tree, B, arr, lens.ctypes.data_as(_I64P), _ptr32(table), ld, _ptr32(seq),
                                _ptr32(pre), last.ctypes.data_as(_I64P), groups), "sgl_build_batch")
     return {"req_to_token": table, "seq_lens": seq, "prefix_lens": pre, "last_nodes": last}
@@ -300,6 +305,15 @@ def sgl_build_batch(tree, token_lists, ld=None, groups=None):
 def sgl_tree_finish(tree, last, row, length):
     r = _i32(row)
     _ok(_lib().sgl_tree_finish(tree, int(last), _ptr32(r), int(length)), "sgl_tree_finish")
+
+
+def sgl_tree_finish_batch(tree, out):
+    """Finish every request of a sgl_build_batch result (its dict)."""
+    last = np.ascontiguousarray(out["last_nodes"], dtype=np.int64)
+    table = np.ascontiguousarray(out["req_to_token"], dtype=np.int32)
+    seq = _i32(out["seq_lens"])
+    _ok(_lib().sgl_tree_finish_batch(tree, len(seq), last.ctypes.data_as(_I64P), _ptr32(table), table.shape[1],
+                                     _ptr32(seq)), "sgl_tree_finish_batch")
 
 
 def sgl_groups_create():

@@ -123,8 +123,11 @@ struct sgl_tree {
 
     int64_t common_pages(const Node* c, const int32_t* toks, int64_t avail) const {
         int64_t lim = std::min<int64_t>((int64_t)c->tokens.size(), avail);
+        const int32_t* a = c->tokens.data();
         int64_t k = 0;
-        while (k < lim && c->tokens[k] == toks[k]) ++k;
+        // whole blocks of 8 tokens first, then token by token
+        while (k + 8 <= lim && std::memcmp(a + k, toks + k, 8 * sizeof(int32_t)) == 0) k += 8;
+        while (k < lim && a[k] == toks[k]) ++k;
         return k / P * P;
     }
 
@@ -141,9 +144,14 @@ struct sgl_tree {
             bool partial = k < (int64_t)c->tokens.size();
             if (partial) c = split(c, k);
             c->last_access = clock;
-            if (slots)
-                for (int32_t pg : c->pages)
-                    for (int32_t o = 0; o < P; ++o) slots->push_back(pg * P + o);
+            if (slots) {
+                if (P == 1) {
+                    slots->insert(slots->end(), c->pages.begin(), c->pages.end());
+                } else {
+                    for (int32_t pg : c->pages)
+                        for (int32_t o = 0; o < P; ++o) slots->push_back(pg * P + o);
+                }
+            }
             pos += k;
             node = c;
             if (partial) break;
@@ -154,10 +162,20 @@ struct sgl_tree {
 
     // Insert full pages; duplicates go back to the free list.
     Node* insert(const int32_t* toks, const int32_t* pages_in, int64_t n_full, int64_t* dup) {
+        return insert_from(&root, toks, pages_in, n_full, dup);
+    }
+    // The same, resuming at `start`, a node whose path from the root holds
+    // exactly the first start->depth + |start->tokens| tokens with the
+    // caller's own pages (a locked node just returned by match for these
+    // tokens): the walk over that path would find the same nodes, split
+    // none of them and find no duplicate page, so only its stamps are
+    // applied.
+    Node* insert_from(Node* start, const int32_t* toks, const int32_t* pages_in, int64_t n_full, int64_t* dup) {
         ++clock;
-        int64_t pos = 0;
         *dup = 0;
-        Node* node = &root;
+        for (Node* x = start; x != &root; x = x->parent) x->last_access = clock;
+        int64_t pos = start == &root ? 0 : start->depth + (int64_t)start->tokens.size();
+        Node* node = start;
         while (pos < n_full) {
             Node* c = find_child(node, toks + pos);
             if (!c) {
@@ -276,6 +294,12 @@ struct sgl_tree {
     // page's consecutive slots or out of range.
     bool pages_of(const int32_t* slots, int64_t n_full, std::vector<int32_t>* pages) const {
         pages->clear();
+        if (P == 1) {   // a slot is its page: range checks, then one copy
+            for (int64_t i = 0; i < n_full; ++i)
+                if (slots[i] < 0 || slots[i] >= num_pages) return false;
+            pages->assign(slots, slots + n_full);
+            return true;
+        }
         for (int64_t i = 0; i < n_full; i += P) {
             int32_t s = slots[i];
             if (s < 0 || s % P) return false;
@@ -483,7 +507,9 @@ int sgl_build_batch(sgl_tree* t, int32_t B, const int32_t* const* tokens, const 
         n_full[r] = L / P * P;
         t->pages_of(row.data(), n_full[r], &pages);
         int64_t dup = 0;
-        Node* last = t->insert(tokens[r], pages.data(), n_full[r], &dup);
+        // mnode is locked and its path holds tokens[0, m) with the slots just
+        // taken from it
+        Node* last = t->insert_from(mnode, tokens[r], pages.data(), n_full[r], &dup);
         t->lock(last);
         t->unlock(mnode);
         lasts[r] = last;
@@ -547,6 +573,17 @@ int sgl_tree_finish(sgl_tree* t, sgl_node last, const int32_t* row, int64_t len)
     if (!t->unlock(n)) return SGL_ERR_STATE;
     int64_t nf = len / t->P * t->P;
     if (len > nf && !t->free_slots(row + nf, len - nf)) return SGL_ERR_INVALID_ARG;
+    return SGL_OK;
+}
+
+int sgl_tree_finish_batch(sgl_tree* t, int32_t B, const sgl_node* last, const int32_t* req_to_token, int64_t ld,
+                          const int32_t* seq_lens) {
+    if (!t || B < 0 || ld < 0 || (B > 0 && (!last || !req_to_token || !seq_lens))) return SGL_ERR_INVALID_ARG;
+    for (int32_t r = 0; r < B; ++r) {
+        if (seq_lens[r] < 0 || seq_lens[r] > ld) return SGL_ERR_INVALID_ARG;
+        const int st = sgl_tree_finish(t, last[r], req_to_token + (int64_t)r * ld, seq_lens[r]);
+        if (st) return st;
+    }
     return SGL_OK;
 }
 

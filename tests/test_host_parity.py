@@ -205,3 +205,32 @@ def test_workload_tables_bit_exact(name):
     _groups_eq(_lib_groups(g), prefix_groups(table, out["seq_lens"]))
     sgl.sgl_groups_destroy(g)
     sgl.sgl_tree_destroy(t)
+
+
+@pytest.mark.parametrize("P", [1, 4])
+def test_finish_batch_equals_finishing_one_by_one(P):
+    """sgl_tree_finish_batch leaves the tree exactly as finishing the batch's
+    requests one by one does (same stats, same later matches and evictions)."""
+    rng = np.random.default_rng(5 + P)
+    base = list(rng.integers(0, 1000, size=90))
+    seqs = [base + list(rng.integers(0, 1000, size=int(n))) for n in rng.integers(0, 40, size=6)] + [base[:17], []]
+    trees = []
+    for batched in (False, True):
+        t = sgl.sgl_tree_create(4096, P, np.arange(4096 // P, dtype=np.int32))
+        out = sgl.sgl_build_batch(t, seqs)
+        if batched:
+            sgl.sgl_tree_finish_batch(t, out)
+        else:
+            for r in range(len(seqs)):
+                sgl.sgl_tree_finish(t, int(out["last_nodes"][r]), out["req_to_token"][r], len(seqs[r]))
+        trees.append(t)
+    try:
+        assert sgl.sgl_tree_stats(trees[0]) == sgl.sgl_tree_stats(trees[1])
+        # the same state: the same eviction, then the same match of every request
+        assert sgl.sgl_tree_evict(trees[0], 64) == sgl.sgl_tree_evict(trees[1], 64)
+        for s in seqs:
+            a, b = sgl.sgl_tree_match(trees[0], s), sgl.sgl_tree_match(trees[1], s)
+            assert a[0] == b[0] and np.array_equal(a[1], b[1])
+    finally:
+        for t in trees:
+            sgl.sgl_tree_destroy(t)
