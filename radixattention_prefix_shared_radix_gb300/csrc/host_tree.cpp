@@ -169,12 +169,14 @@ struct sgl_tree {
     // caller's own pages (a locked node just returned by match for these
     // tokens): the walk over that path would find the same nodes, split
     // none of them and find no duplicate page, so only its stamps are
-    // applied.
+    // applied.  pages_in holds the pages from that node's end on.
     Node* insert_from(Node* start, const int32_t* toks, const int32_t* pages_in, int64_t n_full, int64_t* dup) {
         ++clock;
         *dup = 0;
         for (Node* x = start; x != &root; x = x->parent) x->last_access = clock;
-        int64_t pos = start == &root ? 0 : start->depth + (int64_t)start->tokens.size();
+        const int64_t pos0 = start == &root ? 0 : start->depth + (int64_t)start->tokens.size();
+        const int64_t pg0 = pos0 / P;   // page index of pages_in[0]
+        int64_t pos = pos0;
         Node* node = start;
         while (pos < n_full) {
             Node* c = find_child(node, toks + pos);
@@ -182,7 +184,7 @@ struct sgl_tree {
                 Node* m = new_node();
                 m->parent = node;
                 m->tokens.assign(toks + pos, toks + n_full);
-                m->pages.assign(pages_in + pos / P, pages_in + n_full / P);
+                m->pages.assign(pages_in + (pos / P - pg0), pages_in + (n_full / P - pg0));
                 m->first_pid = next_pid;
                 next_pid += (n_full - pos) / P;
                 m->last_access = clock;
@@ -196,7 +198,7 @@ struct sgl_tree {
             int64_t k = common_pages(c, toks + pos, n_full - pos);
             if (k < (int64_t)c->tokens.size()) c = split(c, k);
             for (int64_t i = 0; i < k / P; ++i) {
-                int32_t mine = pages_in[pos / P + i];
+                int32_t mine = pages_in[pos / P - pg0 + i];
                 if (c->pages[i] != mine) {
                     *dup += P;
                     free_pages.push_back(mine);
@@ -505,7 +507,8 @@ int sgl_build_batch(sgl_tree* t, int32_t B, const int32_t* const* tokens, const 
         }
         row.insert(row.end(), fresh.begin(), fresh.end());
         n_full[r] = L / P * P;
-        t->pages_of(row.data(), n_full[r], &pages);
+        // pages of the unmatched full pages only (the matched ones are the tree's)
+        t->pages_of(row.data() + m, n_full[r] - m, &pages);
         int64_t dup = 0;
         // mnode is locked and its path holds tokens[0, m) with the slots just
         // taken from it
