@@ -231,16 +231,30 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
     }
     const int32_t n_wide = (int32_t)items.size();
     items.insert(items.end(), narrow.begin(), narrow.end());
-    std::vector<std::vector<int32_t>> ents((size_t)B * Hkv);
+    // merge lists of (request, KV head), entries in item order: counted,
+    // then filled (one flat array)
+    const size_t n_keys = (size_t)B * Hkv;
+    std::vector<int32_t> eptr(n_keys + 1, 0);
     int64_t prow = 0;
     for (auto& it : items) {
         it.partial_base = (int32_t)prow;
-        for (int32_t i = 0; i < it.n_mem; ++i) {
-            const int32_t r = g->seg_members[it.mem_begin + i];
-            ents[(size_t)r * Hkv + it.kvh].push_back((int32_t)(prow + (int64_t)i * G));
-        }
+        for (int32_t i = 0; i < it.n_mem; ++i) ++eptr[(size_t)g->seg_members[it.mem_begin + i] * Hkv + it.kvh + 1];
         prow += (int64_t)it.n_mem * G;
         if (prow > INT32_MAX / 256) return SGL_ERR_UNSUPPORTED;
+    }
+    int32_t max_ent = 0;
+    for (size_t k = 0; k < n_keys; ++k) {
+        max_ent = std::max(max_ent, eptr[k + 1]);
+        eptr[k + 1] += eptr[k];
+    }
+    const int64_t n_ent = eptr[n_keys];
+    std::vector<int32_t> ents_flat((size_t)n_ent);
+    {
+        std::vector<int32_t> fill(eptr.begin(), eptr.end() - 1);
+        for (const auto& it : items)
+            for (int32_t i = 0; i < it.n_mem; ++i)
+                ents_flat[fill[(size_t)g->seg_members[it.mem_begin + i] * Hkv + it.kvh]++] =
+                    it.partial_base + i * G;
     }
 
     sgl_plan* plan = new (std::nothrow) sgl_plan();
@@ -257,12 +271,6 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
     plan->n_init = (int32_t)n_init;
     plan->n_tile_ctas = (int32_t)n_tile_ctas;
     plan->n_members = g->num_members;
-    int64_t n_ent = 0;
-    int32_t max_ent = 0;
-    for (auto& v : ents) {
-        n_ent += (int64_t)v.size();
-        max_ent = std::max<int32_t>(max_ent, (int32_t)v.size());
-    }
     plan->n_merge_entries = (int32_t)n_ent;
     plan->chunk_tokens = (int32_t)Cw;
     plan->max_pos = 0;
@@ -297,14 +305,8 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
     // run-time piece counter: next piece to hand out, producers finished
     const uint32_t sched[2] = {(uint32_t)n_init, 0u};
     std::memcpy(plan->blob + plan->off_sched, sched, sizeof(sched));
-    int32_t* mptr = reinterpret_cast<int32_t*>(plan->blob + plan->off_mptr);
-    int32_t* ment = reinterpret_cast<int32_t*>(plan->blob + plan->off_ment);
-    int64_t at = 0;
-    for (size_t i = 0; i < ents.size(); ++i) {
-        mptr[i] = (int32_t)at;
-        for (int32_t e : ents[i]) ment[at++] = e;
-    }
-    mptr[ents.size()] = (int32_t)at;
+    std::memcpy(plan->blob + plan->off_mptr, eptr.data(), eptr.size() * 4);
+    if (n_ent) std::memcpy(plan->blob + plan->off_ment, ents_flat.data(), (size_t)n_ent * 4);
     *plan_out = plan;
     *workspace_bytes = plan->workspace_bytes;
     return SGL_OK;
