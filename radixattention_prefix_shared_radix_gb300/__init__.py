@@ -284,17 +284,24 @@ def sgl_sim_run(tree, requests, policy=SGL_SCHED_LPM, insert_at=SGL_INSERT_AT_PR
 
 def sgl_build_batch(tree, token_lists, ld=None, groups=None):
     """Returns dict(req_to_token [B, ld] int32, seq_lens, prefix_lens, last_nodes) (numpy)."""
-    toks = [_i32(t) for t in token_lists]
+    toks = [t if (isinstance(t, np.ndarray) and t.dtype == np.int32 and t.ndim == 1 and t.flags.c_contiguous)
+            else _i32(t) for t in token_lists]
     B = len(toks)
-    lens = np.array([len(t) for t in toks], dtype=np.int64)
-    ld = int(ld if ld is not None else max([1] + [len(t) for t in toks]))
-    table = np.zeros((B, ld), dtype=np.int32)
+    lens = np.fromiter((t.shape[0] for t in toks), dtype=np.int64, count=B)
+    ld = int(ld if ld is not None else max(1, int(lens.max()) if B else 1))
+    table = np.empty((B, ld), dtype=np.int32)   # every entry is written (-1 past a row's length)
     seq = np.zeros(B, dtype=np.int32)
     pre = np.zeros(B, dtype=np.int32)
     last = np.zeros(B, dtype=np.int64)
-    # the rows' addresses as one array (cheaper than a ctypes pointer per row)
-    ptrs = np.fromiter((t.__array_interface__["data"][0] for t in toks), dtype=np.uint64, count=B)
-    if B == 0:
+    # the rows back to back in one array and their addresses computed in
+    # one step (per-row ctypes or array-interface lookups cost more than
+    # the copy)
+    if B:
+        flat = np.concatenate(toks) if B > 1 else toks[0]
+        offs = np.zeros(B, dtype=np.uint64)
+        np.cumsum(lens[:-1], out=offs[1:])
+        ptrs = offs * np.uint64(4) + np.uint64(flat.ctypes.data)
+    else:
         ptrs = np.zeros(1, dtype=np.uint64)
     arr = ptrs.ctypes.data_as(ctypes.POINTER(_I32P))
     _ok(_lib().sgl_build_batch(tree, B, arr, lens.ctypes.data_as(_I64P), _ptr32(table), ld, _ptr32(seq),
