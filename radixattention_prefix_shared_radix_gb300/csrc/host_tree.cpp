@@ -236,7 +236,7 @@ struct sgl_tree {
             return std::make_pair(v->last_access, v->first_pid + (int64_t)v->pages.size() - 1);
         };
         std::priority_queue<Key, std::vector<Key>, std::greater<Key>> heap;
-        std::vector<Node*> stack(root.children.begin(), root.children.end());
+        std::vector<Node*> stack = root.children;
         while (!stack.empty()) {
             Node* n = stack.back();
             stack.pop_back();
