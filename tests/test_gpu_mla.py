@@ -108,3 +108,35 @@ def test_mla_full_size():
         print("mla_decode: O max-abs %.3g, LSE max-abs %.3g, items %d" % (do, dl, info["num_items"]))
     finally:
         case.close()
+
+
+def test_mla_out_of_pool_slot_is_reported_not_read():
+    case = _mla_case("mla_decode_small")
+    try:
+        w = case.w
+        p = sgl.make_mla_params(case.B, w.Hq, case.S)
+        plan = sgl.sgl_mla_decode_plan(p, case.out["seq_lens"], sgl.sgl_groups_view(case.groups))
+        ws = torch.zeros(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
+        sgl.sgl_plan_upload(plan, ws)
+        table = torch.from_numpy(case.out["req_to_token"]).cuda()
+        # a position of request 3's own suffix (shared positions are read
+        # from the segment's representative row)
+        table[3, int(case.out["seq_lens"][3]) - 1] = case.S + 11
+        qd = case.q_host().cuda()
+        kvd = case.K.cuda()
+        o = torch.empty(case.B, w.Hq, w.dv, dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty(case.B, w.Hq, dtype=torch.float32, device="cuda")
+        seq = torch.from_numpy(case.out["seq_lens"]).cuda()
+        sgl.sgl_mla_decode_attn(qd, kvd, table, seq, plan, o, lse, ws)
+        with pytest.raises(sgl.SglError) as e:
+            sgl.sgl_check(ws)
+        assert e.value.status == -5
+        sgl.sgl_check(ws)          # the word was cleared
+        # a plan that disagrees with the device seq_lens is reported too
+        seq[0] = 1
+        sgl.sgl_mla_decode_attn(qd, kvd, torch.from_numpy(case.out["req_to_token"]).cuda(), seq, plan, o, lse, ws)
+        with pytest.raises(sgl.SglError):
+            sgl.sgl_check(ws)
+        del plan
+    finally:
+        case.close()
