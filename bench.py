@@ -528,12 +528,39 @@ def bench_extend(sgl, W, torch, steps, bf16_peak):
     e1.record()
     torch.cuda.synchronize()
     ms_kv = e0.elapsed_time(e1) / steps
+
+    # the same step over FP8 (E4M3) copies of the pools (per-tensor scales
+    # amax / 448; the new tokens' rows are in the pools as in the bf16 step)
+    def q8(x):
+        sc = float(x.float().abs().max()) / 448.0
+        return W.quantize_e4m3(x, sc), sc
+    k8, ks = q8(kd)
+    v8, vs = q8(vd)
+    p8 = sgl.make_params(sgl.SGL_DTYPE_BF16_FP8KV, len(seqs), w.Hq, w.Hkv, w.d, S, w.page_size, k_scale=ks,
+                         v_scale=vs, host_prefix_lens=pre, host_extend_lens=ext)
+
+    def call_fp8():
+        sgl.sgl_extend_attn(q, k8, v8, table, pre_d, ext_d, p8, o, lse, ws)
+
+    for _ in range(3):
+        call_fp8()
+    torch.cuda.synchronize()
+    sgl.sgl_check(ws)
+    e0.record()
+    for _ in range(steps):
+        call_fp8()
+    e1.record()
+    torch.cuda.synchronize()
+    ms_f8 = e0.elapsed_time(e1) / steps
+    del k8, v8
     return {"workload": EXTEND_WORKLOAD, "tflops": tflops, "ms_per_call": ms, "gflop_per_call": flops / 1e9,
             "roofline": {"bound": "tensor", "achieved": tflops, "peak": bf16_peak, "unit": "TFLOP/s",
                          "frac": tflops / bf16_peak, "peak_source": "measured bf16 burst"},
             "tokens_per_s": int(ext.sum()) / (ms / 1e3), "steps": steps,
             "kv_write_fused": {"ms_per_call": ms_kv, "tflops": flops / (ms_kv / 1e3) / 1e12,
-                               "kv_bytes_written": int(kn.numel() * 2 * 2)}}
+                               "kv_bytes_written": int(kn.numel() * 2 * 2)},
+            "fp8_kv": {"ms_per_call": ms_f8, "tflops": flops / (ms_f8 / 1e3) / 1e12,
+                       "kv_dtype": "e4m3 (per-tensor scales); one K/V stage, codes converted to f16 in shared memory"}}
 
 
 def bench_fp8(sgl, W, torch, w, kd, vd, inst, steps, hbm_peak, num_sms=0):

@@ -70,7 +70,8 @@ enum {
 
 enum { SGL_DTYPE_F32 = 0, SGL_DTYPE_BF16 = 1, SGL_DTYPE_BF16_FP8KV = 2 };
 /* SGL_DTYPE_BF16_FP8KV: Q and O bf16, the K and V pools FP8 E4M3 bytes
- * (decode only); K = k_scale * pool value, V = v_scale * pool value
+ * (decode and extend; the fused KV write of sgl_extend_attn_kvwrite is
+ * SGL_ERR_UNSUPPORTED); K = k_scale * pool value, V = v_scale * pool value
  * (per-tensor scales in sgl_attn_params).  ["SGLang 深度拆解" (the FP8 KV
  * cache halves the KV bytes); CS349D lecture-16 notes §4 (FP8 KV cache)] */
 

@@ -38,11 +38,11 @@ template <int D, bool F8>
 int launch_decode_fused(const sgl_plan* plan, const void* q, const void* kp, const void* vp, const int32_t* r2t,
                         int64_t ld, const int32_t* seq_lens, void* o, float* lse, unsigned char* ws, float scale_log2,
                         cudaStream_t s);
-template <int D>
+template <int D, bool F8>
 int launch_extend_tc(const void* q, const void* kp, const void* vp, const void* kn, const void* vn, void* kw, void* vw,
                      const int32_t* r2t, int64_t ld, const int32_t* pre, const int32_t* ext, int B, int64_t n_rows,
                      int64_t tiles, void* o, float* lse, uint32_t* err, int Hq, int Hkv, int64_t num_slots,
-                     float scale_log2, cudaStream_t s);
+                     float scale_log2, float k_scale, float v_scale, cudaStream_t s);
 }  // namespace sgl
 
 namespace {
@@ -265,10 +265,14 @@ int launch_extend(const sgl_attn_params* p, const void* q, const void* kp, const
         tiles += ((p->host_extend_lens[r] + tq - 1) / tq + 1) / 2;   // CTAs: pairs of query tiles
     }
     if (total_rows == 0) return SGL_OK;
-    if (p->dtype == SGL_DTYPE_BF16) {
+    if (p->dtype == SGL_DTYPE_BF16 || p->dtype == SGL_DTYPE_BF16_FP8KV) {
         if (tiles > INT32_MAX) return SGL_ERR_UNSUPPORTED;
-        int e = sgl::launch_extend_tc<D>(q, kp, vp, kn, vn, kw, vw, r2t, ld, pre, ext, B, total_rows, tiles, o, lse,
-                                         err, Hq, Hkv, p->num_slots, sl2, s);
+        const int e = p->dtype == SGL_DTYPE_BF16_FP8KV
+                          ? sgl::launch_extend_tc<D, true>(q, kp, vp, kn, vn, kw, vw, r2t, ld, pre, ext, B, total_rows,
+                                                           tiles, o, lse, err, Hq, Hkv, p->num_slots, sl2, p->k_scale,
+                                                           p->v_scale, s)
+                          : sgl::launch_extend_tc<D, false>(q, kp, vp, kn, vn, kw, vw, r2t, ld, pre, ext, B, total_rows,
+                                                            tiles, o, lse, err, Hq, Hkv, p->num_slots, sl2, 1.f, 1.f, s);
         if (e) return cuda_status(static_cast<cudaError_t>(e));
     } else {
         if (kn) {
@@ -332,7 +336,8 @@ static int extend_impl(const void* q_new, const void* k_new, const void* v_new, 
                        float* lse, void* workspace, size_t ws_bytes, sgl_stream_t stream) {
     int st = sgl::check_params(params);
     if (st) return st;
-    if (params->dtype == SGL_DTYPE_BF16_FP8KV) return SGL_ERR_UNSUPPORTED;   // FP8 KV: decode only
+    // FP8 KV pools: extend reads them; the fused KV write (bf16 new rows) is not offered
+    if (params->dtype == SGL_DTYPE_BF16_FP8KV && k_new) return SGL_ERR_UNSUPPORTED;
     const int32_t B = params->batch;
     if (B > 0 && (!params->host_extend_lens || !params->host_prefix_lens || !prefix_lens || !extend_lens))
         return SGL_ERR_INVALID_ARG;

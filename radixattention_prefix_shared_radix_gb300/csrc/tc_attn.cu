@@ -29,9 +29,11 @@ using namespace tc;
 
 // two query tiles, 128-position blocks (S MMAs of N = 128: an M = 128
 // tcgen05 MMA costs about the same time for N = 64 as for N = 128), one score
-// buffer each, 2 K/V stages (4 for d = 64), a gather team of 6 warps
-template <int D>
-using ExtCfg = TcCfg<D, false, 2, 2 * (128 / D), 6, 128, 1>;
+// buffer each, 2 K/V stages (4 for d = 64), a gather team of 6 warps.  With
+// an FP8 pool (codes staged by the gather team and converted to f16) one
+// stage for d = 128, whose staging area takes the second stage's room.
+template <int D, bool F8 = false>
+using ExtCfg = TcCfg<D, false, 2, (F8 && D == 128) ? 1 : 2 * (128 / D), 6, 128, 1, F8>;
 
 // Query tile pair (blockIdx.x, blockIdx.y) of the extend batch; false if empty.
 __device__ bool extend_tile_info(const TcArgs& a, int* info) {
@@ -76,11 +78,11 @@ __device__ bool extend_tile_info(const TcArgs& a, int* info) {
     return true;
 }
 
-template <int D>
-__global__ void __launch_bounds__(ExtCfg<D>::kThreads, 1)
+template <int D, bool F8>
+__global__ void __launch_bounds__(ExtCfg<D, F8>::kThreads, 1)
     extend_tc_kernel(const TcArgs a, const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                      const __grid_constant__ CUtensorMap tnk, const __grid_constant__ CUtensorMap tnv) {
-    using C = ExtCfg<D>;
+    using C = ExtCfg<D, F8>;
     using Lay = typename C::Lay;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -114,12 +116,15 @@ __global__ void __launch_bounds__(ExtCfg<D>::kThreads, 1)
     }
 }
 
-template <int D>
+template <int D, bool F8>
 constexpr int extend_smem() {
-    return ExtCfg<D>::Lay::END + 1024;   // + alignment slack
+    return ExtCfg<D, F8>::Lay::END + 1024;   // + alignment slack
 }
-static_assert(extend_smem<128>() <= 232448 && extend_smem<64>() <= 232448, "shared memory per CTA");
-static_assert(extend_smem<128>() > 116 * 1024 && extend_smem<64>() > 116 * 1024,
+static_assert(extend_smem<128, false>() <= 232448 && extend_smem<64, false>() <= 232448 &&
+                  extend_smem<128, true>() <= 232448 && extend_smem<64, true>() <= 232448,
+              "shared memory per CTA");
+static_assert(extend_smem<128, false>() > 116 * 1024 && extend_smem<64, false>() > 116 * 1024 &&
+                  extend_smem<128, true>() > 116 * 1024 && extend_smem<64, true>() > 116 * 1024,
               "one CTA per SM: each allocates all 512 TMEM columns");
 
 }  // namespace
@@ -181,16 +186,20 @@ int encode_pool_maps(const void* kp, const void* vp, int64_t num_slots, int Hkv,
 }  // namespace tc
 
 // Extend over all requests: grid (pairs of query tiles of 128/G new tokens, KV heads).
-template <int D>
+template <int D, bool F8>
 int launch_extend_tc(const void* q, const void* kp, const void* vp, const void* kn, const void* vn, void* kw, void* vw,
                      const int32_t* r2t, int64_t ld, const int32_t* pre, const int32_t* ext, int B, int64_t n_rows,
                      int64_t ctas, void* o, float* lse,
-                     uint32_t* err, int Hq, int Hkv, int64_t num_slots, float scale_log2, cudaStream_t s) {
-    static const int attr = (int)cudaFuncSetAttribute(extend_tc_kernel<D>,
-                                                      cudaFuncAttributeMaxDynamicSharedMemorySize, extend_smem<D>());
+                     uint32_t* err, int Hq, int Hkv, int64_t num_slots, float scale_log2, float k_scale, float v_scale,
+                     cudaStream_t s) {
+    static const int attr = (int)cudaFuncSetAttribute(extend_tc_kernel<D, F8>,
+                                                      cudaFuncAttributeMaxDynamicSharedMemorySize, extend_smem<D, F8>());
     if (attr) return attr;
-    CUtensorMap mk, mv, nk{}, nv{};
-    if (const int e = tc::encode_pool_maps(kp, vp, num_slots, Hkv, D, &mk, &mv)) return e;
+    // the pools' TMA views (an FP8 pool's codes are copied with cp.async:
+    // its maps stay zero and unused)
+    CUtensorMap mk{}, mv{}, nk{}, nv{};
+    if (!F8)
+        if (const int e = tc::encode_pool_maps(kp, vp, num_slots, Hkv, D, &mk, &mv)) return e;
     if (kn) {
         if (const int e = tc::encode_rows_map(kn, n_rows * Hkv, D, &nk)) return e;
         if (const int e = tc::encode_rows_map(vn, n_rows * Hkv, D, &nv)) return e;
@@ -217,15 +226,28 @@ int launch_extend_tc(const void* q, const void* kp, const void* vp, const void* 
     a.G = Hq / Hkv;
     a.num_slots = num_slots;
     a.scale_log2 = scale_log2;
-    extend_tc_kernel<D><<<dim3((unsigned)ctas, (unsigned)Hkv), ExtCfg<D>::kThreads, extend_smem<D>(), s>>>(a, mk, mv, nk, nv);
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    extend_tc_kernel<D, F8><<<dim3((unsigned)ctas, (unsigned)Hkv), ExtCfg<D, F8>::kThreads, extend_smem<D, F8>(), s>>>(
+        a, mk, mv, nk, nv);
     return (int)cudaGetLastError();
 }
 
-template int launch_extend_tc<64>(const void*, const void*, const void*, const void*, const void*, void*, void*,
-                                  const int32_t*, int64_t, const int32_t*, const int32_t*, int, int64_t, int64_t, void*,
-                                  float*, uint32_t*, int, int, int64_t, float, cudaStream_t);
-template int launch_extend_tc<128>(const void*, const void*, const void*, const void*, const void*, void*, void*,
-                                   const int32_t*, int64_t, const int32_t*, const int32_t*, int, int64_t, int64_t,
-                                   void*, float*, uint32_t*, int, int, int64_t, float, cudaStream_t);
+template int launch_extend_tc<64, false>(const void*, const void*, const void*, const void*, const void*, void*,
+                                         void*, const int32_t*, int64_t, const int32_t*, const int32_t*, int,
+                                         int64_t, int64_t, void*, float*, uint32_t*, int, int, int64_t, float,
+                                         float, float, cudaStream_t);
+template int launch_extend_tc<64, true>(const void*, const void*, const void*, const void*, const void*, void*,
+                                         void*, const int32_t*, int64_t, const int32_t*, const int32_t*, int,
+                                         int64_t, int64_t, void*, float*, uint32_t*, int, int, int64_t, float,
+                                         float, float, cudaStream_t);
+template int launch_extend_tc<128, false>(const void*, const void*, const void*, const void*, const void*, void*,
+                                         void*, const int32_t*, int64_t, const int32_t*, const int32_t*, int,
+                                         int64_t, int64_t, void*, float*, uint32_t*, int, int, int64_t, float,
+                                         float, float, cudaStream_t);
+template int launch_extend_tc<128, true>(const void*, const void*, const void*, const void*, const void*, void*,
+                                         void*, const int32_t*, int64_t, const int32_t*, const int32_t*, int,
+                                         int64_t, int64_t, void*, float*, uint32_t*, int, int, int64_t, float,
+                                         float, float, cudaStream_t);
 
 }  // namespace sgl

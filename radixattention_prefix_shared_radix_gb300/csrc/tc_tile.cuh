@@ -200,13 +200,12 @@ struct TcLayout {
 // q * 256 + NSB * BN; decode's Q after O.  P_j (bf16 pairs) overwrites the
 // first BN / 2 columns of its own S buffer.
 //
-// F8 (decode only): the pools hold FP8 E4M3 codes.  The gather team copies
+// F8: the pools hold FP8 E4M3 codes.  The gather team copies
 // them into a staging area with 16-byte cp.async and stores them, converted
 // to f16 (exact), into the same SW128 tiles; Q and P are f16 too, so the MMAs
 // are kind::f16 with f16 operands.
 template <int D, bool DEC, int NQ, int NS, int NG, int BN, int NSB, bool F8 = false>
 struct TcCfg {
-    static_assert(!F8 || DEC, "FP8 pools: decode tiles only");
     static_assert(NQ == 1 || (NQ == 2 && !DEC), "decode tiles use one query tile (Q lives in TMEM)");
     static_assert(BN == 64 || BN == 128, "KV block of 64 or 128 positions");
     static_assert(NSB == 1 || NSB == 2, "one or two score buffers");
@@ -370,7 +369,28 @@ __device__ __forceinline__ void tc_tile_run(const TcArgs& a, const CUtensorMap* 
                     cp_async16(sQ + q * Lay::QTILE + sw128(r, ch, kQRegion), src, ok);
                 }
             }
-            cp_async_arrive_noinc(bar(C::QFULL));
+            if constexpr (F8) {
+                // f16 operands against the f16 K tiles: each lane converts
+                // the Q chunks it copied, in place, once they have landed
+                cp_async_commit();
+                cp_async_wait<0>();
+#pragma unroll
+                for (int q = 0; q < NQ; ++q) {
+                    for (int t = g; t < QI; t += NG) {
+                        const uint32_t qa = sQ + q * Lay::QTILE + sw128(t * RPI + sub, ch, kQRegion);
+                        uint32_t w[4];
+                        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];\n"
+                                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                                     : "r"(qa));
+                        st_shared_v4(qa, bf16x2_to_f16x2(w[0]), bf16x2_to_f16x2(w[1]), bf16x2_to_f16x2(w[2]),
+                                     bf16x2_to_f16x2(w[3]));
+                    }
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(bar(C::QFULL));
+            } else {
+                cp_async_arrive_noinc(bar(C::QFULL));
+            }
         }
         int issued = 0;
         const int32_t* trow = a_r2t + (int64_t)kv_row * a_ld;
@@ -580,7 +600,7 @@ __device__ __forceinline__ void tc_tile_run(const TcArgs& a, const CUtensorMap* 
                 issued = j + 1;
             }
         }
-        if constexpr (!DEC) {
+        if constexpr (!DEC && !F8) {
             // Fused KV write (after the gathers are issued, so that it overlaps the
             // MMAs): this CTA's new tokens (its query tiles' rows / G)
             // for KV head kvh go from the new K/V into their pool slots.  No

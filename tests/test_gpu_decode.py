@@ -327,14 +327,63 @@ def test_decode_fp8_subnormal_codes(name):
         case.close()
 
 
-def test_fp8_kv_extend_is_unsupported():
-    w = W.get("extend_small")
-    p = sgl.make_params(sgl.SGL_DTYPE_BF16_FP8KV, 1, w.Hq, w.Hkv, w.d, 1024, 1, k_scale=1.0, v_scale=1.0,
-                        host_prefix_lens=np.array([0], dtype=np.int32), host_extend_lens=np.array([1], dtype=np.int32))
-    with pytest.raises(sgl.SglError):
-        sgl.sgl_extend_workspace_bytes(p)
+def _fp8_extend(case, ks, vs):
+    pre = case.out["prefix_lens"]
+    ext = case.out["seq_lens"] - pre
+    w = case.w
+    k8, v8 = W.quantize_e4m3(case.K.cuda(), ks), W.quantize_e4m3(case.V.cuda(), vs)
+    p = sgl.make_params(sgl.SGL_DTYPE_BF16_FP8KV, case.B, w.Hq, w.Hkv, w.d, case.S, w.page_size, k_scale=ks,
+                        v_scale=vs, host_prefix_lens=pre, host_extend_lens=ext)
+    ws = torch.zeros(sgl.sgl_extend_workspace_bytes(p), dtype=torch.uint8, device="cuda")
+    qd = case.q_host().cuda()
+    o = torch.empty_like(qd)
+    lse = torch.empty(qd.shape[0], w.Hq, dtype=torch.float32, device="cuda")
+    sgl.sgl_extend_attn(qd, k8, v8, torch.from_numpy(case.out["req_to_token"]).cuda(), torch.from_numpy(pre).cuda(),
+                        torch.from_numpy(ext).cuda(), p, o, lse, ws)
+    sgl.sgl_check(ws)
+    return o.double().cpu().numpy(), lse.cpu().numpy().astype(np.float64), k8.cpu(), v8.cpu(), pre, ext, p
+
+
+@pytest.mark.parametrize("name", ["extend_small", "extend"])
+def test_extend_fp8_kv(name):
+    """Extend (cached prefix + causal new block) over FP8 pools against the
+    oracle on the decoded values: every row at test size, sampled rows of
+    every request at the full size."""
+    from oracle.attention import extend_attention
+    from oracle.fp8 import DequantView
+    case = Case(name)
+    try:
+        ks, vs = 1.0 / 64, 1.0 / 48
+        O, L, k8, v8, pre, ext, p = _fp8_extend(case, ks, vs)
+        rows = None
+        if name == "extend":
+            starts = np.concatenate([[0], np.cumsum(ext)[:-1]])
+            rng = np.random.default_rng(2)
+            rows = []
+            for s0, e in zip(starts, ext):
+                rows += [int(s0), int(s0 + e - 1), int(s0 + 127), int(s0 + 128)] + [int(s0 + x) for x in
+                                                                                    rng.integers(0, e, 4)]
+            rows = sorted(set(rows))
+        Oref, Lref = extend_attention(case.oracle_q(), DequantView(k8, ks), DequantView(v8, vs), case.oracle_table,
+                                      pre, ext, rows=rows)
+        do, dl = assert_close(O, L, Oref, Lref, *tolerances(case.w), rows=rows)
+        print("%s fp8 extend: O max-abs %.3g, LSE max-abs %.3g" % (name, do, dl))
+    finally:
+        case.close()
+
+
+def test_fp8_kv_fused_kv_write_is_unsupported():
+    case = Case("extend_small")
+    try:
+        O, L, k8, v8, pre, ext, p = _fp8_extend(case, 1.0 / 64, 1.0 / 64)
         z = torch.zeros(16, dtype=torch.uint8, device="cuda")
-        sgl.sgl_extend_attn(z, z, z, torch.zeros((1, 1), dtype=torch.int32, device="cuda"),
-                            torch.zeros(1, dtype=torch.int32, device="cuda"),
-                            torch.ones(1, dtype=torch.int32, device="cuda"), p, z, torch.zeros(1, device="cuda"),
-                            torch.zeros(256, dtype=torch.uint8, device="cuda"))
+        with pytest.raises(sgl.SglError) as e:
+            sgl.sgl_extend_attn_kvwrite(z, z, z, k8.cuda(), v8.cuda(), torch.zeros((case.B, 1), dtype=torch.int32,
+                                                                                 device="cuda"),
+                                        torch.zeros(case.B, dtype=torch.int32, device="cuda"),
+                                        torch.ones(case.B, dtype=torch.int32, device="cuda"), p, z,
+                                        torch.zeros(1, device="cuda"), torch.zeros(256, dtype=torch.uint8,
+                                                                                  device="cuda"))
+        assert e.value.status == -3
+    finally:
+        case.close()
