@@ -81,6 +81,19 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+def job_timing(ms_local, bytes_per_rank, world, device):
+    """(max over the ranks of the timed region in ms, whole-job GB/s): every
+    rank processed bytes_per_rank in its timed region (independent replicas,
+    weak scaling).  `device` holds the reduction tensor (cuda under NCCL, cpu
+    under gloo)."""
+    import torch
+    ms_t = torch.tensor([float(ms_local)], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(ms_t, op=torch.distributed.ReduceOp.MAX)
+    ms_max = float(ms_t.item())
+    return ms_max, bytes_per_rank * world / (ms_max / 1e3) / 1e9
+
+
 def kv_bytes_per_token(w):
     return 2 * w.Hkv * w.d * (4 if w.dtype == "f32" else 2)
 
@@ -388,13 +401,9 @@ def run_native(args):
         torch.distributed.barrier()
     clocks.stop()
     ms = e0.elapsed_time(e1)
-    ms_t = torch.tensor([ms], dtype=torch.float64, device="cuda")
-    if world > 1:
-        torch.distributed.all_reduce(ms_t, op=torch.distributed.ReduceOp.MAX)
-    ms_max = float(ms_t.item())
+    ms_max, value = job_timing(ms, total_bytes, world, "cuda")
     for it in inst:
         sgl.sgl_check(it["ws"])
-    value = total_bytes * world / (ms_max / 1e3) / 1e9
     per_call_ms = ms / K
     achieved = (total_bytes / K) / (per_call_ms / 1e3) / 1e9
 
