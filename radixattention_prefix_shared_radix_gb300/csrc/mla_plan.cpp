@@ -7,13 +7,21 @@
 // and all their query heads: the work unit is 64 query rows (member x head)
 // of one segment chunk.  With Hq query heads a unit holds 64 / min(Hq, 64)
 // members and min(Hq, 64) heads ("head group"; Hq = 128 has two groups of 64
-// heads that read the same rows).  Chunks are cut so that about one unit per
-// SM exists (one CTA each, longest first); each writes normalised partial
-// rows that the log-sum-exp merge combines per (request, head group).
+// heads that read the same rows).  Chunks are cut by a cost model of the
+// kernel (measured on GB300: a 32-position block costs about 0.94 us +
+// 0.0394 us per query row of the item, so a 64-row block of a shared prefix
+// costs twice a 16-row block of a request's own suffix, and an item about
+// 1.5 us more to start); of the piece lengths tried, the planner keeps the
+// one whose list schedule (items most costly first, each to the SM that
+// frees first, as CTAs are dispatched) plus the traffic of its partial rows
+// ends earliest.  Each item writes normalised partial rows that the
+// log-sum-exp merge combines per (request, head group).
 #include <algorithm>
 #include <cmath>
 #include <cstring>
+#include <functional>
 #include <new>
+#include <queue>
 #include <vector>
 
 #include "common.h"
@@ -22,6 +30,13 @@ namespace {
 
 constexpr int32_t kMlaRows = 64;    // query rows of one work item
 constexpr int32_t kMlaBlock = 32;   // positions per block of the kernel
+
+// estimated microseconds of one 32-position block for an item of `rows` query rows
+double block_cost(int32_t rows) { return 0.94 + 0.0394 * rows; }
+constexpr double kItemCost = 1.5;   // estimated start cost of one item (us)
+// a partial row (512 fp32) is written by the kernel and read by the merge:
+// 4 KB at about 6 TB/s
+constexpr double kRowCost = 4096.0 / 6.0e6;
 
 }  // namespace
 
@@ -45,30 +60,99 @@ extern "C" int sgl_mla_decode_plan(const sgl_mla_params* p, const int32_t* seq_l
     const int32_t nseg = g->num_segments;
     const int sms = sgl::query_num_sms(p->num_sms);
 
-    // chunk length: about one item per SM (an item reloads its 72 KB of
-    // query rows, so items are kept long), whole 32-position blocks
-    int64_t work = 0;
+    // Chunks: each (segment, member block, head group) unit is cut into
+    // pieces of about T microseconds (whole blocks, at least two); T is
+    // chosen among multiples of the mean work per SM by the end time of the
+    // list schedule of the resulting items.
+    struct Unit {
+        int32_t s, mb, nm, hg;
+        int64_t len;
+        double per_block;
+    };
+    std::vector<Unit> units;
+    double total = 0.0;
     for (int32_t s = 0; s < nseg; ++s) {
         const int32_t nmem = g->seg_member_ptr[s + 1] - g->seg_member_ptr[s];
-        work += (int64_t)(g->seg_end[s] - g->seg_begin[s]) * ((nmem + MB - 1) / MB) * Hg;
-    }
-    int64_t C = (work + sms - 1) / std::max<int64_t>(1, sms);
-    C = std::min<int64_t>(4096, std::max<int64_t>(64, (C + kMlaBlock - 1) / kMlaBlock * kMlaBlock));
-
-    std::vector<sgl::DecItem> items;
-    for (int32_t s = 0; s < nseg; ++s) {
-        const int32_t b = g->seg_begin[s], e = g->seg_end[s];
-        const int32_t m0 = g->seg_member_ptr[s], nmem = g->seg_member_ptr[s + 1] - m0;
+        const int64_t len = g->seg_end[s] - g->seg_begin[s];
         for (int32_t mb = 0; mb < nmem; mb += MB)
-            for (int32_t hg = 0; hg < Hg; ++hg)
-                for (int64_t cb = b; cb < e; cb += C) {
-                    const int32_t ce = (int32_t)std::min<int64_t>(e, cb + C);
-                    items.push_back({g->seg_row[s], (int32_t)cb, ce, hg, m0 + mb, std::min(MB, nmem - mb), 0, 0});
-                }
+            for (int32_t hg = 0; hg < Hg; ++hg) {
+                const int32_t nm = std::min(MB, nmem - mb);
+                const double pb = block_cost(nm * Gp);
+                units.push_back({s, mb, nm, hg, len, pb});
+                total += pb * (double)((len + kMlaBlock - 1) / kMlaBlock);
+            }
     }
-    std::stable_sort(items.begin(), items.end(), [](const sgl::DecItem& x, const sgl::DecItem& y) {
-        return (x.kv_end - x.kv_begin) > (y.kv_end - y.kv_begin);
-    });
+    auto pieces_of = [&](const Unit& u, double T) {   // blocks per piece, pieces
+        const int64_t blocks = (u.len + kMlaBlock - 1) / kMlaBlock;
+        const int64_t per = std::max<int64_t>(2, (int64_t)(T / u.per_block));
+        const int64_t n = std::max<int64_t>(1, (blocks + per - 1) / per);
+        return std::make_pair((blocks + n - 1) / n, n);
+    };
+    auto piece_costs = [&](double T, std::vector<double>& out) {
+        out.clear();
+        int64_t rows = 0;
+        for (const Unit& u : units) {
+            const auto pc = pieces_of(u, T);
+            const int64_t blocks = (u.len + kMlaBlock - 1) / kMlaBlock;
+            for (int64_t k = 0; k < pc.second; ++k) {
+                const int64_t nb = std::min(pc.first, blocks - k * pc.first);
+                if (nb > 0) {
+                    out.push_back(kItemCost + u.per_block * (double)nb);
+                    rows += (int64_t)u.nm * Gp;
+                }
+            }
+        }
+        std::sort(out.begin(), out.end(), std::greater<double>());
+        return kRowCost * (double)rows;
+    };
+    auto makespan = [&](const std::vector<double>& c) {
+        std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
+        const size_t n_sm = std::min<size_t>((size_t)std::max(1, sms), std::max<size_t>(1, c.size()));
+        for (size_t i = 0; i < n_sm; ++i) free_at.push(0.0);
+        double end = 0.0;
+        for (double x : c) {
+            const double t = free_at.top() + x;
+            free_at.pop();
+            free_at.push(t);
+            end = std::max(end, t);
+        }
+        return end;
+    };
+    const double mean = total / std::max(1, sms);
+    double T = mean, best = INFINITY;
+    size_t best_n = 0;
+    std::vector<double> costs;
+    for (int k = 0; k <= 64 && !units.empty(); ++k) {
+        const double t = mean * (0.25 + 0.03 * k);
+        const double merge = piece_costs(t, costs);
+        const double m = makespan(costs) + merge;
+        if (m < best * (1.0 - 1e-9) || (m <= best * (1.0 + 1e-9) && costs.size() < best_n)) {
+            best = m;
+            best_n = costs.size();
+            T = t;
+        }
+    }
+    struct Piece {
+        sgl::DecItem item;
+        double cost;
+    };
+    std::vector<Piece> pieces;
+    int64_t C = 0;   // longest piece (reported as the chunk length)
+    for (const Unit& u : units) {
+        const auto pc = pieces_of(u, T);
+        const int64_t plen = pc.first * kMlaBlock;
+        C = std::max(C, plen);
+        const int32_t b = g->seg_begin[u.s], e = g->seg_end[u.s];
+        for (int64_t cb = b; cb < e; cb += plen) {
+            const int32_t ce = (int32_t)std::min<int64_t>(e, cb + plen);
+            const double cost = kItemCost + u.per_block * (double)((ce - cb + kMlaBlock - 1) / kMlaBlock);
+            pieces.push_back({{g->seg_row[u.s], (int32_t)cb, ce, u.hg, g->seg_member_ptr[u.s] + u.mb, u.nm, 0, 0}, cost});
+        }
+    }
+    std::stable_sort(pieces.begin(), pieces.end(), [](const Piece& x, const Piece& y) { return x.cost > y.cost; });
+    std::vector<sgl::DecItem> items;
+    items.reserve(pieces.size());
+    for (const Piece& pc : pieces) items.push_back(pc.item);
     // partial rows in item order: member i of the item, head j of its group
     // at partial_base + i * Gp + j; merge lists per (request, head group)
     std::vector<std::vector<int32_t>> ents((size_t)B * Hg);
