@@ -20,7 +20,7 @@ Sources (page title, section):
     of the pieces before it) -- the basis of ``extend_attention_kvwrite``
     called chunk by chunk.
 
-Definitions (plain softmax attention; readings listed in the design doc):
+Definitions (plain softmax attention, with the readings taken):
   s_j  = sm_scale * <q[r, h], K[slot(r, j), h // G]>,  j < seq_len[r]
   LSE  = m + ln sum_j exp(s_j - m),  m = max_j s_j       (natural log)
   O    = sum_j exp(s_j - LSE) * V[slot(r, j), h // G]

@@ -12,7 +12,7 @@ token one 512-dimensional latent vector plus a 64-dimensional position part,
 1,152 bytes per token and layer in bf16, and has a single KV "head" that all
 query heads read).
 
-Definitions (readings listed in the design doc): per token the pool holds ONE
+Definitions (with the readings taken): per token the pool holds ONE
 row ``c`` of ``d = 576`` elements (latent first, then the position part).
 For request r and query head h (every head reads the same row):
   s_j  = sm_scale * <q[r, h], c[slot(r, j)]>           (all 576 elements)

@@ -17,7 +17,7 @@ Sources (page title, section):
     completes (inserting only at request end loses sharing between running
     requests).
 
-Readings (listed in the design doc): rounds are discrete; a request is admitted
+Readings: rounds are discrete; a request is admitted
 only if slots for its uncached prompt and its whole output can be allocated
 (evicting LRU leaves), and the first allocation failure ends admission for
 the round; the deferral rule compares the next min(defer_tokens, uncached)

@@ -21,7 +21,7 @@ Sources (page title, section):
     section "1. RadixCache": per-token trie with ``children[token]``,
     ``prefix_match`` returning (matched length, last node), and ``insert``.
 
-Readings taken where the pages are silent (each is listed in the design doc):
+Readings taken where the pages are silent:
   * Structure: one trie node per PAGE (a tuple of ``page_size`` token ids);
     for page_size == 1 this is the pages' per-token trie.  Matching and
     sharing happen in whole pages; a partially filled tail page is never
