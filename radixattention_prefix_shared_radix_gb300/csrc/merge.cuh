@@ -35,9 +35,10 @@ struct MergeArgs {
 };
 
 // Head j of pair idx = (request, KV head), whose entries are
-// ment[e0 .. e0+E): entry e's row for head j is ment[e0 + e] + j.
+// ment[e0 .. e0+E): entry e's row for head j is ment[e0 + e] + j.  `first`
+// is ment[e0 + lane] for lane < min(E, 32), already loaded by the caller.
 template <typename OutT, int D>
-__device__ __noinline__ void merge_head(const MergeArgs& m, int idx, int j, int e0, int E, int lane) {
+__device__ __noinline__ void merge_head(const MergeArgs& m, int idx, int j, int e0, int E, int lane, int first) {
     constexpr int VPL = D / 32;             // columns per lane
     constexpr int U = VPL > 4 ? 4 : 16;     // entries whose rows are in flight together
     static_assert(VPL == 2 || VPL % 4 == 0, "columns per lane");
@@ -47,7 +48,7 @@ __device__ __noinline__ void merge_head(const MergeArgs& m, int idx, int j, int 
     for (int v = 0; v < VPL; ++v) acc[v] = 0.f;
     for (int b = 0; b < E; b += 32) {
         const int n = min(32, E - b);
-        const int prow = lane < n ? __ldg(m.ment + e0 + b + lane) + j : 0;
+        const int prow = lane < n ? (b == 0 ? first : __ldg(m.ment + e0 + b + lane)) + j : 0;
         const float ls = lane < n ? __ldcg(m.plse + prow) : -INFINITY;
         for (int k = 0; k < n; k += U) {
             float x[U][VPL], lu[U];
@@ -120,16 +121,23 @@ __device__ __noinline__ void merge_head(const MergeArgs& m, int idx, int j, int 
 
 // One warp per (request, KV head, query head of the group): the log-sum-exp
 // merge of its entries, or O = 0 / LSE = -inf when the pair has no entries
-// (seq_len 0).  A warp's loads are one round trip for the entry range, one
-// for the entry rows, then the partial rows and LSEs together.
+// (seq_len 0).  The entry range and the first 32 entry rows are plan tables
+// (uploaded from the host before the launch before), so they are read while
+// the launch before is still running; only the partial rows and LSEs, which
+// it writes, are read after the dependency wait.
 template <typename OutT, int D>
 __global__ void __launch_bounds__(128) decode_merge_kernel(const MergeArgs m, int n_pairs) {
-    grid_dep_wait();     // the partials of the launch before
-    grid_dep_launch();
     const int w = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     const int idx = w / m.G, j = w - idx * m.G;
+    int e0 = 0, E = 0, first = 0;
+    if (idx < n_pairs) {
+        e0 = __ldg(m.mptr + idx);
+        E = __ldg(m.mptr + idx + 1) - e0;
+        if (lane < E) first = __ldg(m.ment + e0 + lane);
+    }
+    grid_dep_wait();     // the partials of the launch before
+    grid_dep_launch();
     if (idx >= n_pairs) return;
-    const int e0 = __ldg(m.mptr + idx), E = __ldg(m.mptr + idx + 1) - e0;
     if (E == 0) {
         const int r = idx / m.Hkv, h = idx - r * m.Hkv;
         const int64_t orow = (int64_t)r * m.Hq + h * m.G + j;
@@ -138,7 +146,7 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const MergeArgs m, in
         if (lane == 0) m.lse[orow] = -INFINITY;
         return;
     }
-    merge_head<OutT, D>(m, idx, j, e0, E, lane);
+    merge_head<OutT, D>(m, idx, j, e0, E, lane, first);
 }
 
 }  // namespace sgl
