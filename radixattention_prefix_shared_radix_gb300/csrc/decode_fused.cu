@@ -686,11 +686,11 @@ __global__ void __maxnreg__(128) decode_fused_kernel(const __grid_constant__ Fus
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // launched as a programmatic dependent of the previous kernel in the
-    // stream: everything before its completion is visible after this wait;
-    // the merge launch may be scheduled from now on (it waits for this grid)
-    grid_dep_wait();
-    grid_dep_launch();
+    // Launched as a programmatic dependent of the previous kernel in the
+    // stream.  Until the dependency wait below, the CTA touches only shared
+    // memory, TMEM and the plan tables (uploaded from the host before the
+    // previous kernel, never written by a kernel), so the set-up overlaps
+    // that kernel's tail.
     const int w0 = __ldg(f.wptr + blockIdx.x), w1 = __ldg(f.wptr + blockIdx.x + 1);
     const bool tiles = w1 > w0;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + TL::OFF_TMEM);
@@ -718,6 +718,16 @@ __global__ void __maxnreg__(128) decode_fused_kernel(const __grid_constant__ Fus
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // the first records this CTA reads (plan tables) into L1 while waiting
+    if (tiles && tid == 0) prefetch_l1(f.t.items + w0);
+    if (!tiles && warp >= kFirstProducer && warp < kFirstConsumer && lane == 0) {
+        const int gw = ((int)blockIdx.x - f.n_tile_ctas) * kConsumers + (warp - kFirstProducer);
+        if (gw >= 0 && gw < f.n_init) prefetch_l1(f.narrow + gw);
+    }
+    // everything the previous kernel wrote is visible after this wait; the
+    // merge launch may be scheduled from now on (it waits for this grid)
+    grid_dep_wait();
+    grid_dep_launch();
 
     constexpr int kStreamGate = 3;   // named barrier: tile roles done -> streaming may start
     constexpr int kTileWarps = TC::kThreads / 32;   // softmax, MMA, gather team (incl. the producers)

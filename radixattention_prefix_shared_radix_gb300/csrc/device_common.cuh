@@ -33,6 +33,8 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool v
 // (they wait in turn before touching memory).
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 __device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+// fetch the line holding `p` (a valid global address) into L1
+__device__ __forceinline__ void prefetch_l1(const void* p) { asm volatile("prefetch.global.L1 [%0];\n" ::"l"(p)); }
 
 // An L2 policy that evicts the lines it tags first: for data read exactly
 // once, so that it does not push the kernels' code and tables out of L2.

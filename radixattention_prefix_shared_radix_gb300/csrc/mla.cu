@@ -95,10 +95,12 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const __grid_co
     float* lss = reinterpret_cast<float*>(sm + MlaLayout::OFF_LS);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int rg = warp >> 2, wq = warp & 3, g = lane >> 2, t = lane & 3;
+    // the work item is a plan table (uploaded from the host, never written by
+    // a kernel): its load overlaps the previous kernel's tail; everything the
+    // previous kernel wrote is visible after the dependency wait
+    const DecItem it = a.items[blockIdx.x];
     grid_dep_wait();
     grid_dep_launch();
-
-    const DecItem it = a.items[blockIdx.x];
     const int len = __ldg(a.seq_lens + it.rep_row);
     int e = it.kv_end;
     if (e > len) {
