@@ -267,7 +267,10 @@ int sgl_plan_info(const sgl_plan* plan, sgl_plan_info_t* out);
 /* Copy the plan's device tables into the head of the workspace
  * (device, >= workspace_bytes, 256-byte aligned) on `stream`, and clear its
  * error word.  Needed once after each sgl_decode_plan before decode calls
- * that use the plan; the plan must stay alive until the copy has run. */
+ * that use the plan; the plan must stay alive until the copy has run.
+ * The attention kernels read these tables before their programmatic
+ * dependency wait (while the previous kernel in the stream may still run),
+ * so nothing but this call may write the table region of the workspace. */
 int sgl_plan_upload(const sgl_plan* plan, void* workspace, size_t ws_bytes, sgl_stream_t stream);
 
 /* Decode attention for B requests, one query token each.
