@@ -2,7 +2,9 @@
 invariants, rejected shapes and plan kinds."""
 
 import ctypes
+import time
 
+import numpy as np
 import pytest
 
 import radixattention_prefix_shared_radix_gb300 as sgl
@@ -70,3 +72,53 @@ def test_plan_kinds_are_not_interchangeable(case):
         assert st == -1
     finally:
         gqa_case.close()
+
+
+def test_cost_model_plan_is_deterministic_and_bounded():
+    """The piece length is chosen by simulating the schedule: the same
+    inputs give the same plan, the item count stays within a few waves
+    (partial rows cost merge traffic), and the longest piece is whole
+    32-position blocks."""
+    w = W.get("mla_decode")
+    b = W.make_batch(w, 0)
+    seqs = b.all_tokens()
+    S = 1 << 20
+    tree = sgl.sgl_tree_create(S, w.page_size, np.arange(S, dtype=np.int32))
+    groups = sgl.sgl_groups_create()
+    try:
+        out = sgl.sgl_build_batch(tree, seqs, groups=groups)
+        infos = []
+        for sms in (152, 152, 132, 16):
+            p = sgl.make_mla_params(len(seqs), w.Hq, S, num_sms=sms)
+            infos.append((sms, sgl.sgl_plan_info(sgl.sgl_mla_decode_plan(p, out["seq_lens"],
+                                                                          sgl.sgl_groups_view(groups)))))
+        assert infos[0][1] == infos[1][1]
+        for sms, info in infos:
+            assert info["chunk_tokens"] % 32 == 0 and info["chunk_tokens"] >= 64
+            assert sms // 2 <= info["num_items"] <= 3 * sms + 80, (sms, info)
+    finally:
+        sgl.sgl_groups_destroy(groups)
+        sgl.sgl_tree_destroy(tree)
+
+
+def test_huge_sm_count_and_one_token_segments(case):
+    w = case.w
+    t0 = time.perf_counter()
+    info = sgl.sgl_plan_info(_plan(case, num_sms=1 << 20))
+    assert time.perf_counter() - t0 < 5.0
+    assert info["num_items"] > 0
+    # every request one token long, no sharing: one item per (member block, head group)
+    seqs = [[int(t)] for t in range(7)]
+    S = 1 << 12
+    tree = sgl.sgl_tree_create(S, 1, np.arange(S, dtype=np.int32))
+    groups = sgl.sgl_groups_create()
+    try:
+        out = sgl.sgl_build_batch(tree, seqs, groups=groups)
+        p = sgl.make_mla_params(len(seqs), w.Hq, S, num_sms=152)
+        info = sgl.sgl_plan_info(sgl.sgl_mla_decode_plan(p, out["seq_lens"], sgl.sgl_groups_view(groups)))
+        Hg = max(1, w.Hq // 64)
+        assert info["num_items"] == len(seqs) * Hg
+        assert info["num_merge_entries"] == len(seqs) * Hg
+    finally:
+        sgl.sgl_groups_destroy(groups)
+        sgl.sgl_tree_destroy(tree)
