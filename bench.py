@@ -292,6 +292,8 @@ def e2e_decode(sgl, W, torch, w, tree, kd, vd, inst, steps, num_sms=0):
                            seq=torch.empty(B, dtype=torch.int32).pin_memory(),
                            o=torch.empty_like(it["o"], device="cpu").pin_memory(),
                            lse=torch.empty_like(it["lse"], device="cpu").pin_memory()))
+        pinned[-1]["table_np"] = pinned[-1]["table"].numpy()
+        pinned[-1]["seq_np"] = pinned[-1]["seq"].numpy()
     h2d = d2h = 0
     total_b = 0
     stream = torch.cuda.current_stream()
@@ -299,12 +301,13 @@ def e2e_decode(sgl, W, torch, w, tree, kd, vd, inst, steps, num_sms=0):
     t0 = time.perf_counter()
     for s in range(steps):
         it, pb = inst[s % len(inst)], pinned[s % len(inst)]
-        out = sgl.sgl_build_batch(tree, it["seqs"], ld=it["table"].shape[1], groups=it["groups"])
+        # the slot table and lengths are written straight into the pinned
+        # staging buffers that the host->device copies read
+        out = sgl.sgl_build_batch(tree, it["seqs"], groups=it["groups"], req_to_token=pb["table_np"],
+                                  seq_lens=pb["seq_np"])
         view = sgl.sgl_groups_view(it["groups"])
         p = sgl.make_params(sgl.SGL_DTYPE_BF16, it["B"], w.Hq, w.Hkv, w.d, S, w.page_size, num_sms=num_sms)
         plan = sgl.sgl_decode_plan(p, out["seq_lens"], view)
-        pb["table"].numpy()[:] = out["req_to_token"]
-        pb["seq"].numpy()[:] = out["seq_lens"]
         sgl.sgl_plan_upload(plan, it["ws"])
         it["table"].copy_(pb["table"], non_blocking=True)
         it["seq"].copy_(pb["seq"], non_blocking=True)

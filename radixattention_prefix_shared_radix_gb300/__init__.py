@@ -282,15 +282,33 @@ def sgl_sim_run(tree, requests, policy=SGL_SCHED_LPM, insert_at=SGL_INSERT_AT_PR
     return per, {k: getattr(st, k) for k, _ in SglSimStats._fields_}
 
 
-def sgl_build_batch(tree, token_lists, ld=None, groups=None):
-    """Returns dict(req_to_token [B, ld] int32, seq_lens, prefix_lens, last_nodes) (numpy)."""
+def _out_i32(a, shape, name):
+    """A caller's output array (int32, C-contiguous, of `shape`), or a new one."""
+    if a is None:
+        return np.empty(shape, dtype=np.int32)
+    if not (isinstance(a, np.ndarray) and a.dtype == np.int32 and a.flags.c_contiguous and a.flags.writeable
+            and a.shape == tuple(shape)):
+        raise ValueError("%s must be a writeable C-contiguous int32 array of shape %s" % (name, tuple(shape)))
+    return a
+
+
+def sgl_build_batch(tree, token_lists, ld=None, groups=None, req_to_token=None, seq_lens=None):
+    """Returns dict(req_to_token [B, ld] int32, seq_lens, prefix_lens, last_nodes) (numpy).
+
+    `req_to_token` ([B, ld] int32, C-contiguous) and `seq_lens` ([B] int32)
+    may be given to be written in place (e.g. pinned staging buffers that are
+    copied to the device next); they are the arrays returned."""
     toks = [t if (isinstance(t, np.ndarray) and t.dtype == np.int32 and t.ndim == 1 and t.flags.c_contiguous)
             else _i32(t) for t in token_lists]
     B = len(toks)
     lens = np.fromiter((t.shape[0] for t in toks), dtype=np.int64, count=B)
+    if req_to_token is not None:
+        if ld is not None and int(ld) != req_to_token.shape[-1]:
+            raise ValueError("ld disagrees with req_to_token")
+        ld = req_to_token.shape[-1]
     ld = int(ld if ld is not None else max(1, int(lens.max()) if B else 1))
-    table = np.empty((B, ld), dtype=np.int32)   # every entry is written (-1 past a row's length)
-    seq = np.zeros(B, dtype=np.int32)
+    table = _out_i32(req_to_token, (B, ld), "req_to_token")   # every entry is written (-1 past a row's length)
+    seq = _out_i32(seq_lens, (B,), "seq_lens")
     pre = np.zeros(B, dtype=np.int32)
     last = np.zeros(B, dtype=np.int64)
     # the rows back to back in one array and their addresses computed in

@@ -125,7 +125,10 @@ struct sgl_tree {
         int64_t lim = std::min<int64_t>((int64_t)c->tokens.size(), avail);
         const int32_t* a = c->tokens.data();
         int64_t k = 0;
-        // whole blocks of 8 tokens first, then token by token
+        // whole blocks of 256 tokens, then of 8 tokens, then token by token:
+        // each level only advances over equal ranges, so k ends at the first
+        // mismatch (or lim) as a token-by-token walk would
+        while (k + 256 <= lim && std::memcmp(a + k, toks + k, 256 * sizeof(int32_t)) == 0) k += 256;
         while (k + 8 <= lim && std::memcmp(a + k, toks + k, 8 * sizeof(int32_t)) == 0) k += 8;
         while (k < lim && a[k] == toks[k]) ++k;
         return k / P * P;

@@ -234,3 +234,39 @@ def test_finish_batch_equals_finishing_one_by_one(P):
     finally:
         for t in trees:
             sgl.sgl_tree_destroy(t)
+
+
+def test_build_batch_writes_caller_buffers_in_place():
+    """Given output arrays, sgl_build_batch writes the same table and lengths
+    into them (and returns them) as into arrays of its own; arrays of the
+    wrong type, shape or layout are refused before the tree is touched."""
+    import numpy as np
+    import radixattention_prefix_shared_radix_gb300 as sgl
+    import workloads as W
+    w = W.get("llama3_8b_decode_small")
+    seqs = W.make_batch(w, 0).all_tokens()
+    S = 1 << 14
+    ld = max(len(x) for x in seqs) + 3
+    trees = [sgl.sgl_tree_create(S, 1, np.arange(S, dtype=np.int32)) for _ in range(2)]
+    try:
+        for step in range(2):
+            a = sgl.sgl_build_batch(trees[0], seqs, ld=ld)
+            tab = np.full((len(seqs), ld), 7, dtype=np.int32)
+            seq = np.full(len(seqs), 7, dtype=np.int32)
+            b = sgl.sgl_build_batch(trees[1], seqs, req_to_token=tab, seq_lens=seq)
+            assert b["req_to_token"] is tab and b["seq_lens"] is seq
+            for k in ("req_to_token", "seq_lens", "prefix_lens"):
+                np.testing.assert_array_equal(a[k], b[k])
+            sgl.sgl_tree_finish_batch(trees[0], a)
+            sgl.sgl_tree_finish_batch(trees[1], b)
+        bad = [dict(req_to_token=np.zeros((len(seqs), ld), dtype=np.int64)),
+               dict(req_to_token=np.zeros((len(seqs), ld + 1), dtype=np.int32)[:, :ld]),
+               dict(req_to_token=np.zeros((len(seqs) + 1, ld), dtype=np.int32)),
+               dict(req_to_token=np.zeros((len(seqs), ld), dtype=np.int32), ld=ld + 1),
+               dict(seq_lens=np.zeros(len(seqs) + 1, dtype=np.int32))]
+        for kw in bad:
+            with pytest.raises(ValueError):
+                sgl.sgl_build_batch(trees[1], seqs, **kw)
+    finally:
+        for t in trees:
+            sgl.sgl_tree_destroy(t)
