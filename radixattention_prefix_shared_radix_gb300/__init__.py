@@ -292,16 +292,32 @@ def _out_i32(a, shape, name):
     return a
 
 
-def sgl_build_batch(tree, token_lists, ld=None, groups=None, req_to_token=None, seq_lens=None):
+def sgl_build_batch(tree, token_lists, ld=None, groups=None, req_to_token=None, seq_lens=None, lens=None):
     """Returns dict(req_to_token [B, ld] int32, seq_lens, prefix_lens, last_nodes) (numpy).
+
+    `token_lists` is a sequence of 1-D token arrays, or a [B, cap] int32
+    C-contiguous matrix whose row r holds request r's `lens[r]` tokens
+    first (a serving loop can append each step's token in place and pass
+    the matrix with no per-step copy).
 
     `req_to_token` ([B, ld] int32, C-contiguous) and `seq_lens` ([B] int32)
     may be given to be written in place (e.g. pinned staging buffers that are
     copied to the device next); they are the arrays returned."""
-    toks = [t if (isinstance(t, np.ndarray) and t.dtype == np.int32 and t.ndim == 1 and t.flags.c_contiguous)
-            else _i32(t) for t in token_lists]
-    B = len(toks)
-    lens = np.fromiter((t.shape[0] for t in toks), dtype=np.int64, count=B)
+    mat = isinstance(token_lists, np.ndarray) and token_lists.ndim == 2
+    if mat:
+        if token_lists.dtype != np.int32 or not token_lists.flags.c_contiguous:
+            raise ValueError("a token matrix must be C-contiguous int32")
+        B, cap = token_lists.shape
+        lens = np.full(B, cap, dtype=np.int64) if lens is None else np.asarray(lens, dtype=np.int64).copy()
+        if lens.shape != (B,) or (B and (lens.min() < 0 or lens.max() > cap)):
+            raise ValueError("lens must give B lengths in [0, cap]")
+    else:
+        if lens is not None:
+            raise ValueError("lens is given with a token matrix only")
+        toks = [t if (isinstance(t, np.ndarray) and t.dtype == np.int32 and t.ndim == 1 and t.flags.c_contiguous)
+                else _i32(t) for t in token_lists]
+        B = len(toks)
+        lens = np.fromiter((t.shape[0] for t in toks), dtype=np.int64, count=B)
     if req_to_token is not None:
         if ld is not None and int(ld) != req_to_token.shape[-1]:
             raise ValueError("ld disagrees with req_to_token")
@@ -314,7 +330,10 @@ def sgl_build_batch(tree, token_lists, ld=None, groups=None, req_to_token=None, 
     # the rows back to back in one array and their addresses computed in
     # one step (per-row ctypes or array-interface lookups cost more than
     # the copy)
-    if B:
+    if mat and B:
+        flat = token_lists
+        ptrs = np.arange(B, dtype=np.uint64) * np.uint64(4 * token_lists.shape[1]) + np.uint64(flat.ctypes.data)
+    elif B:
         flat = np.concatenate(toks) if B > 1 else toks[0]
         offs = np.zeros(B, dtype=np.uint64)
         np.cumsum(lens[:-1], out=offs[1:])

@@ -270,3 +270,39 @@ def test_build_batch_writes_caller_buffers_in_place():
     finally:
         for t in trees:
             sgl.sgl_tree_destroy(t)
+
+
+def test_build_batch_from_token_matrix():
+    """A [B, cap] token matrix with per-row lengths gives the same tables as
+    the list of rows; bad matrices or lengths are refused."""
+    import numpy as np
+    import radixattention_prefix_shared_radix_gb300 as sgl
+    import workloads as W
+    w = W.get("fork_tree_small")
+    seqs = W.make_batch(w, 0).all_tokens()
+    B, cap = len(seqs), max(len(x) for x in seqs) + 5
+    mat = np.full((B, cap), 12345, dtype=np.int32)
+    for r, x in enumerate(seqs):
+        mat[r, :len(x)] = x
+    lens = [len(x) for x in seqs]
+    S = 1 << 13
+    trees = [sgl.sgl_tree_create(S, 1, np.arange(S, dtype=np.int32)) for _ in range(2)]
+    try:
+        a = sgl.sgl_build_batch(trees[0], seqs, ld=cap)
+        b = sgl.sgl_build_batch(trees[1], mat, lens=lens, ld=cap)
+        for k in ("req_to_token", "seq_lens", "prefix_lens"):
+            np.testing.assert_array_equal(a[k], b[k])
+        sgl.sgl_tree_finish_batch(trees[0], a)
+        sgl.sgl_tree_finish_batch(trees[1], b)
+        # without lens every row is cap tokens long
+        full = sgl.sgl_build_batch(trees[1], mat[:2].copy())
+        assert list(full["seq_lens"]) == [cap, cap]
+        sgl.sgl_tree_finish_batch(trees[1], full)
+        for args, kw in [((mat.astype(np.int64),), dict(lens=lens)), ((mat[:, ::2],), dict(lens=lens)),
+                         ((mat,), dict(lens=lens[:-1])), ((mat,), dict(lens=[cap + 1] * B)),
+                         ((seqs,), dict(lens=lens))]:
+            with pytest.raises(ValueError):
+                sgl.sgl_build_batch(trees[1], *args, **kw)
+    finally:
+        for t in trees:
+            sgl.sgl_tree_destroy(t)
