@@ -89,15 +89,19 @@ def decode_attention(q, k_pool, v_pool, req_to_token, seq_lens, sm_scale=None, r
     return O, LSE
 
 
-def lse_merge(parts):
+def lse_merge(parts, d=None):
     """Merge partial results [(O_i, LSE_i)] of disjoint key sets into one.
 
     M = max_i LSE_i;  w_i = exp(LSE_i - M);  O = sum w_i O_i / sum w_i;
-    LSE = M + ln sum w_i.  All-empty input gives (0, -inf).
+    LSE = M + ln sum w_i.  No parts, or only empty ones (LSE -inf), give
+    (0, -inf); with no parts at all the zero vector has length ``d`` (0 if
+    not given).
     """
+    if len(parts) == 0:
+        return np.zeros(0 if d is None else d), -math.inf
     lses = np.array([p[1] for p in parts], dtype=np.float64)
     d = len(parts[0][0])
-    if len(parts) == 0 or np.all(np.isneginf(lses)):
+    if np.all(np.isneginf(lses)):
         return np.zeros(d), -math.inf
     M = lses.max()
     w = np.exp(lses - M)

@@ -2,30 +2,47 @@
 
 Test infrastructure only (see ``oracle/__init__``).
 
-Sources (page title, section):
-  * "SGLang：从前端 DSL 到 SRT 服务运行时" (oripoin.cn/posts/sglang-runtime),
-    section "用基数树实现前缀复用": cache-aware scheduling serves the waiting
-    request with the longest shared (cached) prefix first, approximating a
-    depth-first walk of the tree; leaf-first LRU eviction; reference counts
-    keep running requests' nodes.
-  * The CS349D lecture-16 notes (semidirectx.com), §3.1-3.3: a runtime with
-    continuous batching (each request past prefill decodes one token per
-    round), a per-round budget of prompt tokens (chunked prefill), FCFS or
-    longest-prefix-first queueing in which a request whose uncached prefix
-    largely coincides with one admitted in the same round waits for the next
-    round, and insertion of the prompt into the tree when its prefill
-    completes (inserting only at request end loses sharing between running
-    requests).
+What the pages fix, and where:
+  * Queue order.  "SGLang：从前端 DSL 到 SRT 服务运行时" (oripoin.cn), section
+    "用基数树实现前缀复用", fourth bullet: the cache-aware scheduler picks the
+    waiting request whose shared (cached) prefix is longest, which walks the
+    tree roughly depth first; the paper's Theorem 3.1 makes that order
+    optimal for the hit rate when the cache holds at most one longest
+    request.  The CS349D lecture-16 notes (semidirectx.com) §3, fourth bullet
+    of the mini-runtime list: the policy is FCFS or longest-prefix-first.
+  * Deferral.  Same bullet of the notes: under longest-prefix-first, a
+    request whose not-yet-cached prefix largely coincides with a request
+    admitted in the same round waits for the next round.
+  * Rounds.  Notes §3, second and third bullets: continuous batching (every
+    request whose prefill is done decodes one token per round) and chunked
+    prefill (what is left of a per-round budget of prompt tokens goes to the
+    requests still in prefill).
+  * Insertion time.  Notes §3.1, "一个相互作用的例子": the prompt enters the
+    tree when its prefill completes; inserting only at request end loses all
+    sharing between requests that run at the same time.
+  * Eviction and references.  oripoin.cn, same section, first two bullets:
+    leaf-first LRU eviction, and nodes referenced by running requests are
+    never evicted; the cache and the running requests share one pool (third
+    bullet), so admission can evict.
+  * Tight memory.  Notes §3.3: with little KV room the ordering changes which
+    prefixes survive eviction.
 
-Readings: rounds are discrete; a request is admitted
-only if slots for its uncached prompt and its whole output can be allocated
-(evicting LRU leaves), and the first allocation failure ends admission for
-the round; the deferral rule compares the next min(defer_tokens, uncached)
-prompt tokens of requests with equal cached lengths; a finished request
-inserts its whole sequence, releases its references and frees its partial
-tail page; a request that depends on another arrives ``delay`` rounds after
-that one finishes.  Every step is taken in the order the C library's
-``sgl_sim_run`` takes it, so both produce the same numbers.
+Readings where the pages stop short (each is ours):
+  1. A round runs, in this order: arrivals; queue ordering (match lengths
+     from the trie, which refreshes the matched path's LRU stamps); admission
+     in queue order while fewer than ``max_running`` requests run; prefill of
+     up to ``prefill_budget`` prompt tokens in admission order; one decode
+     token for every request whose prefill finished in an earlier round;
+     finishing.
+  2. Admission allocates the uncached prompt and the whole output at once
+     (evicting LRU leaves as needed); the first allocation failure ends
+     admission for the round.
+  3. "Largely coincides" means: equal cached length and equal next
+     ``min(defer_tokens, uncached length)`` prompt tokens.
+  4. A finished request inserts its whole sequence, releases its reference
+     and frees a partial tail page.
+  5. A request that depends on another (the next turn of a conversation)
+     arrives ``delay`` rounds after that one finishes.
 """
 
 from oracle.tree import NoSlotsError

@@ -15,8 +15,11 @@
 //    prompt into the tree at prefill completion rather than at request end.
 //
 // The round structure, allocation at admission and the defer rule's exact
-// form are readings of those descriptions; the oracle (oracle/sched.py)
-// follows the same steps on the oracle trie.
+// form are readings of those descriptions: a round takes arrivals, queue
+// ordering, admission, prefill within the budget, one decode token per
+// request past prefill, then finishing; admission allocates the uncached
+// prompt and the whole output at once; "largely coincides" compares the next
+// defer_tokens uncached prompt tokens of requests with equal cached length.
 
 #include <algorithm>
 #include <cstring>

@@ -110,3 +110,20 @@ def assert_close(O, L, Oref, Lref, otol, ltol, rows=None):
     assert do <= otol, "O max-abs error %.3g > %.3g" % (do, otol)
     assert dl <= ltol, "LSE max-abs error %.3g > %.3g" % (dl, ltol)
     return do, dl
+
+
+def full_and_sampled_rows(ext, full, seed, picks):
+    """Every new-token row of the requests in ``full`` (all query heads: every
+    tile position, causal edge and K/V block of those requests), plus, for the
+    other requests, the first and last rows, the rows at ``picks`` and four
+    random ones."""
+    starts = np.concatenate([[0], np.cumsum(ext)[:-1]])
+    rng = np.random.default_rng(seed)
+    rows = []
+    for r, (s, e) in enumerate(zip(starts, ext)):
+        if r in full:
+            rows += list(range(int(s), int(s + e)))
+        else:
+            rows += [int(s), int(s + e - 1)] + [int(s + p) for p in picks if p < e]
+            rows += [int(s + x) for x in rng.integers(0, e, 4)]
+    return sorted(set(rows))

@@ -15,7 +15,7 @@ import torch
 import radixattention_prefix_shared_radix_gb300 as sgl
 import workloads as W
 from oracle.attention import decode_attention
-from tests._harness import Case, assert_close, run_decode, tolerances
+from tests._harness import Case, assert_close, full_and_sampled_rows, run_decode, tolerances
 
 pytestmark = pytest.mark.gpu
 
@@ -347,8 +347,8 @@ def _fp8_extend(case, ks, vs):
 @pytest.mark.parametrize("name", ["extend_small", "extend"])
 def test_extend_fp8_kv(name):
     """Extend (cached prefix + causal new block) over FP8 pools against the
-    oracle on the decoded values: every row at test size, sampled rows of
-    every request at the full size."""
+    oracle on the decoded values: every row at test size; at the full size
+    every row of request 2 and sampled rows of the others."""
     from oracle.attention import extend_attention
     from oracle.fp8 import DequantView
     case = Case(name)
@@ -357,13 +357,7 @@ def test_extend_fp8_kv(name):
         O, L, k8, v8, pre, ext, p = _fp8_extend(case, ks, vs)
         rows = None
         if name == "extend":
-            starts = np.concatenate([[0], np.cumsum(ext)[:-1]])
-            rng = np.random.default_rng(2)
-            rows = []
-            for s0, e in zip(starts, ext):
-                rows += [int(s0), int(s0 + e - 1), int(s0 + 127), int(s0 + 128)] + [int(s0 + x) for x in
-                                                                                    rng.integers(0, e, 4)]
-            rows = sorted(set(rows))
+            rows = full_and_sampled_rows(ext, (2,), 2, (127, 128))
         Oref, Lref = extend_attention(case.oracle_q(), DequantView(k8, ks), DequantView(v8, vs), case.oracle_table,
                                       pre, ext, rows=rows)
         do, dl = assert_close(O, L, Oref, Lref, *tolerances(case.w), rows=rows)

@@ -2,8 +2,8 @@
 
 Element by element on a scaled-down extend workload (ragged prefixes from 0,
 ragged new blocks from 1 token) and on head-shape variants; at the full
-4096 + 512 workload on sampled rows (first, last and random new tokens of
-every request).  Tolerances as for decode.
+4096 + 512 workload on every row of two whole requests and on sampled rows
+(first, last and random new tokens) of the others.  Tolerances as for decode.
 """
 
 import numpy as np
@@ -12,7 +12,7 @@ import torch
 
 import workloads as W
 from oracle.attention import decode_attention, extend_attention, extend_attention_kvwrite, kv_write
-from tests._harness import Case, assert_close, run_extend, tolerances
+from tests._harness import Case, assert_close, full_and_sampled_rows, run_extend, tolerances
 
 pytestmark = pytest.mark.gpu
 
@@ -83,15 +83,13 @@ def run_extend_last_rows(case, kd, vd):
 
 
 def test_extend_full_size_sampled():
+    """The full 4096 + 512 workload: requests 0 and 5 compared on every row,
+    the other six on sampled rows."""
     case = Case("extend")
     try:
         ext = case.out["seq_lens"] - case.out["prefix_lens"]
-        starts = np.concatenate([[0], np.cumsum(ext)[:-1]])
-        rng = np.random.default_rng(1)
-        rows = []
-        for s, e in zip(starts, ext):
-            rows += [int(s), int(s + e - 1), int(s + 127), int(s + 128)] + [int(s + x) for x in rng.integers(0, e, 4)]
-        do, dl = _check(case, rows=sorted(set(rows)))
+        rows = full_and_sampled_rows(ext, (0, 5), 1, (127, 128))
+        do, dl = _check(case, rows=rows)
         print("extend: O max-abs %.3g, LSE max-abs %.3g" % (do, dl))
     finally:
         case.close()
@@ -201,12 +199,7 @@ def test_extend_kvwrite_full_size_sampled():
         kn, vn = W.to_dtype(w, kf), W.to_dtype(w, vf)
         kd, vd = case.device_pool()
         O, L = _run_kvwrite(case, kd, vd, kn, vn, pre, ext)
-        starts = np.concatenate([[0], np.cumsum(ext)[:-1]])
-        rng = np.random.default_rng(2)
-        rows = []
-        for s, e in zip(starts, ext):
-            rows += [int(s), int(s + e - 1), int(s + 200)] + [int(s + x) for x in rng.integers(0, e, 3)]
-        rows = sorted(set(rows))
+        rows = full_and_sampled_rows(ext, (3, 7), 2, (200,))
         Oref, Lref = extend_attention_kvwrite(case.oracle_q(), kn.double().numpy(), vn.double().numpy(),
                                               W.RowView(case.K), W.RowView(case.V), case.oracle_table, pre, ext,
                                               rows=rows)

@@ -132,6 +132,15 @@ def test_lse_merge_closed_form():
     assert lse_merge([(np.zeros(8), -math.inf)])[1] == -math.inf
 
 
+def test_lse_merge_of_nothing_is_the_empty_context():
+    """No partials at all is an empty key set: O = 0 and LSE = -inf, like an
+    empty context."""
+    o, lse = lse_merge([], d=8)
+    assert lse == -math.inf and o.shape == (8,) and not o.any()
+    o, lse = lse_merge([])
+    assert lse == -math.inf and o.shape == (0,)
+
+
 def test_extend_no_prefix_is_causal_sdpa():
     rng = np.random.default_rng(9)
     Hq, Hkv, d, S = 8, 2, 32, 512
