@@ -63,6 +63,8 @@ def parse():
     ap.add_argument("--no-sched", action="store_true", help="skip the host scheduling simulation")
     ap.add_argument("--no-fp8", action="store_true", help="skip the FP8 KV decode object")
     ap.add_argument("--no-mla", action="store_true", help="skip the MLA decode object")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the fork_tree / multiturn / multiturn_noshare / tiny_fp32 objects")
     ap.add_argument("--pool-slots", type=int, default=0,
                     help="decode pool size override (0: the workload's 2^20 slots); small pools serve ncu captures")
     return ap.parse_args()
@@ -206,12 +208,26 @@ def reference_arm(args, budget_s, steps, warmup):
     }
 
 
+def host_cores():
+    """The host cores this process may run on."""
+    return len(os.sched_getaffinity(0))
+
+
+def set_blas_threads():
+    """BLAS threads = the host cores (before numpy is first imported); the
+    oracle's own loop over requests and heads stays one Python thread."""
+    n = str(host_cores())
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[k] = n
+    return int(n)
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
+    cores = set_blas_threads()
     r = reference_arm(args, args.ref_budget_s, max(1, args.steps), max(0, min(args.warmup, 3)))
-    cores = 1
     line = {
         "metric": METRIC, "value": r["value"], "unit": "GB/s", "impl": "reference", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["seconds_per_step"] * 1e3,
@@ -219,15 +235,17 @@ def run_reference(args):
         "config": {"workload": DECODE_WORKLOAD, "batch": 64, "prefix": 2048, "suffix": "U[64,512]",
                    "heads": "Hq32/Hkv8/d128", "pool_slots": 1 << 20, "sample_requests": r["requests"]},
         "cpu_baseline": {"value": r["value"], "unit": "GB/s", "cores": cores, "kind": "oracle",
-                         "sample": r["sample"]},
+                         "sample": r["sample"] + "; BLAS threads %d, the oracle's loop one Python thread" % cores,
+                         "seconds_per_step": r["seconds_per_step"],
+                         "unshared_seconds_per_step": r["unshared_seconds_per_step"]},
         "e2e": {"value": r["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
 def cpu_baseline_subprocess(budget_s=15.0):
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
-               RANK="0", WORLD_SIZE="1")
+    n = str(host_cores())
+    env = dict(os.environ, OMP_NUM_THREADS=n, OPENBLAS_NUM_THREADS=n, MKL_NUM_THREADS=n, RANK="0", WORLD_SIZE="1")
     cmd = [sys.executable, os.path.abspath(__file__), "--impl", "reference", "--steps", "3", "--warmup", "1",
            "--ref-budget-s", str(budget_s)]
     try:
@@ -237,22 +255,23 @@ def cpu_baseline_subprocess(budget_s=15.0):
                 d = json.loads(l)
                 return dict(d["cpu_baseline"])
     except Exception as e:  # the baseline is context only
-        return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": "failed: %s" % e}
-    return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": "no output"}
+        return {"value": None, "unit": "GB/s", "cores": host_cores(), "kind": "oracle", "sample": "failed: %s" % e}
+    return {"value": None, "unit": "GB/s", "cores": host_cores(), "kind": "oracle", "sample": "no output"}
 
 
 # --------------------------------------------------------------------------- native arm
-def setup_decode(sgl, W, torch, n_inst, num_sms=0, pool_slots=0):
+def setup_decode(sgl, W, torch, n_inst, num_sms=0, pool_slots=0, name=DECODE_WORKLOAD):
     import dataclasses
-    w = W.get(DECODE_WORKLOAD)
+    w = W.get(name)
     if pool_slots:
         w = dataclasses.replace(w, num_slots=int(pool_slots))
-    order, K, V = W.make_pool(w)
-    S = K.shape[0]
+    S = W.pool_slots(w, n_inst)
+    order, K, V = W.make_pool(w, num_slots=S)
     kd, vd = K.cuda(), V.cuda()
     del K, V
     tree = sgl.sgl_tree_create(S, w.page_size, order)
     per_tok = kv_bytes_per_token(w)
+    dt = sgl.SGL_DTYPE_F32 if w.dtype == "f32" else sgl.SGL_DTYPE_BF16
     inst = []
     for i in range(n_inst):
         b = W.make_batch(w, i)
@@ -262,7 +281,7 @@ def setup_decode(sgl, W, torch, n_inst, num_sms=0, pool_slots=0):
         view = sgl.sgl_groups_view(groups)
         gnp = sgl.groups_as_numpy(view)
         ub = int((gnp["seg_end"] - gnp["seg_begin"]).sum()) * per_tok
-        p = sgl.make_params(sgl.SGL_DTYPE_BF16, len(seqs), w.Hq, w.Hkv, w.d, S, w.page_size, num_sms=num_sms)
+        p = sgl.make_params(dt, len(seqs), w.Hq, w.Hkv, w.d, S, w.page_size, num_sms=num_sms)
         plan = sgl.sgl_decode_plan(p, out["seq_lens"], view)
         ws = torch.zeros(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
         sgl.sgl_plan_upload(plan, ws)
@@ -278,52 +297,145 @@ def setup_decode(sgl, W, torch, n_inst, num_sms=0, pool_slots=0):
     return w, tree, kd, vd, inst
 
 
+def graph_time(torch, fn, calls, n):
+    """ms per call of n back-to-back calls fn(calls[j % len(calls)]) captured
+    in one CUDA graph (replayed once to warm, then timed with CUDA events on
+    the current stream)."""
+    n = max(len(calls), n - n % len(calls))
+    g = torch.cuda.CUDAGraph()
+    st = torch.cuda.Stream()
+    st.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(st):
+        with torch.cuda.graph(g, stream=st):
+            for j in range(n):
+                fn(calls[j % len(calls)])
+    torch.cuda.current_stream().wait_stream(st)
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / n, n
+
+
+def bench_decode_workload(sgl, W, torch, name, n_inst, n_calls, hbm_peak, num_sms=0):
+    """Another decode workload timed like the headline: one CUDA graph of
+    back-to-back calls rotating over n_inst batch instances, CUDA events.
+    Returns unique-KV bytes per call, GB/s and fractions of the measured HBM
+    copy peak and of 8 TB/s."""
+    w, tree, kd, vd, inst = setup_decode(sgl, W, torch, n_inst, num_sms, name=name)
+    for s in range(max(3, len(inst))):
+        decode_call(sgl, kd, vd, inst[s % len(inst)])
+    torch.cuda.synchronize()
+    for it in inst:
+        sgl.sgl_check(it["ws"])
+    ms, n = graph_time(torch, lambda it: decode_call(sgl, kd, vd, it), inst, n_calls)
+    for it in inst:
+        sgl.sgl_check(it["ws"])
+    ub = sum(it["ub"] for it in inst) / len(inst)
+    uns = sum(it["unshared"] for it in inst) / len(inst)
+    gbs = ub / (ms / 1e3) / 1e9
+    info = sgl.sgl_plan_info(inst[0]["plan"])
+    r = {"workload": name, "batch": inst[0]["B"], "heads": "Hq%d/Hkv%d/d%d" % (w.Hq, w.Hkv, w.d), "dtype": w.dtype,
+         "page_size": w.page_size, "pool_slots": kd.shape[0], "instances": len(inst),
+         "unique_kv_bytes_per_call": int(ub), "unshared_kv_bytes_per_call": int(uns),
+         "us_per_call": ms * 1e3, "unique_kv_gbs": gbs, "frac_of_hbm": gbs / hbm_peak, "frac_of_8TBs": gbs / 8000.0,
+         "tokens_per_s": inst[0]["B"] / (ms / 1e3), "calls_timed": n,
+         "wide_items": info["num_wide_items"], "items": info["num_items"],
+         "l2": "%d instance(s), %.0f MB unique KV in all (L2 %d MB)" % (len(inst), ub * len(inst) / 1e6,
+                                                                       L2_BYTES // 1000000)}
+    del inst
+    sgl.sgl_tree_destroy(tree)
+    del kd, vd
+    torch.cuda.empty_cache()
+    return r
+
+
 def decode_call(sgl, kd, vd, it):
     sgl.sgl_decode_attn(it["q"], kd, vd, it["table"], it["seq"], it["plan"], it["o"], it["lse"], it["ws"])
 
 
 def e2e_decode(sgl, W, torch, w, tree, kd, vd, inst, steps, num_sms=0):
-    """Public-API step from host buffers; returns (GB/s, h2d bytes/step, d2h bytes/step)."""
+    """Decode steps of a serving loop through the public API from host
+    buffers, on one batch that grows: every step appends one token to every
+    request (a [B, cap] token matrix updated in place), and the step runs
+    sgl_build_batch (match; allocate and insert the new token's slot; emit
+    the prefix groups; the slot table and lengths go straight into pinned
+    staging arrays), sgl_decode_plan, sgl_plan_upload, the pinned H2D copies
+    of q, the table and the lengths, the decode call, the D2H copies of O
+    and LSE, a stream synchronise and sgl_tree_finish_batch (references
+    released, the sequences stay cached).  Returns (GB/s of unique KV, h2d
+    bytes/step, d2h bytes/step, s/step, host us per stage)."""
+    import numpy as np
     S = kd.shape[0]
-    pinned = []
-    for it in inst:
-        B, ld = it["table"].shape
-        pinned.append(dict(q=it["q"].cpu().pin_memory(), table=torch.empty((B, ld), dtype=torch.int32).pin_memory(),
-                           seq=torch.empty(B, dtype=torch.int32).pin_memory(),
-                           o=torch.empty_like(it["o"], device="cpu").pin_memory(),
-                           lse=torch.empty_like(it["lse"], device="cpu").pin_memory()))
-        pinned[-1]["table_np"] = pinned[-1]["table"].numpy()
-        pinned[-1]["seq_np"] = pinned[-1]["seq"].numpy()
+    it = inst[0]
+    B = it["B"]
+    lens0 = np.array([len(t) for t in it["seqs"]], dtype=np.int64)
+    cap = int(lens0.max()) + steps
+    toks = np.zeros((B, cap), dtype=np.int32)
+    for r, t in enumerate(it["seqs"]):
+        toks[r, :len(t)] = t
+    rng = np.random.default_rng(12)
+    toks_new = rng.integers(0, W.VOCAB, size=(steps, B)).astype(np.int32)
+    lens = lens0.copy()
+    ld = cap
+    pq = it["q"].cpu().pin_memory()
+    ptab = torch.empty((B, ld), dtype=torch.int32).pin_memory()
+    pseq = torch.empty(B, dtype=torch.int32).pin_memory()
+    po = torch.empty_like(it["o"], device="cpu").pin_memory()
+    plse = torch.empty_like(it["lse"], device="cpu").pin_memory()
+    tab_np, seq_np = ptab.numpy(), pseq.numpy()
+    dtab = torch.empty((B, ld), dtype=torch.int32, device="cuda")
+    dseq = torch.empty(B, dtype=torch.int32, device="cuda")
+    groups = sgl.sgl_groups_create()
+    # the largest plan of the run sizes the workspace (allocated before timing)
+    ws = torch.zeros(4 * it["plan"].workspace_bytes + (1 << 20), dtype=torch.uint8, device="cuda")
+    per_tok = kv_bytes_per_token(w)
+    ub0 = it["ub"]
+    stage = dict(build=0.0, plan=0.0, upload=0.0, device=0.0, finish=0.0)
     h2d = d2h = 0
     total_b = 0
     stream = torch.cuda.current_stream()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for s in range(steps):
-        it, pb = inst[s % len(inst)], pinned[s % len(inst)]
-        # the slot table and lengths are written straight into the pinned
-        # staging buffers that the host->device copies read
-        out = sgl.sgl_build_batch(tree, it["seqs"], groups=it["groups"], req_to_token=pb["table_np"],
-                                  seq_lens=pb["seq_np"])
-        view = sgl.sgl_groups_view(it["groups"])
-        p = sgl.make_params(sgl.SGL_DTYPE_BF16, it["B"], w.Hq, w.Hkv, w.d, S, w.page_size, num_sms=num_sms)
-        plan = sgl.sgl_decode_plan(p, out["seq_lens"], view)
-        sgl.sgl_plan_upload(plan, it["ws"])
-        it["table"].copy_(pb["table"], non_blocking=True)
-        it["seq"].copy_(pb["seq"], non_blocking=True)
-        it["q"].copy_(pb["q"], non_blocking=True)
-        decode_call(sgl, kd, vd, dict(it, plan=plan))
-        pb["o"].copy_(it["o"], non_blocking=True)
-        pb["lse"].copy_(it["lse"], non_blocking=True)
+        c0 = time.perf_counter()
+        toks[np.arange(B), lens] = toks_new[s]
+        lens += 1
+        out = sgl.sgl_build_batch(tree, toks, groups=groups, req_to_token=tab_np, seq_lens=seq_np, lens=lens)
+        c1 = time.perf_counter()
+        p = sgl.make_params(sgl.SGL_DTYPE_BF16, B, w.Hq, w.Hkv, w.d, S, w.page_size, num_sms=num_sms)
+        plan = sgl.sgl_decode_plan(p, out["seq_lens"], sgl.sgl_groups_view(groups))
+        if plan.workspace_bytes > ws.numel():
+            raise RuntimeError("e2e workspace too small")
+        c2 = time.perf_counter()
+        sgl.sgl_plan_upload(plan, ws)
+        c3 = time.perf_counter()
+        dtab.copy_(ptab, non_blocking=True)
+        dseq.copy_(pseq, non_blocking=True)
+        it["q"].copy_(pq, non_blocking=True)
+        sgl.sgl_decode_attn(it["q"], kd, vd, dtab, dseq, plan, it["o"], it["lse"], ws)
+        po.copy_(it["o"], non_blocking=True)
+        plse.copy_(it["lse"], non_blocking=True)
         stream.synchronize()
+        c4 = time.perf_counter()
         sgl.sgl_tree_finish_batch(tree, out)
+        c5 = time.perf_counter()
+        for k, a, b in (("build", c0, c1), ("plan", c1, c2), ("upload", c2, c3), ("device", c3, c4),
+                        ("finish", c4, c5)):
+            stage[k] += b - a
         if s == 0:
-            h2d = (pb["q"].numel() * 2 + pb["table"].numel() * 4 + pb["seq"].numel() * 4 +
-                   sgl.sgl_plan_info(plan)["upload_bytes"])
-            d2h = pb["o"].numel() * 2 + pb["lse"].numel() * 4
-        total_b += it["ub"]
+            h2d = (pq.numel() * 2 + ptab.numel() * 4 + pseq.numel() * 4 + sgl.sgl_plan_info(plan)["upload_bytes"])
+            d2h = po.numel() * 2 + plse.numel() * 4
+        # the shared prefix is unchanged; every request's own suffix grew by one token
+        total_b += ub0 + (s + 1) * B * per_tok
     el = time.perf_counter() - t0
-    return total_b / el / 1e9, h2d, d2h, el / steps
+    sgl.sgl_check(ws)
+    sgl.sgl_groups_destroy(groups)
+    host_us = {k: v * 1e6 / steps for k, v in stage.items()}
+    return total_b / el / 1e9, h2d, d2h, el / steps, host_us
 
 
 def run_native(args):
@@ -411,10 +523,10 @@ def run_native(args):
     achieved = (total_bytes / K) / (per_call_ms / 1e3) / 1e9
 
     # e2e through the public API from host buffers
-    e2e_gbs = h2d = d2h = e2e_step_s = None
+    e2e_gbs = h2d = d2h = e2e_step_s = e2e_host = None
     if not args.no_e2e:
-        e2e_gbs, h2d, d2h, e2e_step_s = e2e_decode(sgl, W, torch, w, tree, kd, vd, inst,
-                                                   max(1, min(args.e2e_steps, K)), args.num_sms)
+        e2e_gbs, h2d, d2h, e2e_step_s, e2e_host = e2e_decode(sgl, W, torch, w, tree, kd, vd, inst,
+                                                             max(1, min(args.e2e_steps, K)), args.num_sms)
 
     mla = None
     if not args.no_mla and args.only == "all":
@@ -424,6 +536,16 @@ def run_native(args):
     if not args.no_fp8:
         fp8 = bench_fp8(sgl, W, torch, w, kd, vd, inst, min(K, 2000), hbm_peak, args.num_sms)
         fp8["speedup_vs_bf16"] = per_call_ms / fp8["ms_per_call"]
+
+    others = None
+    if not args.no_workloads and args.only == "all":
+        # the other decode workloads: parallel-sampling fork tree, multi-turn
+        # groups at 80% and 0% sharing (inputs larger than L2 per call), and
+        # the tiny fp32 batch (latency only)
+        others = {}
+        for name, n_inst, n_calls in (("fork_tree", 4, 400), ("multiturn", 1, 100), ("multiturn_noshare", 1, 60),
+                                      ("tiny_fp32", 4, 2000)):
+            others[name] = bench_decode_workload(sgl, W, torch, name, n_inst, n_calls, hbm_peak, args.num_sms)
 
     ext = None
     if not args.no_extend and args.only == "all":
@@ -460,7 +582,11 @@ def run_native(args):
                      "frac_of_8TBs": achieved / 8000.0, "traffic": traffic,
                      "kernel": "decode call = decode_fused_kernel + decode_merge_kernel (unique-KV bytes / call time)"},
         "e2e": {"value": e2e_gbs, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_step_s * 1e3 if e2e_step_s else None},
+                "ms_per_step": e2e_step_s * 1e3 if e2e_step_s else None,
+                "step": "one growing batch (batch instance 0): every step appends one token per request "
+                        "(slot allocated and inserted), plans, uploads, copies in, decodes, copies out, "
+                        "synchronises and finishes the batch",
+                "host_us_per_step": e2e_host},
         "gpu_launches": K * launches_per_call,
         "clocks": clocks.summary(),
     }
@@ -468,6 +594,8 @@ def run_native(args):
         line["fp8_kv"] = fp8
     if mla is not None:
         line["mla"] = mla
+    if others is not None:
+        line.update(others)
     if ext is not None:
         line["extend"] = ext
     if rank == 0 and args.only == "all" and not args.no_sched:

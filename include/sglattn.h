@@ -456,19 +456,22 @@ int sgl_check(void* workspace, sgl_stream_t stream);
 
 /* Decode attention without a caller-provided workspace.
  * No counterpart on the pages: this is a convenience for callers that cannot
- * allocate device memory -- code running while a stream is captured into a
- * CUDA graph (cudaMalloc is not allowed there), serving loops whose device
- * memory belongs to another allocator, or latency-critical paths that avoid
+ * allocate device memory -- serving loops whose device memory belongs to
+ * another allocator with a fixed budget, or latency-critical paths that avoid
  * cudaMalloc because it can synchronize the device.
  * Same arguments and result as sgl_decode_attn minus the workspace; the
  * plan is uploaded by the call itself.  Scratch is a fixed 64 MiB array in
  * the library's device image, held by every GPU that loads the library
  * until the process exits; a plan whose workspace_bytes exceeds 64 MiB is
- * rejected with SGL_ERR_WORKSPACE before any GPU work.  The first call on a
- * device looks the array's address up (cudaGetSymbolAddress), so make that
- * first call before any stream capture.  All calls share the array: calls
- * that may overlap on the GPU (different streams, or before the previous
- * call has finished reading it) race and must not be issued.  Out-of-range
+ * rejected with SGL_ERR_WORKSPACE, and every other argument error is
+ * returned, before any GPU work.  The first call on a device looks the
+ * array's address up (cudaGetSymbolAddress, with that device current) and
+ * caches it, so make that first call before any stream capture; a device
+ * reset (cudaDeviceReset) is not supported afterwards.  All calls share the
+ * array, whose contents are the last call's (each call rewrites the plan
+ * tables and clears the error word and merge counters itself): calls that
+ * may overlap on the GPU (different streams, or before the previous call
+ * has finished reading it) race and must not be issued.  Out-of-range
  * slots are skipped as in sgl_decode_attn, but their error word cannot be
  * read back (there is no workspace pointer to give sgl_check).
  * Allocates nothing: no cudaMalloc, cudaFree or allocating library call. */

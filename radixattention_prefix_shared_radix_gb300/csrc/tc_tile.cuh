@@ -1,9 +1,9 @@
 // Attention tiles on the 5th-generation tensor cores (tcgen05 + TMEM): NQ
 // query tiles of 128 rows against the KV positions [kv_begin, kv_end) of one
-// req_to_token row, gathered 64 positions at a time into one K/V stream that
-// the query tiles share.  Used by the extend kernel (two query tiles per CTA)
-// and by the fused decode kernel (one query tile at a time, the CTA's
-// prefix-group tiles one after another).
+// req_to_token row, gathered BN = 128 positions at a time into one K/V
+// stream that the query tiles share.  Used by the extend kernel (two query
+// tiles per CTA) and by the fused decode kernel (its prefix-group tiles one
+// after another).
 //
 // Roles, by warp of the C::kThreads tile threads:
 //   warps 0 .. 4 NQ - 1   softmax: query tile w / 4, thread = query row =
@@ -15,24 +15,25 @@
 //                         tensor [slot * Hkv + head, d]) into 128B-swizzled
 //                         tiles; extend's Q tiles with 16-byte cp.async.
 // Measured on GB300: a warp gets one random-row gather through every ~110
-// cycles, whether one lane issues them or many, so the gather rate grows with
+// cycles, whether one lane or many issue them, so the gather rate grows with
 // the number of warps that issue; hence a team.
-// In decode tiles Q lives in TMEM (columns 256..256+d/2, bf16 pairs, written
-// by the softmax threads from their own rows) and S = Q K^T reads A from
-// TMEM, which leaves the CTA's shared memory to its streaming warps.
+// In single-tile decode configurations Q lives in TMEM (columns after O,
+// bf16 pairs, written by the softmax threads from their own rows) and
+// S = Q K^T reads A from TMEM, which leaves shared memory to the streaming
+// warps; with two query tiles Q is a shared-memory operand.
 // The gather team looks up each block's slots in req_to_token one block
 // ahead.
-// Per 64-position KV block j and query tile q:  S = Q K_j^T (M 128, N 64, K
-// d; both operands K-major) into one of two TMEM score buffers.  The softmax
-// threads read their row (two TMEM loads in flight, one wait), keep a running
-// max m and sum l in base 2 (scores scaled by sm_scale*log2 e inside the
-// exponent's FMA), and write P_j = 2^(s - m) as bf16 pairs back into the first
-// half of the same TMEM buffer; the MMA thread then issues O += P_j V_j with A
-// read from TMEM (M 128, N d, K 64; V an MN-major smem operand) and S_{j+2}
-// into the freed buffer.  O lives in TMEM and is rescaled only when a row's
-// max grows by more than 8 (a factor 2^8, harmless in fp32), by the warp that
-// owns the row, which then waits for PV_{j-1}; otherwise the softmax never
-// waits for the PV products.
+// Per 128-position KV block j and query tile q:  S = Q K_j^T (M 128, N 128,
+// K d; both operands K-major) into one of NSB TMEM score buffers.  The
+// softmax threads read their row in 64-column halves (two TMEM loads in
+// flight, one wait), keep a running max m and sum l in base 2 (scores scaled
+// by sm_scale*log2 e inside the exponent's FMA), and write P_j = 2^(s - m)
+// as bf16 pairs back into the first half of the same TMEM buffer; the MMA
+// thread then issues O += P_j V_j with A read from TMEM (M 128, N d, K 128;
+// V an MN-major smem operand) and S_{j+NSB} into the freed buffer.  O lives
+// in TMEM and is rescaled only when a row's max grows by more than 8 (a
+// factor 2^8, harmless in fp32), by the warp that owns the row, which then
+// waits for PV_{j-1}; otherwise the softmax never waits for the PV products.
 //
 // Barrier phases run on across tiles: J counts the blocks and T the tile sets
 // this CTA has processed, so a CTA can run any number of tile sets back to

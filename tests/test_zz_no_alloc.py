@@ -1,12 +1,14 @@
 """Decode through the no-allocation entry point (GPU).
 
-Some callers cannot allocate device memory (a stream being captured into a
-CUDA graph, a serving loop whose memory another allocator owns, a path that
-must not risk cudaMalloc synchronizing the device).  For them the library
-offers sgl_decode_attn_noalloc, which uses a fixed scratch array in its own
-device image instead of a caller workspace.  This test calls it through the
-C ABI twice in a row and checks both results against sgl_decode_attn with a
-caller workspace, and that a plan too large for the scratch is refused.
+Some callers cannot allocate device memory (a serving loop whose memory
+another allocator owns under a fixed budget, a path that must not risk
+cudaMalloc synchronizing the device).  For them the library offers
+sgl_decode_attn_noalloc, which uses a fixed scratch array in its own device
+image instead of a caller workspace.  This test calls it through the C ABI
+twice in a row and checks both results against sgl_decode_attn with a
+caller workspace, that the calls leave the torch allocator's device memory
+unchanged, and that a plan too large for the scratch, or another argument
+error, is refused.
 """
 
 import numpy as np
@@ -43,11 +45,14 @@ def test_noalloc_matches_workspace_decode_twice():
         sgl.sgl_decode_attn(q, kd, vd, table, seq, plan, o_ref, lse_ref, ws)
         sgl.sgl_check(ws)
         otol, ltol = tolerances(case.w)
-        for _ in range(2):
-            o = torch.full_like(q, float("nan"))
-            lse = torch.full((case.B, case.w.Hq), float("nan"), dtype=torch.float32, device="cuda")
+        outs = [(torch.full_like(q, float("nan")),
+                 torch.full((case.B, case.w.Hq), float("nan"), dtype=torch.float32, device="cuda")) for _ in range(2)]
+        torch.cuda.synchronize()
+        before = torch.cuda.memory_allocated(), torch.cuda.memory_reserved()
+        for o, lse in outs:
             sgl.sgl_decode_attn_noalloc(q, kd, vd, table, seq, plan, o, lse)
             torch.cuda.synchronize()
+            assert (torch.cuda.memory_allocated(), torch.cuda.memory_reserved()) == before
             assert torch.isfinite(lse).all()
             assert (o.float() - o_ref.float()).abs().max().item() <= otol
             assert (lse - lse_ref).abs().max().item() <= ltol
@@ -74,3 +79,22 @@ def test_noalloc_rejects_plan_beyond_scratch():
     finally:
         sgl.sgl_groups_destroy(g)
         sgl.sgl_tree_destroy(tree)
+
+
+def test_noalloc_refuses_a_bad_call_before_gpu_work():
+    """An MLA plan, or a slot table narrower than the plan's positions, is
+    refused with SGL_ERR_INVALID_ARG by the argument checks."""
+    case = Case("llama3_8b_decode_small")
+    try:
+        kd, vd = case.device_pool()
+        plan = sgl.sgl_decode_plan(case.params(), case.out["seq_lens"], sgl.sgl_groups_view(case.groups))
+        q = case.q_host().cuda()
+        seq = torch.from_numpy(case.out["seq_lens"]).cuda()
+        o = torch.empty_like(q)
+        lse = torch.empty(case.B, case.w.Hq, dtype=torch.float32, device="cuda")
+        narrow = torch.from_numpy(np.ascontiguousarray(case.out["req_to_token"][:, :1])).cuda()
+        with pytest.raises(sgl.SglError) as e:
+            sgl.sgl_decode_attn_noalloc(q, kd, vd, narrow, seq, plan, o, lse)
+        assert e.value.status == -1
+    finally:
+        case.close()

@@ -16,7 +16,7 @@ Workloads (shapes of the five configurations the hot path is measured on):
                       2^19-slot pool.
   4 extend            8 requests, each with its own cached 4096-token prefix
                       and 512 new tokens (causal); Hq 64, Hkv 8, d 128;
-                      2^18-slot pool.
+                      2^20-slot pool (the "1M-slot pool" of workload 2).
   5 multiturn         256 requests in groups of 4; per group one context
                       length L ~ lognormal(median 3000, sigma 1) capped to
                       [1, 32768]; the members share the first
@@ -91,7 +91,7 @@ WORKLOADS = {
                           ("fork", dict(prompts=16, prompt=(1024, 1024), forks=8, branch=(256, 256))),
                           num_slots=1 << 19),
     "extend": Workload("extend", 4, "extend", "bf16", 64, 8, 128, 1,
-                       ("extend", dict(n=8, prefix=(4096, 4096), new=(512, 512))), num_slots=1 << 18),
+                       ("extend", dict(n=8, prefix=(4096, 4096), new=(512, 512))), num_slots=1 << 20),
     "multiturn": Workload("multiturn", 5, "decode", "bf16", 32, 8, 128, 16,
                           ("groups", dict(groups=64, size=4, median=3000, sigma=1.0, cap=32768, share=0.8))),
     "multiturn_noshare": Workload("multiturn_noshare", 5, "decode", "bf16", 32, 8, 128, 16,
