@@ -63,7 +63,7 @@ __global__ void __launch_bounds__(128)
     constexpr int E = D / 32;
     const sgl::DecItem it = items[blockIdx.x];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int rows = it.n_mem * G;
+    const int rows = it.n_mem * it.nh * G;
     int kv_end = it.kv_end;
     const int rep_len = __ldg(seq_lens + it.rep_row);
     if (kv_end > rep_len) {
@@ -71,8 +71,10 @@ __global__ void __launch_bounds__(128)
         kv_end = rep_len;
     }
     for (int r = warp; r < rows; r += 4) {
-        const int mem = __ldg(members + it.mem_begin + r / G);
-        const float* qr = q + ((int64_t)mem * Hq + it.kvh * G + r % G) * D + lane * E;
+        // row r: member r / (nh G), KV head kvh + (r / G) % nh, query head r % G of its group
+        const int mem = __ldg(members + it.mem_begin + r / (it.nh * G));
+        const int kvh = it.kvh + (r / G) % it.nh;
+        const float* qr = q + ((int64_t)mem * Hq + kvh * G + r % G) * D + lane * E;
         float qv[E], o[E];
 #pragma unroll
         for (int e = 0; e < E; ++e) {
@@ -83,8 +85,8 @@ __global__ void __launch_bounds__(128)
         for (int pos = it.kv_begin; pos < kv_end; ++pos) {
             const int64_t slot = load_slot(r2t, ld, it.rep_row, pos, num_slots, err);
             if (slot < 0) continue;
-            const float* kr = kp + (slot * Hkv + it.kvh) * D + lane * E;
-            const float* vr = vp + (slot * Hkv + it.kvh) * D + lane * E;
+            const float* kr = kp + (slot * Hkv + kvh) * D + lane * E;
+            const float* vr = vp + (slot * Hkv + kvh) * D + lane * E;
             float dot = 0.f;
 #pragma unroll
             for (int e = 0; e < E; ++e) dot = fmaf(qv[e], kr[e], dot);

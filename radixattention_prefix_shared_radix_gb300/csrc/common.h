@@ -21,24 +21,28 @@ int query_num_sms(int32_t requested);
 // SGL_OK or SGL_ERR_INVALID_ARG.
 int validate_groups(int32_t B, const int32_t* seq_lens, const sgl_prefix_groups* g);
 
-// Decode work item: one KV chunk of one prefix-group segment for one KV head
-// and one block of the segment's members.  Laid out in the workspace.
+// Decode work item: one KV chunk of one prefix-group segment for a block of
+// `nh` consecutive KV heads and one block of the segment's members.  Laid out
+// in the workspace.  Its query rows are ordered member, then KV head of the
+// block, then query head of the group: row ((i * nh) + hh) * G + g is member
+// i's query head (kvh + hh) * G + g, and partial row partial_base + row holds
+// its result.
 struct DecItem {
     int32_t rep_row;       // request row whose req_to_token slots are read
     int32_t kv_begin;      // first position of the chunk
     int32_t kv_end;        // one past the last position
-    int32_t kvh;           // KV head
+    int32_t kvh;           // first KV head of the block
     int32_t mem_begin;     // first member in the plan's member array
-    int32_t n_mem;         // members in this block (rows = n_mem * G)
-    int32_t partial_base;  // first partial row; row = member_idx * G + head_in_group
-    int32_t pad;
+    int32_t n_mem;         // members in this block
+    int32_t partial_base;  // first partial row
+    int32_t nh;            // KV heads in the block (1 for tensor-core tiles)
 };
 static_assert(sizeof(DecItem) == 32, "DecItem is 32 bytes");
 
-// Decode schedule constant (bf16 persistent kernel): each CTA runs the tile
-// roles (7 warps) for its prefix-group tiles and kDecNarrowWarps streaming
-// consumer warps for narrow pieces, each fed by its own producer warp.
-constexpr int kDecNarrowWarps = 4;
+// Decode schedule constant (bf16 persistent kernel): a narrow piece covers up
+// to kDecHeadBlock KV heads of its positions (one consumer warp each); each
+// CTA runs one stream of such pieces, fed by one producer warp.
+constexpr int kDecHeadBlock = 8;
 
 // Workspace header (first 256 bytes): error word + plan dimensions.
 struct WsHeader {

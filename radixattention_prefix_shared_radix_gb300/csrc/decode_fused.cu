@@ -13,45 +13,52 @@
 //               tc_tile.cuh over this CTA's wide items: a chunk of a shared
 //               segment against up to 128 query rows (member request x query
 //               head of one KV head); warps 5-10 are the tiles' gather team;
-//   warps 7-10  streaming producers: each issues the cp.async gathers of one
-//               consumer's K/V rows into its shared-memory ring (in CTAs
-//               with wide items, once the tiles are done);
-//   warps 11-14 streaming consumers: each runs narrow pieces (at most 8
-//               query rows: one request's G heads, or a few members of a
-//               small group) on the tensor cores: its launch piece, then
-//               pieces its producer takes from a run-time counter, so faster
-//               SMs stream more and all finish together.
-// The tiles are bound by latency and the tensor pipe, the streams by HBM.
-// The planner puts the wide items on the first CTAs (as many as balance the
-// streaming work); their streaming warps wait at a barrier until the tiles are
-// done and then take pieces from the run-time counter, so an SM never runs
-// both kinds at once (measured: co-running them cost the streams most of
-// their instruction-cache hits).  Producers and consumers are separate
-// warps so the copies keep flowing while the consumers compute, and there is
-// one producer per consumer: measured on GB300, a warp issuing random
-// 256-byte-row cp.async gathers gets one instruction through every ~80-100
-// cycles once the SM's load pipe is busy, so the SM's issue rate (and HBM
-// bandwidth) grows with the number of issuing warps.
+//   warp 2      the streaming lookup warp: pieces, slots, piece fields;
+//   warps 3-6   the streaming producers (bulk copies of whole token rows);
+//   warps 7-14  streaming consumers, one per KV head of the current piece
+//   (in CTAs with wide items, the streaming roles start once the tiles are
+//   done).
+// A narrow piece is a run of positions of one request segment (a request's
+// own suffix, or a small group's) for a block of up to 8 consecutive KV
+// heads, with at most 8 query rows per head (members x G query heads).  In
+// the pool [slot, Hkv, d] a token's K (or V) row for those heads is one
+// contiguous run of nh * d elements, moved with one cp.async.bulk.
+// Measured on GB300: random 2 KB token rows gather at 6.8-7.1 TB/s from 152
+// SMs; on 32 SMs (HBM not saturated) one warp issuing them reaches 54 GB/s
+// per SM and four warps 117 GB/s (a warp gets about one bulk copy through
+// every 100 cycles), hence four producer warps; 256-byte rows of one head,
+// as 16-byte cp.async, stalled near 32 GB/s per SM on the copy issue.  The
+// lookup warp takes every global-latency wait (piece counter, records,
+// slot table) off the producers.  The tiles are bound by latency and the tensor
+// pipe, the streams by HBM.  The planner puts the wide items on the first
+// CTAs (as many as balance the streaming work); their streaming warps wait
+// at a barrier until the tiles are done and then take pieces from the
+// run-time counter, so an SM never runs both kinds at once (measured:
+// co-running them cost the streams most of their instruction-cache hits).
 //
-// Streaming ring per consumer: 4 stages of 16 positions (K and V rows, 8 KB)
-// with a descriptor each (first position, piece, flags), a FULL mbarrier per
-// stage (each producer lane arrives when its copies have landed:
-// cp.async.mbarrier.arrive.noinc, and lane 0 once more to release the
-// descriptor) and an EMPTY mbarrier (the consumer arrives when it has read
-// the stage).  The producer looks slots up six steps ahead with 4-byte
-// cp.async into a small slot ring, so no register ever waits on a load in
-// flight; its own cp.async groups order slot lookups before their use.
+// Streaming ring: NSF stages of 16 positions, each the 16 K rows then the
+// 16 V rows of those positions, a row every nh * d * (element bytes) + 16
+// bytes: the 16-byte pad puts 8 consecutive rows in distinct banks, so the
+// consumers' ldmatrix reads need no swizzle (a bulk copy lands a whole row
+// contiguously).  Per stage a FULL mbarrier (the producer's arrival with the
+// stage's byte count; the copies complete it), an EMPTY mbarrier (one
+// arrival per consumer warp) and a 32-byte descriptor (first position,
+// piece, flags).  The lookup warp fills a slot ring of 8 steps (4-byte
+// cp.async of each step's slots, plus the piece fields), so no producer
+// register ever waits on a load in flight.  A piece's query rows land in
+// the Q slot with its first stage
+// (one bulk copy per member and KV head: the head's G query heads are
+// consecutive rows of q); the consumers release the slot (QEMPTY) once
+// their fragments are in registers.
 //
-// Consumer, per 16-position step (mma.sync m16n8k16, bf16 in, fp32 acc;
-// query rows in the MMA's N dimension):
+// Consumer warp c, per 16-position step, for KV head kvh + c of the piece
+// (mma.sync m16n8k16, bf16 in, fp32 acc; the head's query rows in the MMA's
+// N dimension):
 //   S^T [16 pos x 8 rows] = K [16 x d] . Q^T [d x 8 rows]
 //   O^T [d x 8 rows]     += V^T [d x 16 pos] . P^T [16 pos x 8 rows]
-// K and V rows are XOR-swizzled [16 x d] tiles (ldmatrix for K,
-// ldmatrix.trans for V^T, conflict-free); P^T moves from the accumulator
-// layout to the B-operand layout with movmatrix.  A piece's query rows are
-// staged by the producer with the piece's first step (two Q slots, released
-// by the consumer through a QEMPTY barrier), so the consumer's loop touches
-// nothing but shared memory.
+// ldmatrix for K, ldmatrix.trans for V^T; P^T moves from the accumulator
+// layout to the B-operand layout with movmatrix.  The consumers' loop
+// touches nothing but shared memory.
 //
 // Every item writes normalised partial rows (O fp32, LSE natural log); the
 // merge launch (merge.cuh) combines each (request, KV head)'s partials once
@@ -67,51 +74,51 @@ namespace {
 using namespace sgldev;
 using namespace tc;
 
-constexpr int kConsumers = kDecNarrowWarps;              // streaming consumer warps per CTA
-constexpr int kProducers = kConsumers;                   // one per consumer
-constexpr int kNS = 2;                                   // ring stages per consumer (tile CTA: beside the tiles' K/V rings)
-constexpr int kNSF = 4;                                  // ring stages per consumer (streaming CTA)
+constexpr int kHB = kDecHeadBlock;                       // consumer warps = KV heads of a piece (at most)
 constexpr int kNP = 16;                                  // KV positions per step
-constexpr int kQD = 6;                                   // slot lookups ahead (steps per consumer)
-constexpr int kSQ = 8;                                   // slot ring entries per consumer
-constexpr int kSlotEntry = 128;                         // 16 slots + step and piece fields (see below)
-constexpr int kGrabAhead = 4;                            // take the next piece this many steps before the end
-constexpr int kFirstProducer = 7;                        // after the tile roles' softmax, MMA and own gather warps
-static_assert(DecCfg<128>::kThreads == 32 * (kFirstProducer + kProducers) && DecCfg<64>::kThreads == DecCfg<128>::kThreads,
-              "the tile roles' gather team is warps 5 .. 10: two of its own and the four producers");
+constexpr int kSQ = 8;                                   // slot ring entries (lookups ahead of the copies)
+constexpr int kSlotEntry = 128;                          // 16 slots + step and piece fields (see below)
+constexpr int kLookup = 2;                               // the lookup warp
+constexpr int kFirstProducer = 3;
+constexpr int kProducers = 4;                            // each issues 8 of a stage's 32 row copies
 constexpr int kFirstConsumer = kFirstProducer + kProducers;
-constexpr int kFusedThreads = 32 * (kFirstConsumer + kConsumers);
-static_assert(kSQ >= kQD && (kSQ & (kSQ - 1)) == 0 && kQD >= kNSF - 1, "slot ring");
+constexpr int kFusedThreads = 32 * (kFirstConsumer + kHB);
+static_assert(DecCfg<128>::kThreads <= kFusedThreads && DecCfg<64>::kThreads == DecCfg<128>::kThreads,
+              "the tile roles fit in the CTA");
+static_assert((kSQ & (kSQ - 1)) == 0, "slot ring");
+static_assert((2 * kNP) % kProducers == 0 && 2 * kNP / kProducers <= 32, "row copies per producer warp");
 
 template <int D, bool F8 = false>
 struct FusedLayout {
     using TL = typename DecCfg<D, F8>::Lay;
-    static constexpr int TILEB = kNP * D * (F8 ? 1 : 2);   // one K (or V) tile of a step
-    static constexpr int STAGE = 2 * TILEB;
-    static constexpr int RING = kNS * STAGE;             // per consumer, beside the tile roles
-    static constexpr int RING_F = kNSF * STAGE;          // per consumer, CTA without tiles (from offset 0)
-    static constexpr int SLOTW = kSQ * kSlotEntry;       // slot ring per consumer
-    // Layout from offset 0: the tile roles' TMEM address and broadcast area
-    // (up to TL::KEEP), then the rings of a CTA with tiles, the slot rings,
-    // descriptors and Q slots.  These are used only once the CTA's tiles are
-    // done, so they overlap the rest of the tile roles' area (TL::KEEP ..
-    // TL::END: stages, barriers, staging).  A CTA without tiles puts its
-    // deeper rings at offset 0.  The streaming barriers, initialised at
+    static constexpr int ES = F8 ? 1 : 2;                // bytes per pool element
+    static constexpr int PITCH = kHB * D * ES + 16;      // one token's K (or V) row of a head block, padded
+    static constexpr int STAGE = 2 * kNP * PITCH;        // K rows, then V rows
+    static constexpr int QSLOT = kHB * 8 * D * 2;        // [head][8 rows][d] bf16
+    static constexpr int SLOTW = kSQ * kSlotEntry;
+    static constexpr int FIXED = 1024 + QSLOT + SLOTW + 8 * 32 + 64 + (2 * 8 + 1 + 2 * kSQ) * 8 + 1024;
+    static constexpr int NSF0 = (232448 - FIXED) / STAGE;
+    static constexpr int NSF = NSF0 > 8 ? 8 : NSF0;      // ring stages
+    // Layout: the tile roles' TMEM address and broadcast area (up to
+    // TL::KEEP); from 1024 the ring, the Q slot, the slot ring and the stage
+    // descriptors.  These are used only once the CTA's tiles are done, so
+    // they overlap the rest of the tile roles' area (TL::KEEP .. TL::END:
+    // stages, barriers, staging).  The streaming barriers, initialised at
     // launch, come after everything.
-    static constexpr int OFF_RING = (TL::KEEP + 127) / 128 * 128;
-    static constexpr int END_RINGS = (OFF_RING + kConsumers * RING) > kConsumers * RING_F
-                                         ? (OFF_RING + kConsumers * RING) : kConsumers * RING_F;
-    static constexpr int OFF_SLOT = END_RINGS;
-    static constexpr int QSLOT = 8 * D * 2;              // query rows of one piece (at most 8)
-    static constexpr int OFF_DESC = OFF_SLOT + kConsumers * SLOTW;   // kNSF stage descriptors (32 B) per consumer
-    static constexpr int OFF_Q = (OFF_DESC + kConsumers * kNSF * 32 + 127) / 128 * 128;   // 2 Q slots per consumer
-    static constexpr int END_Q = OFF_Q + kConsumers * 2 * QSLOT;
-    // FULL[kNSF], EMPTY[kNSF], QEMPTY[2] per consumer
-    static constexpr int OFF_SBAR = ((END_Q > TL::END ? END_Q : TL::END) + 7) / 8 * 8;
-    static constexpr int END = OFF_SBAR + kConsumers * (2 * kNSF + 2) * 8;
+    static constexpr int OFF_RING = 1024;
+    static constexpr int OFF_Q = OFF_RING + NSF * STAGE;
+    static constexpr int OFF_SLOT = OFF_Q + QSLOT;
+    static constexpr int OFF_DESC = OFF_SLOT + SLOTW;
+    static constexpr int OFF_LREC = OFF_DESC + NSF * 32;   // launch piece: record (32 B), members (32 B)
+    static constexpr int END_S = OFF_LREC + 64;
+    // FULL[NSF], EMPTY[NSF], QEMPTY, SLOTFULL[kSQ], SLOTFREE[kSQ]
+    static constexpr int OFF_SBAR = ((END_S > TL::END ? END_S : TL::END) + 7) / 8 * 8;
+    static constexpr int END = OFF_SBAR + (2 * NSF + 1 + 2 * kSQ) * 8;
     static constexpr int TOTAL = END + 1024;             // + alignment slack
-    static_assert(OFF_SBAR >= TL::END && OFF_SBAR >= END_Q, "streaming barriers clear of every other area");
+    static_assert(NSF >= 3, "ring depth");
+    static_assert(OFF_SBAR >= TL::END && OFF_SBAR >= END_S, "streaming barriers clear of every other area");
     static_assert(TOTAL <= 232448, "shared memory per CTA");
+    static_assert(TL::KEEP <= OFF_RING, "the ring clears the tile roles' kept area");
 };
 
 struct FusedArgs {
@@ -119,7 +126,7 @@ struct FusedArgs {
     const int32_t* wptr;   // [n_ctas + 1] wide items of each CTA
     const DecItem* narrow; // narrow pieces, longest first
     int n_narrow;
-    int n_init;            // pieces assigned at launch: streaming consumer w starts on piece w
+    int n_init;            // pieces assigned at launch: streaming CTA w starts on piece w
     int n_tile_ctas;       // CTAs 0 .. n_tile_ctas-1 run the wide items first
     uint32_t* sched;       // [2] next piece to hand out, producers finished (restored at the end)
 };
@@ -139,13 +146,6 @@ __device__ __forceinline__ void mma16816_f16(float* c, const uint32_t* a, uint32
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// 16-byte chunk c of row r of an FP8 [16 x D] stage tile (rows of D bytes),
-// XOR-swizzled so that the consumer's fragment reads (below) are free of
-// bank conflicts for D = 128 (two-way for D = 64).
-template <int D>
-__device__ __forceinline__ uint32_t fswz(int r, int c) {
-    return (uint32_t)(r * D + ((c ^ (D == 128 ? (r & 7) : ((r >> 1) & 3))) << 4));
-}
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t d;
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
@@ -159,293 +159,112 @@ __device__ __forceinline__ void lds64(uint32_t addr, uint32_t* w) {
 }
 
 // stage descriptor flags
-constexpr int kFirst = 1;   // first step of its piece: its query rows are in the stage's Q slot
-constexpr int kEnd = 4;     // no more pieces: the consumer stops
+constexpr int kFirst = 1;   // first step of its piece: its query rows are in the Q slot
+constexpr int kEnd = 4;     // no more pieces: the consumers stop
 
 // slot-ring entry (one looked-up step): 16 slots, then
-constexpr int kEntKvh = 64, kEntP0 = 72, kEntFlags = 76, kEntCm = 80, kEntPb = 84, kEntRows = 88;
-constexpr int kEntMem = 96;   // 8 ints: member request of each query row (first step only)
+constexpr int kEntKvh = 64, kEntP0 = 68, kEntFlags = 72, kEntCm = 76, kEntPb = 80, kEntNh = 84, kEntNm = 88;
+constexpr int kEntMem = 96;   // 8 ints: the piece's member requests (first step only)
 // stage descriptor
-constexpr int kDescP0 = 0, kDescFlags = 4, kDescCm = 8, kDescPb = 12, kDescRows = 16, kDescQ = 20;
+constexpr int kDescP0 = 0, kDescFlags = 4, kDescCm = 8, kDescPb = 12, kDescRows = 16, kDescNh = 20;
 
 // ---------------------------------------------------------------------------
-// Producer
+// Lookup warp (one per CTA)
 // ---------------------------------------------------------------------------
-// Walks this consumer's pieces (its launch piece, then pieces taken from the
-// run-time counter), looks up each step's slots kQD steps ahead (4-byte
-// cp.async into the slot ring, with the step's KV head, position and flags,
-// and for a first step the piece's partial base, rows, clamped end and the
-// member request of each query row), and for each step waits for the ring
-// stage to be free, issues the K/V row copies (and, for a first step, the
-// piece's query rows into one of two Q slots once the consumer has released
-// it), writes the stage descriptor and arrives on the stage's FULL barrier
-// (32 lanes when their copies land + lane 0 releasing the descriptor).  The
-// next piece is fetched in phases spread over the steps (take a number from
-// the counter; load its record; load its members and seq_len), so no register
-// waits on a load in flight.
-template <int D, int NS, bool F8 = false>
-__device__ __noinline__ void stream_producer(const FusedArgs& f, int gw, uint32_t ring, uint32_t sring,
-                                             uint32_t desc, uint32_t qbuf, uint32_t full, uint32_t empty,
-                                             uint32_t qempty, int lane) {
-    using Lay = FusedLayout<D, F8>;
-    constexpr int CPR = D / 8;                 // 16-byte chunks per row
-    constexpr int RPI = 32 / CPR;              // rows per warp instruction
+// Walks this CTA's pieces (its launch piece, whose record and members were
+// loaded before the dependency wait, then pieces taken from the run-time
+// counter) and fills the slot ring up to kSQ steps ahead of the producers:
+// per step the 16 slots (4-byte cp.async from req_to_token; positions past
+// the piece's end marked), the step's first KV head, position and flags,
+// and for a piece's first step its partial base, clamped end, head and
+// member counts and member requests.  Each entry's barrier (SLOTFULL)
+// completes when the lanes' cp.async have landed and lane 0 has written the
+// fields; the producers free it (SLOTFREE).  An entry with no KV head ends
+// the stream.  Global loads (the counter, records, seq_lens) stall only this
+// warp, which runs ahead of the copies.
+template <int D, bool F8>
+__device__ __noinline__ void stream_lookup(const FusedArgs& f, int gw, uint32_t lrec, uint32_t sring,
+                                           uint32_t sfull, uint32_t sfree, int lane) {
     constexpr int32_t kPastEnd = INT32_MIN;
-    // argument fields in registers: every cp.async below clobbers memory
-    const bf16* const kp = f.t.kp;
-    const bf16* const vp = f.t.vp;
-    const bf16* const qp = f.t.q;
     const int32_t* const r2t = f.t.r2t;
     const int32_t* const members = f.t.members;
     const int32_t* const seq_lens = f.t.seq_lens;
     const int64_t ld = f.t.ld;
     uint32_t* const err = f.t.err;
-    const int Hq = f.t.Hq, Hkv = f.t.Hkv, G = f.t.G;
-    const int64_t num_slots = f.t.num_slots;
     const DecItem* const pieces = f.narrow;
     const int n_narrow = f.n_narrow;
     uint32_t* const sched = f.sched;
-    // streamed K/V rows are read once: evict them from L2 first, which keeps
-    // the code, the tables and the partial rows there across calls
-    const uint64_t kv_pol = l2_evict_first_policy();
-
-    // next-piece pipeline: 0 take a number, 1 number in flight (lane 0),
-    // 2 record in flight, 3 members / seq_len in flight, 4 ready;
-    // `none` once the counter ran out
-    int nx_id = 0, nx_stage = 0, taken = 0;
-    int nx_row = 0, nx_b = 0, nx_e = 0, nx_h = 0, nx_mb = 0, nx_nm = 0, nx_pb = 0, nx_mem = 0, nx_len = 0;
-    bool none = false;
-    auto load_record = [&]() {
-        if (nx_id < n_narrow) {
-            const int4* rp = reinterpret_cast<const int4*>(pieces + nx_id);
-            const int4 x = __ldg(rp), y = __ldg(rp + 1);
-            nx_row = x.x;
-            nx_b = x.y;
-            nx_e = x.z;
-            nx_h = x.w;
-            nx_mb = y.x;
-            nx_nm = y.y;
-            nx_pb = y.z;
-        } else {
-            none = true;
-        }
-    };
-    // the launch piece: its record is waited for once; its seq_len and
-    // members are loaded now and used only when its first step is issued
     const bool launch = gw >= 0 && gw < f.n_init;
-    int lp_len = 0, lp_mem = 0, lp_b = 0, lp_e = 0, lp_pb = 0, lp_rows = 0;
-    if (launch) {
-        nx_id = gw;
-        load_record();
-        nx_stage = 3;
-        lp_len = __ldg(seq_lens + nx_row);
-        lp_mem = lane < nx_nm * G ? __ldg(members + nx_mb + lane / G) : 0;
-        lp_b = nx_b;
-        lp_e = nx_e;
-        lp_pb = nx_pb;
-        lp_rows = nx_nm * G;
-    }
-    auto advance = [&]() {
-        if (none) return;
-        if (nx_stage == 0) {
-            if (lane == 0) taken = (int)atomicAdd(sched, 1u);
-            nx_stage = 1;
-        } else if (nx_stage == 1) {
-            nx_id = __shfl_sync(0xffffffffu, taken, 0);
-            load_record();
-            nx_stage = 2;
-        } else if (nx_stage == 2) {
-            nx_len = __ldg(seq_lens + nx_row);
-            nx_mem = lane < nx_nm * G ? __ldg(members + nx_mb + lane / G) : 0;
-            nx_stage = 3;
-        } else if (nx_stage == 3) {
-            nx_stage = 4;
-        }
-    };
-    if (launch) nx_stage = 4;
-    bool launch_entry_pending = launch;
-
-    // slot cursor over the current piece
-    bool have = false, done = false;
-    bool prologue = true;   // the first kQD lookups: no grab-ahead, which would put the next piece's
-                            // dependent loads (counter, record, members) before the first step
-    int row = 0, e = 0, h = 0, sp = 0, nlook = 0;
-    auto look_up = [&]() {
+    bool timed_out = false;
+    int nlook = 0;
+    // one ring entry: wait for it to be free, fill it, arm its barrier
+    auto entry = [&](int kvh, int row, int p0, int e, int flags, int cm, int pb, int nh, int nm, int mem) {
         const int ent = nlook & (kSQ - 1);
         const uint32_t eb = sring + ent * kSlotEntry;
-        int kvh = -1, p0 = 0, flags = 0;
-        if (!done && (!have || sp >= e)) {
-            while (!none && nx_stage < 4) advance();
-            if (none) {
-                have = false;
-                done = true;
-            } else {
-                have = true;
-                row = nx_row;
-                sp = nx_b;
-                e = nx_e;
-                h = nx_h;
-                flags = kFirst;
-                if (launch_entry_pending) {
-                    launch_entry_pending = false;   // fields come from lp_* when step 0 is issued
-                } else {
-                    int cm = nx_e;
-                    if (nx_e > nx_len) {   // planned beyond seq_len: mask the excess, flag it
-                        if (lane == 0) atomicOr(err, 2u);
-                        cm = nx_len > nx_b ? nx_len : nx_b;
-                    }
-                    if (lane == 0) {
-                        st_shared_s32(eb + kEntCm, cm);
-                        st_shared_s32(eb + kEntPb, nx_pb);
-                        st_shared_s32(eb + kEntRows, nx_nm * G);
-                    }
-                    if (lane < 8) st_shared_s32(eb + kEntMem + 4 * lane, nx_mem);
-                }
-                nx_stage = 0;
-            }
+        if (!timed_out && !mbar_wait(sfree + 8 * ent, ((nlook / kSQ) & 1) ^ 1)) {
+            atomicOr(err, 4u);
+            timed_out = true;
         }
-        if (have && !done) {
-            kvh = h;
-            p0 = sp;
-            const int p = sp + lane;
-            if (lane < kNP) {
-                if (p < e)
-                    cp_async4(eb + lane * 4, r2t + (int64_t)row * ld + p);
-                else
-                    st_shared_s32(eb + lane * 4, kPastEnd);
-            }
-            sp += kNP;
+        if (timed_out) return;
+        if (lane < kNP) {
+            const int p = p0 + lane;
+            if (kvh >= 0 && p < e)
+                cp_async4(eb + lane * 4, r2t + (int64_t)row * ld + p);
+            else
+                st_shared_s32(eb + lane * 4, kPastEnd);
         }
         if (lane == 0) {
             st_shared_s32(eb + kEntKvh, kvh);
             st_shared_s32(eb + kEntP0, p0);
             st_shared_s32(eb + kEntFlags, flags);
-        }
-        ++nlook;
-        // Take the next number only near the end of the current piece: the
-        // counter then runs dry only when the work does, and CTAs that join
-        // late (tile CTAs) still find pieces.
-        if (!prologue && (nx_stage != 0 || !have || done || (e - sp + kNP - 1) / kNP <= kGrabAhead)) advance();
-    };
-    // one cp.async group per step's lookup: the first step waits for its
-    // own slots only
-#pragma unroll 1
-    for (int k = 0; k < kQD; ++k) {
-        look_up();
-        cp_async_commit();
-    }
-    prologue = false;
-
-    bool timed_out = false;
-    int nq = 0;   // pieces started (Q slot uses)
-    for (int r = 0;; ++r) {
-        // the lookup of step r was committed kQD groups ago
-        cp_async_wait<kQD - 1>();
-        __syncwarp();
-        const int ent = r & (kSQ - 1);
-        const uint32_t eb = sring + ent * kSlotEntry;
-        const int kvh = ld_shared_s32(eb + kEntKvh);
-        const int flags = ld_shared_s32(eb + kEntFlags);
-        const int st = r % NS;
-        if (!timed_out && !mbar_wait_sleep(empty + 8 * st, ((r / NS) & 1) ^ 1)) {
-            atomicOr(err, 4u);
-            timed_out = true;
-        }
-        const uint32_t db = desc + st * 32;
-        if (kvh >= 0) {
-            int32_t sl = lane < kNP ? ld_shared_s32(eb + lane * 4) : kPastEnd;
-            if (sl == kPastEnd) {
-                sl = -1;
-            } else if (sl < 0 || sl >= num_slots) {
-                atomicOr(err, 1u);
-                sl = -1;
-            }
-            const uint32_t kd = ring + st * Lay::STAGE, vd = kd + Lay::TILEB;
-            if constexpr (F8) {
-                // FP8 rows of D bytes, [16 x D] tiles with swizzled chunks
-                constexpr int CPB = D / 16, RPB = 32 / CPB;
-                const int chb = lane % CPB;
-                const uint8_t* kp8 = reinterpret_cast<const uint8_t*>(kp);
-                const uint8_t* vp8 = reinterpret_cast<const uint8_t*>(vp);
-#pragma unroll
-                for (int k = 0; k < kNP / RPB; ++k) {
-                    const int rl = k * RPB + lane / CPB;
-                    const int32_t sr = __shfl_sync(0xffffffffu, sl, rl);
-                    const int64_t off = sr >= 0 ? ((int64_t)sr * Hkv + kvh) * D + chb * 16 : 0;
-                    cp_async16_pol(kd + fswz<D>(rl, chb), kp8 + off, sr >= 0, kv_pol);
-                    cp_async16_pol(vd + fswz<D>(rl, chb), vp8 + off, sr >= 0, kv_pol);
-                }
-            } else {
-                const int ch = lane % CPR;
-#pragma unroll
-                for (int k = 0; k < kNP / RPI; ++k) {
-                    const int rl = k * RPI + lane / CPR;
-                    const int32_t sr = __shfl_sync(0xffffffffu, sl, rl);
-                    const int64_t off = sr >= 0 ? ((int64_t)sr * Hkv + kvh) * D + ch * 8 : 0;
-                    cp_async16_pol(kd + swz<D>(rl, ch), kp + off, sr >= 0, kv_pol);
-                    cp_async16_pol(vd + swz<D>(rl, ch), vp + off, sr >= 0, kv_pol);
-                }
-            }
-            const int ch = lane % CPR;
             if (flags & kFirst) {
-                // the piece's query rows (at most 8) into Q slot nq & 1, swizzled
-                const int qs = nq & 1;
-                if (!timed_out && !mbar_wait_sleep(qempty + 8 * qs, ((nq >> 1) & 1) ^ 1)) {
-                    atomicOr(err, 4u);
-                    timed_out = true;
-                }
-                const bool lp = launch && r == 0;   // the launch piece's first step
-                int cm, pb, rows;
-                if (lp) {
-                    cm = lp_e;
-                    if (lp_e > lp_len) {
-                        if (lane == 0) atomicOr(err, 2u);
-                        cm = lp_len > lp_b ? lp_len : lp_b;
-                    }
-                    pb = lp_pb;
-                    rows = lp_rows;
-                } else {
-                    cm = ld_shared_s32(eb + kEntCm);
-                    pb = ld_shared_s32(eb + kEntPb);
-                    rows = ld_shared_s32(eb + kEntRows);
-                }
-                const uint32_t qd = qbuf + qs * Lay::QSLOT;
-#pragma unroll
-                for (int k = 0; k < 8 / RPI; ++k) {
-                    const int rq = k * RPI + lane / CPR;
-                    const bool ok = rq < rows;
-                    const int lpm = __shfl_sync(0xffffffffu, lp_mem, rq);
-                    const int mem = lp ? lpm : ld_shared_s32(eb + kEntMem + 4 * rq);
-                    const bf16* src = ok ? qp + ((int64_t)mem * Hq + kvh * G + rq % G) * D + ch * 8 : qp;
-                    cp_async16(qd + swz<D>(rq, ch), src, ok);
-                }
-                if (lane == 0) {
-                    st_shared_s32(db + kDescCm, cm);
-                    st_shared_s32(db + kDescPb, pb);
-                    st_shared_s32(db + kDescRows, rows);
-                    st_shared_s32(db + kDescQ, qs);
-                }
-                ++nq;
+                st_shared_s32(eb + kEntCm, cm);
+                st_shared_s32(eb + kEntPb, pb);
+                st_shared_s32(eb + kEntNh, nh);
+                st_shared_s32(eb + kEntNm, nm);
             }
         }
-        if (lane == 0) {
-            st_shared_s32(db + kDescP0, ld_shared_s32(eb + kEntP0));
-            st_shared_s32(db + kDescFlags, kvh >= 0 ? flags : kEnd);
-        }
-        cp_async_arrive_noinc(full + 8 * st);    // each lane, when its copies have landed
+        if ((flags & kFirst) && lane < 8) st_shared_s32(eb + kEntMem + 4 * lane, mem);
+        cp_async_arrive_noinc(sfull + 8 * ent);   // each lane, once its lookups have landed
         __syncwarp();
-        if (lane == 0) mbar_arrive(full + 8 * st);   // releases the descriptor
-        if (kvh < 0) break;
-        __syncwarp();   // every lane has read entry r before it is refilled
-        look_up();      // step r + kQD
-        cp_async_commit();
+        if (lane == 0) mbar_arrive(sfull + 8 * ent);   // the fields
+        ++nlook;
+    };
+    bool first_piece = true;
+    for (;;) {
+        int row, b, e, kvh, mb, nm, pb, nh, mem;
+        if (first_piece && launch) {
+            row = ld_shared_s32(lrec); b = ld_shared_s32(lrec + 4); e = ld_shared_s32(lrec + 8);
+            kvh = ld_shared_s32(lrec + 12); mb = ld_shared_s32(lrec + 16); nm = ld_shared_s32(lrec + 20);
+            pb = ld_shared_s32(lrec + 24); nh = ld_shared_s32(lrec + 28);
+            mem = lane < 8 ? ld_shared_s32(lrec + 32 + 4 * lane) : 0;
+        } else {
+            int taken = 0;
+            if (lane == 0) taken = (int)atomicAdd(sched, 1u);
+            taken = __shfl_sync(0xffffffffu, taken, 0);
+            if (taken >= n_narrow) break;
+            const int4* rp = reinterpret_cast<const int4*>(pieces + taken);
+            const int4 x = __ldg(rp), y = __ldg(rp + 1);
+            row = x.x; b = x.y; e = x.z; kvh = x.w;
+            mb = y.x; nm = y.y; pb = y.z; nh = y.w;
+            mem = lane < nm ? __ldg(members + mb + lane) : 0;
+        }
+        first_piece = false;
+        const int len = __ldg(seq_lens + row);
+        int cm = e;
+        if (e > len) {   // planned beyond seq_len: mask the excess, flag it
+            if (lane == 0) atomicOr(err, 2u);
+            cm = len > b ? len : b;
+        }
+        for (int sp = b; sp < e; sp += kNP)
+            entry(kvh, row, sp, e, sp == b ? kFirst : 0, cm, pb, nh, nm, mem);
     }
+    entry(-1, 0, 0, 0, 0, 0, 0, 0, 0, 0);   // the end of the stream
     cp_async_wait<0>();
-    // The last producer to finish restores the counter for the next call
-    // (every producer has taken its last number by then).
+    // The last lookup warp to finish restores the counter for the next call
+    // (every CTA has taken its last number by then).
     if (lane == 0) {
-        const uint32_t total = gridDim.x * (uint32_t)kProducers;
-        if (atomicAdd(sched + 1, 1u) + 1 == total) {
+        if (atomicAdd(sched + 1, 1u) + 1 == gridDim.x) {
             sched[0] = (uint32_t)f.n_init;
             sched[1] = 0u;
             __threadfence();
@@ -454,27 +273,192 @@ __device__ __noinline__ void stream_producer(const FusedArgs& f, int gw, uint32_
 }
 
 // ---------------------------------------------------------------------------
-// Consumer: only shared memory in its loop (stages, descriptors, Q slots)
+// Producer warp p of kProducers
 // ---------------------------------------------------------------------------
-template <int D, int NS, bool F8 = false>
-__device__ __noinline__ void stream_consumer(const FusedArgs& f, uint32_t ring, uint32_t desc, uint32_t qbuf,
+// For each step (slot-ring entry, in order): waits for the entry and for the
+// ring stage to be free, zero-fills its rows without data (positions past
+// the piece's end, or slots outside the pool), arrives on the stage's FULL
+// barrier with its byte count and issues its bulk copies: lane t < 8 moves
+// row 8p + t of the stage (rows 0-15 the K rows of the step's 16 positions,
+// 16-31 the V rows).  Measured on GB300: one warp gets a bulk copy through
+// about every 100 cycles, so four warps share the stage's 32 row copies.
+// Producer 0 also writes the stage descriptor and, for a piece's first step,
+// copies its query rows into the Q slot once the consumers have released it.
+// The entry is freed once read.
+template <int D, bool F8>
+__device__ __noinline__ void stream_producer(const FusedArgs& f, int pw, uint32_t ring, uint32_t sring,
+                                             uint32_t desc, uint32_t qbuf, uint32_t full, uint32_t empty,
+                                             uint32_t qempty, uint32_t sfull, uint32_t sfree, int lane) {
+    using Lay = FusedLayout<D, F8>;
+    constexpr int NS = Lay::NSF;
+    constexpr int ES = Lay::ES;
+    constexpr int32_t kPastEnd = INT32_MIN;
+    constexpr int RPW = 2 * kNP / kProducers;   // rows per producer warp and step
+    // argument fields in registers: every asm below clobbers memory
+    const uint8_t* const kp = reinterpret_cast<const uint8_t*>(f.t.kp);
+    const uint8_t* const vp = reinterpret_cast<const uint8_t*>(f.t.vp);
+    const bf16* const qp = f.t.q;
+    uint32_t* const err = f.t.err;
+    const int Hq = f.t.Hq, Hkv = f.t.Hkv, G = f.t.G;
+    const int64_t num_slots = f.t.num_slots;
+    // streamed K/V rows are read once: evict them from L2 first, which keeps
+    // the code, the tables and the partial rows there across calls
+    const uint64_t kv_pol = l2_evict_first_policy();
+    const bool lead = pw == 0;
+    const int idx = pw * RPW + lane;          // this lane's row of a stage (lane < RPW)
+    const bool mine = lane < RPW;
+    const int tok = idx & (kNP - 1);
+
+    // After a wait gives up, the producer stops touching the ring and its
+    // barriers (the consumers' and the lookup warp's own bounded waits end
+    // their loops).
+    bool timed_out = false;
+    int nq = 0;            // pieces started (Q slot uses)
+    int cur_nh = 0;        // KV heads of the piece being issued
+    int last_armed = -1;   // last step whose FULL phase this warp's copies complete
+    int last_arrived = -1; // last step that arrived on a FULL barrier (armed, or the end marker)
+    for (int r = 0; !timed_out; ++r) {
+        const int ent = r & (kSQ - 1);
+        const uint32_t eb = sring + ent * kSlotEntry;
+        if (!mbar_wait(sfull + 8 * ent, (uint32_t)(r / kSQ) & 1u)) {
+            atomicOr(err, 4u);
+            timed_out = true;
+            break;
+        }
+        const int kvh = ld_shared_s32(eb + kEntKvh);
+        const int flags = ld_shared_s32(eb + kEntFlags);
+        const int st = r % NS;
+        if (!mbar_wait(empty + 8 * st, ((r / NS) & 1) ^ 1)) {
+            atomicOr(err, 4u);
+            timed_out = true;
+            break;
+        }
+        const uint32_t db = desc + st * 32;
+        const uint32_t fb = full + 8 * st;
+        const uint32_t sb = ring + st * Lay::STAGE;
+        if (kvh < 0) {
+            if (lane == 0) {
+                if (lead) st_shared_s32(db + kDescFlags, kEnd);
+                mbar_arrive(fb);
+            }
+            last_arrived = r;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(sfree + 8 * ent);
+            break;
+        }
+        const bool first = (flags & kFirst) != 0;
+        int nm = 0;
+        if (first) {
+            cur_nh = ld_shared_s32(eb + kEntNh);
+            nm = ld_shared_s32(eb + kEntNm);
+            if (lead && !mbar_wait(qempty, (nq & 1) ^ 1)) {
+                atomicOr(err, 4u);
+                timed_out = true;
+                break;
+            }
+        }
+        const uint32_t rowb = (uint32_t)(cur_nh * D * ES);
+        int32_t sl = mine ? ld_shared_s32(eb + tok * 4) : kPastEnd;
+        bool ok = mine && sl != kPastEnd;
+        if (ok && (sl < 0 || sl >= num_slots)) {
+            if (idx < kNP) atomicOr(err, 1u);
+            ok = false;
+        }
+        const uint32_t vmask = __ballot_sync(0xffffffffu, ok);
+        // rows without data are zeroed: their scores are masked, and a zero V
+        // row keeps 0 * V finite
+        uint32_t zm = ~vmask & ((1u << RPW) - 1u);
+        if (zm) {
+            while (zm) {
+                const int b = __ffs(zm) - 1;
+                zm &= zm - 1;
+                const int zi = pw * RPW + b;
+                const uint32_t zr = sb + (uint32_t)((zi >> 4) * kNP + (zi & (kNP - 1))) * Lay::PITCH;
+                for (uint32_t c = (uint32_t)lane * 16u; c < rowb; c += 512u) st_shared_v4(zr + c, 0u, 0u, 0u, 0u);
+            }
+            // the stage's next use writes these rows through the async proxy
+            fence_proxy_async_smem();
+        }
+        uint32_t bytes = (uint32_t)__popc(vmask) * rowb;
+        // the lead's first step also carries the piece's query rows: member
+        // i's G query heads of KV head kvh + hh are G consecutive rows of q
+        const int nqc = (first && lead) ? nm * cur_nh : 0;   // query copies (at most 64)
+        bytes += (uint32_t)(nqc * G * D * 2);
+        if (lead && lane == 0) {
+            st_shared_s32(db + kDescP0, ld_shared_s32(eb + kEntP0));
+            st_shared_s32(db + kDescFlags, flags);
+            if (first) {
+                st_shared_s32(db + kDescCm, ld_shared_s32(eb + kEntCm));
+                st_shared_s32(db + kDescPb, ld_shared_s32(eb + kEntPb));
+                st_shared_s32(db + kDescRows, nm * G);
+                st_shared_s32(db + kDescNh, cur_nh);
+            }
+        }
+        int qmem0 = 0, qmem1 = 0;   // members of this lane's query copies (k = lane, lane + 32)
+        if (nqc > 0) {
+            const int k0 = lane, k1 = lane + 32;
+            if (k0 < nqc) qmem0 = ld_shared_s32(eb + kEntMem + 4 * (k0 / cur_nh));
+            if (k1 < nqc) qmem1 = ld_shared_s32(eb + kEntMem + 4 * (k1 / cur_nh));
+        }
+        __syncwarp();
+        if (lane == 0) mbar_expect_tx(fb, bytes);   // the arrival, plus the bytes the copies complete
+        __syncwarp();
+        if (ok)
+            bulk_g2s_pol(sb + (uint32_t)((idx >> 4) * kNP + tok) * Lay::PITCH,
+                         (idx < kNP ? kp : vp) + ((int64_t)sl * Hkv + kvh) * (D * ES), rowb, fb, kv_pol);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int k = lane + 32 * j;
+            if (k < nqc) {
+                const int qi = k / cur_nh, qh = k - qi * cur_nh;
+                bulk_g2s(qbuf + (uint32_t)((qh * 8 + qi * G) * D * 2),
+                         qp + ((int64_t)(j ? qmem1 : qmem0) * Hq + (kvh + qh) * G) * D, (uint32_t)(G * D * 2), fb);
+            }
+        }
+        if (first && lead) ++nq;
+        last_armed = last_arrived = r;
+        __syncwarp();   // every lane has read the entry
+        if (lane == 0) mbar_arrive(sfree + 8 * ent);
+    }
+    // This warp's bulk copies have landed before it leaves (normally long
+    // since: the consumers read them): an armed phase completes only when
+    // they have.  Only steps whose stage no later step arrived on are waited
+    // for (a later phase of the same stage would flip the parity back).
+    // Bounded waits.
+    const int s0 = last_arrived - NS + 1 > 0 ? last_arrived - NS + 1 : 0;
+    for (int s = s0; s <= last_armed; ++s)
+        if (!mbar_wait(full + 8 * (s % NS), (uint32_t)(s / NS) & 1u)) atomicOr(err, 4u);
+}
+
+// ---------------------------------------------------------------------------
+// Consumer warp c: KV head kvh + c of each piece (idle, but keeping the
+// barrier counts, when the piece has fewer heads); only shared memory in its
+// loop (stages, descriptors, Q slot)
+// ---------------------------------------------------------------------------
+template <int D, bool F8>
+__device__ __noinline__ void stream_consumer(const FusedArgs& f, int c, uint32_t ring, uint32_t desc, uint32_t qbuf,
                                              uint32_t full, uint32_t empty, uint32_t qempty, int lane) {
     using Lay = FusedLayout<D, F8>;
+    constexpr int NS = Lay::NSF;
+    constexpr int P = Lay::PITCH;
     constexpr int MT = D / 16;                 // m-tiles of O^T
     const int g = lane >> 2, t = lane & 3;
     float* const po = f.t.po;
     float* const plse = f.t.plse;
     uint32_t* const err = f.t.err;
+    const int G = f.t.G;
     // FP8 pools: the K scale goes into the score scale, the V scale into the
     // final normalisation (both are per tensor, so they factor out)
     const float sc = F8 ? f.t.scale_log2 * f.t.k_scale : f.t.scale_log2;
     const float vsc = F8 ? f.t.v_scale : 1.f;
+    const uint32_t hoff = (uint32_t)(c * D * Lay::ES);   // this warp's head within a row
+    const uint32_t qb = qbuf + (uint32_t)(c * 8 * D * 2);   // this warp's head in the Q slot
 
     uint32_t qcur[D / 8];
     float o[MT][4];
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    bool have = false;
-    int cur_pb = 0, cur_rows = 0, cm = 0;
+    bool have = false, active = false;
+    int cur_pb = 0, cur_rows = 0, cur_nh = 0, cm = 0;
     auto finish_item = [&]() {
         float s0 = l0, s1 = l1;
 #pragma unroll
@@ -484,75 +468,80 @@ __device__ __noinline__ void stream_consumer(const FusedArgs& f, uint32_t ring, 
         }
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-            const int r = 2 * t + hh;
+            const int r = 2 * t + hh;   // query row of this head: member r / G, query head r % G
             if (r < cur_rows) {
+                const int64_t prow = (int64_t)cur_pb + ((r / G) * cur_nh + c) * G + r % G;
                 const float ll = hh ? s1 : s0, mm = hh ? m1 : m0;
                 const float inv = ll > 0.f ? vsc / ll : 0.f;
                 if constexpr (F8) {
                     // m-tile i rows g, g + 8 stand for d = (D/8) g + 2i, + 1
-                    float* dst = po + ((int64_t)cur_pb + r) * D + (D / 8) * g;
+                    float* dst = po + prow * D + (D / 8) * g;
 #pragma unroll
                     for (int i = 0; i < MT; ++i)
                         *reinterpret_cast<float2*>(dst + 2 * i) = make_float2(o[i][hh] * inv, o[i][2 + hh] * inv);
                 } else {
-                    float* dst = po + ((int64_t)cur_pb + r) * D + g;
+                    float* dst = po + prow * D + g;
 #pragma unroll
                     for (int i = 0; i < MT; ++i) {
                         dst[16 * i] = o[i][hh] * inv;
                         dst[16 * i + 8] = o[i][2 + hh] * inv;
                     }
                 }
-                if (g == 0) plse[(int64_t)cur_pb + r] = ll > 0.f ? (mm + log2f(ll)) * kLn2 : -INFINITY;
+                if (g == 0) plse[prow] = ll > 0.f ? (mm + log2f(ll)) * kLn2 : -INFINITY;
             }
         }
     };
 
-    bool timed_out = false;
-    int nq = 0;
-    for (int c = 0;; ++c) {
-        const int st = c % NS;
-        if (!timed_out && !mbar_wait_sleep(full + 8 * st, (c / NS) & 1)) {
+    for (int cs = 0;; ++cs) {
+        const int st = cs % NS;
+        if (!mbar_wait(full + 8 * st, (cs / NS) & 1)) {
             atomicOr(err, 4u);
-            timed_out = true;
+            break;
         }
         const uint32_t db = desc + st * 32;
         const int cp0 = ld_shared_s32(db + kDescP0), flags = ld_shared_s32(db + kDescFlags);
-        if ((flags & kEnd) || timed_out) break;
+        if (flags & kEnd) break;
         if (flags & kFirst) {
-            if (have) finish_item();
+            if (have && active) finish_item();
             have = true;
             cm = ld_shared_s32(db + kDescCm);
             cur_pb = ld_shared_s32(db + kDescPb);
             cur_rows = ld_shared_s32(db + kDescRows);
-            const int qs = ld_shared_s32(db + kDescQ);
-            // Q^T fragments: row g (the N index), k-step ks -> chunks 2ks, 2ks+1
-            const uint32_t qb = qbuf + qs * Lay::QSLOT;
-            if constexpr (F8) {
-                // row g's elements (D/4) t .. (D/4) t + D/4 - 1, in order:
-                // k-step ks takes elements 4 ks .. 4 ks + 3 of the run (the
-                // order of the lane's K codes below), as f16
+            cur_nh = ld_shared_s32(db + kDescNh);
+            active = c < cur_nh;
+            if (active) {
+                // Q^T fragments: row g (the N index), k-step ks -> chunks 2ks, 2ks+1
+                if constexpr (F8) {
+                    // row g's elements (D/4) t .. (D/4) t + D/4 - 1, in order:
+                    // k-step ks takes elements 4 ks .. 4 ks + 3 of the run (the
+                    // order of the lane's K codes below), as f16
 #pragma unroll
-                for (int j = 0; j < D / 32; ++j) lds128(qb + swz<D>(g, (D / 32) * t + j), qcur + 4 * j);
+                    for (int j = 0; j < D / 32; ++j) lds128(qb + g * (D * 2) + ((D / 32) * t + j) * 16, qcur + 4 * j);
 #pragma unroll
-                for (int k = 0; k < D / 8; ++k) qcur[k] = bf16x2_to_f16x2(qcur[k]);
-            } else {
+                    for (int k = 0; k < D / 8; ++k) qcur[k] = bf16x2_to_f16x2(qcur[k]);
+                } else {
 #pragma unroll
-                for (int kp2 = 0; kp2 < D / 32; ++kp2) {
-                    const int rq = lane & 7, chunk = 4 * kp2 + (lane >> 3);
-                    ldsm_x4(qb + swz<D>(rq, chunk), qcur[4 * kp2], qcur[4 * kp2 + 1], qcur[4 * kp2 + 2],
-                            qcur[4 * kp2 + 3]);
+                    for (int kp2 = 0; kp2 < D / 32; ++kp2) {
+                        const int rq = lane & 7, chunk = 4 * kp2 + (lane >> 3);
+                        ldsm_x4(qb + rq * (D * 2) + chunk * 16, qcur[4 * kp2], qcur[4 * kp2 + 1], qcur[4 * kp2 + 2],
+                                qcur[4 * kp2 + 3]);
+                    }
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(qempty + 8 * qs);   // the Q slot may be refilled
-            ++nq;
+            if (lane == 0) mbar_arrive(qempty);   // the Q slot may be refilled
 #pragma unroll
             for (int i = 0; i < MT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
             m0 = m1 = -INFINITY;
             l0 = l1 = 0.f;
         }
+        if (!active) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty + 8 * st);
+            continue;
+        }
         // ---- one step of the current piece at positions cp0 .. cp0+15
-        const uint32_t kb = ring + st * Lay::STAGE, vb = kb + Lay::TILEB;
+        const uint32_t kb = ring + st * Lay::STAGE + hoff, vb = kb + kNP * P;
         // FP8 stages go straight from the codes into MMA fragments.  The d
         // index of S^T = K Q^T is contracted, so lane (g, t) takes the D/4
         // codes (D/4) t .. of K rows g and g + 8, in order, as its k-slots
@@ -568,15 +557,15 @@ __device__ __noinline__ void stream_consumer(const FusedArgs& f, uint32_t ring, 
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
 #pragma unroll
-                for (int j = 0; j < D / 64; ++j) lds128(kb + fswz<D>(g + 8 * h, (D / 64) * t + j), kw[h] + 4 * j);
+                for (int j = 0; j < D / 64; ++j) lds128(kb + (g + 8 * h) * P + ((D / 64) * t + j) * 16, kw[h] + 4 * j);
             }
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int r = 2 * t + (e & 1) + 8 * (e >> 1);
                 if constexpr (D == 128)
-                    lds128(vb + fswz<D>(r, g), vw[e]);
+                    lds128(vb + r * P + 16 * g, vw[e]);
                 else
-                    lds64(vb + fswz<D>(r, g >> 1) + 8 * (g & 1), vw[e]);
+                    lds64(vb + r * P + 8 * g, vw[e]);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(empty + 8 * st);   // the stage may be refilled
@@ -592,7 +581,7 @@ __device__ __noinline__ void stream_consumer(const FusedArgs& f, uint32_t ring, 
                 mma16816_f16((ks & 1) ? s2 : s, ka, qcur[2 * ks], qcur[2 * ks + 1]);
             } else {
                 const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
-                ldsm_x4(kb + swz<D>(row, 2 * ks + (lane >> 4)), ka[0], ka[1], ka[2], ka[3]);
+                ldsm_x4(kb + row * P + (2 * ks + (lane >> 4)) * 16, ka[0], ka[1], ka[2], ka[3]);
                 mma16816((ks & 1) ? s2 : s, ka, qcur[2 * ks], qcur[2 * ks + 1]);
             }
         }
@@ -646,14 +635,16 @@ __device__ __noinline__ void stream_consumer(const FusedArgs& f, uint32_t ring, 
                 mma16816_f16(o[i], va, pb0, pb1);
             } else {
                 const int row = (lane & 7) + (lane >> 4) * 8;
-                ldsm_x4_t(vb + swz<D>(row, 2 * i + ((lane >> 3) & 1)), va[0], va[1], va[2], va[3]);
+                ldsm_x4_t(vb + row * P + (2 * i + ((lane >> 3) & 1)) * 16, va[0], va[1], va[2], va[3]);
                 mma16816(o[i], va, pb0, pb1);
             }
         }
-        __syncwarp();
-        if (!F8 && lane == 0) mbar_arrive(empty + 8 * st);   // the stage may be refilled
+        if constexpr (!F8) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty + 8 * st);   // the stage may be refilled
+        }
     }
-    if (have) finish_item();
+    if (have && active) finish_item();
 }
 
 // ---------------------------------------------------------------------------
@@ -695,19 +686,20 @@ __global__ void __maxnreg__(128) decode_fused_kernel(const __grid_constant__ Fus
     const bool tiles = w1 > w0;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + TL::OFF_TMEM);
     int* info = reinterpret_cast<int*>(sm + TL::OFF_INFO);
+    constexpr int NSF = Lay::NSF;
     const uint32_t sbar = smem_u32(sm + Lay::OFF_SBAR);
-    auto full_of = [&](int c) { return sbar + (uint32_t)(c * (2 * kNSF + 2)) * 8; };
-    auto empty_of = [&](int c) { return sbar + (uint32_t)(c * (2 * kNSF + 2) + kNSF) * 8; };
-    auto qempty_of = [&](int c) { return sbar + (uint32_t)(c * (2 * kNSF + 2) + 2 * kNSF) * 8; };
+    const uint32_t sfull = sbar, sempty = sbar + 8 * NSF, sqempty = sbar + 16 * NSF;
+    const uint32_t slfull = sqempty + 8, slfree = slfull + 8 * kSQ;
     if (tid == 0) {
         if (tiles) tc_init_barriers<TC>(smem_u32(sm + TL::OFF_BAR));
-        for (int c = 0; c < kConsumers; ++c) {
-            for (int s = 0; s < kNSF; ++s) {
-                mbar_init(full_of(c) + 8 * s, 33);    // the producer's 32 lanes + its descriptor release
-                mbar_init(empty_of(c) + 8 * s, 1);    // the consumer
-            }
-            mbar_init(qempty_of(c), 1);
-            mbar_init(qempty_of(c) + 8, 1);
+        for (int s = 0; s < NSF; ++s) {
+            mbar_init(sfull + 8 * s, kProducers);   // every producer's arrival (with its bytes)
+            mbar_init(sempty + 8 * s, kHB);         // every consumer warp
+        }
+        mbar_init(sqempty, kHB);
+        for (int e = 0; e < kSQ; ++e) {
+            mbar_init(slfull + 8 * e, 33);          // the lookup lanes' cp.async + the fields
+            mbar_init(slfree + 8 * e, kProducers);  // every producer
         }
         mbar_fence_init();
     }
@@ -720,9 +712,19 @@ __global__ void __maxnreg__(128) decode_fused_kernel(const __grid_constant__ Fus
     tc_fence_after();
     // the first records this CTA reads (plan tables) into L1 while waiting
     if (tiles && tid == 0) prefetch_l1(f.t.items + w0);
-    if (!tiles && warp >= kFirstProducer && warp < kFirstConsumer && lane == 0) {
-        const int gw = ((int)blockIdx.x - f.n_tile_ctas) * kConsumers + (warp - kFirstProducer);
-        if (gw >= 0 && gw < f.n_init) prefetch_l1(f.narrow + gw);
+    // a streaming CTA's launch piece: its record and members (plan tables)
+    // into shared memory while the previous kernel finishes
+    const int gw = !tiles && (int)blockIdx.x >= f.n_tile_ctas ? (int)blockIdx.x - f.n_tile_ctas : -1;
+    const uint32_t lrec = smem_u32(sm + Lay::OFF_LREC);
+    if (warp == kLookup && gw >= 0 && gw < f.n_init) {
+        const int4* rp = reinterpret_cast<const int4*>(f.narrow + gw);
+        const int4 x = __ldg(rp), y = __ldg(rp + 1);
+        if (lane == 0) {
+            st_shared_v4(lrec, (uint32_t)x.x, (uint32_t)x.y, (uint32_t)x.z, (uint32_t)x.w);
+            st_shared_v4(lrec + 16, (uint32_t)y.x, (uint32_t)y.y, (uint32_t)y.z, (uint32_t)y.w);
+        }
+        if (lane < 8) st_shared_s32(lrec + 32 + 4 * lane, lane < y.y ? __ldg(f.t.members + y.x + lane) : 0);
+        __syncwarp();
     }
     // everything the previous kernel wrote is visible after this wait; the
     // merge launch may be scheduled from now on (it waits for this grid)
@@ -730,10 +732,10 @@ __global__ void __maxnreg__(128) decode_fused_kernel(const __grid_constant__ Fus
     grid_dep_launch();
 
     constexpr int kStreamGate = 3;   // named barrier: tile roles done -> streaming may start
-    constexpr int kTileWarps = TC::kThreads / 32;   // softmax, MMA, gather team (incl. the producers)
+    constexpr int kTileWarps = TC::kThreads / 32;   // softmax, MMA, gather team
     if (tiles && warp < kTileWarps) {
-        // the tile roles; the producer warps are part of the gather team and
-        // go on to stream once the CTA's tiles are done
+        // the tile roles; their warps 2-10 go on to stream (lookup,
+        // producers, four of the consumers) once the CTA's tiles are done
         const uint32_t tbase = *tslot;
         TcState st{0u, 0u, false};
         for (int w = w0; w < w1; ++w) {
@@ -749,28 +751,16 @@ __global__ void __maxnreg__(128) decode_fused_kernel(const __grid_constant__ Fus
     }
     // streaming warps of CTAs with tiles start once the tiles are done
     if (tiles && warp >= kTileWarps) named_bar(kStreamGate, kFusedThreads);
-    if (warp >= kFirstProducer && warp < kFirstConsumer) {
-        const int c = warp - kFirstProducer;
-        const int gws = (int)blockIdx.x >= f.n_tile_ctas ? ((int)blockIdx.x - f.n_tile_ctas) * kConsumers + c : -1;
-        const uint32_t sring = smem_u32(sm + Lay::OFF_SLOT + c * Lay::SLOTW);
-        const uint32_t desc = smem_u32(sm + Lay::OFF_DESC + c * kNSF * 32);
-        const uint32_t qb = smem_u32(sm + Lay::OFF_Q + c * 2 * Lay::QSLOT);
-        if (tiles)
-            stream_producer<D, kNS, F8>(f, gws, smem_u32(sm + Lay::OFF_RING + c * Lay::RING), sring, desc, qb,
-                                        full_of(c), empty_of(c), qempty_of(c), lane);
-        else
-            stream_producer<D, kNSF, F8>(f, gws, smem_u32(sm + c * Lay::RING_F), sring, desc, qb, full_of(c),
-                                         empty_of(c), qempty_of(c), lane);
+    const uint32_t ring = smem_u32(sm + Lay::OFF_RING), qb = smem_u32(sm + Lay::OFF_Q);
+    const uint32_t desc = smem_u32(sm + Lay::OFF_DESC);
+    const uint32_t sring = smem_u32(sm + Lay::OFF_SLOT);
+    if (warp == kLookup) {
+        stream_lookup<D, F8>(f, gw, lrec, sring, slfull, slfree, lane);
+    } else if (warp >= kFirstProducer && warp < kFirstConsumer) {
+        stream_producer<D, F8>(f, warp - kFirstProducer, ring, sring, desc, qb, sfull, sempty, sqempty, slfull,
+                               slfree, lane);
     } else if (warp >= kFirstConsumer) {
-        const int c = warp - kFirstConsumer;
-        const uint32_t desc = smem_u32(sm + Lay::OFF_DESC + c * kNSF * 32);
-        const uint32_t qb = smem_u32(sm + Lay::OFF_Q + c * 2 * Lay::QSLOT);
-        if (tiles)
-            stream_consumer<D, kNS, F8>(f, smem_u32(sm + Lay::OFF_RING + c * Lay::RING), desc, qb, full_of(c),
-                                        empty_of(c), qempty_of(c), lane);
-        else
-            stream_consumer<D, kNSF, F8>(f, smem_u32(sm + c * Lay::RING_F), desc, qb, full_of(c), empty_of(c),
-                                         qempty_of(c), lane);
+        stream_consumer<D, F8>(f, warp - kFirstConsumer, ring, desc, qb, sfull, sempty, sqempty, lane);
     }
     tc_fence_before();
     __syncthreads();

@@ -349,6 +349,15 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
                  "l"(src), "r"(bytes), "r"(bar)
                  : "memory");
 }
+// bulk_g2s with an L2 cache policy.
+__device__ __forceinline__ void bulk_g2s_pol(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                             uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+        "%4;\n" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(pol)
+        : "memory");
+}
 // TMA gather of four 128-byte row pieces: rows r0..r3, columns x..x+63 (bf16)
 // of the 2-D tensor `tmap` (box 64 x 1, 128-byte swizzle) into 512
 // consecutive shared bytes at `dst`, completing `bar`'s transaction count.

@@ -12,9 +12,11 @@
 //     member blocks of up to 128 rows x chunks of whole 128-position
 //     multiples, dealt to a set of tile CTAs sized with the streaming work
 //     (cost model below);
-//   * every other segment (at most 8 rows: a request's own suffix, or a
-//     small group) is narrow: its positions, per KV head, are cut into
-//     pieces handed to the streaming warps at run time, longest first;
+//   * every other segment (at most 8 rows per KV head: a request's own
+//     suffix, or a small group) is narrow: its positions, for blocks of up
+//     to 8 consecutive KV heads (a token's K or V row of those heads is one
+//     contiguous run in the pool), are cut into pieces handed to the
+//     streaming CTAs at run time, longest first;
 //   * each item writes its rows' normalised partial O and LSE (fp32); the
 //     merge list of (request, KV head) names every partial row to combine.
 // The fp32 path runs the same items one CTA each.
@@ -117,19 +119,26 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
     const int32_t MBw = std::max(1, 128 / G);
     const int sms = sgl::query_num_sms(p->num_sms);
 
-    struct Unit {   // narrow work: one member block of a segment for one KV head
-        int32_t rep_row, b, e, kvh, mem_begin, n_mem;
+    // Narrow work streams in blocks of HP consecutive KV heads (one stream
+    // per CTA, one consumer warp per head); the fp32 kernel runs one item
+    // per CTA and takes one head per item.
+    const int32_t HP = p->dtype == SGL_DTYPE_F32 ? 1 : std::min<int32_t>(Hkv, sgl::kDecHeadBlock);
+    struct Unit {   // narrow work: one member block of a segment for a block of KV heads
+        int32_t rep_row, b, e, kvh, mem_begin, n_mem, nh;
     };
     std::vector<Unit> units;
-    int64_t units_n = 0;
+    int64_t units_n = 0;     // position-heads
+    int64_t units_pos = 0;   // positions (each for a block of heads)
     int64_t max_wide = 0;
     for (int32_t s = 0; s < nseg; ++s) {
         const int32_t b = g->seg_begin[s], e = g->seg_end[s];
         const int32_t m0 = g->seg_member_ptr[s], nmem = g->seg_member_ptr[s + 1] - m0;
         if (nmem <= MBn) {
-            for (int32_t h = 0; h < Hkv; ++h) {
-                units.push_back({g->seg_row[s], b, e, h, m0, nmem});
-                units_n += e - b;
+            for (int32_t h = 0; h < Hkv; h += HP) {
+                const int32_t nh = std::min(HP, Hkv - h);
+                units.push_back({g->seg_row[s], b, e, h, m0, nmem, nh});
+                units_n += (int64_t)(e - b) * nh;
+                units_pos += e - b;
             }
         } else {
             max_wide = std::max<int64_t>(max_wide, e - b);
@@ -141,8 +150,8 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
     // and instruction cache); the other CTAs stream from the start.  Chunk
     // length and tile CTA count come from a cost model of this kernel on
     // GB300 (measured): a tile costs ~2 us plus ~2.5 us per 128-position
-    // block; a streaming SM handles ~64 (d=128) position-heads per us after
-    // ~6 us of start-up.  The chunk length with the earliest estimated finish
+    // block; a streaming SM handles ~88 (d=128) position-heads per us after
+    // ~4 us of start-up.  The chunk length with the earliest estimated finish
     // is taken (tile CTAs at most half the CTAs).
     auto wide_items_for = [&](int64_t Cw) {
         int64_t n = 0;
@@ -153,7 +162,7 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
         }
         return n;
     };
-    const double rate = 64.0 * 128.0 / p->head_dim;   // streamed position-heads per us per SM
+    const double rate = 88.0 * 128.0 / p->head_dim;   // streamed position-heads per us per SM
     int64_t Cw = 128, n_tile_ctas = 0;
     if (max_wide > 0) {
         double best = 1e300;
@@ -165,7 +174,7 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
             const double tile_us = per * (2.0 + 2.5 * (double)c / 128.0);
             // streaming CTAs work from ~5 us; a tile CTA streams only what is
             // left when its tiles are done, which the estimate ignores
-            const double F = std::max(tile_us, 6.0 + (double)units_n /
+            const double F = std::max(tile_us, 4.0 + (double)units_n /
                                                      ((double)std::max<int64_t>(1, n_ctas - T) * rate));
             if (F < best) {
                 best = F;
@@ -185,29 +194,29 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
             for (int32_t blk = 0; blk < nblk; ++blk) {
                 const int32_t mb = blk * MBw, nm = std::min(MBw, nmem - mb);
                 for (int32_t h = 0; h < Hkv; ++h)
-                    wide.push_back({g->seg_row[s], (int32_t)cb, ce, h, m0 + mb, nm, 0, 0});
+                    wide.push_back({g->seg_row[s], (int32_t)cb, ce, h, m0 + mb, nm, 0, 1});
             }
         }
     }
 
-    // Narrow units are cut into pieces of at most Pmax positions (about one
-    // even share of a streaming consumer: measured on GB300, half that size
-    // cost ~1 us more per call in per-piece work, 0.6 of it starved the
-    // tail; a cut makes one more partial to merge),
-    // no piece shorter than one 16-position step unless its unit is, ordered
-    // longest first.  Each consumer of a streaming CTA starts on its own
-    // piece; the rest (and all work of tile CTAs' consumers, once their tiles
-    // are done) are handed out at run time from a counter, so SMs that stream
-    // faster take more.
-    const int64_t n_cons = (n_ctas - n_tile_ctas) * sgl::kDecNarrowWarps;
-    int64_t Pmax = (int64_t)std::ceil((double)units_n / (double)std::max<int64_t>(1, n_cons));
-    Pmax = std::min<int64_t>(1024, std::max<int64_t>(64, (Pmax + 15) / 16 * 16));
+    // Narrow units are cut into pieces of at most Pmax positions (about half
+    // an even share of a stream, so that the run-time counter can balance
+    // the tail; a cut makes one more partial to merge), no
+    // piece shorter than one 16-position step unless its unit is, ordered
+    // longest first.  Each streaming CTA starts on its own piece; the rest
+    // (and all work of tile CTAs' streams, once their tiles are done) are
+    // handed out at run time from a counter, so SMs that stream faster take
+    // more.
+    const int64_t n_cons = n_ctas - n_tile_ctas;
+    int64_t Pmax = (int64_t)std::ceil((double)units_pos / (double)std::max<int64_t>(1, 2 * n_cons));
+    Pmax = std::min<int64_t>(2048, std::max<int64_t>(32, (Pmax + 15) / 16 * 16));
     std::vector<sgl::DecItem> narrow;
     for (const Unit& u : units) {
         for (int64_t pos = u.b; pos < u.e;) {
             int64_t take = std::min<int64_t>(u.e - pos, Pmax);
             if (u.e - pos - take < 16) take = u.e - pos;   // no tail piece under one step
-            narrow.push_back({u.rep_row, (int32_t)pos, (int32_t)(pos + take), u.kvh, u.mem_begin, u.n_mem, 0, 0});
+            narrow.push_back(
+                {u.rep_row, (int32_t)pos, (int32_t)(pos + take), u.kvh, u.mem_begin, u.n_mem, 0, u.nh});
             pos += take;
         }
     }
@@ -238,8 +247,10 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
     int64_t prow = 0;
     for (auto& it : items) {
         it.partial_base = (int32_t)prow;
-        for (int32_t i = 0; i < it.n_mem; ++i) ++eptr[(size_t)g->seg_members[it.mem_begin + i] * Hkv + it.kvh + 1];
-        prow += (int64_t)it.n_mem * G;
+        for (int32_t i = 0; i < it.n_mem; ++i)
+            for (int32_t hh = 0; hh < it.nh; ++hh)
+                ++eptr[(size_t)g->seg_members[it.mem_begin + i] * Hkv + it.kvh + hh + 1];
+        prow += (int64_t)it.n_mem * it.nh * G;
         if (prow > INT32_MAX / 256) return SGL_ERR_UNSUPPORTED;
     }
     int32_t max_ent = 0;
@@ -253,8 +264,9 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
         std::vector<int32_t> fill(eptr.begin(), eptr.end() - 1);
         for (const auto& it : items)
             for (int32_t i = 0; i < it.n_mem; ++i)
-                ents_flat[fill[(size_t)g->seg_members[it.mem_begin + i] * Hkv + it.kvh]++] =
-                    it.partial_base + i * G;
+                for (int32_t hh = 0; hh < it.nh; ++hh)
+                    ents_flat[fill[(size_t)g->seg_members[it.mem_begin + i] * Hkv + it.kvh + hh]++] =
+                        it.partial_base + (i * it.nh + hh) * G;
     }
 
     sgl_plan* plan = new (std::nothrow) sgl_plan();
