@@ -15,12 +15,13 @@
 //               head of one KV head); warps 5-10 are the tiles' gather team;
 //   warp 2      the streaming lookup warp: pieces, slots, piece fields;
 //   warps 3-6   the streaming producers (bulk copies of whole token rows);
-//   warps 7-14  streaming consumers, one per KV head of the current piece
+//   warps 7-14  streaming consumers, 8 query rows of one KV head each
 //   (in CTAs with wide items, the streaming roles start once the tiles are
 //   done).
 // A narrow piece is a run of positions of one request segment (a request's
 // own suffix, or a small group's) for a block of up to 8 consecutive KV
-// heads, with at most 8 query rows per head (members x G query heads).  In
+// heads with at most 8 query rows per head (members x G query heads), or of
+// up to 4 heads with at most 16 rows per head (two consumer warps each).  In
 // the pool [slot, Hkv, d] a token's K (or V) row for those heads is one
 // contiguous run of nh * d elements, moved with one cp.async.bulk.
 // Measured on GB300: random 2 KB token rows gather at 6.8-7.1 TB/s from 152
@@ -51,9 +52,9 @@
 // consecutive rows of q); the consumers release the slot (QEMPTY) once
 // their fragments are in registers.
 //
-// Consumer warp c, per 16-position step, for KV head kvh + c of the piece
-// (mma.sync m16n8k16, bf16 in, fp32 acc; the head's query rows in the MMA's
-// N dimension):
+// Consumer warp, per 16-position step, for its KV head and 8 query rows of
+// the piece (mma.sync m16n8k16, bf16 in, fp32 acc; the query rows in the
+// MMA's N dimension):
 //   S^T [16 pos x 8 rows] = K [16 x d] . Q^T [d x 8 rows]
 //   O^T [d x 8 rows]     += V^T [d x 16 pos] . P^T [16 pos x 8 rows]
 // ldmatrix for K, ldmatrix.trans for V^T; P^T moves from the accumulator
@@ -94,7 +95,7 @@ struct FusedLayout {
     static constexpr int ES = F8 ? 1 : 2;                // bytes per pool element
     static constexpr int PITCH = kHB * D * ES + 16;      // one token's K (or V) row of a head block, padded
     static constexpr int STAGE = 2 * kNP * PITCH;        // K rows, then V rows
-    static constexpr int QSLOT = kHB * 8 * D * 2;        // [head][8 rows][d] bf16
+    static constexpr int QSLOT = kHB * 8 * D * 2;        // [head][8 or 16 rows][d] bf16 (8 x 8 or 4 x 16)
     static constexpr int SLOTW = kSQ * kSlotEntry;
     static constexpr int FIXED = 1024 + QSLOT + SLOTW + 8 * 32 + 64 + (2 * 8 + 1 + 2 * kSQ) * 8 + 1024;
     static constexpr int NSF0 = (232448 - FIXED) / STAGE;
@@ -411,7 +412,7 @@ __device__ __noinline__ void stream_producer(const FusedArgs& f, int pw, uint32_
             const int k = lane + 32 * j;
             if (k < nqc) {
                 const int qi = k / cur_nh, qh = k - qi * cur_nh;
-                bulk_g2s(qbuf + (uint32_t)((qh * 8 + qi * G) * D * 2),
+                bulk_g2s(qbuf + (uint32_t)((qh * (nm * G > 8 ? 16 : 8) + qi * G) * D * 2),
                          qp + ((int64_t)(j ? qmem1 : qmem0) * Hq + (kvh + qh) * G) * D, (uint32_t)(G * D * 2), fb);
             }
         }
@@ -431,9 +432,9 @@ __device__ __noinline__ void stream_producer(const FusedArgs& f, int pw, uint32_
 }
 
 // ---------------------------------------------------------------------------
-// Consumer warp c: KV head kvh + c of each piece (idle, but keeping the
-// barrier counts, when the piece has fewer heads); only shared memory in its
-// loop (stages, descriptors, Q slot)
+// Consumer warp c: 8 query rows of one KV head of each piece (idle, but
+// keeping the barrier counts, when the piece has fewer heads or rows); only
+// shared memory in its loop (stages, descriptors, Q slot)
 // ---------------------------------------------------------------------------
 template <int D, bool F8>
 __device__ __noinline__ void stream_consumer(const FusedArgs& f, int c, uint32_t ring, uint32_t desc, uint32_t qbuf,
@@ -451,8 +452,12 @@ __device__ __noinline__ void stream_consumer(const FusedArgs& f, int c, uint32_t
     // final normalisation (both are per tensor, so they factor out)
     const float sc = F8 ? f.t.scale_log2 * f.t.k_scale : f.t.scale_log2;
     const float vsc = F8 ? f.t.v_scale : 1.f;
-    const uint32_t hoff = (uint32_t)(c * D * Lay::ES);   // this warp's head within a row
-    const uint32_t qb = qbuf + (uint32_t)(c * 8 * D * 2);   // this warp's head in the Q slot
+    // Per piece: a head with at most 8 query rows takes one consumer warp
+    // (warp c: KV head kvh + c), one with more takes two (warp c: head
+    // kvh + c / 2, rows 8 (c % 2) ..); hw is this warp's head in the piece,
+    // r0 its first row of the head.
+    uint32_t hoff = 0, qb = qbuf;   // this warp's head within a K/V row, its rows in the Q slot
+    int hw = 0, r0 = 0;
 
     uint32_t qcur[D / 8];
     float o[MT][4];
@@ -468,9 +473,9 @@ __device__ __noinline__ void stream_consumer(const FusedArgs& f, int c, uint32_t
         }
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-            const int r = 2 * t + hh;   // query row of this head: member r / G, query head r % G
+            const int r = r0 + 2 * t + hh;   // query row of this head: member r / G, query head r % G
             if (r < cur_rows) {
-                const int64_t prow = (int64_t)cur_pb + ((r / G) * cur_nh + c) * G + r % G;
+                const int64_t prow = (int64_t)cur_pb + ((r / G) * cur_nh + hw) * G + r % G;
                 const float ll = hh ? s1 : s0, mm = hh ? m1 : m0;
                 const float inv = ll > 0.f ? vsc / ll : 0.f;
                 if constexpr (F8) {
@@ -508,7 +513,12 @@ __device__ __noinline__ void stream_consumer(const FusedArgs& f, int c, uint32_t
             cur_pb = ld_shared_s32(db + kDescPb);
             cur_rows = ld_shared_s32(db + kDescRows);
             cur_nh = ld_shared_s32(db + kDescNh);
-            active = c < cur_nh;
+            const int wph = cur_rows > 8 ? 2 : 1;   // consumer warps per head
+            hw = c / wph;
+            r0 = (c - hw * wph) * 8;
+            active = hw < cur_nh && r0 < cur_rows;
+            hoff = (uint32_t)(hw * D * Lay::ES);
+            qb = qbuf + (uint32_t)((hw * 8 * wph + r0) * D * 2);
             if (active) {
                 // Q^T fragments: row g (the N index), k-step ks -> chunks 2ks, 2ks+1
                 if constexpr (F8) {

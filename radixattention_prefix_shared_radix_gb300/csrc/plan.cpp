@@ -12,11 +12,12 @@
 //     member blocks of up to 128 rows x chunks of whole 128-position
 //     multiples, dealt to a set of tile CTAs sized with the streaming work
 //     (cost model below);
-//   * every other segment (at most 8 rows per KV head: a request's own
+//   * every other segment (at most 16 rows per KV head: a request's own
 //     suffix, or a small group) is narrow: its positions, for blocks of up
-//     to 8 consecutive KV heads (a token's K or V row of those heads is one
-//     contiguous run in the pool), are cut into pieces handed to the
-//     streaming CTAs at run time, longest first;
+//     to 8 consecutive KV heads (4 when a head has more than 8 rows; a
+//     token's K or V row of those heads is one contiguous run in the pool),
+//     are cut into pieces handed to the streaming CTAs at run time, longest
+//     first;
 //   * each item writes its rows' normalised partial O and LSE (fp32); the
 //     merge list of (request, KV head) names every partial row to combine.
 // The fp32 path runs the same items one CTA each.
@@ -112,33 +113,36 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
     st = sgl::validate_groups(B, seq_lens, g);
     if (st) return st;
 
-    // Narrow segments (at most 8 query rows: member x query head of a KV
-    // head) go to the streaming warps; wider ones to the tensor-core tiles
-    // in member blocks of up to 128 rows.
-    const int32_t MBn = std::max(1, 8 / G);
+    // Narrow segments (at most 16 query rows per KV head: members x query
+    // heads of the group) go to the streaming warps; wider ones to the
+    // tensor-core tiles in member blocks of up to 128 rows.
+    const int32_t MBn = std::max(1, 16 / G);
     const int32_t MBw = std::max(1, 128 / G);
     const int sms = sgl::query_num_sms(p->num_sms);
 
-    // Narrow work streams in blocks of HP consecutive KV heads (one stream
-    // per CTA, one consumer warp per head); the fp32 kernel runs one item
-    // per CTA and takes one head per item.
-    const int32_t HP = p->dtype == SGL_DTYPE_F32 ? 1 : std::min<int32_t>(Hkv, sgl::kDecHeadBlock);
+    // Narrow work streams in blocks of consecutive KV heads (one stream per
+    // CTA): up to 8 heads with one consumer warp each when a head has at
+    // most 8 query rows, else up to 4 heads with two consumer warps each;
+    // the fp32 kernel runs one item per CTA and takes one head per item.
+    auto head_block = [&](int32_t nmem) -> int32_t {
+        if (p->dtype == SGL_DTYPE_F32) return 1;
+        return std::min<int32_t>(Hkv, nmem * G <= 8 ? sgl::kDecHeadBlock : sgl::kDecHeadBlock / 2);
+    };
     struct Unit {   // narrow work: one member block of a segment for a block of KV heads
         int32_t rep_row, b, e, kvh, mem_begin, n_mem, nh;
     };
     std::vector<Unit> units;
     int64_t units_n = 0;     // position-heads
-    int64_t units_pos = 0;   // positions (each for a block of heads)
     int64_t max_wide = 0;
     for (int32_t s = 0; s < nseg; ++s) {
         const int32_t b = g->seg_begin[s], e = g->seg_end[s];
         const int32_t m0 = g->seg_member_ptr[s], nmem = g->seg_member_ptr[s + 1] - m0;
         if (nmem <= MBn) {
+            const int32_t HP = head_block(nmem);
             for (int32_t h = 0; h < Hkv; h += HP) {
                 const int32_t nh = std::min(HP, Hkv - h);
                 units.push_back({g->seg_row[s], b, e, h, m0, nmem, nh});
                 units_n += (int64_t)(e - b) * nh;
-                units_pos += e - b;
             }
         } else {
             max_wide = std::max<int64_t>(max_wide, e - b);
@@ -208,10 +212,13 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
     // handed out at run time from a counter, so SMs that stream faster take
     // more.
     const int64_t n_cons = n_ctas - n_tile_ctas;
-    int64_t Pmax = (int64_t)std::ceil((double)units_pos / (double)std::max<int64_t>(1, 2 * n_cons));
-    Pmax = std::min<int64_t>(2048, std::max<int64_t>(32, (Pmax + 15) / 16 * 16));
+    // (in position-heads, so that a piece of a 4-head block is as long in
+    // bytes as one of an 8-head block)
+    const int64_t Pph = (int64_t)std::ceil((double)units_n / (double)std::max<int64_t>(1, 2 * n_cons));
     std::vector<sgl::DecItem> narrow;
     for (const Unit& u : units) {
+        int64_t Pmax = (Pph + u.nh - 1) / u.nh;
+        Pmax = std::min<int64_t>(2048, std::max<int64_t>(32, (Pmax + 15) / 16 * 16));
         for (int64_t pos = u.b; pos < u.e;) {
             int64_t take = std::min<int64_t>(u.e - pos, Pmax);
             if (u.e - pos - take < 16) take = u.e - pos;   // no tail piece under one step
