@@ -9,10 +9,11 @@
 // read once: a segment shared by many requests is read once for all of them.
 //
 // One CTA per SM (the planner's n_ctas), 480 threads:
-//   warps 0-10  (CTAs with wide items) the tcgen05 tile roles of
+//   all warps   (CTAs with wide items, first) the tcgen05 tile roles of
 //               tc_tile.cuh over this CTA's wide items: a chunk of a shared
 //               segment against up to 128 query rows (member request x query
-//               head of one KV head); warps 5-10 are the tiles' gather team;
+//               head of one KV head): warps 0-3 softmax, 4 MMA, 5-14 the
+//               gather team;
 //   warp 2      the streaming lookup warp: pieces, slots, piece fields;
 //   warps 3-6   the streaming producers (bulk copies of whole token rows);
 //   warps 7-14  streaming consumers, 8 query rows of one KV head each
@@ -84,8 +85,8 @@ constexpr int kFirstProducer = 3;
 constexpr int kProducers = 4;                            // each issues 8 of a stage's 32 row copies
 constexpr int kFirstConsumer = kFirstProducer + kProducers;
 constexpr int kFusedThreads = 32 * (kFirstConsumer + kHB);
-static_assert(DecCfg<128>::kThreads <= kFusedThreads && DecCfg<64>::kThreads == DecCfg<128>::kThreads,
-              "the tile roles fit in the CTA");
+static_assert(DecCfg<128>::kThreads == kFusedThreads && DecCfg<64>::kThreads == kFusedThreads,
+              "the tile roles take the whole CTA");
 static_assert((kSQ & (kSQ - 1)) == 0, "slot ring");
 static_assert((2 * kNP) % kProducers == 0 && 2 * kNP / kProducers <= 32, "row copies per producer warp");
 
@@ -741,11 +742,10 @@ __global__ void __maxnreg__(128) decode_fused_kernel(const __grid_constant__ Fus
     grid_dep_wait();
     grid_dep_launch();
 
-    constexpr int kStreamGate = 3;   // named barrier: tile roles done -> streaming may start
-    constexpr int kTileWarps = TC::kThreads / 32;   // softmax, MMA, gather team
-    if (tiles && warp < kTileWarps) {
-        // the tile roles; their warps 2-10 go on to stream (lookup,
-        // producers, four of the consumers) once the CTA's tiles are done
+    static_assert(TC::kThreads == kFusedThreads, "every warp has a tile role");
+    if (tiles) {
+        // the tile roles (all warps); warps 2-14 go on to stream (lookup,
+        // producers, consumers) once the CTA's tiles are done
         const uint32_t tbase = *tslot;
         TcState st{0u, 0u, false};
         for (int w = w0; w < w1; ++w) {
@@ -755,12 +755,11 @@ __global__ void __maxnreg__(128) decode_fused_kernel(const __grid_constant__ Fus
             tc_tile_run<TC>(f.t, &tmk, &tmv, nullptr, nullptr, ti, sm, tbase, st, tid);
             named_bar(kTileBar, TC::kThreads);
         }
-        // the streaming areas overlap the tile roles' barriers
+        // the streaming areas overlap the tile roles' barriers: invalidated
+        // before any streaming role starts
         if (tid == 0) tc_inval_barriers<TC>(smem_u32(sm + TL::OFF_BAR));
-        asm volatile("bar.arrive %0, %1;\n" ::"r"(kStreamGate), "r"(kFusedThreads) : "memory");
+        named_bar(kTileBar, TC::kThreads);
     }
-    // streaming warps of CTAs with tiles start once the tiles are done
-    if (tiles && warp >= kTileWarps) named_bar(kStreamGate, kFusedThreads);
     const uint32_t ring = smem_u32(sm + Lay::OFF_RING), qb = smem_u32(sm + Lay::OFF_Q);
     const uint32_t desc = smem_u32(sm + Lay::OFF_DESC);
     const uint32_t sring = smem_u32(sm + Lay::OFF_SLOT);

@@ -244,12 +244,15 @@ struct TcCfg {
 
 // The decode tiles' configuration: one query tile with Q in TMEM, 128-position
 // blocks (S MMAs of N = 128), two score buffers so that the softmax of block
-// j + 1 overlaps PV_j and S_{j+2}, a gather team of six warps, and three K/V
-// stages: with the S lookahead a K stage is free only once S of the block
-// two earlier has run, and the third stage gives the gather of K_{j+2} a
-// whole block more (two with FP8 pools, whose staging area takes the room).
+// j + 1 overlaps PV_j and S_{j+2}, a gather team of ten warps (every warp of
+// the decode CTA has a tile role: a block's 128 gathers of 512 bytes take
+// a warp ~110 cycles each to issue, so the block's issue time falls with
+// the team's size), and three K/V stages: with the S lookahead a K stage is
+// free only once S of the block two earlier has run, and the third stage
+// gives the gather of K_{j+2} a whole block more (two with FP8 pools, whose
+// staging area takes the room).
 template <int D, bool F8 = false>
-using DecCfg = TcCfg<D, true, 1, F8 ? 2 : 3, 6, 128, 2, F8>;
+using DecCfg = TcCfg<D, true, 1, F8 ? 2 : 3, 10, 128, 2, F8>;
 
 struct TileInfo {
     int kv_row, kv_begin, kv_end, kvh;
