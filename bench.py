@@ -320,11 +320,12 @@ def graph_time(torch, fn, calls, n):
     return e0.elapsed_time(e1) / n, n
 
 
-def bench_decode_workload(sgl, W, torch, name, n_inst, n_calls, hbm_peak, num_sms=0):
+def bench_decode_workload(sgl, W, torch, name, n_inst, n_calls, hbm_peak, num_sms=0, fp8=False):
     """Another decode workload timed like the headline: one CUDA graph of
     back-to-back calls rotating over n_inst batch instances, CUDA events.
     Returns unique-KV bytes per call, GB/s and fractions of the measured HBM
-    copy peak and of 8 TB/s."""
+    copy peak and of 8 TB/s; with fp8, the same batches on an E4M3 copy of
+    the pool too."""
     w, tree, kd, vd, inst = setup_decode(sgl, W, torch, n_inst, num_sms, name=name)
     for s in range(max(3, len(inst))):
         decode_call(sgl, kd, vd, inst[s % len(inst)])
@@ -346,6 +347,9 @@ def bench_decode_workload(sgl, W, torch, name, n_inst, n_calls, hbm_peak, num_sm
          "wide_items": info["num_wide_items"], "items": info["num_items"],
          "l2": "%d instance(s), %.0f MB unique KV in all (L2 %d MB)" % (len(inst), ub * len(inst) / 1e6,
                                                                        L2_BYTES // 1000000)}
+    if fp8:
+        r["fp8_kv"] = bench_fp8(sgl, W, torch, w, kd, vd, inst, n_calls, hbm_peak, num_sms, name=name)
+        r["fp8_kv"]["speedup_vs_bf16"] = ms / r["fp8_kv"]["ms_per_call"]
     del inst
     sgl.sgl_tree_destroy(tree)
     del kd, vd
@@ -543,9 +547,10 @@ def run_native(args):
         # groups at 80% and 0% sharing (inputs larger than L2 per call), and
         # the tiny fp32 batch (latency only)
         others = {}
-        for name, n_inst, n_calls in (("fork_tree", 4, 400), ("multiturn", 1, 100), ("multiturn_noshare", 1, 60),
-                                      ("tiny_fp32", 4, 2000)):
-            others[name] = bench_decode_workload(sgl, W, torch, name, n_inst, n_calls, hbm_peak, args.num_sms)
+        for name, n_inst, n_calls, f8 in (("fork_tree", 4, 400, True), ("multiturn", 1, 100, True),
+                                          ("multiturn_noshare", 1, 60, True), ("tiny_fp32", 4, 2000, False)):
+            others[name] = bench_decode_workload(sgl, W, torch, name, n_inst, n_calls, hbm_peak, args.num_sms,
+                                                 fp8=f8 and not args.no_fp8)
 
     ext = None
     if not args.no_extend and args.only == "all":
@@ -703,7 +708,7 @@ def bench_extend(sgl, W, torch, steps, bf16_peak):
                        "kv_dtype": "e4m3 (per-tensor scales); one K/V stage, codes converted to f16 in shared memory"}}
 
 
-def bench_fp8(sgl, W, torch, w, kd, vd, inst, steps, hbm_peak, num_sms=0):
+def bench_fp8(sgl, W, torch, w, kd, vd, inst, steps, hbm_peak, num_sms=0, name=None):
     """The same decode batches on an FP8 (E4M3) copy of the pool: per-tensor
     scales amax / 448, codes from torch's round-to-nearest conversion (input
     preparation only; the decode call reads the codes)."""
@@ -758,10 +763,12 @@ def bench_fp8(sgl, W, torch, w, kd, vd, inst, steps, hbm_peak, num_sms=0):
     ms = e0.elapsed_time(e1) / n
     ub = sum(c["ub"] for c in calls) / len(calls)
     gbs = ub / (ms / 1e3) / 1e9
-    return {"workload": DECODE_WORKLOAD, "kv_dtype": "e4m3 (per-tensor scales)", "ms_per_call": ms,
+    del k8, v8
+    torch.cuda.empty_cache()
+    return {"workload": name or DECODE_WORKLOAD, "kv_dtype": "e4m3 (per-tensor scales)", "ms_per_call": ms,
             "unique_kv_bytes_per_call": int(ub), "unique_kv_gbs": gbs, "frac_of_hbm": gbs / hbm_peak,
             "tokens_per_s": inst[0]["B"] / (ms / 1e3), "calls_timed": n,
-            "path": "same plan as bf16: shared prefixes on tcgen05 tiles (codes converted to f16 in shared memory), the rest on streaming warps"}
+            "path": "same plan as bf16: prefixes shared by many requests on tcgen05 tiles (codes converted to f16 in shared memory), the rest streamed (codes straight into MMA fragments)"}
 
 
 def bench_mla(sgl, W, torch, steps, bf16_peak, hbm_peak, num_sms=0):

@@ -50,8 +50,59 @@ namespace {
 using namespace sgldev;
 
 // ---------------------------------------------------------------------------
+// KV write into FP8 pools: each new bf16 K/V element goes to its slot as the
+// E4M3 code of value / scale (IEEE fp32 division), rounded to nearest even
+// and saturated to the largest finite E4M3 value (cvt.rn.satfinite), one
+// thread per 8 elements.  Out-of-pool slots are skipped and set bit 0 of the
+// error word.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t e4m3x2_of(float lo, float hi) {
+    uint16_t h;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(h) : "f"(hi), "f"(lo));
+    return h;
+}
+__global__ void kv_scatter_e4m3(const uint4* __restrict__ kn, const uint4* __restrict__ vn, uint2* __restrict__ kw,
+                                uint2* __restrict__ vw, const int32_t* __restrict__ r2t, int64_t ld,
+                                const int32_t* __restrict__ pre, const int32_t* __restrict__ ext, int B, int64_t n_rows,
+                                int Hkv, int chunks, int64_t num_slots, uint32_t* err, float k_scale, float v_scale) {
+    const int64_t per_row = (int64_t)Hkv * chunks;   // 8-element groups per token row
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n_rows * per_row * 2;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const bool v = i >= n_rows * per_row;
+        const int64_t k = v ? i - n_rows * per_row : i;
+        const int64_t row = k / per_row, within = k - row * per_row;
+        int r = 0;
+        int64_t acc = 0;
+        for (; r < B; ++r) {
+            const int e = __ldg(ext + r);
+            if (row < acc + e) break;
+            acc += e;
+        }
+        if (r >= B) continue;
+        const int32_t sl = __ldg(r2t + (int64_t)r * ld + __ldg(pre + r) + (row - acc));
+        if (sl < 0 || sl >= num_slots) {
+            if (within == 0) atomicOr(err, 1u);
+            continue;
+        }
+        const uint4 x = __ldg((v ? vn : kn) + row * per_row + within);
+        const float sc = v ? v_scale : k_scale;
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+        uint32_t c[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            c[j] = e4m3x2_of(__fdiv_rn(__uint_as_float(w[j] << 16), sc),
+                             __fdiv_rn(__uint_as_float(w[j] & 0xffff0000u), sc));
+        (v ? vw : kw)[(int64_t)sl * per_row + within] = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Decode partial kernel (fp32, CUDA cores, no tensor cores): one warp per
-// query row of the item, lanes split head_dim; exact fp32 FFMA dot products.
+// query row of the item, 32 positions at a time with one position per lane:
+// each lane takes its position's whole dot product (exact fp32 FFMA, the
+// query row broadcast from shared memory), the warp combines the 32 scores
+// with shuffles, and for O the lanes split head_dim and run over the 32
+// positions, whose V rows are all independent loads.
 // ---------------------------------------------------------------------------
 template <int D>
 __global__ void __launch_bounds__(128)
@@ -60,7 +111,8 @@ __global__ void __launch_bounds__(128)
                        const sgl::DecItem* __restrict__ items, const int32_t* __restrict__ members,
                        float* __restrict__ po, float* __restrict__ plse, uint32_t* __restrict__ err, int Hq, int Hkv,
                        int G, int64_t num_slots, float scale_log2) {
-    constexpr int E = D / 32;
+    constexpr int E = D / 32;   // O columns per lane
+    __shared__ __align__(16) float qs[4][D];
     const sgl::DecItem it = items[blockIdx.x];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int rows = it.n_mem * it.nh * G;
@@ -74,37 +126,63 @@ __global__ void __launch_bounds__(128)
         // row r: member r / (nh G), KV head kvh + (r / G) % nh, query head r % G of its group
         const int mem = __ldg(members + it.mem_begin + r / (it.nh * G));
         const int kvh = it.kvh + (r / G) % it.nh;
-        const float* qr = q + ((int64_t)mem * Hq + kvh * G + r % G) * D + lane * E;
-        float qv[E], o[E];
+        const float* qr = q + ((int64_t)mem * Hq + kvh * G + r % G) * D;
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-            qv[e] = qr[e];
-            o[e] = 0.f;
-        }
+        for (int e = 0; e < E; ++e) qs[warp][lane + 32 * e] = qr[lane + 32 * e];
+        __syncwarp();
+        const float4* q4 = reinterpret_cast<const float4*>(qs[warp]);
+        float o[E];
+#pragma unroll
+        for (int e = 0; e < E; ++e) o[e] = 0.f;
         float m = -INFINITY, l = 0.f;
-        for (int pos = it.kv_begin; pos < kv_end; ++pos) {
-            const int64_t slot = load_slot(r2t, ld, it.rep_row, pos, num_slots, err);
-            if (slot < 0) continue;
-            const float* kr = kp + (slot * Hkv + kvh) * D + lane * E;
-            const float* vr = vp + (slot * Hkv + kvh) * D + lane * E;
-            float dot = 0.f;
+        for (int p0 = it.kv_begin; p0 < kv_end; p0 += 32) {
+            const int p = p0 + lane;
+            const int64_t slot = p < kv_end ? load_slot(r2t, ld, it.rep_row, p, num_slots, err) : -1;
+            float s = -INFINITY;
+            if (slot >= 0) {
+                const float4* kr = reinterpret_cast<const float4*>(kp + (slot * Hkv + kvh) * D);
+                float dot = 0.f;
 #pragma unroll
-            for (int e = 0; e < E; ++e) dot = fmaf(qv[e], kr[e], dot);
+                for (int c = 0; c < D / 4; ++c) {
+                    const float4 k4 = __ldg(kr + c), q4c = q4[c];
+                    dot = fmaf(q4c.x, k4.x, dot);
+                    dot = fmaf(q4c.y, k4.y, dot);
+                    dot = fmaf(q4c.z, k4.z, dot);
+                    dot = fmaf(q4c.w, k4.w, dot);
+                }
+                s = dot * scale_log2;
+            }
+            float cmax = s;
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-            const float s = dot * scale_log2;
-            const float mn = fmaxf(m, s);
-            const float a = exp2f(m - mn), p = exp2f(s - mn);
-            l = l * a + p;
+            for (int off = 16; off > 0; off >>= 1) cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, off));
+            const float mn = fmaxf(m, cmax);
+            if (mn == -INFINITY) continue;   // nothing in this chunk (nor before)
+            const float a = exp2f(m - mn);   // 0 while nothing was accumulated
+            const float pj = exp2f(s - mn);  // 0 for masked positions
+            float psum = pj;
 #pragma unroll
-            for (int e = 0; e < E; ++e) o[e] = fmaf(p, vr[e], o[e] * a);
+            for (int off = 16; off > 0; off >>= 1) psum += __shfl_xor_sync(0xffffffffu, psum, off);
+            l = l * a + psum;
+#pragma unroll
+            for (int e = 0; e < E; ++e) o[e] *= a;
+#pragma unroll 8
+            for (int j = 0; j < 32; ++j) {
+                const float pb = __shfl_sync(0xffffffffu, pj, j);
+                const int64_t sj = __shfl_sync(0xffffffffu, slot, j);
+                if (sj >= 0) {
+                    const float* vr = vp + (sj * Hkv + kvh) * D;
+#pragma unroll
+                    for (int e = 0; e < E; ++e) o[e] = fmaf(pb, __ldg(vr + lane + 32 * e), o[e]);
+                }
+            }
             m = mn;
         }
         const int64_t prow = (int64_t)it.partial_base + r;
         const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
-        for (int e = 0; e < E; ++e) po[prow * D + lane * E + e] = o[e] * inv;
+        for (int e = 0; e < E; ++e) po[prow * D + lane + 32 * e] = o[e] * inv;
         if (lane == 0) plse[prow] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+        __syncwarp();   // qs[warp] is rewritten for the next row
     }
 }
 
@@ -269,6 +347,17 @@ int launch_extend(const sgl_attn_params* p, const void* q, const void* kp, const
     if (total_rows == 0) return SGL_OK;
     if (p->dtype == SGL_DTYPE_BF16 || p->dtype == SGL_DTYPE_BF16_FP8KV) {
         if (tiles > INT32_MAX) return SGL_ERR_UNSUPPORTED;
+        if (p->dtype == SGL_DTYPE_BF16_FP8KV && kn) {
+            // FP8 pools: the new rows are quantised into the pool first, and
+            // the extend then reads every position from the pool (so the new
+            // block is attended at its stored, quantised values)
+            kv_scatter_e4m3<<<1024, 256, 0, s>>>(static_cast<const uint4*>(kn), static_cast<const uint4*>(vn),
+                                                 static_cast<uint2*>(kw), static_cast<uint2*>(vw), r2t, ld, pre, ext,
+                                                 B, total_rows, Hkv, D / 8, p->num_slots, err, p->k_scale,
+                                                 p->v_scale);
+            kn = vn = nullptr;
+            kw = vw = nullptr;
+        }
         const int e = p->dtype == SGL_DTYPE_BF16_FP8KV
                           ? sgl::launch_extend_tc<D, true>(q, kp, vp, kn, vn, kw, vw, r2t, ld, pre, ext, B, total_rows,
                                                            tiles, o, lse, err, Hq, Hkv, p->num_slots, sl2, p->k_scale,
@@ -338,8 +427,6 @@ static int extend_impl(const void* q_new, const void* k_new, const void* v_new, 
                        float* lse, void* workspace, size_t ws_bytes, sgl_stream_t stream) {
     int st = sgl::check_params(params);
     if (st) return st;
-    // FP8 KV pools: extend reads them; the fused KV write (bf16 new rows) is not offered
-    if (params->dtype == SGL_DTYPE_BF16_FP8KV && k_new) return SGL_ERR_UNSUPPORTED;
     const int32_t B = params->batch;
     if (B > 0 && (!params->host_extend_lens || !params->host_prefix_lens || !prefix_lens || !extend_lens))
         return SGL_ERR_INVALID_ARG;

@@ -528,8 +528,12 @@ __device__ __noinline__ void stream_consumer(const FusedArgs& f, int c, uint32_t
                     // order of the lane's K codes below), as f16
 #pragma unroll
                     for (int j = 0; j < D / 32; ++j) lds128(qb + g * (D * 2) + ((D / 32) * t + j) * 16, qcur + 4 * j);
+                    uint32_t bad = 0u;
 #pragma unroll
-                    for (int k = 0; k < D / 8; ++k) qcur[k] = bf16x2_to_f16x2(qcur[k]);
+                    for (int k = 0; k < D / 8; ++k) qcur[k] = bf16x2_to_f16x2_chk(qcur[k], bad);
+                    // (Q slot rows past the piece's rows hold stale bytes that
+                    // only ever meet their own, unused, output columns)
+                    if (bad && r0 + g < cur_rows) atomicOr(f.t.err, kErrQRange);
                 } else {
 #pragma unroll
                     for (int kp2 = 0; kp2 < D / 32; ++kp2) {

@@ -137,6 +137,14 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t x) {
     asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(y) : "f"(b), "f"(a));
     return y;
 }
+// The same, noting in `bad` a value that f16 cannot hold: |x| >= 65536 (the
+// largest bf16 below it, 65280, is an f16 value), an infinity or a NaN.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_chk(uint32_t x, uint32_t& bad) {
+    bad |= ((x & 0x7fffu) >= 0x4780u) | (((x >> 16) & 0x7fffu) >= 0x4780u);
+    return bf16x2_to_f16x2(x);
+}
+// error word bit 3: a query element outside f16's range met an FP8 pool
+constexpr uint32_t kErrQRange = 8u;
 __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
     uint32_t y;
     asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(y) : "f"(hi), "f"(lo));

@@ -378,6 +378,7 @@ __device__ __forceinline__ void tc_tile_run(const TcArgs& a, const CUtensorMap* 
                 // the Q chunks it copied, in place, once they have landed
                 cp_async_commit();
                 cp_async_wait<0>();
+                uint32_t qbad = 0u;
 #pragma unroll
                 for (int q = 0; q < NQ; ++q) {
                     for (int t = g; t < QI; t += NG) {
@@ -386,10 +387,11 @@ __device__ __forceinline__ void tc_tile_run(const TcArgs& a, const CUtensorMap* 
                         asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];\n"
                                      : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
                                      : "r"(qa));
-                        st_shared_v4(qa, bf16x2_to_f16x2(w[0]), bf16x2_to_f16x2(w[1]), bf16x2_to_f16x2(w[2]),
-                                     bf16x2_to_f16x2(w[3]));
+                        st_shared_v4(qa, bf16x2_to_f16x2_chk(w[0], qbad), bf16x2_to_f16x2_chk(w[1], qbad),
+                                     bf16x2_to_f16x2_chk(w[2], qbad), bf16x2_to_f16x2_chk(w[3], qbad));
                     }
                 }
+                if (qbad) atomicOr(a_err, kErrQRange);
                 fence_proxy_async_smem();
                 mbar_arrive(bar(C::QFULL));
             } else {
@@ -745,8 +747,10 @@ __device__ __forceinline__ void tc_tile_run(const TcArgs& a, const CUtensorMap* 
                     w[4 * k + 3] = v.w;
                 }
                 if constexpr (F8) {   // f16 operands against the f16 K tiles
+                    uint32_t qbad = 0u;
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) w[k] = bf16x2_to_f16x2(w[k]);
+                    for (int k = 0; k < 32; ++k) w[k] = bf16x2_to_f16x2_chk(w[k], qbad);
+                    if (qbad) atomicOr(a_err, kErrQRange);
                 }
                 tst32u(tlQ + 32 * c, w);
             }

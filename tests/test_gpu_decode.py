@@ -366,18 +366,89 @@ def test_extend_fp8_kv(name):
         case.close()
 
 
-def test_fp8_kv_fused_kv_write_is_unsupported():
+@pytest.mark.parametrize("name", ["extend_small", "extend"])
+def test_fp8_kv_fused_kv_write(name):
+    """The fused KV write into FP8 pools: afterwards the pool holds, bit for
+    bit, the oracle's E4M3 codes of each new row / scale at its slot (every
+    other slot untouched), and the result equals the oracle's extend over the
+    written pool (at the full size: every row of request 2, sampled rows of
+    the others)."""
+    from oracle.attention import extend_attention
+    from oracle.fp8 import DequantView, kv_write_e4m3
+    case = Case(name)
+    try:
+        w = case.w
+        pre = case.out["prefix_lens"]
+        ext = case.out["seq_lens"] - pre
+        ks, vs = 1.0 / 64, 1.0 / 48
+        k8, v8 = W.quantize_e4m3(case.K, ks), W.quantize_e4m3(case.V, vs)
+        kf, vf = W.make_new_kv(w, int(ext.sum()))
+        kn, vn = W.to_dtype(w, kf), W.to_dtype(w, vf)
+        kd, vd = k8.cuda(), v8.cuda()
+        p = sgl.make_params(sgl.SGL_DTYPE_BF16_FP8KV, case.B, w.Hq, w.Hkv, w.d, case.S, w.page_size, k_scale=ks,
+                            v_scale=vs, host_prefix_lens=pre, host_extend_lens=ext)
+        ws = torch.zeros(sgl.sgl_extend_workspace_bytes(p), dtype=torch.uint8, device="cuda")
+        qd = case.q_host().cuda()
+        o = torch.empty_like(qd)
+        lse = torch.empty(qd.shape[0], w.Hq, dtype=torch.float32, device="cuda")
+        sgl.sgl_extend_attn_kvwrite(qd, kn.cuda(), vn.cuda(), kd, vd, torch.from_numpy(case.out["req_to_token"]).cuda(),
+                                    torch.from_numpy(pre).cuda(), torch.from_numpy(ext).cuda(), p, o, lse, ws)
+        sgl.sgl_check(ws)
+        Kexp, Vexp = kv_write_e4m3(k8.numpy().copy(), v8.numpy().copy(), kn.float().numpy(), vn.float().numpy(), ks,
+                                   vs, case.oracle_table, pre, ext)
+        assert np.array_equal(kd.cpu().numpy(), Kexp) and np.array_equal(vd.cpu().numpy(), Vexp)
+        rows = full_and_sampled_rows(ext, (2,), 4, (127, 128)) if name == "extend" else None
+        Oref, Lref = extend_attention(case.oracle_q(), DequantView(torch.from_numpy(Kexp), ks),
+                                      DequantView(torch.from_numpy(Vexp), vs), case.oracle_table, pre, ext, rows=rows)
+        do, dl = assert_close(o.double().cpu().numpy(), lse.cpu().numpy().astype(np.float64), Oref, Lref,
+                              *tolerances(w), rows=rows)
+        print("%s fp8 fused write: O max-abs %.3g, LSE max-abs %.3g" % (name, do, dl))
+    finally:
+        case.close()
+
+
+def test_fp8_query_outside_f16_is_reported():
+    """With FP8 pools the query enters the MMAs as f16: an element of
+    magnitude 2^16 or more (no f16 value) is reported by sgl_check as
+    SGL_ERR_BOUNDS -- on the tile path and the streaming path of decode and
+    in extend -- while the same call with the element in range is clean."""
+    from tests._harness import run_extend
+    ks = vs = 1.0 / 64
+    case = Case("llama3_8b_decode_small")
+    try:
+        w = case.w
+        k8, v8 = W.quantize_e4m3(case.K, ks).cuda(), W.quantize_e4m3(case.V, vs).cuda()
+        p = sgl.make_params(sgl.SGL_DTYPE_BF16_FP8KV, case.B, w.Hq, w.Hkv, w.d, case.S, w.page_size, k_scale=ks,
+                            v_scale=vs)
+        plan = sgl.sgl_decode_plan(p, case.out["seq_lens"], sgl.sgl_groups_view(case.groups))
+        assert sgl.sgl_plan_info(plan)["num_wide_items"] > 0   # request 0 is on a tile and on a stream
+        ws = torch.zeros(max(plan.workspace_bytes, 256), dtype=torch.uint8, device="cuda")
+        sgl.sgl_plan_upload(plan, ws)
+        table = torch.from_numpy(case.out["req_to_token"]).cuda()
+        seq = torch.from_numpy(case.out["seq_lens"]).cuda()
+        for big, expect in ((65280.0, None), (65536.0, -5), (-1e6, -5)):
+            qd = case.q_host().clone()
+            qd[0, 0, 5] = big
+            qd = qd.cuda()
+            o = torch.empty_like(qd)
+            lse = torch.empty(case.B, w.Hq, dtype=torch.float32, device="cuda")
+            sgl.sgl_decode_attn(qd, k8, v8, table, seq, plan, o, lse, ws)
+            if expect is None:
+                sgl.sgl_check(ws)
+            else:
+                with pytest.raises(sgl.SglError) as e:
+                    sgl.sgl_check(ws)
+                assert e.value.status == expect
+        del plan
+    finally:
+        case.close()
     case = Case("extend_small")
     try:
-        O, L, k8, v8, pre, ext, p = _fp8_extend(case, 1.0 / 64, 1.0 / 64)
-        z = torch.zeros(16, dtype=torch.uint8, device="cuda")
+        big_q = case.q_host().clone()
+        big_q[3, 1, 7] = 1e5
+        case.b.q = big_q.float().numpy()
         with pytest.raises(sgl.SglError) as e:
-            sgl.sgl_extend_attn_kvwrite(z, z, z, k8.cuda(), v8.cuda(), torch.zeros((case.B, 1), dtype=torch.int32,
-                                                                                 device="cuda"),
-                                        torch.zeros(case.B, dtype=torch.int32, device="cuda"),
-                                        torch.ones(case.B, dtype=torch.int32, device="cuda"), p, z,
-                                        torch.zeros(1, device="cuda"), torch.zeros(256, dtype=torch.uint8,
-                                                                                  device="cuda"))
-        assert e.value.status == -3
+            _fp8_extend(case, ks, vs)
+        assert e.value.status == -5
     finally:
         case.close()
