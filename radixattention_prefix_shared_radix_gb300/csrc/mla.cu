@@ -27,6 +27,7 @@
 #include "common.h"
 #include "device_common.cuh"
 #include "merge.cuh"
+#include "mla_tile.cuh"
 
 namespace sgl {
 namespace {
@@ -70,6 +71,7 @@ struct MlaArgs {
     int Hq, Gp;
     int64_t num_slots;
     float scale_log2;         // sm_scale * log2(e)
+    int n_tile;               // CTAs 0 .. n_tile - 1 run the tcgen05 tile pairs (mla_tile.cuh)
 };
 
 // 16-byte chunk c of row r of a [rows][576] bf16 tile
@@ -85,8 +87,17 @@ __device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r
     asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];\n" : "=r"(r0), "=r"(r1) : "r"(addr));
 }
 
-__global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const __grid_constant__ MlaArgs a) {
-    extern __shared__ __align__(128) uint8_t smem_raw[];
+__global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const __grid_constant__ MlaArgs a,
+                                                                 const __grid_constant__ CUtensorMap tmap) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    if ((int)blockIdx.x < a.n_tile) {
+        // a tile pair's output half on the tensor cores
+        uint8_t* sm1 = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+        const mlat::TileArgs ta{a.q, a.r2t, a.ld, a.seq_lens, a.items, a.members, a.po, a.plse, a.err,
+                                a.Hq, a.Gp, a.num_slots, a.scale_log2};
+        mlat::mla_tile_run(ta, &tmap, (int)blockIdx.x >> 1, (int)blockIdx.x & 1, sm1, (int)threadIdx.x);
+        return;
+    }
     uint8_t* sm = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
     const uint32_t sQ = smem_u32(sm + MlaLayout::OFF_Q), sKV = smem_u32(sm + MlaLayout::OFF_KV);
     const uint32_t sP = smem_u32(sm + MlaLayout::OFF_P);
@@ -317,8 +328,9 @@ extern "C" int sgl_mla_decode_attn(const void* q, const void* kv_pool, const int
         return SGL_ERR_INVALID_ARG;
     auto* ws = static_cast<unsigned char*>(workspace);
     auto s = reinterpret_cast<cudaStream_t>(stream);
+    constexpr int kSmem = MlaLayout::TOTAL > mlat::Lay::TOTAL ? MlaLayout::TOTAL : mlat::Lay::TOTAL;
     static const cudaError_t attr =
-        cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, MlaLayout::TOTAL);
+        cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (attr != cudaSuccess) {
         set_cuda_error((int)attr);
         return SGL_ERR_CUDA;
@@ -338,6 +350,16 @@ extern "C" int sgl_mla_decode_attn(const void* q, const void* kv_pool, const int
     a.Gp = plan->G;
     a.num_slots = p.num_slots;
     a.scale_log2 = p.sm_scale * kLog2e;
+    a.n_tile = plan->n_wide;
+    // the tiles' TMA view of the pool, [num_slots, 576] (left zero, and
+    // unused, without tiles)
+    CUtensorMap tmap{};
+    if (plan->n_wide > 0) {
+        if (const int te = tc::encode_rows_map(kv_pool, p.num_slots, kDC, &tmap)) {
+            set_cuda_error(te);
+            return SGL_ERR_CUDA;
+        }
+    }
     // both launches are programmatic dependents of the kernel before them
     cudaLaunchAttribute pdl[1];
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -350,8 +372,8 @@ extern "C" int sgl_mla_decode_attn(const void* q, const void* kv_pool, const int
     if (plan->n_items > 0) {
         cfg.gridDim = dim3((unsigned)plan->n_items);
         cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = MlaLayout::TOTAL;
-        e = cudaLaunchKernelEx(&cfg, mla_decode_kernel, a);
+        cfg.dynamicSmemBytes = kSmem;
+        e = cudaLaunchKernelEx(&cfg, mla_decode_kernel, a, tmap);
         if (e != cudaSuccess) {
             set_cuda_error((int)e);
             return SGL_ERR_CUDA;

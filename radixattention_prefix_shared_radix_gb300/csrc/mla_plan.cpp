@@ -7,7 +7,11 @@
 // and all their query heads: the work unit is 64 query rows (member x head)
 // of one segment chunk.  With Hq query heads a unit holds 64 / min(Hq, 64)
 // members and min(Hq, 64) heads ("head group"; Hq = 128 has two groups of 64
-// heads that read the same rows).  Chunks are cut by a cost model of the
+// heads that read the same rows).  Two full units of one segment (e.g. two
+// blocks of members sharing a prefix, or the two head groups of a request at
+// Hq = 128) read the same rows: they are paired into a 128-row tcgen05 tile
+// (mla_tile.cuh) run by two CTAs, one per half of the output columns; the
+// other units run as mma.sync items.  Chunks are cut by a cost model of the
 // kernel (measured on GB300: a 32-position block costs about 0.94 us +
 // 0.0394 us per query row of the item, so a 64-row block of a shared prefix
 // costs twice a 16-row block of a request's own suffix, and an item about
@@ -34,6 +38,10 @@ constexpr int32_t kMlaBlock = 32;   // positions per block of the kernel
 // estimated microseconds of one 32-position block for an item of `rows` query rows
 double block_cost(int32_t rows) { return 0.94 + 0.0394 * rows; }
 constexpr double kItemCost = 1.5;   // estimated start cost of one item (us)
+// tcgen05 tile pairs (two 64-row units, two CTAs): estimated microseconds of
+// one 32-position block and of a tile's start (Q load, first gathers)
+constexpr double kTileBlock = 1.2;
+constexpr double kTileStart = 3.0;
 // a partial row (512 fp32) is written by the kernel and read by the merge:
 // 4 KB at about 6 TB/s
 constexpr double kRowCost = 4096.0 / 6.0e6;
@@ -67,20 +75,40 @@ extern "C" int sgl_mla_decode_plan(const sgl_mla_params* p, const int32_t* seq_l
     struct Unit {
         int32_t s, mb, nm, hg;
         int64_t len;
-        double per_block;
+        double per_block;   // per block of this unit (a pair: per block of each of its two CTAs)
+        int32_t partner;    // the pair's second unit (this is the first), -1 single, -2 second of a pair
     };
     std::vector<Unit> units;
     double total = 0.0;
     for (int32_t s = 0; s < nseg; ++s) {
         const int32_t nmem = g->seg_member_ptr[s + 1] - g->seg_member_ptr[s];
         const int64_t len = g->seg_end[s] - g->seg_begin[s];
+        const size_t first = units.size();
         for (int32_t mb = 0; mb < nmem; mb += MB)
             for (int32_t hg = 0; hg < Hg; ++hg) {
                 const int32_t nm = std::min(MB, nmem - mb);
-                const double pb = block_cost(nm * Gp);
-                units.push_back({s, mb, nm, hg, len, pb});
-                total += pb * (double)((len + kMlaBlock - 1) / kMlaBlock);
+                units.push_back({s, mb, nm, hg, len, block_cost(nm * Gp), -1});
             }
+        // pairs of full units of this segment, in order
+        if (len >= 2 * kMlaBlock) {
+            int32_t open = -1;
+            for (size_t i = first; i < units.size(); ++i) {
+                if (units[i].nm * Gp != kMlaRows) continue;
+                if (open < 0) {
+                    open = (int32_t)i;
+                } else {
+                    units[open].partner = (int32_t)i;
+                    units[open].per_block = kTileBlock;
+                    units[i].partner = -2;
+                    open = -1;
+                }
+            }
+        }
+        for (size_t i = first; i < units.size(); ++i) {
+            if (units[i].partner == -2) continue;
+            const double ctas = units[i].partner >= 0 ? 2.0 : 1.0;
+            total += ctas * units[i].per_block * (double)((len + kMlaBlock - 1) / kMlaBlock);
+        }
     }
     auto pieces_of = [&](const Unit& u, double T) {   // blocks per piece, pieces
         const int64_t blocks = (u.len + kMlaBlock - 1) / kMlaBlock;
@@ -92,13 +120,20 @@ extern "C" int sgl_mla_decode_plan(const sgl_mla_params* p, const int32_t* seq_l
         out.clear();
         int64_t rows = 0;
         for (const Unit& u : units) {
+            if (u.partner == -2) continue;
             const auto pc = pieces_of(u, T);
             const int64_t blocks = (u.len + kMlaBlock - 1) / kMlaBlock;
             for (int64_t k = 0; k < pc.second; ++k) {
                 const int64_t nb = std::min(pc.first, blocks - k * pc.first);
                 if (nb > 0) {
-                    out.push_back(kItemCost + u.per_block * (double)nb);
-                    rows += (int64_t)u.nm * Gp;
+                    if (u.partner >= 0) {   // a tile piece: two CTAs
+                        out.push_back(kTileStart + u.per_block * (double)nb);
+                        out.push_back(kTileStart + u.per_block * (double)nb);
+                        rows += 2 * kMlaRows;
+                    } else {
+                        out.push_back(kItemCost + u.per_block * (double)nb);
+                        rows += (int64_t)u.nm * Gp;
+                    }
                 }
             }
         }
@@ -133,25 +168,41 @@ extern "C" int sgl_mla_decode_plan(const sgl_mla_params* p, const int32_t* seq_l
         }
     }
     struct Piece {
-        sgl::DecItem item;
+        sgl::DecItem item, second;   // second: the pair's other unit (tile pieces)
         double cost;
     };
-    std::vector<Piece> pieces;
+    std::vector<Piece> pieces, tiles;
     int64_t C = 0;   // longest piece (reported as the chunk length)
     for (const Unit& u : units) {
+        if (u.partner == -2) continue;
         const auto pc = pieces_of(u, T);
         const int64_t plen = pc.first * kMlaBlock;
         C = std::max(C, plen);
         const int32_t b = g->seg_begin[u.s], e = g->seg_end[u.s];
         for (int64_t cb = b; cb < e; cb += plen) {
             const int32_t ce = (int32_t)std::min<int64_t>(e, cb + plen);
-            const double cost = kItemCost + u.per_block * (double)((ce - cb + kMlaBlock - 1) / kMlaBlock);
-            pieces.push_back({{g->seg_row[u.s], (int32_t)cb, ce, u.hg, g->seg_member_ptr[u.s] + u.mb, u.nm, 0, 0}, cost});
+            const int64_t nb = (ce - cb + kMlaBlock - 1) / kMlaBlock;
+            const sgl::DecItem it{g->seg_row[u.s], (int32_t)cb, ce, u.hg, g->seg_member_ptr[u.s] + u.mb, u.nm, 0, 1};
+            if (u.partner >= 0) {
+                const Unit& v = units[(size_t)u.partner];
+                const sgl::DecItem it2{g->seg_row[v.s], (int32_t)cb, ce, v.hg, g->seg_member_ptr[v.s] + v.mb, v.nm, 0, 1};
+                tiles.push_back({it, it2, kTileStart + u.per_block * (double)nb});
+            } else {
+                pieces.push_back({it, it, kItemCost + u.per_block * (double)nb});
+            }
         }
     }
-    std::stable_sort(pieces.begin(), pieces.end(), [](const Piece& x, const Piece& y) { return x.cost > y.cost; });
+    auto by_cost = [](const Piece& x, const Piece& y) { return x.cost > y.cost; };
+    std::stable_sort(tiles.begin(), tiles.end(), by_cost);
+    std::stable_sort(pieces.begin(), pieces.end(), by_cost);
+    // items: the tile pieces' two units each (CTAs 2 t and 2 t + 1 both run
+    // tile t, one output half each), then the mma.sync pieces
     std::vector<sgl::DecItem> items;
-    items.reserve(pieces.size());
+    items.reserve(2 * tiles.size() + pieces.size());
+    for (const Piece& pc : tiles) {
+        items.push_back(pc.item);
+        items.push_back(pc.second);
+    }
     for (const Piece& pc : pieces) items.push_back(pc.item);
     // partial rows in item order: member i of the item, head j of its group
     // at partial_base + i * Gp + j; merge lists per (request, head group)
@@ -183,7 +234,7 @@ extern "C" int sgl_mla_decode_plan(const sgl_mla_params* p, const int32_t* seq_l
     ap.num_sms = p->num_sms;
     plan->G = Gp;
     plan->n_items = (int32_t)items.size();
-    plan->n_wide = 0;
+    plan->n_wide = (int32_t)(2 * tiles.size());   // tile CTAs (items 0 .. n_wide - 1, two per tile)
     plan->n_partial_rows = (int32_t)prow;
     plan->n_ctas = plan->n_items;
     plan->n_members = g->num_members;
@@ -219,7 +270,7 @@ extern "C" int sgl_mla_decode_plan(const sgl_mla_params* p, const int32_t* seq_l
         return SGL_ERR_INVALID_ARG;
     }
     std::memset(plan->blob, 0, plan->tables_bytes);
-    sgl::WsHeader hdr{0u, sgl::kWsMagic, plan->n_items, 0, plan->n_partial_rows, plan->n_ctas};
+    sgl::WsHeader hdr{0u, sgl::kWsMagic, plan->n_items, plan->n_wide, plan->n_partial_rows, plan->n_ctas};
     std::memcpy(plan->blob, &hdr, sizeof(hdr));
     if (!items.empty()) std::memcpy(plan->blob + plan->off_items, items.data(), items.size() * sizeof(sgl::DecItem));
     if (g->num_members) std::memcpy(plan->blob + plan->off_members, g->seg_members, (size_t)g->num_members * 4);

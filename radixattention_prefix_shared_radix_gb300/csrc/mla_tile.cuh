@@ -1,0 +1,377 @@
+// MLA grouped decode on the 5th-generation tensor cores: the shared-prefix
+// work of the MLA decode as tcgen05/TMEM tiles (CS349D lecture-16 notes,
+// SGLang case study, §4 "More engineering": MLA with the decompression
+// matrices absorbed, attention in the 576-dim latent space by a grouped
+// decode kernel; §5.1: one stored row per token, read by every query head).
+//
+// A tile is 128 query rows -- two 64-row work units of the plan (member x
+// head of a head group) that read the same chunk of one prefix-group
+// segment -- against that chunk, in blocks of 32 positions.  Its output has
+// 512 columns (the latent), whose fp32 accumulator for 128 rows alone fills
+// all of TMEM, so a tile runs on two CTAs: CTA half h accumulates output
+// columns 256 h .. 256 h + 255, and both compute the block's scores.
+// Per block j (two score buffers, two K/V stages; the MMA thread issues S_0,
+// then per block PV_j and S_{j+1}):
+//   S_j = Q K_j^T   M 128, N 32, K 576: 36 MMAs, both operands K-major
+//                   128B-swizzled shared memory (Q resident, 144 KB);
+//   softmax         thread = query row = TMEM lane: the 32 scores, a running
+//                   max (O rescaled only when it grows by more than 2^8),
+//                   P_j = 2^(s - m) as bf16 pairs back into the buffer;
+//   O += P_j V_j    M 128, N 256, K 32: A = P from TMEM, B = this half's 256
+//                   latent columns of the same shared rows (MN-major).
+// The stored rows are gathered once per block by TMA tile::gather4 (four
+// 128-byte row pieces per copy; the pool viewed as a [slot, 576] tensor with
+// 64 x 1 boxes and the 128-byte swizzle) and serve as both K and V.
+// Measured on GB300: an M = 128 tcgen05 MMA takes 46 cycles at N = 32,
+// 64 at N = 128 and 128 at N = 256, with A from shared memory or TMEM and B
+// K- or MN-major alike.
+// Roles (512 threads): warps 0-3 softmax, warp 4 the MMA thread (and TMEM
+// owner), warps 5-15 the gather team (a warp gets one gather4 through about
+// every 110 cycles, so a block's 72 copies are spread over eleven warps);
+// all warps load Q first.  Every wait is
+// bounded: one that gives up sets bit 2 of the error word and the CTA runs to
+// its end without hanging (its results are then garbage, and flagged).
+#pragma once
+
+#include <cuda.h>
+
+#include "tc_tile.cuh"
+
+namespace sgl {
+namespace mlat {
+
+using namespace sgldev;
+using namespace tc;
+
+constexpr int kDC = 576;                  // stored row: latent + position part
+constexpr int kDV = 512;                  // output: the latent
+constexpr int kBN = 32;                   // positions per block
+constexpr int kNS = 2;                    // K/V stages
+constexpr int kRows = 128;                // query rows of a tile (two 64-row units)
+constexpr int kNReg = kDC / 64;           // 64-element regions of a row: 9
+constexpr int kQReg = kRows * 128;        // Q region: 128 rows x 128 bytes
+constexpr int kKReg = kBN * 128;          // K/V region of a stage: 32 rows x 128 bytes
+constexpr int kStage = kNReg * kKReg;     // 36 KB
+constexpr int kNG = 11;                   // gather warps (5 .. 15)
+constexpr int kOps = kNReg * (kBN / 4);   // gather4 copies per block: 72
+constexpr int kOpw = (kOps + kNG - 1) / kNG;   // per gather warp: 12
+constexpr int kOCols = kDV / 2;           // output columns of one CTA: 256
+static_assert(kOpw <= 32, "one gather per lane");
+
+struct Lay {
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_KV = OFF_Q + kNReg * kQReg;                 // 147456
+    static constexpr int OFF_BAR = OFF_KV + kNS * kStage;                // 221184
+    // barriers: KFULL[2], KEMPTY[2], SFULL[2], PFULL[2], OFULL, DONE
+    static constexpr int KFULL(int s) { return s; }
+    static constexpr int KEMPTY(int s) { return 2 + s; }
+    static constexpr int SFULL(int b) { return 4 + b; }
+    static constexpr int PFULL(int b) { return 6 + b; }
+    static constexpr int OFULL = 8;
+    static constexpr int DONE = 9;
+    static constexpr int kNumBars = 10;
+    static constexpr int OFF_TMEM = OFF_BAR + 128;
+    static constexpr int OFF_MEM = OFF_TMEM + 16;   // the two units' member requests (at most 4 each)
+    static constexpr int END = OFF_MEM + 32;
+    static constexpr int TOTAL = END + 1024;   // + alignment slack (the 128B swizzle wants 1024-byte alignment)
+    static_assert(TOTAL <= 232448, "shared memory per CTA");
+};
+
+// TMEM columns: O (this half's 256 columns) first, then the two score buffers
+constexpr int kTO = 0;
+constexpr int kTS = kOCols;
+
+struct TileArgs {
+    const bf16* q;            // [B, Hq, 576]
+    const int32_t* r2t;       // [B, ld]
+    int64_t ld;
+    const int32_t* seq_lens;
+    const DecItem* items;     // the tile's two units are items 2 t and 2 t + 1
+    const int32_t* members;
+    float* po;                // partial rows [rows, 512]
+    float* plse;
+    uint32_t* err;
+    int Hq, Gp;
+    int64_t num_slots;
+    float scale_log2;
+};
+
+// 16 TMEM columns of this thread's lane from registers (P: 32 bf16 values)
+__device__ __forceinline__ void tst16u(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
+}
+
+// One tile half: `t` the tile (items 2 t, 2 t + 1), `h` the output half.
+// `sm` is the 1024-aligned shared base, `tid` < 512.
+__device__ __forceinline__ void mla_tile_run(const TileArgs& a, const CUtensorMap* tmap, int t, int h, uint8_t* sm,
+                                             int tid) {
+    const int warp = tid >> 5, lane = tid & 31;
+    const uint32_t sQ = smem_u32(sm + Lay::OFF_Q), sKV = smem_u32(sm + Lay::OFF_KV);
+    const uint32_t bar0 = smem_u32(sm + Lay::OFF_BAR);
+    auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + Lay::OFF_TMEM);
+    uint32_t* const err = a.err;
+    bool timed_out = false;
+    auto wait = [&](int b, uint32_t par) {
+        if (timed_out) return;
+        if (!mbar_wait(bar(b), par)) {
+            atomicOr(err, 4u);
+            timed_out = true;
+        }
+    };
+
+    // the tile's units (plan tables) and its chunk
+    const DecItem u0 = a.items[2 * t], u1 = a.items[2 * t + 1];
+    if (tid == 0) {
+        for (int s = 0; s < kNS; ++s) {
+            mbar_init(bar(Lay::KFULL(s)), kNG);
+            mbar_init(bar(Lay::KEMPTY(s)), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(Lay::SFULL(b)), 1);
+            mbar_init(bar(Lay::PFULL(b)), 128);
+        }
+        mbar_init(bar(Lay::OFULL), 1);
+        mbar_init(bar(Lay::DONE), 1);
+        mbar_fence_init();
+    }
+    if (warp == 4) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;\n" ::"r"(smem_u32(tslot)));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
+    }
+    grid_dep_wait();
+    grid_dep_launch();
+    const int len = __ldg(a.seq_lens + u0.rep_row);
+    int e = u0.kv_end;
+    if (e > len) {
+        if (tid == 0) atomicOr(err, 2u);
+        e = len;
+    }
+    const int b = u0.kv_begin;
+    const int nb = e > b ? (e - b + kBN - 1) / kBN : 0;
+    const int rows0 = u0.n_mem * a.Gp, rows1 = u1.n_mem * a.Gp;
+    // the units' member requests (plan table) into shared memory first, so
+    // that no Q copy below waits on a load
+    int* mtab = reinterpret_cast<int*>(sm + Lay::OFF_MEM);
+    if (tid < 8) {
+        const int u = tid >> 2, k = tid & 3;
+        const DecItem& it = u ? u1 : u0;
+        mtab[tid] = k < it.n_mem ? __ldg(a.members + it.mem_begin + k) : 0;
+    }
+    __syncthreads();
+
+    // Q: 128 rows (unit 0's rows, then unit 1's at 64; zeros past each
+    // unit's rows) x 72 chunks of 16 bytes into the 9 SW128 regions, by every
+    // thread; the tensor cores read it after the barrier below
+    for (int i = tid; i < kRows * (kDC / 8); i += 512) {
+        const int r = i / (kDC / 8), c = i - r * (kDC / 8);
+        const int u = r >> 6, ri = r & 63;
+        const bool ok = ri < (u ? rows1 : rows0);
+        const int mem = mtab[4 * u + ri / a.Gp];
+        const int hg = u ? u1.kvh : u0.kvh;
+        const bf16* src = ok ? a.q + ((int64_t)mem * a.Hq + hg * a.Gp + ri % a.Gp) * kDC + c * 8 : a.q;
+        cp_async16(sQ + sw128(r, c, kQReg), src, ok);
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tslot;
+
+    if (warp >= 5 && warp < 5 + kNG) {
+        // ------------------------------------------------------------ gather
+        const int g = warp - 5;
+        const int o = g * kOpw + lane;
+        const int nmine = max(0, min(kOps - g * kOpw, kOpw));
+        const bool mine = lane < nmine;
+        const int reg = o % kNReg, quad = o / kNReg;
+        const int32_t* trow = a.r2t + (int64_t)u0.rep_row * a.ld;
+        const uint32_t bytes = (uint32_t)nmine * 512u;
+        int issued = 0;
+        for (int j = 0; j < nb; ++j) {
+            const int st = j % kNS;
+            // this lane's four rows (positions past the range re-read the
+            // last position: finite data, masked scores)
+            int r[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int p = min(b + j * kBN + 4 * quad + k, e - 1);
+                int32_t sl = mine ? __ldg(trow + p) : 0;
+                if (sl < 0 || sl >= a.num_slots) {
+                    if (mine && reg == 0) atomicOr(err, 1u);
+                    sl = 0;
+                }
+                r[k] = sl;
+            }
+            wait(Lay::KEMPTY(st), ((j / kNS) & 1) ^ 1);
+            if (__any_sync(0xffffffffu, timed_out)) {
+                timed_out = true;
+                break;
+            }
+            if (lane == 0) mbar_expect_tx(bar(Lay::KFULL(st)), bytes);
+            __syncwarp();
+            if (mine)
+                tma_gather4(sKV + st * kStage + reg * kKReg + quad * 512, tmap, reg * 64, r[0], r[1], r[2], r[3],
+                            bar(Lay::KFULL(st)));
+            issued = j + 1;
+        }
+        // this warp's copies have landed before it leaves (bounded)
+        for (int j = max(0, issued - kNS); j < issued; ++j)
+            if (!mbar_wait(bar(Lay::KFULL(j % kNS)), (uint32_t)(j / kNS) & 1u)) atomicOr(err, 4u);
+    } else if (warp == 4) {
+        // ------------------------------------------------------------ MMA
+        if (lane == 0) {
+            constexpr uint32_t IS = idesc_bf16(128, kBN, false);
+            constexpr uint32_t IO = idesc_bf16(128, kOCols, true);
+            auto mma_s = [&](int j) {
+                const uint32_t kb = sKV + (j % kNS) * kStage;
+                const uint32_t tS = tbase + kTS + (j & 1) * kBN;
+#pragma unroll 4
+                for (int ks = 0; ks < kDC / 16; ++ks) {
+                    const uint32_t off = (ks & 3) * 32;   // 16 elements within the 64-element region
+                    tc_mma(tS, sdesc(sQ + (ks >> 2) * kQReg + off, 16, 1024),
+                           sdesc(kb + (ks >> 2) * kKReg + off, 16, 1024), IS, ks > 0);
+                }
+                tc_commit(bar(Lay::SFULL(j & 1)));
+            };
+            // S_0; then per block PV_j as soon as P_j is ready (which frees
+            // block j's stage for the gather of block j + 2) and S_{j+1},
+            // whose stage was freed one block earlier: each gather overlaps
+            // a whole block's work
+            if (nb > 0) {
+                wait(Lay::KFULL(0), 0);
+                tc_fence_after();
+                mma_s(0);
+            }
+            for (int j = 0; j < nb; ++j) {
+                wait(Lay::PFULL(j & 1), (uint32_t)(j >> 1) & 1u);
+                tc_fence_after();
+                const uint32_t vb = sKV + (j % kNS) * kStage + 4 * h * kKReg;
+                const uint32_t tP = tbase + kTS + (j & 1) * kBN;
+#pragma unroll
+                for (int kk = 0; kk < kBN / 16; ++kk)
+                    tc_mma_tmem_a(tbase + kTO, tP + kk * 8, sdesc(vb + kk * 2048, kKReg, 1024), IO,
+                                  (j > 0 || kk > 0) ? 1u : 0u);
+                tc_commit(bar(Lay::KEMPTY(j % kNS)));
+                tc_commit(bar(Lay::OFULL));
+                if (j + 1 < nb) {   // into block j-1's score buffer, read by PV_{j-1} (issued before it)
+                    wait(Lay::KFULL((j + 1) % kNS), (uint32_t)((j + 1) / kNS) & 1u);
+                    tc_fence_after();
+                    mma_s(j + 1);
+                }
+            }
+            // every MMA has finished before this thread leaves (bounded)
+            tc_commit(bar(Lay::DONE));
+            if (!mbar_wait(bar(Lay::DONE), 0)) atomicOr(err, 4u);
+        }
+        __syncwarp();
+    } else if (warp < 4) {
+        // ------------------------------------------------------------ softmax
+        const int i = tid;   // row == TMEM lane
+        const uint32_t lq = (uint32_t)(warp * 32) << 16;
+        const uint32_t tl = tbase + lq;
+        const float sc = a.scale_log2;
+        float m_used = -INFINITY, l0 = 0.f, l1 = 0.f;
+        auto scale_o = [&](float f) {
+            float v[32];
+#pragma unroll 1
+            for (int c = 0; c < kOCols / 32; ++c) {
+                tld32(tl + kTO + 32 * c, v);
+#pragma unroll
+                for (int k = 0; k < 32; ++k) v[k] *= f;
+                tst32(tl + kTO + 32 * c, v);
+            }
+        };
+        for (int j = 0; j < nb; ++j) {
+            wait(Lay::SFULL(j & 1), (uint32_t)(j >> 1) & 1u);
+            tc_fence_after();
+            const uint32_t tS = tl + kTS + (j & 1) * kBN;
+            float s[32];
+            tld32(tS, s);
+            const int pos0 = b + j * kBN;
+            if (pos0 + kBN > e) {
+#pragma unroll
+                for (int k = 0; k < 32; ++k) s[k] = pos0 + k < e ? s[k] : -INFINITY;
+            }
+            float mc[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int k = 0; k < 32; k += 8) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) mc[c] = fmax3f(mc[c], s[k + 2 * c], s[k + 2 * c + 1]);
+            }
+            const float mx = fmax3f(mc[0], mc[1], fmaxf(mc[2], mc[3])) * sc;
+            const float m_new = fmaxf(m_used, mx);
+            const bool need = m_new > m_used + 8.f;   // also true for the first finite max
+            const bool resc = need && m_used != -INFINITY;
+            if (__any_sync(0xffffffffu, resc)) {
+                const float f = resc ? exp2f(m_used - m_new) : 1.f;
+                l0 *= f;
+                l1 *= f;
+                if (j > 0) {   // O holds blocks < j: wait for PV_{j-1}
+                    wait(Lay::OFULL, (uint32_t)(j - 1) & 1u);
+                    tc_fence_after();
+                    scale_o(f);
+                }
+            }
+            if (need) m_used = m_new;
+            const float nmu = m_used == -INFINITY ? 0.f : -m_used;
+            uint32_t pk[16];
+#pragma unroll
+            for (int k = 0; k < 32; k += 2) {
+                float x0, x1;
+                ffma2_sc(x0, x1, s[k], s[k + 1], sc, nmu);
+                const float p0 = ex2_ftz(x0), p1 = ex2_ftz(x1);   // -inf -> 0
+                fadd2_acc(l0, l1, p0, p1);
+                pk[k / 2] = pack_bf16(p0, p1);
+            }
+            tst16u(tS, pk);   // P over the scores already read
+            tc_fence_before();
+            mbar_arrive(bar(Lay::PFULL(j & 1)));
+        }
+        // epilogue: this half's 256 columns of O / l, once every PV is done
+        wait(Lay::DONE, 0);
+        tc_fence_after();
+        const float l = l0 + l1;
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const int u = i >> 6, ri = i & 63;
+        const bool ok = ri < (u ? rows1 : rows0);
+        const int64_t prow = (int64_t)(u ? u1.partial_base : u0.partial_base) + ri;
+#pragma unroll 1
+        for (int c = 0; c < kOCols / 32; c += 2) {
+            float v[64];
+            if (nb > 0) {
+                tld32_nw(tl + kTO + 32 * c, v);
+                tld32_nw(tl + kTO + 32 * c + 32, v + 32);
+                tld_wait();
+            } else {
+#pragma unroll
+                for (int k = 0; k < 64; ++k) v[k] = 0.f;
+            }
+            if (ok) {
+                float* dst = a.po + prow * kDV + kOCols * h + 32 * c;
+#pragma unroll
+                for (int k = 0; k < 64; k += 4)
+                    *reinterpret_cast<float4*>(dst + k) =
+                        make_float4(v[k] * inv, v[k + 1] * inv, v[k + 2] * inv, v[k + 3] * inv);
+            }
+        }
+        if (ok && h == 0) a.plse[prow] = l > 0.f ? (m_used + log2f(l)) * kLn2 : -INFINITY;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 4) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;\n" ::"r"(tbase));
+    }
+}
+
+}  // namespace mlat
+}  // namespace sgl

@@ -32,7 +32,17 @@ def test_every_partial_row_group_is_merged_once(case, num_sms):
     Gp = min(w.Hq, 64)
     info = sgl.sgl_plan_info(_plan(case, num_sms=num_sms))
     assert info["num_partial_rows"] == info["num_merge_entries"] * Gp
-    assert info["num_wide_items"] == 0 and info["chunk_tokens"] % 32 == 0
+    # tile pieces are two units each (two CTAs, one per output half)
+    assert info["num_wide_items"] % 2 == 0 and info["num_wide_items"] <= info["num_items"]
+    assert info["chunk_tokens"] % 32 == 0
+
+
+def test_segments_with_two_full_units_become_tiles(case):
+    # a segment that holds two full 64-row units (members x heads of a head
+    # group) is read by a tcgen05 tile pair; these workloads have such
+    # segments (a shared prefix; or one request's two head groups at Hq 128)
+    info = sgl.sgl_plan_info(_plan(case))
+    assert info["num_wide_items"] > 0
 
 
 def test_items_cover_every_member_once_per_position(case):
