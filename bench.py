@@ -57,6 +57,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-budget-s", type=float, default=60.0)
     ap.add_argument("--num-sms", type=int, default=0, help="decode planning target (0: the device's SM count)")
+    ap.add_argument("--workload", default="",
+                    help="time only this decode workload (fork_tree, multiturn, multiturn_noshare, tiny_fp32; "
+                         "profiling), with --instances instances and --steps calls")
     ap.add_argument("--only", choices=["all", "decode", "extend", "mla"], default="all",
                     help="decode: skip the extend line; extend: time only the extend workload (profiling)")
     ap.add_argument("--no-e2e", action="store_true")
@@ -461,6 +464,13 @@ def run_native(args):
         if rank == 0:
             print(json.dumps({"metric": "mla decode ms per call", "value": r["ms_per_call"], "unit": "ms",
                               "n_gpus": world, "mla": r}), flush=True)
+        return
+    if args.workload:
+        r = bench_decode_workload(sgl, W, torch, args.workload, args.instances, max(1, args.steps), hbm_peak,
+                                  args.num_sms, fp8=not args.no_fp8)
+        if rank == 0:
+            print(json.dumps({"metric": "decode us per call", "value": r["us_per_call"], "unit": "us",
+                              "n_gpus": world, args.workload: r}), flush=True)
         return
     if args.only == "extend":
         ext = bench_extend(sgl, W, torch, max(3, args.extend_steps), bf16_peak)
