@@ -366,15 +366,18 @@ def decode_call(sgl, kd, vd, it):
 
 def e2e_decode(sgl, W, torch, w, tree, kd, vd, inst, steps, num_sms=0):
     """Decode steps of a serving loop through the public API from host
-    buffers, on one batch that grows: every step appends one token to every
-    request (a [B, cap] token matrix updated in place), and the step runs
-    sgl_build_batch (match; allocate and insert the new token's slot; emit
-    the prefix groups; the slot table and lengths go straight into pinned
-    staging arrays), sgl_decode_plan, sgl_plan_upload, the pinned H2D copies
-    of q, the table and the lengths, the decode call, the D2H copies of O
-    and LSE, a stream synchronise and sgl_tree_finish_batch (references
-    released, the sequences stay cached).  Returns (GB/s of unique KV, h2d
-    bytes/step, d2h bytes/step, s/step, host us per stage)."""
+    buffers, on one batch that grows.  Step 0 runs sgl_build_batch (match;
+    allocate and insert the unmatched tail; emit the prefix groups; the slot
+    table and lengths go straight into pinned staging arrays); every later
+    step runs sgl_batch_append (one new slot per request, the groups' private
+    tails grow by one; the tree is untouched while the requests run).  Every
+    step then runs sgl_decode_plan, sgl_plan_upload, the pinned H2D copies of
+    q, the table and the lengths, the decode call, the D2H copies of O and
+    LSE and a stream synchronise.  After the last step
+    sgl_tree_cache_finished_batch caches every sequence (prompt plus the
+    decoded tokens) and releases the requests.  All of it is timed.  Returns
+    (GB/s of unique KV, h2d bytes/step, d2h bytes/step, s/step, host us per
+    stage, build and finish amortised over the steps)."""
     import numpy as np
     S = kd.shape[0]
     it = inst[0]
@@ -386,7 +389,6 @@ def e2e_decode(sgl, W, torch, w, tree, kd, vd, inst, steps, num_sms=0):
         toks[r, :len(t)] = t
     rng = np.random.default_rng(12)
     toks_new = rng.integers(0, W.VOCAB, size=(steps, B)).astype(np.int32)
-    lens = lens0.copy()
     ld = cap
     pq = it["q"].cpu().pin_memory()
     ptab = torch.empty((B, ld), dtype=torch.int32).pin_memory()
@@ -401,7 +403,8 @@ def e2e_decode(sgl, W, torch, w, tree, kd, vd, inst, steps, num_sms=0):
     ws = torch.zeros(4 * it["plan"].workspace_bytes + (1 << 20), dtype=torch.uint8, device="cuda")
     per_tok = kv_bytes_per_token(w)
     ub0 = it["ub"]
-    stage = dict(build=0.0, plan=0.0, upload=0.0, device=0.0, finish=0.0)
+    rows = np.arange(B)
+    stage = dict(build=0.0, append=0.0, plan=0.0, upload=0.0, device=0.0, finish=0.0)
     h2d = d2h = 0
     total_b = 0
     stream = torch.cuda.current_stream()
@@ -409,12 +412,14 @@ def e2e_decode(sgl, W, torch, w, tree, kd, vd, inst, steps, num_sms=0):
     t0 = time.perf_counter()
     for s in range(steps):
         c0 = time.perf_counter()
-        toks[np.arange(B), lens] = toks_new[s]
-        lens += 1
-        out = sgl.sgl_build_batch(tree, toks, groups=groups, req_to_token=tab_np, seq_lens=seq_np, lens=lens)
+        if s == 0:
+            out = sgl.sgl_build_batch(tree, toks, groups=groups, req_to_token=tab_np, seq_lens=seq_np, lens=lens0)
+        else:
+            sgl.sgl_batch_append(tree, tab_np, seq_np, groups)
+            toks[rows, seq_np - 1] = toks_new[s]
         c1 = time.perf_counter()
         p = sgl.make_params(sgl.SGL_DTYPE_BF16, B, w.Hq, w.Hkv, w.d, S, w.page_size, num_sms=num_sms)
-        plan = sgl.sgl_decode_plan(p, out["seq_lens"], sgl.sgl_groups_view(groups))
+        plan = sgl.sgl_decode_plan(p, seq_np, sgl.sgl_groups_view(groups))
         if plan.workspace_bytes > ws.numel():
             raise RuntimeError("e2e workspace too small")
         c2 = time.perf_counter()
@@ -428,17 +433,18 @@ def e2e_decode(sgl, W, torch, w, tree, kd, vd, inst, steps, num_sms=0):
         plse.copy_(it["lse"], non_blocking=True)
         stream.synchronize()
         c4 = time.perf_counter()
-        sgl.sgl_tree_finish_batch(tree, out)
-        c5 = time.perf_counter()
-        for k, a, b in (("build", c0, c1), ("plan", c1, c2), ("upload", c2, c3), ("device", c3, c4),
-                        ("finish", c4, c5)):
+        for k, a, b in (("build" if s == 0 else "append", c0, c1), ("plan", c1, c2), ("upload", c2, c3),
+                        ("device", c3, c4)):
             stage[k] += b - a
         if s == 0:
             h2d = (pq.numel() * 2 + ptab.numel() * 4 + pseq.numel() * 4 + sgl.sgl_plan_info(plan)["upload_bytes"])
             d2h = po.numel() * 2 + plse.numel() * 4
-        # the shared prefix is unchanged; every request's own suffix grew by one token
-        total_b += ub0 + (s + 1) * B * per_tok
+        # the shared prefix is unchanged; every request's own suffix grew by one token a step
+        total_b += ub0 + s * B * per_tok
+    c5 = time.perf_counter()
+    sgl.sgl_tree_cache_finished_batch(tree, toks, out)
     el = time.perf_counter() - t0
+    stage["finish"] += time.perf_counter() - c5
     sgl.sgl_check(ws)
     sgl.sgl_groups_destroy(groups)
     host_us = {k: v * 1e6 / steps for k, v in stage.items()}

@@ -70,9 +70,12 @@ enum {
 
 enum { SGL_DTYPE_F32 = 0, SGL_DTYPE_BF16 = 1, SGL_DTYPE_BF16_FP8KV = 2 };
 /* SGL_DTYPE_BF16_FP8KV: Q and O bf16, the K and V pools FP8 E4M3 bytes
- * (decode and extend; the fused KV write of sgl_extend_attn_kvwrite is
- * SGL_ERR_UNSUPPORTED); K = k_scale * pool value, V = v_scale * pool value
- * (per-tensor scales in sgl_attn_params).  ["SGLang 深度拆解" (the FP8 KV
+ * (decode and extend); K = k_scale * pool value, V = v_scale * pool value
+ * (per-tensor scales in sgl_attn_params).  sgl_extend_attn_kvwrite takes
+ * bf16 k_new / v_new and stores round-to-nearest-even E4M3 codes of
+ * k_new / k_scale and v_new / v_scale (saturating at +-448, NaN kept).  The
+ * query enters the tensor cores as f16: a query element outside the f16
+ * range sets SGL_ERR_BOUNDS for sgl_check.  ["SGLang 深度拆解" (the FP8 KV
  * cache halves the KV bytes); CS349D lecture-16 notes §4 (FP8 KV cache)] */
 
 /* Name of a status code (static string). */
@@ -205,6 +208,45 @@ int sgl_tree_finish(sgl_tree* tree, sgl_node last, const int32_t* row, int64_t l
  * finished). */
 int sgl_tree_finish_batch(sgl_tree* tree, int32_t B, const sgl_node* last, const int32_t* req_to_token, int64_t ld,
                           const int32_t* seq_lens);
+
+/* One decode step of a running batch (after sgl_build_batch): request r
+ * gains one token at position seq_lens[r].  Its slot is the first slot of
+ * a fresh page when seq_lens[r] is a multiple of the page size, else the
+ * slot after req_to_token[r, seq_lens[r] - 1] (the request's private tail
+ * page).  The step's fresh pages come from one allocation (evicting LRU
+ * leaves if needed) and go to the requests in order.  Writes
+ * req_to_token[r, seq_lens[r]] and increments seq_lens[r].  The tree is not
+ * touched: the new tokens are cached when the request ends
+ * (sgl_tree_cache_finished).  If groups != NULL it must hold this batch's
+ * prefix groups (from sgl_build_batch or an earlier append); each request's
+ * private trailing segment grows by one position, or a private one-position
+ * segment is added where its context ended in a shared segment.
+ * req_to_token: host [B, ld], seq_lens: host [B], both updated in place.
+ * SGL_ERR_INVALID_ARG (a row already ld long, a tail slot that is not
+ * followed by a slot of the same page, groups that do not cover the batch)
+ * and SGL_ERR_NO_SLOTS change nothing but the cache that allocation
+ * evicted.
+ * ["SGLang 深度拆解" (chenxutan.com) §1.3 (the CPU scheduler caches a
+ * request's sequence when it finishes); CS349D lecture-16 notes §3.1
+ * (continuous batching, the prompt inserted at prefill completion)] */
+int sgl_batch_append(sgl_tree* tree, int32_t B, int32_t* req_to_token, int64_t ld, int32_t* seq_lens,
+                     sgl_groups* groups);
+
+/* A request ends and its sequence is cached: the full pages of tokens[0,
+ * len) go into the tree with the slots of row (host, its req_to_token row),
+ * resuming at `last` (the node the request holds, whose path must be this
+ * sequence's prefix with these slots); duplicate pages go to the free list;
+ * then the request's reference is released and a partial tail page freed.
+ * *dup_len (may be NULL) = duplicate tokens freed.  SGL_ERR_STATE: `last`
+ * is stale or not referenced; SGL_ERR_INVALID_ARG: the path or the slots
+ * disagree (nothing changed). */
+int sgl_tree_cache_finished(sgl_tree* tree, sgl_node last, const int32_t* tokens, const int32_t* row, int64_t len,
+                            int64_t* dup_len);
+/* sgl_tree_cache_finished for requests 0 .. B-1 in order: tokens host array
+ * of B host pointers, last host [B], req_to_token host [B, ld], seq_lens
+ * host [B].  Stops at the first error and returns it. */
+int sgl_tree_cache_finished_batch(sgl_tree* tree, int32_t B, const int32_t* const* tokens, const sgl_node* last,
+                                  const int32_t* req_to_token, int64_t ld, const int32_t* seq_lens);
 
 int sgl_groups_create(sgl_groups** out);
 void sgl_groups_destroy(sgl_groups* groups);
@@ -437,7 +479,8 @@ int sgl_sim_run(sgl_tree* tree, const sgl_sim_config* cfg, int32_t n, const sgl_
  * same rows have been written: new token i of request r attends to the
  * cached positions 0..prefix_lens[r]-1 (read from the pool) and to new
  * tokens 0..i (read from k_new / v_new directly in the bf16 path; the fp32
- * path writes the pool first and reads it).  An out-of-pool slot is not
+ * and FP8-pool paths write the pool first and read it, so with an FP8 pool
+ * the new tokens are seen as their stored E4M3 values).  An out-of-pool slot is not
  * written and sets SGL_ERR_BOUNDS for sgl_check.  Repeated calls over the
  * chunks of a long prompt (prefix_lens = tokens already cached) are a
  * chunked prefill.

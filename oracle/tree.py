@@ -272,3 +272,49 @@ def build_batch(trie, batch_tokens):
             trie.free_slots(tail)
         raise
     return rows, lasts, private
+
+
+def append_step(trie, rows):
+    """One decode step of a running batch: every row gains one slot.
+
+    The new tokens are not inserted into the trie: a sequence is cached when
+    its request ends ("SGLang 深度拆解" (chenxutan.com) §1.3, the CPU
+    scheduler's first step; the CS349D lecture-16 notes §3.1 insert the
+    prompt at prefill completion and let the running request hold the
+    rest).  Reading: "SGLang 深度解读" section "2. Scheduler" also shows a
+    per-token insert of each decoded token; that variant is a sgl_build_batch
+    of the grown sequences each step.  A row whose length is a multiple of
+    the page size opens a fresh page (its first slot); any other row takes
+    the next slot of its own partial tail page.
+
+    Reading (the pages are silent on the order): the step's fresh pages come
+    from one allocation of (rows needing a page) x page_size tokens and are
+    handed to the rows in order.  ``rows`` (lists of slots) are extended in
+    place.
+    """
+    need = sum(1 for row in rows if len(row) % trie.P == 0)
+    fresh = trie.alloc(need * trie.P)
+    k = 0
+    for row in rows:
+        if len(row) % trie.P == 0:
+            row.append(fresh[k * trie.P])
+            k += 1
+        else:
+            row.append(row[-1] + 1)
+
+
+def cache_finished(trie, last, tokens, row):
+    """A request ends: insert its whole sequence (full pages) with its slots,
+    release the reference it held on ``last``, free its partial tail page.
+
+    Source: a finished request's sequence and KV pages are inserted into the
+    cache as the decode batch drops it ("SGLang 深度拆解" (chenxutan.com)
+    §1.3; "SGLang 深度解读" section "2. Scheduler"); references released
+    at request end (bhfrc.com/news/45689 §3.2).  Returns the duplicate
+    tokens the insert freed.
+    """
+    dup, _ = trie.insert(tokens, row)
+    trie.unlock(last)
+    n_full = (len(row) // trie.P) * trie.P
+    trie.free_slots(row[n_full:])
+    return dup

@@ -111,6 +111,10 @@ _SIGS = {
                                        _I32P, _I32P, _I64P, _P]),
     "sgl_tree_finish": (ctypes.c_int, [_P, ctypes.c_int64, _I32P, ctypes.c_int64]),
     "sgl_tree_finish_batch": (ctypes.c_int, [_P, ctypes.c_int32, _I64P, _I32P, ctypes.c_int64, _I32P]),
+    "sgl_batch_append": (ctypes.c_int, [_P, ctypes.c_int32, _I32P, ctypes.c_int64, _I32P, _P]),
+    "sgl_tree_cache_finished": (ctypes.c_int, [_P, ctypes.c_int64, _I32P, _I32P, ctypes.c_int64, _I64P]),
+    "sgl_tree_cache_finished_batch": (ctypes.c_int, [_P, ctypes.c_int32, ctypes.POINTER(_I32P), _I64P, _I32P,
+                                                     ctypes.c_int64, _I32P]),
     "sgl_groups_create": (ctypes.c_int, [ctypes.POINTER(_P)]),
     "sgl_groups_destroy": (None, [_P]),
     "sgl_groups_view": (ctypes.c_int, [_P, ctypes.POINTER(SglPrefixGroups)]),
@@ -344,6 +348,56 @@ def sgl_build_batch(tree, token_lists, ld=None, groups=None, req_to_token=None, 
     _ok(_lib().sgl_build_batch(tree, B, arr, lens.ctypes.data_as(_I64P), _ptr32(table), ld, _ptr32(seq),
                                _ptr32(pre), last.ctypes.data_as(_I64P), groups), "sgl_build_batch")
     return {"req_to_token": table, "seq_lens": seq, "prefix_lens": pre, "last_nodes": last}
+
+
+def sgl_batch_append(tree, req_to_token, seq_lens, groups=None):
+    """One decode step of a running batch, in place: row r of `req_to_token`
+    ([B, ld] int32, C-contiguous, writeable) gets a slot at position
+    seq_lens[r] and `seq_lens` ([B] int32) grows by one; `groups` (the
+    batch's prefix groups, or None) is updated to match."""
+    B = seq_lens.shape[0] if isinstance(seq_lens, np.ndarray) else -1
+    table = _out_i32(req_to_token, (B, req_to_token.shape[-1]), "req_to_token")
+    seq = _out_i32(seq_lens, (B,), "seq_lens")
+    _ok(_lib().sgl_batch_append(tree, B, _ptr32(table), table.shape[1], _ptr32(seq), groups), "sgl_batch_append")
+
+
+def sgl_tree_cache_finished(tree, last, tokens, row, length):
+    """Cache a finished request's sequence and release it; returns the
+    duplicate tokens freed."""
+    t, r = _i32(tokens), _i32(row)
+    if t.shape[0] < length or r.shape[0] < length:
+        raise ValueError("tokens and row must hold `length` entries")
+    dup = ctypes.c_int64(0)
+    _ok(_lib().sgl_tree_cache_finished(tree, int(last), _ptr32(t), _ptr32(r), int(length), ctypes.byref(dup)),
+        "sgl_tree_cache_finished")
+    return dup.value
+
+
+def sgl_tree_cache_finished_batch(tree, tokens, out):
+    """sgl_tree_cache_finished for every request of a batch: `tokens` is a
+    [B, cap] int32 token matrix (row r holds at least out["seq_lens"][r]
+    tokens) or a list of B token arrays; `out` a sgl_build_batch result
+    (its dict), possibly advanced by sgl_batch_append."""
+    last = np.ascontiguousarray(out["last_nodes"], dtype=np.int64)
+    table = np.ascontiguousarray(out["req_to_token"], dtype=np.int32)
+    seq = _i32(out["seq_lens"])
+    B = len(seq)
+    if isinstance(tokens, np.ndarray) and tokens.ndim == 2:
+        if tokens.dtype != np.int32 or not tokens.flags.c_contiguous or tokens.shape[0] != B:
+            raise ValueError("a token matrix must be C-contiguous int32 with B rows")
+        if B and int(seq.max()) > tokens.shape[1]:
+            raise ValueError("a row of the token matrix is shorter than its length")
+        keep = tokens
+        ptrs = np.arange(B, dtype=np.uint64) * np.uint64(4 * tokens.shape[1]) + np.uint64(tokens.ctypes.data)
+    else:
+        keep = [_i32(x) for x in tokens]
+        if len(keep) != B or any(k.shape[0] < n for k, n in zip(keep, seq)):
+            raise ValueError("one token array of at least seq_lens[r] tokens per request")
+        ptrs = np.array([k.ctypes.data for k in keep] or [0], dtype=np.uint64)
+    arr = ptrs.ctypes.data_as(ctypes.POINTER(_I32P))
+    _ok(_lib().sgl_tree_cache_finished_batch(tree, B, arr, last.ctypes.data_as(_I64P), _ptr32(table), table.shape[1],
+                                             _ptr32(seq)), "sgl_tree_cache_finished_batch")
+    del keep
 
 
 def sgl_tree_finish(tree, last, row, length):

@@ -593,6 +593,148 @@ int sgl_tree_finish_batch(sgl_tree* t, int32_t B, const sgl_node* last, const in
     return SGL_OK;
 }
 
+// One decode step of a running batch.  The new tokens stay out of the tree
+// until their request ends (the CPU scheduler of "SGLang 深度拆解" §1.3
+// caches a sequence when its request finishes; the CS349D notes §3.1 insert
+// the prompt at prefill completion): each row gets one slot, from a fresh page
+// when its length is a multiple of the page size, else the next slot of its
+// private tail page.  The fresh pages of the step are allocated in one call
+// and handed out in request order.
+int sgl_batch_append(sgl_tree* t, int32_t B, int32_t* req_to_token, int64_t ld, int32_t* seq_lens,
+                     sgl_groups* g) {
+    if (!t || B < 0 || ld < 1 || (B > 0 && (!req_to_token || !seq_lens))) return SGL_ERR_INVALID_ARG;
+    const int32_t P = t->P;
+    const int64_t S = t->num_pages * P;
+    int64_t need = 0;
+    for (int32_t r = 0; r < B; ++r) {
+        const int64_t L = seq_lens[r];
+        if (L < 0 || L >= ld) return SGL_ERR_INVALID_ARG;
+        if (L % P == 0) {
+            ++need;
+        } else {
+            const int32_t prev = req_to_token[(int64_t)r * ld + L - 1];
+            if (prev < 0 || prev + 1 >= S || (prev + 1) % P == 0) return SGL_ERR_INVALID_ARG;
+        }
+    }
+    // each request's last segment: the one of its segments that ends at its length
+    std::vector<int32_t> last_seg;
+    if (g) {
+        last_seg.assign(B, -1);
+        const int32_t ns = (int32_t)g->seg_begin.size();
+        for (int32_t s = 0; s < ns; ++s) {
+            for (int32_t k = g->seg_member_ptr[s]; k < g->seg_member_ptr[s + 1]; ++k) {
+                const int32_t m = g->seg_members[k];
+                if (m < 0 || m >= B) return SGL_ERR_INVALID_ARG;
+                if (g->seg_end[s] == seq_lens[m]) last_seg[m] = s;
+            }
+        }
+        for (int32_t r = 0; r < B; ++r)
+            if (seq_lens[r] > 0 && last_seg[r] < 0) return SGL_ERR_INVALID_ARG;
+    }
+    std::vector<int32_t> fresh;
+    if (!t->alloc(need * P, &fresh)) return SGL_ERR_NO_SLOTS;
+    int64_t k = 0;
+    bool new_segs = false;
+    for (int32_t r = 0; r < B; ++r) {
+        int32_t* row = req_to_token + (int64_t)r * ld;
+        const int32_t L = seq_lens[r];
+        row[L] = L % P == 0 ? fresh[(k++) * P] : row[L - 1] + 1;
+        seq_lens[r] = L + 1;
+        if (g) {
+            const int32_t s = last_seg[r];
+            if (s >= 0 && g->seg_member_ptr[s + 1] - g->seg_member_ptr[s] == 1) {
+                g->seg_end[s] = L + 1;   // a private trailing segment grows
+                last_seg[r] = -2;
+            } else {
+                new_segs = true;
+            }
+        }
+    }
+    if (new_segs) {
+        // requests whose context ended in a shared segment (or was empty) get
+        // a private one-token segment; the order stays (seg_row, seg_begin)
+        struct Row {
+            int32_t rep, begin, end, m0, m1;
+        };
+        std::vector<Row> rows;
+        const int32_t ns = (int32_t)g->seg_begin.size();
+        for (int32_t s = 0; s < ns; ++s)
+            rows.push_back({g->seg_row[s], g->seg_begin[s], g->seg_end[s], g->seg_member_ptr[s],
+                            g->seg_member_ptr[s + 1]});
+        std::vector<int32_t> solo;
+        for (int32_t r = 0; r < B; ++r)
+            if (last_seg[r] != -2) solo.push_back(r);
+        for (int32_t r : solo) rows.push_back({r, seq_lens[r] - 1, seq_lens[r], -1 - r, 0});
+        std::stable_sort(rows.begin(), rows.end(), [](const Row& a, const Row& b) {
+            return a.rep != b.rep ? a.rep < b.rep : a.begin < b.begin;
+        });
+        sgl_groups n;
+        n.clear();
+        for (const Row& x : rows) {
+            n.seg_begin.push_back(x.begin);
+            n.seg_end.push_back(x.end);
+            n.seg_row.push_back(x.rep);
+            if (x.m0 < 0) {
+                n.seg_members.push_back(-1 - x.m0);
+            } else {
+                n.seg_members.insert(n.seg_members.end(), g->seg_members.begin() + x.m0,
+                                     g->seg_members.begin() + x.m1);
+            }
+            n.seg_member_ptr.push_back((int32_t)n.seg_members.size());
+        }
+        *g = std::move(n);
+    }
+    return SGL_OK;
+}
+
+// A request ends: its whole sequence goes into the tree ("SGLang 深度拆解"
+// §1.3, completed sequences are cached), resuming at the node it holds, then
+// its reference is released and a partial tail page freed.
+int sgl_tree_cache_finished(sgl_tree* t, sgl_node last, const int32_t* tokens, const int32_t* row, int64_t len,
+                            int64_t* dup_len) {
+    if (!t || len < 0 || (len > 0 && (!tokens || !row))) return SGL_ERR_INVALID_ARG;
+    Node* n = t->node_of(last);
+    if (!n) return SGL_ERR_STATE;
+    for (Node* x = n; x != &t->root; x = x->parent)
+        if (x->ref <= 0) return SGL_ERR_STATE;
+    const int32_t P = t->P;
+    const int64_t end = n == &t->root ? 0 : n->depth + (int64_t)n->tokens.size();
+    if (end > len) return SGL_ERR_INVALID_ARG;
+    // the held path must be this sequence's own prefix, with its slots
+    for (Node* x = n; x != &t->root; x = x->parent) {
+        const int64_t d = x->depth, m = (int64_t)x->tokens.size();
+        if (std::memcmp(x->tokens.data(), tokens + d, m * sizeof(int32_t)) != 0) return SGL_ERR_INVALID_ARG;
+        for (int64_t i = 0; i < m / P; ++i)
+            if (row[d + i * P] != x->pages[i] * P) return SGL_ERR_INVALID_ARG;
+    }
+    const int64_t n_full = len / P * P;
+    std::vector<int32_t> pages;
+    if (!t->pages_of(row + end, n_full - end, &pages)) return SGL_ERR_INVALID_ARG;
+    if (len > n_full) {
+        for (int64_t i = n_full; i < len; ++i)
+            if (row[i] < 0 || row[i] / P >= t->num_pages) return SGL_ERR_INVALID_ARG;
+    }
+    int64_t dup = 0;
+    t->insert_from(n, tokens, pages.data(), n_full, &dup);
+    t->unlock(n);
+    if (len > n_full) t->free_slots(row + n_full, len - n_full);
+    if (dup_len) *dup_len = dup;
+    return SGL_OK;
+}
+
+int sgl_tree_cache_finished_batch(sgl_tree* t, int32_t B, const int32_t* const* tokens, const sgl_node* last,
+                                  const int32_t* req_to_token, int64_t ld, const int32_t* seq_lens) {
+    if (!t || B < 0 || ld < 0 || (B > 0 && (!tokens || !last || !req_to_token || !seq_lens)))
+        return SGL_ERR_INVALID_ARG;
+    for (int32_t r = 0; r < B; ++r) {
+        if (seq_lens[r] < 0 || seq_lens[r] > ld) return SGL_ERR_INVALID_ARG;
+        const int st = sgl_tree_cache_finished(t, last[r], tokens[r], req_to_token + (int64_t)r * ld, seq_lens[r],
+                                               nullptr);
+        if (st) return st;
+    }
+    return SGL_OK;
+}
+
 int sgl_groups_from_table(const int32_t* table, int64_t ld, const int32_t* seq_lens, int32_t B,
                           sgl_groups* g) {
     if (!g || B < 0 || (B > 0 && (!table || !seq_lens))) return SGL_ERR_INVALID_ARG;

@@ -306,3 +306,164 @@ def test_build_batch_from_token_matrix():
     finally:
         for t in trees:
             sgl.sgl_tree_destroy(t)
+
+
+def _append_run(P, seed, steps):
+    """A batch built, advanced `steps` decode steps with sgl_batch_append and
+    cached with sgl_tree_cache_finished_batch, against the oracle's
+    append_step / cache_finished on the same operations."""
+    from oracle.tree import append_step, cache_finished
+    rnd = random.Random(seed * 7 + P)
+    pages = rnd.choice([24, 40, 400])
+    pair = Pair(pages, P, rnd.sample(range(pages), pages))
+    try:
+        # some cache first (finished requests), so that appends may evict
+        for _ in range(3):
+            base = [rnd.randint(0, 2) for _ in range(rnd.randint(0, 9))]
+            pair.batch([base + [rnd.randint(0, 2) for _ in range(rnd.randint(0, 6))] for _ in range(2)])
+            while pair.live:
+                pair.finish(0)
+        base = [rnd.randint(0, 2) for _ in range(rnd.randint(0, 12))]
+        seqs = []
+        for _ in range(rnd.randint(1, 5)):
+            if seqs and rnd.random() < 0.3:
+                seqs.append(list(seqs[0]))     # an identical request: its context ends in a shared segment
+            else:
+                seqs.append(base[:rnd.randint(0, len(base))] + [rnd.randint(0, 2) for _ in range(rnd.randint(0, 5))])
+        try:
+            rows, lasts, _ = build_batch(pair.o, seqs)
+        except NoSlotsError:
+            return "no slots at build"
+        B = len(seqs)
+        ld = max(len(s) for s in seqs) + steps
+        g = sgl.sgl_groups_create()
+        out = sgl.sgl_build_batch(pair.t, seqs, ld=ld, groups=g)
+        table, seq = out["req_to_token"], out["seq_lens"]
+        toks = np.zeros((B, ld), dtype=np.int32)
+        for r, s in enumerate(seqs):
+            toks[r, :len(s)] = s
+        # identical requests keep generating identical tokens half of the time
+        same = rnd.random() < 0.5
+        status = "ok"
+        for step in range(steps):
+            try:
+                append_step(pair.o, rows)
+                failed = False
+            except NoSlotsError:
+                failed = True
+            if failed:
+                with pytest.raises(sgl.SglError) as e:
+                    sgl.sgl_batch_append(pair.t, table, seq, g)
+                assert e.value.status == -2
+                status = "no slots at step %d" % step
+                pair.check_stats()
+                break
+            sgl.sgl_batch_append(pair.t, table, seq, g)
+            new = [rnd.randint(0, 2) for _ in range(B)]
+            for r in range(B):
+                if same and seqs[r] == seqs[0] and toks[r, :seq[r] - 1].tolist() == toks[0, :seq[0] - 1].tolist():
+                    new[r] = new[0]
+                toks[r, seq[r] - 1] = new[r]
+            for r, row in enumerate(rows):
+                assert seq[r] == len(row)
+                assert table[r, :len(row)].tolist() == list(row)
+                assert np.all(table[r, len(row):] == -1)
+            ogroups = prefix_groups(table, seq)
+            _groups_eq(_lib_groups(g), ogroups)
+            pair.check_stats()
+        for r in range(B):
+            cache_finished(pair.o, lasts[r], toks[r, :len(rows[r])].tolist(), rows[r])
+        sgl.sgl_tree_cache_finished_batch(pair.t, toks, out)
+        sgl.sgl_groups_destroy(g)
+        pair.check_stats()
+        assert sgl.sgl_tree_stats(pair.t)["locked_tokens"] == 0
+        # the same cache: the same matches of every finished sequence, the same eviction
+        for r in range(B):
+            pair.match(toks[r, :len(rows[r])].tolist())
+        pair.evict(rnd.randint(1, 4 * P))
+        pair.alloc_free(rnd.randint(0, 3 * P))
+        pair.check_stats()
+        return status
+    finally:
+        pair.close()
+
+
+@pytest.mark.parametrize("P", [1, 2, 4])
+@pytest.mark.parametrize("seed", range(20))
+def test_append_and_cache_finished_bit_exact(P, seed):
+    _append_run(P, seed, steps=1 + seed % 9)
+
+
+def test_append_runs_out_of_slots_like_the_oracle():
+    """Small pools: some runs end with SGL_ERR_NO_SLOTS at an append, as the
+    oracle does at the same step."""
+    statuses = [_append_run(P, 100 + s, steps=60) for P in (1, 2) for s in range(12)]
+    assert any(st.startswith("no slots at step") for st in statuses), statuses
+
+
+def test_append_growing_batch_keeps_the_tree_small():
+    """Decode steps through sgl_batch_append leave the tree alone: its node
+    count after many steps equals the count after the build, and the groups
+    still equal those computed from the table."""
+    w = W.get("llama3_8b_decode_small")
+    seqs = W.make_batch(w, 0).all_tokens()
+    S = 1 << 15
+    t = sgl.sgl_tree_create(S, 1, np.arange(S, dtype=np.int32))
+    g = sgl.sgl_groups_create()
+    steps = 40
+    try:
+        out = sgl.sgl_build_batch(t, seqs, ld=max(len(s) for s in seqs) + steps, groups=g)
+        n0 = sgl.sgl_tree_stats(t)["num_nodes"]
+        for _ in range(steps):
+            sgl.sgl_batch_append(t, out["req_to_token"], out["seq_lens"], g)
+        assert sgl.sgl_tree_stats(t)["num_nodes"] == n0
+        _groups_eq(_lib_groups(g), prefix_groups(out["req_to_token"], out["seq_lens"]))
+        g2 = sgl.sgl_groups_create()
+        sgl.sgl_groups_from_table(out["req_to_token"], out["seq_lens"], g2)
+        _groups_eq(_lib_groups(g), _lib_groups(g2))
+        sgl.sgl_groups_destroy(g2)
+    finally:
+        sgl.sgl_groups_destroy(g)
+        sgl.sgl_tree_destroy(t)
+
+
+def test_append_and_cache_finished_refuse_bad_input():
+    t = sgl.sgl_tree_create(64, 2, np.arange(32, dtype=np.int32))
+    g = sgl.sgl_groups_create()
+    try:
+        seqs = [[1, 2, 3], [1, 2, 3, 4]]
+        out = sgl.sgl_build_batch(t, seqs, ld=4, groups=g)
+        before = sgl.sgl_tree_stats(t)
+        tab, seq = out["req_to_token"], out["seq_lens"]
+        with pytest.raises(sgl.SglError) as e:      # row 1 is already ld long
+            sgl.sgl_batch_append(t, tab, seq, g)
+        assert e.value.status == -1
+        assert seq.tolist() == [3, 4] and sgl.sgl_tree_stats(t) == before
+        empty = sgl.sgl_groups_create()
+        tab2 = np.full((2, 8), -1, dtype=np.int32)
+        tab2[:, :4] = tab
+        with pytest.raises(sgl.SglError) as e:      # groups of another batch
+            sgl.sgl_batch_append(t, tab2, seq, empty)
+        assert e.value.status == -1
+        sgl.sgl_groups_destroy(empty)
+        bad = tab2.copy()
+        bad[0, 2] = bad[0, 2] + 1                   # tail slot followed by another page's slot
+        with pytest.raises(sgl.SglError) as e:
+            sgl.sgl_batch_append(t, bad, seq.copy(), None)
+        assert e.value.status == -1
+        assert sgl.sgl_tree_stats(t) == before
+        last = int(out["last_nodes"][1])
+        with pytest.raises(sgl.SglError) as e:      # tokens disagree with the held path
+            sgl.sgl_tree_cache_finished(t, last, [1, 9, 3, 4], tab[1], 4)
+        assert e.value.status == -1
+        with pytest.raises(sgl.SglError) as e:      # slots disagree with the held path
+            sgl.sgl_tree_cache_finished(t, last, [1, 2, 3, 4], tab[0][[0, 1, 2, 2]] * 0 + 30, 4)
+        assert e.value.status == -1
+        assert sgl.sgl_tree_stats(t) == before
+        assert sgl.sgl_tree_cache_finished(t, last, [1, 2, 3, 4], tab[1], 4) == 0
+        with pytest.raises(sgl.SglError) as e:      # its reference is gone
+            sgl.sgl_tree_cache_finished(t, last, [1, 2, 3, 4], tab[1], 4)
+        assert e.value.status == -6
+    finally:
+        sgl.sgl_groups_destroy(g)
+        sgl.sgl_tree_destroy(t)
