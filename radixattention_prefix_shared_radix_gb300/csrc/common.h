@@ -39,10 +39,12 @@ struct DecItem {
 };
 static_assert(sizeof(DecItem) == 32, "DecItem is 32 bytes");
 
-// Decode schedule constant (bf16 persistent kernel): a narrow piece covers up
-// to kDecHeadBlock KV heads of its positions (one consumer warp each); each
-// CTA runs one stream of such pieces, fed by one producer warp.
+// Decode schedule constants (bf16 persistent kernel): a narrow piece covers
+// up to kDecHeadBlock KV heads of its positions (one or two consumer warps
+// each) for up to kDecPieceMembers member requests (the member slots of the
+// kernel's lookup ring entry).
 constexpr int kDecHeadBlock = 8;
+constexpr int kDecPieceMembers = 8;
 
 // Workspace header (first 256 bytes): error word + plan dimensions.
 struct WsHeader {

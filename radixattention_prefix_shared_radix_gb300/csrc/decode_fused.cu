@@ -44,14 +44,16 @@
 // consumers' ldmatrix reads need no swizzle (a bulk copy lands a whole row
 // contiguously).  Per stage a FULL mbarrier (the producer's arrival with the
 // stage's byte count; the copies complete it), an EMPTY mbarrier (one
-// arrival per consumer warp) and a 32-byte descriptor (first position,
-// piece, flags).  The lookup warp fills a slot ring of 8 steps (4-byte
-// cp.async of each step's slots, plus the piece fields), so no producer
-// register ever waits on a load in flight.  A piece's query rows land in
-// the Q slot with its first stage
-// (one bulk copy per member and KV head: the head's G query heads are
-// consecutive rows of q); the consumers release the slot (QEMPTY) once
-// their fragments are in registers.
+// arrival per consumer warp) and a 64-byte descriptor (first position,
+// flags; for a piece's first step the piece's fields and member requests).
+// The lookup warp fills a slot ring of 8 steps (4-byte cp.async of each
+// step's slots, plus the piece fields), so no producer register ever waits
+// on a load in flight.  At a piece's first step each consumer lane loads its
+// query row's fragment straight from q (L2-resident: q is read by every
+// piece of its requests); nothing in the ring waits for the consumers to be
+// done with the previous piece, so the next piece's copies are in flight
+// while they finish it (measured: a Q slot refilled between pieces left the
+// ring empty for ~2 us at every piece boundary).
 //
 // Consumer warp, per 16-position step, for its KV head and 8 query rows of
 // the piece (mma.sync m16n8k16, bf16 in, fp32 acc; the query rows in the
@@ -59,8 +61,8 @@
 //   S^T [16 pos x 8 rows] = K [16 x d] . Q^T [d x 8 rows]
 //   O^T [d x 8 rows]     += V^T [d x 16 pos] . P^T [16 pos x 8 rows]
 // ldmatrix for K, ldmatrix.trans for V^T; P^T moves from the accumulator
-// layout to the B-operand layout with movmatrix.  The consumers' loop
-// touches nothing but shared memory.
+// layout to the B-operand layout with movmatrix.  Apart from a piece's
+// query fragments, the consumers' loop touches nothing but shared memory.
 //
 // Every item writes normalised partial rows (O fp32, LSE natural log); the
 // merge launch (merge.cuh) combines each (request, KV head)'s partials once
@@ -96,26 +98,25 @@ struct FusedLayout {
     static constexpr int ES = F8 ? 1 : 2;                // bytes per pool element
     static constexpr int PITCH = kHB * D * ES + 16;      // one token's K (or V) row of a head block, padded
     static constexpr int STAGE = 2 * kNP * PITCH;        // K rows, then V rows
-    static constexpr int QSLOT = kHB * 8 * D * 2;        // [head][8 or 16 rows][d] bf16 (8 x 8 or 4 x 16)
     static constexpr int SLOTW = kSQ * kSlotEntry;
-    static constexpr int FIXED = 1024 + QSLOT + SLOTW + 8 * 32 + 64 + (2 * 8 + 1 + 2 * kSQ) * 8 + 1024;
+    static constexpr int DESC = 64;                      // stage descriptor bytes
+    static constexpr int FIXED = 1024 + SLOTW + 8 * DESC + 64 + (2 * 8 + 2 * kSQ) * 8 + 1024;
     static constexpr int NSF0 = (232448 - FIXED) / STAGE;
     static constexpr int NSF = NSF0 > 8 ? 8 : NSF0;      // ring stages
     // Layout: the tile roles' TMEM address and broadcast area (up to
-    // TL::KEEP); from 1024 the ring, the Q slot, the slot ring and the stage
+    // TL::KEEP); from 1024 the ring, the slot ring and the stage
     // descriptors.  These are used only once the CTA's tiles are done, so
     // they overlap the rest of the tile roles' area (TL::KEEP .. TL::END:
     // stages, barriers, staging).  The streaming barriers, initialised at
     // launch, come after everything.
     static constexpr int OFF_RING = 1024;
-    static constexpr int OFF_Q = OFF_RING + NSF * STAGE;
-    static constexpr int OFF_SLOT = OFF_Q + QSLOT;
+    static constexpr int OFF_SLOT = OFF_RING + NSF * STAGE;
     static constexpr int OFF_DESC = OFF_SLOT + SLOTW;
-    static constexpr int OFF_LREC = OFF_DESC + NSF * 32;   // launch piece: record (32 B), members (32 B)
+    static constexpr int OFF_LREC = OFF_DESC + NSF * DESC;   // launch piece: record (32 B), members (32 B)
     static constexpr int END_S = OFF_LREC + 64;
-    // FULL[NSF], EMPTY[NSF], QEMPTY, SLOTFULL[kSQ], SLOTFREE[kSQ]
+    // FULL[NSF], EMPTY[NSF], SLOTFULL[kSQ], SLOTFREE[kSQ]
     static constexpr int OFF_SBAR = ((END_S > TL::END ? END_S : TL::END) + 7) / 8 * 8;
-    static constexpr int END = OFF_SBAR + (2 * NSF + 1 + 2 * kSQ) * 8;
+    static constexpr int END = OFF_SBAR + (2 * NSF + 2 * kSQ) * 8;
     static constexpr int TOTAL = END + 1024;             // + alignment slack
     static_assert(NSF >= 3, "ring depth");
     static_assert(OFF_SBAR >= TL::END && OFF_SBAR >= END_S, "streaming barriers clear of every other area");
@@ -161,14 +162,17 @@ __device__ __forceinline__ void lds64(uint32_t addr, uint32_t* w) {
 }
 
 // stage descriptor flags
-constexpr int kFirst = 1;   // first step of its piece: its query rows are in the Q slot
+constexpr int kFirst = 1;   // first step of its piece: the descriptor carries the piece's fields
 constexpr int kEnd = 4;     // no more pieces: the consumers stop
 
 // slot-ring entry (one looked-up step): 16 slots, then
 constexpr int kEntKvh = 64, kEntP0 = 68, kEntFlags = 72, kEntCm = 76, kEntPb = 80, kEntNh = 84, kEntNm = 88;
-constexpr int kEntMem = 96;   // 8 ints: the piece's member requests (first step only)
-// stage descriptor
-constexpr int kDescP0 = 0, kDescFlags = 4, kDescCm = 8, kDescPb = 12, kDescRows = 16, kDescNh = 20;
+constexpr int kEntMem = 96;   // kDecPieceMembers ints: the piece's member requests (first step only)
+static_assert(kEntMem + 4 * kDecPieceMembers <= kSlotEntry, "a slot entry holds a piece's members");
+// stage descriptor (a piece's first step also carries the piece's first KV
+// head and member requests, from which the consumers load their query rows)
+constexpr int kDescP0 = 0, kDescFlags = 4, kDescCm = 8, kDescPb = 12, kDescRows = 16, kDescNh = 20, kDescKvh = 24;
+constexpr int kDescMem = 32;   // kDecPieceMembers ints
 
 // ---------------------------------------------------------------------------
 // Lookup warp (one per CTA)
@@ -199,8 +203,10 @@ __device__ __noinline__ void stream_lookup(const FusedArgs& f, int gw, uint32_t 
     const bool launch = gw >= 0 && gw < f.n_init;
     bool timed_out = false;
     int nlook = 0;
-    // one ring entry: wait for it to be free, fill it, arm its barrier
-    auto entry = [&](int kvh, int row, int p0, int e, int flags, int cm, int pb, int nh, int nm, int mem) {
+    // one ring entry: wait for it to be free, fill it, arm its barrier.  A
+    // piece's first entry also records its end clamped to seq_len (len, whose
+    // load is only waited for once the slot lookups are issued)
+    auto entry = [&](int kvh, int row, int p0, int e, int flags, int len, int pb, int nh, int nm, int mem) {
         const int ent = nlook & (kSQ - 1);
         const uint32_t eb = sring + ent * kSlotEntry;
         if (!timed_out && !mbar_wait(sfree + 8 * ent, ((nlook / kSQ) & 1) ^ 1)) {
@@ -220,13 +226,18 @@ __device__ __noinline__ void stream_lookup(const FusedArgs& f, int gw, uint32_t 
             st_shared_s32(eb + kEntP0, p0);
             st_shared_s32(eb + kEntFlags, flags);
             if (flags & kFirst) {
+                int cm = e;
+                if (e > len) {   // planned beyond seq_len: mask the excess, flag it
+                    atomicOr(err, 2u);
+                    cm = len > p0 ? len : p0;
+                }
                 st_shared_s32(eb + kEntCm, cm);
                 st_shared_s32(eb + kEntPb, pb);
                 st_shared_s32(eb + kEntNh, nh);
                 st_shared_s32(eb + kEntNm, nm);
             }
         }
-        if ((flags & kFirst) && lane < 8) st_shared_s32(eb + kEntMem + 4 * lane, mem);
+        if ((flags & kFirst) && lane < kDecPieceMembers) st_shared_s32(eb + kEntMem + 4 * lane, mem);
         cp_async_arrive_noinc(sfull + 8 * ent);   // each lane, once its lookups have landed
         __syncwarp();
         if (lane == 0) mbar_arrive(sfull + 8 * ent);   // the fields
@@ -239,7 +250,7 @@ __device__ __noinline__ void stream_lookup(const FusedArgs& f, int gw, uint32_t 
             row = ld_shared_s32(lrec); b = ld_shared_s32(lrec + 4); e = ld_shared_s32(lrec + 8);
             kvh = ld_shared_s32(lrec + 12); mb = ld_shared_s32(lrec + 16); nm = ld_shared_s32(lrec + 20);
             pb = ld_shared_s32(lrec + 24); nh = ld_shared_s32(lrec + 28);
-            mem = lane < 8 ? ld_shared_s32(lrec + 32 + 4 * lane) : 0;
+            mem = lane < kDecPieceMembers ? ld_shared_s32(lrec + 32 + 4 * lane) : 0;
         } else {
             int taken = 0;
             if (lane == 0) taken = (int)atomicAdd(sched, 1u);
@@ -253,13 +264,8 @@ __device__ __noinline__ void stream_lookup(const FusedArgs& f, int gw, uint32_t 
         }
         first_piece = false;
         const int len = __ldg(seq_lens + row);
-        int cm = e;
-        if (e > len) {   // planned beyond seq_len: mask the excess, flag it
-            if (lane == 0) atomicOr(err, 2u);
-            cm = len > b ? len : b;
-        }
         for (int sp = b; sp < e; sp += kNP)
-            entry(kvh, row, sp, e, sp == b ? kFirst : 0, cm, pb, nh, nm, mem);
+            entry(kvh, row, sp, e, sp == b ? kFirst : 0, len, pb, nh, nm, mem);
     }
     entry(-1, 0, 0, 0, 0, 0, 0, 0, 0, 0);   // the end of the stream
     cp_async_wait<0>();
@@ -284,13 +290,14 @@ __device__ __noinline__ void stream_lookup(const FusedArgs& f, int gw, uint32_t 
 // row 8p + t of the stage (rows 0-15 the K rows of the step's 16 positions,
 // 16-31 the V rows).  Measured on GB300: one warp gets a bulk copy through
 // about every 100 cycles, so four warps share the stage's 32 row copies.
-// Producer 0 also writes the stage descriptor and, for a piece's first step,
-// copies its query rows into the Q slot once the consumers have released it.
-// The entry is freed once read.
+// Producer 0 also writes the stage descriptor (for a piece's first step
+// with the piece's fields and member requests).  A piece's first step waits
+// for nothing but a free stage, so the next piece's data is in flight while
+// the consumers finish the last one.  The entry is freed once read.
 template <int D, bool F8>
 __device__ __noinline__ void stream_producer(const FusedArgs& f, int pw, uint32_t ring, uint32_t sring,
-                                             uint32_t desc, uint32_t qbuf, uint32_t full, uint32_t empty,
-                                             uint32_t qempty, uint32_t sfull, uint32_t sfree, int lane) {
+                                             uint32_t desc, uint32_t full, uint32_t empty, uint32_t sfull,
+                                             uint32_t sfree, int lane) {
     using Lay = FusedLayout<D, F8>;
     constexpr int NS = Lay::NSF;
     constexpr int ES = Lay::ES;
@@ -299,9 +306,8 @@ __device__ __noinline__ void stream_producer(const FusedArgs& f, int pw, uint32_
     // argument fields in registers: every asm below clobbers memory
     const uint8_t* const kp = reinterpret_cast<const uint8_t*>(f.t.kp);
     const uint8_t* const vp = reinterpret_cast<const uint8_t*>(f.t.vp);
-    const bf16* const qp = f.t.q;
     uint32_t* const err = f.t.err;
-    const int Hq = f.t.Hq, Hkv = f.t.Hkv, G = f.t.G;
+    const int Hkv = f.t.Hkv, G = f.t.G;
     const int64_t num_slots = f.t.num_slots;
     // streamed K/V rows are read once: evict them from L2 first, which keeps
     // the code, the tables and the partial rows there across calls
@@ -315,7 +321,6 @@ __device__ __noinline__ void stream_producer(const FusedArgs& f, int pw, uint32_
     // barriers (the consumers' and the lookup warp's own bounded waits end
     // their loops).
     bool timed_out = false;
-    int nq = 0;            // pieces started (Q slot uses)
     int cur_nh = 0;        // KV heads of the piece being issued
     int last_armed = -1;   // last step whose FULL phase this warp's copies complete
     int last_arrived = -1; // last step that arrived on a FULL barrier (armed, or the end marker)
@@ -335,7 +340,7 @@ __device__ __noinline__ void stream_producer(const FusedArgs& f, int pw, uint32_
             timed_out = true;
             break;
         }
-        const uint32_t db = desc + st * 32;
+        const uint32_t db = desc + st * Lay::DESC;
         const uint32_t fb = full + 8 * st;
         const uint32_t sb = ring + st * Lay::STAGE;
         if (kvh < 0) {
@@ -349,16 +354,7 @@ __device__ __noinline__ void stream_producer(const FusedArgs& f, int pw, uint32_
             break;
         }
         const bool first = (flags & kFirst) != 0;
-        int nm = 0;
-        if (first) {
-            cur_nh = ld_shared_s32(eb + kEntNh);
-            nm = ld_shared_s32(eb + kEntNm);
-            if (lead && !mbar_wait(qempty, (nq & 1) ^ 1)) {
-                atomicOr(err, 4u);
-                timed_out = true;
-                break;
-            }
-        }
+        if (first) cur_nh = ld_shared_s32(eb + kEntNh);
         const uint32_t rowb = (uint32_t)(cur_nh * D * ES);
         int32_t sl = mine ? ld_shared_s32(eb + tok * 4) : kPastEnd;
         bool ok = mine && sl != kPastEnd;
@@ -381,43 +377,26 @@ __device__ __noinline__ void stream_producer(const FusedArgs& f, int pw, uint32_
             // the stage's next use writes these rows through the async proxy
             fence_proxy_async_smem();
         }
-        uint32_t bytes = (uint32_t)__popc(vmask) * rowb;
-        // the lead's first step also carries the piece's query rows: member
-        // i's G query heads of KV head kvh + hh are G consecutive rows of q
-        const int nqc = (first && lead) ? nm * cur_nh : 0;   // query copies (at most 64)
-        bytes += (uint32_t)(nqc * G * D * 2);
+        const uint32_t bytes = (uint32_t)__popc(vmask) * rowb;
         if (lead && lane == 0) {
             st_shared_s32(db + kDescP0, ld_shared_s32(eb + kEntP0));
             st_shared_s32(db + kDescFlags, flags);
             if (first) {
                 st_shared_s32(db + kDescCm, ld_shared_s32(eb + kEntCm));
                 st_shared_s32(db + kDescPb, ld_shared_s32(eb + kEntPb));
-                st_shared_s32(db + kDescRows, nm * G);
+                st_shared_s32(db + kDescRows, ld_shared_s32(eb + kEntNm) * G);
                 st_shared_s32(db + kDescNh, cur_nh);
+                st_shared_s32(db + kDescKvh, kvh);
             }
         }
-        int qmem0 = 0, qmem1 = 0;   // members of this lane's query copies (k = lane, lane + 32)
-        if (nqc > 0) {
-            const int k0 = lane, k1 = lane + 32;
-            if (k0 < nqc) qmem0 = ld_shared_s32(eb + kEntMem + 4 * (k0 / cur_nh));
-            if (k1 < nqc) qmem1 = ld_shared_s32(eb + kEntMem + 4 * (k1 / cur_nh));
-        }
+        if (lead && first && lane < kDecPieceMembers)
+            st_shared_s32(db + kDescMem + 4 * lane, ld_shared_s32(eb + kEntMem + 4 * lane));
         __syncwarp();
         if (lane == 0) mbar_expect_tx(fb, bytes);   // the arrival, plus the bytes the copies complete
         __syncwarp();
         if (ok)
             bulk_g2s_pol(sb + (uint32_t)((idx >> 4) * kNP + tok) * Lay::PITCH,
                          (idx < kNP ? kp : vp) + ((int64_t)sl * Hkv + kvh) * (D * ES), rowb, fb, kv_pol);
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const int k = lane + 32 * j;
-            if (k < nqc) {
-                const int qi = k / cur_nh, qh = k - qi * cur_nh;
-                bulk_g2s(qbuf + (uint32_t)((qh * (nm * G > 8 ? 16 : 8) + qi * G) * D * 2),
-                         qp + ((int64_t)(j ? qmem1 : qmem0) * Hq + (kvh + qh) * G) * D, (uint32_t)(G * D * 2), fb);
-            }
-        }
-        if (first && lead) ++nq;
         last_armed = last_arrived = r;
         __syncwarp();   // every lane has read the entry
         if (lane == 0) mbar_arrive(sfree + 8 * ent);
@@ -435,11 +414,12 @@ __device__ __noinline__ void stream_producer(const FusedArgs& f, int pw, uint32_
 // ---------------------------------------------------------------------------
 // Consumer warp c: 8 query rows of one KV head of each piece (idle, but
 // keeping the barrier counts, when the piece has fewer heads or rows); only
-// shared memory in its loop (stages, descriptors, Q slot)
+// shared memory in its loop (stages, descriptors) but for a piece's query
+// fragments
 // ---------------------------------------------------------------------------
 template <int D, bool F8>
-__device__ __noinline__ void stream_consumer(const FusedArgs& f, int c, uint32_t ring, uint32_t desc, uint32_t qbuf,
-                                             uint32_t full, uint32_t empty, uint32_t qempty, int lane) {
+__device__ __noinline__ void stream_consumer(const FusedArgs& f, int c, uint32_t ring, uint32_t desc, uint32_t full,
+                                             uint32_t empty, int lane) {
     using Lay = FusedLayout<D, F8>;
     constexpr int NS = Lay::NSF;
     constexpr int P = Lay::PITCH;
@@ -457,8 +437,10 @@ __device__ __noinline__ void stream_consumer(const FusedArgs& f, int c, uint32_t
     // (warp c: KV head kvh + c), one with more takes two (warp c: head
     // kvh + c / 2, rows 8 (c % 2) ..); hw is this warp's head in the piece,
     // r0 its first row of the head.
-    uint32_t hoff = 0, qb = qbuf;   // this warp's head within a K/V row, its rows in the Q slot
+    uint32_t hoff = 0;   // this warp's head within a K/V row
     int hw = 0, r0 = 0;
+    const bf16* const qp = f.t.q;
+    const int Hq = f.t.Hq;
 
     uint32_t qcur[D / 8];
     float o[MT][4];
@@ -504,7 +486,7 @@ __device__ __noinline__ void stream_consumer(const FusedArgs& f, int c, uint32_t
             atomicOr(err, 4u);
             break;
         }
-        const uint32_t db = desc + st * 32;
+        const uint32_t db = desc + st * Lay::DESC;
         const int cp0 = ld_shared_s32(db + kDescP0), flags = ld_shared_s32(db + kDescFlags);
         if (flags & kEnd) break;
         if (flags & kFirst) {
@@ -519,32 +501,40 @@ __device__ __noinline__ void stream_consumer(const FusedArgs& f, int c, uint32_t
             r0 = (c - hw * wph) * 8;
             active = hw < cur_nh && r0 < cur_rows;
             hoff = (uint32_t)(hw * D * Lay::ES);
-            qb = qbuf + (uint32_t)((hw * 8 * wph + r0) * D * 2);
             if (active) {
+                // this lane's query row r0 + g: member (r0 + g) / G of the
+                // piece, query head (kvh + hw) G + (r0 + g) % G; zero past the
+                // piece's rows (their output columns are never used)
+                const int rq = r0 + g;
+                const bool okq = rq < cur_rows;
+                const int mq = okq ? ld_shared_s32(db + kDescMem + 4 * (rq / G)) : 0;
+                const bf16* qrow =
+                    qp + ((int64_t)mq * Hq + (ld_shared_s32(db + kDescKvh) + hw) * G + rq % G) * D;
                 // Q^T fragments: row g (the N index), k-step ks -> chunks 2ks, 2ks+1
                 if constexpr (F8) {
                     // row g's elements (D/4) t .. (D/4) t + D/4 - 1, in order:
                     // k-step ks takes elements 4 ks .. 4 ks + 3 of the run (the
                     // order of the lane's K codes below), as f16
+                    const uint4* src = reinterpret_cast<const uint4*>(qrow + (D / 4) * t);
 #pragma unroll
-                    for (int j = 0; j < D / 32; ++j) lds128(qb + g * (D * 2) + ((D / 32) * t + j) * 16, qcur + 4 * j);
+                    for (int j = 0; j < D / 32; ++j) {
+                        const uint4 v = okq ? __ldg(src + j) : make_uint4(0u, 0u, 0u, 0u);
+                        qcur[4 * j] = v.x;
+                        qcur[4 * j + 1] = v.y;
+                        qcur[4 * j + 2] = v.z;
+                        qcur[4 * j + 3] = v.w;
+                    }
                     uint32_t bad = 0u;
 #pragma unroll
                     for (int k = 0; k < D / 8; ++k) qcur[k] = bf16x2_to_f16x2_chk(qcur[k], bad);
-                    // (Q slot rows past the piece's rows hold stale bytes that
-                    // only ever meet their own, unused, output columns)
-                    if (bad && r0 + g < cur_rows) atomicOr(f.t.err, kErrQRange);
+                    if (bad) atomicOr(f.t.err, kErrQRange);
                 } else {
+                    // chunk k (elements 8k .. 8k+7): the lane's pair 2t, 2t+1
+                    const uint32_t* src = reinterpret_cast<const uint32_t*>(qrow) + t;
 #pragma unroll
-                    for (int kp2 = 0; kp2 < D / 32; ++kp2) {
-                        const int rq = lane & 7, chunk = 4 * kp2 + (lane >> 3);
-                        ldsm_x4(qb + rq * (D * 2) + chunk * 16, qcur[4 * kp2], qcur[4 * kp2 + 1], qcur[4 * kp2 + 2],
-                                qcur[4 * kp2 + 3]);
-                    }
+                    for (int k = 0; k < D / 8; ++k) qcur[k] = okq ? __ldg(src + 4 * k) : 0u;
                 }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(qempty);   // the Q slot may be refilled
 #pragma unroll
             for (int i = 0; i < MT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
             m0 = m1 = -INFINITY;
@@ -703,15 +693,14 @@ __global__ void __maxnreg__(128) decode_fused_kernel(const __grid_constant__ Fus
     int* info = reinterpret_cast<int*>(sm + TL::OFF_INFO);
     constexpr int NSF = Lay::NSF;
     const uint32_t sbar = smem_u32(sm + Lay::OFF_SBAR);
-    const uint32_t sfull = sbar, sempty = sbar + 8 * NSF, sqempty = sbar + 16 * NSF;
-    const uint32_t slfull = sqempty + 8, slfree = slfull + 8 * kSQ;
+    const uint32_t sfull = sbar, sempty = sbar + 8 * NSF;
+    const uint32_t slfull = sbar + 16 * NSF, slfree = slfull + 8 * kSQ;
     if (tid == 0) {
         if (tiles) tc_init_barriers<TC>(smem_u32(sm + TL::OFF_BAR));
         for (int s = 0; s < NSF; ++s) {
             mbar_init(sfull + 8 * s, kProducers);   // every producer's arrival (with its bytes)
             mbar_init(sempty + 8 * s, kHB);         // every consumer warp
         }
-        mbar_init(sqempty, kHB);
         for (int e = 0; e < kSQ; ++e) {
             mbar_init(slfull + 8 * e, 33);          // the lookup lanes' cp.async + the fields
             mbar_init(slfree + 8 * e, kProducers);  // every producer
@@ -738,7 +727,8 @@ __global__ void __maxnreg__(128) decode_fused_kernel(const __grid_constant__ Fus
             st_shared_v4(lrec, (uint32_t)x.x, (uint32_t)x.y, (uint32_t)x.z, (uint32_t)x.w);
             st_shared_v4(lrec + 16, (uint32_t)y.x, (uint32_t)y.y, (uint32_t)y.z, (uint32_t)y.w);
         }
-        if (lane < 8) st_shared_s32(lrec + 32 + 4 * lane, lane < y.y ? __ldg(f.t.members + y.x + lane) : 0);
+        if (lane < kDecPieceMembers)
+            st_shared_s32(lrec + 32 + 4 * lane, lane < y.y ? __ldg(f.t.members + y.x + lane) : 0);
         __syncwarp();
     }
     // everything the previous kernel wrote is visible after this wait; the
@@ -764,17 +754,20 @@ __global__ void __maxnreg__(128) decode_fused_kernel(const __grid_constant__ Fus
         if (tid == 0) tc_inval_barriers<TC>(smem_u32(sm + TL::OFF_BAR));
         named_bar(kTileBar, TC::kThreads);
     }
-    const uint32_t ring = smem_u32(sm + Lay::OFF_RING), qb = smem_u32(sm + Lay::OFF_Q);
+    const uint32_t ring = smem_u32(sm + Lay::OFF_RING);
     const uint32_t desc = smem_u32(sm + Lay::OFF_DESC);
     const uint32_t sring = smem_u32(sm + Lay::OFF_SLOT);
     if (warp == kLookup) {
         stream_lookup<D, F8>(f, gw, lrec, sring, slfull, slfree, lane);
     } else if (warp >= kFirstProducer && warp < kFirstConsumer) {
-        stream_producer<D, F8>(f, warp - kFirstProducer, ring, sring, desc, qb, sfull, sempty, sqempty, slfull,
+        stream_producer<D, F8>(f, warp - kFirstProducer, ring, sring, desc, sfull, sempty, slfull,
                                slfree, lane);
     } else if (warp >= kFirstConsumer) {
-        stream_consumer<D, F8>(f, warp - kFirstConsumer, ring, desc, qb, sfull, sempty, sqempty, lane);
+        stream_consumer<D, F8>(f, warp - kFirstConsumer, ring, desc, sfull, sempty, lane);
     }
+    // the tiles' partial rows went out as bulk copies from the softmax
+    // threads (0-127): complete before the grid is
+    if (tiles && tid < 128) bulk_wait_all();
     tc_fence_before();
     __syncthreads();
     if (tiles && warp == 4) {

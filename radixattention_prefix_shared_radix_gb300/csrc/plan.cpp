@@ -116,7 +116,8 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
     // Narrow segments (at most 16 query rows per KV head: members x query
     // heads of the group) go to the streaming warps; wider ones to the
     // tensor-core tiles in member blocks of up to 128 rows.
-    const int32_t MBn = std::max(1, 16 / G);
+    // (a piece carries at most kDecPieceMembers member requests)
+    const int32_t MBn = std::max(1, std::min(sgl::kDecPieceMembers, 16 / G));
     const int32_t MBw = std::max(1, 128 / G);
     const int sms = sgl::query_num_sms(p->num_sms);
 

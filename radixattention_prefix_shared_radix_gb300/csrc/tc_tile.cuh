@@ -865,6 +865,13 @@ __device__ __forceinline__ void tc_tile_run(const TcArgs& a, const CUtensorMap* 
             const float l = l0 + l1;
             const float inv = l > 0.f ? (F8 ? a.v_scale : 1.f) / l : 0.f;
             const float lse = l > 0.f ? (m_used + log2f(l)) * kLn2 : -INFINITY;
+            // decode: the row goes through shared memory (the K/V stages are
+            // idle once every MMA is done; rows padded by 16 bytes, so a
+            // warp's 16-byte stores meet no bank twice) and out with one bulk
+            // copy, instead of 32 lanes storing into 32 rows at once
+            constexpr int OPITCH = D * 4 + 16;
+            static_assert(!DEC || 128 * OPITCH <= 2 * NS * Lay::KTILE, "the O rows fit the K and V stages");
+            const uint32_t so = sK + (uint32_t)(i * OPITCH);
 #pragma unroll 1
             for (int c = 0; c < D / 32; c += 2) {
                 float v[64];
@@ -876,29 +883,32 @@ __device__ __forceinline__ void tc_tile_run(const TcArgs& a, const CUtensorMap* 
 #pragma unroll
                     for (int k = 0; k < 64; ++k) v[k] = 0.f;
                 }
-                if (i < rows) {
-                    if constexpr (DEC) {
-                        float* dst = a_po + ((int64_t)i7 + i) * D + 32 * c;
+                if constexpr (DEC) {
 #pragma unroll
-                        for (int k = 0; k < 64; k += 4)
-                            *reinterpret_cast<float4*>(dst + k) =
-                                make_float4(v[k] * inv, v[k + 1] * inv, v[k + 2] * inv, v[k + 3] * inv);
-                    } else {
-                        const int64_t orow = ((int64_t)i6 + i / a_G) * a_Hq + kvh * a_G + i % a_G;
-                        bf16* dst = a_o + orow * D + 32 * c;
+                    for (int k = 0; k < 64; k += 4)
+                        st_shared_v4(so + (uint32_t)((32 * c + k) * 4), __float_as_uint(v[k] * inv),
+                                     __float_as_uint(v[k + 1] * inv), __float_as_uint(v[k + 2] * inv),
+                                     __float_as_uint(v[k + 3] * inv));
+                } else if (i < rows) {
+                    const int64_t orow = ((int64_t)i6 + i / a_G) * a_Hq + kvh * a_G + i % a_G;
+                    bf16* dst = a_o + orow * D + 32 * c;
 #pragma unroll
-                        for (int k = 0; k < 64; k += 8)
-                            *reinterpret_cast<uint4*>(dst + k) = make_uint4(
-                                pack_bf16(v[k] * inv, v[k + 1] * inv), pack_bf16(v[k + 2] * inv, v[k + 3] * inv),
-                                pack_bf16(v[k + 4] * inv, v[k + 5] * inv), pack_bf16(v[k + 6] * inv, v[k + 7] * inv));
-                    }
+                    for (int k = 0; k < 64; k += 8)
+                        *reinterpret_cast<uint4*>(dst + k) = make_uint4(
+                            pack_bf16(v[k] * inv, v[k + 1] * inv), pack_bf16(v[k + 2] * inv, v[k + 3] * inv),
+                            pack_bf16(v[k + 4] * inv, v[k + 5] * inv), pack_bf16(v[k + 6] * inv, v[k + 7] * inv));
                 }
             }
-            if (i < rows) {
-                if constexpr (DEC)
+            if constexpr (DEC) {
+                fence_proxy_async_smem();   // the row's stores, before the async proxy reads them
+                if (i < rows) {
+                    bulk_s2g(a_po + ((int64_t)i7 + i) * D, so, (uint32_t)(D * 4));
+                    bulk_commit();
                     a_plse[(int64_t)i7 + i] = lse;
-                else
-                    a_lse[((int64_t)i6 + i / a_G) * a_Hq + kvh * a_G + i % a_G] = lse;
+                }
+                bulk_wait_read_all();   // the stages are free again once read
+            } else if (i < rows) {
+                a_lse[((int64_t)i6 + i / a_G) * a_Hq + kvh * a_G + i % a_G] = lse;
             }
         }
         tc_fence_before();

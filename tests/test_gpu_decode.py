@@ -71,6 +71,20 @@ def test_decode_head_shapes(dtype, Hq, Hkv, d):
         case.close()
 
 
+@pytest.mark.parametrize("Hq,Hkv,d", [(8, 8, 128), (8, 8, 64), (16, 8, 128), (32, 8, 128)])
+def test_decode_many_members_per_head(Hq, Hkv, d):
+    """A prefix shared by 12 requests: 12 x G query rows per KV head (a
+    streaming piece takes at most 8 member requests, so G = 1 and 2 put it
+    on tiles, as G = 4 does)."""
+    w = W.Workload("members", 2, "decode", "bf16", Hq, Hkv, d, 1,
+                   ("star", dict(n=12, prefix=150, suffix=(1, 90))), num_slots=4096)
+    case = Case(None, workload=w)
+    try:
+        _check(case)
+    finally:
+        case.close()
+
+
 def test_decode_edge_batch():
     """Empty context, one-token contexts, a request that is a prefix of
     another, identical requests, a branch that starts at position 0."""

@@ -43,3 +43,19 @@ def test_fp8_pool_plans_like_bf16(case):
 def test_fp8_scales_must_be_positive(case, ks, vs):
     with pytest.raises(sgl.SglError):
         _plan(case, sgl.SGL_DTYPE_BF16_FP8KV, k_scale=ks, v_scale=vs)
+
+
+def test_a_piece_takes_at_most_eight_member_requests():
+    """G = 1 and 2: a segment of 9..16 members has at most 16 query rows per
+    KV head but more members than a streaming piece carries, so it is
+    planned on tiles."""
+    import workloads as W
+    for Hq, Hkv, n, wide in ((8, 8, 12, True), (8, 8, 8, False), (16, 8, 12, True), (16, 8, 8, False)):
+        w = W.Workload("members", 2, "decode", "bf16", Hq, Hkv, 128, 1,
+                       ("star", dict(n=n, prefix=150, suffix=(1, 90))), num_slots=4096)
+        c = Case(None, workload=w)
+        try:
+            info = _plan(c, sgl.SGL_DTYPE_BF16)
+            assert (info["num_wide_items"] > 0) == wide, (Hq, Hkv, n, info)
+        finally:
+            c.close()
