@@ -328,7 +328,7 @@ int launch_decode(const sgl_plan* plan, const void* q, const void* kp, const voi
     sgl::MergeArgs m{po, plse, reinterpret_cast<const int32_t*>(ws + plan->off_mptr),
                      reinterpret_cast<const int32_t*>(ws + plan->off_ment), o, lse, Hq, Hkv, G};
     const int n_pairs = p.batch * Hkv;
-    sgl::decode_merge_kernel<float, D><<<(n_pairs * G + 3) / 4, 128, 0, s>>>(m, n_pairs);
+    sgl::decode_merge_kernel<float, D><<<sgl::merge_blocks<D>(n_pairs, G), 128, 0, s>>>(m, n_pairs);
     return cuda_status(cudaGetLastError());
 }
 

@@ -836,7 +836,7 @@ int launch_decode_fused(const sgl_plan* plan, const void* q, const void* kp, con
     MergeArgs m{a.po, a.plse, reinterpret_cast<const int32_t*>(ws + plan->off_mptr),
                 reinterpret_cast<const int32_t*>(ws + plan->off_ment), o, lse, a.Hq, a.Hkv, a.G};
     const int n_pairs = p.batch * a.Hkv;
-    cfg.gridDim = dim3((unsigned)((n_pairs * a.G + 3) / 4));
+    cfg.gridDim = dim3((unsigned)merge_blocks<D>(n_pairs, a.G));
     cfg.blockDim = dim3(128);
     cfg.dynamicSmemBytes = 0;
     return (int)cudaLaunchKernelEx(&cfg, decode_merge_kernel<bf16, D>, m, n_pairs);

@@ -388,6 +388,12 @@ __device__ __forceinline__ void tma_load_row(uint32_t dst, const void* tmap, int
         "l"(tmap), "r"(x), "r"(y), "r"(bar)
         : "memory");
 }
+// TMA load of one box (the map's box: 64 bf16 columns x its rows) at column
+// x, row y into consecutive 128-byte rows from `dst` (1024-byte aligned for
+// the 128-byte swizzle).
+__device__ __forceinline__ void tma_load_box(uint32_t dst, const void* tmap, int x, int y, uint32_t bar) {
+    tma_load_row(dst, tmap, x, y, bar);
+}
 // Arrive on `bar` once every cp.async this thread issued so far has landed
 // (the barrier's expected count includes this arrival).
 __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {

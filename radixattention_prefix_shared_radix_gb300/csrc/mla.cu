@@ -88,14 +88,15 @@ __device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r
 }
 
 __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const __grid_constant__ MlaArgs a,
-                                                                 const __grid_constant__ CUtensorMap tmap) {
+                                                                 const __grid_constant__ CUtensorMap tmap,
+                                                                 const __grid_constant__ CUtensorMap tmq) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     if ((int)blockIdx.x < a.n_tile) {
         // a tile pair's output half on the tensor cores
         uint8_t* sm1 = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
         const mlat::TileArgs ta{a.q, a.r2t, a.ld, a.seq_lens, a.items, a.members, a.po, a.plse, a.err,
                                 a.Hq, a.Gp, a.num_slots, a.scale_log2};
-        mlat::mla_tile_run(ta, &tmap, (int)blockIdx.x >> 1, (int)blockIdx.x & 1, sm1, (int)threadIdx.x);
+        mlat::mla_tile_run(ta, &tmap, &tmq, (int)blockIdx.x >> 1, (int)blockIdx.x & 1, sm1, (int)threadIdx.x);
         return;
     }
     uint8_t* sm = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
@@ -351,11 +352,14 @@ extern "C" int sgl_mla_decode_attn(const void* q, const void* kv_pool, const int
     a.num_slots = p.num_slots;
     a.scale_log2 = p.sm_scale * kLog2e;
     a.n_tile = plan->n_wide;
-    // the tiles' TMA view of the pool, [num_slots, 576] (left zero, and
-    // unused, without tiles)
-    CUtensorMap tmap{};
+    // the tiles' TMA views of the pool, [num_slots, 576] in single rows, and
+    // of q, [B * Hq, 576] in boxes of 16 rows (left zero, and unused,
+    // without tiles)
+    CUtensorMap tmap{}, tmq{};
     if (plan->n_wide > 0) {
-        if (const int te = tc::encode_rows_map(kv_pool, p.num_slots, kDC, &tmap)) {
+        int te = tc::encode_rows_map(kv_pool, p.num_slots, kDC, &tmap);
+        if (!te) te = tc::encode_rows_map(q, (int64_t)p.batch * p.num_qo_heads, kDC, &tmq, 16);
+        if (te) {
             set_cuda_error(te);
             return SGL_ERR_CUDA;
         }
@@ -373,7 +377,7 @@ extern "C" int sgl_mla_decode_attn(const void* q, const void* kv_pool, const int
         cfg.gridDim = dim3((unsigned)plan->n_items);
         cfg.blockDim = dim3(kThreads);
         cfg.dynamicSmemBytes = kSmem;
-        e = cudaLaunchKernelEx(&cfg, mla_decode_kernel, a, tmap);
+        e = cudaLaunchKernelEx(&cfg, mla_decode_kernel, a, tmap, tmq);
         if (e != cudaSuccess) {
             set_cuda_error((int)e);
             return SGL_ERR_CUDA;
@@ -383,7 +387,7 @@ extern "C" int sgl_mla_decode_attn(const void* q, const void* kv_pool, const int
     MergeArgs m{a.po, a.plse, reinterpret_cast<const int32_t*>(ws + plan->off_mptr),
                 reinterpret_cast<const int32_t*>(ws + plan->off_ment), o, lse, a.Hq, p.num_kv_heads, plan->G};
     const int n_pairs = p.batch * p.num_kv_heads;
-    cfg.gridDim = dim3((unsigned)((n_pairs * plan->G + 3) / 4));
+    cfg.gridDim = dim3((unsigned)merge_blocks<kDV>(n_pairs, plan->G));
     cfg.blockDim = dim3(128);
     cfg.dynamicSmemBytes = 0;
     e = cudaLaunchKernelEx(&cfg, decode_merge_kernel<bf16, kDV>, m, n_pairs);

@@ -62,14 +62,19 @@ struct Lay {
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_KV = OFF_Q + kNReg * kQReg;                 // 147456
     static constexpr int OFF_BAR = OFF_KV + kNS * kStage;                // 221184
-    // barriers: KFULL[2], KEMPTY[2], SFULL[2], PFULL[2], OFULL, DONE
+    // barriers: KFULL[2], KEMPTY[2], SFULL[2], PFULL[2], OFULL, DONE, QFULL
     static constexpr int KFULL(int s) { return s; }
     static constexpr int KEMPTY(int s) { return 2 + s; }
     static constexpr int SFULL(int b) { return 4 + b; }
     static constexpr int PFULL(int b) { return 6 + b; }
     static constexpr int OFULL = 8;
     static constexpr int DONE = 9;
-    static constexpr int kNumBars = 10;
+    static constexpr int QFULL = 10;
+    static constexpr int kNumBars = 11;
+    // epilogue: this half's O rows (256 fp32 + 16 bytes of pad each) staged
+    // in the Q area, which is free once every MMA is done
+    static constexpr int OPITCH = kOCols * 4 + 16;
+    static_assert(kRows * OPITCH <= OFF_KV - OFF_Q, "the O rows fit the Q area");
     static constexpr int OFF_TMEM = OFF_BAR + 128;
     static constexpr int OFF_MEM = OFF_TMEM + 16;   // the two units' member requests (at most 4 each)
     static constexpr int END = OFF_MEM + 32;
@@ -109,8 +114,8 @@ __device__ __forceinline__ void tst16u(uint32_t taddr, const uint32_t (&r)[16]) 
 
 // One tile half: `t` the tile (items 2 t, 2 t + 1), `h` the output half.
 // `sm` is the 1024-aligned shared base, `tid` < 512.
-__device__ __forceinline__ void mla_tile_run(const TileArgs& a, const CUtensorMap* tmap, int t, int h, uint8_t* sm,
-                                             int tid) {
+__device__ __forceinline__ void mla_tile_run(const TileArgs& a, const CUtensorMap* tmap, const CUtensorMap* tmq, int t,
+                                             int h, uint8_t* sm, int tid) {
     const int warp = tid >> 5, lane = tid & 31;
     const uint32_t sQ = smem_u32(sm + Lay::OFF_Q), sKV = smem_u32(sm + Lay::OFF_KV);
     const uint32_t bar0 = smem_u32(sm + Lay::OFF_BAR);
@@ -139,6 +144,7 @@ __device__ __forceinline__ void mla_tile_run(const TileArgs& a, const CUtensorMa
         }
         mbar_init(bar(Lay::OFULL), 1);
         mbar_init(bar(Lay::DONE), 1);
+        mbar_init(bar(Lay::QFULL), 1);
         mbar_fence_init();
     }
     if (warp == 4) {
@@ -166,20 +172,30 @@ __device__ __forceinline__ void mla_tile_run(const TileArgs& a, const CUtensorMa
     }
     __syncthreads();
 
-    // Q: 128 rows (unit 0's rows, then unit 1's at 64; zeros past each
-    // unit's rows) x 72 chunks of 16 bytes into the 9 SW128 regions, by every
-    // thread; the tensor cores read it after the barrier below
-    for (int i = tid; i < kRows * (kDC / 8); i += 512) {
-        const int r = i / (kDC / 8), c = i - r * (kDC / 8);
-        const int u = r >> 6, ri = r & 63;
-        const bool ok = ri < (u ? rows1 : rows0);
-        const int mem = mtab[4 * u + ri / a.Gp];
-        const int hg = u ? u1.kvh : u0.kvh;
-        const bf16* src = ok ? a.q + ((int64_t)mem * a.Hq + hg * a.Gp + ri % a.Gp) * kDC + c * 8 : a.q;
-        cp_async16(sQ + sw128(r, c, kQReg), src, ok);
+    // Q: 128 rows (unit 0's rows, then unit 1's at 64) x 9 SW128 regions by
+    // TMA, 16 rows a box: a member's Gp heads (a multiple of 16) are Gp
+    // consecutive rows of q.  Rows past a unit's members are zeroed (their
+    // outputs are not written; zeros keep their scores finite).
+    {
+        const int qunits = 2 * (64 / 16) * kNReg;   // 72 boxes
+        if (tid == 0) mbar_expect_tx(bar(Lay::QFULL), (uint32_t)((rows0 + rows1) / 16 * kNReg * 2048));
+        __syncthreads();
+        if (tid < qunits) {
+            const int reg = tid % kNReg, bx = tid / kNReg;   // box: rows 16 bx .. of the tile
+            const int r = 16 * bx, u = r >> 6, ri = r & 63;
+            if (ri < (u ? rows1 : rows0)) {
+                const int mem = mtab[4 * u + ri / a.Gp];
+                const int hg = u ? u1.kvh : u0.kvh;
+                tma_load_box(sQ + reg * kQReg + r * 128, tmq, reg * 64, mem * a.Hq + hg * a.Gp + ri % a.Gp,
+                             bar(Lay::QFULL));
+            }
+        }
+        for (int i = tid; i < kRows * 8 * kNReg; i += 512) {   // 16-byte chunks of absent rows
+            const int r = i / (8 * kNReg), k = i - r * (8 * kNReg);
+            if ((r & 63) >= ((r >> 6) ? rows1 : rows0))
+                st_shared_v4(sQ + (k >> 3) * kQReg + r * 128 + (k & 7) * 16, 0u, 0u, 0u, 0u);
+        }
     }
-    cp_async_commit();
-    cp_async_wait<0>();
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -246,6 +262,7 @@ __device__ __forceinline__ void mla_tile_run(const TileArgs& a, const CUtensorMa
             // block j's stage for the gather of block j + 2) and S_{j+1},
             // whose stage was freed one block earlier: each gather overlaps
             // a whole block's work
+            wait(Lay::QFULL, 0);
             if (nb > 0) {
                 wait(Lay::KFULL(0), 0);
                 tc_fence_after();
@@ -344,6 +361,9 @@ __device__ __forceinline__ void mla_tile_run(const TileArgs& a, const CUtensorMa
         const int u = i >> 6, ri = i & 63;
         const bool ok = ri < (u ? rows1 : rows0);
         const int64_t prow = (int64_t)(u ? u1.partial_base : u0.partial_base) + ri;
+        // the row through shared memory (padded rows: a warp's 16-byte
+        // stores meet no bank twice), out with one bulk copy
+        const uint32_t so = sQ + (uint32_t)(i * Lay::OPITCH);
 #pragma unroll 1
         for (int c = 0; c < kOCols / 32; c += 2) {
             float v[64];
@@ -355,15 +375,19 @@ __device__ __forceinline__ void mla_tile_run(const TileArgs& a, const CUtensorMa
 #pragma unroll
                 for (int k = 0; k < 64; ++k) v[k] = 0.f;
             }
-            if (ok) {
-                float* dst = a.po + prow * kDV + kOCols * h + 32 * c;
 #pragma unroll
-                for (int k = 0; k < 64; k += 4)
-                    *reinterpret_cast<float4*>(dst + k) =
-                        make_float4(v[k] * inv, v[k + 1] * inv, v[k + 2] * inv, v[k + 3] * inv);
-            }
+            for (int k = 0; k < 64; k += 4)
+                st_shared_v4(so + (uint32_t)((32 * c + k) * 4), __float_as_uint(v[k] * inv),
+                             __float_as_uint(v[k + 1] * inv), __float_as_uint(v[k + 2] * inv),
+                             __float_as_uint(v[k + 3] * inv));
         }
-        if (ok && h == 0) a.plse[prow] = l > 0.f ? (m_used + log2f(l)) * kLn2 : -INFINITY;
+        fence_proxy_async_smem();
+        if (ok) {
+            bulk_s2g(a.po + prow * kDV + kOCols * h, so, (uint32_t)(kOCols * 4));
+            bulk_commit();
+            if (h == 0) a.plse[prow] = l > 0.f ? (m_used + log2f(l)) * kLn2 : -INFINITY;
+        }
+        bulk_wait_all();   // written before the grid completes
     }
     tc_fence_before();
     __syncthreads();

@@ -144,13 +144,13 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return enc;
 }
 
-int encode_rows_map(const void* base, int64_t rows, int D, CUtensorMap* m) {
+int encode_rows_map(const void* base, int64_t rows, int D, CUtensorMap* m, int box_rows) {
     const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return (int)cudaErrorNotSupported;
-    if (rows <= 0 || rows > (int64_t)INT32_MAX) return (int)cudaErrorInvalidValue;
+    if (rows <= 0 || rows > (int64_t)INT32_MAX || box_rows < 1 || box_rows > 256) return (int)cudaErrorInvalidValue;
     const cuuint64_t gdim[2] = {(cuuint64_t)D, (cuuint64_t)rows};
     const cuuint64_t gstride[1] = {(cuuint64_t)D * 2};
-    const cuuint32_t box[2] = {64, 1};
+    const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
     const cuuint32_t estride[2] = {1, 1};
     const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride, box, estride,
                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,

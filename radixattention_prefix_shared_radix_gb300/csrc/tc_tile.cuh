@@ -923,8 +923,9 @@ __device__ __forceinline__ void tc_tile_run(const TcArgs& a, const CUtensorMap* 
 // reused while the pools and shape are the same.  Returns a cudaError_t.
 int encode_pool_maps(const void* kp, const void* vp, int64_t num_slots, int Hkv, int D, CUtensorMap* mk,
                      CUtensorMap* mv);
-// Host: the same view of any [rows, D] bf16 tensor (not cached).
-int encode_rows_map(const void* base, int64_t rows, int D, CUtensorMap* m);
+// Host: the same view of any [rows, D] bf16 tensor (not cached), with boxes
+// of 64 columns x box_rows rows.
+int encode_rows_map(const void* base, int64_t rows, int D, CUtensorMap* m, int box_rows = 1);
 
 }  // namespace tc
 }  // namespace sgl
