@@ -11,9 +11,11 @@ GB/s: the K/V bytes of every prefix-group segment counted once per step.
   * Device value: K steps replayed from CUDA graphs, rotating over batch
     instances whose combined unique KV is several times the 129 MB L2, CUDA
     events around the K steps, max over ranks.
-  * e2e: the same metric through the public API from host buffers -- tree
-    match + tables + prefix groups, planning, plan upload, pinned H2D of q
-    and the tables, the decode call, D2H of O and LSE -- wall clock per step.
+  * e2e: the same metric through the public API from host buffers on one
+    growing batch -- the batch built from the tree, then per step one new
+    slot per request (table and prefix groups grown), planning, plan upload,
+    pinned H2D of q and the tables, the decode call, D2H of O and LSE, and
+    at the end the sequences cached in the tree -- wall clock per step.
   * extend: TFLOP/s of the chunked-prefill workload (8 requests, cached
     4096-token prefix + 512 causal new tokens, Hq 64 / Hkv 8), unmasked
     query-key pairs x 4 d FLOP.
@@ -604,9 +606,10 @@ def run_native(args):
                      "kernel": "decode call = decode_fused_kernel + decode_merge_kernel (unique-KV bytes / call time)"},
         "e2e": {"value": e2e_gbs, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_step_s * 1e3 if e2e_step_s else None,
-                "step": "one growing batch (batch instance 0): every step appends one token per request "
-                        "(slot allocated and inserted), plans, uploads, copies in, decodes, copies out, "
-                        "synchronises and finishes the batch",
+                "step": "one growing batch (batch instance 0): step 0 builds it from the tree, every later "
+                        "step appends one token per request (a slot allocated, the table and prefix groups "
+                        "grown), then each step plans, uploads, copies in, decodes, copies out and "
+                        "synchronises; after the last step every sequence is cached in the tree and released",
                 "host_us_per_step": e2e_host},
         "gpu_launches": K * launches_per_call,
         "clocks": clocks.summary(),
@@ -853,7 +856,7 @@ def bench_mla(sgl, W, torch, steps, bf16_peak, hbm_peak, num_sms=0):
             "batch": calls[0]["B"], "ms_per_call": ms, "unique_kv_bytes_per_call": int(ub),
             "unique_kv_gbs": ub / (ms / 1e3) / 1e9, "frac_of_hbm": ub / (ms / 1e3) / 1e9 / hbm_peak,
             "attention_tflops": tf,
-            "roofline": {"bound": "tensor (mma.sync)", "achieved": tf, "peak": bf16_peak, "unit": "TFLOP/s",
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": bf16_peak, "unit": "TFLOP/s",
                          "frac": tf / bf16_peak, "peak_source": "measured bf16 burst (tcgen05 / cuBLAS)"},
             "items": info["num_items"], "chunk_tokens": info["chunk_tokens"], "calls_timed": n,
             "tokens_per_s": calls[0]["B"] / (ms / 1e3)}
