@@ -15,7 +15,8 @@ GB/s: the K/V bytes of every prefix-group segment counted once per step.
     growing batch -- the batch built from the tree, then per step one new
     slot per request (table and prefix groups grown), planning, plan upload,
     pinned H2D of q and the tables, the decode call, D2H of O and LSE, and
-    at the end the sequences cached in the tree -- wall clock per step.
+    at the end the sequences cached in the tree -- wall clock per step, the
+    host preparing step s+1 while the GPU runs step s.
   * extend: TFLOP/s of the chunked-prefill workload (8 requests, cached
     4096-token prefix + 512 causal new tokens, Hq 64 / Hkv 8), unmasked
     query-key pairs x 4 d FLOP.
@@ -366,21 +367,37 @@ def decode_call(sgl, kd, vd, it):
     sgl.sgl_decode_attn(it["q"], kd, vd, it["table"], it["seq"], it["plan"], it["o"], it["lse"], it["ws"])
 
 
+REPLAN = 32   # e2e: decode steps between plans
+
+
 def e2e_decode(sgl, W, torch, w, tree, kd, vd, inst, steps, num_sms=0):
     """Decode steps of a serving loop through the public API from host
-    buffers, on one batch that grows.  Step 0 runs sgl_build_batch (match;
-    allocate and insert the unmatched tail; emit the prefix groups; the slot
-    table and lengths go straight into pinned staging arrays); every later
-    step runs sgl_batch_append (one new slot per request, the groups' private
-    tails grow by one; the tree is untouched while the requests run).  Every
-    step then runs sgl_decode_plan, sgl_plan_upload, the pinned H2D copies of
-    q, the table and the lengths, the decode call, the D2H copies of O and
-    LSE and a stream synchronise.  After the last step
-    sgl_tree_cache_finished_batch caches every sequence (prompt plus the
-    decoded tokens) and releases the requests.  All of it is timed.  Returns
-    (GB/s of unique KV, h2d bytes/step, d2h bytes/step, s/step, host us per
-    stage, build and finish amortised over the steps)."""
+    buffers, on one batch that grows, with the host one step ahead of the
+    GPU (the overlap scheduling of the CS349D lecture-16 notes §2.2: while
+    the GPU runs step s, the CPU prepares all of step s+1's metadata).
+    Step 0 runs sgl_build_batch (match; allocate and insert the unmatched
+    tail; emit the prefix groups; the slot table goes straight into the
+    pinned staging buffer); every later step's metadata is sgl_batch_append
+    (one new slot per request, the table and prefix groups grown; the tree
+    untouched).  A plan is reused while the requests grow (its trailing
+    pieces read up to the run-time lengths) and rebuilt every REPLAN steps
+    (sgl_decode_plan, then sgl_plan_upload into the other of two workspaces,
+    while the GPU runs the step before).  Each step copies its inputs (Q, the slot table, the
+    lengths: one pinned buffer laid out like one device buffer) to the
+    device in one copy, runs the decode call, copies O and LSE back in one
+    copy and waits for them.  After the last step
+    sgl_tree_cache_finished_batch caches every sequence.  All of it is
+    timed.  The per-step GPU calls go straight to the C ABI with the
+    buffers' addresses taken once (as a C or C++ serving loop would call
+    it).  The table needs no second staging buffer: an append only writes
+    positions past every row's length in the step in flight, which that
+    step never reads; the lengths are copied into the staging buffer when
+    their step is launched.  Returns (GB/s of unique KV, h2d bytes/step,
+    d2h bytes/step, s/step, host us per stage, build and finish amortised
+    over the steps)."""
+    import ctypes
     import numpy as np
+    lib = sgl._lib()
     S = kd.shape[0]
     it = inst[0]
     B = it["B"]
@@ -392,62 +409,99 @@ def e2e_decode(sgl, W, torch, w, tree, kd, vd, inst, steps, num_sms=0):
     rng = np.random.default_rng(12)
     toks_new = rng.integers(0, W.VOCAB, size=(steps, B)).astype(np.int32)
     ld = cap
-    pq = it["q"].cpu().pin_memory()
-    ptab = torch.empty((B, ld), dtype=torch.int32).pin_memory()
-    pseq = torch.empty(B, dtype=torch.int32).pin_memory()
-    po = torch.empty_like(it["o"], device="cpu").pin_memory()
-    plse = torch.empty_like(it["lse"], device="cpu").pin_memory()
-    tab_np, seq_np = ptab.numpy(), pseq.numpy()
-    dtab = torch.empty((B, ld), dtype=torch.int32, device="cuda")
-    dseq = torch.empty(B, dtype=torch.int32, device="cuda")
+    # inputs [q | req_to_token | seq_lens], outputs [O | LSE], each one
+    # pinned host buffer and one device buffer of the same layout
+    qb, tb, sb = it["q"].numel() * 2, B * ld * 4, B * 4
+    ob, lb = it["o"].numel() * 2, it["lse"].numel() * 4
+    hin = torch.empty(qb + tb + sb, dtype=torch.uint8).pin_memory()
+    din = torch.empty(qb + tb + sb, dtype=torch.uint8, device="cuda")
+    hout = torch.empty(ob + lb, dtype=torch.uint8).pin_memory()
+    dout = torch.empty(ob + lb, dtype=torch.uint8, device="cuda")
+    hin[:qb].view(torch.bfloat16).copy_(it["q"].cpu().reshape(-1).view(torch.bfloat16))
+    tab_np = hin[qb:qb + tb].view(torch.int32).view(B, ld).numpy()
+    hseq_np = hin[qb + tb:].view(torch.int32).numpy()
+    seq_np = np.zeros(B, dtype=np.int32)   # the lengths the host side works on
     groups = sgl.sgl_groups_create()
-    # the largest plan of the run sizes the workspace (allocated before timing)
-    ws = torch.zeros(4 * it["plan"].workspace_bytes + (1 << 20), dtype=torch.uint8, device="cuda")
+    # the largest plan of the run sizes the workspaces (allocated before timing)
+    wsz = 4 * it["plan"].workspace_bytes + (1 << 20)
+    ws = [torch.zeros(wsz, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    vp = ctypes.c_void_p
+    base_in, base_out = din.data_ptr(), dout.data_ptr()
+    args_fixed = dict(q=vp(base_in), k=vp(kd.data_ptr()), v=vp(vd.data_ptr()), tab=vp(base_in + qb),
+                      seq=vp(base_in + qb + tb), o=vp(base_out), lse=vp(base_out + ob))
+    ws_ptr = [vp(x.data_ptr()) for x in ws]
+    stream = vp(torch.cuda.current_stream().cuda_stream)
     per_tok = kv_bytes_per_token(w)
     ub0 = it["ub"]
     rows = np.arange(B)
-    stage = dict(build=0.0, append=0.0, plan=0.0, upload=0.0, device=0.0, finish=0.0)
-    h2d = d2h = 0
+    stage = dict(build=0.0, append=0.0, plan=0.0, upload=0.0, launch=0.0, wait=0.0, finish=0.0)
+    done = torch.cuda.Event()
     total_b = 0
-    stream = torch.cuda.current_stream()
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for s in range(steps):
-        c0 = time.perf_counter()
-        if s == 0:
-            out = sgl.sgl_build_batch(tree, toks, groups=groups, req_to_token=tab_np, seq_lens=seq_np, lens=lens0)
-        else:
-            sgl.sgl_batch_append(tree, tab_np, seq_np, groups)
-            toks[rows, seq_np - 1] = toks_new[s]
+
+    def plan_step():
         c1 = time.perf_counter()
         p = sgl.make_params(sgl.SGL_DTYPE_BF16, B, w.Hq, w.Hkv, w.d, S, w.page_size, num_sms=num_sms)
-        plan = sgl.sgl_decode_plan(p, seq_np, sgl.sgl_groups_view(groups))
-        if plan.workspace_bytes > ws.numel():
+        pl = sgl.sgl_decode_plan(p, seq_np, sgl.sgl_groups_view(groups))
+        if pl.workspace_bytes > wsz:
             raise RuntimeError("e2e workspace too small")
-        c2 = time.perf_counter()
-        sgl.sgl_plan_upload(plan, ws)
-        c3 = time.perf_counter()
-        dtab.copy_(ptab, non_blocking=True)
-        dseq.copy_(pseq, non_blocking=True)
-        it["q"].copy_(pq, non_blocking=True)
-        sgl.sgl_decode_attn(it["q"], kd, vd, dtab, dseq, plan, it["o"], it["lse"], ws)
-        po.copy_(it["o"], non_blocking=True)
-        plse.copy_(it["lse"], non_blocking=True)
-        stream.synchronize()
-        c4 = time.perf_counter()
-        for k, a, b in (("build" if s == 0 else "append", c0, c1), ("plan", c1, c2), ("upload", c2, c3),
-                        ("device", c3, c4)):
-            stage[k] += b - a
-        if s == 0:
-            h2d = (pq.numel() * 2 + ptab.numel() * 4 + pseq.numel() * 4 + sgl.sgl_plan_info(plan)["upload_bytes"])
-            d2h = po.numel() * 2 + plse.numel() * 4
+        stage["plan"] += time.perf_counter() - c1
+        return pl
+
+    def upload(pl, k):
+        c1 = time.perf_counter()
+        st = lib.sgl_plan_upload(pl.handle, ws_ptr[k], wsz, stream)
+        if st:
+            raise sgl.SglError(st, "sgl_plan_upload")
+        stage["upload"] += time.perf_counter() - c1
+
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    c0 = time.perf_counter()
+    out = sgl.sgl_build_batch(tree, toks, groups=groups, req_to_token=tab_np, seq_lens=seq_np, lens=lens0)
+    stage["build"] += time.perf_counter() - c0
+    plan = plan_step()
+    upload(plan, 0)
+    up_bytes = sgl.sgl_plan_info(plan)["upload_bytes"]
+    d2h = ob + lb
+    a = args_fixed
+    cur = 0   # the workspace of the plan in use
+    for s in range(steps):
+        c0 = time.perf_counter()
+        hseq_np[:] = seq_np
+        din.copy_(hin, non_blocking=True)
+        st = lib.sgl_decode_attn(a["q"], a["k"], a["v"], a["tab"], ld, a["seq"], plan.handle, a["o"], a["lse"],
+                                 ws_ptr[cur], wsz, stream)
+        if st:
+            raise sgl.SglError(st, "sgl_decode_attn")
+        hout.copy_(dout, non_blocking=True)
+        done.record()
+        stage["launch"] += time.perf_counter() - c0
         # the shared prefix is unchanged; every request's own suffix grew by one token a step
         total_b += ub0 + s * B * per_tok
+        nxt = None
+        if s + 1 < steps:
+            # step s+1's metadata while the GPU runs step s
+            c0 = time.perf_counter()
+            sgl.sgl_batch_append(tree, tab_np, seq_np, groups)
+            toks[rows, seq_np - 1] = toks_new[s + 1]
+            stage["append"] += time.perf_counter() - c0
+            if (s + 1) % REPLAN == 0:
+                nxt = plan_step()
+                upload(nxt, cur ^ 1)
+                up_bytes += sgl.sgl_plan_info(nxt)["upload_bytes"]
+        c0 = time.perf_counter()
+        done.synchronize()   # step s's O and LSE are on the host
+        stage["wait"] += time.perf_counter() - c0
+        if nxt is not None:
+            plan = nxt
+            cur ^= 1
+    h2d = qb + tb + sb + up_bytes // steps
     c5 = time.perf_counter()
     sgl.sgl_tree_cache_finished_batch(tree, toks, out)
     el = time.perf_counter() - t0
     stage["finish"] += time.perf_counter() - c5
-    sgl.sgl_check(ws)
+    for x in ws:
+        sgl.sgl_check(x)
     sgl.sgl_groups_destroy(groups)
     host_us = {k: v * 1e6 / steps for k, v in stage.items()}
     return total_b / el / 1e9, h2d, d2h, el / steps, host_us
@@ -606,10 +660,15 @@ def run_native(args):
                      "kernel": "decode call = decode_fused_kernel + decode_merge_kernel (unique-KV bytes / call time)"},
         "e2e": {"value": e2e_gbs, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_step_s * 1e3 if e2e_step_s else None,
-                "step": "one growing batch (batch instance 0): step 0 builds it from the tree, every later "
-                        "step appends one token per request (a slot allocated, the table and prefix groups "
-                        "grown), then each step plans, uploads, copies in, decodes, copies out and "
-                        "synchronises; after the last step every sequence is cached in the tree and released",
+                "step": "one growing batch (batch instance 0), the host one step ahead of the GPU: step 0 "
+                        "builds it from the tree; while the GPU runs step s the host appends one token per "
+                        "request for step s+1 (a slot allocated, the table and prefix groups grown) and, "
+                        "every %d steps, plans the batch anew and uploads the plan to a second workspace "
+                        "(in between the plan is reused: its trailing pieces read the run-time lengths); "
+                        "each step copies Q, the table and the " % REPLAN +
+                        "lengths in (one pinned buffer, one copy), decodes (the C ABI called with the buffers' "
+                        "addresses), copies O and LSE out (one copy) and waits for them; after the last step "
+                        "every sequence is cached in the tree and released",
                 "host_us_per_step": e2e_host},
         "gpu_launches": K * launches_per_call,
         "clocks": clocks.summary(),

@@ -289,7 +289,18 @@ typedef struct sgl_plan sgl_plan;
  * host [B]; groups: the batch's prefix groups.  *workspace_bytes = device
  * workspace the call needs (plan tables + partials + error word).
  * Segments whose end exceeds their representative's seq_len:
- * SGL_ERR_INVALID_ARG. */
+ * SGL_ERR_INVALID_ARG.
+ * A plan stays valid for later decode calls on the same batch after its
+ * requests have grown at their ends (sgl_batch_append): each request's last
+ * piece -- over its own trailing positions, or an empty piece at its end
+ * when its context ends in a shared segment -- reads up to the request's
+ * device seq_len at run time (bounded by ld; a length below the planned
+ * one sets error bit 1).  Growth lengthens only those pieces, so the work
+ * balance of a reused plan degrades slowly; any other change of the batch
+ * (requests added or removed, a different sharing) needs a new plan.
+ * [decode steps of a running batch: "SGLang 深度拆解" (chenxutan.com) §1.3;
+ * the scheduler prepares the next batch ahead of the GPU: CS349D
+ * lecture-16 notes §2.2] */
 int sgl_decode_plan(const sgl_attn_params* params, const int32_t* seq_lens, const sgl_prefix_groups* groups,
                     sgl_plan** plan_out, size_t* workspace_bytes);
 void sgl_plan_destroy(sgl_plan* plan);

@@ -118,7 +118,13 @@ __global__ void __launch_bounds__(128)
     const int rows = it.n_mem * it.nh * G;
     int kv_end = it.kv_end;
     const int rep_len = __ldg(seq_lens + it.rep_row);
-    if (kv_end > rep_len) {
+    if (kv_end == sgl::kDecToSeqEnd) {   // a request's trailing piece: to its length now (within its row)
+        kv_end = rep_len;
+        if (kv_end > ld || kv_end < it.kv_begin) {
+            if (threadIdx.x == 0) atomicOr(err, 2u);
+            kv_end = kv_end > ld ? (int)ld : it.kv_begin;
+        }
+    } else if (kv_end > rep_len) {
         if (threadIdx.x == 0) atomicOr(err, 2u);
         kv_end = rep_len;
     }

@@ -38,6 +38,10 @@ struct DecItem {
     int32_t nh;            // KV heads in the block (1 for tensor-core tiles)
 };
 static_assert(sizeof(DecItem) == 32, "DecItem is 32 bytes");
+// kv_end of a request's last piece (its own trailing positions): the piece
+// runs to the request's seq_len at run time, so a plan stays valid while the
+// batch's requests grow at their ends (decode steps).
+constexpr int32_t kDecToSeqEnd = 0x7fffffff;
 
 // Decode schedule constants (bf16 persistent kernel): a narrow piece covers
 // up to kDecHeadBlock KV heads of its positions (one or two consumer warps

@@ -263,8 +263,19 @@ __device__ __noinline__ void stream_lookup(const FusedArgs& f, int gw, uint32_t 
             mem = lane < nm ? __ldg(members + mb + lane) : 0;
         }
         first_piece = false;
-        const int len = __ldg(seq_lens + row);
-        for (int sp = b; sp < e; sp += kNP)
+        int len = __ldg(seq_lens + row);
+        if (e == kDecToSeqEnd) {
+            // a request's trailing piece runs to its length now (within its
+            // row of the table; a length below the piece's start is an error)
+            if (len > ld || len < b) {
+                if (lane == 0) atomicOr(err, 2u);
+                len = len > ld ? (int)ld : b;
+            }
+            e = len;
+        }
+        // at least one step, so that an empty piece still writes its
+        // (empty) partial rows for the merge
+        for (int sp = b; sp < e || sp == b; sp += kNP)
             entry(kvh, row, sp, e, sp == b ? kFirst : 0, len, pb, nh, nm, mem);
     }
     entry(-1, 0, 0, 0, 0, 0, 0, 0, 0, 0);   // the end of the stream

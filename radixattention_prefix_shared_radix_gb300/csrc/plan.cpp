@@ -131,23 +131,43 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
     };
     struct Unit {   // narrow work: one member block of a segment for a block of KV heads
         int32_t rep_row, b, e, kvh, mem_begin, n_mem, nh;
+        bool tail;      // a request's own trailing positions: its last piece runs to seq_len at run time
     };
+    // The plan's member list: the groups' members, then one entry per
+    // request whose context does not end in a segment of its own (it ends
+    // in a shared segment, or is empty); such a request gets an empty
+    // trailing unit at its end, so that every request has a piece that
+    // reads its positions past the planned length when the batch has grown
+    // (decode steps reuse the plan; the kernels read seq_lens).
+    std::vector<int32_t> mem(g->seg_members, g->seg_members + g->num_members);
+    std::vector<int32_t> own_tail(B, -1);   // segment that is request r's own trailing segment
+    for (int32_t s = 0; s < nseg; ++s) {
+        const int32_t m0 = g->seg_member_ptr[s], m1 = g->seg_member_ptr[s + 1];
+        if (m1 - m0 == 1 && g->seg_end[s] == seq_lens[g->seg_members[m0]]) own_tail[g->seg_members[m0]] = s;
+    }
     std::vector<Unit> units;
     int64_t units_n = 0;     // position-heads
     int64_t max_wide = 0;
+    auto add_units = [&](int32_t rep, int32_t b, int32_t e, int32_t m0, int32_t nmem, bool tail) {
+        const int32_t HP = head_block(nmem);
+        for (int32_t h = 0; h < Hkv; h += HP) {
+            const int32_t nh = std::min(HP, Hkv - h);
+            units.push_back({rep, b, e, h, m0, nmem, nh, tail});
+            units_n += (int64_t)(e - b) * nh;
+        }
+    };
     for (int32_t s = 0; s < nseg; ++s) {
         const int32_t b = g->seg_begin[s], e = g->seg_end[s];
         const int32_t m0 = g->seg_member_ptr[s], nmem = g->seg_member_ptr[s + 1] - m0;
-        if (nmem <= MBn) {
-            const int32_t HP = head_block(nmem);
-            for (int32_t h = 0; h < Hkv; h += HP) {
-                const int32_t nh = std::min(HP, Hkv - h);
-                units.push_back({g->seg_row[s], b, e, h, m0, nmem, nh});
-                units_n += (int64_t)(e - b) * nh;
-            }
-        } else {
+        if (nmem <= MBn)
+            add_units(g->seg_row[s], b, e, m0, nmem, nmem == 1 && own_tail[g->seg_members[m0]] == s);
+        else
             max_wide = std::max<int64_t>(max_wide, e - b);
-        }
+    }
+    for (int32_t r = 0; r < B; ++r) {
+        if (own_tail[r] >= 0) continue;
+        mem.push_back(r);
+        add_units(r, seq_lens[r], seq_lens[r], (int32_t)mem.size() - 1, 1, true);
     }
     const int64_t n_ctas = sms;
     // Wide chunks run on tile CTAs whose streaming warps start only when
@@ -216,21 +236,28 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
     // (in position-heads, so that a piece of a 4-head block is as long in
     // bytes as one of an 8-head block)
     const int64_t Pph = (int64_t)std::ceil((double)units_n / (double)std::max<int64_t>(1, 2 * n_cons));
-    std::vector<sgl::DecItem> narrow;
+    std::vector<std::pair<int32_t, sgl::DecItem>> cut;   // (planned length, piece)
     for (const Unit& u : units) {
         int64_t Pmax = (Pph + u.nh - 1) / u.nh;
         Pmax = std::min<int64_t>(2048, std::max<int64_t>(32, (Pmax + 15) / 16 * 16));
-        for (int64_t pos = u.b; pos < u.e;) {
+        for (int64_t pos = u.b; pos < u.e || (pos == u.b && u.tail);) {
             int64_t take = std::min<int64_t>(u.e - pos, Pmax);
             if (u.e - pos - take < 16) take = u.e - pos;   // no tail piece under one step
-            narrow.push_back(
-                {u.rep_row, (int32_t)pos, (int32_t)(pos + take), u.kvh, u.mem_begin, u.n_mem, 0, u.nh});
+            const bool last = pos + take == u.e;
+            cut.push_back({(int32_t)take,
+                           {u.rep_row, (int32_t)pos, last && u.tail ? sgl::kDecToSeqEnd : (int32_t)(pos + take), u.kvh,
+                            u.mem_begin, u.n_mem, 0, u.nh}});
             pos += take;
+            if (take == 0) break;   // (an empty trailing unit: one piece)
         }
     }
-    std::stable_sort(narrow.begin(), narrow.end(), [](const sgl::DecItem& x, const sgl::DecItem& y) {
-        return (x.kv_end - x.kv_begin) > (y.kv_end - y.kv_begin);
+    std::stable_sort(cut.begin(), cut.end(), [](const std::pair<int32_t, sgl::DecItem>& x,
+                                                const std::pair<int32_t, sgl::DecItem>& y) {
+        return x.first > y.first;
     });
+    std::vector<sgl::DecItem> narrow;
+    narrow.reserve(cut.size());
+    for (const auto& c : cut) narrow.push_back(c.second);
     const int64_t n_init = std::min<int64_t>((int64_t)narrow.size(), n_cons);
 
     // wide items round-robin over the tile CTAs (the first n_tile_ctas)
@@ -257,7 +284,7 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
         it.partial_base = (int32_t)prow;
         for (int32_t i = 0; i < it.n_mem; ++i)
             for (int32_t hh = 0; hh < it.nh; ++hh)
-                ++eptr[(size_t)g->seg_members[it.mem_begin + i] * Hkv + it.kvh + hh + 1];
+                ++eptr[(size_t)mem[it.mem_begin + i] * Hkv + it.kvh + hh + 1];
         prow += (int64_t)it.n_mem * it.nh * G;
         if (prow > INT32_MAX / 256) return SGL_ERR_UNSUPPORTED;
     }
@@ -273,7 +300,7 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
         for (const auto& it : items)
             for (int32_t i = 0; i < it.n_mem; ++i)
                 for (int32_t hh = 0; hh < it.nh; ++hh)
-                    ents_flat[fill[(size_t)g->seg_members[it.mem_begin + i] * Hkv + it.kvh + hh]++] =
+                    ents_flat[fill[(size_t)mem[it.mem_begin + i] * Hkv + it.kvh + hh]++] =
                         it.partial_base + (i * it.nh + hh) * G;
     }
 
@@ -290,7 +317,7 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
     plan->n_narrow = (int32_t)narrow.size();
     plan->n_init = (int32_t)n_init;
     plan->n_tile_ctas = (int32_t)n_tile_ctas;
-    plan->n_members = g->num_members;
+    plan->n_members = (int32_t)mem.size();
     plan->n_merge_entries = (int32_t)n_ent;
     plan->chunk_tokens = (int32_t)Cw;
     plan->max_pos = 0;
@@ -301,7 +328,7 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
     const size_t A = sgl::kWsAlign;
     plan->off_items = A;
     plan->off_members = align_up(plan->off_items + items.size() * sizeof(sgl::DecItem), A);
-    plan->off_wptr = align_up(plan->off_members + (size_t)g->num_members * 4, A);
+    plan->off_wptr = align_up(plan->off_members + mem.size() * 4, A);
     plan->off_sched = align_up(plan->off_wptr + wptr.size() * 4, A);
     plan->off_mptr = align_up(plan->off_sched + 2 * 4, A);
     plan->off_ment = align_up(plan->off_mptr + ((size_t)B * Hkv + 1) * 4, A);
@@ -320,7 +347,7 @@ int sgl_decode_plan(const sgl_attn_params* p, const int32_t* seq_lens, const sgl
     sgl::WsHeader hdr{0u, sgl::kWsMagic, plan->n_items, plan->n_wide, plan->n_partial_rows, plan->n_ctas};
     std::memcpy(plan->blob, &hdr, sizeof(hdr));
     if (!items.empty()) std::memcpy(plan->blob + plan->off_items, items.data(), items.size() * sizeof(sgl::DecItem));
-    if (g->num_members) std::memcpy(plan->blob + plan->off_members, g->seg_members, (size_t)g->num_members * 4);
+    if (!mem.empty()) std::memcpy(plan->blob + plan->off_members, mem.data(), mem.size() * 4);
     std::memcpy(plan->blob + plan->off_wptr, wptr.data(), wptr.size() * 4);
     // run-time piece counter: next piece to hand out, producers finished
     const uint32_t sched[2] = {(uint32_t)n_init, 0u};

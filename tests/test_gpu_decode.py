@@ -466,3 +466,74 @@ def test_fp8_query_outside_f16_is_reported():
         assert e.value.status == -5
     finally:
         case.close()
+
+
+@pytest.mark.parametrize("name,steps", [("llama3_8b_decode_small", 1), ("llama3_8b_decode_small", 9),
+                                        ("fork_tree_small", 40), ("multiturn_small", 23), ("tiny_fp32", 5)])
+def test_plan_reused_after_decode_steps(name, steps):
+    """A plan made for a batch stays valid after every request has grown by
+    `steps` tokens (sgl_batch_append): the requests' trailing pieces read up
+    to the grown seq_lens.  The batch adds a copy of request 0 (its context
+    ends in a shared segment) and an empty request; the result equals the
+    oracle on the grown batch, whose table the oracle builds with its own
+    append_step."""
+    from oracle.tree import append_step
+    w = W.get(name)
+    base = W.make_batch(w, 0).all_tokens()
+    seqs = list(base) + [list(base[0]), []]
+    rng = np.random.default_rng(31 + steps)
+    q = rng.standard_normal((len(seqs), w.Hq, w.d), dtype=np.float32)
+    case = Case(None, workload=w, seqs=seqs, q=q)
+    try:
+        B = case.B
+        ld = case.out["req_to_token"].shape[1] + steps
+        tab = np.full((B, ld), -1, dtype=np.int32)
+        tab[:, :ld - steps] = case.out["req_to_token"]
+        seq = case.out["seq_lens"].copy()
+        p = case.params()
+        plan = sgl.sgl_decode_plan(p, seq, sgl.sgl_groups_view(case.groups))
+        ws = torch.zeros(max(plan.workspace_bytes, 256), dtype=torch.uint8, device="cuda")
+        sgl.sgl_plan_upload(plan, ws)
+        rows = [list(case.oracle_table[r, :seq[r]]) for r in range(B)]
+        for _ in range(steps):
+            sgl.sgl_batch_append(case.tree, tab, seq, None)
+            append_step(case.trie, rows)
+        oracle_table = np.full((B, ld), -1, dtype=np.int64)
+        for r, row in enumerate(rows):
+            oracle_table[r, :len(row)] = row
+        kd, vd = case.device_pool()
+        qd = case.q_host().cuda()
+        o = torch.empty_like(qd)
+        lse = torch.empty(B, w.Hq, dtype=torch.float32, device="cuda")
+        sgl.sgl_decode_attn(qd, kd, vd, torch.from_numpy(tab).cuda(), torch.from_numpy(seq).cuda(), plan, o, lse, ws)
+        sgl.sgl_check(ws)
+        Oref, Lref = decode_attention(case.oracle_q(), W.RowView(case.K), W.RowView(case.V), oracle_table,
+                                      np.array([len(r) for r in rows]))
+        assert_close(o.double().cpu().numpy(), lse.cpu().numpy().astype(np.float64), Oref, Lref, *tolerances(w))
+    finally:
+        case.close()
+
+
+def test_reused_plan_reports_a_batch_that_shrank():
+    """A request shorter than its planned trailing piece start sets error bit
+    1 (SGL_ERR_BOUNDS from sgl_check) instead of reading stale positions."""
+    case = Case("llama3_8b_decode_small")
+    try:
+        p = case.params()
+        seq = case.out["seq_lens"].copy()
+        plan = sgl.sgl_decode_plan(p, seq, sgl.sgl_groups_view(case.groups))
+        ws = torch.zeros(max(plan.workspace_bytes, 256), dtype=torch.uint8, device="cuda")
+        sgl.sgl_plan_upload(plan, ws)
+        kd, vd = case.device_pool()
+        qd = case.q_host().cuda()
+        o = torch.empty_like(qd)
+        lse = torch.empty(case.B, case.w.Hq, dtype=torch.float32, device="cuda")
+        short = seq.copy()
+        short[0] = 1   # request 0 shrank below its planned pieces
+        sgl.sgl_decode_attn(qd, kd, vd, torch.from_numpy(case.out["req_to_token"]).cuda(),
+                            torch.from_numpy(short).cuda(), plan, o, lse, ws)
+        with pytest.raises(sgl.SglError) as e:
+            sgl.sgl_check(ws)
+        assert e.value.status == -5
+    finally:
+        case.close()
