@@ -39,9 +39,10 @@ constexpr int32_t kMlaBlock = 32;   // positions per block of the kernel
 double block_cost(int32_t rows) { return 0.94 + 0.0394 * rows; }
 constexpr double kItemCost = 1.5;   // estimated start cost of one item (us)
 // tcgen05 tile pairs (two 64-row units, two CTAs): estimated microseconds of
-// one 32-position block and of a tile's start (Q load, first gathers)
-constexpr double kTileBlock = 1.2;
-constexpr double kTileStart = 3.0;
+// one 32-position block and of a tile's fixed cost (Q load and first
+// gathers, ~6 us; epilogue, ~3 us), from GB300 timelines of the tiles
+constexpr double kTileBlock = 2.1;
+constexpr double kTileStart = 9.0;
 // a partial row (512 fp32) is written by the kernel and read by the merge:
 // 4 KB at about 6 TB/s
 constexpr double kRowCost = 4096.0 / 6.0e6;
