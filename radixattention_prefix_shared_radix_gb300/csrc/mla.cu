@@ -43,6 +43,7 @@ constexpr int kSlotRing = 4;       // slot lists of blocks (one more than the st
 constexpr int kThreads = 512;      // 16 warps: 4 row groups x 4
 constexpr int kRowB = kDC * 2;     // bytes per stored row (bf16)
 constexpr int kCPR = kDC / 8;      // 16-byte chunks per row
+constexpr int kSPP = kBN + 8;      // pitch of a partial-score row (fp32; the padding spreads the banks)
 
 struct MlaLayout {
     static constexpr int OFF_Q = 0;                                  // [64][576] bf16
@@ -52,7 +53,8 @@ struct MlaLayout {
     static constexpr int OFF_MX = OFF_SLOT + kSlotRing * kBN * 4;    // [4 groups][4 warps][16] fp32
     static constexpr int OFF_LS = OFF_MX + 16 * 16 * 4;              // the same, for the row sums
     static constexpr int OFF_MEM = OFF_LS + 16 * 16 * 4;             // the item's member requests (at most 4)
-    static constexpr int END = OFF_MEM + 16;
+    static constexpr int OFF_SP = OFF_MEM + 16;                      // small items: [4 groups][16][kSPP] fp32 partial S
+    static constexpr int END = OFF_SP + 4 * 16 * kSPP * 4;
     static constexpr int TOTAL = END + 128;                          // + alignment slack
     static_assert(TOTAL <= 232448, "shared memory per CTA");
 };
@@ -161,8 +163,9 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const __grid_co
     store(2, f2);
     int pend = fetch(3);   // block 3's raw slot, stored in the first iteration
     __syncthreads();
-    // the item's query rows (zeros past R), with block 0's copies
-    for (int i = tid; i < kRT * kCPR; i += kThreads) {
+    // the item's query rows (zeros past R; a small item reads 16), with block 0's copies
+    const int q_rows = R <= 16 ? 16 : kRT;
+    for (int i = tid; i < q_rows * kCPR; i += kThreads) {
         const int r = i / kCPR, c = i - r * kCPR;
         const bool ok = r < R;
         const int mem = ok ? mems[r / a.Gp] : 0;
@@ -171,6 +174,161 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_kernel(const __grid_co
     }
     copy(0);
     copy(1);
+
+    if (R <= 16) {
+        // ---- an item of at most 16 query rows (a request's own suffix x
+        // its heads): every warp takes part in each block.  Row group rg
+        // computes S over k-steps 9 rg .. 9 rg + 8 (a quarter of the 576
+        // elements) for positions 8 wq .. 8 wq + 7; the four partial scores
+        // meet in shared memory and every group sums them in the same order,
+        // so all groups hold the same scores and run the same softmax; group
+        // 0 writes P, and warp w = 4 rg + wq accumulates output columns
+        // 32 w .. 32 w + 31.
+        float* sps = reinterpret_cast<float*>(sm + MlaLayout::OFF_SP);
+        float o4[4][4];
+#pragma unroll
+        for (int n = 0; n < 4; ++n) o4[n][0] = o4[n][1] = o4[n][2] = o4[n][3] = 0.f;
+        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;   // rows g and g + 8
+        const int bar_id = 1 + rg;
+        for (int j = 0; j < nb; ++j) {
+            store(j + 3, pend);
+            pend = fetch(j + 4);
+            copy(j + 2);
+            cp_async_wait<2>();   // block j has landed
+            __syncthreads();
+            const uint32_t st = sKV + (uint32_t)((j % kStages) * kBN * kRowB);
+            {
+                constexpr int NQ = kDC / 16 / 4;   // k-steps per row group
+                const int k0 = NQ * rg;
+                float sp[4] = {0.f, 0.f, 0.f, 0.f};
+                uint32_t qa[2][4], kb[2][2];
+                auto load_s = [&](int ks, int buf) {
+                    ldsm_x4(sQ + rswz(lane & 15, 2 * ks + (lane >> 4)), qa[buf][0], qa[buf][1], qa[buf][2],
+                            qa[buf][3]);
+                    ldsm_x2(st + rswz(8 * wq + (lane & 7), 2 * ks + ((lane >> 3) & 1)), kb[buf][0], kb[buf][1]);
+                };
+                load_s(k0, 0);
+#pragma unroll
+                for (int i = 0; i < NQ; ++i) {
+                    if (i + 1 < NQ) load_s(k0 + i + 1, (i + 1) & 1);
+                    mma16816(sp, qa[i & 1], kb[i & 1][0], kb[i & 1][1]);
+                }
+                float* d0 = sps + (rg * 16 + g) * kSPP + 8 * wq + 2 * t;
+                *reinterpret_cast<float2*>(d0) = make_float2(sp[0], sp[1]);
+                *reinterpret_cast<float2*>(d0 + 8 * kSPP) = make_float2(sp[2], sp[3]);
+            }
+            __syncthreads();
+            float sum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float* d0 = sps + (k * 16 + g) * kSPP + 8 * wq + 2 * t;
+                const float2 ra = *reinterpret_cast<const float2*>(d0);
+                const float2 rb = *reinterpret_cast<const float2*>(d0 + 8 * kSPP);
+                sum[0] += ra.x;
+                sum[1] += ra.y;
+                sum[2] += rb.x;
+                sum[3] += rb.y;
+            }
+            const int pos = b + j * kBN + 8 * wq + 2 * t;
+            const bool v0 = pos < e, v1 = pos + 1 < e;
+            const float x00 = v0 ? sum[0] * a.scale_log2 : -INFINITY;
+            const float x01 = v1 ? sum[1] * a.scale_log2 : -INFINITY;
+            const float x10 = v0 ? sum[2] * a.scale_log2 : -INFINITY;
+            const float x11 = v1 ? sum[3] * a.scale_log2 : -INFINITY;
+            float bm0 = fmaxf(x00, x01), bm1 = fmaxf(x10, x11);
+            bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, 1));
+            bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, 2));
+            bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, 1));
+            bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, 2));
+            if (t == 0) {
+                mxs[(rg * 4 + wq) * 16 + g] = bm0;
+                mxs[(rg * 4 + wq) * 16 + g + 8] = bm1;
+            }
+            named_bar(bar_id, 128);
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                bm0 = fmaxf(bm0, mxs[(rg * 4 + w) * 16 + g]);
+                bm1 = fmaxf(bm1, mxs[(rg * 4 + w) * 16 + g + 8]);
+            }
+            const float n0 = fmaxf(m0, bm0), n1 = fmaxf(m1, bm1);
+            const float al0 = (m0 == -INFINITY) ? 0.f : exp2f(m0 - n0);
+            const float al1 = (m1 == -INFINITY) ? 0.f : exp2f(m1 - n1);
+            if (n0 > m0 || n1 > m1) {
+                l0 *= al0;
+                l1 *= al1;
+#pragma unroll
+                for (int n = 0; n < 4; ++n) {
+                    o4[n][0] *= al0;
+                    o4[n][1] *= al0;
+                    o4[n][2] *= al1;
+                    o4[n][3] *= al1;
+                }
+            }
+            m0 = n0;
+            m1 = n1;
+            const float u0 = m0 == -INFINITY ? 0.f : m0, u1 = m1 == -INFINITY ? 0.f : m1;
+            const float p00 = exp2f(x00 - u0), p01 = exp2f(x01 - u0), p10 = exp2f(x10 - u1), p11 = exp2f(x11 - u1);
+            l0 += p00 + p01;
+            l1 += p10 + p11;
+            if (rg == 0) {
+                asm volatile("st.shared.b32 [%0], %1;\n" ::"r"(sP + pswz(g, wq) + 4 * t), "r"(pack_bf16(p00, p01))
+                             : "memory");
+                asm volatile("st.shared.b32 [%0], %1;\n" ::"r"(sP + pswz(g + 8, wq) + 4 * t),
+                             "r"(pack_bf16(p10, p11))
+                             : "memory");
+            }
+            __syncthreads();   // P of all 32 positions, for every warp
+            {
+                uint32_t pa[2][4];
+                ldsm_x4(sP + pswz(lane & 15, lane >> 4), pa[0][0], pa[0][1], pa[0][2], pa[0][3]);
+                ldsm_x4(sP + pswz(lane & 15, 2 + (lane >> 4)), pa[1][0], pa[1][1], pa[1][2], pa[1][3]);
+#pragma unroll
+                for (int np = 0; np < 2; ++np) {
+#pragma unroll
+                    for (int ks = 0; ks < 2; ++ks) {
+                        uint32_t vb[4];
+                        ldsm_x4_t(st + rswz(16 * ks + (lane & 7) + ((lane >> 3) & 1) * 8, 4 * warp + 2 * np + (lane >> 4)),
+                                  vb[0], vb[1], vb[2], vb[3]);
+                        mma16816(o4[2 * np], pa[ks], vb[0], vb[1]);
+                        mma16816(o4[2 * np + 1], pa[ks], vb[2], vb[3]);
+                    }
+                }
+            }
+            __syncthreads();   // stage j % kStages, P and the partial scores are free again
+        }
+        asm volatile("cp.async.wait_all;\n" ::: "memory");
+        // row sums over the quad and the group's four warps (every group
+        // holds the same sums), then this warp's 32 columns of the rows
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+        l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+        if (t == 0) {
+            lss[(rg * 4 + wq) * 16 + g] = l0;
+            lss[(rg * 4 + wq) * 16 + g + 8] = l1;
+        }
+        named_bar(bar_id, 128);
+        float L0 = 0.f, L1 = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            L0 += lss[(rg * 4 + w) * 16 + g];
+            L1 += lss[(rg * 4 + w) * 16 + g + 8];
+        }
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const int row = g + 8 * hh;
+            if (row >= R) continue;
+            const float L = hh ? L1 : L0, m = hh ? m1 : m0;
+            const float inv = L > 0.f ? 1.f / L : 0.f;
+            float* dst = a.po + ((int64_t)it.partial_base + row) * kDV + 32 * warp + 2 * t;
+#pragma unroll
+            for (int n = 0; n < 4; ++n)
+                *reinterpret_cast<float2*>(dst + 8 * n) = make_float2(o4[n][2 * hh] * inv, o4[n][2 * hh + 1] * inv);
+            if (warp == 0 && t == 0)
+                a.plse[(int64_t)it.partial_base + row] = L > 0.f ? (m + log2f(L)) * kLn2 : -INFINITY;
+        }
+        return;
+    }
 
     float o[16][4];
 #pragma unroll

@@ -12,10 +12,11 @@
 // Hq = 128) read the same rows: they are paired into a 128-row tcgen05 tile
 // (mla_tile.cuh) run by two CTAs, one per half of the output columns; the
 // other units run as mma.sync items.  Chunks are cut by a cost model of the
-// kernel (measured on GB300: a 32-position block costs about 0.94 us +
-// 0.0394 us per query row of the item, so a 64-row block of a shared prefix
-// costs twice a 16-row block of a request's own suffix, and an item about
-// 1.5 us more to start); of the piece lengths tried, the planner keeps the
+// kernel (measured on GB300: a 32-position block of a tile pair costs ~2.1 us
+// per CTA after ~9 us of fixed cost; an item of at most 16 rows, e.g. a
+// request's own suffix at Hq = 16, ~1.8 us per block after ~3.1 us; larger
+// items ~0.94 us + 0.0394 us per query row per block after ~1.5 us); of the
+// piece lengths tried, the planner keeps the
 // one whose list schedule (items most costly first, each to the SM that
 // frees first, as CTAs are dispatched) plus the traffic of its partial rows
 // ends earliest.  Each item writes normalised partial rows that the
@@ -35,9 +36,11 @@ namespace {
 constexpr int32_t kMlaRows = 64;    // query rows of one work item
 constexpr int32_t kMlaBlock = 32;   // positions per block of the kernel
 
-// estimated microseconds of one 32-position block for an item of `rows` query rows
-double block_cost(int32_t rows) { return 0.94 + 0.0394 * rows; }
-constexpr double kItemCost = 1.5;   // estimated start cost of one item (us)
+// estimated microseconds of one 32-position block for an item of `rows` query
+// rows, and of an item's start (an item of at most 16 rows spreads each block
+// over all 16 warps of the CTA: ~1.8 us per block after ~3.1 us, measured)
+double block_cost(int32_t rows) { return rows <= 16 ? 1.785 : 0.94 + 0.0394 * rows; }
+double item_start(int32_t rows) { return rows <= 16 ? 3.1 : 1.5; }
 // tcgen05 tile pairs (two 64-row units, two CTAs): estimated microseconds of
 // one 32-position block and of a tile's fixed cost (Q load and first
 // gathers, ~6 us; epilogue, ~3 us), from GB300 timelines of the tiles
@@ -132,7 +135,7 @@ extern "C" int sgl_mla_decode_plan(const sgl_mla_params* p, const int32_t* seq_l
                         out.push_back(kTileStart + u.per_block * (double)nb);
                         rows += 2 * kMlaRows;
                     } else {
-                        out.push_back(kItemCost + u.per_block * (double)nb);
+                        out.push_back(item_start(u.nm * Gp) + u.per_block * (double)nb);
                         rows += (int64_t)u.nm * Gp;
                     }
                 }
@@ -189,7 +192,7 @@ extern "C" int sgl_mla_decode_plan(const sgl_mla_params* p, const int32_t* seq_l
                 const sgl::DecItem it2{g->seg_row[v.s], (int32_t)cb, ce, v.hg, g->seg_member_ptr[v.s] + v.mb, v.nm, 0, 1};
                 tiles.push_back({it, it2, kTileStart + u.per_block * (double)nb});
             } else {
-                pieces.push_back({it, it, kItemCost + u.per_block * (double)nb});
+                pieces.push_back({it, it, item_start(u.nm * Gp) + u.per_block * (double)nb});
             }
         }
     }

@@ -701,7 +701,12 @@ __device__ __forceinline__ void tc_tile_run(const TcArgs& a, const CUtensorMap* 
                     for (int kk = 0; kk < BN / 16; ++kk)
                         tc_mma_tmem_a(tbase + 256 * q + C::kOCol, tP + kk * 8, sdesc(vb + kk * 2048, KR, 1024), IO,
                                       (j > 0 || kk > 0) ? 1u : 0u);
-                    tc_commit(bar(C::OFULL(q)));
+                    // O is complete for block j once PV_j is: awaited by a
+                    // softmax warp that rescales O, with two score buffers
+                    // only (with one, S_{j+1} follows PV_j in this thread's
+                    // order, so its SFULL implies it; a commit costs the
+                    // tensor pipe tens of cycles)
+                    if constexpr (NSB > 1) tc_commit(bar(C::OFULL(q)));
                     if (q == NQ - 1 || !has(NQ - 1)) tc_commit(bar(C::VEMPTY(st)));   // after the block's last PV
                     if (next) {
                         if (!kb) kb = k_ready(J + NSB);
