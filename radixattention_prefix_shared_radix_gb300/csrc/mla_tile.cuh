@@ -62,15 +62,14 @@ struct Lay {
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_KV = OFF_Q + kNReg * kQReg;                 // 147456
     static constexpr int OFF_BAR = OFF_KV + kNS * kStage;                // 221184
-    // barriers: KFULL[2], KEMPTY[2], SFULL[2], PFULL[2], OFULL, DONE, QFULL
+    // barriers: KFULL[2], KEMPTY[2], SFULL[2], PFULL[2], DONE, QFULL
     static constexpr int KFULL(int s) { return s; }
     static constexpr int KEMPTY(int s) { return 2 + s; }
     static constexpr int SFULL(int b) { return 4 + b; }
     static constexpr int PFULL(int b) { return 6 + b; }
-    static constexpr int OFULL = 8;
-    static constexpr int DONE = 9;
-    static constexpr int QFULL = 10;
-    static constexpr int kNumBars = 11;
+    static constexpr int DONE = 8;
+    static constexpr int QFULL = 9;
+    static constexpr int kNumBars = 10;
     // epilogue: this half's O rows (256 fp32 + 16 bytes of pad each) staged
     // in the Q area, which is free once every MMA is done
     static constexpr int OPITCH = kOCols * 4 + 16;
@@ -142,7 +141,6 @@ __device__ __forceinline__ void mla_tile_run(const TileArgs& a, const CUtensorMa
             mbar_init(bar(Lay::SFULL(b)), 1);
             mbar_init(bar(Lay::PFULL(b)), 128);
         }
-        mbar_init(bar(Lay::OFULL), 1);
         mbar_init(bar(Lay::DONE), 1);
         mbar_init(bar(Lay::QFULL), 1);
         mbar_fence_init();
@@ -278,7 +276,6 @@ __device__ __forceinline__ void mla_tile_run(const TileArgs& a, const CUtensorMa
                     tc_mma_tmem_a(tbase + kTO, tP + kk * 8, sdesc(vb + kk * 2048, kKReg, 1024), IO,
                                   (j > 0 || kk > 0) ? 1u : 0u);
                 tc_commit(bar(Lay::KEMPTY(j % kNS)));
-                tc_commit(bar(Lay::OFULL));
                 if (j + 1 < nb) {   // into block j-1's score buffer, read by PV_{j-1} (issued before it)
                     wait(Lay::KFULL((j + 1) % kNS), (uint32_t)((j + 1) / kNS) & 1u);
                     tc_fence_after();
@@ -332,11 +329,10 @@ __device__ __forceinline__ void mla_tile_run(const TileArgs& a, const CUtensorMa
                 const float f = resc ? exp2f(m_used - m_new) : 1.f;
                 l0 *= f;
                 l1 *= f;
-                if (j > 0) {   // O holds blocks < j: wait for PV_{j-1}
-                    wait(Lay::OFULL, (uint32_t)(j - 1) & 1u);
-                    tc_fence_after();
-                    scale_o(f);
-                }
+                // O holds blocks < j: PV_{j-1} is complete, since S_j was
+                // committed after it by the same thread (a commit covers all
+                // of the thread's earlier MMAs)
+                if (j > 0) scale_o(f);
             }
             if (need) m_used = m_new;
             const float nmu = m_used == -INFINITY ? 0.f : -m_used;

@@ -230,14 +230,13 @@ struct TcCfg {
     // per query tile: S ready and P ready per score buffer (one barrier per
     // buffer, so the softmax warps can never be two phases ahead of the MMA
     // thread's wait: block j + NSB needs S_{j+NSB}, which is issued only after
-    // the MMA thread has consumed block j's P), O updated
-    static constexpr int SFULL(int q, int b) { return 1 + 4 * NS + 5 * q + b; }
-    static constexpr int PFULL(int q, int b) { return 1 + 4 * NS + 5 * q + 2 + b; }
-    static constexpr int OFULL(int q) { return 1 + 4 * NS + 5 * q + 4; }
+    // the MMA thread has consumed block j's P)
+    static constexpr int SFULL(int q, int b) { return 1 + 4 * NS + 4 * q + b; }
+    static constexpr int PFULL(int q, int b) { return 1 + 4 * NS + 4 * q + 2 + b; }
     // every MMA of the tile set has finished (one phase per tile set, so
-    // the waits on it are never ambiguous, unlike a wait on OFULL's last
-    // phase when earlier phases may still be pending)
-    static constexpr int DONE = 1 + 4 * NS + 5 * NQ;
+    // the waits on it are never ambiguous, unlike a wait on a per-block
+    // barrier's last phase when earlier phases may still be pending)
+    static constexpr int DONE = 1 + 4 * NS + 4 * NQ;
     static constexpr int kNumBars = DONE + 1;
     static_assert(kNumBars <= 48, "barrier area");
 };
@@ -296,7 +295,6 @@ __device__ __forceinline__ void tc_init_barriers(uint32_t bar0) {
             mbar_init(bar(C::SFULL(q, b)), 1);
             mbar_init(bar(C::PFULL(q, b)), 128);
         }
-        mbar_init(bar(C::OFULL(q)), 1);
     }
     mbar_init(bar(C::DONE), 1);
 }
@@ -701,13 +699,11 @@ __device__ __forceinline__ void tc_tile_run(const TcArgs& a, const CUtensorMap* 
                     for (int kk = 0; kk < BN / 16; ++kk)
                         tc_mma_tmem_a(tbase + 256 * q + C::kOCol, tP + kk * 8, sdesc(vb + kk * 2048, KR, 1024), IO,
                                       (j > 0 || kk > 0) ? 1u : 0u);
-                    // O is complete for block j once PV_j is: awaited by a
-                    // softmax warp that rescales O, with two score buffers
-                    // only (with one, S_{j+1} follows PV_j in this thread's
-                    // order, so its SFULL implies it; a commit costs the
-                    // tensor pipe tens of cycles)
-                    if constexpr (NSB > 1) tc_commit(bar(C::OFULL(q)));
-                    if (q == NQ - 1 || !has(NQ - 1)) tc_commit(bar(C::VEMPTY(st)));   // after the block's last PV
+                    // after the block's last PV: the stage's V is free, and O
+                    // holds every block up to j (what a softmax warp that
+                    // rescales O waits for; one commit serves both, and a
+                    // commit costs the tensor pipe tens of cycles)
+                    if (q == NQ - 1 || !has(NQ - 1)) tc_commit(bar(C::VEMPTY(st)));
                     if (next) {
                         if (!kb) kb = k_ready(J + NSB);
                         mma_s(q, J + NSB, kb);
@@ -781,8 +777,10 @@ __device__ __forceinline__ void tc_tile_run(const TcArgs& a, const CUtensorMap* 
                 tc_fence_after();
                 // With one score buffer, S_j was issued after PV_{j-1}: O is
                 // final for blocks < j.  With two, a warp that rescales waits
-                // for PV_{j-1} first (the OFULL barrier cannot run two phases
-                // ahead of this wait: its next phase needs this warp's P_j).
+                // for PV_{j-1} first, on block j-1's V-stage EMPTY barrier
+                // (committed after the block's last PV; that stage's next
+                // phase needs PV_{j-1+NS}, hence this warp's P_{j-1+NS}, so
+                // the phase waited for is never ambiguous).
                 bool o_ready = NSB == 1 || j == 0;
                 const uint32_t tS = tl + b * BN;
                 // the block in 64-column halves: max, then 2^(s sc - m) as bf16
@@ -821,7 +819,7 @@ __device__ __forceinline__ void tc_tile_run(const TcArgs& a, const CUtensorMap* 
                         // O holds blocks < j at the old max
                         if (j > 0) {
                             if (!o_ready) {
-                                wait(C::OFULL(q), (J - 1) & 1);
+                                wait(C::VEMPTY((J - 1) % NS), ((J - 1) / NS) & 1u);
                                 tc_fence_after();
                                 o_ready = true;
                             }
