@@ -87,7 +87,9 @@ __device__ __forceinline__ void tc_mma_tmem_a(uint32_t tmem, uint32_t a_tmem, ui
             "r"(tmem),
         "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc));
 }
-__device__ __forceinline__ void tst32u(uint32_t taddr, const uint32_t (&r)[32]) {
+// 32 consecutive TMEM columns of this thread's lane, without waiting for the
+// store to complete (tst_wait before the columns are read back or published).
+__device__ __forceinline__ void tst32u_nw(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%"
         "18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(taddr),
@@ -96,7 +98,11 @@ __device__ __forceinline__ void tst32u(uint32_t taddr, const uint32_t (&r)[32]) 
         "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
         "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
         : "memory");
-    asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void tst_wait() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
+__device__ __forceinline__ void tst32u(uint32_t taddr, const uint32_t (&r)[32]) {
+    tst32u_nw(taddr, r);
+    tst_wait();
 }
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar)
@@ -116,6 +122,25 @@ __device__ __forceinline__ void tld32_nw(uint32_t taddr, float* v) {
           "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
           "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
           "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+// 64 consecutive TMEM columns of this thread's lane in one load (measured:
+// one x64 load slows concurrent MMAs less than two x32 loads of the same
+// columns), without waiting.
+__device__ __forceinline__ void tld64_nw(uint32_t taddr, float* v) {
+    uint32_t* r = reinterpret_cast<uint32_t*>(v);
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+        "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,"
+        "%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+          "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+          "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+          "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+          "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
         : "r"(taddr));
 }
 __device__ __forceinline__ void tld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
@@ -790,8 +815,7 @@ __device__ __forceinline__ void tc_tile_run(const TcArgs& a, const CUtensorMap* 
                     const int pos0 = kv_begin + j * BN + 64 * h;
                     const bool full_blk = pos0 + 63 < kv_end && pos0 + 63 <= lim;
                     float srow[64];
-                    tld32_nw(tS + 64 * h, srow);
-                    tld32_nw(tS + 64 * h + 32, srow + 32);
+                    tld64_nw(tS + 64 * h, srow);
                     tld_wait();
                     // max on the raw scores (the scale is positive), scaled
                     // once; four independent chains of 3-input max
@@ -826,6 +850,7 @@ __device__ __forceinline__ void tc_tile_run(const TcArgs& a, const CUtensorMap* 
                             scale_o(f);
                         }
                         // this block's earlier halves are at the old max too
+                        if (h > 0) tst_wait();   // their P stores have landed
                         for (int h2 = 0; h2 < h; ++h2) {
                             uint32_t w[32];
                             tld32_nw(tS + 32 * h2, reinterpret_cast<float*>(w));
@@ -857,8 +882,9 @@ __device__ __forceinline__ void tc_tile_run(const TcArgs& a, const CUtensorMap* 
                         fadd2_acc(l0, l1, p0, p1);
                         pk[k / 2] = F8 ? pack_f16(p0, p1) : pack_bf16(p0, p1);
                     }
-                    tst32u(tS + 32 * h, pk);   // P over scores already read
+                    tst32u_nw(tS + 32 * h, pk);   // P over scores already read
                 }
+                tst_wait();   // the block's P stores have landed before they are published
                 tc_fence_before();
                 mbar_arrive(bar(C::PFULL(q, b)));
             }
