@@ -520,8 +520,11 @@ int sgl_check(void* workspace, sgl_stream_t stream);
  * rejected with SGL_ERR_WORKSPACE, and every other argument error is
  * returned, before any GPU work.  The first call on a device looks the
  * array's address up (cudaGetSymbolAddress, with that device current) and
- * caches it, so make that first call before any stream capture; a device
- * reset (cudaDeviceReset) is not supported afterwards.  All calls share the
+ * caches it; a device reset (cudaDeviceReset) is not supported afterwards.
+ * Each call copies the plan's tables from the plan's host memory, so the
+ * call is not meant for stream capture (a captured copy would re-read that
+ * memory at every replay): graphs capture sgl_decode_attn with a workspace
+ * uploaded beforehand by sgl_plan_upload.  All calls share the
  * array, whose contents are the last call's (each call rewrites the plan
  * tables and clears the error word and merge counters itself): calls that
  * may overlap on the GPU (different streams, or before the previous call
