@@ -382,10 +382,10 @@ def e2e_decode(sgl, W, torch, w, tree, kd, vd, inst, steps, num_sms=0):
     untouched).  A plan is reused while the requests grow (its trailing
     pieces read up to the run-time lengths) and rebuilt every REPLAN steps
     (sgl_decode_plan, then sgl_plan_upload into the other of two workspaces,
-    while the GPU runs the step before).  Each step copies its inputs (Q, the slot table, the
-    lengths: one pinned buffer laid out like one device buffer) to the
-    device in one copy, runs the decode call, copies O and LSE back in one
-    copy and waits for them.  After the last step
+    while the GPU runs the step before).  Each step is one sgl_decode_step
+    call: its inputs (Q, the slot table, the lengths: one pinned buffer laid
+    out like one device buffer) to the device in one copy, the decode, O and
+    LSE back in one copy; the loop then waits for them.  After the last step
     sgl_tree_cache_finished_batch caches every sequence.  All of it is
     timed.  The per-step GPU calls go straight to the C ABI with the
     buffers' addresses taken once (as a C or C++ serving loop would call
@@ -430,6 +430,8 @@ def e2e_decode(sgl, W, torch, w, tree, kd, vd, inst, steps, num_sms=0):
     args_fixed = dict(q=vp(base_in), k=vp(kd.data_ptr()), v=vp(vd.data_ptr()), tab=vp(base_in + qb),
                       seq=vp(base_in + qb + tb), o=vp(base_out), lse=vp(base_out + ob))
     ws_ptr = [vp(x.data_ptr()) for x in ws]
+    hin_p, hout_p = vp(hin.data_ptr()), vp(hout.data_ptr())
+    nin, nout = qb + tb + sb, ob + lb
     stream = vp(torch.cuda.current_stream().cuda_stream)
     per_tok = kv_bytes_per_token(w)
     ub0 = it["ub"]
@@ -468,12 +470,10 @@ def e2e_decode(sgl, W, torch, w, tree, kd, vd, inst, steps, num_sms=0):
     for s in range(steps):
         c0 = time.perf_counter()
         hseq_np[:] = seq_np
-        din.copy_(hin, non_blocking=True)
-        st = lib.sgl_decode_attn(a["q"], a["k"], a["v"], a["tab"], ld, a["seq"], plan.handle, a["o"], a["lse"],
-                                 ws_ptr[cur], wsz, stream)
+        st = lib.sgl_decode_step(hin_p, a["q"], nin, a["q"], a["k"], a["v"], a["tab"], ld, a["seq"], plan.handle,
+                                 a["o"], a["lse"], a["o"], hout_p, nout, ws_ptr[cur], wsz, stream)
         if st:
-            raise sgl.SglError(st, "sgl_decode_attn")
-        hout.copy_(dout, non_blocking=True)
+            raise sgl.SglError(st, "sgl_decode_step")
         done.record()
         stage["launch"] += time.perf_counter() - c0
         # the shared prefix is unchanged; every request's own suffix grew by one token a step
@@ -666,8 +666,9 @@ def run_native(args):
                         "every %d steps, plans the batch anew and uploads the plan to a second workspace "
                         "(in between the plan is reused: its trailing pieces read the run-time lengths); "
                         "each step copies Q, the table and the " % REPLAN +
-                        "lengths in (one pinned buffer, one copy), decodes (the C ABI called with the buffers' "
-                        "addresses), copies O and LSE out (one copy) and waits for them; after the last step "
+                        "lengths in (one pinned buffer, one copy), decodes and copies O and LSE out (one copy), "
+                        "all by one sgl_decode_step call of the C ABI with the buffers' addresses, and waits "
+                        "for them; after the last step "
                         "every sequence is cached in the tree and released",
                 "host_us_per_step": e2e_host},
         "gpu_launches": K * launches_per_call,

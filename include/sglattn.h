@@ -342,6 +342,26 @@ int sgl_decode_attn(const void* q, const void* k_pool, const void* v_pool, const
                     int64_t ld, const int32_t* seq_lens, const sgl_plan* plan, void* o, float* lse,
                     void* workspace, size_t ws_bytes, sgl_stream_t stream);
 
+/* One decode step from host memory, in one call: copy in_bytes from
+ * in_host (host memory, pinned for an asynchronous copy) to in_dev (device),
+ * run sgl_decode_attn with the given device pointers -- which normally
+ * point into in_dev: the step's q, its req_to_token rows and seq_lens staged
+ * together -- and copy out_bytes from out_dev (device, normally holding o
+ * and lse) to out_host, all queued on `stream` in that order.  in_bytes or
+ * out_bytes may be 0 (that copy is skipped).  The caller waits on the stream
+ * (or an event recorded after the call) before reading out_host, and must
+ * not rewrite in_host before the input copy has run.  Every argument check
+ * of sgl_decode_attn, and in_host/in_dev (out_dev/out_host) present when
+ * in_bytes (out_bytes) is not 0, is made before any GPU work: on a refusal
+ * nothing is queued.
+ * [a decode step's metadata prepared on the CPU and moved to the device
+ * while the GPU runs the step before: CS349D lecture-16 notes §2.2;
+ * "SGLang 深度解读" (luoboask.github.io) section 2, Scheduler] */
+int sgl_decode_step(const void* in_host, void* in_dev, size_t in_bytes, const void* q, const void* k_pool,
+                    const void* v_pool, const int32_t* req_to_token, int64_t ld, const int32_t* seq_lens,
+                    const sgl_plan* plan, void* o, float* lse, const void* out_dev, void* out_host, size_t out_bytes,
+                    void* workspace, size_t ws_bytes, sgl_stream_t stream);
+
 /* ---------------------------------------------------------------------
  * MLA grouped decode (CS349D lecture-16 notes, SGLang case study: §4 "More
  * engineering", DeepSeek's MLA with the decompression matrices absorbed

@@ -125,6 +125,8 @@ _SIGS = {
     "sgl_plan_info": (ctypes.c_int, [_P, ctypes.POINTER(SglPlanInfo)]),
     "sgl_plan_upload": (ctypes.c_int, [_P, _P, ctypes.c_size_t, _P]),
     "sgl_decode_attn": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_int64, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "sgl_decode_step": (ctypes.c_int, [_P, _P, ctypes.c_size_t, _P, _P, _P, _P, ctypes.c_int64, _P, _P, _P, _P, _P,
+                                       _P, ctypes.c_size_t, _P, ctypes.c_size_t, _P]),
     "sgl_extend_workspace_bytes": (ctypes.c_int, [ctypes.POINTER(SglAttnParams), ctypes.POINTER(ctypes.c_size_t)]),
     "sgl_extend_attn": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_int64, _P, _P, ctypes.POINTER(SglAttnParams),
                                        _P, _P, _P, ctypes.c_size_t, _P]),
@@ -510,6 +512,42 @@ def sgl_decode_attn(q, k_pool, v_pool, req_to_token, seq_lens, plan, o, lse, wor
                                _dev(req_to_token, "req_to_token"), req_to_token.shape[1], _dev(seq_lens, "seq_lens"),
                                plan.handle, _dev(o, "o"), _dev(lse, "lse"), _dev(workspace, "workspace"),
                                workspace.numel() * workspace.element_size(), _stream(stream)), "sgl_decode_attn")
+
+
+def _host(t, what):
+    import torch
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise TypeError("%s must be a host tensor" % what)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % what)
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _in_region(t, region, what):
+    """A CUDA tensor that lies inside the device tensor `region`."""
+    p = _dev(t, what)
+    lo, n = region.data_ptr(), region.numel() * region.element_size()
+    if not (lo <= t.data_ptr() and t.data_ptr() + t.numel() * t.element_size() <= lo + n):
+        raise ValueError("%s must lie inside its staging tensor" % what)
+    return p
+
+
+def sgl_decode_step(in_host, in_dev, q, k_pool, v_pool, req_to_token, seq_lens, plan, o, lse, out_dev, out_host,
+                    workspace, stream=None):
+    """One decode step from host memory: in_host -> in_dev (which holds q,
+    req_to_token and seq_lens), the decode, out_dev (holding o and lse) ->
+    out_host, queued on the stream by one library call."""
+    nin = in_host.numel() * in_host.element_size()
+    nout = out_host.numel() * out_host.element_size()
+    if in_dev.numel() * in_dev.element_size() != nin or out_dev.numel() * out_dev.element_size() != nout:
+        raise ValueError("staging tensors differ in size from their host buffers")
+    _ok(_lib().sgl_decode_step(_host(in_host, "in_host"), _dev(in_dev, "in_dev"), nin,
+                               _in_region(q, in_dev, "q"), _dev(k_pool, "k_pool"), _dev(v_pool, "v_pool"),
+                               _in_region(req_to_token, in_dev, "req_to_token"), req_to_token.shape[1],
+                               _in_region(seq_lens, in_dev, "seq_lens"), plan.handle,
+                               _in_region(o, out_dev, "o"), _in_region(lse, out_dev, "lse"), _dev(out_dev, "out_dev"),
+                               _host(out_host, "out_host"), nout, _dev(workspace, "workspace"),
+                               workspace.numel() * workspace.element_size(), _stream(stream)), "sgl_decode_step")
 
 
 def make_mla_params(batch, num_qo_heads, num_slots, latent_dim=512, rope_dim=64, page_size=1, sm_scale=0.0,

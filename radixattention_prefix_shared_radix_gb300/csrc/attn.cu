@@ -413,14 +413,9 @@ int sgl_plan_upload(const sgl_plan* plan, void* workspace, size_t ws_bytes, sgl_
 int sgl_decode_attn(const void* q, const void* k_pool, const void* v_pool, const int32_t* req_to_token, int64_t ld,
                     const int32_t* seq_lens, const sgl_plan* plan, void* o, float* lse, void* workspace,
                     size_t ws_bytes, sgl_stream_t stream) {
-    if (!plan || plan->kind != 0) return SGL_ERR_INVALID_ARG;
-    const int32_t B = plan->params.batch;
-    if (B > 0 && (!q || !o || !lse || !seq_lens)) return SGL_ERR_INVALID_ARG;
-    if (plan->n_items > 0 && (!k_pool || !v_pool || !req_to_token || ld < plan->max_pos)) return SGL_ERR_INVALID_ARG;
-    if (!workspace || !aligned(workspace, sgl::kWsAlign) || ws_bytes < plan->workspace_bytes)
-        return SGL_ERR_WORKSPACE;
-    if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(o, 16))
-        return SGL_ERR_INVALID_ARG;
+    if (const int st = sgl::decode_arg_status(plan, q, k_pool, v_pool, req_to_token, ld, seq_lens, o, lse, workspace,
+                                              ws_bytes))
+        return st;
     auto* ws = static_cast<unsigned char*>(workspace);
     auto s = reinterpret_cast<cudaStream_t>(stream);
     if (plan->params.head_dim == 128) return launch_decode<128>(plan, q, k_pool, v_pool, req_to_token, ld, seq_lens, o, lse, ws, s);

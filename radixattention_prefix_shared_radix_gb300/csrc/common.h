@@ -93,3 +93,21 @@ struct sgl_plan {
     size_t workspace_bytes;      // total device workspace
     unsigned char* blob;         // host copy of [0, tables_bytes)
 };
+
+namespace sgl {
+// The argument checks of sgl_decode_attn, all on the host, so that every
+// refusal comes before any GPU work (shared with sgl_decode_step, which
+// checks before its input copy).
+inline int decode_arg_status(const sgl_plan* plan, const void* q, const void* k_pool, const void* v_pool,
+                             const int32_t* req_to_token, int64_t ld, const int32_t* seq_lens, const void* o,
+                             const float* lse, const void* workspace, size_t ws_bytes) {
+    auto aligned = [](const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; };
+    if (!plan || plan->kind != 0) return SGL_ERR_INVALID_ARG;
+    const int32_t B = plan->params.batch;
+    if (B > 0 && (!q || !o || !lse || !seq_lens)) return SGL_ERR_INVALID_ARG;
+    if (plan->n_items > 0 && (!k_pool || !v_pool || !req_to_token || ld < plan->max_pos)) return SGL_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, kWsAlign) || ws_bytes < plan->workspace_bytes) return SGL_ERR_WORKSPACE;
+    if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(o, 16)) return SGL_ERR_INVALID_ARG;
+    return SGL_OK;
+}
+}  // namespace sgl

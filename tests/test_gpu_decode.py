@@ -537,3 +537,73 @@ def test_reused_plan_reports_a_batch_that_shrank():
         assert e.value.status == -5
     finally:
         case.close()
+
+
+def _packed(case):
+    """A step's inputs in one pinned host buffer [q | req_to_token | seq_lens]
+    and its outputs [O | LSE], with device staging tensors of the same
+    layout and views into them."""
+    q = case.q_host()
+    table = np.ascontiguousarray(case.out["req_to_token"], dtype=np.int32)
+    seq = np.ascontiguousarray(case.out["seq_lens"], dtype=np.int32)
+    qb, tb, sb = q.numel() * q.element_size(), table.nbytes, seq.nbytes
+    ob, lb = qb, case.B * case.w.Hq * 4
+    hin = torch.empty(qb + tb + sb, dtype=torch.uint8).pin_memory()
+    hin[:qb].copy_(q.reshape(-1).view(torch.uint8))
+    hin[qb:qb + tb].copy_(torch.from_numpy(table).reshape(-1).view(torch.uint8))
+    hin[qb + tb:].copy_(torch.from_numpy(seq).view(torch.uint8))
+    din = torch.empty_like(hin, device="cuda")
+    hout = torch.full((ob + lb,), 0xAB, dtype=torch.uint8).pin_memory()
+    dout = torch.empty_like(hout, device="cuda")
+    views = dict(q=din[:qb].view(q.dtype).view(q.shape), table=din[qb:qb + tb].view(torch.int32).view(table.shape),
+                 seq=din[qb + tb:].view(torch.int32), o=dout[:ob].view(q.dtype).view(q.shape),
+                 lse=dout[ob:].view(torch.float32).view(case.B, case.w.Hq))
+    return hin, din, hout, dout, views, ob
+
+
+@pytest.mark.parametrize("name", ["llama3_8b_decode_small", "tiny_fp32"])
+def test_decode_step_from_host_memory(name):
+    """sgl_decode_step (input copy, decode, output copy in one call) gives the
+    same bytes as the copies and sgl_decode_attn made separately, and the
+    oracle's result."""
+    case = Case(name)
+    try:
+        kd, vd = case.device_pool()
+        plan = sgl.sgl_decode_plan(case.params(), case.out["seq_lens"], sgl.sgl_groups_view(case.groups))
+        ws = torch.zeros(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
+        sgl.sgl_plan_upload(plan, ws)
+        hin, din, hout, dout, v, ob = _packed(case)
+        sgl.sgl_decode_step(hin, din, v["q"], kd, vd, v["table"], v["seq"], plan, v["o"], v["lse"], dout, hout, ws)
+        torch.cuda.synchronize()
+        sgl.sgl_check(ws)
+        o_ref = torch.empty_like(v["o"])
+        lse_ref = torch.empty_like(v["lse"])
+        sgl.sgl_decode_attn(v["q"], kd, vd, v["table"], v["seq"], plan, o_ref, lse_ref, ws)
+        torch.cuda.synchronize()
+        assert torch.equal(hout[:ob], o_ref.reshape(-1).view(torch.uint8).cpu())
+        assert torch.equal(hout[ob:], lse_ref.reshape(-1).view(torch.uint8).cpu())
+        O = hout[:ob].view(v["o"].dtype).view(v["o"].shape).double().numpy()
+        L = hout[ob:].view(torch.float32).view(case.B, case.w.Hq).double().numpy()
+        Oref, Lref = decode_attention(case.oracle_q(), W.RowView(case.K), W.RowView(case.V), case.oracle_table,
+                                      case.out["seq_lens"])
+        assert_close(O, L, Oref, Lref, *tolerances(case.w))
+    finally:
+        case.close()
+
+
+def test_decode_step_refuses_before_any_copy():
+    """A refused step queues nothing: the host output buffer keeps its bytes."""
+    case = Case("llama3_8b_decode_small")
+    try:
+        kd, vd = case.device_pool()
+        plan = sgl.sgl_decode_plan(case.params(), case.out["seq_lens"], sgl.sgl_groups_view(case.groups))
+        hin, din, hout, dout, v, ob = _packed(case)
+        small = torch.zeros(256, dtype=torch.uint8, device="cuda")   # below the plan's workspace
+        with pytest.raises(sgl.SglError) as e:
+            sgl.sgl_decode_step(hin, din, v["q"], kd, vd, v["table"], v["seq"], plan, v["o"], v["lse"], dout, hout,
+                                small)
+        assert e.value.status == -7
+        torch.cuda.synchronize()
+        assert bool((hout == 0xAB).all())
+    finally:
+        case.close()
