@@ -38,7 +38,7 @@
 // Roles (512 threads): warps 0-3 softmax, warp 4 the MMA thread (and TMEM
 // owner), warps 5-15 the gather team (a warp gets one gather4 through about
 // every 110 cycles, so a block's 72 copies are spread over eleven warps);
-// all warps load Q first.  Before the dependency wait a CTA reads only plan
+// threads 0-71 issue Q's TMA boxes first.  Before the dependency wait a CTA reads only plan
 // tables (its units and their member requests).  Every wait is
 // bounded: one that gives up sets bit 2 of the error word and the CTA runs to
 // its end without hanging (its results are then garbage, and flagged).
